@@ -1,0 +1,214 @@
+/*
+ * spec.h -- C ABI of the GB300 verify-step library (libspec.so).
+ *
+ * The library runs the greedy, lossless speculative-decoding verify step of a
+ * DeepSeekMoE-style (or dense SwiGLU) decoder on one GPU: one target forward
+ * scores each sequence's last committed token plus K draft tokens against a
+ * paged, prefix-shared KV cache, takes the greedy argmax of every row, keeps
+ * the longest draft prefix that agrees with it, appends the target's bonus
+ * token, and commits or rolls back the KV rows on the device.
+ *
+ * Sources for the operations (page title and section):
+ *  - "End-to-end OCR expert model architecture and acceleration principles",
+ *    section 6.1 (the target scores all draft positions in one teacher-forced
+ *    forward; accept the agreeing prefix left to right, the target supplies
+ *    the token at the first divergence) and section 7 (draft -> verify ->
+ *    append loop); section 9 (continuous batching, KV-cache management).
+ *  - "Jina-OCR-v1: efficient document parsing with speculative decoding and
+ *    dense verifiable rewards", abstract (greedy verification is lossless),
+ *    section 3 (compressed visual prefix, DeepSeekMoE decoder ~570M active).
+ *  - "Jina AI releases jina-ocr-v1" (64 routed + 2 shared experts, top-6;
+ *    greedy verification keeps the longest matching prefix).
+ *  - "OCRia-1 technical report guide", inference stack (31-token block drafts,
+ *    FP8 weights, shared prompt-prefix reuse).
+ *
+ * Conventions for every entry point:
+ *  - Return 0 on success or a negative SPEC_ERR_* code; spec_strerror() names
+ *    it and spec_last_error() gives a message for the last failure on the
+ *    calling thread. No C++ exception crosses this boundary.
+ *  - On failure the sequence state is unchanged (a verify step commits all of
+ *    its sequences or none).
+ *  - The caller owns every array it passes and may reuse it once the call
+ *    returns. Arguments are host pointers unless the name ends in "_dev".
+ *  - The library owns the weights, the KV page pool and its CUDA graphs. All
+ *    device work is ordered on the stream given to spec_init_model. Calls
+ *    without a "_dev" suffix return only after their results are in host
+ *    memory; "_dev" calls only enqueue work.
+ *  - A model handle is not thread-safe; distinct handles are independent.
+ */
+#ifndef SPEC_H_
+#define SPEC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- error codes ------------------------------------------------------- */
+#define SPEC_OK            0
+#define SPEC_ERR_ARG      -1   /* bad argument (id, size, token out of range) */
+#define SPEC_ERR_NO_PAGES -2   /* KV page pool exhausted                       */
+#define SPEC_ERR_CUDA     -3   /* a CUDA call failed (see spec_last_error)     */
+#define SPEC_ERR_STATE    -4   /* call not valid in the sequence's state       */
+#define SPEC_ERR_NOMEM    -5   /* host or device allocation failed             */
+#define SPEC_ERR_UNSUPPORTED -6 /* configuration outside what the kernels take */
+
+/* ---- storage dtypes ------------------------------------------------------ */
+#define SPEC_F32  0   /* IEEE binary32                                         */
+#define SPEC_BF16 1   /* bfloat16 (top half of binary32, round-to-nearest-even) */
+#define SPEC_FP8  2   /* OCP E4M3 codes + one fp32 scale per output row        */
+
+/* Model and pool shape. n_experts == 0 selects a dense SwiGLU FFN, stored as
+ * one always-on ("shared") expert of width `inter` (n_shared must be 1).
+ * Routed experts use top_k of n_experts, softmax weights without
+ * renormalisation; shared experts are added with weight 1.
+ * head_dim must be 64 or 128; page_size a multiple of 16; max_draft <= 31. */
+typedef struct spec_config {
+  int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim;
+  int32_t n_experts, top_k, n_shared, inter, vocab;
+  int32_t wdtype;        /* SPEC_F32 / SPEC_BF16 / SPEC_FP8 (attention + experts) */
+  int32_t page_size;     /* tokens per KV page                                    */
+  int32_t n_pages;       /* pages in the pool                                     */
+  int32_t max_seqs;      /* sequence slots (ids 0..max_seqs-1)                    */
+  int32_t max_ctx;       /* longest sequence (prompt + output + max_draft + 1)    */
+  int32_t max_draft;     /* K: every verify step scores K+1 rows per sequence     */
+  int32_t max_batch;     /* sequences per verify step                             */
+  int32_t prefill_chunk; /* rows per prefill pass (0 = library default)           */
+  float rope_theta, rms_eps;
+} spec_config;
+
+/* ---- weights ------------------------------------------------------------- */
+/* Tensors are passed as an array of host pointers in this order (global, then
+ * 13 per layer):
+ *   0 tok_embed [V, h]          f32 if wdtype == F32, else bf16
+ *   1 final_norm [h]            f32
+ *   2 lm_head [V, h]            f32 if wdtype == F32, else bf16
+ *   per layer l, index 3 + 13 l + j:
+ *   j=0 attn_norm [h] f32       j=1 w_qkv [(Hq+2Hkv) d, h] wdtype (rows: q heads,
+ *                                   then k heads, then v heads; each head d rows)
+ *   j=2 s_qkv [(Hq+2Hkv) d] f32 (FP8 only)
+ *   j=3 w_o [h, Hq d] wdtype    j=4 s_o [h] f32 (FP8 only)
+ *   j=5 ffn_norm [h] f32        j=6 w_router [E, h] (f32 if F32 model, else bf16;
+ *                                   absent when E == 0)
+ *   j=7 w_gate [E+S, inter, h]  j=8 s_gate [E+S, inter] f32 (FP8 only)
+ *   j=9 w_up [E+S, inter, h]    j=10 s_up [E+S, inter] f32 (FP8 only)
+ *   j=11 w_down [E+S, h, inter] j=12 s_down [E+S, h] f32 (FP8 only)
+ * Matrices are row-major [out, in]; experts 0..E-1 are routed, E..E+S-1
+ * shared. Absent tensors have 0 bytes and their pointer may be NULL. */
+int spec_tensor_count(const spec_config* cfg);
+/* Byte size of tensor `index` (0 for absent ones), or a negative error. */
+int64_t spec_tensor_bytes(const spec_config* cfg, int index);
+
+typedef struct spec_model spec_model;
+
+/* Validate `cfg`, allocate the device weights, KV pool and step buffers,
+ * upload `host_tensors` (spec_tensor_count() pointers in the order above) and
+ * build the RoPE tables. `cuda_stream` is a cudaStream_t; 0 makes the library
+ * create and own a non-blocking stream (the legacy default stream cannot be
+ * captured into the CUDA graphs the steps replay). Errors: SPEC_ERR_ARG (bad shape), SPEC_ERR_UNSUPPORTED,
+ * SPEC_ERR_NOMEM, SPEC_ERR_CUDA. */
+int spec_init_model(const spec_config* cfg, const void* const* host_tensors,
+                    uintptr_t cuda_stream, spec_model** out_model);
+int spec_free_model(spec_model* m);
+
+/* Register a prompt prefix shared by many sequences (the OCRia-1 guide's
+ * shared prompt-prefix reuse): its KV rows are computed once, and its full
+ * pages are referenced (refcounted) by every sequence prefilled with it.
+ * tok: n_tok host token ids. */
+int spec_register_prefix(spec_model* m, const int32_t* tok, int n_tok,
+                         int32_t* out_prefix_id);
+int spec_release_prefix(spec_model* m, int32_t prefix_id);
+
+/* Prefill sequence slot `seq_id` (must be free) with the prompt
+ * [prefix tokens (prefix_id >= 0)] ++ vis_embeds_dev rows ++ tok. vis_embeds_dev
+ * is a DEVICE pointer to n_vis rows of `hidden` values in the activation
+ * storage type (f32 for F32 models, bf16 otherwise); tok are host ids.
+ * Writes the first generated token (greedy argmax of the last prompt row).
+ * Errors: SPEC_ERR_ARG, SPEC_ERR_STATE (slot busy), SPEC_ERR_NO_PAGES. */
+int spec_prefill(spec_model* m, int32_t seq_id, int32_t prefix_id,
+                 const void* vis_embeds_dev, int n_vis, const int32_t* tok, int n_tok,
+                 int32_t* out_first_token);
+
+/* One verify step for one sequence: scores [last committed token, draft_tokens
+ * (n_draft of them, 0 <= n_draft <= max_draft)], then commits the accepted
+ * prefix and the bonus token. n_draft = 0 is a plain greedy decoding step.
+ * out_accepted_len = number of drafts accepted (0..n_draft); the step commits
+ * out_accepted_len + 1 tokens: the accepted drafts then *out_bonus_token. */
+int spec_verify_step(spec_model* m, int32_t seq_id, const int32_t* draft_tokens,
+                     int n_draft, int32_t* out_accepted_len, int32_t* out_bonus_token);
+
+/* Batched verify step over n_seq distinct sequences (1 <= n_seq <= max_batch).
+ * drafts: [n_seq, max_draft] host ids (row s uses its first n_draft[s]).
+ * Outputs out_accepted[n_seq], out_bonus[n_seq] (host). */
+int spec_verify_step_batch(spec_model* m, int n_seq, const int32_t* seq_ids,
+                           const int32_t* drafts, const int32_t* n_draft,
+                           int32_t* out_accepted, int32_t* out_bonus);
+
+/* Device-resident variant: all arrays are device pointers, nothing is copied
+ * to or read back by the host and the call returns once the step is enqueued.
+ * The sequences must have KV pages reserved for the step (spec_reserve_seq);
+ * the host's view of their lengths is refreshed by spec_sync_seqs(). */
+int spec_verify_step_batch_dev(spec_model* m, int n_seq, const int32_t* seq_ids_dev,
+                               const int32_t* drafts_dev, const int32_t* n_draft_dev,
+                               int32_t* out_accepted_dev, int32_t* out_bonus_dev);
+
+/* Reserve KV pages so sequence `seq_id` can grow to n_tokens positions without
+ * host involvement; the commit kernel keeps these pages. */
+int spec_reserve_seq(spec_model* m, int32_t seq_id, int n_tokens);
+/* Wait for the stream, then read back every sequence's length and block table
+ * into the host allocator's view. */
+int spec_sync_seqs(spec_model* m);
+
+/* Release sequence slot `seq_id`: its pages return to the pool (shared prefix
+ * pages only when their last reference goes). */
+int spec_release_seq(spec_model* m, int32_t seq_id);
+
+/* Sequence state queries (host view; call spec_sync_seqs after _dev steps).
+ * out_len = KV positions held (prompt + committed tokens - 1);
+ * generated tokens so far are copied to out_tokens (up to cap). */
+int spec_seq_info(spec_model* m, int32_t seq_id, int32_t* out_len, int32_t* out_n_generated);
+int spec_seq_tokens(spec_model* m, int32_t seq_id, int32_t* out_tokens, int cap);
+/* Block table of `seq_id` as held on the device (page ids, -1 = none). */
+int spec_seq_block_table(spec_model* m, int32_t seq_id, int32_t* out_pages, int cap,
+                         int32_t* out_n);
+int spec_free_pages(spec_model* m);
+
+/* Debug: like spec_verify_step_batch but writes the fp32 logits of every
+ * scored row to logits_dev ([n_seq * (max_draft+1), vocab], device) and does
+ * NOT commit (sequence state unchanged). */
+int spec_debug_logits(spec_model* m, int n_seq, const int32_t* seq_ids,
+                      const int32_t* drafts, float* logits_dev);
+
+/* Number of kernel launches one verify step of n_seq sequences enqueues. */
+int spec_step_launches(spec_model* m, int n_seq);
+
+const char* spec_strerror(int code);
+const char* spec_last_error(void);
+
+/* ---- paged KV allocator (host only; usable without a GPU) ---------------- */
+/* The same allocator the model uses, exposed for tests and tooling. Pages
+ * hold page_size consecutive positions; a sequence's block table lists its
+ * pages in position order. Prefix pages are refcounted. */
+typedef struct spec_pool spec_pool;
+int spec_pool_create(int n_pages, int page_size, int max_seqs, int max_pages_per_seq,
+                     spec_pool** out);
+int spec_pool_destroy(spec_pool* p);
+/* Make seq hold pages for positions [0, n_tokens); allocates as needed. */
+int spec_pool_reserve(spec_pool* p, int32_t seq, int n_tokens);
+/* Commit: keep pages covering max(new_len, keep_pages*page_size) positions,
+ * release the rest; the sequence length becomes new_len. */
+int spec_pool_commit(spec_pool* p, int32_t seq, int new_len, int keep_pages);
+int spec_pool_release(spec_pool* p, int32_t seq);
+/* Share the first n_pages pages of `src_seq` with the empty sequence `dst`
+ * (refcount + 1 each). */
+int spec_pool_share(spec_pool* p, int32_t src_seq, int n_pages, int32_t dst);
+int spec_pool_block_table(spec_pool* p, int32_t seq, int32_t* out, int cap, int32_t* out_n);
+int spec_pool_refcount(spec_pool* p, int32_t page);
+int spec_pool_free_count(spec_pool* p);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_H_ */

@@ -1,0 +1,278 @@
+"""ctypes binding of libspec.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls (declared in
+``include/spec.h``) and does no computation of its own: all work of the verify
+step runs in the library's CUDA kernels. Loading fails loudly when the
+library has not been built; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspec.so")
+
+SPEC_F32, SPEC_BF16, SPEC_FP8 = 0, 1, 2
+ERRORS = {-1: "SPEC_ERR_ARG", -2: "SPEC_ERR_NO_PAGES", -3: "SPEC_ERR_CUDA", -4: "SPEC_ERR_STATE",
+          -5: "SPEC_ERR_NOMEM", -6: "SPEC_ERR_UNSUPPORTED"}
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class spec_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "n_experts", "top_k", "n_shared",
+        "inter", "vocab", "wdtype", "page_size", "n_pages", "max_seqs", "max_ctx", "max_draft",
+        "max_batch", "prefill_chunk")] + [("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)]
+
+
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_lib: Optional[ctypes.CDLL] = None
+
+# (name, restype, argtypes) of every exported entry point
+_SIGS = [
+    ("spec_tensor_count", ctypes.c_int, [ctypes.POINTER(spec_config)]),
+    ("spec_tensor_bytes", ctypes.c_int64, [ctypes.POINTER(spec_config), ctypes.c_int]),
+    ("spec_init_model", ctypes.c_int, [ctypes.POINTER(spec_config), ctypes.POINTER(ctypes.c_void_p),
+                                       ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)]),
+    ("spec_free_model", ctypes.c_int, [ctypes.c_void_p]),
+    ("spec_register_prefix", ctypes.c_int, [ctypes.c_void_p, _I32P, ctypes.c_int, _I32P]),
+    ("spec_release_prefix", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    ("spec_prefill", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                    ctypes.c_int, _I32P, ctypes.c_int, _I32P]),
+    ("spec_verify_step", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, _I32P, ctypes.c_int, _I32P, _I32P]),
+    ("spec_verify_step_batch", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, _I32P, _I32P, _I32P, _I32P,
+                                              _I32P]),
+    ("spec_verify_step_batch_dev", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                  ctypes.c_void_p]),
+    ("spec_reserve_seq", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int]),
+    ("spec_sync_seqs", ctypes.c_int, [ctypes.c_void_p]),
+    ("spec_release_seq", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    ("spec_seq_info", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, _I32P, _I32P]),
+    ("spec_seq_tokens", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, _I32P, ctypes.c_int]),
+    ("spec_seq_block_table", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, _I32P, ctypes.c_int, _I32P]),
+    ("spec_free_pages", ctypes.c_int, [ctypes.c_void_p]),
+    ("spec_debug_logits", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, _I32P, _I32P, ctypes.c_void_p]),
+    ("spec_step_launches", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    ("spec_strerror", ctypes.c_char_p, [ctypes.c_int]),
+    ("spec_last_error", ctypes.c_char_p, []),
+    ("spec_pool_create", ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.POINTER(ctypes.c_void_p)]),
+    ("spec_pool_destroy", ctypes.c_int, [ctypes.c_void_p]),
+    ("spec_pool_reserve", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int]),
+    ("spec_pool_commit", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int, ctypes.c_int]),
+    ("spec_pool_release", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    ("spec_pool_share", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int, ctypes.c_int32]),
+    ("spec_pool_block_table", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, _I32P, ctypes.c_int, _I32P]),
+    ("spec_pool_refcount", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    ("spec_pool_free_count", ctypes.c_int, [ctypes.c_void_p]),
+]
+EXPORTS = [s[0] for s in _SIGS]
+
+
+def lib() -> ctypes.CDLL:
+    """Load libspec.so (built by ``build.py``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with lossless_speculative_decoding_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, res, args in _SIGS:
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def _check(rc: int) -> int:
+    if rc < 0:
+        raise SpecError(rc, lib().spec_last_error().decode())
+    return rc
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(_I32P)
+
+
+def _ptr(x) -> int:
+    """Device pointer of a torch tensor or a raw integer address."""
+    if x is None:
+        return 0
+    return int(x.data_ptr()) if hasattr(x, "data_ptr") else int(x)
+
+
+def make_config(**kw) -> spec_config:
+    c = spec_config()
+    c.rope_theta, c.rms_eps = 10000.0, 1e-6
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def spec_tensor_count(cfg: spec_config) -> int:
+    return _check(lib().spec_tensor_count(ctypes.byref(cfg)))
+
+
+def spec_tensor_bytes(cfg: spec_config, index: int) -> int:
+    return _check(lib().spec_tensor_bytes(ctypes.byref(cfg), index))
+
+
+def spec_init_model(cfg: spec_config, host_tensors: Sequence[np.ndarray], cuda_stream: int = 0) -> int:
+    n = spec_tensor_count(cfg)
+    if len(host_tensors) != n:
+        raise ValueError(f"expected {n} tensors, got {len(host_tensors)}")
+    arrs = [np.ascontiguousarray(a) for a in host_tensors]
+    for i, a in enumerate(arrs):
+        want = spec_tensor_bytes(cfg, i)
+        if a.nbytes != want:
+            raise ValueError(f"tensor {i}: {a.nbytes} bytes, expected {want}")
+    ptrs = (ctypes.c_void_p * n)(*[a.ctypes.data if a.nbytes else None for a in arrs])
+    out = ctypes.c_void_p()
+    _check(lib().spec_init_model(ctypes.byref(cfg), ptrs, cuda_stream, ctypes.byref(out)))
+    return out.value
+
+
+def spec_free_model(m: int) -> None:
+    _check(lib().spec_free_model(m))
+
+
+def spec_register_prefix(m: int, tokens) -> int:
+    t = _i32(tokens)
+    out = ctypes.c_int32()
+    _check(lib().spec_register_prefix(m, _p(t), len(t), ctypes.byref(out)))
+    return out.value
+
+
+def spec_release_prefix(m: int, prefix_id: int) -> None:
+    _check(lib().spec_release_prefix(m, prefix_id))
+
+
+def spec_prefill(m: int, seq_id: int, prefix_id: int, vis_embeds_dev, n_vis: int, tokens) -> int:
+    t = _i32(tokens if tokens is not None else [])
+    out = ctypes.c_int32()
+    _check(lib().spec_prefill(m, seq_id, prefix_id, _ptr(vis_embeds_dev), n_vis, _p(t), len(t), ctypes.byref(out)))
+    return out.value
+
+
+def spec_verify_step(m: int, seq_id: int, drafts) -> tuple:
+    d = _i32(drafts)
+    a, b = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().spec_verify_step(m, seq_id, _p(d), len(d), ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def spec_verify_step_batch(m: int, seq_ids, drafts, n_draft) -> tuple:
+    s, d, n = _i32(seq_ids), _i32(drafts), _i32(n_draft)
+    acc, bon = np.zeros(len(s), np.int32), np.zeros(len(s), np.int32)
+    _check(lib().spec_verify_step_batch(m, len(s), _p(s), _p(d), _p(n), _p(acc), _p(bon)))
+    return acc, bon
+
+
+def spec_verify_step_batch_dev(m: int, n_seq: int, seq_ids_dev, drafts_dev, n_draft_dev, out_acc_dev,
+                               out_bonus_dev) -> None:
+    _check(lib().spec_verify_step_batch_dev(m, n_seq, _ptr(seq_ids_dev), _ptr(drafts_dev), _ptr(n_draft_dev),
+                                            _ptr(out_acc_dev), _ptr(out_bonus_dev)))
+
+
+def spec_reserve_seq(m: int, seq_id: int, n_tokens: int) -> None:
+    _check(lib().spec_reserve_seq(m, seq_id, n_tokens))
+
+
+def spec_sync_seqs(m: int) -> None:
+    _check(lib().spec_sync_seqs(m))
+
+
+def spec_release_seq(m: int, seq_id: int) -> None:
+    _check(lib().spec_release_seq(m, seq_id))
+
+
+def spec_seq_info(m: int, seq_id: int) -> tuple:
+    n, g = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().spec_seq_info(m, seq_id, ctypes.byref(n), ctypes.byref(g)))
+    return n.value, g.value
+
+
+def spec_seq_tokens(m: int, seq_id: int) -> np.ndarray:
+    _, n = spec_seq_info(m, seq_id)
+    out = np.zeros(max(n, 1), np.int32)
+    k = _check(lib().spec_seq_tokens(m, seq_id, _p(out), n))
+    return out[:k]
+
+
+def spec_seq_block_table(m: int, seq_id: int, cap: int = 4096) -> np.ndarray:
+    out = np.full(cap, -1, np.int32)
+    n = ctypes.c_int32()
+    _check(lib().spec_seq_block_table(m, seq_id, _p(out), cap, ctypes.byref(n)))
+    return out[:n.value]
+
+
+def spec_free_pages(m: int) -> int:
+    return _check(lib().spec_free_pages(m))
+
+
+def spec_debug_logits(m: int, seq_ids, drafts, logits_dev) -> None:
+    s, d = _i32(seq_ids), _i32(drafts)
+    _check(lib().spec_debug_logits(m, len(s), _p(s), _p(d), _ptr(logits_dev)))
+
+
+def spec_step_launches(m: int, n_seq: int) -> int:
+    return _check(lib().spec_step_launches(m, n_seq))
+
+
+def spec_strerror(code: int) -> str:
+    return lib().spec_strerror(code).decode()
+
+
+# ---- host-only allocator ----------------------------------------------------
+def spec_pool_create(n_pages: int, page_size: int, max_seqs: int, max_pages_per_seq: int) -> int:
+    out = ctypes.c_void_p()
+    _check(lib().spec_pool_create(n_pages, page_size, max_seqs, max_pages_per_seq, ctypes.byref(out)))
+    return out.value
+
+
+def spec_pool_destroy(p: int) -> None:
+    _check(lib().spec_pool_destroy(p))
+
+
+def spec_pool_reserve(p: int, seq: int, n_tokens: int) -> int:
+    return lib().spec_pool_reserve(p, seq, n_tokens)
+
+
+def spec_pool_commit(p: int, seq: int, new_len: int, keep_pages: int = 0) -> int:
+    return lib().spec_pool_commit(p, seq, new_len, keep_pages)
+
+
+def spec_pool_release(p: int, seq: int) -> int:
+    return lib().spec_pool_release(p, seq)
+
+
+def spec_pool_share(p: int, src: int, n_pages: int, dst: int) -> int:
+    return lib().spec_pool_share(p, src, n_pages, dst)
+
+
+def spec_pool_block_table(p: int, seq: int, cap: int = 4096) -> list:
+    out = np.zeros(cap, np.int32)
+    n = ctypes.c_int32()
+    _check(lib().spec_pool_block_table(p, seq, _p(out), cap, ctypes.byref(n)))
+    return out[:n.value].tolist()
+
+
+def spec_pool_refcount(p: int, page: int) -> int:
+    return lib().spec_pool_refcount(p, page)
+
+
+def spec_pool_free_count(p: int) -> int:
+    return lib().spec_pool_free_count(p)

@@ -1,0 +1,291 @@
+// Small kernels of the verify step: RoPE tables, row assembly + embedding,
+// RMSNorm + router + top-k + token permutation, expert combine, and the
+// acceptance / KV-commit kernel.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace spec {
+
+// cos/sin of p * theta^(-2i/d) for every position and frequency, evaluated in
+// double precision and rounded once to fp32.
+__global__ void k_rope_table(int max_ctx, int half, int d, double theta, float* cos_t, float* sin_t) {
+  const size_t n = (size_t)max_ctx * half;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int p = (int)(i / half), j = (int)(i % half);
+    const double inv = pow(theta, -(2.0 * j) / (double)d);
+    const double a = (double)p * inv;
+    cos_t[i] = (float)cos(a);
+    sin_t[i] = (float)sin(a);
+  }
+}
+
+void launch_rope_table(const Dims& D, float* cos_t, float* sin_t, cudaStream_t st) {
+  k_rope_table<<<1024, 256, 0, st>>>(D.max_ctx, D.d / 2, D.d, (double)D.theta, cos_t, sin_t);
+}
+
+__device__ __forceinline__ void embed_row(const Dims& D, const void* tok_embed, int tok, float* x) {
+  for (int k = threadIdx.x; k < D.h; k += blockDim.x) x[k] = load_act(tok_embed, (size_t)tok * D.h + k, D.act_f32);
+}
+
+// Verify rows: for sequence slot s of the step, row j holds the last
+// committed token (j = 0) or draft j, at position seq_len + j.
+__global__ void k_assemble_verify(Dims D, DevState S, StepBuf B, const void* tok_embed, int n_seq, int K) {
+  const int R = K + 1;
+  const int row = blockIdx.x, s = row / R, j = row % R;
+  const int max_batch = B.max_batch;
+  const int seq = B.step_in[s];
+  int tok = j == 0 ? S.last_tok[seq] : B.step_in[max_batch + s * K + (j - 1)];
+  if (tok < 0 || tok >= D.V) {
+    if (threadIdx.x == 0) atomicOr(S.err, DERR_TOKEN);
+    tok = 0;
+  }
+  if (threadIdx.x == 0) {
+    B.row_tok[row] = tok;
+    B.row_pos[row] = S.seq_len[seq] + j;
+    B.row_seq[row] = seq;
+  }
+  embed_row(D, tok_embed, tok, B.x + (size_t)row * D.h);
+}
+
+// Prefill rows: row_src[i] >= 0 is a token id, row_src[i] < 0 selects visual
+// row -(row_src[i] + 1) of `vis` (activation storage type).
+__global__ void k_assemble_prefill(Dims D, DevState S, StepBuf B, const void* tok_embed, const void* vis,
+                                   int seq, int pos0) {
+  const int row = blockIdx.x;
+  const int src = B.row_src[row];
+  if (threadIdx.x == 0) {
+    B.row_tok[row] = src;
+    B.row_pos[row] = pos0 + row;
+    B.row_seq[row] = seq;
+  }
+  float* x = B.x + (size_t)row * D.h;
+  if (src >= 0) {
+    embed_row(D, tok_embed, src, x);
+  } else {
+    const size_t vr = (size_t)(-(src + 1));
+    for (int k = threadIdx.x; k < D.h; k += blockDim.x) x[k] = load_act(vis, vr * D.h + k, D.act_f32);
+  }
+}
+
+void launch_assemble_verify(const Dims& D, const DevState& S, const StepBuf& B, const void* tok_embed, int n_seq,
+                            int K, cudaStream_t st) {
+  k_assemble_verify<<<n_seq * (K + 1), 256, 0, st>>>(D, S, B, tok_embed, n_seq, K);
+}
+
+void launch_assemble_prefill(const Dims& D, const DevState& S, const StepBuf& B, const void* tok_embed,
+                             const void* vis, int seq, int pos0, int T, cudaStream_t st) {
+  k_assemble_prefill<<<T, 256, 0, st>>>(D, S, B, tok_embed, vis, seq, pos0);
+}
+
+// ---------------------------------------------------------------------------
+// FFN input RMSNorm + router + top-k, one block per row; the last block to
+// finish builds the per-expert pair lists. Probabilities: softmax over all E
+// experts; the top-k are taken in (probability desc, id asc) order and used
+// without renormalisation ("Jina AI releases jina-ocr-v1": 64 routed + 2
+// shared experts, top-6). Pair id = row * NS + slot (slots 0..k-1 routed,
+// k..k+S-1 shared). Active list: routed experts with rows, in id order, then
+// the shared experts with every row.
+template <class RT>
+__global__ void __launch_bounds__(256) k_router(Dims D, StepBuf B, const float* __restrict__ gamma,
+                                                const RT* __restrict__ Wr, int T) {
+  extern __shared__ __align__(16) float sm[];
+  float* u = sm;                 // [h]
+  float* logit = u + D.h;        // [E]
+  __shared__ float red[32];
+  __shared__ int s_last;
+  const int row = blockIdx.x;
+  const float* x = B.x + (size_t)row * D.h;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < D.h; k += blockDim.x) ss = fmaf(x[k], x[k], ss);
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / (float)D.h + D.eps);
+  for (int k = threadIdx.x; k < D.h; k += blockDim.x) {
+    const float v = (x[k] * inv) * gamma[k];
+    u[k] = v;
+    B.u[(size_t)row * D.h + k] = v;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (D.E > 0) {
+    constexpr int EP = Elt<RT>::per16;
+    for (int e = warp; e < D.E; e += blockDim.x / 32) {
+      float acc = 0.f;
+      for (int k = lane * EP; k < D.h; k += 32 * EP) {
+        float w[EP];
+        unpack<RT>(*reinterpret_cast<const uint4*>(Wr + (size_t)e * D.h + k), w);
+#pragma unroll
+        for (int i = 0; i < EP; ++i) acc = fmaf(w[i], u[k + i], acc);
+      }
+      acc = warp_sum(acc);
+      if (lane == 0) logit[e] = acc;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float m = -INFINITY;
+      for (int e = 0; e < D.E; ++e) m = fmaxf(m, logit[e]);
+      float z = 0.f;
+      for (int e = 0; e < D.E; ++e) { logit[e] = expf(logit[e] - m); z += logit[e]; }
+      for (int e = 0; e < D.E; ++e) logit[e] = logit[e] / z;
+      for (int i = 0; i < D.k; ++i) {
+        int best = -1;
+        for (int e = 0; e < D.E; ++e) {
+          if (logit[e] < 0.f) continue;              // already taken
+          if (best < 0 || logit[e] > logit[best]) best = e;
+        }
+        B.ids[row * D.k + i] = best;
+        B.wts[row * D.k + i] = logit[best];
+        logit[best] = -1.f;
+      }
+    }
+  }
+  // ---- last block builds the permutation ----
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int prev = atomicAdd(B.counter, 1);
+    s_last = (prev == (int)gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  int* cnt = reinterpret_cast<int*>(sm);          // reuse: [E] counts, [E] offsets
+  int* offs = cnt + (D.E > 0 ? D.E : 1);
+  const int nk = T * D.k;
+  for (int e = threadIdx.x; e < D.E; e += blockDim.x) {
+    int c = 0;
+    for (int j = 0; j < nk; ++j) c += (__ldcg(B.ids + j) == e);
+    cnt[e] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int o = 0, na = 0;
+    for (int e = 0; e < D.E; ++e) {
+      offs[e] = o;
+      if (cnt[e] > 0) {
+        B.act_expert[na] = e; B.act_off[na] = o; B.act_cnt[na] = cnt[e];
+        ++na;
+      }
+      o += cnt[e];
+    }
+    for (int s = 0; s < D.S; ++s) {
+      B.act_expert[na] = D.E + s; B.act_off[na] = nk + s * T; B.act_cnt[na] = T;
+      ++na;
+    }
+    *B.n_active = na;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < D.E; e += blockDim.x) {
+    if (cnt[e] == 0) continue;
+    int c = offs[e];
+    for (int j = 0; j < nk; ++j)
+      if (__ldcg(B.ids + j) == e) B.perm[c++] = (j / D.k) * D.NS + (j % D.k);
+  }
+  for (int i = threadIdx.x; i < D.S * T; i += blockDim.x) {
+    const int s = i / T, r = i % T;
+    B.perm[nk + i] = r * D.NS + D.k + s;
+  }
+  if (threadIdx.x == 0) *B.counter = 0;
+}
+
+cudaError_t configure_small_kernels() {
+  cudaError_t e = allow_dyn_smem(k_router<float>);
+  cudaError_t f = allow_dyn_smem(k_router<bf16_t>);
+  return e != cudaSuccess ? e : f;
+}
+
+void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
+  const size_t sm = (size_t)(D.h + (D.E > 0 ? D.E : 1) * 2) * sizeof(float);
+  if (D.act_f32) {
+    k_router<float><<<T, 256, sm, st>>>(D, B, W.ffn_norm, (const float*)W.w_router, T);
+  } else {
+    k_router<bf16_t><<<T, 256, sm, st>>>(D, B, W.ffn_norm, (const bf16_t*)W.w_router, T);
+  }
+}
+
+// x[r] += sum over slots (routed weight p, shared weight 1) of y[r*NS + slot],
+// slots in order.
+__global__ void k_combine(Dims D, StepBuf B) {
+  const int r = blockIdx.x;
+  for (int j = threadIdx.x; j < D.h; j += blockDim.x) {
+    float acc = 0.f;
+    for (int s = 0; s < D.NS; ++s) {
+      const float w = s < D.k ? B.wts[r * D.k + s] : 1.f;
+      acc = fmaf(w, B.y[((size_t)r * D.NS + s) * D.h + j], acc);
+    }
+    B.x[(size_t)r * D.h + j] += acc;
+  }
+}
+
+void launch_expert_gemvs(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
+
+void launch_experts(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
+  launch_expert_gemvs(D, B, W, T, st);
+  k_combine<<<T, 256, 0, st>>>(D, B);
+}
+
+// ---------------------------------------------------------------------------
+// Acceptance + commit, one thread per sequence of the step ("End-to-end OCR
+// expert model ...", section 6.1: accept the agreeing prefix from the left,
+// the target supplies the token at the first divergence). With g the greedy
+// tokens of the K+1 rows: a = max{i <= n_draft : d_j = g_(j-1) for j <= i},
+// bonus = g_a. The sequence keeps the KV of its last token and the a accepted
+// drafts (length n + a + 1); the rejected rows' slots are stale and are
+// overwritten by the next step. Pages wholly past max(new length, reserved
+// pages) leave the block table (-1); the host allocator mirrors this.
+__global__ void k_commit(Dims D, DevState S, StepBuf B, int n_seq, int K) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= n_seq) return;
+  const int max_batch = B.max_batch;
+  const int R = K + 1;
+  const int seq = B.step_in[s];
+  const int* d = B.step_in + max_batch + s * K;
+  const int nd = min(max(B.step_in[max_batch + max_batch * K + s], 0), K);
+  const int* g = B.g + s * R;
+  int a = 0;
+  while (a < nd && d[a] == g[a]) ++a;
+  const int bonus = g[a];
+  const int n = S.seq_len[seq];
+  const int new_len = n + a + 1;
+  int no = S.n_out[seq];
+  int* out = S.out_tok + (size_t)seq * D.max_ctx;
+  for (int j = 0; j < a; ++j)
+    if (no + j < D.max_ctx) out[no + j] = d[j];
+  if (no + a < D.max_ctx) out[no + a] = bonus;
+  S.n_out[seq] = no + a + 1;
+  S.seq_len[seq] = new_len;
+  S.last_tok[seq] = bonus;
+  int keep = (new_len + D.P - 1) / D.P;
+  if (S.keep_pages[seq] > keep) keep = S.keep_pages[seq];
+  int* bt = const_cast<int*>(S.bt) + (size_t)seq * D.max_pages;
+  for (int i = keep; i < D.max_pages; ++i) bt[i] = -1;
+  B.step_out[s] = a;
+  B.step_out[max_batch + s] = bonus;
+}
+
+void launch_commit(const Dims& D, const DevState& S, const StepBuf& B, int n_seq, int K, cudaStream_t st) {
+  k_commit<<<(n_seq + 63) / 64, 64, 0, st>>>(D, S, B, n_seq, K);
+}
+
+// Copy device-resident step inputs into the staging block.
+__global__ void k_stage_dev(StepBuf B, int n_seq, int K, const int* seq_ids, const int* drafts,
+                            const int* n_draft) {
+  const int max_batch = B.max_batch;
+  for (int i = threadIdx.x; i < n_seq; i += blockDim.x) {
+    B.step_in[i] = seq_ids[i];
+    B.step_in[max_batch + max_batch * K + i] = n_draft[i];
+  }
+  for (int i = threadIdx.x; i < n_seq * K; i += blockDim.x) B.step_in[max_batch + i] = drafts[i];
+}
+
+void launch_stage_dev(const StepBuf& B, int n_seq, int K, const int* seq_ids, const int* drafts,
+                      const int* n_draft, cudaStream_t st) {
+  k_stage_dev<<<1, 256, 0, st>>>(B, n_seq, K, seq_ids, drafts, n_draft);
+}
+
+int launches_per_step(const Dims& D) {
+  // assemble + per layer (qkv, attn part, attn merge, oproj, router, gate/up,
+  // down, combine) + lm head + argmax reduce + commit
+  return 1 + D.L * 8 + 2 + 1;
+}
+
+}  // namespace spec

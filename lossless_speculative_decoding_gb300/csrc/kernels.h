@@ -1,0 +1,110 @@
+// Internal launch interface of the verify-step kernels (not part of the C ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace spec {
+
+constexpr int ATT_CHUNK = 64;     // keys per split-KV chunk (fixed at absolute positions)
+constexpr int GEMV_TP = 4;        // activation rows per GEMV pass
+constexpr int GEMV_WARPS = 8;     // warps per GEMV block
+constexpr int GEMV_G = 4;         // 16-byte weight chunks loaded per lane before use
+
+struct LayerW {
+  const float* attn_norm;
+  const void* w_qkv; const float* s_qkv;
+  const void* w_o; const float* s_o;
+  const float* ffn_norm;
+  const void* w_router;
+  const void* w_gate; const float* s_gate;
+  const void* w_up; const float* s_up;
+  const void* w_down; const float* s_down;
+};
+
+// Shapes and device state shared by every kernel of a model.
+struct Dims {
+  int L, h, Hq, Hkv, d, E, k, S, inter, V;
+  int wdtype;            // 0 f32, 1 bf16, 2 fp8 (attention + experts)
+  int act_f32;           // KV cache / embeddings / LM head in f32 (else bf16)
+  int P;                 // page size
+  int max_pages;         // block-table row length
+  int max_ctx;
+  int NS;                // slots per row = k + S
+  float eps, theta;
+  size_t page_elems;     // elements per KV page (all layers)
+};
+
+struct DevState {
+  void* kv;              // [n_pages][L][2][Hkv][P][d]
+  const int* bt;         // [slots][max_pages]
+  int* seq_len;          // [slots]
+  int* last_tok;         // [slots]
+  int* keep_pages;       // [slots]
+  int* out_tok;          // [slots][max_ctx]
+  int* n_out;            // [slots]
+  const float* rope_cos; // [max_ctx][d/2]
+  const float* rope_sin;
+  int* err;              // device error bits
+};
+
+// Per-step scratch (sized for the largest T the model runs).
+struct StepBuf {
+  int* row_tok; int* row_pos; int* row_seq; int* row_src;
+  float* x;          // [T, h] residual stream
+  float* q;          // [T, Hq, d]
+  float* att_o;      // [T, Hq, n_chunk_max, d] partial outputs
+  float* att_ml;     // [T, Hq, n_chunk_max, 2] partial (max, sum)
+  float* o;          // [T, Hq*d]
+  float* u;          // [T, h] normed FFN input
+  int* ids; float* wts;              // [T, k]
+  int* perm;                         // [T*NS] pair ids grouped by expert
+  int* act_expert; int* act_off; int* act_cnt; int* n_active;  // active-expert list
+  int* counter;                      // arrival counters (kept at zero between launches)
+  float* h_act;      // [T*NS, inter]
+  float* y;          // [T*NS, h]
+  float* am_val; int* am_idx;        // [T, n_vocab_blocks] argmax partials
+  int* g;            // [T] greedy tokens
+  int* step_in;      // staging: [seq ids (max_batch) | drafts (max_batch*K) | n_draft (max_batch)]
+  int* step_out;     // staging: [acc (max_batch) | bonus (max_batch)]
+  int n_chunk_max;
+  int n_vblocks;
+  int max_batch;      // staging block capacity (sequences per step)
+};
+
+void launch_rope_table(const Dims& D, float* cos_t, float* sin_t, cudaStream_t st);
+void launch_assemble_verify(const Dims& D, const DevState& S, const StepBuf& B, const void* tok_embed,
+                            int n_seq, int K, cudaStream_t st);
+void launch_assemble_prefill(const Dims& D, const DevState& S, const StepBuf& B, const void* tok_embed,
+                             const void* vis, int seq, int pos0, int T, cudaStream_t st);
+void launch_qkv(const Dims& D, const DevState& S, const StepBuf& B, const LayerW& W, int layer, int T,
+                cudaStream_t st);
+void launch_attention(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
+                      cudaStream_t st);
+void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
+void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
+void launch_experts(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
+void launch_lmhead(const Dims& D, const StepBuf& B, const void* lm_head, const float* final_norm,
+                   const float* x, int T, float* logits_dbg, cudaStream_t st);
+void launch_commit(const Dims& D, const DevState& S, const StepBuf& B, int n_seq, int K, cudaStream_t st);
+void launch_stage_dev(const StepBuf& B, int n_seq, int K, const int* seq_ids, const int* drafts,
+                      const int* n_draft, cudaStream_t st);
+int launches_per_step(const Dims& D);
+// Opt a kernel in to the largest dynamic shared memory the device allows
+// next to its static shared memory (an upper bound: occupancy follows the
+// bytes each launch asks for). Called at model set-up, never during capture.
+template <class K>
+inline cudaError_t allow_dyn_smem(K kernel) {
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+  return e;
+}
+cudaError_t configure_gemv_kernels();
+cudaError_t configure_attn_kernels();
+cudaError_t configure_small_kernels();
+
+}  // namespace spec

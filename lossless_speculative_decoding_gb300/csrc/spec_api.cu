@@ -1,0 +1,734 @@
+// C-ABI runtime of the verify-step library: model state, weight upload,
+// prefill, verify steps (replayed as CUDA graphs per batch size), sequence
+// and prefix management over the paged KV pool.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "../../include/spec.h"
+#include "kernels.h"
+#include "kv_pool.h"
+
+using namespace spec;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+#define CU(call)                                                                   \
+  do {                                                                             \
+    cudaError_t e_ = (call);                                                       \
+    if (e_ != cudaSuccess)                                                         \
+      return fail(SPEC_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+constexpr int PER_LAYER = 13;
+constexpr int N_GLOBAL = 3;
+constexpr int MAX_PREFIXES = 16;
+
+int elt_bytes(int dtype) { return dtype == SPEC_F32 ? 4 : dtype == SPEC_BF16 ? 2 : 1; }
+
+// (bytes) of tensor `idx` for `c`; -1 for a bad index.
+int64_t tensor_bytes(const spec_config& c, int idx) {
+  const int64_t h = c.hidden, d = c.head_dim, V = c.vocab;
+  const int side = c.wdtype == SPEC_F32 ? SPEC_F32 : SPEC_BF16;
+  const bool fp8 = c.wdtype == SPEC_FP8;
+  const int64_t F = c.n_experts + c.n_shared, qkv = (int64_t)(c.n_q_heads + 2 * c.n_kv_heads) * d;
+  if (idx < 0 || idx >= N_GLOBAL + PER_LAYER * c.n_layers) return -1;
+  if (idx == 0 || idx == 2) return V * h * elt_bytes(side);
+  if (idx == 1) return h * 4;
+  const int j = (idx - N_GLOBAL) % PER_LAYER;
+  const int w = elt_bytes(c.wdtype);
+  switch (j) {
+    case 0: return h * 4;
+    case 1: return qkv * h * w;
+    case 2: return fp8 ? qkv * 4 : 0;
+    case 3: return h * c.n_q_heads * d * w;
+    case 4: return fp8 ? h * 4 : 0;
+    case 5: return h * 4;
+    case 6: return (int64_t)c.n_experts * h * elt_bytes(side);
+    case 7: return F * c.inter * h * w;
+    case 8: return fp8 ? F * c.inter * 4 : 0;
+    case 9: return F * c.inter * h * w;
+    case 10: return fp8 ? F * c.inter * 4 : 0;
+    case 11: return F * h * c.inter * w;
+    case 12: return fp8 ? F * h * 4 : 0;
+  }
+  return -1;
+}
+
+int check_config(const spec_config& c) {
+  if (c.n_layers < 1 || c.hidden < 64 || c.n_q_heads < 1 || c.n_kv_heads < 1 || c.vocab < 4)
+    return fail(SPEC_ERR_ARG, "config: non-positive shape");
+  if (c.head_dim != 64 && c.head_dim != 128) return fail(SPEC_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (c.n_q_heads % c.n_kv_heads) return fail(SPEC_ERR_ARG, "n_q_heads must be a multiple of n_kv_heads");
+  if (c.wdtype < SPEC_F32 || c.wdtype > SPEC_FP8) return fail(SPEC_ERR_ARG, "wdtype");
+  if (c.n_experts < 0 || c.top_k < 0 || c.n_shared < 0 || c.inter < 4) return fail(SPEC_ERR_ARG, "ffn shape");
+  if (c.n_experts > 0 && (c.top_k < 1 || c.top_k > c.n_experts || c.top_k > 16))
+    return fail(SPEC_ERR_ARG, "top_k must be in [1, min(n_experts, 16)]");
+  if (c.n_experts == 0 && (c.n_shared != 1 || c.top_k != 0))
+    return fail(SPEC_ERR_ARG, "a dense FFN is one shared expert with top_k = 0");
+  if (c.n_experts + c.n_shared < 1) return fail(SPEC_ERR_ARG, "no FFN experts");
+  if (c.page_size < 16 || c.page_size % 16) return fail(SPEC_ERR_ARG, "page_size must be a multiple of 16");
+  if (c.max_draft < 0 || c.max_draft > 31) return fail(SPEC_ERR_ARG, "max_draft must be in [0, 31]");
+  if (c.max_seqs < 1 || c.max_batch < 1 || c.max_batch > c.max_seqs) return fail(SPEC_ERR_ARG, "max_seqs/max_batch");
+  if (c.max_ctx < c.max_draft + 2) return fail(SPEC_ERR_ARG, "max_ctx too small");
+  if (c.n_pages < 1) return fail(SPEC_ERR_ARG, "n_pages");
+  const int w = elt_bytes(c.wdtype);
+  // 16-byte vector loads along every reduction dimension
+  if ((c.hidden * w) % 16 || (c.inter * w) % 16 || (c.n_q_heads * c.head_dim * w) % 16 ||
+      (c.hidden * elt_bytes(c.wdtype == SPEC_F32 ? SPEC_F32 : SPEC_BF16)) % 16)
+    return fail(SPEC_ERR_UNSUPPORTED, "reduction dims must be multiples of 16 bytes");
+  if (c.hidden % 4 || c.inter % 4 || c.vocab % 4) return fail(SPEC_ERR_UNSUPPORTED, "dims must be multiples of 4");
+  return SPEC_OK;
+}
+
+struct Prefix {
+  bool live = false;
+  int slot = -1;                 // hidden pool slot holding the prefix pages
+  std::vector<int32_t> tokens;
+  int full_pages = 0;
+};
+
+}  // namespace
+
+struct spec_model {
+  spec_config cfg{};
+  cudaStream_t stream = nullptr;
+  Dims D{};
+  DevState S{};
+  StepBuf B{};
+  int K = 0, R = 1, Tmax = 1, prefill_chunk = 256;
+  std::vector<void*> allocs;
+  std::vector<void*> wptr;         // device pointer per tensor (nullptr if absent)
+  std::vector<LayerW> layers;
+  void* tok_embed = nullptr;
+  void* lm_head = nullptr;
+  float* final_norm = nullptr;
+  std::unique_ptr<KvPool> pool;
+  int n_slots = 0;                 // max_seqs + MAX_PREFIXES
+  std::vector<char> busy;
+  std::vector<int32_t> seq_len_h, last_tok_h, keep_h;
+  std::vector<std::vector<int32_t>> gen;   // generated tokens (host view)
+  std::vector<int32_t> bt_h;               // host copy of the device block tables
+  std::vector<Prefix> prefixes;
+  std::map<int, cudaGraphExec_t> graphs;
+  int32_t* pin_in = nullptr;       // pinned staging (host)
+  int32_t* pin_out = nullptr;
+  int step_in_n = 0, step_out_n = 0;
+  bool host_dirty = false;         // device state newer than host view (after _dev steps)
+  bool own_stream = false;
+
+  ~spec_model() {
+    for (auto& g : graphs) cudaGraphExecDestroy(g.second);
+    if (own_stream) cudaStreamDestroy(stream);
+    for (void* p : allocs) cudaFree(p);
+    if (pin_in) cudaFreeHost(pin_in);
+    if (pin_out) cudaFreeHost(pin_out);
+  }
+
+  template <class T>
+  int dalloc(T** p, size_t n) {
+    void* q = nullptr;
+    if (n == 0) n = 1;
+    cudaError_t e = cudaMalloc(&q, n * sizeof(T));
+    if (e != cudaSuccess) return fail(SPEC_ERR_NOMEM, std::string("cudaMalloc: ") + cudaGetErrorString(e));
+    allocs.push_back(q);
+    *p = reinterpret_cast<T*>(q);
+    return SPEC_OK;
+  }
+
+  int check_err() {
+    int e = 0;
+    CU(cudaMemcpyAsync(&e, S.err, sizeof(int), cudaMemcpyDeviceToHost, stream));
+    CU(cudaStreamSynchronize(stream));
+    if (e) {
+      CU(cudaMemsetAsync(S.err, 0, sizeof(int), stream));
+      return fail(SPEC_ERR_STATE, "device error bits " + std::to_string(e) +
+                                       " (1 page, 2 token, 4 position out of range)");
+    }
+    return SPEC_OK;
+  }
+
+  // Upload block-table row of `slot` from the host allocator.
+  int push_table(int slot) {
+    const auto& t = pool->table(slot);
+    int32_t* row = bt_h.data() + (size_t)slot * D.max_pages;
+    std::fill(row, row + D.max_pages, -1);
+    std::copy(t.begin(), t.end(), row);
+    CU(cudaMemcpyAsync(const_cast<int*>(S.bt) + (size_t)slot * D.max_pages, row, D.max_pages * sizeof(int32_t),
+                       cudaMemcpyHostToDevice, stream));
+    return SPEC_OK;
+  }
+
+  int push_seq_scalars(int slot) {
+    CU(cudaMemcpyAsync(S.seq_len + slot, &seq_len_h[slot], 4, cudaMemcpyHostToDevice, stream));
+    CU(cudaMemcpyAsync(S.last_tok + slot, &last_tok_h[slot], 4, cudaMemcpyHostToDevice, stream));
+    CU(cudaMemcpyAsync(S.keep_pages + slot, &keep_h[slot], 4, cudaMemcpyHostToDevice, stream));
+    return SPEC_OK;
+  }
+
+  // Enqueue one forward over T rows already assembled in B (row meta + x).
+  void enqueue_layers(int T, int R_rows) {
+    for (int l = 0; l < D.L; ++l) {
+      const LayerW& W = layers[l];
+      launch_qkv(D, S, B, W, l, T, stream);
+      launch_attention(D, S, B, l, T, R_rows, stream);
+      launch_oproj(D, B, W, T, stream);
+      launch_router(D, B, W, T, stream);
+      launch_experts(D, B, W, T, stream);
+    }
+  }
+
+  void enqueue_verify(int n_seq, float* logits_dbg, bool commit) {
+    const int T = n_seq * R;
+    launch_assemble_verify(D, S, B, tok_embed, n_seq, K, stream);
+    enqueue_layers(T, R);
+    launch_lmhead(D, B, lm_head, final_norm, B.x, T, logits_dbg, stream);
+    if (commit) launch_commit(D, S, B, n_seq, K, stream);
+  }
+
+  int graph_for(int n_seq, cudaGraphExec_t* out) {
+    auto it = graphs.find(n_seq);
+    if (it != graphs.end()) { *out = it->second; return SPEC_OK; }
+    cudaGraph_t g;
+    CU(cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal));
+    enqueue_verify(n_seq, nullptr, true);
+    cudaError_t e = cudaStreamEndCapture(stream, &g);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, std::string("graph capture: ") + cudaGetErrorString(e));
+    cudaGraphExec_t ge;
+    e = cudaGraphInstantiate(&ge, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(e));
+    graphs[n_seq] = ge;
+    *out = ge;
+    return SPEC_OK;
+  }
+
+  bool seq_ok(int s) const { return s >= 0 && s < cfg.max_seqs && busy[s]; }
+};
+
+// ---------------------------------------------------------------------------
+extern "C" {
+
+const char* spec_strerror(int code) {
+  switch (code) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_ARG: return "invalid argument";
+    case SPEC_ERR_NO_PAGES: return "KV page pool exhausted";
+    case SPEC_ERR_CUDA: return "CUDA error";
+    case SPEC_ERR_STATE: return "invalid state";
+    case SPEC_ERR_NOMEM: return "out of memory";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported configuration";
+  }
+  return "unknown error";
+}
+
+const char* spec_last_error(void) { return g_last_error.c_str(); }
+
+int spec_tensor_count(const spec_config* cfg) {
+  if (!cfg || cfg->n_layers < 1) return fail(SPEC_ERR_ARG, "config");
+  return N_GLOBAL + PER_LAYER * cfg->n_layers;
+}
+
+int64_t spec_tensor_bytes(const spec_config* cfg, int index) {
+  if (!cfg) return fail(SPEC_ERR_ARG, "config");
+  const int64_t b = tensor_bytes(*cfg, index);
+  return b < 0 ? fail(SPEC_ERR_ARG, "tensor index") : b;
+}
+
+int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, uintptr_t cuda_stream,
+                     spec_model** out_model) {
+  if (!cfg_in || !out_model || !host_tensors) return fail(SPEC_ERR_ARG, "null argument");
+  *out_model = nullptr;
+  int rc = check_config(*cfg_in);
+  if (rc) return rc;
+  std::unique_ptr<spec_model> m(new spec_model());
+  spec_config& c = m->cfg;
+  c = *cfg_in;
+  m->stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+  if (m->stream == nullptr) {   // the legacy default stream cannot be captured into a graph
+    CU(cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking));
+    m->own_stream = true;
+  }
+  m->K = c.max_draft;
+  m->R = c.max_draft + 1;
+  m->prefill_chunk = c.prefill_chunk > 0 ? c.prefill_chunk : 256;
+  m->Tmax = std::max(c.max_batch * m->R, m->prefill_chunk);
+  Dims& D = m->D;
+  D.L = c.n_layers; D.h = c.hidden; D.Hq = c.n_q_heads; D.Hkv = c.n_kv_heads; D.d = c.head_dim;
+  D.E = c.n_experts; D.k = c.top_k; D.S = c.n_shared; D.inter = c.inter; D.V = c.vocab;
+  D.wdtype = c.wdtype; D.act_f32 = c.wdtype == SPEC_F32; D.P = c.page_size;
+  D.max_ctx = c.max_ctx; D.NS = c.top_k + c.n_shared; D.eps = c.rms_eps; D.theta = c.rope_theta;
+  D.max_pages = (c.max_ctx + c.page_size - 1) / c.page_size;
+  D.page_elems = (size_t)c.n_layers * 2 * c.n_kv_heads * c.page_size * c.head_dim;
+  const size_t kv_elt = D.act_f32 ? 4 : 2;
+
+  CU(configure_gemv_kernels());
+  CU(configure_attn_kernels());
+  CU(configure_small_kernels());
+
+  // ---- weights ----
+  const int nt = N_GLOBAL + PER_LAYER * c.n_layers;
+  m->wptr.assign(nt, nullptr);
+  for (int i = 0; i < nt; ++i) {
+    const int64_t nb = tensor_bytes(c, i);
+    if (nb == 0) continue;
+    if (!host_tensors[i]) return fail(SPEC_ERR_ARG, "missing tensor " + std::to_string(i));
+    char* p = nullptr;
+    if ((rc = m->dalloc(&p, (size_t)nb))) return rc;
+    CU(cudaMemcpy(p, host_tensors[i], (size_t)nb, cudaMemcpyHostToDevice));
+    m->wptr[i] = p;
+  }
+  m->tok_embed = m->wptr[0];
+  m->final_norm = (float*)m->wptr[1];
+  m->lm_head = m->wptr[2];
+  for (int l = 0; l < c.n_layers; ++l) {
+    void** w = m->wptr.data() + N_GLOBAL + PER_LAYER * l;
+    LayerW L;
+    L.attn_norm = (const float*)w[0]; L.w_qkv = w[1]; L.s_qkv = (const float*)w[2];
+    L.w_o = w[3]; L.s_o = (const float*)w[4]; L.ffn_norm = (const float*)w[5]; L.w_router = w[6];
+    L.w_gate = w[7]; L.s_gate = (const float*)w[8]; L.w_up = w[9]; L.s_up = (const float*)w[10];
+    L.w_down = w[11]; L.s_down = (const float*)w[12];
+    m->layers.push_back(L);
+  }
+
+  // ---- KV pool and sequence state ----
+  m->n_slots = c.max_seqs + MAX_PREFIXES;
+  m->pool.reset(new KvPool(c.n_pages, c.page_size, m->n_slots, D.max_pages));
+  if ((rc = m->dalloc((char**)&m->S.kv, (size_t)c.n_pages * D.page_elems * kv_elt))) return rc;
+  int* bt = nullptr;
+  if ((rc = m->dalloc(&bt, (size_t)m->n_slots * D.max_pages))) return rc;
+  m->S.bt = bt;
+  CU(cudaMemset(bt, 0xFF, (size_t)m->n_slots * D.max_pages * sizeof(int)));
+  if ((rc = m->dalloc(&m->S.seq_len, m->n_slots))) return rc;
+  if ((rc = m->dalloc(&m->S.last_tok, m->n_slots))) return rc;
+  if ((rc = m->dalloc(&m->S.keep_pages, m->n_slots))) return rc;
+  if ((rc = m->dalloc(&m->S.n_out, m->n_slots))) return rc;
+  if ((rc = m->dalloc(&m->S.out_tok, (size_t)m->n_slots * c.max_ctx))) return rc;
+  if ((rc = m->dalloc(&m->S.err, 1))) return rc;
+  CU(cudaMemset(m->S.seq_len, 0, m->n_slots * 4));
+  CU(cudaMemset(m->S.last_tok, 0, m->n_slots * 4));
+  CU(cudaMemset(m->S.keep_pages, 0, m->n_slots * 4));
+  CU(cudaMemset(m->S.n_out, 0, m->n_slots * 4));
+  CU(cudaMemset(m->S.err, 0, 4));
+  float *rc_cos = nullptr, *rc_sin = nullptr;
+  if ((rc = m->dalloc(&rc_cos, (size_t)c.max_ctx * (c.head_dim / 2)))) return rc;
+  if ((rc = m->dalloc(&rc_sin, (size_t)c.max_ctx * (c.head_dim / 2)))) return rc;
+  m->S.rope_cos = rc_cos;
+  m->S.rope_sin = rc_sin;
+  launch_rope_table(D, rc_cos, rc_sin, m->stream);
+  m->busy.assign(m->n_slots, 0);
+  m->seq_len_h.assign(m->n_slots, 0);
+  m->last_tok_h.assign(m->n_slots, 0);
+  m->keep_h.assign(m->n_slots, 0);
+  m->gen.assign(m->n_slots, {});
+  m->bt_h.assign((size_t)m->n_slots * D.max_pages, -1);
+  m->prefixes.assign(MAX_PREFIXES, Prefix());
+
+  // ---- step buffers ----
+  StepBuf& B = m->B;
+  const int T = m->Tmax, NS = D.NS;
+  B.n_chunk_max = (c.max_ctx + ATT_CHUNK - 1) / ATT_CHUNK;
+  B.n_vblocks = (c.vocab + GEMV_WARPS * 4 - 1) / (GEMV_WARPS * 4);
+  B.max_batch = c.max_batch;
+  const int max_active = (D.E > 0 ? std::min(D.E, T * std::max(D.k, 1)) : 0) + D.S;
+  if ((rc = m->dalloc(&B.row_tok, T)) || (rc = m->dalloc(&B.row_pos, T)) || (rc = m->dalloc(&B.row_seq, T)) ||
+      (rc = m->dalloc(&B.row_src, T)) || (rc = m->dalloc(&B.x, (size_t)T * D.h)) ||
+      (rc = m->dalloc(&B.q, (size_t)T * D.Hq * D.d)) ||
+      (rc = m->dalloc(&B.att_o, (size_t)T * D.Hq * B.n_chunk_max * D.d)) ||
+      (rc = m->dalloc(&B.att_ml, (size_t)T * D.Hq * B.n_chunk_max * 2)) ||
+      (rc = m->dalloc(&B.o, (size_t)T * D.Hq * D.d)) || (rc = m->dalloc(&B.u, (size_t)T * D.h)) ||
+      (rc = m->dalloc(&B.ids, (size_t)T * std::max(D.k, 1))) ||
+      (rc = m->dalloc(&B.wts, (size_t)T * std::max(D.k, 1))) || (rc = m->dalloc(&B.perm, (size_t)T * NS)) ||
+      (rc = m->dalloc(&B.act_expert, max_active)) || (rc = m->dalloc(&B.act_off, max_active)) ||
+      (rc = m->dalloc(&B.act_cnt, max_active)) || (rc = m->dalloc(&B.n_active, 1)) ||
+      (rc = m->dalloc(&B.counter, 4)) || (rc = m->dalloc(&B.h_act, (size_t)T * NS * D.inter)) ||
+      (rc = m->dalloc(&B.y, (size_t)T * NS * D.h)) ||
+      (rc = m->dalloc(&B.am_val, (size_t)T * B.n_vblocks)) || (rc = m->dalloc(&B.am_idx, (size_t)T * B.n_vblocks)) ||
+      (rc = m->dalloc(&B.g, T)))
+    return rc;
+  m->step_in_n = c.max_batch * (2 + m->K);
+  m->step_out_n = 2 * c.max_batch;
+  if ((rc = m->dalloc(&B.step_in, m->step_in_n)) || (rc = m->dalloc(&B.step_out, m->step_out_n))) return rc;
+  CU(cudaMemset(B.counter, 0, 4 * sizeof(int)));
+  CU(cudaMemset(B.step_in, 0, m->step_in_n * sizeof(int)));
+  CU(cudaMallocHost(&m->pin_in, std::max(m->step_in_n, T) * sizeof(int32_t)));
+  CU(cudaMallocHost(&m->pin_out, std::max(m->step_out_n, T) * sizeof(int32_t)));
+  CU(cudaStreamSynchronize(m->stream));
+  CU(cudaGetLastError());
+  *out_model = m.release();
+  return SPEC_OK;
+}
+
+int spec_free_model(spec_model* m) {
+  if (!m) return fail(SPEC_ERR_ARG, "null model");
+  cudaStreamSynchronize(m->stream);
+  delete m;
+  return SPEC_OK;
+}
+
+// Run the prompt rows [start, start + n) of slot `slot` (rows described by
+// `src`: token id >= 0 or -(visual row + 1)); returns the greedy token of the
+// last row in *out_tok when out_tok != nullptr.
+static int run_prefill_rows(spec_model* m, int slot, const std::vector<int32_t>& src, int start,
+                            const void* vis, int32_t* out_tok) {
+  const int n = (int)src.size();
+  int first = -1;
+  for (int c0 = 0; c0 < n; c0 += m->prefill_chunk) {
+    const int T = std::min(m->prefill_chunk, n - c0);
+    std::memcpy(m->pin_in, src.data() + c0, T * sizeof(int32_t));
+    CU(cudaMemcpyAsync(m->B.row_src, m->pin_in, T * sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
+    launch_assemble_prefill(m->D, m->S, m->B, m->tok_embed, vis, slot, start + c0, T, m->stream);
+    m->enqueue_layers(T, T);
+    if (c0 + T == n && out_tok) {
+      launch_lmhead(m->D, m->B, m->lm_head, m->final_norm, m->B.x + (size_t)(T - 1) * m->D.h, 1, nullptr,
+                    m->stream);
+      CU(cudaMemcpyAsync(m->pin_out, m->B.g, sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
+    }
+    // the staging buffer is reused by the next chunk
+    CU(cudaStreamSynchronize(m->stream));
+    CU(cudaGetLastError());
+    if (c0 + T == n && out_tok) first = m->pin_out[0];
+  }
+  int rc = m->check_err();
+  if (rc) return rc;
+  if (out_tok) *out_tok = first;
+  return SPEC_OK;
+}
+
+int spec_register_prefix(spec_model* m, const int32_t* tok, int n_tok, int32_t* out_prefix_id) {
+  if (!m || !tok || n_tok < 1 || !out_prefix_id) return fail(SPEC_ERR_ARG, "bad prefix arguments");
+  for (int i = 0; i < n_tok; ++i)
+    if (tok[i] < 0 || tok[i] >= m->cfg.vocab) return fail(SPEC_ERR_ARG, "prefix token out of range");
+  if (n_tok + m->R + 1 > m->cfg.max_ctx) return fail(SPEC_ERR_ARG, "prefix longer than max_ctx");
+  int id = -1;
+  for (int i = 0; i < MAX_PREFIXES; ++i)
+    if (!m->prefixes[i].live) { id = i; break; }
+  if (id < 0) return fail(SPEC_ERR_STATE, "no free prefix slot");
+  const int slot = m->cfg.max_seqs + id;
+  int rc = m->pool->reserve(slot, n_tok);
+  if (rc) return fail(rc, "prefix: KV pool exhausted");
+  if ((rc = m->push_table(slot))) { m->pool->release(slot); return rc; }
+  std::vector<int32_t> src(tok, tok + n_tok);
+  rc = run_prefill_rows(m, slot, src, 0, nullptr, nullptr);
+  if (rc) { m->pool->release(slot); m->push_table(slot); return rc; }
+  Prefix& p = m->prefixes[id];
+  p.live = true;
+  p.slot = slot;
+  p.tokens = src;
+  p.full_pages = n_tok / m->cfg.page_size;
+  // keep only the full pages: the partial tail is recomputed by each user
+  m->pool->commit(slot, p.full_pages * m->cfg.page_size, 0);
+  if ((rc = m->push_table(slot))) return rc;
+  CU(cudaStreamSynchronize(m->stream));
+  *out_prefix_id = id;
+  return SPEC_OK;
+}
+
+int spec_release_prefix(spec_model* m, int32_t prefix_id) {
+  if (!m || prefix_id < 0 || prefix_id >= MAX_PREFIXES || !m->prefixes[prefix_id].live)
+    return fail(SPEC_ERR_ARG, "bad prefix id");
+  Prefix& p = m->prefixes[prefix_id];
+  m->pool->release(p.slot);
+  int rc = m->push_table(p.slot);
+  p = Prefix();
+  CU(cudaStreamSynchronize(m->stream));
+  return rc;
+}
+
+int spec_prefill(spec_model* m, int32_t seq_id, int32_t prefix_id, const void* vis_embeds_dev, int n_vis,
+                 const int32_t* tok, int n_tok, int32_t* out_first_token) {
+  if (!m || !out_first_token || n_vis < 0 || n_tok < 0 || (n_tok > 0 && !tok) || (n_vis > 0 && !vis_embeds_dev))
+    return fail(SPEC_ERR_ARG, "bad prefill arguments");
+  if (seq_id < 0 || seq_id >= m->cfg.max_seqs) return fail(SPEC_ERR_ARG, "seq_id out of range");
+  if (m->busy[seq_id]) return fail(SPEC_ERR_STATE, "sequence slot busy");
+  if (m->host_dirty) return fail(SPEC_ERR_STATE, "call spec_sync_seqs after device-resident steps");
+  const Prefix* pre = nullptr;
+  if (prefix_id >= 0) {
+    if (prefix_id >= MAX_PREFIXES || !m->prefixes[prefix_id].live) return fail(SPEC_ERR_ARG, "bad prefix id");
+    pre = &m->prefixes[prefix_id];
+  }
+  for (int i = 0; i < n_tok; ++i)
+    if (tok[i] < 0 || tok[i] >= m->cfg.vocab) return fail(SPEC_ERR_ARG, "token out of range");
+  const int n_pre = pre ? (int)pre->tokens.size() : 0;
+  const int len = n_pre + n_vis + n_tok;
+  if (len < 1) return fail(SPEC_ERR_ARG, "empty prompt");
+  if (len + m->R > m->cfg.max_ctx) return fail(SPEC_ERR_ARG, "prompt + draft rows exceed max_ctx");
+  KvPool& pool = *m->pool;
+  int start = 0;
+  if (pre && pre->full_pages > 0) {
+    int rc = pool.share(pre->slot, pre->full_pages, seq_id);
+    if (rc) return fail(rc, "prefix share failed");
+    start = pre->full_pages * m->cfg.page_size;
+  }
+  int rc = pool.reserve(seq_id, len + m->R);
+  if (rc) { pool.release(seq_id); return fail(rc, "KV pool exhausted"); }
+  if ((rc = m->push_table(seq_id))) { pool.release(seq_id); return rc; }
+  std::vector<int32_t> src;
+  src.reserve(len - start);
+  for (int p = start; p < len; ++p) {
+    if (p < n_pre) src.push_back(pre->tokens[p]);
+    else if (p < n_pre + n_vis) src.push_back(-(p - n_pre) - 1);
+    else src.push_back(tok[p - n_pre - n_vis]);
+  }
+  int32_t first = -1;
+  rc = run_prefill_rows(m, seq_id, src, start, vis_embeds_dev, &first);
+  if (rc) { pool.release(seq_id); m->push_table(seq_id); return rc; }
+  m->busy[seq_id] = 1;
+  m->seq_len_h[seq_id] = len;
+  m->last_tok_h[seq_id] = first;
+  m->keep_h[seq_id] = 0;
+  m->gen[seq_id].assign(1, first);
+  pool.set_length(seq_id, len);
+  int one = 1;
+  if ((rc = m->push_seq_scalars(seq_id))) return rc;
+  CU(cudaMemcpyAsync(m->S.out_tok + (size_t)seq_id * m->cfg.max_ctx, &first, 4, cudaMemcpyHostToDevice, m->stream));
+  CU(cudaMemcpyAsync(m->S.n_out + seq_id, &one, 4, cudaMemcpyHostToDevice, m->stream));
+  CU(cudaStreamSynchronize(m->stream));
+  *out_first_token = first;
+  return SPEC_OK;
+}
+
+// Host-mode step common to spec_verify_step(_batch) and spec_debug_logits.
+static int verify_host(spec_model* m, int n_seq, const int32_t* seq_ids, const int32_t* drafts,
+                       const int32_t* n_draft, int32_t* out_acc, int32_t* out_bonus, float* logits_dev) {
+  if (!m || n_seq < 1 || n_seq > m->cfg.max_batch || !seq_ids) return fail(SPEC_ERR_ARG, "bad batch");
+  if (m->K > 0 && !drafts) return fail(SPEC_ERR_ARG, "null drafts");
+  if (m->host_dirty) return fail(SPEC_ERR_STATE, "call spec_sync_seqs after device-resident steps");
+  const int K = m->K, mb = m->cfg.max_batch;
+  for (int s = 0; s < n_seq; ++s) {
+    const int q = seq_ids[s];
+    if (!m->seq_ok(q)) return fail(SPEC_ERR_ARG, "sequence " + std::to_string(q) + " not prefilled");
+    for (int t = 0; t < s; ++t)
+      if (seq_ids[t] == q) return fail(SPEC_ERR_ARG, "duplicate sequence in batch");
+    const int nd = n_draft ? n_draft[s] : K;
+    if (nd < 0 || nd > K) return fail(SPEC_ERR_ARG, "n_draft out of range");
+    for (int j = 0; j < K; ++j) {
+      const int d = drafts[s * K + j];
+      if (j < nd && (d < 0 || d >= m->cfg.vocab)) return fail(SPEC_ERR_ARG, "draft token out of range");
+    }
+    if (m->seq_len_h[q] + m->R > m->cfg.max_ctx) return fail(SPEC_ERR_ARG, "sequence reached max_ctx");
+  }
+  // a0: pages for positions n .. n+K of every sequence
+  for (int s = 0; s < n_seq; ++s) {
+    const int q = seq_ids[s];
+    const size_t before = m->pool->table(q).size();
+    int rc = m->pool->reserve(q, m->seq_len_h[q] + m->R);
+    if (rc) return fail(rc, "KV pool exhausted");
+    if (m->pool->table(q).size() != before && (rc = m->push_table(q))) return rc;
+  }
+  int32_t* in = m->pin_in;
+  std::fill(in, in + m->step_in_n, 0);
+  for (int s = 0; s < n_seq; ++s) {
+    in[s] = seq_ids[s];
+    const int nd = n_draft ? n_draft[s] : K;
+    for (int j = 0; j < K; ++j) in[mb + s * K + j] = (j < nd && drafts) ? drafts[s * K + j] : 0;
+    in[mb + mb * K + s] = nd;
+  }
+  CU(cudaMemcpyAsync(m->B.step_in, in, m->step_in_n * sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
+  if (logits_dev) {
+    m->enqueue_verify(n_seq, logits_dev, false);
+    CU(cudaStreamSynchronize(m->stream));
+    CU(cudaGetLastError());
+    return m->check_err();
+  }
+  cudaGraphExec_t ge;
+  int rc = m->graph_for(n_seq, &ge);
+  if (rc) return rc;
+  CU(cudaGraphLaunch(ge, m->stream));
+  CU(cudaMemcpyAsync(m->pin_out, m->B.step_out, m->step_out_n * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                     m->stream));
+  CU(cudaStreamSynchronize(m->stream));
+  if ((rc = m->check_err())) return rc;
+  for (int s = 0; s < n_seq; ++s) {
+    const int q = seq_ids[s];
+    const int a = m->pin_out[s], bonus = m->pin_out[mb + s];
+    const int nd = n_draft ? n_draft[s] : K;
+    for (int j = 0; j < a; ++j) m->gen[q].push_back(drafts[s * K + j]);
+    m->gen[q].push_back(bonus);
+    m->seq_len_h[q] += a + 1;
+    m->last_tok_h[q] = bonus;
+    // mirror the device-side trim of the block table
+    m->pool->commit(q, m->seq_len_h[q], m->keep_h[q]);
+    int32_t* row = m->bt_h.data() + (size_t)q * m->D.max_pages;
+    const auto& t = m->pool->table(q);
+    std::fill(row, row + m->D.max_pages, -1);
+    std::copy(t.begin(), t.end(), row);
+    (void)nd;
+    if (out_acc) out_acc[s] = a;
+    if (out_bonus) out_bonus[s] = bonus;
+  }
+  return SPEC_OK;
+}
+
+int spec_verify_step(spec_model* m, int32_t seq_id, const int32_t* draft_tokens, int n_draft,
+                     int32_t* out_accepted_len, int32_t* out_bonus_token) {
+  if (!m) return fail(SPEC_ERR_ARG, "null model");
+  if (n_draft < 0 || n_draft > m->K || (n_draft > 0 && !draft_tokens)) return fail(SPEC_ERR_ARG, "bad drafts");
+  std::vector<int32_t> d(std::max(m->K, 1), 0);
+  for (int j = 0; j < n_draft; ++j) d[j] = draft_tokens[j];
+  return verify_host(m, 1, &seq_id, d.data(), &n_draft, out_accepted_len, out_bonus_token, nullptr);
+}
+
+int spec_verify_step_batch(spec_model* m, int n_seq, const int32_t* seq_ids, const int32_t* drafts,
+                           const int32_t* n_draft, int32_t* out_accepted, int32_t* out_bonus) {
+  if (!out_accepted || !out_bonus) return fail(SPEC_ERR_ARG, "null outputs");
+  return verify_host(m, n_seq, seq_ids, drafts, n_draft, out_accepted, out_bonus, nullptr);
+}
+
+int spec_debug_logits(spec_model* m, int n_seq, const int32_t* seq_ids, const int32_t* drafts, float* logits_dev) {
+  if (!logits_dev) return fail(SPEC_ERR_ARG, "null logits buffer");
+  return verify_host(m, n_seq, seq_ids, drafts, nullptr, nullptr, nullptr, logits_dev);
+}
+
+int spec_verify_step_batch_dev(spec_model* m, int n_seq, const int32_t* seq_ids_dev, const int32_t* drafts_dev,
+                               const int32_t* n_draft_dev, int32_t* out_accepted_dev, int32_t* out_bonus_dev) {
+  if (!m || n_seq < 1 || n_seq > m->cfg.max_batch || !seq_ids_dev || !n_draft_dev ||
+      (m->K > 0 && !drafts_dev) || !out_accepted_dev || !out_bonus_dev)
+    return fail(SPEC_ERR_ARG, "bad device step arguments");
+  cudaGraphExec_t ge;
+  int rc = m->graph_for(n_seq, &ge);
+  if (rc) return rc;
+  launch_stage_dev(m->B, n_seq, m->K, seq_ids_dev, drafts_dev, n_draft_dev, m->stream);
+  CU(cudaGraphLaunch(ge, m->stream));
+  CU(cudaMemcpyAsync(out_accepted_dev, m->B.step_out, n_seq * sizeof(int32_t), cudaMemcpyDeviceToDevice, m->stream));
+  CU(cudaMemcpyAsync(out_bonus_dev, m->B.step_out + m->cfg.max_batch, n_seq * sizeof(int32_t),
+                     cudaMemcpyDeviceToDevice, m->stream));
+  m->host_dirty = true;
+  return SPEC_OK;
+}
+
+int spec_reserve_seq(spec_model* m, int32_t seq_id, int n_tokens) {
+  if (!m || !m->seq_ok(seq_id) || n_tokens < 0 || n_tokens > m->cfg.max_ctx) return fail(SPEC_ERR_ARG, "bad reserve");
+  if (m->host_dirty) return fail(SPEC_ERR_STATE, "call spec_sync_seqs after device-resident steps");
+  int rc = m->pool->reserve(seq_id, n_tokens);
+  if (rc) return fail(rc, "KV pool exhausted");
+  m->keep_h[seq_id] = KvPool::pages_for(n_tokens, m->cfg.page_size);
+  if ((rc = m->push_table(seq_id)) || (rc = m->push_seq_scalars(seq_id))) return rc;
+  CU(cudaStreamSynchronize(m->stream));
+  return SPEC_OK;
+}
+
+int spec_sync_seqs(spec_model* m) {
+  if (!m) return fail(SPEC_ERR_ARG, "null model");
+  CU(cudaStreamSynchronize(m->stream));
+  int rc = m->check_err();
+  if (rc) return rc;
+  const int ns = m->cfg.max_seqs;
+  std::vector<int32_t> len(ns), last(ns), nout(ns);
+  CU(cudaMemcpy(len.data(), m->S.seq_len, ns * 4, cudaMemcpyDeviceToHost));
+  CU(cudaMemcpy(last.data(), m->S.last_tok, ns * 4, cudaMemcpyDeviceToHost));
+  CU(cudaMemcpy(nout.data(), m->S.n_out, ns * 4, cudaMemcpyDeviceToHost));
+  for (int q = 0; q < ns; ++q) {
+    if (!m->busy[q]) continue;
+    const int n = std::min(nout[q], m->cfg.max_ctx);
+    m->gen[q].resize(n);
+    if (n) CU(cudaMemcpy(m->gen[q].data(), m->S.out_tok + (size_t)q * m->cfg.max_ctx, n * 4, cudaMemcpyDeviceToHost));
+    m->seq_len_h[q] = len[q];
+    m->last_tok_h[q] = last[q];
+    m->pool->commit(q, len[q], m->keep_h[q]);
+    int32_t* row = m->bt_h.data() + (size_t)q * m->D.max_pages;
+    const auto& t = m->pool->table(q);
+    std::fill(row, row + m->D.max_pages, -1);
+    std::copy(t.begin(), t.end(), row);
+  }
+  m->host_dirty = false;
+  return SPEC_OK;
+}
+
+int spec_release_seq(spec_model* m, int32_t seq_id) {
+  if (!m || !m->seq_ok(seq_id)) return fail(SPEC_ERR_ARG, "sequence not active");
+  if (m->host_dirty) return fail(SPEC_ERR_STATE, "call spec_sync_seqs after device-resident steps");
+  m->pool->release(seq_id);
+  m->busy[seq_id] = 0;
+  m->seq_len_h[seq_id] = 0;
+  m->keep_h[seq_id] = 0;
+  m->gen[seq_id].clear();
+  int rc = m->push_table(seq_id);
+  if (rc) return rc;
+  if ((rc = m->push_seq_scalars(seq_id))) return rc;
+  CU(cudaStreamSynchronize(m->stream));
+  return SPEC_OK;
+}
+
+int spec_seq_info(spec_model* m, int32_t seq_id, int32_t* out_len, int32_t* out_n_generated) {
+  if (!m || !m->seq_ok(seq_id)) return fail(SPEC_ERR_ARG, "sequence not active");
+  if (out_len) *out_len = m->seq_len_h[seq_id];
+  if (out_n_generated) *out_n_generated = (int32_t)m->gen[seq_id].size();
+  return SPEC_OK;
+}
+
+int spec_seq_tokens(spec_model* m, int32_t seq_id, int32_t* out_tokens, int cap) {
+  if (!m || !m->seq_ok(seq_id) || !out_tokens || cap < 0) return fail(SPEC_ERR_ARG, "bad arguments");
+  const auto& g = m->gen[seq_id];
+  const int n = std::min<int>(cap, (int)g.size());
+  std::copy(g.begin(), g.begin() + n, out_tokens);
+  return n;
+}
+
+int spec_seq_block_table(spec_model* m, int32_t seq_id, int32_t* out_pages, int cap, int32_t* out_n) {
+  if (!m || seq_id < 0 || seq_id >= m->n_slots || !out_pages || cap < 0) return fail(SPEC_ERR_ARG, "bad arguments");
+  std::vector<int32_t> row(m->D.max_pages);
+  CU(cudaStreamSynchronize(m->stream));
+  CU(cudaMemcpy(row.data(), m->S.bt + (size_t)seq_id * m->D.max_pages, m->D.max_pages * 4, cudaMemcpyDeviceToHost));
+  int n = 0;
+  while (n < m->D.max_pages && row[n] >= 0) ++n;
+  for (int i = 0; i < std::min(cap, m->D.max_pages); ++i) out_pages[i] = row[i];
+  if (out_n) *out_n = n;
+  return SPEC_OK;
+}
+
+int spec_free_pages(spec_model* m) {
+  if (!m) return fail(SPEC_ERR_ARG, "null model");
+  return m->pool->free_count();
+}
+
+int spec_step_launches(spec_model* m, int n_seq) {
+  if (!m || n_seq < 1) return fail(SPEC_ERR_ARG, "bad arguments");
+  return launches_per_step(m->D);
+}
+
+// ---- host-only allocator entry points --------------------------------------
+struct spec_pool { KvPool p; spec_pool(int a, int b, int c, int d) : p(a, b, c, d) {} };
+
+int spec_pool_create(int n_pages, int page_size, int max_seqs, int max_pages_per_seq, spec_pool** out) {
+  if (!out || n_pages < 1 || page_size < 1 || max_seqs < 1 || max_pages_per_seq < 1)
+    return fail(SPEC_ERR_ARG, "bad pool shape");
+  *out = new spec_pool(n_pages, page_size, max_seqs, max_pages_per_seq);
+  return SPEC_OK;
+}
+int spec_pool_destroy(spec_pool* p) { delete p; return SPEC_OK; }
+int spec_pool_reserve(spec_pool* p, int32_t seq, int n_tokens) {
+  return p ? p->p.reserve(seq, n_tokens) : SPEC_ERR_ARG;
+}
+int spec_pool_commit(spec_pool* p, int32_t seq, int new_len, int keep_pages) {
+  return p ? p->p.commit(seq, new_len, keep_pages) : SPEC_ERR_ARG;
+}
+int spec_pool_release(spec_pool* p, int32_t seq) { return p ? p->p.release(seq) : SPEC_ERR_ARG; }
+int spec_pool_share(spec_pool* p, int32_t src_seq, int n_pages, int32_t dst) {
+  return p ? p->p.share(src_seq, n_pages, dst) : SPEC_ERR_ARG;
+}
+int spec_pool_block_table(spec_pool* p, int32_t seq, int32_t* out, int cap, int32_t* out_n) {
+  if (!p || !p->p.valid_seq(seq) || !out) return SPEC_ERR_ARG;
+  const auto& t = p->p.table(seq);
+  const int n = std::min<int>(cap, (int)t.size());
+  std::copy(t.begin(), t.begin() + n, out);
+  if (out_n) *out_n = (int32_t)t.size();
+  return SPEC_OK;
+}
+int spec_pool_refcount(spec_pool* p, int32_t page) { return p ? p->p.refcount(page) : SPEC_ERR_ARG; }
+int spec_pool_free_count(spec_pool* p) { return p ? p->p.free_count() : SPEC_ERR_ARG; }
+
+}  // extern "C"

@@ -1,0 +1,100 @@
+"""Object wrapper over the C ABI: one model handle plus convenience calls.
+
+Device memory for visual-embedding rows and step buffers comes from PyTorch;
+every computation runs in libspec.so. ``cfg`` may be any object with the
+decoder shape attributes (n_layers, hidden, n_q_heads, n_kv_heads, head_dim,
+n_experts, top_k, n_shared, inter, vocab, wdtype, rope_theta, rms_eps).
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import numpy as np
+
+from . import binding as B
+
+
+def bf16_bits(a: np.ndarray) -> np.ndarray:
+    """float32 values that are already bf16-exact -> their bf16 bit patterns."""
+    b = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    if np.any(b & 0xFFFF):
+        raise ValueError("visual rows of a bf16 model must be bf16-exact")
+    return (b >> 16).astype(np.uint16)
+
+
+class SpecModel:
+    def __init__(self, cfg, tensors: Sequence[np.ndarray], *, page_size: int = 16, n_pages: int = 1024,
+                 max_seqs: int = 1, max_ctx: int = 2048, max_draft: int = 3, max_batch: Optional[int] = None,
+                 prefill_chunk: int = 0, stream=None):
+        import torch
+        self.torch = torch
+        self.cfg = cfg
+        self.stream = stream if stream is not None else torch.cuda.Stream()
+        self.c = B.make_config(
+            n_layers=cfg.n_layers, hidden=cfg.hidden, n_q_heads=cfg.n_q_heads, n_kv_heads=cfg.n_kv_heads,
+            head_dim=cfg.head_dim, n_experts=cfg.n_experts, top_k=cfg.top_k, n_shared=cfg.n_shared,
+            inter=cfg.inter, vocab=cfg.vocab, wdtype=cfg.wdtype, page_size=page_size, n_pages=n_pages,
+            max_seqs=max_seqs, max_ctx=max_ctx, max_draft=max_draft,
+            max_batch=max_batch if max_batch is not None else max_seqs, prefill_chunk=prefill_chunk,
+            rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps)
+        self.K = max_draft
+        self.h = B.spec_init_model(self.c, tensors, int(self.stream.cuda_stream))
+
+    def close(self) -> None:
+        if self.h:
+            B.spec_free_model(self.h)
+            self.h = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- prompts ---------------------------------------------------------------
+    def visual_to_device(self, visual: np.ndarray):
+        torch = self.torch
+        if len(visual) == 0:
+            return None
+        if self.cfg.wdtype == B.SPEC_F32:
+            return torch.from_numpy(np.ascontiguousarray(visual, np.float32)).cuda()
+        return torch.from_numpy(bf16_bits(visual).view(np.int16)).cuda()
+
+    def _ready(self, t):
+        # uploads run on torch's current stream; the library uses its own
+        self.torch.cuda.current_stream().synchronize()
+        return t
+
+    def prefill(self, seq: int, visual: np.ndarray, tokens, prefix_id: int = -1) -> int:
+        dev = self._ready(self.visual_to_device(visual))
+        return B.spec_prefill(self.h, seq, prefix_id, dev, len(visual), tokens)
+
+    def register_prefix(self, tokens) -> int:
+        return B.spec_register_prefix(self.h, tokens)
+
+    # -- steps -----------------------------------------------------------------
+    def verify(self, seq: int, drafts) -> tuple:
+        return B.spec_verify_step(self.h, seq, drafts)
+
+    def verify_batch(self, seq_ids, drafts: np.ndarray, n_draft) -> tuple:
+        return B.spec_verify_step_batch(self.h, seq_ids, np.asarray(drafts, np.int32).reshape(-1), n_draft)
+
+    def debug_logits(self, seq_ids, drafts: np.ndarray) -> np.ndarray:
+        torch = self.torch
+        n = len(seq_ids) * (self.K + 1)
+        out = self._ready(torch.empty((n, self.cfg.vocab), dtype=torch.float32, device="cuda"))
+        B.spec_debug_logits(self.h, seq_ids, np.asarray(drafts, np.int32).reshape(-1), out)
+        self.stream.synchronize()
+        return out.cpu().numpy()
+
+    def tokens(self, seq: int) -> np.ndarray:
+        return B.spec_seq_tokens(self.h, seq)
+
+    def length(self, seq: int) -> int:
+        return B.spec_seq_info(self.h, seq)[0]
+
+    def block_table(self, seq: int) -> np.ndarray:
+        return B.spec_seq_block_table(self.h, seq)
+
+    def release(self, seq: int) -> None:
+        B.spec_release_seq(self.h, seq)
