@@ -184,6 +184,29 @@ int spec_debug_logits(spec_model* m, int n_seq, const int32_t* seq_ids,
 /* Number of kernel launches one verify step of n_seq sequences enqueues. */
 int spec_step_launches(spec_model* m, int n_seq);
 
+/* ---- profiling ------------------------------------------------------------ */
+/* Per kernel class: summed device time (ms, CUDA events on the model's stream
+ * around each launch), launch count, and work units (active experts for the
+ * expert kernels, 0 otherwise). */
+typedef struct spec_kernel_stat {
+  float ms;
+  int32_t launches;
+  int64_t units;
+} spec_kernel_stat;
+#define SPEC_KCLASS_COUNT 13
+/* Run n_steps device-resident verify steps WITHOUT graph replay, bracketing
+ * every kernel launch with CUDA events. Arguments as in
+ * spec_verify_step_batch_dev; step s reads drafts_dev + s * drafts_step_stride.
+ * Fills out[0..n_out) and returns the number of classes written. The host view
+ * of the sequences must be refreshed with spec_sync_seqs afterwards. */
+int spec_profile_steps_dev(spec_model* m, int n_seq, const int32_t* seq_ids_dev, const int32_t* drafts_dev,
+                           const int32_t* n_draft_dev, int n_steps, int drafts_step_stride,
+                           spec_kernel_stat* out, int n_out);
+const char* spec_kernel_class_name(int cls);
+/* Host<->device bytes moved by the library's step calls since init (inputs
+ * staged, block-table rows uploaded, results read back). */
+int spec_io_bytes(spec_model* m, int64_t* out_h2d, int64_t* out_d2h);
+
 const char* spec_strerror(int code);
 const char* spec_last_error(void);
 

@@ -27,6 +27,13 @@ class SpecError(RuntimeError):
         self.code = code
 
 
+class spec_kernel_stat(ctypes.Structure):
+    _fields_ = [("ms", ctypes.c_float), ("launches", ctypes.c_int32), ("units", ctypes.c_int64)]
+
+
+SPEC_KCLASS_COUNT = 13
+
+
 class spec_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "n_experts", "top_k", "n_shared",
@@ -63,6 +70,12 @@ _SIGS = [
     ("spec_free_pages", ctypes.c_int, [ctypes.c_void_p]),
     ("spec_debug_logits", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, _I32P, _I32P, ctypes.c_void_p]),
     ("spec_step_launches", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    ("spec_profile_steps_dev", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                              ctypes.POINTER(spec_kernel_stat), ctypes.c_int]),
+    ("spec_kernel_class_name", ctypes.c_char_p, [ctypes.c_int]),
+    ("spec_io_bytes", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64),
+                                     ctypes.POINTER(ctypes.c_int64)]),
     ("spec_strerror", ctypes.c_char_p, [ctypes.c_int]),
     ("spec_last_error", ctypes.c_char_p, []),
     ("spec_pool_create", ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -230,6 +243,25 @@ def spec_debug_logits(m: int, seq_ids, drafts, logits_dev) -> None:
 
 def spec_step_launches(m: int, n_seq: int) -> int:
     return _check(lib().spec_step_launches(m, n_seq))
+
+
+def spec_profile_steps_dev(m: int, n_seq: int, seq_ids_dev, drafts_dev, n_draft_dev, n_steps: int,
+                           drafts_step_stride: int) -> dict:
+    out = (spec_kernel_stat * SPEC_KCLASS_COUNT)()
+    n = _check(lib().spec_profile_steps_dev(m, n_seq, _ptr(seq_ids_dev), _ptr(drafts_dev), _ptr(n_draft_dev),
+                                            n_steps, drafts_step_stride, out, SPEC_KCLASS_COUNT))
+    return {spec_kernel_class_name(i): dict(ms=out[i].ms, launches=out[i].launches, units=out[i].units)
+            for i in range(n)}
+
+
+def spec_kernel_class_name(cls: int) -> str:
+    return lib().spec_kernel_class_name(cls).decode()
+
+
+def spec_io_bytes(m: int) -> tuple:
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().spec_io_bytes(m, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
 
 
 def spec_strerror(code: int) -> str:

@@ -166,7 +166,7 @@ cudaError_t configure_attn_kernels() {
   return e != cudaSuccess ? e : f;
 }
 
-void launch_attention(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
+void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
                       cudaStream_t st) {
   const int RG = R < 32 ? R : 32;
   const int groups = ((T + R - 1) / R) * ((R + RG - 1) / RG);
@@ -183,6 +183,9 @@ void launch_attention(const Dims& D, const DevState& S, const StepBuf& B, int la
   } else {
     k_attn_part<64><<<grid, ATT_THREADS, sm, st>>>(D, S, B, layer, T, R, RG, CS);
   }
+}
+
+void launch_attn_merge(const Dims& D, const StepBuf& B, int T, cudaStream_t st) {
   k_attn_merge<<<T, 128, 0, st>>>(D, B, T);
 }
 

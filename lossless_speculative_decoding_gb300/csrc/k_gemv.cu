@@ -421,24 +421,25 @@ void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaS
   }
 }
 
-void launch_expert_gemvs(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
+void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
   const int max_active = (D.E > 0 ? (D.E < T * D.k ? D.E : T * D.k) : 0) + D.S;
   dim3 g1(cdiv(D.inter / 4, GEMV_WARPS), max_active, cdiv(T, GEMV_TP));
-  dim3 g2(cdiv(D.h / 4, GEMV_WARPS), max_active, cdiv(T, GEMV_TP));
   const size_t sm1 = (size_t)GEMV_TP * D.h * sizeof(float);
+  switch (D.wdtype) {
+    case 0: k_gateup<float><<<g1, 256, sm1, st>>>(D, B, (const float*)W.w_gate, nullptr, (const float*)W.w_up, nullptr); break;
+    case 1: k_gateup<bf16_t><<<g1, 256, sm1, st>>>(D, B, (const bf16_t*)W.w_gate, nullptr, (const bf16_t*)W.w_up, nullptr); break;
+    default: k_gateup<fp8_t><<<g1, 256, sm1, st>>>(D, B, (const fp8_t*)W.w_gate, W.s_gate, (const fp8_t*)W.w_up, W.s_up);
+  }
+}
+
+void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
+  const int max_active = (D.E > 0 ? (D.E < T * D.k ? D.E : T * D.k) : 0) + D.S;
+  dim3 g2(cdiv(D.h / 4, GEMV_WARPS), max_active, cdiv(T, GEMV_TP));
   const size_t sm2 = (size_t)GEMV_TP * D.inter * sizeof(float);
   switch (D.wdtype) {
-    case 0:
-      k_gateup<float><<<g1, 256, sm1, st>>>(D, B, (const float*)W.w_gate, nullptr, (const float*)W.w_up, nullptr);
-      k_down<float><<<g2, 256, sm2, st>>>(D, B, (const float*)W.w_down, nullptr);
-      break;
-    case 1:
-      k_gateup<bf16_t><<<g1, 256, sm1, st>>>(D, B, (const bf16_t*)W.w_gate, nullptr, (const bf16_t*)W.w_up, nullptr);
-      k_down<bf16_t><<<g2, 256, sm2, st>>>(D, B, (const bf16_t*)W.w_down, nullptr);
-      break;
-    default:
-      k_gateup<fp8_t><<<g1, 256, sm1, st>>>(D, B, (const fp8_t*)W.w_gate, W.s_gate, (const fp8_t*)W.w_up, W.s_up);
-      k_down<fp8_t><<<g2, 256, sm2, st>>>(D, B, (const fp8_t*)W.w_down, W.s_down);
+    case 0: k_down<float><<<g2, 256, sm2, st>>>(D, B, (const float*)W.w_down, nullptr); break;
+    case 1: k_down<bf16_t><<<g2, 256, sm2, st>>>(D, B, (const bf16_t*)W.w_down, nullptr); break;
+    default: k_down<fp8_t><<<g2, 256, sm2, st>>>(D, B, (const fp8_t*)W.w_down, W.s_down);
   }
 }
 
@@ -451,7 +452,8 @@ void launch_lmhead(const Dims& D, const StepBuf& B, const void* lm_head, const f
   } else {
     k_lmhead<bf16_t><<<grid, 256, sm, st>>>(D, B, (const bf16_t*)lm_head, final_norm, x, T, logits_dbg);
   }
-  k_argmax_reduce<<<T, 256, 0, st>>>(B, T, B.g);
 }
+
+void launch_argmax(const StepBuf& B, int T, cudaStream_t st) { k_argmax_reduce<<<T, 256, 0, st>>>(B, T, B.g); }
 
 }  // namespace spec

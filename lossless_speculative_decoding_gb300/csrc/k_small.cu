@@ -216,12 +216,7 @@ __global__ void k_combine(Dims D, StepBuf B) {
   }
 }
 
-void launch_expert_gemvs(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
-
-void launch_experts(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
-  launch_expert_gemvs(D, B, W, T, st);
-  k_combine<<<T, 256, 0, st>>>(D, B);
-}
+void launch_combine(const Dims& D, const StepBuf& B, int T, cudaStream_t st) { k_combine<<<T, 256, 0, st>>>(D, B); }
 
 // ---------------------------------------------------------------------------
 // Acceptance + commit, one thread per sequence of the step ("End-to-end OCR
@@ -260,6 +255,11 @@ __global__ void k_commit(Dims D, DevState S, StepBuf B, int n_seq, int K) {
   for (int i = keep; i < D.max_pages; ++i) bt[i] = -1;
   B.step_out[s] = a;
   B.step_out[max_batch + s] = bonus;
+  if (s == 0) B.step_out[2 * max_batch] = *S.err;
+  int* ua = reinterpret_cast<int*>(B.out_ptrs[0]);
+  int* ub = reinterpret_cast<int*>(B.out_ptrs[1]);
+  if (ua) ua[s] = a;
+  if (ub) ub[s] = bonus;
 }
 
 void launch_commit(const Dims& D, const DevState& S, const StepBuf& B, int n_seq, int K, cudaStream_t st) {
@@ -268,8 +268,12 @@ void launch_commit(const Dims& D, const DevState& S, const StepBuf& B, int n_seq
 
 // Copy device-resident step inputs into the staging block.
 __global__ void k_stage_dev(StepBuf B, int n_seq, int K, const int* seq_ids, const int* drafts,
-                            const int* n_draft) {
+                            const int* n_draft, int* out_acc, int* out_bonus) {
   const int max_batch = B.max_batch;
+  if (threadIdx.x == 0) {
+    B.out_ptrs[0] = reinterpret_cast<unsigned long long>(out_acc);
+    B.out_ptrs[1] = reinterpret_cast<unsigned long long>(out_bonus);
+  }
   for (int i = threadIdx.x; i < n_seq; i += blockDim.x) {
     B.step_in[i] = seq_ids[i];
     B.step_in[max_batch + max_batch * K + i] = n_draft[i];
@@ -278,8 +282,8 @@ __global__ void k_stage_dev(StepBuf B, int n_seq, int K, const int* seq_ids, con
 }
 
 void launch_stage_dev(const StepBuf& B, int n_seq, int K, const int* seq_ids, const int* drafts,
-                      const int* n_draft, cudaStream_t st) {
-  k_stage_dev<<<1, 256, 0, st>>>(B, n_seq, K, seq_ids, drafts, n_draft);
+                      const int* n_draft, int* out_acc, int* out_bonus, cudaStream_t st) {
+  k_stage_dev<<<1, 256, 0, st>>>(B, n_seq, K, seq_ids, drafts, n_draft, out_acc, out_bonus);
 }
 
 int launches_per_step(const Dims& D) {

@@ -65,7 +65,9 @@ struct StepBuf {
   float* am_val; int* am_idx;        // [T, n_vocab_blocks] argmax partials
   int* g;            // [T] greedy tokens
   int* step_in;      // staging: [seq ids (max_batch) | drafts (max_batch*K) | n_draft (max_batch)]
-  int* step_out;     // staging: [acc (max_batch) | bonus (max_batch)]
+  int* step_out;     // staging: [acc (max_batch) | bonus (max_batch) | device error bits]
+  unsigned long long* out_ptrs;  // [2] caller device outputs (acc, bonus) of a _dev step; 0 = none.
+                                 // Lives just before step_in so one host copy refreshes both.
   int n_chunk_max;
   int n_vblocks;
   int max_batch;      // staging block capacity (sequences per step)
@@ -78,16 +80,24 @@ void launch_assemble_prefill(const Dims& D, const DevState& S, const StepBuf& B,
                              const void* vis, int seq, int pos0, int T, cudaStream_t st);
 void launch_qkv(const Dims& D, const DevState& S, const StepBuf& B, const LayerW& W, int layer, int T,
                 cudaStream_t st);
-void launch_attention(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
+void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
                       cudaStream_t st);
+void launch_attn_merge(const Dims& D, const StepBuf& B, int T, cudaStream_t st);
 void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
 void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
-void launch_experts(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
+void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
+void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
+void launch_combine(const Dims& D, const StepBuf& B, int T, cudaStream_t st);
 void launch_lmhead(const Dims& D, const StepBuf& B, const void* lm_head, const float* final_norm,
                    const float* x, int T, float* logits_dbg, cudaStream_t st);
+void launch_argmax(const StepBuf& B, int T, cudaStream_t st);
+
+// Kernel classes (for profiling); order matches spec_kernel_class_name().
+enum KClass { KC_ASSEMBLE, KC_QKV, KC_ATTN, KC_MERGE, KC_OPROJ, KC_ROUTER, KC_GATEUP, KC_DOWN, KC_COMBINE,
+              KC_LMHEAD, KC_ARGMAX, KC_COMMIT, KC_STAGE, KC_COUNT };
 void launch_commit(const Dims& D, const DevState& S, const StepBuf& B, int n_seq, int K, cudaStream_t st);
 void launch_stage_dev(const StepBuf& B, int n_seq, int K, const int* seq_ids, const int* drafts,
-                      const int* n_draft, cudaStream_t st);
+                      const int* n_draft, int* out_acc, int* out_bonus, cudaStream_t st);
 int launches_per_step(const Dims& D);
 // Opt a kernel in to the largest dynamic shared memory the device allows
 // next to its static shared memory (an upper bound: occupancy follows the

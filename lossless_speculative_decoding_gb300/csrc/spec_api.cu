@@ -129,6 +129,7 @@ struct spec_model {
   int step_in_n = 0, step_out_n = 0;
   bool host_dirty = false;         // device state newer than host view (after _dev steps)
   bool own_stream = false;
+  int64_t h2d_bytes = 0, d2h_bytes = 0;   // host<->device bytes moved by step calls
 
   ~spec_model() {
     for (auto& g : graphs) cudaGraphExecDestroy(g.second);
@@ -169,6 +170,7 @@ struct spec_model {
     std::copy(t.begin(), t.end(), row);
     CU(cudaMemcpyAsync(const_cast<int*>(S.bt) + (size_t)slot * D.max_pages, row, D.max_pages * sizeof(int32_t),
                        cudaMemcpyHostToDevice, stream));
+    h2d_bytes += (int64_t)D.max_pages * sizeof(int32_t);
     return SPEC_OK;
   }
 
@@ -179,24 +181,49 @@ struct spec_model {
     return SPEC_OK;
   }
 
-  // Enqueue one forward over T rows already assembled in B (row meta + x).
-  void enqueue_layers(int T, int R_rows) {
-    for (int l = 0; l < D.L; ++l) {
-      const LayerW& W = layers[l];
-      launch_qkv(D, S, B, W, l, T, stream);
-      launch_attention(D, S, B, l, T, R_rows, stream);
-      launch_oproj(D, B, W, T, stream);
-      launch_router(D, B, W, T, stream);
-      launch_experts(D, B, W, T, stream);
+  // Profiling: events around every launch, active-expert counts per router.
+  struct Prof {
+    std::vector<cudaEvent_t> ev;
+    std::vector<int> cls;
+    int n = 0;
+    int32_t* act = nullptr;      // pinned
+    int nact = 0;
+  };
+
+  template <class F>
+  void run_k(Prof* p, int cls, F&& launch) {
+    if (p) cudaEventRecord(p->ev[2 * p->n], stream);
+    launch();
+    if (p) {
+      cudaEventRecord(p->ev[2 * p->n + 1], stream);
+      p->cls[p->n] = cls;
+      p->n++;
     }
   }
 
-  void enqueue_verify(int n_seq, float* logits_dbg, bool commit) {
+  // Enqueue one forward over T rows already assembled in B (row meta + x).
+  void enqueue_layers(int T, int R_rows, Prof* p = nullptr) {
+    for (int l = 0; l < D.L; ++l) {
+      const LayerW& W = layers[l];
+      run_k(p, KC_QKV, [&] { launch_qkv(D, S, B, W, l, T, stream); });
+      run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, stream); });
+      run_k(p, KC_MERGE, [&] { launch_attn_merge(D, B, T, stream); });
+      run_k(p, KC_OPROJ, [&] { launch_oproj(D, B, W, T, stream); });
+      run_k(p, KC_ROUTER, [&] { launch_router(D, B, W, T, stream); });
+      if (p) cudaMemcpyAsync(p->act + p->nact++, B.n_active, 4, cudaMemcpyDeviceToHost, stream);
+      run_k(p, KC_GATEUP, [&] { launch_gateup(D, B, W, T, stream); });
+      run_k(p, KC_DOWN, [&] { launch_down(D, B, W, T, stream); });
+      run_k(p, KC_COMBINE, [&] { launch_combine(D, B, T, stream); });
+    }
+  }
+
+  void enqueue_verify(int n_seq, float* logits_dbg, bool commit, Prof* p = nullptr) {
     const int T = n_seq * R;
-    launch_assemble_verify(D, S, B, tok_embed, n_seq, K, stream);
-    enqueue_layers(T, R);
-    launch_lmhead(D, B, lm_head, final_norm, B.x, T, logits_dbg, stream);
-    if (commit) launch_commit(D, S, B, n_seq, K, stream);
+    run_k(p, KC_ASSEMBLE, [&] { launch_assemble_verify(D, S, B, tok_embed, n_seq, K, stream); });
+    enqueue_layers(T, R, p);
+    run_k(p, KC_LMHEAD, [&] { launch_lmhead(D, B, lm_head, final_norm, B.x, T, logits_dbg, stream); });
+    run_k(p, KC_ARGMAX, [&] { launch_argmax(B, T, stream); });
+    if (commit) run_k(p, KC_COMMIT, [&] { launch_commit(D, S, B, n_seq, K, stream); });
   }
 
   int graph_for(int n_seq, cudaGraphExec_t* out) {
@@ -360,11 +387,15 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
       (rc = m->dalloc(&B.g, T)))
     return rc;
   m->step_in_n = c.max_batch * (2 + m->K);
-  m->step_out_n = 2 * c.max_batch;
-  if ((rc = m->dalloc(&B.step_in, m->step_in_n)) || (rc = m->dalloc(&B.step_out, m->step_out_n))) return rc;
+  m->step_out_n = 2 * c.max_batch + 1;   // acc | bonus | device error bits
+  // [out_ptrs (2 x 64-bit) | step inputs]: one host copy refreshes both
+  int* stage = nullptr;
+  if ((rc = m->dalloc(&stage, 4 + m->step_in_n)) || (rc = m->dalloc(&B.step_out, m->step_out_n))) return rc;
+  B.out_ptrs = reinterpret_cast<unsigned long long*>(stage);
+  B.step_in = stage + 4;
   CU(cudaMemset(B.counter, 0, 4 * sizeof(int)));
-  CU(cudaMemset(B.step_in, 0, m->step_in_n * sizeof(int)));
-  CU(cudaMallocHost(&m->pin_in, std::max(m->step_in_n, T) * sizeof(int32_t)));
+  CU(cudaMemset(stage, 0, (4 + m->step_in_n) * sizeof(int)));
+  CU(cudaMallocHost(&m->pin_in, std::max(4 + m->step_in_n, T) * sizeof(int32_t)));
   CU(cudaMallocHost(&m->pin_out, std::max(m->step_out_n, T) * sizeof(int32_t)));
   CU(cudaStreamSynchronize(m->stream));
   CU(cudaGetLastError());
@@ -395,6 +426,7 @@ static int run_prefill_rows(spec_model* m, int slot, const std::vector<int32_t>&
     if (c0 + T == n && out_tok) {
       launch_lmhead(m->D, m->B, m->lm_head, m->final_norm, m->B.x + (size_t)(T - 1) * m->D.h, 1, nullptr,
                     m->stream);
+      launch_argmax(m->B, 1, m->stream);
       CU(cudaMemcpyAsync(m->pin_out, m->B.g, sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
     }
     // the staging buffer is reused by the next chunk
@@ -529,15 +561,17 @@ static int verify_host(spec_model* m, int n_seq, const int32_t* seq_ids, const i
     if (rc) return fail(rc, "KV pool exhausted");
     if (m->pool->table(q).size() != before && (rc = m->push_table(q))) return rc;
   }
-  int32_t* in = m->pin_in;
-  std::fill(in, in + m->step_in_n, 0);
+  std::fill(m->pin_in, m->pin_in + 4 + m->step_in_n, 0);    // out_ptrs = 0: results go to step_out
+  int32_t* in = m->pin_in + 4;
   for (int s = 0; s < n_seq; ++s) {
     in[s] = seq_ids[s];
     const int nd = n_draft ? n_draft[s] : K;
     for (int j = 0; j < K; ++j) in[mb + s * K + j] = (j < nd && drafts) ? drafts[s * K + j] : 0;
     in[mb + mb * K + s] = nd;
   }
-  CU(cudaMemcpyAsync(m->B.step_in, in, m->step_in_n * sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
+  CU(cudaMemcpyAsync(m->B.out_ptrs, m->pin_in, (4 + m->step_in_n) * sizeof(int32_t), cudaMemcpyHostToDevice,
+                     m->stream));
+  m->h2d_bytes += (int64_t)(4 + m->step_in_n) * sizeof(int32_t);
   if (logits_dev) {
     m->enqueue_verify(n_seq, logits_dev, false);
     CU(cudaStreamSynchronize(m->stream));
@@ -550,8 +584,14 @@ static int verify_host(spec_model* m, int n_seq, const int32_t* seq_ids, const i
   CU(cudaGraphLaunch(ge, m->stream));
   CU(cudaMemcpyAsync(m->pin_out, m->B.step_out, m->step_out_n * sizeof(int32_t), cudaMemcpyDeviceToHost,
                      m->stream));
+  m->d2h_bytes += (int64_t)m->step_out_n * sizeof(int32_t);
   CU(cudaStreamSynchronize(m->stream));
-  if ((rc = m->check_err())) return rc;
+  if (m->pin_out[2 * mb] != 0) {   // device error bits, copied by the commit kernel
+    CU(cudaMemsetAsync(m->S.err, 0, sizeof(int), m->stream));
+    CU(cudaStreamSynchronize(m->stream));
+    return fail(SPEC_ERR_STATE, "device error bits " + std::to_string(m->pin_out[2 * mb]) +
+                                    " (1 page, 2 token, 4 position out of range); step not committed on the host");
+  }
   for (int s = 0; s < n_seq; ++s) {
     const int q = seq_ids[s];
     const int a = m->pin_out[s], bonus = m->pin_out[mb + s];
@@ -601,12 +641,72 @@ int spec_verify_step_batch_dev(spec_model* m, int n_seq, const int32_t* seq_ids_
   cudaGraphExec_t ge;
   int rc = m->graph_for(n_seq, &ge);
   if (rc) return rc;
-  launch_stage_dev(m->B, n_seq, m->K, seq_ids_dev, drafts_dev, n_draft_dev, m->stream);
+  launch_stage_dev(m->B, n_seq, m->K, seq_ids_dev, drafts_dev, n_draft_dev, out_accepted_dev, out_bonus_dev,
+                   m->stream);
   CU(cudaGraphLaunch(ge, m->stream));
-  CU(cudaMemcpyAsync(out_accepted_dev, m->B.step_out, n_seq * sizeof(int32_t), cudaMemcpyDeviceToDevice, m->stream));
-  CU(cudaMemcpyAsync(out_bonus_dev, m->B.step_out + m->cfg.max_batch, n_seq * sizeof(int32_t),
-                     cudaMemcpyDeviceToDevice, m->stream));
   m->host_dirty = true;
+  return SPEC_OK;
+}
+
+int spec_profile_steps_dev(spec_model* m, int n_seq, const int32_t* seq_ids_dev, const int32_t* drafts_dev,
+                           const int32_t* n_draft_dev, int n_steps, int drafts_step_stride, spec_kernel_stat* out,
+                           int n_out) {
+  if (!m || n_seq < 1 || n_seq > m->cfg.max_batch || n_steps < 1 || !out || n_out < 1 || !seq_ids_dev ||
+      !n_draft_dev || (m->K > 0 && !drafts_dev))
+    return fail(SPEC_ERR_ARG, "bad profile arguments");
+  const int per_step = launches_per_step(m->D) + 1;
+  spec_model::Prof p;
+  p.ev.resize(2 * per_step);
+  p.cls.resize(per_step);
+  for (auto& e : p.ev) CU(cudaEventCreate(&e));
+  CU(cudaMallocHost(&p.act, m->D.L * sizeof(int32_t)));
+  std::vector<double> ms(KC_COUNT, 0.0);
+  std::vector<int64_t> launches(KC_COUNT, 0), units(KC_COUNT, 0);
+  int rc = SPEC_OK;
+  for (int s = 0; s < n_steps && rc == SPEC_OK; ++s) {
+    p.n = 0;
+    p.nact = 0;
+    const int32_t* d = drafts_dev ? drafts_dev + (size_t)s * drafts_step_stride : nullptr;
+    m->run_k(&p, KC_STAGE,
+             [&] { launch_stage_dev(m->B, n_seq, m->K, seq_ids_dev, d, n_draft_dev, nullptr, nullptr, m->stream); });
+    m->enqueue_verify(n_seq, nullptr, true, &p);
+    cudaError_t e = cudaStreamSynchronize(m->stream);
+    if (e != cudaSuccess) { rc = fail(SPEC_ERR_CUDA, cudaGetErrorString(e)); break; }
+    for (int i = 0; i < p.n; ++i) {
+      float t = 0.f;
+      cudaEventElapsedTime(&t, p.ev[2 * i], p.ev[2 * i + 1]);
+      ms[p.cls[i]] += t;
+      launches[p.cls[i]] += 1;
+    }
+    for (int i = 0; i < p.nact; ++i) {
+      units[KC_GATEUP] += p.act[i];
+      units[KC_DOWN] += p.act[i];
+    }
+  }
+  for (auto& e : p.ev) cudaEventDestroy(e);
+  cudaFreeHost(p.act);
+  m->host_dirty = true;
+  if (rc) return rc;
+  for (int i = 0; i < std::min(n_out, (int)KC_COUNT); ++i) {
+    out[i].ms = (float)ms[i];
+    out[i].launches = (int32_t)launches[i];
+    out[i].units = units[i];
+  }
+  return std::min(n_out, (int)KC_COUNT);
+}
+
+const char* spec_kernel_class_name(int cls) {
+  static const char* names[KC_COUNT] = {"assemble", "qkv_rope_kvwrite", "attn_splitkv", "attn_merge",
+                                        "oproj_residual", "router_topk_permute", "expert_gateup_swiglu",
+                                        "expert_down", "expert_combine", "lmhead_argmax", "argmax_reduce",
+                                        "accept_commit", "stage_inputs"};
+  return (cls >= 0 && cls < KC_COUNT) ? names[cls] : "";
+}
+
+int spec_io_bytes(spec_model* m, int64_t* out_h2d, int64_t* out_d2h) {
+  if (!m) return fail(SPEC_ERR_ARG, "null model");
+  if (out_h2d) *out_h2d = m->h2d_bytes;
+  if (out_d2h) *out_d2h = m->d2h_bytes;
   return SPEC_OK;
 }
 

@@ -433,3 +433,27 @@ def expected_accept_iid(q: float, k: int) -> float:
 def expected_accept_geometric(p: float, k: int) -> float:
     """E[min(L, k)] for P(L = l) = (1-p)^l p."""
     return sum((1 - p) ** i for i in range(1, k + 1))
+
+
+def draft_schedule(drafter: Drafter, ref: Sequence[int], n_steps: int, k: int, seq: int = 0):
+    """Plan a drafter's proposals for ``n_steps`` consecutive verify steps of one
+    sequence whose greedy continuation is ``ref`` (ref[0] = first generated
+    token). Because the synthetic drafter is built around the reference, it
+    knows how many of its proposals agree with it: step s proposes from the
+    committed count n_s, and n_(s+1) = n_s + (leading agreeing drafts) + 1.
+    Returns (drafts [n_steps, k] int32, agreeing prefix lengths [n_steps],
+    committed counts before each step [n_steps])."""
+    drafts = np.zeros((n_steps, k), np.int32)
+    agree = np.zeros(n_steps, np.int32)
+    n_before = np.zeros(n_steps, np.int64)
+    n = 1
+    for s in range(n_steps):
+        d = drafter.propose(ref, n, k, seq, s)
+        drafts[s] = d
+        a = 0
+        while a < k and n + a < len(ref) and int(d[a]) == int(ref[n + a]):
+            a += 1
+        agree[s] = a
+        n_before[s] = n
+        n += a + 1
+    return drafts, agree, n_before

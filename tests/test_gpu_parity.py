@@ -219,3 +219,61 @@ def test_bf16_fp8_dense_parity(cfg, rel):
         toks += d[:a] + [b]
     # rows whose expert routing flips at a near-tie may exceed the bar; none expected here
     assert n_bad == 0, (n_bad, n_rows)
+
+
+def test_device_resident_steps_match_host_steps(tiny):
+    """Device-resident steps (inputs and outputs in HBM, graph replay, no host
+    sync) commit exactly what host-driven steps commit; the profiler path too."""
+    import torch
+    from lossless_speculative_decoding_gb300 import binding as B
+    w, om, prompt, ref, _ = tiny
+    gm = gpu_model(TINY_W.model, w, max_ctx=512, max_draft=3)
+    drafter = syn.Drafter("iid", 0.6, TINY_W.model.vocab, seed=4)
+    drafts, agree, n_before = syn.draft_schedule(drafter, ref, 30, 3)
+    gm.prefill(0, prompt.visual, prompt.tokens)
+    B.spec_reserve_seq(gm.h, 0, 400)
+    with torch.cuda.stream(gm.stream):
+        d = torch.from_numpy(drafts.reshape(-1).copy()).cuda()
+        sid = torch.zeros(1, dtype=torch.int32, device="cuda")
+        nd = torch.full((1,), 3, dtype=torch.int32, device="cuda")
+        acc = torch.full((30,), -1, dtype=torch.int32, device="cuda")
+        bon = torch.full((30,), -1, dtype=torch.int32, device="cuda")
+    gm.stream.synchronize()
+    for s in range(20):
+        B.spec_verify_step_batch_dev(gm.h, 1, sid, d.data_ptr() + 12 * s, nd, acc.data_ptr() + 4 * s,
+                                     bon.data_ptr() + 4 * s)
+    stats = B.spec_profile_steps_dev(gm.h, 1, sid, d.data_ptr() + 12 * 20, nd, 10, 3)
+    B.spec_sync_seqs(gm.h)
+    gm.stream.synchronize()
+    assert np.array_equal(acc.cpu().numpy()[:20], agree[:20])
+    assert (bon.cpu().numpy()[:20] >= 0).all()
+    n = int(n_before[29] + agree[29] + 1)
+    assert np.array_equal(gm.tokens(0)[:n], ref[:n])
+    assert stats["expert_gateup_swiglu"]["launches"] == 10 * TINY_W.model.n_layers
+    assert stats["lmhead_argmax"]["ms"] > 0
+    assert stats["expert_gateup_swiglu"]["units"] >= 10 * TINY_W.model.n_layers
+
+
+def test_errors_leave_state_unchanged(tiny):
+    from lossless_speculative_decoding_gb300 import binding as B
+    w, om, prompt, ref, _ = tiny
+    gm = gpu_model(TINY_W.model, w, max_ctx=256, max_draft=3, n_pages=6)
+    with pytest.raises(B.SpecError) as e:
+        gm.verify(0, [1, 2, 3])                                # not prefilled
+    assert e.value.code == -1
+    gm.prefill(0, prompt.visual, prompt.tokens)
+    L = gm.length(0)
+    with pytest.raises(B.SpecError):
+        gm.verify(0, [1, 2, 5000])                             # token out of range
+    with pytest.raises(B.SpecError):
+        gm.verify(0, [1, 2, 3, 4])                             # too many drafts
+    assert gm.length(0) == L
+    # pool exhaustion: 6 pages of 16 = 96 positions; the prompt uses 72 + 4
+    steps = 0
+    with pytest.raises(B.SpecError) as e:
+        for _ in range(100):
+            gm.verify(0, [])
+            steps += 1
+    assert e.value.code == -2 and gm.length(0) == L + steps
+    gm.release(0)
+    assert B.spec_free_pages(gm.h) == 6
