@@ -193,7 +193,7 @@ typedef struct spec_kernel_stat {
   int32_t launches;
   int64_t units;
 } spec_kernel_stat;
-#define SPEC_KCLASS_COUNT 13
+#define SPEC_KCLASS_COUNT 10
 /* Run n_steps device-resident verify steps WITHOUT graph replay, bracketing
  * every kernel launch with CUDA events. Arguments as in
  * spec_verify_step_batch_dev; step s reads drafts_dev + s * drafts_step_stride.
@@ -209,6 +209,25 @@ int spec_io_bytes(spec_model* m, int64_t* out_h2d, int64_t* out_d2h);
 
 const char* spec_strerror(int code);
 const char* spec_last_error(void);
+
+/* ---- kernel-level entry points (device pointers, enqueued on cuda_stream) - */
+/* Final RMSNorm + LM head + greedy argmax for T rows without writing logits
+ * (the target's token at every verified position: "Jina-OCR-v1", abstract,
+ * greedy verification; "End-to-end OCR expert model ...", section 6.1):
+ *   out_tokens_dev[t] = argmax_v  sum_k W[v][k] * gamma[k] * x[t][k] / rms(x[t]),
+ *   rms(z) = sqrt(mean(z^2) + eps); ties keep the lowest index v.
+ * x_dev: [T, hidden] f32. w_dev: [vocab, hidden] row-major, w_dtype SPEC_F32 or
+ * SPEC_BF16. gamma_dev: [hidden] f32. scratch_dev: caller-owned device memory
+ * of at least spec_lmhead_argmax_scratch_bytes(T, vocab) bytes (per-block
+ * (max, index) candidates), fully rewritten by each call. vocab must be a
+ * multiple of 4, a weight row a multiple of 16 bytes, hidden <= 12288.
+ * Returns after enqueueing; errors: SPEC_ERR_ARG, SPEC_ERR_UNSUPPORTED,
+ * SPEC_ERR_CUDA (launch failure). */
+int64_t spec_lmhead_argmax_scratch_bytes(int T, int vocab);
+int spec_lmhead_argmax(const float* x_dev, int T, int hidden, int vocab, const void* w_dev, int w_dtype,
+                       const float* gamma_dev, float eps, void* scratch_dev, size_t scratch_bytes,
+                       int32_t* out_tokens_dev, uintptr_t cuda_stream);
+
 
 /* ---- paged KV allocator (host only; usable without a GPU) ---------------- */
 /* The same allocator the model uses, exposed for tests and tooling. Pages

@@ -31,7 +31,7 @@ class spec_kernel_stat(ctypes.Structure):
     _fields_ = [("ms", ctypes.c_float), ("launches", ctypes.c_int32), ("units", ctypes.c_int64)]
 
 
-SPEC_KCLASS_COUNT = 13
+SPEC_KCLASS_COUNT = 10
 
 
 class spec_config(ctypes.Structure):
@@ -76,6 +76,10 @@ _SIGS = [
     ("spec_kernel_class_name", ctypes.c_char_p, [ctypes.c_int]),
     ("spec_io_bytes", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64),
                                      ctypes.POINTER(ctypes.c_int64)]),
+    ("spec_lmhead_argmax_scratch_bytes", ctypes.c_int64, [ctypes.c_int, ctypes.c_int]),
+    ("spec_lmhead_argmax", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
+                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t]),
     ("spec_strerror", ctypes.c_char_p, [ctypes.c_int]),
     ("spec_last_error", ctypes.c_char_p, []),
     ("spec_pool_create", ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -262,6 +266,16 @@ def spec_io_bytes(m: int) -> tuple:
     a, b = ctypes.c_int64(), ctypes.c_int64()
     _check(lib().spec_io_bytes(m, ctypes.byref(a), ctypes.byref(b)))
     return a.value, b.value
+
+
+def spec_lmhead_argmax_scratch_bytes(T: int, vocab: int) -> int:
+    return _check(lib().spec_lmhead_argmax_scratch_bytes(T, vocab))
+
+
+def spec_lmhead_argmax(x_dev, T: int, hidden: int, vocab: int, w_dev, w_dtype: int, gamma_dev, eps: float,
+                       scratch_dev, scratch_bytes: int, out_tokens_dev, cuda_stream: int = 0) -> None:
+    _check(lib().spec_lmhead_argmax(_ptr(x_dev), T, hidden, vocab, _ptr(w_dev), w_dtype, _ptr(gamma_dev), eps,
+                                    _ptr(scratch_dev), scratch_bytes, _ptr(out_tokens_dev), cuda_stream))
 
 
 def spec_strerror(code: int) -> str:

@@ -9,7 +9,8 @@
 // (page by page, converted to fp32 in shared memory) and serves every query
 // row of one sequence group and every q head that shares that kv head (GQA).
 // A partial (unnormalised output, running max, running sum) per (row, head,
-// chunk) is merged in chunk order by k_attn_merge.
+// chunk) goes to scratch; the last block of a (group, kv head) to finish
+// merges them in chunk order.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -26,11 +27,12 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
   float* Vs = Ks + ATT_CHUNK * KLD;                 // [64][D_HEAD]
   float* Qw = Vs + ATT_CHUNK * D_HEAD;              // [warps][D_HEAD]
   float* Pw = Qw + (ATT_THREADS / 32) * D_HEAD;     // [warps][64]
+  __shared__ int s_last;
   const int hk = blockIdx.y;
   const int gps = (R + RG - 1) / RG;
   const int s = blockIdx.z / gps, sub = blockIdx.z % gps;
   const int r0 = s * R + sub * RG;
-  if (r0 >= T) return;
+  if (r0 >= T) return;                              // whole group past T: no block of it counts
   const int nr = min(RG, min(R - sub * RG, T - r0));
   const int seq = B.row_seq[r0];
   const int maxpos = B.row_pos[r0 + nr - 1];
@@ -137,27 +139,50 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
       __syncwarp();
     }
   }
-}
-
-// Merge the chunk partials of each (row, q head) in chunk order:
-// M = max m_c, L = sum l_c e^(m_c - M), o = sum o_c e^(m_c - M) / L.
-__global__ void k_attn_merge(Dims D, StepBuf B, int T) {
-  const int row = blockIdx.x;
-  const int pos = B.row_pos[row];
-  const int nc = pos / ATT_CHUNK + 1;
-  for (int i = threadIdx.x; i < D.Hq * D.d; i += blockDim.x) {
-    const int hq = i / D.d, j = i % D.d;
+  // ---- the last of the CS chunk-slot blocks of this (group, kv head) merges ----
+  __syncthreads();
+  int* ctr = B.cnt_att + (size_t)blockIdx.z * D.Hkv + hk;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = (atomicAdd(ctr, 1) == (int)gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // M = max_c m_c, L = sum_c l_c e^(m_c - M), o = sum_c o_c e^(m_c - M) / L,
+  // chunks in order; one warp per (row, q head) of the group
+  for (int p = warp; p < npairs; p += ATT_THREADS / 32) {
+    const int row = r0 + p / G;
+    const int hq = hk * G + p % G;
+    const int nc = B.row_pos[row] / ATT_CHUNK + 1;
     const size_t base = ((size_t)row * D.Hq + hq) * B.n_chunk_max;
     float M = -INFINITY;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, B.att_ml[(base + c) * 2]);
-    float L = 0.f, O = 0.f;
-    for (int c = 0; c < nc; ++c) {
-      const float w = expf(B.att_ml[(base + c) * 2] - M);
-      L = fmaf(B.att_ml[(base + c) * 2 + 1], w, L);
-      O = fmaf(B.att_o[(base + c) * D.d + j], w, O);
+    for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldcg(B.att_ml + (base + c) * 2));
+    M = warp_max(M);
+    float Ll = 0.f;
+    for (int c = lane; c < nc; c += 32)
+      Ll = fmaf(__ldcg(B.att_ml + (base + c) * 2 + 1), expf(__ldcg(B.att_ml + (base + c) * 2) - M), Ll);
+    const float L = warp_sum(Ll);
+    float* out = B.o + (size_t)row * D.Hq * D_HEAD + (size_t)hq * D_HEAD;
+    if constexpr (D_HEAD == 128) {
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = 0; c < nc; ++c) {
+        const float w = expf(__ldcg(B.att_ml + (base + c) * 2) - M);
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(B.att_o + (base + c) * D_HEAD) + lane);
+        o.x = fmaf(v.x, w, o.x); o.y = fmaf(v.y, w, o.y); o.z = fmaf(v.z, w, o.z); o.w = fmaf(v.w, w, o.w);
+      }
+      reinterpret_cast<float4*>(out)[lane] = make_float4(o.x / L, o.y / L, o.z / L, o.w / L);
+    } else {
+      float2 o = make_float2(0.f, 0.f);
+      for (int c = 0; c < nc; ++c) {
+        const float w = expf(__ldcg(B.att_ml + (base + c) * 2) - M);
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(B.att_o + (base + c) * D_HEAD) + lane);
+        o.x = fmaf(v.x, w, o.x); o.y = fmaf(v.y, w, o.y);
+      }
+      reinterpret_cast<float2*>(out)[lane] = make_float2(o.x / L, o.y / L);
     }
-    B.o[(size_t)row * D.Hq * D.d + i] = O / L;
   }
+  if (threadIdx.x == 0) *ctr = 0;
 }
 
 cudaError_t configure_attn_kernels() {
@@ -185,8 +210,5 @@ void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int la
   }
 }
 
-void launch_attn_merge(const Dims& D, const StepBuf& B, int T, cudaStream_t st) {
-  k_attn_merge<<<T, 128, 0, st>>>(D, B, T);
-}
 
 }  // namespace spec

@@ -279,32 +279,65 @@ __global__ void __launch_bounds__(256) k_gateup(Dims D, StepBuf B, const WT* __r
   B.h_act[(size_t)pairs[t] * D.inter + j] = silu(g) * uu;
 }
 
-// Expert down projection: y[pair][o] = sum_j W_d[e][o][j] * h_act[pair][j].
+// Expert down projection y[pair][o] = sum_j W_d[e][o][j] * h_act[pair][j],
+// then the combine: the last block to finish a 32-column tile of the output
+// (over all expert slots and row passes) adds, for every row r and column o
+// of the tile, sum over slots s (in order) of w[r][s] * y[r*NS + s][o] to the
+// residual x (routed weight p, shared weight 1).
 template <class WT>
 __global__ void __launch_bounds__(256) k_down(Dims D, StepBuf B, const WT* __restrict__ Wd,
-                                              const float* __restrict__ sd) {
+                                              const float* __restrict__ sd, int T) {
   extern __shared__ __align__(16) float xs[];
+  __shared__ int s_last;
   const int slot = blockIdx.y;
-  if (slot >= *B.n_active) return;
-  const int cnt = B.act_cnt[slot], off = B.act_off[slot], e = B.act_expert[slot];
   const int p0 = blockIdx.z * GEMV_TP;
-  if (p0 >= cnt) return;
-  const int nvalid = min(GEMV_TP, cnt - p0);
-  const int* pairs = B.perm + off + p0;
-  stage_rows(xs, D.inter, nvalid, [&](int t) { return B.h_act + (size_t)pairs[t] * D.inter; }, nullptr, 0.f);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int unit = blockIdx.x * GEMV_WARPS + warp;
-  if (unit * 4 >= D.h) return;
-  const WT* wr[4];
+  int cnt = 0, off = 0, e = 0;
+  bool work = slot < *B.n_active;
+  if (work) {
+    cnt = B.act_cnt[slot]; off = B.act_off[slot]; e = B.act_expert[slot];
+    work = p0 < cnt;
+  }
+  if (work) {                                       // block-uniform branch
+    const int nvalid = min(GEMV_TP, cnt - p0);
+    const int* pairs = B.perm + off + p0;
+    stage_rows(xs, D.inter, nvalid, [&](int t) { return B.h_act + (size_t)pairs[t] * D.inter; }, nullptr, 0.f);
+    const int unit = blockIdx.x * GEMV_WARPS + warp;
+    if (unit * 4 < D.h) {
+      const WT* wr[4];
 #pragma unroll
-  for (int r = 0; r < 4; ++r) wr[r] = Wd + ((size_t)e * D.h + unit * 4 + r) * D.inter;
-  float acc[16];
-  gemv_lane<WT, 4, GEMV_TP>(wr, D.inter, xs, D.inter, acc);
-  const float val = reduce_scatter<16>(acc);
-  const int v = (lane >> 1) & 15, r = v / GEMV_TP, t = v % GEMV_TP;
-  if ((lane & 1) || t >= nvalid) return;
-  const int o = unit * 4 + r;
-  B.y[(size_t)pairs[t] * D.h + o] = sd != nullptr ? val * sd[(size_t)e * D.h + o] : val;
+      for (int r = 0; r < 4; ++r) wr[r] = Wd + ((size_t)e * D.h + unit * 4 + r) * D.inter;
+      float acc[16];
+      gemv_lane<WT, 4, GEMV_TP>(wr, D.inter, xs, D.inter, acc);
+      const float val = reduce_scatter<16>(acc);
+      const int v = (lane >> 1) & 15, r = v / GEMV_TP, t = v % GEMV_TP;
+      if (!(lane & 1) && t < nvalid) {
+        const int o = unit * 4 + r;
+        B.y[(size_t)pairs[t] * D.h + o] = sd != nullptr ? val * sd[(size_t)e * D.h + o] : val;
+      }
+    }
+  }
+  __syncthreads();
+  int* ctr = B.cnt_down + blockIdx.x;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = (atomicAdd(ctr, 1) == (int)(gridDim.y * gridDim.z) - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int c0 = blockIdx.x * GEMV_WARPS * 4;
+  const int ncol = min(GEMV_WARPS * 4, D.h - c0);
+  for (int i = threadIdx.x; i < T * ncol; i += blockDim.x) {
+    const int r = i / ncol, j = c0 + i % ncol;
+    float acc = 0.f;
+    for (int s2 = 0; s2 < D.NS; ++s2) {
+      const float w = s2 < D.k ? B.wts[r * D.k + s2] : 1.f;
+      acc = fmaf(w, __ldcg(B.y + ((size_t)r * D.NS + s2) * D.h + j), acc);
+    }
+    B.x[(size_t)r * D.h + j] += acc;
+  }
+  if (threadIdx.x == 0) *ctr = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -314,7 +347,7 @@ __global__ void __launch_bounds__(256) k_down(Dims D, StepBuf B, const WT* __res
 template <class WT>
 __global__ void __launch_bounds__(256) k_lmhead(Dims D, StepBuf B, const WT* __restrict__ W,
                                                 const float* __restrict__ gamma, const float* __restrict__ x,
-                                                int T, float* __restrict__ logits_dbg) {
+                                                int T, float* __restrict__ logits_dbg, bool fused) {
   extern __shared__ __align__(16) float xs[];
   __shared__ float cand[GEMV_TP][GEMV_WARPS * 4];
   const int t0 = blockIdx.y * GEMV_TP;
@@ -349,6 +382,36 @@ __global__ void __launch_bounds__(256) k_lmhead(Dims D, StepBuf B, const WT* __r
     B.am_val[(size_t)(t0 + tt) * B.n_vblocks + blockIdx.x] = best;
     B.am_idx[(size_t)(t0 + tt) * B.n_vblocks + blockIdx.x] = bi;
   }
+  if (!fused) return;
+  // the last block of this row pass reduces every block's candidate:
+  // larger value wins, equal values keep the lower index
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = (atomicAdd(B.cnt_lm + blockIdx.y, 1) == (int)gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (warp < nvalid) {
+    const size_t base = (size_t)(t0 + warp) * B.n_vblocks;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int i = lane; i < B.n_vblocks; i += 32) {
+      const float c = __ldcg(B.am_val + base + i);
+      const int ci = __ldcg(B.am_idx + base + i);
+      if (c > bv || (c == bv && ci < bi)) { bv = c; bi = ci; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == 0) B.g[t0 + warp] = bi;
+  }
+  if (threadIdx.x == 0) B.cnt_lm[blockIdx.y] = 0;
 }
 
 // Reduce the per-block candidates of each row: larger value wins, equal
@@ -437,20 +500,22 @@ void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaSt
   dim3 g2(cdiv(D.h / 4, GEMV_WARPS), max_active, cdiv(T, GEMV_TP));
   const size_t sm2 = (size_t)GEMV_TP * D.inter * sizeof(float);
   switch (D.wdtype) {
-    case 0: k_down<float><<<g2, 256, sm2, st>>>(D, B, (const float*)W.w_down, nullptr); break;
-    case 1: k_down<bf16_t><<<g2, 256, sm2, st>>>(D, B, (const bf16_t*)W.w_down, nullptr); break;
-    default: k_down<fp8_t><<<g2, 256, sm2, st>>>(D, B, (const fp8_t*)W.w_down, W.s_down);
+    case 0: k_down<float><<<g2, 256, sm2, st>>>(D, B, (const float*)W.w_down, nullptr, T); break;
+    case 1: k_down<bf16_t><<<g2, 256, sm2, st>>>(D, B, (const bf16_t*)W.w_down, nullptr, T); break;
+    default: k_down<fp8_t><<<g2, 256, sm2, st>>>(D, B, (const fp8_t*)W.w_down, W.s_down, T);
   }
 }
 
 void launch_lmhead(const Dims& D, const StepBuf& B, const void* lm_head, const float* final_norm,
-                   const float* x, int T, float* logits_dbg, cudaStream_t st) {
+                   const float* x, int T, float* logits_dbg, bool fuse_argmax, cudaStream_t st) {
   dim3 grid(B.n_vblocks, cdiv(T, GEMV_TP));
   const size_t sm = (size_t)GEMV_TP * D.h * sizeof(float);
   if (D.act_f32) {
-    k_lmhead<float><<<grid, 256, sm, st>>>(D, B, (const float*)lm_head, final_norm, x, T, logits_dbg);
+    k_lmhead<float><<<grid, 256, sm, st>>>(D, B, (const float*)lm_head, final_norm, x, T, logits_dbg,
+                                           fuse_argmax);
   } else {
-    k_lmhead<bf16_t><<<grid, 256, sm, st>>>(D, B, (const bf16_t*)lm_head, final_norm, x, T, logits_dbg);
+    k_lmhead<bf16_t><<<grid, 256, sm, st>>>(D, B, (const bf16_t*)lm_head, final_norm, x, T, logits_dbg,
+                                            fuse_argmax);
   }
 }
 

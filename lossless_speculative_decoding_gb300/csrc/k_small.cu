@@ -90,10 +90,11 @@ __global__ void __launch_bounds__(256) k_router(Dims D, StepBuf B, const float* 
                                                 const RT* __restrict__ Wr, int T) {
   extern __shared__ __align__(16) float sm[];
   float* u = sm;                 // [h]
-  float* logit = u + D.h;        // [E]
+  float* prob = u + D.h;         // [E]
   __shared__ float red[32];
   __shared__ int s_last;
   const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* x = B.x + (size_t)row * D.h;
   float ss = 0.f;
   for (int k = threadIdx.x; k < D.h; k += blockDim.x) ss = fmaf(x[k], x[k], ss);
@@ -105,7 +106,6 @@ __global__ void __launch_bounds__(256) k_router(Dims D, StepBuf B, const float* 
     B.u[(size_t)row * D.h + k] = v;
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (D.E > 0) {
     constexpr int EP = Elt<RT>::per16;
     for (int e = warp; e < D.E; e += blockDim.x / 32) {
@@ -117,28 +117,56 @@ __global__ void __launch_bounds__(256) k_router(Dims D, StepBuf B, const float* 
         for (int i = 0; i < EP; ++i) acc = fmaf(w[i], u[k + i], acc);
       }
       acc = warp_sum(acc);
-      if (lane == 0) logit[e] = acc;
+      if (lane == 0) prob[e] = acc;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (warp == 0) {
+      // softmax over E <= 256 logits, lane l owning experts l, l+32, ...
+      constexpr int MAXE = 8;
+      float v[MAXE];
       float m = -INFINITY;
-      for (int e = 0; e < D.E; ++e) m = fmaxf(m, logit[e]);
+#pragma unroll
+      for (int i = 0; i < MAXE; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < D.E ? prob[e] : -INFINITY;
+        m = fmaxf(m, v[i]);
+      }
+      m = warp_max(m);
       float z = 0.f;
-      for (int e = 0; e < D.E; ++e) { logit[e] = expf(logit[e] - m); z += logit[e]; }
-      for (int e = 0; e < D.E; ++e) logit[e] = logit[e] / z;
-      for (int i = 0; i < D.k; ++i) {
-        int best = -1;
-        for (int e = 0; e < D.E; ++e) {
-          if (logit[e] < 0.f) continue;              // already taken
-          if (best < 0 || logit[e] > logit[best]) best = e;
+#pragma unroll
+      for (int i = 0; i < MAXE; ++i) {
+        v[i] = (lane + 32 * i < D.E) ? expf(v[i] - m) : 0.f;
+        z += v[i];
+      }
+      z = warp_sum(z);
+#pragma unroll
+      for (int i = 0; i < MAXE; ++i) v[i] = (lane + 32 * i < D.E) ? v[i] / z : -1.f;
+      // top-k: k rounds of a warp argmax, (probability desc, id asc)
+      for (int r = 0; r < D.k; ++r) {
+        float bv = -1.f;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < MAXE; ++i) {
+          const int e = lane + 32 * i;
+          if (v[i] > bv) { bv = v[i]; bi = e; }      // increasing e: ties keep the lower id
         }
-        B.ids[row * D.k + i] = best;
-        B.wts[row * D.k + i] = logit[best];
-        logit[best] = -1.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (lane == 0) {
+          B.ids[row * D.k + r] = bi;
+          B.wts[row * D.k + r] = bv;
+        }
+#pragma unroll
+        for (int i = 0; i < MAXE; ++i)
+          if (lane + 32 * i == bi) v[i] = -1.f;        // taken
       }
     }
   }
-  // ---- last block builds the permutation ----
+  // ---- the last block to finish builds the permutation ----
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -148,12 +176,15 @@ __global__ void __launch_bounds__(256) k_router(Dims D, StepBuf B, const float* 
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  int* cnt = reinterpret_cast<int*>(sm);          // reuse: [E] counts, [E] offsets
-  int* offs = cnt + (D.E > 0 ? D.E : 1);
   const int nk = T * D.k;
+  int* s_ids = reinterpret_cast<int*>(sm);        // reuse: [nk] ids, [E] counts, [E] offsets
+  int* cnt = s_ids + nk;
+  int* offs = cnt + (D.E > 0 ? D.E : 1);
+  for (int j = threadIdx.x; j < nk; j += blockDim.x) s_ids[j] = __ldcg(B.ids + j);
+  __syncthreads();
   for (int e = threadIdx.x; e < D.E; e += blockDim.x) {
     int c = 0;
-    for (int j = 0; j < nk; ++j) c += (__ldcg(B.ids + j) == e);
+    for (int j = 0; j < nk; ++j) c += (s_ids[j] == e);
     cnt[e] = c;
   }
   __syncthreads();
@@ -178,7 +209,7 @@ __global__ void __launch_bounds__(256) k_router(Dims D, StepBuf B, const float* 
     if (cnt[e] == 0) continue;
     int c = offs[e];
     for (int j = 0; j < nk; ++j)
-      if (__ldcg(B.ids + j) == e) B.perm[c++] = (j / D.k) * D.NS + (j % D.k);
+      if (s_ids[j] == e) B.perm[c++] = (j / D.k) * D.NS + (j % D.k);
   }
   for (int i = threadIdx.x; i < D.S * T; i += blockDim.x) {
     const int s = i / T, r = i % T;
@@ -194,29 +225,15 @@ cudaError_t configure_small_kernels() {
 }
 
 void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
-  const size_t sm = (size_t)(D.h + (D.E > 0 ? D.E : 1) * 2) * sizeof(float);
+  const int E1 = D.E > 0 ? D.E : 1;
+  const size_t words = (size_t)D.h + E1 > (size_t)T * D.k + 2 * E1 ? (size_t)D.h + E1 : (size_t)T * D.k + 2 * E1;
+  const size_t sm = words * sizeof(float);
   if (D.act_f32) {
     k_router<float><<<T, 256, sm, st>>>(D, B, W.ffn_norm, (const float*)W.w_router, T);
   } else {
     k_router<bf16_t><<<T, 256, sm, st>>>(D, B, W.ffn_norm, (const bf16_t*)W.w_router, T);
   }
 }
-
-// x[r] += sum over slots (routed weight p, shared weight 1) of y[r*NS + slot],
-// slots in order.
-__global__ void k_combine(Dims D, StepBuf B) {
-  const int r = blockIdx.x;
-  for (int j = threadIdx.x; j < D.h; j += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < D.NS; ++s) {
-      const float w = s < D.k ? B.wts[r * D.k + s] : 1.f;
-      acc = fmaf(w, B.y[((size_t)r * D.NS + s) * D.h + j], acc);
-    }
-    B.x[(size_t)r * D.h + j] += acc;
-  }
-}
-
-void launch_combine(const Dims& D, const StepBuf& B, int T, cudaStream_t st) { k_combine<<<T, 256, 0, st>>>(D, B); }
 
 // ---------------------------------------------------------------------------
 // Acceptance + commit, one thread per sequence of the step ("End-to-end OCR
@@ -287,9 +304,10 @@ void launch_stage_dev(const StepBuf& B, int n_seq, int K, const int* seq_ids, co
 }
 
 int launches_per_step(const Dims& D) {
-  // assemble + per layer (qkv, attn part, attn merge, oproj, router, gate/up,
-  // down, combine) + lm head + argmax reduce + commit
-  return 1 + D.L * 8 + 2 + 1;
+  // assemble + per layer (qkv + RoPE + KV write, split-KV attention + merge,
+  // O-proj + residual, router + top-k + permute, gate/up + SwiGLU, down +
+  // combine) + LM head + argmax + accept/commit
+  return 1 + D.L * 6 + 1 + 1;
 }
 
 }  // namespace spec

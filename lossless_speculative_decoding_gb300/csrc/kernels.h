@@ -59,7 +59,10 @@ struct StepBuf {
   int* ids; float* wts;              // [T, k]
   int* perm;                         // [T*NS] pair ids grouped by expert
   int* act_expert; int* act_off; int* act_cnt; int* n_active;  // active-expert list
-  int* counter;                      // arrival counters (kept at zero between launches)
+  int* counter;                      // router arrival counter (kept at zero between launches)
+  int* cnt_att;                      // [Tmax * Hkv] attention arrivals per (row group, kv head)
+  int* cnt_down;                     // [ceil(h/32)] expert-down arrivals per output column tile
+  int* cnt_lm;                       // [ceil(Tmax/TP)] LM-head arrivals per row pass
   float* h_act;      // [T*NS, inter]
   float* y;          // [T*NS, h]
   float* am_val; int* am_idx;        // [T, n_vocab_blocks] argmax partials
@@ -82,23 +85,23 @@ void launch_qkv(const Dims& D, const DevState& S, const StepBuf& B, const LayerW
                 cudaStream_t st);
 void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
                       cudaStream_t st);
-void launch_attn_merge(const Dims& D, const StepBuf& B, int T, cudaStream_t st);
 void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
 void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
 void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
 void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
-void launch_combine(const Dims& D, const StepBuf& B, int T, cudaStream_t st);
 void launch_lmhead(const Dims& D, const StepBuf& B, const void* lm_head, const float* final_norm,
-                   const float* x, int T, float* logits_dbg, cudaStream_t st);
+                   const float* x, int T, float* logits_dbg, bool fuse_argmax, cudaStream_t st);
 void launch_argmax(const StepBuf& B, int T, cudaStream_t st);
 
 // Kernel classes (for profiling); order matches spec_kernel_class_name().
-enum KClass { KC_ASSEMBLE, KC_QKV, KC_ATTN, KC_MERGE, KC_OPROJ, KC_ROUTER, KC_GATEUP, KC_DOWN, KC_COMBINE,
-              KC_LMHEAD, KC_ARGMAX, KC_COMMIT, KC_STAGE, KC_COUNT };
+enum KClass { KC_ASSEMBLE, KC_QKV, KC_ATTN, KC_OPROJ, KC_ROUTER, KC_GATEUP, KC_DOWN, KC_LMHEAD, KC_COMMIT,
+              KC_STAGE, KC_COUNT };
 void launch_commit(const Dims& D, const DevState& S, const StepBuf& B, int n_seq, int K, cudaStream_t st);
 void launch_stage_dev(const StepBuf& B, int n_seq, int K, const int* seq_ids, const int* drafts,
                       const int* n_draft, int* out_acc, int* out_bonus, cudaStream_t st);
 int launches_per_step(const Dims& D);
+// Record `msg` as the calling thread's last error (spec_last_error) and return code.
+int set_last_error(int code, const char* msg);
 // Opt a kernel in to the largest dynamic shared memory the device allows
 // next to its static shared memory (an upper bound: occupancy follows the
 // bytes each launch asks for). Called at model set-up, never during capture.

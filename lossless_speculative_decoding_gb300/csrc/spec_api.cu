@@ -4,7 +4,10 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cstdio>
+#include <thread>
 #include <cstring>
 #include <map>
 #include <memory>
@@ -77,6 +80,7 @@ int check_config(const spec_config& c) {
   if (c.n_experts < 0 || c.top_k < 0 || c.n_shared < 0 || c.inter < 4) return fail(SPEC_ERR_ARG, "ffn shape");
   if (c.n_experts > 0 && (c.top_k < 1 || c.top_k > c.n_experts || c.top_k > 16))
     return fail(SPEC_ERR_ARG, "top_k must be in [1, min(n_experts, 16)]");
+  if (c.n_experts > 256) return fail(SPEC_ERR_UNSUPPORTED, "at most 256 routed experts");
   if (c.n_experts == 0 && (c.n_shared != 1 || c.top_k != 0))
     return fail(SPEC_ERR_ARG, "a dense FFN is one shared expert with top_k = 0");
   if (c.n_experts + c.n_shared < 1) return fail(SPEC_ERR_ARG, "no FFN experts");
@@ -102,6 +106,8 @@ struct Prefix {
 };
 
 }  // namespace
+
+int spec::set_last_error(int code, const char* msg) { return fail(code, msg); }
 
 struct spec_model {
   spec_config cfg{};
@@ -130,6 +136,7 @@ struct spec_model {
   bool host_dirty = false;         // device state newer than host view (after _dev steps)
   bool own_stream = false;
   int64_t h2d_bytes = 0, d2h_bytes = 0;   // host<->device bytes moved by step calls
+  std::atomic<int> prof_gate{1};           // profiler: stream held until a step is enqueued
 
   ~spec_model() {
     for (auto& g : graphs) cudaGraphExecDestroy(g.second);
@@ -207,13 +214,11 @@ struct spec_model {
       const LayerW& W = layers[l];
       run_k(p, KC_QKV, [&] { launch_qkv(D, S, B, W, l, T, stream); });
       run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, stream); });
-      run_k(p, KC_MERGE, [&] { launch_attn_merge(D, B, T, stream); });
       run_k(p, KC_OPROJ, [&] { launch_oproj(D, B, W, T, stream); });
       run_k(p, KC_ROUTER, [&] { launch_router(D, B, W, T, stream); });
       if (p) cudaMemcpyAsync(p->act + p->nact++, B.n_active, 4, cudaMemcpyDeviceToHost, stream);
       run_k(p, KC_GATEUP, [&] { launch_gateup(D, B, W, T, stream); });
       run_k(p, KC_DOWN, [&] { launch_down(D, B, W, T, stream); });
-      run_k(p, KC_COMBINE, [&] { launch_combine(D, B, T, stream); });
     }
   }
 
@@ -221,8 +226,7 @@ struct spec_model {
     const int T = n_seq * R;
     run_k(p, KC_ASSEMBLE, [&] { launch_assemble_verify(D, S, B, tok_embed, n_seq, K, stream); });
     enqueue_layers(T, R, p);
-    run_k(p, KC_LMHEAD, [&] { launch_lmhead(D, B, lm_head, final_norm, B.x, T, logits_dbg, stream); });
-    run_k(p, KC_ARGMAX, [&] { launch_argmax(B, T, stream); });
+    run_k(p, KC_LMHEAD, [&] { launch_lmhead(D, B, lm_head, final_norm, B.x, T, logits_dbg, true, stream); });
     if (commit) run_k(p, KC_COMMIT, [&] { launch_commit(D, S, B, n_seq, K, stream); });
   }
 
@@ -381,7 +385,8 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
       (rc = m->dalloc(&B.wts, (size_t)T * std::max(D.k, 1))) || (rc = m->dalloc(&B.perm, (size_t)T * NS)) ||
       (rc = m->dalloc(&B.act_expert, max_active)) || (rc = m->dalloc(&B.act_off, max_active)) ||
       (rc = m->dalloc(&B.act_cnt, max_active)) || (rc = m->dalloc(&B.n_active, 1)) ||
-      (rc = m->dalloc(&B.counter, 4)) || (rc = m->dalloc(&B.h_act, (size_t)T * NS * D.inter)) ||
+      (rc = m->dalloc(&B.counter, 4)) || (rc = m->dalloc(&B.cnt_att, (size_t)T * D.Hkv)) ||
+      (rc = m->dalloc(&B.cnt_down, (D.h + 31) / 32)) || (rc = m->dalloc(&B.cnt_lm, (T + GEMV_TP - 1) / GEMV_TP)) || (rc = m->dalloc(&B.h_act, (size_t)T * NS * D.inter)) ||
       (rc = m->dalloc(&B.y, (size_t)T * NS * D.h)) ||
       (rc = m->dalloc(&B.am_val, (size_t)T * B.n_vblocks)) || (rc = m->dalloc(&B.am_idx, (size_t)T * B.n_vblocks)) ||
       (rc = m->dalloc(&B.g, T)))
@@ -394,6 +399,9 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
   B.out_ptrs = reinterpret_cast<unsigned long long*>(stage);
   B.step_in = stage + 4;
   CU(cudaMemset(B.counter, 0, 4 * sizeof(int)));
+  CU(cudaMemset(B.cnt_att, 0, (size_t)T * D.Hkv * sizeof(int)));
+  CU(cudaMemset(B.cnt_down, 0, ((D.h + 31) / 32) * sizeof(int)));
+  CU(cudaMemset(B.cnt_lm, 0, ((T + GEMV_TP - 1) / GEMV_TP) * sizeof(int)));
   CU(cudaMemset(stage, 0, (4 + m->step_in_n) * sizeof(int)));
   CU(cudaMallocHost(&m->pin_in, std::max(4 + m->step_in_n, T) * sizeof(int32_t)));
   CU(cudaMallocHost(&m->pin_out, std::max(m->step_out_n, T) * sizeof(int32_t)));
@@ -424,9 +432,8 @@ static int run_prefill_rows(spec_model* m, int slot, const std::vector<int32_t>&
     launch_assemble_prefill(m->D, m->S, m->B, m->tok_embed, vis, slot, start + c0, T, m->stream);
     m->enqueue_layers(T, T);
     if (c0 + T == n && out_tok) {
-      launch_lmhead(m->D, m->B, m->lm_head, m->final_norm, m->B.x + (size_t)(T - 1) * m->D.h, 1, nullptr,
+      launch_lmhead(m->D, m->B, m->lm_head, m->final_norm, m->B.x + (size_t)(T - 1) * m->D.h, 1, nullptr, true,
                     m->stream);
-      launch_argmax(m->B, 1, m->stream);
       CU(cudaMemcpyAsync(m->pin_out, m->B.g, sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
     }
     // the staging buffer is reused by the next chunk
@@ -648,6 +655,14 @@ int spec_verify_step_batch_dev(spec_model* m, int n_seq, const int32_t* seq_ids_
   return SPEC_OK;
 }
 
+// Host-side gate for the profiler: the stream waits in this host function
+// until every launch of the step is enqueued, so the events around each kernel
+// time the kernel rather than the host's enqueue latency. Bounded wait.
+static void CUDART_CB profile_gate(void* arg) {
+  auto* flag = static_cast<std::atomic<int>*>(arg);
+  for (int i = 0; i < 20000 && flag->load() == 0; ++i) std::this_thread::sleep_for(std::chrono::microseconds(100));
+}
+
 int spec_profile_steps_dev(spec_model* m, int n_seq, const int32_t* seq_ids_dev, const int32_t* drafts_dev,
                            const int32_t* n_draft_dev, int n_steps, int drafts_step_stride, spec_kernel_stat* out,
                            int n_out) {
@@ -666,10 +681,13 @@ int spec_profile_steps_dev(spec_model* m, int n_seq, const int32_t* seq_ids_dev,
   for (int s = 0; s < n_steps && rc == SPEC_OK; ++s) {
     p.n = 0;
     p.nact = 0;
+    m->prof_gate.store(0);
+    CU(cudaLaunchHostFunc(m->stream, profile_gate, &m->prof_gate));
     const int32_t* d = drafts_dev ? drafts_dev + (size_t)s * drafts_step_stride : nullptr;
     m->run_k(&p, KC_STAGE,
              [&] { launch_stage_dev(m->B, n_seq, m->K, seq_ids_dev, d, n_draft_dev, nullptr, nullptr, m->stream); });
     m->enqueue_verify(n_seq, nullptr, true, &p);
+    m->prof_gate.store(1);
     cudaError_t e = cudaStreamSynchronize(m->stream);
     if (e != cudaSuccess) { rc = fail(SPEC_ERR_CUDA, cudaGetErrorString(e)); break; }
     for (int i = 0; i < p.n; ++i) {
@@ -696,10 +714,9 @@ int spec_profile_steps_dev(spec_model* m, int n_seq, const int32_t* seq_ids_dev,
 }
 
 const char* spec_kernel_class_name(int cls) {
-  static const char* names[KC_COUNT] = {"assemble", "qkv_rope_kvwrite", "attn_splitkv", "attn_merge",
-                                        "oproj_residual", "router_topk_permute", "expert_gateup_swiglu",
-                                        "expert_down", "expert_combine", "lmhead_argmax", "argmax_reduce",
-                                        "accept_commit", "stage_inputs"};
+  static const char* names[KC_COUNT] = {"assemble", "qkv_rope_kvwrite", "attn_splitkv_merge", "oproj_residual",
+                                        "router_topk_permute", "expert_gateup_swiglu", "expert_down_combine",
+                                        "lmhead_argmax", "accept_commit", "stage_inputs"};
   return (cls >= 0 && cls < KC_COUNT) ? names[cls] : "";
 }
 
