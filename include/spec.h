@@ -228,6 +228,25 @@ int spec_lmhead_argmax(const float* x_dev, int T, int hidden, int vocab, const v
                        const float* gamma_dev, float eps, void* scratch_dev, size_t scratch_bytes,
                        int32_t* out_tokens_dev, uintptr_t cuda_stream);
 
+/* Same computation as spec_lmhead_argmax for callers that cannot allocate
+ * device memory (no cudaMalloc of their own, none by the library): the
+ * candidate scratch is a fixed device array inside the library, sized for
+ * SPEC_LMHEAD_NOALLOC_MAX_PAIRS (max, index) pairs (2 MiB), which every GPU
+ * that loads the library holds until the process exits. The pages describe
+ * nothing like it; it exists only for such callers.
+ *  - Sizes with T * ceil(vocab / 32) > SPEC_LMHEAD_NOALLOC_MAX_PAIRS are
+ *    rejected with SPEC_ERR_ARG.
+ *  - The first call on a device resolves the array's address and sets the
+ *    kernels' attributes (with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the array and each call rewrites every
+ *    candidate it reads, so no state carries over; calls whose kernels
+ *    overlap on the GPU (different streams, no ordering) race on it.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine. */
+#define SPEC_LMHEAD_NOALLOC_MAX_PAIRS 262144
+int spec_lmhead_argmax_noalloc(const float* x_dev, int T, int hidden, int vocab, const void* w_dev,
+                               int w_dtype, const float* gamma_dev, float eps, int32_t* out_tokens_dev,
+                               uintptr_t cuda_stream);
 
 /* ---- paged KV allocator (host only; usable without a GPU) ---------------- */
 /* The same allocator the model uses, exposed for tests and tooling. Pages

@@ -80,6 +80,9 @@ _SIGS = [
     ("spec_lmhead_argmax", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
                                           ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t]),
+    ("spec_lmhead_argmax_noalloc", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
+                                                  ctypes.c_void_p, ctypes.c_size_t]),
     ("spec_strerror", ctypes.c_char_p, [ctypes.c_int]),
     ("spec_last_error", ctypes.c_char_p, []),
     ("spec_pool_create", ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -276,6 +279,15 @@ def spec_lmhead_argmax(x_dev, T: int, hidden: int, vocab: int, w_dev, w_dtype: i
                        scratch_dev, scratch_bytes: int, out_tokens_dev, cuda_stream: int = 0) -> None:
     _check(lib().spec_lmhead_argmax(_ptr(x_dev), T, hidden, vocab, _ptr(w_dev), w_dtype, _ptr(gamma_dev), eps,
                                     _ptr(scratch_dev), scratch_bytes, _ptr(out_tokens_dev), cuda_stream))
+
+
+SPEC_LMHEAD_NOALLOC_MAX_PAIRS = 262144
+
+
+def spec_lmhead_argmax_noalloc(x_dev, T: int, hidden: int, vocab: int, w_dev, w_dtype: int, gamma_dev,
+                               eps: float, out_tokens_dev, cuda_stream: int = 0) -> None:
+    _check(lib().spec_lmhead_argmax_noalloc(_ptr(x_dev), T, hidden, vocab, _ptr(w_dev), w_dtype, _ptr(gamma_dev),
+                                            eps, _ptr(out_tokens_dev), cuda_stream))
 
 
 def spec_strerror(code: int) -> str:
