@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--profile-steps", type=int, default=64)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (small same-shape cases for ncu captures)")
     return ap.parse_args()
 
 
@@ -274,6 +276,9 @@ def run_ours(args):
     from lossless_speculative_decoding_gb300.runtime import SpecModel
 
     wl = syn.WORKLOADS[args.workload]
+    if args.layers:
+        import dataclasses
+        wl = dataclasses.replace(wl, model=syn.scaled(wl.model, n_layers=args.layers))
     cfg = wl.model
     if wl.batch != 1:
         raise SystemExit(f"bench.py runs the batch-1 workloads; {wl.name} has batch {wl.batch}")
@@ -398,7 +403,7 @@ def run_ours(args):
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": {syn.F32: "f32", syn.BF16: "bf16", syn.FP8: "e4m3 weights / f32 activations"}[cfg.wdtype],
             "data": "synthetic (random-init weights, N(0,1) visual rows, seeded drafter)",
-            "config": {"workload": wl.name, "model": cfg.name, "batch": wl.batch, "n_draft": K,
+            "config": {"workload": wl.name, "model": cfg.name, "layers": cfg.n_layers, "batch": wl.batch, "n_draft": K,
                        "draft_match_prob": wl.q, "prompt_rows": prompt.length, "page_size": wl.page_size,
                        "tau": committed / KS, "l2": "weights read per step (>2 GB) exceed the 126 MB L2",
                        "parallelism": f"replicas x{ws}"},

@@ -103,4 +103,54 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its writes are visible (a no-op when the kernel
+// was launched without the attribute), and allow the next kernel to start
+// its independent prologue. Every kernel waits in every block before it
+// exits, so completion stays transitive along the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Acceptance + commit of sequence slot s of a verify step ("End-to-end OCR
+// expert model ...", section 6.1: accept the agreeing prefix from the left,
+// the target supplies the token at the first divergence). With g the greedy
+// tokens of the K+1 rows: a = max{i <= n_draft : d_j = g_(j-1) for j <= i},
+// bonus = g_a. The sequence keeps the KV of its last token and the a accepted
+// drafts (length n + a + 1); the rejected rows' slots are stale and are
+// overwritten by the next step. Pages wholly past max(new length, reserved
+// pages) leave the block table (-1); the host allocator mirrors this.
+__device__ __forceinline__ void commit_seq(const Dims& D, const DevState& S, const StepBuf& B, int s, int K,
+                                           const int* g_rows) {
+  const int max_batch = B.max_batch;
+  const int R = K + 1;
+  const int seq = B.step_in[s];
+  const int* d = B.step_in + max_batch + s * K;
+  const int nd = min(max(B.step_in[max_batch + max_batch * K + s], 0), K);
+  const int* g = g_rows + s * R;
+  int a = 0;
+  while (a < nd && d[a] == g[a]) ++a;
+  const int bonus = g[a];
+  const int n = S.seq_len[seq];
+  const int new_len = n + a + 1;
+  const int no = S.n_out[seq];
+  int* out = S.out_tok + (size_t)seq * D.max_ctx;
+  for (int j = 0; j < a; ++j)
+    if (no + j < D.max_ctx) out[no + j] = d[j];
+  if (no + a < D.max_ctx) out[no + a] = bonus;
+  S.n_out[seq] = no + a + 1;
+  S.seq_len[seq] = new_len;
+  S.last_tok[seq] = bonus;
+  int keep = (new_len + D.P - 1) / D.P;
+  if (S.keep_pages[seq] > keep) keep = S.keep_pages[seq];
+  int* bt = const_cast<int*>(S.bt) + (size_t)seq * D.max_pages;
+  for (int i = keep; i < D.max_pages; ++i) bt[i] = -1;
+  B.step_out[s] = a;
+  B.step_out[max_batch + s] = bonus;
+  if (s == 0) B.step_out[2 * max_batch] = *S.err;
+  int* ua = reinterpret_cast<int*>(B.out_ptrs[0]);
+  int* ub = reinterpret_cast<int*>(B.out_ptrs[1]);
+  if (ua) ua[s] = a;
+  if (ub) ub[s] = bonus;
+}
+
 }  // namespace spec

@@ -1,0 +1,228 @@
+// Shared building blocks of the weight-streaming GEMV kernels.
+//
+// A warp owns R weight rows ("a unit") and streams them with 16-byte
+// non-allocating loads, 32 lanes side by side; each lane accumulates its
+// chunks in increasing order and a fixed butterfly reduce-scatter combines
+// the lanes. Nothing in an output's arithmetic depends on T, on the row's
+// place in the batch or on the launch shape.
+#pragma once
+#include "common.cuh"
+
+namespace spec {
+
+// ---------------------------------------------------------------------------
+// Warp reduce-scatter of N partial sums (N = 16 or 32): after it, the lane
+// returns the full warp sum of value index (N == 32 ? lane : lane >> 1).
+// The pairing tree is the same for every value index.
+template <int N>
+__device__ __forceinline__ float reduce_scatter(float (&a)[N]) {
+  const int lane = threadIdx.x & 31;
+  int n = N;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    if (n > 1) {
+      const bool up = (lane & m) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        if (i < n / 2) {
+          const float send = up ? a[i] : a[i + n / 2];
+          const float keep = up ? a[i + n / 2] : a[i];
+          a[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+      n >>= 1;
+    } else {
+      a[0] += __shfl_xor_sync(0xffffffffu, a[0], m);
+    }
+  }
+  return a[0];
+}
+
+// Group q (of per16/4) of four elements of a 16-byte vector, as floats.
+template <class WT, int Q> __device__ __forceinline__ void unpack4(const uint4& v, float* o);
+template <> __device__ __forceinline__ void unpack4<float, 0>(const uint4& v, float* o) {
+  o[0] = __uint_as_float(v.x); o[1] = __uint_as_float(v.y); o[2] = __uint_as_float(v.z); o[3] = __uint_as_float(v.w);
+}
+__device__ __forceinline__ void bf2(uint32_t w, float* o) {
+  o[0] = __uint_as_float(w << 16); o[1] = __uint_as_float(w & 0xFFFF0000u);
+}
+template <> __device__ __forceinline__ void unpack4<bf16_t, 0>(const uint4& v, float* o) { bf2(v.x, o); bf2(v.y, o + 2); }
+template <> __device__ __forceinline__ void unpack4<bf16_t, 1>(const uint4& v, float* o) { bf2(v.z, o); bf2(v.w, o + 2); }
+__device__ __forceinline__ void f8x4(uint32_t w, float* o) {
+  __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFF), __NV_E4M3);
+  __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+  float2 a = __half22float2(*reinterpret_cast<__half2*>(&lo));
+  float2 b = __half22float2(*reinterpret_cast<__half2*>(&hi));
+  o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+}
+template <> __device__ __forceinline__ void unpack4<fp8_t, 0>(const uint4& v, float* o) { f8x4(v.x, o); }
+template <> __device__ __forceinline__ void unpack4<fp8_t, 1>(const uint4& v, float* o) { f8x4(v.y, o); }
+template <> __device__ __forceinline__ void unpack4<fp8_t, 2>(const uint4& v, float* o) { f8x4(v.z, o); }
+template <> __device__ __forceinline__ void unpack4<fp8_t, 3>(const uint4& v, float* o) { f8x4(v.w, o); }
+
+template <class WT, int R, int TP, int Q>
+__device__ __forceinline__ void fma_group(const uint4 (&wv)[R], const float* xs, int ldxs, int k,
+                                          float (&acc)[R * TP]) {
+  float xv[TP][4];
+#pragma unroll
+  for (int t = 0; t < TP; ++t) {
+    const float4 x4 = *reinterpret_cast<const float4*>(xs + t * ldxs + k + 4 * Q);
+    xv[t][0] = x4.x; xv[t][1] = x4.y; xv[t][2] = x4.z; xv[t][3] = x4.w;
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    float w[4];
+    unpack4<WT, Q>(wv[r], w);
+#pragma unroll
+    for (int t = 0; t < TP; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[r * TP + t] = fmaf(w[e], xv[t][e], acc[r * TP + t]);
+  }
+}
+
+// acc[r*TP + t] = sum_k W[row r][k] * xs[t][k] over this lane's 16-byte chunks
+// (chunk c = lane, lane + 32, ... in increasing order).
+template <class WT, int R, int TP>
+__device__ __forceinline__ void gemv_lane(const WT* const (&wrow)[R], int K, const float* xs, int ldxs,
+                                          float (&acc)[R * TP]) {
+  constexpr int EP = Elt<WT>::per16;
+  const int nch = K / EP;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < R * TP; ++i) acc[i] = 0.f;
+  for (int c0 = lane; c0 < nch; c0 += 32 * GEMV_G) {
+    uint4 wv[GEMV_G][R];
+#pragma unroll
+    for (int g = 0; g < GEMV_G; ++g) {
+      const int c = c0 + g * 32;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        wv[g][r] = (c < nch) ? ld_stream(wrow[r] + (size_t)c * EP) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int g = 0; g < GEMV_G; ++g) {
+      const int c = c0 + g * 32;
+      if (c < nch) {
+        const int k = c * EP;
+        fma_group<WT, R, TP, 0>(wv[g], xs, ldxs, k, acc);
+        if constexpr (EP >= 8) fma_group<WT, R, TP, 1>(wv[g], xs, ldxs, k, acc);
+        if constexpr (EP >= 16) {
+          fma_group<WT, R, TP, 2>(wv[g], xs, ldxs, k, acc);
+          fma_group<WT, R, TP, 3>(wv[g], xs, ldxs, k, acc);
+        }
+      }
+    }
+  }
+}
+
+// Stage TP activation rows into shared memory (zeros past `nvalid`).
+// src_row(t) gives the source row pointer. With gamma != nullptr each row is
+// RMS-normalised: x / sqrt(mean(x^2) + eps) * gamma (warp t sums row t).
+template <class F>
+__device__ __forceinline__ void stage_rows(float* xs, int K, int nvalid, F src_row, const float* gamma,
+                                           float eps) {
+  __shared__ float inv[GEMV_TP];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (gamma != nullptr && warp < GEMV_TP) {
+    float ss = 0.f;
+    if (warp < nvalid) {
+      const float* x = src_row(warp);
+      for (int k = lane; k < K; k += 32) ss = fmaf(x[k], x[k], ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) inv[warp] = 1.0f / sqrtf(ss / (float)K + eps);
+  }
+  __syncthreads();
+  for (int t = 0; t < GEMV_TP; ++t) {
+    const float* x = t < nvalid ? src_row(t) : nullptr;
+    const float sc = gamma != nullptr ? inv[t] : 1.f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+      float v = 0.f;
+      if (x) v = gamma != nullptr ? (x[k] * sc) * gamma[k] : x[k];
+      xs[t * K + k] = v;
+    }
+  }
+  __syncthreads();
+}
+
+
+// ---------------------------------------------------------------------------
+// Streaming variant: activation rows are read from global memory (through L1)
+// instead of shared memory, optionally scaled by gamma per column; the first
+// group of a unit's weight chunks can be loaded ahead (before the kernel waits
+// for its predecessor, or before the previous unit's reduction).
+template <class WT, int R, int G>
+__device__ __forceinline__ void load_group(uint4 (&wv)[G][R], const WT* const (&wr)[R], int nch, int c0) {
+  constexpr int EP = Elt<WT>::per16;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int c = c0 + 32 * g;
+#pragma unroll
+    for (int r = 0; r < R; ++r) wv[g][r] = c < nch ? ld_stream(wr[r] + (size_t)c * EP) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <class WT, int R, int TP, int Q>
+__device__ __forceinline__ void fma_q(const uint4 (&wv)[R], const float* const (&xr)[TP], const float* gamma, int k,
+                                      float (&acc)[R * TP]) {
+  float4 gq = make_float4(1.f, 1.f, 1.f, 1.f);
+  if (gamma != nullptr) gq = __ldg(reinterpret_cast<const float4*>(gamma + k + 4 * Q));
+  float xv[TP][4];
+#pragma unroll
+  for (int t = 0; t < TP; ++t) {
+    float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (xr[t] != nullptr) x4 = __ldg(reinterpret_cast<const float4*>(xr[t] + k + 4 * Q));
+    xv[t][0] = x4.x * gq.x; xv[t][1] = x4.y * gq.y; xv[t][2] = x4.z * gq.z; xv[t][3] = x4.w * gq.w;
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    float w[4];
+    unpack4<WT, Q>(wv[r], w);
+#pragma unroll
+    for (int t = 0; t < TP; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[r * TP + t] = fmaf(w[e], xv[t][e], acc[r * TP + t]);
+  }
+}
+
+// acc[r*TP + t] = sum_k W[row r][k] * (gamma[k]) * x_t[k] over this lane's
+// chunks in increasing order. wv holds the unit's first chunk group on entry.
+template <class WT, int R, int TP, int G>
+__device__ __forceinline__ void unit_dot(uint4 (&wv)[G][R], const WT* const (&wr)[R], int K,
+                                         const float* const (&xr)[TP], const float* gamma, float (&acc)[R * TP]) {
+  constexpr int EP = Elt<WT>::per16;
+  const int nch = K / EP, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < R * TP; ++i) acc[i] = 0.f;
+  for (int c0 = lane; c0 < nch; c0 += 32 * G) {
+    if (c0 != lane) load_group<WT, R, G>(wv, wr, nch, c0);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int c = c0 + 32 * g;
+      if (c < nch) {
+        const int k = c * EP;
+        fma_q<WT, R, TP, 0>(wv[g], xr, gamma, k, acc);
+        if constexpr (EP >= 8) fma_q<WT, R, TP, 1>(wv[g], xr, gamma, k, acc);
+        if constexpr (EP >= 16) {
+          fma_q<WT, R, TP, 2>(wv[g], xr, gamma, k, acc);
+          fma_q<WT, R, TP, 3>(wv[g], xr, gamma, k, acc);
+        }
+      }
+    }
+  }
+}
+
+// Inverse RMS of rows [0, T) of x into inv[] (shared), warp r handling rows
+// r, r+8, ...: 1 / sqrt(mean(x^2) + eps).
+__device__ __forceinline__ void row_inv_rms(const float* x, int T, int K, float eps, float* inv) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < T; r += blockDim.x / 32) {
+    const float* xr = x + (size_t)r * K;
+    float ss = 0.f;
+    for (int k = lane; k < K; k += 32) ss = fmaf(xr[k], xr[k], ss);
+    ss = warp_sum(ss);
+    if (lane == 0) inv[r] = 1.0f / sqrtf(ss / (float)K + eps);
+  }
+}
+
+}  // namespace spec

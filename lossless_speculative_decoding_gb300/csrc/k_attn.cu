@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
   float* Qw = Vs + ATT_CHUNK * D_HEAD;              // [warps][D_HEAD]
   float* Pw = Qw + (ATT_THREADS / 32) * D_HEAD;     // [warps][64]
   __shared__ int s_last;
+  pdl_wait();
+  pdl_trigger();
   const int hk = blockIdx.y;
   const int gps = (R + RG - 1) / RG;
   const int s = blockIdx.z / gps, sub = blockIdx.z % gps;
@@ -203,11 +205,8 @@ void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int la
   const int dh = D.d;
   const size_t sm = (size_t)(ATT_CHUNK * (dh + 4) + ATT_CHUNK * dh + (ATT_THREADS / 32) * (dh + ATT_CHUNK)) *
                     sizeof(float);
-  if (dh == 128) {
-    k_attn_part<128><<<grid, ATT_THREADS, sm, st>>>(D, S, B, layer, T, R, RG, CS);
-  } else {
-    k_attn_part<64><<<grid, ATT_THREADS, sm, st>>>(D, S, B, layer, T, R, RG, CS);
-  }
+  if (dh == 128) launch_k(k_attn_part<128>, grid, dim3(ATT_THREADS), sm, st, D, S, B, layer, T, R, RG, CS);
+  else launch_k(k_attn_part<64>, grid, dim3(ATT_THREADS), sm, st, D, S, B, layer, T, R, RG, CS);
 }
 
 

@@ -30,6 +30,8 @@ __device__ __forceinline__ void embed_row(const Dims& D, const void* tok_embed, 
 // Verify rows: for sequence slot s of the step, row j holds the last
 // committed token (j = 0) or draft j, at position seq_len + j.
 __global__ void k_assemble_verify(Dims D, DevState S, StepBuf B, const void* tok_embed, int n_seq, int K) {
+  pdl_wait();
+  pdl_trigger();
   const int R = K + 1;
   const int row = blockIdx.x, s = row / R, j = row % R;
   const int max_batch = B.max_batch;
@@ -51,6 +53,8 @@ __global__ void k_assemble_verify(Dims D, DevState S, StepBuf B, const void* tok
 // row -(row_src[i] + 1) of `vis` (activation storage type).
 __global__ void k_assemble_prefill(Dims D, DevState S, StepBuf B, const void* tok_embed, const void* vis,
                                    int seq, int pos0) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x;
   const int src = B.row_src[row];
   if (threadIdx.x == 0) {
@@ -69,31 +73,38 @@ __global__ void k_assemble_prefill(Dims D, DevState S, StepBuf B, const void* to
 
 void launch_assemble_verify(const Dims& D, const DevState& S, const StepBuf& B, const void* tok_embed, int n_seq,
                             int K, cudaStream_t st) {
-  k_assemble_verify<<<n_seq * (K + 1), 256, 0, st>>>(D, S, B, tok_embed, n_seq, K);
+  launch_k(k_assemble_verify, dim3(n_seq * (K + 1)), dim3(256), 0, st, D, S, B, tok_embed, n_seq, K);
 }
 
 void launch_assemble_prefill(const Dims& D, const DevState& S, const StepBuf& B, const void* tok_embed,
                              const void* vis, int seq, int pos0, int T, cudaStream_t st) {
-  k_assemble_prefill<<<T, 256, 0, st>>>(D, S, B, tok_embed, vis, seq, pos0);
+  launch_k(k_assemble_prefill, dim3(T), dim3(256), 0, st, D, S, B, tok_embed, vis, seq, pos0);
 }
 
 // ---------------------------------------------------------------------------
-// FFN input RMSNorm + router + top-k, one block per row; the last block to
-// finish builds the per-expert pair lists. Probabilities: softmax over all E
-// experts; the top-k are taken in (probability desc, id asc) order and used
-// without renormalisation ("Jina AI releases jina-ocr-v1": 64 routed + 2
-// shared experts, top-6). Pair id = row * NS + slot (slots 0..k-1 routed,
-// k..k+S-1 shared). Active list: routed experts with rows, in id order, then
-// the shared experts with every row.
+// FFN input RMSNorm + router + top-k + token permutation. Grid (T rows,
+// ceil(E/16) expert groups): each block normalises its row (u, written once
+// by group 0) and computes the router logits of 16 experts, every warp
+// issuing all loads of its two expert rows at once. The last group block of a
+// row computes that row's softmax over all E experts and its top-k (in
+// (probability desc, id asc) order, used without renormalisation: "Jina AI
+// releases jina-ocr-v1", 64 routed + 2 shared experts, top-6); the last row
+// builds the per-expert pair lists. Pair id = row * NS + slot (slots 0..k-1
+// routed, k..k+S-1 shared). Active list: routed experts with rows, in id
+// order, then the shared experts with every row.
+constexpr int RT_EXPERTS = 16;     // experts per router block
+constexpr int RT_MAXC = 8;         // 16-byte chunks per lane loaded at once
+
 template <class RT>
 __global__ void __launch_bounds__(256) k_router(Dims D, StepBuf B, const float* __restrict__ gamma,
                                                 const RT* __restrict__ Wr, int T) {
   extern __shared__ __align__(16) float sm[];
   float* u = sm;                 // [h]
-  float* prob = u + D.h;         // [E]
   __shared__ float red[32];
   __shared__ int s_last;
-  const int row = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x, grp = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* x = B.x + (size_t)row * D.h;
   float ss = 0.f;
@@ -103,75 +114,103 @@ __global__ void __launch_bounds__(256) k_router(Dims D, StepBuf B, const float* 
   for (int k = threadIdx.x; k < D.h; k += blockDim.x) {
     const float v = (x[k] * inv) * gamma[k];
     u[k] = v;
-    B.u[(size_t)row * D.h + k] = v;
+    if (grp == 0) B.u[(size_t)row * D.h + k] = v;
   }
   __syncthreads();
   if (D.E > 0) {
     constexpr int EP = Elt<RT>::per16;
-    for (int e = warp; e < D.E; e += blockDim.x / 32) {
-      float acc = 0.f;
-      for (int k = lane * EP; k < D.h; k += 32 * EP) {
-        float w[EP];
-        unpack<RT>(*reinterpret_cast<const uint4*>(Wr + (size_t)e * D.h + k), w);
+    const int nch = D.h / EP;
+    const int e0 = grp * RT_EXPERTS + warp * 2;
+    float acc[2] = {0.f, 0.f};
+    for (int cb = lane; cb < nch; cb += 32 * RT_MAXC) {
+      uint4 wv[2][RT_MAXC];
 #pragma unroll
-        for (int i = 0; i < EP; ++i) acc = fmaf(w[i], u[k + i], acc);
-      }
-      acc = warp_sum(acc);
-      if (lane == 0) prob[e] = acc;
+      for (int ee = 0; ee < 2; ++ee)
+#pragma unroll
+        for (int m = 0; m < RT_MAXC; ++m) {
+          const int c = cb + 32 * m;
+          wv[ee][m] = (e0 + ee < D.E && c < nch) ? ld_stream(Wr + (size_t)(e0 + ee) * D.h + (size_t)c * EP)
+                                                  : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+      for (int ee = 0; ee < 2; ++ee)
+#pragma unroll
+        for (int m = 0; m < RT_MAXC; ++m) {
+          const int c = cb + 32 * m;
+          if (c < nch) {
+            float w[EP];
+            unpack<RT>(wv[ee][m], w);
+#pragma unroll
+            for (int i = 0; i < EP; ++i) acc[ee] = fmaf(w[i], u[c * EP + i], acc[ee]);
+          }
+        }
     }
-    __syncthreads();
-    if (warp == 0) {
-      // softmax over E <= 256 logits, lane l owning experts l, l+32, ...
-      constexpr int MAXE = 8;
-      float v[MAXE];
-      float m = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < MAXE; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = e < D.E ? prob[e] : -INFINITY;
-        m = fmaxf(m, v[i]);
-      }
-      m = warp_max(m);
-      float z = 0.f;
-#pragma unroll
-      for (int i = 0; i < MAXE; ++i) {
-        v[i] = (lane + 32 * i < D.E) ? expf(v[i] - m) : 0.f;
-        z += v[i];
-      }
-      z = warp_sum(z);
-#pragma unroll
-      for (int i = 0; i < MAXE; ++i) v[i] = (lane + 32 * i < D.E) ? v[i] / z : -1.f;
-      // top-k: k rounds of a warp argmax, (probability desc, id asc)
-      for (int r = 0; r < D.k; ++r) {
-        float bv = -1.f;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < MAXE; ++i) {
-          const int e = lane + 32 * i;
-          if (v[i] > bv) { bv = v[i]; bi = e; }      // increasing e: ties keep the lower id
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if (lane == 0) {
-          B.ids[row * D.k + r] = bi;
-          B.wts[row * D.k + r] = bv;
-        }
-#pragma unroll
-        for (int i = 0; i < MAXE; ++i)
-          if (lane + 32 * i == bi) v[i] = -1.f;        // taken
-      }
+    for (int ee = 0; ee < 2; ++ee) {
+      const float v = warp_sum(acc[ee]);
+      if (lane == 0 && e0 + ee < D.E) B.rlogit[(size_t)row * D.E + e0 + ee] = v;
     }
   }
-  // ---- the last block to finish builds the permutation ----
+  // ---- the last expert-group block of this row: softmax + top-k ----
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const int prev = atomicAdd(B.counter, 1);
-    s_last = (prev == (int)gridDim.x - 1);
+    s_last = (atomicAdd(B.cnt_row + row, 1) == (int)gridDim.y - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (D.E > 0 && warp == 0) {
+    // softmax over E <= 256 logits, lane l owning experts l, l+32, ...
+    constexpr int MAXE = 8;
+    float v[MAXE];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < MAXE; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < D.E ? __ldcg(B.rlogit + (size_t)row * D.E + e) : -INFINITY;
+      m = fmaxf(m, v[i]);
+    }
+    m = warp_max(m);
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < MAXE; ++i) {
+      v[i] = (lane + 32 * i < D.E) ? expf(v[i] - m) : 0.f;
+      z += v[i];
+    }
+    z = warp_sum(z);
+#pragma unroll
+    for (int i = 0; i < MAXE; ++i) v[i] = (lane + 32 * i < D.E) ? v[i] / z : -1.f;
+    // top-k: k rounds of a warp argmax, (probability desc, id asc)
+    for (int r = 0; r < D.k; ++r) {
+      float bv = -1.f;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < MAXE; ++i) {
+        const int e = lane + 32 * i;
+        if (v[i] > bv) { bv = v[i]; bi = e; }      // increasing e: ties keep the lower id
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0) {
+        B.ids[row * D.k + r] = bi;
+        B.wts[row * D.k + r] = bv;
+      }
+#pragma unroll
+      for (int i = 0; i < MAXE; ++i)
+        if (lane + 32 * i == bi) v[i] = -1.f;        // taken
+    }
+  }
+  if (threadIdx.x == 0) B.cnt_row[row] = 0;
+  // ---- the last row builds the permutation ----
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = (atomicAdd(B.counter, 1) == (int)gridDim.x - 1);
   }
   __syncthreads();
   if (!s_last) return;
@@ -226,61 +265,27 @@ cudaError_t configure_small_kernels() {
 
 void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
   const int E1 = D.E > 0 ? D.E : 1;
-  const size_t words = (size_t)D.h + E1 > (size_t)T * D.k + 2 * E1 ? (size_t)D.h + E1 : (size_t)T * D.k + 2 * E1;
+  const size_t words = (size_t)D.h > (size_t)T * D.k + 2 * E1 ? (size_t)D.h : (size_t)T * D.k + 2 * E1;
   const size_t sm = words * sizeof(float);
+  const dim3 grid(T, D.E > 0 ? (D.E + RT_EXPERTS - 1) / RT_EXPERTS : 1);
   if (D.act_f32) {
-    k_router<float><<<T, 256, sm, st>>>(D, B, W.ffn_norm, (const float*)W.w_router, T);
+    launch_k(k_router<float>, grid, dim3(256), sm, st, D, B, W.ffn_norm, (const float*)W.w_router, T);
   } else {
-    k_router<bf16_t><<<T, 256, sm, st>>>(D, B, W.ffn_norm, (const bf16_t*)W.w_router, T);
+    launch_k(k_router<bf16_t>, grid, dim3(256), sm, st, D, B, W.ffn_norm, (const bf16_t*)W.w_router, T);
   }
 }
 
 // ---------------------------------------------------------------------------
-// Acceptance + commit, one thread per sequence of the step ("End-to-end OCR
-// expert model ...", section 6.1: accept the agreeing prefix from the left,
-// the target supplies the token at the first divergence). With g the greedy
-// tokens of the K+1 rows: a = max{i <= n_draft : d_j = g_(j-1) for j <= i},
-// bonus = g_a. The sequence keeps the KV of its last token and the a accepted
-// drafts (length n + a + 1); the rejected rows' slots are stale and are
-// overwritten by the next step. Pages wholly past max(new length, reserved
-// pages) leave the block table (-1); the host allocator mirrors this.
+// Acceptance + commit as its own kernel (one thread per sequence); the
+// verify step normally runs it inside the LM head's last block.
 __global__ void k_commit(Dims D, DevState S, StepBuf B, int n_seq, int K) {
+  pdl_wait();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
-  if (s >= n_seq) return;
-  const int max_batch = B.max_batch;
-  const int R = K + 1;
-  const int seq = B.step_in[s];
-  const int* d = B.step_in + max_batch + s * K;
-  const int nd = min(max(B.step_in[max_batch + max_batch * K + s], 0), K);
-  const int* g = B.g + s * R;
-  int a = 0;
-  while (a < nd && d[a] == g[a]) ++a;
-  const int bonus = g[a];
-  const int n = S.seq_len[seq];
-  const int new_len = n + a + 1;
-  int no = S.n_out[seq];
-  int* out = S.out_tok + (size_t)seq * D.max_ctx;
-  for (int j = 0; j < a; ++j)
-    if (no + j < D.max_ctx) out[no + j] = d[j];
-  if (no + a < D.max_ctx) out[no + a] = bonus;
-  S.n_out[seq] = no + a + 1;
-  S.seq_len[seq] = new_len;
-  S.last_tok[seq] = bonus;
-  int keep = (new_len + D.P - 1) / D.P;
-  if (S.keep_pages[seq] > keep) keep = S.keep_pages[seq];
-  int* bt = const_cast<int*>(S.bt) + (size_t)seq * D.max_pages;
-  for (int i = keep; i < D.max_pages; ++i) bt[i] = -1;
-  B.step_out[s] = a;
-  B.step_out[max_batch + s] = bonus;
-  if (s == 0) B.step_out[2 * max_batch] = *S.err;
-  int* ua = reinterpret_cast<int*>(B.out_ptrs[0]);
-  int* ub = reinterpret_cast<int*>(B.out_ptrs[1]);
-  if (ua) ua[s] = a;
-  if (ub) ub[s] = bonus;
+  if (s < n_seq) commit_seq(D, S, B, s, K, B.g);
 }
 
 void launch_commit(const Dims& D, const DevState& S, const StepBuf& B, int n_seq, int K, cudaStream_t st) {
-  k_commit<<<(n_seq + 63) / 64, 64, 0, st>>>(D, S, B, n_seq, K);
+  launch_k(k_commit, dim3((n_seq + 63) / 64), dim3(64), 0, st, D, S, B, n_seq, K);
 }
 
 // Copy device-resident step inputs into the staging block.
@@ -306,8 +311,8 @@ void launch_stage_dev(const StepBuf& B, int n_seq, int K, const int* seq_ids, co
 int launches_per_step(const Dims& D) {
   // assemble + per layer (qkv + RoPE + KV write, split-KV attention + merge,
   // O-proj + residual, router + top-k + permute, gate/up + SwiGLU, down +
-  // combine) + LM head + argmax + accept/commit
-  return 1 + D.L * 6 + 1 + 1;
+  // combine) + LM head with argmax and accept/commit
+  return 1 + D.L * 6 + 1;
 }
 
 }  // namespace spec

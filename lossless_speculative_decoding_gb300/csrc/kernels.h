@@ -30,6 +30,7 @@ struct Dims {
   int max_pages;         // block-table row length
   int max_ctx;
   int NS;                // slots per row = k + S
+  int n_sm;              // streaming multiprocessors (persistent grids)
   float eps, theta;
   size_t page_elems;     // elements per KV page (all layers)
 };
@@ -59,9 +60,11 @@ struct StepBuf {
   int* ids; float* wts;              // [T, k]
   int* perm;                         // [T*NS] pair ids grouped by expert
   int* act_expert; int* act_off; int* act_cnt; int* n_active;  // active-expert list
-  int* counter;                      // router arrival counter (kept at zero between launches)
+  int* counter;                      // router arrival counter over rows (kept at zero between launches)
+  float* rlogit;                     // [Tmax, E] router logits
+  int* cnt_row;                      // [Tmax] router arrivals per row (expert-group blocks)
   int* cnt_att;                      // [Tmax * Hkv] attention arrivals per (row group, kv head)
-  int* cnt_down;                     // [ceil(h/32)] expert-down arrivals per output column tile
+  int* cnt_down;                     // [h/4 + 1] expert-down arrivals per 4-column output tile
   int* cnt_lm;                       // [ceil(Tmax/TP)] LM-head arrivals per row pass
   float* h_act;      // [T*NS, inter]
   float* y;          // [T*NS, h]
@@ -91,6 +94,12 @@ void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, cuda
 void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
 void launch_lmhead(const Dims& D, const StepBuf& B, const void* lm_head, const float* final_norm,
                    const float* x, int T, float* logits_dbg, bool fuse_argmax, cudaStream_t st);
+// Streaming LM head + argmax for the verify step / prefill; with commit, its
+// last block also accepts and commits the n_seq sequences (K drafts each).
+void launch_lmhead_step(const Dims& D, const DevState& S, const StepBuf& B, const void* lm_head,
+                        const float* final_norm, const float* x, int T, float* logits_dbg, bool commit, int n_seq,
+                        int K, cudaStream_t st);
+int lmhead_step_warps(const Dims& D);
 void launch_argmax(const StepBuf& B, int T, cudaStream_t st);
 
 // Kernel classes (for profiling); order matches spec_kernel_class_name().
@@ -102,6 +111,29 @@ void launch_stage_dev(const StepBuf& B, int n_seq, int K, const int* seq_ids, co
 int launches_per_step(const Dims& D);
 // Record `msg` as the calling thread's last error (spec_last_error) and return code.
 int set_last_error(int code, const char* msg);
+// Programmatic dependent launch is used for every step kernel unless this
+// thread turns it off (the profiler does, so its events bracket one kernel).
+inline bool& pdl_enabled() {
+  static thread_local bool on = true;
+  return on;
+}
+
+template <class... KArgs, class... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Opt a kernel in to the largest dynamic shared memory the device allows
 // next to its static shared memory (an upper bound: occupancy follows the
 // bytes each launch asks for). Called at model set-up, never during capture.
@@ -117,6 +149,7 @@ inline cudaError_t allow_dyn_smem(K kernel) {
   return e;
 }
 cudaError_t configure_gemv_kernels();
+cudaError_t configure_stream_kernels();
 cudaError_t configure_attn_kernels();
 cudaError_t configure_small_kernels();
 

@@ -226,8 +226,9 @@ struct spec_model {
     const int T = n_seq * R;
     run_k(p, KC_ASSEMBLE, [&] { launch_assemble_verify(D, S, B, tok_embed, n_seq, K, stream); });
     enqueue_layers(T, R, p);
-    run_k(p, KC_LMHEAD, [&] { launch_lmhead(D, B, lm_head, final_norm, B.x, T, logits_dbg, true, stream); });
-    if (commit) run_k(p, KC_COMMIT, [&] { launch_commit(D, S, B, n_seq, K, stream); });
+    run_k(p, KC_LMHEAD, [&] {
+      launch_lmhead_step(D, S, B, lm_head, final_norm, B.x, T, logits_dbg, commit, n_seq, K, stream);
+    });
   }
 
   int graph_for(int n_seq, cudaGraphExec_t* out) {
@@ -303,10 +304,16 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
   D.wdtype = c.wdtype; D.act_f32 = c.wdtype == SPEC_F32; D.P = c.page_size;
   D.max_ctx = c.max_ctx; D.NS = c.top_k + c.n_shared; D.eps = c.rms_eps; D.theta = c.rope_theta;
   D.max_pages = (c.max_ctx + c.page_size - 1) / c.page_size;
+  {
+    int dev = 0;
+    CU(cudaGetDevice(&dev));
+    CU(cudaDeviceGetAttribute(&D.n_sm, cudaDevAttrMultiProcessorCount, dev));
+  }
   D.page_elems = (size_t)c.n_layers * 2 * c.n_kv_heads * c.page_size * c.head_dim;
   const size_t kv_elt = D.act_f32 ? 4 : 2;
 
   CU(configure_gemv_kernels());
+  CU(configure_stream_kernels());
   CU(configure_attn_kernels());
   CU(configure_small_kernels());
 
@@ -372,7 +379,7 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
   StepBuf& B = m->B;
   const int T = m->Tmax, NS = D.NS;
   B.n_chunk_max = (c.max_ctx + ATT_CHUNK - 1) / ATT_CHUNK;
-  B.n_vblocks = (c.vocab + GEMV_WARPS * 4 - 1) / (GEMV_WARPS * 4);
+  B.n_vblocks = lmhead_step_warps(D);             // one argmax candidate per LM-head warp
   B.max_batch = c.max_batch;
   const int max_active = (D.E > 0 ? std::min(D.E, T * std::max(D.k, 1)) : 0) + D.S;
   if ((rc = m->dalloc(&B.row_tok, T)) || (rc = m->dalloc(&B.row_pos, T)) || (rc = m->dalloc(&B.row_seq, T)) ||
@@ -385,8 +392,9 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
       (rc = m->dalloc(&B.wts, (size_t)T * std::max(D.k, 1))) || (rc = m->dalloc(&B.perm, (size_t)T * NS)) ||
       (rc = m->dalloc(&B.act_expert, max_active)) || (rc = m->dalloc(&B.act_off, max_active)) ||
       (rc = m->dalloc(&B.act_cnt, max_active)) || (rc = m->dalloc(&B.n_active, 1)) ||
-      (rc = m->dalloc(&B.counter, 4)) || (rc = m->dalloc(&B.cnt_att, (size_t)T * D.Hkv)) ||
-      (rc = m->dalloc(&B.cnt_down, (D.h + 31) / 32)) || (rc = m->dalloc(&B.cnt_lm, (T + GEMV_TP - 1) / GEMV_TP)) || (rc = m->dalloc(&B.h_act, (size_t)T * NS * D.inter)) ||
+      (rc = m->dalloc(&B.counter, 4)) || (rc = m->dalloc(&B.rlogit, (size_t)T * std::max(D.E, 1))) ||
+      (rc = m->dalloc(&B.cnt_row, T)) || (rc = m->dalloc(&B.cnt_att, (size_t)T * D.Hkv)) ||
+      (rc = m->dalloc(&B.cnt_down, D.h / 4 + 1)) || (rc = m->dalloc(&B.cnt_lm, (T + GEMV_TP - 1) / GEMV_TP)) || (rc = m->dalloc(&B.h_act, (size_t)T * NS * D.inter)) ||
       (rc = m->dalloc(&B.y, (size_t)T * NS * D.h)) ||
       (rc = m->dalloc(&B.am_val, (size_t)T * B.n_vblocks)) || (rc = m->dalloc(&B.am_idx, (size_t)T * B.n_vblocks)) ||
       (rc = m->dalloc(&B.g, T)))
@@ -399,8 +407,9 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
   B.out_ptrs = reinterpret_cast<unsigned long long*>(stage);
   B.step_in = stage + 4;
   CU(cudaMemset(B.counter, 0, 4 * sizeof(int)));
+  CU(cudaMemset(B.cnt_row, 0, (size_t)T * sizeof(int)));
   CU(cudaMemset(B.cnt_att, 0, (size_t)T * D.Hkv * sizeof(int)));
-  CU(cudaMemset(B.cnt_down, 0, ((D.h + 31) / 32) * sizeof(int)));
+  CU(cudaMemset(B.cnt_down, 0, (D.h / 4 + 1) * sizeof(int)));
   CU(cudaMemset(B.cnt_lm, 0, ((T + GEMV_TP - 1) / GEMV_TP) * sizeof(int)));
   CU(cudaMemset(stage, 0, (4 + m->step_in_n) * sizeof(int)));
   CU(cudaMallocHost(&m->pin_in, std::max(4 + m->step_in_n, T) * sizeof(int32_t)));
@@ -432,8 +441,8 @@ static int run_prefill_rows(spec_model* m, int slot, const std::vector<int32_t>&
     launch_assemble_prefill(m->D, m->S, m->B, m->tok_embed, vis, slot, start + c0, T, m->stream);
     m->enqueue_layers(T, T);
     if (c0 + T == n && out_tok) {
-      launch_lmhead(m->D, m->B, m->lm_head, m->final_norm, m->B.x + (size_t)(T - 1) * m->D.h, 1, nullptr, true,
-                    m->stream);
+      launch_lmhead_step(m->D, m->S, m->B, m->lm_head, m->final_norm, m->B.x + (size_t)(T - 1) * m->D.h, 1,
+                         nullptr, false, 0, 0, m->stream);
       CU(cudaMemcpyAsync(m->pin_out, m->B.g, sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
     }
     // the staging buffer is reused by the next chunk
@@ -675,6 +684,11 @@ int spec_profile_steps_dev(spec_model* m, int n_seq, const int32_t* seq_ids_dev,
   p.cls.resize(per_step);
   for (auto& e : p.ev) CU(cudaEventCreate(&e));
   CU(cudaMallocHost(&p.act, m->D.L * sizeof(int32_t)));
+  struct PdlOff {
+    bool saved;
+    PdlOff() : saved(pdl_enabled()) { pdl_enabled() = false; }   // events bracket single kernels
+    ~PdlOff() { pdl_enabled() = saved; }
+  } pdl_off;
   std::vector<double> ms(KC_COUNT, 0.0);
   std::vector<int64_t> launches(KC_COUNT, 0), units(KC_COUNT, 0);
   int rc = SPEC_OK;

@@ -277,3 +277,34 @@ def test_errors_leave_state_unchanged(tiny):
     assert e.value.code == -2 and gm.length(0) == L + steps
     gm.release(0)
     assert B.spec_free_pages(gm.h) == 6
+
+
+MOE_MID = syn.scaled(syn.MOE3B, name="moe-mid-bf16", n_layers=2, vocab=32768)
+
+
+def test_mid_size_lossless_and_parity():
+    """3B-MoE per-layer shapes (h 1280, 64 experts top-6 + 2 shared, inter 896)
+    with 2 layers and a 32K vocabulary: every persistent GEMV loop runs several
+    work items per warp. Speculative decoding (K = 3) must reproduce, token for
+    token, a one-row-per-step greedy model, and the verify rows must match the
+    oracle within 2e-2 of each row's range."""
+    w = syn.generate_weights(MOE_MID, 3)
+    wl = syn.Workload("mid", MOE_MID, 1, 3, "iid", 0.576, (256, 0, 0), 16, 0, (80,))
+    prompt = syn.make_prompts(wl)[0]
+    g0 = gpu_model(MOE_MID, w, max_ctx=512, max_draft=0)
+    greedy, _ = run_spec(g0, 0, prompt, 80, 0, lambda n, m, s: [])
+    g0.close()
+    g3 = gpu_model(MOE_MID, w, max_ctx=512, max_draft=3)
+    toks, steps = run_spec(g3, 0, prompt, 80, 3, _drafter_vs(greedy, 0.576, MOE_MID.vocab))
+    assert np.array_equal(toks, greedy)
+    assert sum(a for _, a, _ in steps) > 0
+    # verify rows at the final state against the oracle
+    om = oracle.OracleModel(w)
+    cache = oracle.KVCache(MOE_MID)
+    x = oracle.prompt_embeddings(om, prompt)
+    rows = np.concatenate([x, om.tok_embed[toks[:-1]]])
+    oracle.forward(om, cache, rows, np.arange(len(rows)))
+    d = [int(t) for t in np.random.default_rng(1).integers(0, MOE_MID.vocab, 3)]
+    lg = g3.debug_logits([0], np.array(d))
+    ol = oracle.verify_rows(om, cache, int(toks[-1]), d)
+    assert row_tol_ok(lg, ol, 2e-2).all()
