@@ -162,7 +162,8 @@ def class_bytes(cfg, stats: dict, T: int, ctx_sum: float, n_steps: int) -> dict:
         n("expert_gateup_swiglu") * (T * h * 4 + T * NS * cfg.inter * 4)
     out["expert_down"] = u("expert_down") * h * (cfg.inter * we + sc) + \
         n("expert_down") * (T * NS * cfg.inter * 4 + T * NS * h * 4)
-    out["lmhead_argmax"] = n("lmhead_argmax") * (cfg.vocab * h * se + T * h * 4)
+    out["expert_combine"] = n("expert_combine") * (T * NS * h * 4 + 2 * T * h * 4)
+    out["lmhead_argmax_commit"] = n("lmhead_argmax_commit") * (cfg.vocab * h * se + T * h * 4)
     return out
 
 

@@ -193,7 +193,7 @@ typedef struct spec_kernel_stat {
   int32_t launches;
   int64_t units;
 } spec_kernel_stat;
-#define SPEC_KCLASS_COUNT 10
+#define SPEC_KCLASS_COUNT 11
 /* Run n_steps device-resident verify steps WITHOUT graph replay, bracketing
  * every kernel launch with CUDA events. Arguments as in
  * spec_verify_step_batch_dev; step s reads drafts_dev + s * drafts_step_stride.

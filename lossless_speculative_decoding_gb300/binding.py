@@ -31,7 +31,7 @@ class spec_kernel_stat(ctypes.Structure):
     _fields_ = [("ms", ctypes.c_float), ("launches", ctypes.c_int32), ("units", ctypes.c_int64)]
 
 
-SPEC_KCLASS_COUNT = 10
+SPEC_KCLASS_COUNT = 11
 
 
 class spec_config(ctypes.Structure):

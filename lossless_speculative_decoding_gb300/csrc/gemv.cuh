@@ -212,14 +212,140 @@ __device__ __forceinline__ void unit_dot(uint4 (&wv)[G][R], const WT* const (&wr
   }
 }
 
+// ---------------------------------------------------------------------------
+// Paired accumulation: each output keeps two partial sums -- even and odd
+// elements of every chunk, in increasing chunk order -- updated by one packed
+// fma.rn.f32x2 (each half rounds exactly like fmaf), and returns their sum.
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float sum2(unsigned long long v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return a + b;
+}
+__device__ __forceinline__ void ffma2(unsigned long long& acc, unsigned long long w, unsigned long long x) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(w), "l"(x));
+}
+
+// Four elements of group Q of a 16-byte weight vector as two packed pairs.
+template <class WT, int Q>
+__device__ __forceinline__ void wpairs(const uint4& v, unsigned long long& p0, unsigned long long& p1) {
+  float w[4];
+  unpack4<WT, Q>(v, w);
+  p0 = pack2(w[0], w[1]);
+  p1 = pack2(w[2], w[3]);
+}
+
+template <class WT, int R, int TP, int Q>
+__device__ __forceinline__ void fma2_q(const uint4 (&wv)[R], const float* const (&xr)[TP], int k,
+                                       unsigned long long (&acc)[R * TP]) {
+  unsigned long long xa[TP], xb[TP];
+#pragma unroll
+  for (int t = 0; t < TP; ++t) {
+    float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (xr[t] != nullptr) x4 = *reinterpret_cast<const float4*>(xr[t] + k + 4 * Q);
+    xa[t] = pack2(x4.x, x4.y);
+    xb[t] = pack2(x4.z, x4.w);
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    unsigned long long w0, w1;
+    wpairs<WT, Q>(wv[r], w0, w1);
+#pragma unroll
+    for (int t = 0; t < TP; ++t) {
+      ffma2(acc[r * TP + t], w0, xa[t]);
+      ffma2(acc[r * TP + t], w1, xb[t]);
+    }
+  }
+}
+
+// out[r*TP + t] = sum_k W[row r][k] * x_t[k] over this lane's chunks
+// (increasing order, even/odd pairs). x rows may live in shared or global
+// memory (plain loads); wv holds the unit's first chunk group on entry.
+template <class WT, int R, int TP, int G>
+__device__ __forceinline__ void unit_dot2(uint4 (&wv)[G][R], const WT* const (&wr)[R], int K,
+                                          const float* const (&xr)[TP], float (&out)[R * TP]) {
+  constexpr int EP = Elt<WT>::per16;
+  const int nch = K / EP, lane = threadIdx.x & 31;
+  unsigned long long acc[R * TP];
+#pragma unroll
+  for (int i = 0; i < R * TP; ++i) acc[i] = 0ull;
+  for (int c0 = lane; c0 < nch; c0 += 32 * G) {
+    if (c0 != lane) load_group<WT, R, G>(wv, wr, nch, c0);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int c = c0 + 32 * g;
+      if (c < nch) {
+        const int k = c * EP;
+        fma2_q<WT, R, TP, 0>(wv[g], xr, k, acc);
+        if constexpr (EP >= 8) fma2_q<WT, R, TP, 1>(wv[g], xr, k, acc);
+        if constexpr (EP >= 16) {
+          fma2_q<WT, R, TP, 2>(wv[g], xr, k, acc);
+          fma2_q<WT, R, TP, 3>(wv[g], xr, k, acc);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < R * TP; ++i) out[i] = sum2(acc[i]);
+}
+
+// Stage rows [t0, t0 + n) of x (row stride K) into xs[TP][K] as
+// (x * inv[t]) * gamma[k] (gamma may be null: plain copy); zeros past n.
+__device__ __forceinline__ void stage_norm(float* xs, const float* x, int t0, int n, int K, const float* inv,
+                                           const float* gamma) {
+  const int K4 = K / 4;
+#pragma unroll 4
+  for (int i = threadIdx.x; i < GEMV_TP * K4; i += blockDim.x) {
+    const int t = i / K4, k4 = i % K4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < n) {
+      v = reinterpret_cast<const float4*>(x + (size_t)(t0 + t) * K)[k4];
+      if (gamma != nullptr) {
+        const float s = inv[t0 + t];
+        const float4 g = reinterpret_cast<const float4*>(gamma)[k4];
+        v = make_float4((v.x * s) * g.x, (v.y * s) * g.y, (v.z * s) * g.z, (v.w * s) * g.w);
+      }
+    }
+    reinterpret_cast<float4*>(xs)[i] = v;
+  }
+}
+
+// One element of the expert combine: x[t][kcol] + sum over slots s (in
+// order) of w[t][s] * y[t*NS + s][kcol] (routed weight p, shared weight 1).
+__device__ __forceinline__ float combine_one(const float* x, const float* y, const float* wts, int t, int kcol,
+                                             int K, int NS, int k) {
+  float a = 0.f;
+  for (int s = 0; s < NS; ++s) {
+    const float w = s < k ? wts[t * k + s] : 1.f;
+    a = fmaf(w, y[((size_t)t * NS + s) * K + kcol], a);
+  }
+  return x[(size_t)t * K + kcol] + a;
+}
+
 // Inverse RMS of rows [0, T) of x into inv[] (shared), warp r handling rows
-// r, r+8, ...: 1 / sqrt(mean(x^2) + eps).
+// r, r+8, ...: 1 / sqrt(mean(x^2) + eps). Each lane issues up to eight
+// float4 loads at once (K must be a multiple of 4); lane partials are added in
+// a fixed order, so the result depends only on the row.
 __device__ __forceinline__ void row_inv_rms(const float* x, int T, int K, float eps, float* inv) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K4 = K / 4;
   for (int r = warp; r < T; r += blockDim.x / 32) {
-    const float* xr = x + (size_t)r * K;
+    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)r * K);
     float ss = 0.f;
-    for (int k = lane; k < K; k += 32) ss = fmaf(xr[k], xr[k], ss);
+    for (int b = lane; b < K4; b += 32 * 8) {
+      float4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = (b + 32 * i < K4) ? xr[b + 32 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        ss = fmaf(v[i].x, v[i].x, ss); ss = fmaf(v[i].y, v[i].y, ss);
+        ss = fmaf(v[i].z, v[i].z, ss); ss = fmaf(v[i].w, v[i].w, ss);
+      }
+    }
     ss = warp_sum(ss);
     if (lane == 0) inv[r] = 1.0f / sqrtf(ss / (float)K + eps);
   }

@@ -18,15 +18,71 @@ namespace spec {
 
 constexpr int ATT_THREADS = 128;
 
-template <int D_HEAD>
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+// Eight consecutive K elements of the storage type as floats.
+template <class KT> __device__ __forceinline__ void load8(const KT* p, float* o);
+template <> __device__ __forceinline__ void load8<float>(const float* p, float* o) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+template <> __device__ __forceinline__ void load8<bf16_t>(const bf16_t* p, float* o) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = __uint_as_float(w[i] << 16);
+    o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+// N (2 or 4) consecutive V elements of the storage type as floats.
+template <class KT, int N> __device__ __forceinline__ void loadv(const KT* p, float* o);
+template <> __device__ __forceinline__ void loadv<float, 4>(const float* p, float* o) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+}
+template <> __device__ __forceinline__ void loadv<float, 2>(const float* p, float* o) {
+  const float2 a = *reinterpret_cast<const float2*>(p);
+  o[0] = a.x; o[1] = a.y;
+}
+template <> __device__ __forceinline__ void loadv<bf16_t, 4>(const bf16_t* p, float* o) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  o[0] = __uint_as_float(v.x << 16); o[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  o[2] = __uint_as_float(v.y << 16); o[3] = __uint_as_float(v.y & 0xFFFF0000u);
+}
+template <> __device__ __forceinline__ void loadv<bf16_t, 2>(const bf16_t* p, float* o) {
+  const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+  o[0] = __uint_as_float(v << 16); o[1] = __uint_as_float(v & 0xFFFF0000u);
+}
+
+template <int D_HEAD, class KT>
+struct AttSmem {
+  static constexpr int KST = D_HEAD + 16 / (int)sizeof(KT);   // padded K row (one extra 16-byte piece)
+  static constexpr size_t k_bytes = (size_t)ATT_CHUNK * KST * sizeof(KT);
+  static constexpr size_t v_bytes = (size_t)ATT_CHUNK * D_HEAD * sizeof(KT);
+  static constexpr size_t q_bytes = (size_t)(ATT_THREADS / 32) * D_HEAD * sizeof(float);
+  static constexpr size_t p_bytes = (size_t)(ATT_THREADS / 32) * ATT_CHUNK * sizeof(float);
+  static constexpr size_t total = k_bytes + v_bytes + q_bytes + p_bytes + ATT_CHUNK * sizeof(int);
+};
+
+template <int D_HEAD, class KT>
 __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, StepBuf B, int layer, int T,
                                                            int R, int RG, int CS) {
-  constexpr int KLD = D_HEAD + 4;                  // padded row stride of K in shared memory
-  extern __shared__ __align__(16) float sm[];
-  float* Ks = sm;                                   // [64][KLD]
-  float* Vs = Ks + ATT_CHUNK * KLD;                 // [64][D_HEAD]
-  float* Qw = Vs + ATT_CHUNK * D_HEAD;              // [warps][D_HEAD]
-  float* Pw = Qw + (ATT_THREADS / 32) * D_HEAD;     // [warps][64]
+  using L = AttSmem<D_HEAD, KT>;
+  constexpr int KST = L::KST;
+  constexpr int PPR = D_HEAD * (int)sizeof(KT) / 16;          // 16-byte pieces per key row
+  extern __shared__ __align__(16) unsigned char smraw[];
+  KT* Ks = reinterpret_cast<KT*>(smraw);                        // [64][KST]
+  KT* Vs = reinterpret_cast<KT*>(smraw + L::k_bytes);           // [64][D_HEAD]
+  float* Qw = reinterpret_cast<float*>(smraw + L::k_bytes + L::v_bytes);    // [warps][D_HEAD]
+  float* Pw = Qw + (ATT_THREADS / 32) * D_HEAD;                 // [warps][64]
+  int* pg = reinterpret_cast<int*>(Pw + (ATT_THREADS / 32) * ATT_CHUNK);  // [64] page of each key
   __shared__ int s_last;
   pdl_wait();
   pdl_trigger();
@@ -44,6 +100,7 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
   const float scale = 1.0f / sqrtf((float)D_HEAD);
   const size_t head_off = (((size_t)layer * 2) * D.Hkv + hk) * D.P * D_HEAD;   // K of (layer, hk)
   const size_t v_off = (size_t)D.Hkv * D.P * D_HEAD;                            // K -> V
+  const KT* kv = reinterpret_cast<const KT*>(S.kv);
   float* qw = Qw + warp * D_HEAD;
   float* pw = Pw + warp * ATT_CHUNK;
 
@@ -51,36 +108,25 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
     const int k0 = c * ATT_CHUNK;
     const int nk = min(ATT_CHUNK, maxpos + 1 - k0);
     __syncthreads();
-    // ---- stage K and V of keys [k0, k0 + nk) (16-byte vectors) ----
-    constexpr int VPK = D_HEAD / 4;                  // float4 per key row
-    for (int i = threadIdx.x; i < ATT_CHUNK * VPK; i += ATT_THREADS) {
-      const int key = i / VPK, c4 = (i % VPK) * 4;
-      float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-      if (key < nk) {
-        const int pos = k0 + key;
-        const int page = S.bt[(size_t)seq * D.max_pages + pos / D.P];
-        if (page >= 0) {
-          const size_t e = (size_t)page * D.page_elems + head_off + (size_t)(pos % D.P) * D_HEAD + c4;
-          if (D.act_f32) {
-            const float* kvp = reinterpret_cast<const float*>(S.kv);
-            kv = *reinterpret_cast<const float4*>(kvp + e);
-            vv = *reinterpret_cast<const float4*>(kvp + e + v_off);
-          } else {
-            const uint16_t* kvp = reinterpret_cast<const uint16_t*>(S.kv);
-            const uint2 a = *reinterpret_cast<const uint2*>(kvp + e);
-            const uint2 b = *reinterpret_cast<const uint2*>(kvp + e + v_off);
-            kv = make_float4(__uint_as_float(a.x << 16), __uint_as_float(a.x & 0xFFFF0000u),
-                             __uint_as_float(a.y << 16), __uint_as_float(a.y & 0xFFFF0000u));
-            vv = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xFFFF0000u),
-                             __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xFFFF0000u));
-          }
-        } else if (threadIdx.x == 0) {
-          atomicOr(S.err, DERR_PAGE);
-        }
-      }
-      *reinterpret_cast<float4*>(Ks + key * KLD + c4) = kv;
-      *reinterpret_cast<float4*>(Vs + key * D_HEAD + c4) = vv;
+    // ---- pages of the chunk's keys, then every 16-byte piece of K and V in flight at once ----
+    for (int key = threadIdx.x; key < nk; key += ATT_THREADS) {
+      const int page = S.bt[(size_t)seq * D.max_pages + (k0 + key) / D.P];
+      pg[key] = page;
+      if (page < 0) atomicOr(S.err, DERR_PAGE);
     }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 2 * nk * PPR; i += ATT_THREADS) {
+      const int isv = i >= nk * PPR;
+      const int j = isv ? i - nk * PPR : i;
+      const int key = j / PPR, piece = j % PPR;
+      const int page = pg[key];
+      if (page < 0) continue;
+      const size_t e = (size_t)page * D.page_elems + head_off + (isv ? v_off : 0) +
+                       (size_t)((k0 + key) % D.P) * D_HEAD + piece * (16 / sizeof(KT));
+      KT* dst = isv ? Vs + key * D_HEAD + piece * (16 / sizeof(KT)) : Ks + key * KST + piece * (16 / sizeof(KT));
+      cp_async16(dst, kv + e);
+    }
+    cp_async_wait_all();
     __syncthreads();
     // ---- one warp per (row, q head) pair ----
     for (int p = warp; p < npairs; p += ATT_THREADS / 32) {
@@ -91,21 +137,25 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
       const float* qg = B.q + ((size_t)row * D.Hq + hq) * D_HEAD;
       for (int i = lane; i < D_HEAD; i += 32) qw[i] = qg[i];
       __syncwarp();
-      // scores of keys lane and lane + 32
+      // scores of keys lane and lane + 32 (padded K rows: conflict-free 16-byte reads)
       float sc[2];
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         const int key = lane + 32 * h2;
         float acc = 0.f;
-        const float* kr = Ks + key * KLD;
-#pragma unroll 8
-        for (int j = 0; j < D_HEAD; j += 4) {
-          const float4 q4 = *reinterpret_cast<const float4*>(qw + j);
-          const float4 k4 = *reinterpret_cast<const float4*>(kr + j);
-          acc = fmaf(q4.x, k4.x, acc); acc = fmaf(q4.y, k4.y, acc);
-          acc = fmaf(q4.z, k4.z, acc); acc = fmaf(q4.w, k4.w, acc);
+        const KT* kr = Ks + key * KST;
+#pragma unroll 4
+        for (int j = 0; j < D_HEAD; j += 8) {
+          float kf[8];
+          load8<KT>(kr + j, kf);
+          const float4 qa = *reinterpret_cast<const float4*>(qw + j);
+          const float4 qb = *reinterpret_cast<const float4*>(qw + j + 4);
+          acc = fmaf(qa.x, kf[0], acc); acc = fmaf(qa.y, kf[1], acc);
+          acc = fmaf(qa.z, kf[2], acc); acc = fmaf(qa.w, kf[3], acc);
+          acc = fmaf(qb.x, kf[4], acc); acc = fmaf(qb.y, kf[5], acc);
+          acc = fmaf(qb.z, kf[6], acc); acc = fmaf(qb.w, kf[7], acc);
         }
-        sc[h2] = (k0 + key <= pos && key < nk) ? acc * scale : -INFINITY;
+        sc[h2] = (key < nk && k0 + key <= pos) ? acc * scale : -INFINITY;
       }
       const float m = warp_max(fmaxf(sc[0], sc[1]));
       const float p0 = expf(sc[0] - m), p1 = expf(sc[1] - m);
@@ -116,24 +166,19 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
       // o[j] = sum_key p[key] * V[key][j], keys in order
       const size_t pidx = ((size_t)row * D.Hq + hq) * B.n_chunk_max + c;
       float* og = B.att_o + pidx * D_HEAD;
-      if constexpr (D_HEAD == 128) {
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int key = 0; key < nk; ++key) {
-          const float pk = pw[key];
-          const float4 v4 = *reinterpret_cast<const float4*>(Vs + key * D_HEAD + 4 * lane);
-          o.x = fmaf(pk, v4.x, o.x); o.y = fmaf(pk, v4.y, o.y);
-          o.z = fmaf(pk, v4.z, o.z); o.w = fmaf(pk, v4.w, o.w);
-        }
-        *reinterpret_cast<float4*>(og + 4 * lane) = o;
-      } else {
-        float2 o = make_float2(0.f, 0.f);
-        for (int key = 0; key < nk; ++key) {
-          const float pk = pw[key];
-          const float2 v2 = *reinterpret_cast<const float2*>(Vs + key * D_HEAD + 2 * lane);
-          o.x = fmaf(pk, v2.x, o.x); o.y = fmaf(pk, v2.y, o.y);
-        }
-        *reinterpret_cast<float2*>(og + 2 * lane) = o;
+      constexpr int NV = D_HEAD / 32;               // dims per lane (4 or 2)
+      float o[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) o[i] = 0.f;
+      for (int key = 0; key < nk; ++key) {
+        const float pk = pw[key];
+        float vf[NV];
+        loadv<KT, NV>(Vs + key * D_HEAD + NV * lane, vf);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) o[i] = fmaf(pk, vf[i], o[i]);
       }
+      if constexpr (NV == 4) *reinterpret_cast<float4*>(og + 4 * lane) = make_float4(o[0], o[1], o[2], o[3]);
+      else *reinterpret_cast<float2*>(og + 2 * lane) = make_float2(o[0], o[1]);
       if (lane == 0) {
         B.att_ml[pidx * 2] = m;
         B.att_ml[pidx * 2 + 1] = l;
@@ -188,9 +233,12 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
 }
 
 cudaError_t configure_attn_kernels() {
-  cudaError_t e = allow_dyn_smem(k_attn_part<128>);
-  cudaError_t f = allow_dyn_smem(k_attn_part<64>);
-  return e != cudaSuccess ? e : f;
+  cudaError_t e = cudaSuccess, r;
+#define ALLOW(k) if ((r = allow_dyn_smem(k)) != cudaSuccess) e = r
+  ALLOW((k_attn_part<128, float>)); ALLOW((k_attn_part<128, bf16_t>));
+  ALLOW((k_attn_part<64, float>)); ALLOW((k_attn_part<64, bf16_t>));
+#undef ALLOW
+  return e;
 }
 
 void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
@@ -198,16 +246,17 @@ void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int la
   const int RG = R < 32 ? R : 32;
   const int groups = ((T + R - 1) / R) * ((R + RG - 1) / RG);
   // chunk slots: enough blocks to fill the GPU when few groups are live
-  int CS = (304 + groups * D.Hkv - 1) / (groups * D.Hkv);
+  int CS = (2 * D.n_sm + groups * D.Hkv - 1) / (groups * D.Hkv);
   if (CS < 1) CS = 1;
   if (CS > B.n_chunk_max) CS = B.n_chunk_max;
-  dim3 grid(CS, D.Hkv, groups);
-  const int dh = D.d;
-  const size_t sm = (size_t)(ATT_CHUNK * (dh + 4) + ATT_CHUNK * dh + (ATT_THREADS / 32) * (dh + ATT_CHUNK)) *
-                    sizeof(float);
-  if (dh == 128) launch_k(k_attn_part<128>, grid, dim3(ATT_THREADS), sm, st, D, S, B, layer, T, R, RG, CS);
-  else launch_k(k_attn_part<64>, grid, dim3(ATT_THREADS), sm, st, D, S, B, layer, T, R, RG, CS);
+  const dim3 grid(CS, D.Hkv, groups), blk(ATT_THREADS);
+  if (D.d == 128) {
+    if (D.act_f32) launch_k(k_attn_part<128, float>, grid, blk, AttSmem<128, float>::total, st, D, S, B, layer, T, R, RG, CS);
+    else launch_k(k_attn_part<128, bf16_t>, grid, blk, AttSmem<128, bf16_t>::total, st, D, S, B, layer, T, R, RG, CS);
+  } else {
+    if (D.act_f32) launch_k(k_attn_part<64, float>, grid, blk, AttSmem<64, float>::total, st, D, S, B, layer, T, R, RG, CS);
+    else launch_k(k_attn_part<64, bf16_t>, grid, blk, AttSmem<64, bf16_t>::total, st, D, S, B, layer, T, R, RG, CS);
+  }
 }
-
 
 }  // namespace spec

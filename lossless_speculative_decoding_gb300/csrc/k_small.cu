@@ -1,7 +1,8 @@
 // Small kernels of the verify step: RoPE tables, row assembly + embedding,
 // RMSNorm + router + top-k + token permutation, expert combine, and the
 // acceptance / KV-commit kernel.
-#include "common.cuh"
+#include "gemv.cuh"
+#include "route.cuh"
 #include "kernels.h"
 
 namespace spec {
@@ -82,74 +83,125 @@ void launch_assemble_prefill(const Dims& D, const DevState& S, const StepBuf& B,
 }
 
 // ---------------------------------------------------------------------------
-// FFN input RMSNorm + router + top-k + token permutation. Grid (T rows,
-// ceil(E/16) expert groups): each block normalises its row (u, written once
-// by group 0) and computes the router logits of 16 experts, every warp
-// issuing all loads of its two expert rows at once. The last group block of a
-// row computes that row's softmax over all E experts and its top-k (in
-// (probability desc, id asc) order, used without renormalisation: "Jina AI
-// releases jina-ocr-v1", 64 routed + 2 shared experts, top-6); the last row
-// builds the per-expert pair lists. Pair id = row * NS + slot (slots 0..k-1
-// routed, k..k+S-1 shared). Active list: routed experts with rows, in id
-// order, then the shared experts with every row.
-constexpr int RT_EXPERTS = 16;     // experts per router block
+// FFN input RMSNorm + router + top-k + token permutation. The router
+// probabilities are a softmax over all E experts; the top-k are taken in
+// (probability desc, id asc) order and used without renormalisation ("Jina AI
+// releases jina-ocr-v1", 64 routed + 2 shared experts, top-6). Pair id =
+// row * NS + slot (slots 0..k-1 routed, k..k+S-1 shared). Active list:
+// routed experts with rows, in id order, then the shared experts with every
+// row. The logits come from (row, 16-expert group) blocks; at T <= 8 the
+// expert gate/up kernel then runs the top-k and permutation in each block's
+// prologue, otherwise the last block of a row takes its top-k and the last
+// row builds the permutation. All paths use the same routines in route.cuh,
+// so a row's routing does not depend on T.
+constexpr int RT_EXPERTS = 16;     // experts per router block (multi-block shape)
 constexpr int RT_MAXC = 8;         // 16-byte chunks per lane loaded at once
+constexpr int RT_SMALL_T = 8;      // rows handled by the single-block shape
 
+// u = (x * inv) * gamma of one row, into shared (and global when ug != null).
+__device__ __forceinline__ void router_u(const float* x, float inv, const float* gamma, int h, float* us,
+                                         float* ug) {
+  for (int k = threadIdx.x; k < h; k += blockDim.x) {
+    const float v = (x[k] * inv) * gamma[k];
+    us[k] = v;
+    if (ug) ug[k] = v;
+  }
+}
+
+// Logits of experts e0, e0+1 for nt rows of u (shared, row stride h), by one
+// warp: every lane loads all its chunks of both expert rows at once (up to
+// 32 * RT_MAXC chunks per pass), then for each row accumulates chunk by chunk
+// in increasing order; store(t, ee, logit) receives the warp sums.
+template <class RT, class Store>
+__device__ __forceinline__ void router_logits2(const RT* Wr, int E, int h, int e0, const float* us, int nt,
+                                               Store store) {
+  constexpr int EP = Elt<RT>::per16;
+  const int lane = threadIdx.x & 31;
+  const int nch = h / EP;
+  // h <= 32 * RT_MAXC * EP is checked at init, so one pass covers the row
+  uint4 wv[2][RT_MAXC];
+#pragma unroll
+  for (int ee = 0; ee < 2; ++ee)
+#pragma unroll
+    for (int m = 0; m < RT_MAXC; ++m) {
+      const int c = lane + 32 * m;
+      wv[ee][m] = (e0 + ee < E && c < nch) ? ld_stream(Wr + (size_t)(e0 + ee) * h + (size_t)c * EP)
+                                            : make_uint4(0, 0, 0, 0);
+    }
+  for (int t = 0; t < nt; ++t) {
+    float a0 = 0.f, a1 = 0.f;
+    const float* ut = us + (size_t)t * h;
+#pragma unroll
+    for (int m = 0; m < RT_MAXC; ++m) {
+      const int c = lane + 32 * m;
+      if (c < nch) {
+        float w0[EP], w1[EP];
+        unpack<RT>(wv[0][m], w0);
+        unpack<RT>(wv[1][m], w1);
+#pragma unroll
+        for (int i = 0; i < EP; ++i) {
+          const float x = ut[c * EP + i];
+          a0 = fmaf(w0[i], x, a0);
+          a1 = fmaf(w1[i], x, a1);
+        }
+      }
+    }
+    a0 = warp_sum(a0);
+    a1 = warp_sum(a1);
+    store(t, 0, a0);
+    store(t, 1, a1);
+  }
+}
+
+// Logits-only shape (T <= 8): grid (T rows, ceil(E/16) expert groups); each
+// block normalises its row (u, written once by group 0) and writes the router
+// logits of 16 experts. The expert gate/up kernel then takes the softmax,
+// top-k and permutation in its prologue.
+template <class RT>
+__global__ void __launch_bounds__(256) k_router_logits(Dims D, StepBuf B, const float* __restrict__ gamma,
+                                                       const RT* __restrict__ Wr, int T, const float* xres) {
+  extern __shared__ __align__(16) float sm[];
+  float* us = sm;                 // [h]
+  __shared__ float inv[1];
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x, grp = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
+  const float* x = xres + (size_t)row * D.h;
+  if (warp == 0) row_inv_rms(x, 1, D.h, D.eps, inv);
+  __syncthreads();
+  router_u(x, inv[0], gamma, D.h, us, grp == 0 ? B.u + (size_t)row * D.h : nullptr);
+  __syncthreads();
+  if (D.E > 0) {
+    const int e0 = grp * RT_EXPERTS + warp * 2;
+    router_logits2<RT>(Wr, D.E, D.h, e0, us, 1, [&](int, int ee, float v) {
+      if ((threadIdx.x & 31) == 0 && e0 + ee < D.E) B.rlogit[(size_t)row * D.E + e0 + ee] = v;
+    });
+  }
+}
+
+// Multi-block shape: grid (T rows, ceil(E/16) expert groups).
 template <class RT>
 __global__ void __launch_bounds__(256) k_router(Dims D, StepBuf B, const float* __restrict__ gamma,
-                                                const RT* __restrict__ Wr, int T) {
+                                                const RT* __restrict__ Wr, int T, const float* xres) {
   extern __shared__ __align__(16) float sm[];
-  float* u = sm;                 // [h]
-  __shared__ float red[32];
+  float* us = sm;                 // [h]
+  __shared__ float inv[1];
   __shared__ int s_last;
   pdl_wait();
   pdl_trigger();
   const int row = blockIdx.x, grp = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float* x = B.x + (size_t)row * D.h;
-  float ss = 0.f;
-  for (int k = threadIdx.x; k < D.h; k += blockDim.x) ss = fmaf(x[k], x[k], ss);
-  ss = block_sum(ss, red);
-  const float inv = 1.0f / sqrtf(ss / (float)D.h + D.eps);
-  for (int k = threadIdx.x; k < D.h; k += blockDim.x) {
-    const float v = (x[k] * inv) * gamma[k];
-    u[k] = v;
-    if (grp == 0) B.u[(size_t)row * D.h + k] = v;
-  }
+  const int warp = threadIdx.x >> 5;
+  const float* x = xres + (size_t)row * D.h;
+  if (warp == 0) row_inv_rms(x, 1, D.h, D.eps, inv);
+  __syncthreads();
+  router_u(x, inv[0], gamma, D.h, us, grp == 0 ? B.u + (size_t)row * D.h : nullptr);
   __syncthreads();
   if (D.E > 0) {
-    constexpr int EP = Elt<RT>::per16;
-    const int nch = D.h / EP;
     const int e0 = grp * RT_EXPERTS + warp * 2;
-    float acc[2] = {0.f, 0.f};
-    for (int cb = lane; cb < nch; cb += 32 * RT_MAXC) {
-      uint4 wv[2][RT_MAXC];
-#pragma unroll
-      for (int ee = 0; ee < 2; ++ee)
-#pragma unroll
-        for (int m = 0; m < RT_MAXC; ++m) {
-          const int c = cb + 32 * m;
-          wv[ee][m] = (e0 + ee < D.E && c < nch) ? ld_stream(Wr + (size_t)(e0 + ee) * D.h + (size_t)c * EP)
-                                                  : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-      for (int ee = 0; ee < 2; ++ee)
-#pragma unroll
-        for (int m = 0; m < RT_MAXC; ++m) {
-          const int c = cb + 32 * m;
-          if (c < nch) {
-            float w[EP];
-            unpack<RT>(wv[ee][m], w);
-#pragma unroll
-            for (int i = 0; i < EP; ++i) acc[ee] = fmaf(w[i], u[c * EP + i], acc[ee]);
-          }
-        }
-    }
-#pragma unroll
-    for (int ee = 0; ee < 2; ++ee) {
-      const float v = warp_sum(acc[ee]);
-      if (lane == 0 && e0 + ee < D.E) B.rlogit[(size_t)row * D.E + e0 + ee] = v;
-    }
+    router_logits2<RT>(Wr, D.E, D.h, e0, us, 1, [&](int, int ee, float v) {
+      if ((threadIdx.x & 31) == 0 && e0 + ee < D.E) B.rlogit[(size_t)row * D.E + e0 + ee] = v;
+    });
   }
   // ---- the last expert-group block of this row: softmax + top-k ----
   __syncthreads();
@@ -161,49 +213,10 @@ __global__ void __launch_bounds__(256) k_router(Dims D, StepBuf B, const float* 
   if (!s_last) return;
   __threadfence();
   if (D.E > 0 && warp == 0) {
-    // softmax over E <= 256 logits, lane l owning experts l, l+32, ...
-    constexpr int MAXE = 8;
-    float v[MAXE];
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < MAXE; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = e < D.E ? __ldcg(B.rlogit + (size_t)row * D.E + e) : -INFINITY;
-      m = fmaxf(m, v[i]);
-    }
-    m = warp_max(m);
-    float z = 0.f;
-#pragma unroll
-    for (int i = 0; i < MAXE; ++i) {
-      v[i] = (lane + 32 * i < D.E) ? expf(v[i] - m) : 0.f;
-      z += v[i];
-    }
-    z = warp_sum(z);
-#pragma unroll
-    for (int i = 0; i < MAXE; ++i) v[i] = (lane + 32 * i < D.E) ? v[i] / z : -1.f;
-    // top-k: k rounds of a warp argmax, (probability desc, id asc)
-    for (int r = 0; r < D.k; ++r) {
-      float bv = -1.f;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < MAXE; ++i) {
-        const int e = lane + 32 * i;
-        if (v[i] > bv) { bv = v[i]; bi = e; }      // increasing e: ties keep the lower id
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-      }
-      if (lane == 0) {
-        B.ids[row * D.k + r] = bi;
-        B.wts[row * D.k + r] = bv;
-      }
-#pragma unroll
-      for (int i = 0; i < MAXE; ++i)
-        if (lane + 32 * i == bi) v[i] = -1.f;        // taken
-    }
+    float* lgs = us;                              // reuse: this row's logits via L2
+    for (int e = threadIdx.x; e < D.E; e += 32) lgs[e] = __ldcg(B.rlogit + (size_t)row * D.E + e);
+    __syncwarp();
+    router_topk(lgs, D.E, D.k, B.ids + row * D.k, B.wts + row * D.k);
   }
   if (threadIdx.x == 0) B.cnt_row[row] = 0;
   // ---- the last row builds the permutation ----
@@ -215,65 +228,39 @@ __global__ void __launch_bounds__(256) k_router(Dims D, StepBuf B, const float* 
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const int nk = T * D.k;
-  int* s_ids = reinterpret_cast<int*>(sm);        // reuse: [nk] ids, [E] counts, [E] offsets
-  int* cnt = s_ids + nk;
-  int* offs = cnt + (D.E > 0 ? D.E : 1);
-  for (int j = threadIdx.x; j < nk; j += blockDim.x) s_ids[j] = __ldcg(B.ids + j);
+  int* s_ids = reinterpret_cast<int*>(sm);
+  for (int j = threadIdx.x; j < T * D.k; j += blockDim.x) s_ids[j] = __ldcg(B.ids + j);
   __syncthreads();
-  for (int e = threadIdx.x; e < D.E; e += blockDim.x) {
-    int c = 0;
-    for (int j = 0; j < nk; ++j) c += (s_ids[j] == e);
-    cnt[e] = c;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int o = 0, na = 0;
-    for (int e = 0; e < D.E; ++e) {
-      offs[e] = o;
-      if (cnt[e] > 0) {
-        B.act_expert[na] = e; B.act_off[na] = o; B.act_cnt[na] = cnt[e];
-        ++na;
-      }
-      o += cnt[e];
-    }
-    for (int s = 0; s < D.S; ++s) {
-      B.act_expert[na] = D.E + s; B.act_off[na] = nk + s * T; B.act_cnt[na] = T;
-      ++na;
-    }
-    *B.n_active = na;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < D.E; e += blockDim.x) {
-    if (cnt[e] == 0) continue;
-    int c = offs[e];
-    for (int j = 0; j < nk; ++j)
-      if (s_ids[j] == e) B.perm[c++] = (j / D.k) * D.NS + (j % D.k);
-  }
-  for (int i = threadIdx.x; i < D.S * T; i += blockDim.x) {
-    const int s = i / T, r = i % T;
-    B.perm[nk + i] = r * D.NS + D.k + s;
-  }
+  router_permute(D, T, s_ids, s_ids + T * D.k, RouteOut{B.act_expert, B.act_off, B.act_cnt, B.n_active, B.perm});
   if (threadIdx.x == 0) *B.counter = 0;
 }
 
 cudaError_t configure_small_kernels() {
-  cudaError_t e = allow_dyn_smem(k_router<float>);
-  cudaError_t f = allow_dyn_smem(k_router<bf16_t>);
-  return e != cudaSuccess ? e : f;
+  cudaError_t e = cudaSuccess, r;
+#define ALLOW(k) if ((r = allow_dyn_smem(k)) != cudaSuccess) e = r
+  ALLOW(k_router<float>); ALLOW(k_router<bf16_t>);
+  ALLOW(k_router_logits<float>); ALLOW(k_router_logits<bf16_t>);
+#undef ALLOW
+  return e;
 }
 
-void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
+void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, const float* xres, cudaStream_t st) {
   const int E1 = D.E > 0 ? D.E : 1;
-  const size_t words = (size_t)D.h > (size_t)T * D.k + 2 * E1 ? (size_t)D.h : (size_t)T * D.k + 2 * E1;
-  const size_t sm = words * sizeof(float);
+  const size_t perm_words = (size_t)T * D.k + 2 * E1;
   const dim3 grid(T, D.E > 0 ? (D.E + RT_EXPERTS - 1) / RT_EXPERTS : 1);
-  if (D.act_f32) {
-    launch_k(k_router<float>, grid, dim3(256), sm, st, D, B, W.ffn_norm, (const float*)W.w_router, T);
-  } else {
-    launch_k(k_router<bf16_t>, grid, dim3(256), sm, st, D, B, W.ffn_norm, (const bf16_t*)W.w_router, T);
+  if (T <= RT_SMALL_T) {
+    const size_t sm = (size_t)D.h * sizeof(float);
+    if (D.act_f32) launch_k(k_router_logits<float>, grid, dim3(256), sm, st, D, B, W.ffn_norm, (const float*)W.w_router, T, xres);
+    else launch_k(k_router_logits<bf16_t>, grid, dim3(256), sm, st, D, B, W.ffn_norm, (const bf16_t*)W.w_router, T, xres);
+    return;
   }
+  const size_t words = (size_t)D.h > perm_words ? (size_t)D.h : perm_words;
+  const size_t sm = words * sizeof(float);
+  if (D.act_f32) launch_k(k_router<float>, grid, dim3(256), sm, st, D, B, W.ffn_norm, (const float*)W.w_router, T, xres);
+  else launch_k(k_router<bf16_t>, grid, dim3(256), sm, st, D, B, W.ffn_norm, (const bf16_t*)W.w_router, T, xres);
 }
+
+bool route_in_gateup(int T) { return T <= RT_SMALL_T; }
 
 // ---------------------------------------------------------------------------
 // Acceptance + commit as its own kernel (one thread per sequence); the
@@ -308,11 +295,12 @@ void launch_stage_dev(const StepBuf& B, int n_seq, int K, const int* seq_ids, co
   k_stage_dev<<<1, 256, 0, st>>>(B, n_seq, K, seq_ids, drafts, n_draft, out_acc, out_bonus);
 }
 
-int launches_per_step(const Dims& D) {
+int launches_per_step(const Dims& D, int T) {
   // assemble + per layer (qkv + RoPE + KV write, split-KV attention + merge,
-  // O-proj + residual, router + top-k + permute, gate/up + SwiGLU, down +
+  // O-proj + residual, router + top-k + permute, gate/up + SwiGLU, down,
   // combine) + LM head with argmax and accept/commit
-  return 1 + D.L * 6 + 1;
+  (void)T;
+  return 1 + D.L * 7 + 1;
 }
 
 }  // namespace spec

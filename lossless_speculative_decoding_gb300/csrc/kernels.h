@@ -85,30 +85,34 @@ void launch_assemble_verify(const Dims& D, const DevState& S, const StepBuf& B, 
 void launch_assemble_prefill(const Dims& D, const DevState& S, const StepBuf& B, const void* tok_embed,
                              const void* vis, int seq, int pos0, int T, cudaStream_t st);
 void launch_qkv(const Dims& D, const DevState& S, const StepBuf& B, const LayerW& W, int layer, int T,
-                cudaStream_t st);
+                const float* x, cudaStream_t st);
 void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
                       cudaStream_t st);
-void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
-void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
+void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, float* xres, cudaStream_t st);
+void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, const float* xres, cudaStream_t st);
 void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
+// At small T the router kernel writes only logits and gate/up routes in its prologue.
+bool route_in_gateup(int T);
 void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
+// In-place expert combine of the residual x.
+void launch_combine(const Dims& D, const StepBuf& B, float* x, int T, cudaStream_t st);
 void launch_lmhead(const Dims& D, const StepBuf& B, const void* lm_head, const float* final_norm,
                    const float* x, int T, float* logits_dbg, bool fuse_argmax, cudaStream_t st);
 // Streaming LM head + argmax for the verify step / prefill; with commit, its
 // last block also accepts and commits the n_seq sequences (K drafts each).
 void launch_lmhead_step(const Dims& D, const DevState& S, const StepBuf& B, const void* lm_head,
-                        const float* final_norm, const float* x, int T, float* logits_dbg, bool commit, int n_seq,
-                        int K, cudaStream_t st);
+                        const float* final_norm, const float* x, int T, float* logits_dbg, bool commit,
+                        int n_seq, int K, cudaStream_t st);
 int lmhead_step_warps(const Dims& D);
 void launch_argmax(const StepBuf& B, int T, cudaStream_t st);
 
 // Kernel classes (for profiling); order matches spec_kernel_class_name().
-enum KClass { KC_ASSEMBLE, KC_QKV, KC_ATTN, KC_OPROJ, KC_ROUTER, KC_GATEUP, KC_DOWN, KC_LMHEAD, KC_COMMIT,
-              KC_STAGE, KC_COUNT };
+enum KClass { KC_ASSEMBLE, KC_QKV, KC_ATTN, KC_OPROJ, KC_ROUTER, KC_GATEUP, KC_DOWN, KC_COMBINE, KC_LMHEAD,
+              KC_COMMIT, KC_STAGE, KC_COUNT };
 void launch_commit(const Dims& D, const DevState& S, const StepBuf& B, int n_seq, int K, cudaStream_t st);
 void launch_stage_dev(const StepBuf& B, int n_seq, int K, const int* seq_ids, const int* drafts,
                       const int* n_draft, int* out_acc, int* out_bonus, cudaStream_t st);
-int launches_per_step(const Dims& D);
+int launches_per_step(const Dims& D, int T);
 // Record `msg` as the calling thread's last error (spec_last_error) and return code.
 int set_last_error(int code, const char* msg);
 // Programmatic dependent launch is used for every step kernel unless this

@@ -81,6 +81,8 @@ int check_config(const spec_config& c) {
   if (c.n_experts > 0 && (c.top_k < 1 || c.top_k > c.n_experts || c.top_k > 16))
     return fail(SPEC_ERR_ARG, "top_k must be in [1, min(n_experts, 16)]");
   if (c.n_experts > 256) return fail(SPEC_ERR_UNSUPPORTED, "at most 256 routed experts");
+  if (c.n_experts > 0 && c.hidden * elt_bytes(c.wdtype == SPEC_F32 ? SPEC_F32 : SPEC_BF16) > 32 * 8 * 16)
+    return fail(SPEC_ERR_UNSUPPORTED, "router rows above 4 KiB");
   if (c.n_experts == 0 && (c.n_shared != 1 || c.top_k != 0))
     return fail(SPEC_ERR_ARG, "a dense FFN is one shared expert with top_k = 0");
   if (c.n_experts + c.n_shared < 1) return fail(SPEC_ERR_ARG, "no FFN experts");
@@ -208,26 +210,30 @@ struct spec_model {
     }
   }
 
-  // Enqueue one forward over T rows already assembled in B (row meta + x).
-  void enqueue_layers(int T, int R_rows, Prof* p = nullptr) {
+  // Enqueue one forward over T rows already assembled in B (row meta + x);
+  // returns the residual buffer holding the final rows.
+  const float* enqueue_layers(int T, int R_rows, Prof* p = nullptr) {
+    float* cur = B.x;
     for (int l = 0; l < D.L; ++l) {
       const LayerW& W = layers[l];
-      run_k(p, KC_QKV, [&] { launch_qkv(D, S, B, W, l, T, stream); });
+      run_k(p, KC_QKV, [&] { launch_qkv(D, S, B, W, l, T, cur, stream); });
       run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, stream); });
-      run_k(p, KC_OPROJ, [&] { launch_oproj(D, B, W, T, stream); });
-      run_k(p, KC_ROUTER, [&] { launch_router(D, B, W, T, stream); });
-      if (p) cudaMemcpyAsync(p->act + p->nact++, B.n_active, 4, cudaMemcpyDeviceToHost, stream);
+      run_k(p, KC_OPROJ, [&] { launch_oproj(D, B, W, T, cur, stream); });
+      run_k(p, KC_ROUTER, [&] { launch_router(D, B, W, T, cur, stream); });
       run_k(p, KC_GATEUP, [&] { launch_gateup(D, B, W, T, stream); });
+      if (p) cudaMemcpyAsync(p->act + p->nact++, B.n_active, 4, cudaMemcpyDeviceToHost, stream);
       run_k(p, KC_DOWN, [&] { launch_down(D, B, W, T, stream); });
+      run_k(p, KC_COMBINE, [&] { launch_combine(D, B, cur, T, stream); });
     }
+    return cur;
   }
 
   void enqueue_verify(int n_seq, float* logits_dbg, bool commit, Prof* p = nullptr) {
     const int T = n_seq * R;
     run_k(p, KC_ASSEMBLE, [&] { launch_assemble_verify(D, S, B, tok_embed, n_seq, K, stream); });
-    enqueue_layers(T, R, p);
+    const float* xf = enqueue_layers(T, R, p);
     run_k(p, KC_LMHEAD, [&] {
-      launch_lmhead_step(D, S, B, lm_head, final_norm, B.x, T, logits_dbg, commit, n_seq, K, stream);
+      launch_lmhead_step(D, S, B, lm_head, final_norm, xf, T, logits_dbg, commit, n_seq, K, stream);
     });
   }
 
@@ -439,10 +445,10 @@ static int run_prefill_rows(spec_model* m, int slot, const std::vector<int32_t>&
     std::memcpy(m->pin_in, src.data() + c0, T * sizeof(int32_t));
     CU(cudaMemcpyAsync(m->B.row_src, m->pin_in, T * sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
     launch_assemble_prefill(m->D, m->S, m->B, m->tok_embed, vis, slot, start + c0, T, m->stream);
-    m->enqueue_layers(T, T);
+    const float* xf = m->enqueue_layers(T, T);
     if (c0 + T == n && out_tok) {
-      launch_lmhead_step(m->D, m->S, m->B, m->lm_head, m->final_norm, m->B.x + (size_t)(T - 1) * m->D.h, 1,
-                         nullptr, false, 0, 0, m->stream);
+      launch_lmhead_step(m->D, m->S, m->B, m->lm_head, m->final_norm, xf + (size_t)(T - 1) * m->D.h, 1, nullptr,
+                         false, 0, 0, m->stream);
       CU(cudaMemcpyAsync(m->pin_out, m->B.g, sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
     }
     // the staging buffer is reused by the next chunk
@@ -678,7 +684,7 @@ int spec_profile_steps_dev(spec_model* m, int n_seq, const int32_t* seq_ids_dev,
   if (!m || n_seq < 1 || n_seq > m->cfg.max_batch || n_steps < 1 || !out || n_out < 1 || !seq_ids_dev ||
       !n_draft_dev || (m->K > 0 && !drafts_dev))
     return fail(SPEC_ERR_ARG, "bad profile arguments");
-  const int per_step = launches_per_step(m->D) + 1;
+  const int per_step = launches_per_step(m->D, n_seq * m->R) + 1;
   spec_model::Prof p;
   p.ev.resize(2 * per_step);
   p.cls.resize(per_step);
@@ -729,8 +735,8 @@ int spec_profile_steps_dev(spec_model* m, int n_seq, const int32_t* seq_ids_dev,
 
 const char* spec_kernel_class_name(int cls) {
   static const char* names[KC_COUNT] = {"assemble", "qkv_rope_kvwrite", "attn_splitkv_merge", "oproj_residual",
-                                        "router_topk_permute", "expert_gateup_swiglu", "expert_down_combine",
-                                        "lmhead_argmax", "accept_commit", "stage_inputs"};
+                                        "router_topk_permute", "expert_gateup_swiglu", "expert_down",
+                                        "expert_combine", "lmhead_argmax_commit", "accept_commit", "stage_inputs"};
   return (cls >= 0 && cls < KC_COUNT) ? names[cls] : "";
 }
 
@@ -828,7 +834,7 @@ int spec_free_pages(spec_model* m) {
 
 int spec_step_launches(spec_model* m, int n_seq) {
   if (!m || n_seq < 1) return fail(SPEC_ERR_ARG, "bad arguments");
-  return launches_per_step(m->D);
+  return launches_per_step(m->D, n_seq * m->R);
 }
 
 // ---- host-only allocator entry points --------------------------------------
