@@ -13,7 +13,7 @@ namespace spec {
 constexpr int WARP = 32;
 
 // Error bits a kernel may raise (read back by the host after a step).
-enum : int { DERR_PAGE = 1, DERR_TOKEN = 2, DERR_POS = 4 };
+enum : int { DERR_PAGE = 1, DERR_TOKEN = 2, DERR_POS = 4, DERR_TIMEOUT = 8 };
 
 // ---- storage element types --------------------------------------------------
 struct bf16_t { uint16_t v; };

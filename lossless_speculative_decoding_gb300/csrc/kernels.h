@@ -1,5 +1,6 @@
 // Internal launch interface of the verify-step kernels (not part of the C ABI).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -105,6 +106,43 @@ void launch_lmhead_step(const Dims& D, const DevState& S, const StepBuf& B, cons
                         int n_seq, int K, cudaStream_t st);
 int lmhead_step_warps(const Dims& D);
 void launch_argmax(const StepBuf& B, int T, cudaStream_t st);
+
+// ---- tensor-core GEMM (k_tc.cu) ---------------------------------------------
+enum TcEpi { TC_STORE = 0, TC_SWIGLU = 1, TC_ADD = 2, TC_ARGMAX = 3, TC_SCATTER = 4 };
+
+struct TcParams {
+  int K;                  // reduction length (multiple of 64)
+  int Mg;                 // weight rows per group (multiple of 128)
+  int N;                  // activation rows when not grouped
+  int ldo;                // output row stride (elements)
+  int epi;                // TcEpi
+  int row0;               // added to the weight row in argmax candidates
+  // groups (nullptr: group = blockIdx.y, rows [0, N))
+  const int* g_expert;
+  const int* g_off;
+  const int* g_cnt;
+  const int* g_n;
+  float* out_f32;         // STORE [off+n][col] / ADD (+=) / SCATTER [perm[off+n]][col]
+  uint16_t* out_bf16;     // SWIGLU [off+n][col]
+  const int* perm;
+  const float* scale;     // per weight row (nullable)
+  const float* scale2;    // per weight row of the second operand (SWIGLU up)
+  float* am_val;          // ARGMAX candidates [off+n][am_ld]
+  int* am_idx;
+  int am_ld;
+  int* err;
+};
+
+struct TcMaps {
+  CUtensorMap a, a2, b;
+  int dual;
+};
+
+// 2D bf16 tensor map: rows of `inner` elements, box 64 x box_rows, 128-byte
+// swizzle. Returns 0 on success.
+int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+void launch_tc_gemm(const TcMaps& maps, const TcParams& P, int m_tiles, int groups, int n_tiles, cudaStream_t st);
+cudaError_t configure_tc_kernels();
 
 // Kernel classes (for profiling); order matches spec_kernel_class_name().
 enum KClass { KC_ASSEMBLE, KC_QKV, KC_ATTN, KC_OPROJ, KC_ROUTER, KC_GATEUP, KC_DOWN, KC_COMBINE, KC_LMHEAD,
