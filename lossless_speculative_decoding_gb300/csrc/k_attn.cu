@@ -218,7 +218,18 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
         const float4 v = __ldcg(reinterpret_cast<const float4*>(B.att_o + (base + c) * D_HEAD) + lane);
         o.x = fmaf(v.x, w, o.x); o.y = fmaf(v.y, w, o.y); o.z = fmaf(v.z, w, o.z); o.w = fmaf(v.w, w, o.w);
       }
-      reinterpret_cast<float4*>(out)[lane] = make_float4(o.x / L, o.y / L, o.z / L, o.w / L);
+      const float4 r = make_float4(o.x / L, o.y / L, o.z / L, o.w / L);
+      reinterpret_cast<float4*>(out)[lane] = r;
+      if (B.o_bf16 != nullptr) {
+        const size_t e = (size_t)row * D.Hq * D_HEAD + (size_t)hq * D_HEAD + 4 * lane;
+        const float rv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint16_t hi = f_to_bf16(rv[i]);
+          B.o_bf16[e + i] = hi;
+          B.o_lo[e + i] = f_to_bf16(rv[i] - bf16_to_f(hi));
+        }
+      }
     } else {
       float2 o = make_float2(0.f, 0.f);
       for (int c = 0; c < nc; ++c) {
@@ -226,7 +237,18 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
         const float2 v = __ldcg(reinterpret_cast<const float2*>(B.att_o + (base + c) * D_HEAD) + lane);
         o.x = fmaf(v.x, w, o.x); o.y = fmaf(v.y, w, o.y);
       }
-      reinterpret_cast<float2*>(out)[lane] = make_float2(o.x / L, o.y / L);
+      const float2 r = make_float2(o.x / L, o.y / L);
+      reinterpret_cast<float2*>(out)[lane] = r;
+      if (B.o_bf16 != nullptr) {
+        const size_t e = (size_t)row * D.Hq * D_HEAD + (size_t)hq * D_HEAD + 2 * lane;
+        const float rv[2] = {r.x, r.y};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint16_t hi = f_to_bf16(rv[i]);
+          B.o_bf16[e + i] = hi;
+          B.o_lo[e + i] = f_to_bf16(rv[i] - bf16_to_f(hi));
+        }
+      }
     }
   }
   if (threadIdx.x == 0) *ctr = 0;

@@ -244,11 +244,12 @@ cudaError_t configure_small_kernels() {
   return e;
 }
 
-void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, const float* xres, cudaStream_t st) {
+void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, const float* xres, bool full,
+                   cudaStream_t st) {
   const int E1 = D.E > 0 ? D.E : 1;
   const size_t perm_words = (size_t)T * D.k + 2 * E1;
   const dim3 grid(T, D.E > 0 ? (D.E + RT_EXPERTS - 1) / RT_EXPERTS : 1);
-  if (T <= RT_SMALL_T) {
+  if (!full && T <= RT_SMALL_T) {
     const size_t sm = (size_t)D.h * sizeof(float);
     if (D.act_f32) launch_k(k_router_logits<float>, grid, dim3(256), sm, st, D, B, W.ffn_norm, (const float*)W.w_router, T, xres);
     else launch_k(k_router_logits<bf16_t>, grid, dim3(256), sm, st, D, B, W.ffn_norm, (const bf16_t*)W.w_router, T, xres);

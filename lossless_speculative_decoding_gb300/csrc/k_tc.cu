@@ -1,9 +1,12 @@
 // Tensor-core (tcgen05) GEMM for verify steps and prefill at T >= 16 rows.
 //
 // D[m, n] = sum_k W[m, k] * X[n, k]: weights W (bf16, row-major = K-major)
-// fill the MMA's M = 128 rows, activation rows X (bf16, K-major) its N <= 256
-// columns, so a CTA streams one 128-row weight tile once for all of its
-// tokens. Tiles of 64 K-elements (one 128-byte swizzle row) are brought into
+// fill the MMA's M = 128 rows, activation rows X its N <= 128 columns, so a
+// CTA streams one 128-row weight tile once for all of its tokens. The
+// activations are given as two bf16 operands, X = X_hi + X_lo (about 16
+// mantissa bits), and both are multiplied into the same fp32 accumulator, so
+// the result keeps near-fp32 activation precision while the weights stay
+// exact bf16. Tiles of 64 K-elements (one 128-byte swizzle row) are brought into
 // shared memory by TMA (cp.async.bulk.tensor, 128-byte swizzle) through a
 // multi-stage mbarrier pipeline; one thread issues tcgen05.mma into a TMEM
 // accumulator (fp32, lane = weight row, column = token); four warps read it
@@ -25,13 +28,13 @@ namespace spec {
 constexpr int TC_BM = 128;            // weight rows per CTA (MMA M)
 constexpr int TC_BK = 64;             // K elements per stage (128 bytes of bf16)
 constexpr int TC_NSUB = 32;           // activation rows per TMA box
-constexpr int TC_MAXN = 256;          // columns per CTA
+constexpr int TC_MAXN = 128;          // columns per CTA
 constexpr uint32_t TC_WAIT_LIMIT = 1u << 20;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;        // 16 KB
-constexpr int TC_B_BYTES = TC_MAXN * TC_BK * 2;      // 32 KB
+constexpr int TC_B_BYTES = TC_MAXN * TC_BK * 2;      // 16 KB (hi) + 16 KB (lo)
 
 __host__ __device__ constexpr int tc_stages(int dual) { return dual ? 3 : 4; }
-__host__ __device__ constexpr int tc_stage_bytes(int dual) { return TC_A_BYTES * (1 + dual) + TC_B_BYTES; }
+__host__ __device__ constexpr int tc_stage_bytes(int dual) { return TC_A_BYTES * (1 + dual) + 2 * TC_B_BYTES; }
 __host__ __device__ constexpr int tc_smem_bytes(int dual) { return tc_stages(dual) * tc_stage_bytes(dual) + 1024 + 256; }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -84,7 +87,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 template <int DUAL>
 __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUtensorMap mapA,
                                                      const __grid_constant__ CUtensorMap mapA2,
-                                                     const __grid_constant__ CUtensorMap mapB, TcParams P) {
+                                                     const __grid_constant__ CUtensorMap mapB,
+                                                     const __grid_constant__ CUtensorMap mapBlo, TcParams P) {
   constexpr int STAGES = tc_stages(DUAL);
   constexpr int SB = tc_stage_bytes(DUAL);
   extern __shared__ unsigned char smem_raw[];
@@ -105,10 +109,10 @@ __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUte
   if (n0 >= cnt) return;
   const int nrows = min(TC_MAXN, cnt - n0);
   const int nsub = (nrows + TC_NSUB - 1) / TC_NSUB;
-  const int N = nsub * TC_NSUB;                       // MMA N: multiple of 32, <= 256
+  const int N = nsub * TC_NSUB;                       // MMA N: multiple of 32, <= 128
   const int KT = P.K / TC_BK;
   const int wrow = grp * P.Mg + mt * TC_BM;           // first weight row of the tile
-  constexpr uint32_t NCOL = DUAL ? 512 : 256;         // TMEM columns
+  constexpr uint32_t NCOL = DUAL ? 2 * TC_MAXN : TC_MAXN;   // TMEM columns
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2 * STAGES + 1; ++i)
@@ -128,7 +132,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUte
 
   if (warp == 0 && lane == 0) {
     // ---- TMA producer ----
-    const uint32_t bytes = TC_A_BYTES * (1 + DUAL) + nsub * TC_NSUB * TC_BK * 2;
+    const uint32_t bytes = TC_A_BYTES * (1 + DUAL) + (P.split ? 2 : 1) * nsub * TC_NSUB * TC_BK * 2;
     for (int kt = 0; kt < KT; ++kt) {
       const int s = kt % STAGES;
       if (kt >= STAGES && !mbar_wait(smem_u32(bars + STAGES + s), ((kt / STAGES) - 1) & 1)) {
@@ -142,8 +146,12 @@ __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUte
       tma_2d(smem_u32(st), &mapA, kt * TC_BK, wrow, full);
       if (DUAL) tma_2d(smem_u32(st + TC_A_BYTES), &mapA2, kt * TC_BK, wrow, full);
       unsigned char* bt = st + TC_A_BYTES * (1 + DUAL);
-      for (int j = 0; j < nsub; ++j)
+      for (int j = 0; j < nsub; ++j) {
         tma_2d(smem_u32(bt + j * TC_NSUB * TC_BK * 2), &mapB, kt * TC_BK, off + n0 + j * TC_NSUB, full);
+        if (P.split)
+          tma_2d(smem_u32(bt + TC_B_BYTES + j * TC_NSUB * TC_BK * 2), &mapBlo, kt * TC_BK, off + n0 + j * TC_NSUB,
+                 full);
+      }
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
@@ -162,18 +170,22 @@ __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUte
       const uint32_t b0 = a0 + TC_A_BYTES * (1 + DUAL);
 #pragma unroll
       for (int k = 0; k < TC_BK / 16; ++k) {
-        const uint64_t ad = sw128_desc(a0 + k * 32), bd = sw128_desc(b0 + k * 32);
-        const uint32_t acc = (kt | k) != 0;
-        asm volatile(
-            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-            " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-            ::"r"(tmem), "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
-        if (DUAL) {
-          const uint64_t ad2 = sw128_desc(a0 + TC_A_BYTES + k * 32);
+        // hi then (optionally) lo activations into the same accumulator
+        for (int part = 0; part < (P.split ? 2 : 1); ++part) {
+          const uint64_t bd = sw128_desc(b0 + part * TC_B_BYTES + k * 32);
+          const uint32_t acc = (kt | k | part) != 0;
+          const uint64_t ad = sw128_desc(a0 + k * 32);
           asm volatile(
               "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
               " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-              ::"r"(tmem + (uint32_t)TC_MAXN), "l"(ad2), "l"(bd), "r"(idesc), "r"(acc));
+              ::"r"(tmem), "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
+          if (DUAL) {
+            const uint64_t ad2 = sw128_desc(a0 + TC_A_BYTES + k * 32);
+            asm volatile(
+                "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+                ::"r"(tmem + (uint32_t)TC_MAXN), "l"(ad2), "l"(bd), "r"(idesc), "r"(acc));
+          }
         }
       }
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -252,7 +264,10 @@ __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUte
       } else if (P.epi == TC_SCATTER) {
         P.out_f32[(size_t)P.perm[r] * P.ldo + col] = val;
       } else if (DUAL && P.epi == TC_SWIGLU) {
-        P.out_bf16[r * P.ldo + col] = f_to_bf16(silu(val) * (u2[j] * sc2));
+        const float hv = silu(val) * (u2[j] * sc2);
+        const uint16_t hi = f_to_bf16(hv);
+        P.out_bf16[r * P.ldo + col] = hi;
+        if (P.out_bf16_lo) P.out_bf16_lo[r * P.ldo + col] = f_to_bf16(hv - bf16_to_f(hi));
       }
     }
   }
@@ -294,10 +309,11 @@ int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t row
 }  // namespace spec
 
 // ---------------------------------------------------------------------------
-// Kernel-level entry point (tests and tools): out[n][m] = sum_k A[m][k] B[n][k]
-// (dual = 0) or out_bf16[n][m] = silu(A[m]·B[n]) * (A2[m]·B[n]) (dual = 1).
-extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const void* b_dev, int M, int N, int K,
-                                 int dual, void* out_dev, int* err_dev, uintptr_t cuda_stream) {
+// Kernel-level entry point (tests and tools): with X = B (+ B_lo when given),
+// out[n][m] = sum_k A[m][k] X[n][k] (dual = 0) or
+// out_bf16[n][m] = silu(A[m]·X[n]) * (A2[m]·X[n]) (dual = 1).
+extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const void* b_dev, const void* b_lo_dev,
+                                 int M, int N, int K, int dual, void* out_dev, int* err_dev, uintptr_t cuda_stream) {
   using namespace spec;
   if (!a_dev || !b_dev || !out_dev || !err_dev || (dual && !a2_dev)) return set_last_error(-1, "null pointer");
   if (M < TC_BM || M % TC_BM || K < TC_BK || K % TC_BK || N < 1) return set_last_error(-1, "M, K multiples of 128, 64");
@@ -309,14 +325,16 @@ extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const vo
   TcMaps maps;
   maps.dual = dual;
   if (tc_make_map(&maps.a, a_dev, K, M, TC_BM) || (dual && tc_make_map(&maps.a2, a2_dev, K, M, TC_BM)) ||
-      tc_make_map(&maps.b, b_dev, K, N, TC_NSUB))
+      tc_make_map(&maps.b, b_dev, K, N, TC_NSUB) || (b_lo_dev && tc_make_map(&maps.blo, b_lo_dev, K, N, TC_NSUB)))
     return set_last_error(-6, "tensor map encoding failed");
   if (!dual) maps.a2 = maps.a;
+  if (!b_lo_dev) maps.blo = maps.b;
   TcParams P = {};
   P.K = K; P.Mg = M; P.N = N; P.ldo = M; P.epi = dual ? TC_SWIGLU : TC_STORE;
   P.out_f32 = dual ? nullptr : reinterpret_cast<float*>(out_dev);
   P.out_bf16 = dual ? reinterpret_cast<uint16_t*>(out_dev) : nullptr;
   P.err = err_dev;
+  P.split = b_lo_dev != nullptr;
   launch_tc_gemm(maps, P, M / TC_BM, 1, (N + TC_MAXN - 1) / TC_MAXN, reinterpret_cast<cudaStream_t>(cuda_stream));
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? 0 : set_last_error(-3, cudaGetErrorString(e));
@@ -333,9 +351,9 @@ cudaError_t configure_tc_kernels() {
 void launch_tc_gemm(const TcMaps& maps, const TcParams& P, int m_tiles, int groups, int n_tiles, cudaStream_t st) {
   const dim3 grid(m_tiles, groups, n_tiles), blk(128);
   if (maps.dual)
-    k_tc_gemm<1><<<grid, blk, tc_smem_bytes(1), st>>>(maps.a, maps.a2, maps.b, P);
+    k_tc_gemm<1><<<grid, blk, tc_smem_bytes(1), st>>>(maps.a, maps.a2, maps.b, maps.blo, P);
   else
-    k_tc_gemm<0><<<grid, blk, tc_smem_bytes(0), st>>>(maps.a, maps.a, maps.b, P);
+    k_tc_gemm<0><<<grid, blk, tc_smem_bytes(0), st>>>(maps.a, maps.a, maps.b, maps.blo, P);
 }
 
 }  // namespace spec

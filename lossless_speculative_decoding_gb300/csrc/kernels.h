@@ -71,6 +71,17 @@ struct StepBuf {
   float* y;          // [T*NS, h]
   float* am_val; int* am_idx;        // [T, n_vocab_blocks] argmax partials
   int* g;            // [T] greedy tokens
+  // tensor-core path operands (null when the model streams with SIMT GEMVs)
+  float* qkv;             // [T, (Hq+2Hkv) d] QKV GEMM output
+  // each bf16 operand X is stored as hi = bf16(X) and lo = bf16(X - hi)
+  uint16_t* xn_bf16;      // [T, h] RMS-normalised rows
+  uint16_t* xn_lo;
+  uint16_t* o_bf16;       // [T, Hq d] attention output
+  uint16_t* o_lo;
+  uint16_t* xperm;        // [T*NS, h] FFN input rows in expert-permuted order
+  uint16_t* xperm_lo;
+  uint16_t* hperm;        // [T*NS, inter] SwiGLU output in expert-permuted order
+  uint16_t* hperm_lo;
   int* step_in;      // staging: [seq ids (max_batch) | drafts (max_batch*K) | n_draft (max_batch)]
   int* step_out;     // staging: [acc (max_batch) | bonus (max_batch) | device error bits]
   unsigned long long* out_ptrs;  // [2] caller device outputs (acc, bonus) of a _dev step; 0 = none.
@@ -90,7 +101,9 @@ void launch_qkv(const Dims& D, const DevState& S, const StepBuf& B, const LayerW
 void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
                       cudaStream_t st);
 void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, float* xres, cudaStream_t st);
-void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, const float* xres, cudaStream_t st);
+// full: always compute top-k and the permutation (the tensor-core path needs them)
+void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, const float* xres, bool full,
+                   cudaStream_t st);
 void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
 // At small T the router kernel writes only logits and gate/up routes in its prologue.
 bool route_in_gateup(int T);
@@ -123,7 +136,9 @@ struct TcParams {
   const int* g_cnt;
   const int* g_n;
   float* out_f32;         // STORE [off+n][col] / ADD (+=) / SCATTER [perm[off+n]][col]
-  uint16_t* out_bf16;     // SWIGLU [off+n][col]
+  uint16_t* out_bf16;     // SWIGLU [off+n][col] (hi part)
+  uint16_t* out_bf16_lo;  // SWIGLU low part (value - hi), nullable
+  int split;              // activations given as hi + lo operands
   const int* perm;
   const float* scale;     // per weight row (nullable)
   const float* scale2;    // per weight row of the second operand (SWIGLU up)
@@ -134,7 +149,7 @@ struct TcParams {
 };
 
 struct TcMaps {
-  CUtensorMap a, a2, b;
+  CUtensorMap a, a2, b, blo;   // weights, second weights (dual), activations hi, lo
   int dual;
 };
 
@@ -143,6 +158,12 @@ struct TcMaps {
 int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 void launch_tc_gemm(const TcMaps& maps, const TcParams& P, int m_tiles, int groups, int n_tiles, cudaStream_t st);
 cudaError_t configure_tc_kernels();
+void launch_norm_bf16(const Dims& D, const float* x, const float* gamma, uint16_t* out, uint16_t* out_lo, int T,
+                      cudaStream_t st);
+void launch_rope_kv(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, cudaStream_t st);
+void launch_gather_bf16(const Dims& D, const StepBuf& B, int T, cudaStream_t st);
+void launch_argmax_commit(const Dims& D, const DevState& S, const StepBuf& B, int T, int ld, bool commit, int n_seq,
+                          int K, cudaStream_t st);
 
 // Kernel classes (for profiling); order matches spec_kernel_class_name().
 enum KClass { KC_ASSEMBLE, KC_QKV, KC_ATTN, KC_OPROJ, KC_ROUTER, KC_GATEUP, KC_DOWN, KC_COMBINE, KC_LMHEAD,

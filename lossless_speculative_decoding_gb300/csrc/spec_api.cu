@@ -139,6 +139,13 @@ struct spec_model {
   bool own_stream = false;
   int64_t h2d_bytes = 0, d2h_bytes = 0;   // host<->device bytes moved by step calls
   std::atomic<int> prof_gate{1};           // profiler: stream held until a step is enqueued
+  // tensor-core path (bf16 weights, more than 8 rows per step): tensor maps of
+  // every weight and of the bf16 activation operands
+  bool use_tc = false;
+  struct TcLayer { CUtensorMap qkv, o, gate, up, down; };
+  std::vector<TcLayer> tcl;
+  CUtensorMap tc_lm, tc_xn, tc_o, tc_xperm, tc_hperm;          // activations: hi
+  CUtensorMap tc_xn_lo, tc_o_lo, tc_xperm_lo, tc_hperm_lo;     //              lo
 
   ~spec_model() {
     for (auto& g : graphs) cudaGraphExecDestroy(g.second);
@@ -210,16 +217,65 @@ struct spec_model {
     }
   }
 
+  // Tensor-core GEMM launches. Dense: one group covering T rows. Grouped: the
+  // active-expert list of the step (rows of the permuted operand).
+  void tc_dense(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, int K, int M, int T, int epi,
+                float* out, int ldo) {
+    TcMaps mp;
+    mp.a = a; mp.a2 = a; mp.b = b; mp.blo = blo; mp.dual = 0;
+    TcParams P = {};
+    P.K = K; P.Mg = M; P.N = T; P.ldo = ldo; P.epi = epi; P.out_f32 = out; P.err = S.err; P.split = 1;
+    if (epi == TC_ARGMAX) { P.am_val = B.am_val; P.am_idx = B.am_idx; P.am_ld = M / 128; }
+    launch_tc_gemm(mp, P, M / 128, 1, (T + 127) / 128, stream);
+  }
+  void tc_grouped(const CUtensorMap& a, const CUtensorMap* a2, const CUtensorMap& b, const CUtensorMap& blo, int K,
+                  int Mg, int T, int epi, float* out_f32, uint16_t* out_bf16, uint16_t* out_lo, int ldo) {
+    TcMaps mp;
+    mp.a = a; mp.a2 = a2 ? *a2 : a; mp.b = b; mp.blo = blo; mp.dual = a2 ? 1 : 0;
+    TcParams P = {};
+    P.K = K; P.Mg = Mg; P.N = T; P.ldo = ldo; P.epi = epi; P.out_f32 = out_f32; P.out_bf16 = out_bf16;
+    P.out_bf16_lo = out_lo; P.split = 1;
+    P.perm = B.perm; P.err = S.err;
+    P.g_expert = B.act_expert; P.g_off = B.act_off; P.g_cnt = B.act_cnt; P.g_n = B.n_active;
+    const int max_active = (D.E > 0 ? std::min(D.E, T * D.k) : 0) + D.S;
+    launch_tc_gemm(mp, P, Mg / 128, max_active, (T + 127) / 128, stream);
+  }
+
   // Enqueue one forward over T rows already assembled in B (row meta + x);
   // returns the residual buffer holding the final rows.
   const float* enqueue_layers(int T, int R_rows, Prof* p = nullptr) {
     float* cur = B.x;
+    const int qkv_rows = (D.Hq + 2 * D.Hkv) * D.d;
     for (int l = 0; l < D.L; ++l) {
       const LayerW& W = layers[l];
+      if (use_tc) {
+        const TcLayer& M = tcl[l];
+        run_k(p, KC_QKV, [&] {
+          launch_norm_bf16(D, cur, W.attn_norm, B.xn_bf16, B.xn_lo, T, stream);
+          tc_dense(M.qkv, tc_xn, tc_xn_lo, D.h, qkv_rows, T, TC_STORE, B.qkv, qkv_rows);
+          launch_rope_kv(D, S, B, l, T, stream);
+        });
+        run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, stream); });
+        run_k(p, KC_OPROJ, [&] { tc_dense(M.o, tc_o, tc_o_lo, D.Hq * D.d, D.h, T, TC_ADD, cur, D.h); });
+        run_k(p, KC_ROUTER, [&] {
+          launch_router(D, B, W, T, cur, true, stream);
+          launch_gather_bf16(D, B, T, stream);
+        });
+        run_k(p, KC_GATEUP, [&] {
+          tc_grouped(M.gate, &M.up, tc_xperm, tc_xperm_lo, D.h, D.inter, T, TC_SWIGLU, nullptr, B.hperm, B.hperm_lo,
+                     D.inter);
+        });
+        if (p) cudaMemcpyAsync(p->act + p->nact++, B.n_active, 4, cudaMemcpyDeviceToHost, stream);
+        run_k(p, KC_DOWN, [&] {
+          tc_grouped(M.down, nullptr, tc_hperm, tc_hperm_lo, D.inter, D.h, T, TC_SCATTER, B.y, nullptr, nullptr, D.h);
+        });
+        run_k(p, KC_COMBINE, [&] { launch_combine(D, B, cur, T, stream); });
+        continue;
+      }
       run_k(p, KC_QKV, [&] { launch_qkv(D, S, B, W, l, T, cur, stream); });
       run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, stream); });
       run_k(p, KC_OPROJ, [&] { launch_oproj(D, B, W, T, cur, stream); });
-      run_k(p, KC_ROUTER, [&] { launch_router(D, B, W, T, cur, stream); });
+      run_k(p, KC_ROUTER, [&] { launch_router(D, B, W, T, cur, false, stream); });
       run_k(p, KC_GATEUP, [&] { launch_gateup(D, B, W, T, stream); });
       if (p) cudaMemcpyAsync(p->act + p->nact++, B.n_active, 4, cudaMemcpyDeviceToHost, stream);
       run_k(p, KC_DOWN, [&] { launch_down(D, B, W, T, stream); });
@@ -228,13 +284,23 @@ struct spec_model {
     return cur;
   }
 
+  // Final norm + LM head + argmax over rows [0, T) of x (+ commit).
+  void enqueue_lmhead(const float* x, int T, float* logits_dbg, bool commit, int n_seq) {
+    if (!use_tc) {
+      launch_lmhead_step(D, S, B, lm_head, final_norm, x, T, logits_dbg, commit, n_seq, K, stream);
+      return;
+    }
+    launch_norm_bf16(D, x, final_norm, B.xn_bf16, B.xn_lo, T, stream);
+    if (logits_dbg) tc_dense(tc_lm, tc_xn, tc_xn_lo, D.h, D.V, T, TC_STORE, logits_dbg, D.V);
+    tc_dense(tc_lm, tc_xn, tc_xn_lo, D.h, D.V, T, TC_ARGMAX, nullptr, 0);
+    launch_argmax_commit(D, S, B, T, D.V / 128, commit, n_seq, K, stream);
+  }
+
   void enqueue_verify(int n_seq, float* logits_dbg, bool commit, Prof* p = nullptr) {
     const int T = n_seq * R;
     run_k(p, KC_ASSEMBLE, [&] { launch_assemble_verify(D, S, B, tok_embed, n_seq, K, stream); });
     const float* xf = enqueue_layers(T, R, p);
-    run_k(p, KC_LMHEAD, [&] {
-      launch_lmhead_step(D, S, B, lm_head, final_norm, xf, T, logits_dbg, commit, n_seq, K, stream);
-    });
+    run_k(p, KC_LMHEAD, [&] { enqueue_lmhead(xf, T, logits_dbg, commit, n_seq); });
   }
 
   int graph_for(int n_seq, cudaGraphExec_t* out) {
@@ -405,6 +471,45 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
       (rc = m->dalloc(&B.am_val, (size_t)T * B.n_vblocks)) || (rc = m->dalloc(&B.am_idx, (size_t)T * B.n_vblocks)) ||
       (rc = m->dalloc(&B.g, T)))
     return rc;
+  // tensor-core path: bf16 weights with more than 8 rows per verify step
+  {
+    const int qkv_rows = (D.Hq + 2 * D.Hkv) * D.d;
+    const bool shapes = D.h % 128 == 0 && qkv_rows % 128 == 0 && D.inter % 128 == 0 && D.V % 128 == 0 &&
+                        (D.Hq * D.d) % 64 == 0 && D.h % 64 == 0 && D.inter % 64 == 0;
+    m->use_tc = c.wdtype == SPEC_BF16 && c.max_batch * m->R > 8 && shapes;
+  }
+  if (m->use_tc) {
+    const int qkv_rows = (D.Hq + 2 * D.Hkv) * D.d;
+    if ((rc = m->dalloc(&B.qkv, (size_t)T * qkv_rows)) || (rc = m->dalloc(&B.xn_bf16, (size_t)T * D.h)) ||
+        (rc = m->dalloc(&B.xn_lo, (size_t)T * D.h)) || (rc = m->dalloc(&B.o_bf16, (size_t)T * D.Hq * D.d)) ||
+        (rc = m->dalloc(&B.o_lo, (size_t)T * D.Hq * D.d)) || (rc = m->dalloc(&B.xperm, (size_t)T * NS * D.h)) ||
+        (rc = m->dalloc(&B.xperm_lo, (size_t)T * NS * D.h)) || (rc = m->dalloc(&B.hperm, (size_t)T * NS * D.inter)) ||
+        (rc = m->dalloc(&B.hperm_lo, (size_t)T * NS * D.inter)))
+      return rc;
+    CU(configure_tc_kernels());
+    const int F = D.E + D.S;
+    m->tcl.resize(D.L);
+    int bad = 0;
+    for (int l = 0; l < D.L; ++l) {
+      const LayerW& W = m->layers[l];
+      auto& M = m->tcl[l];
+      bad |= tc_make_map(&M.qkv, W.w_qkv, D.h, qkv_rows, 128);
+      bad |= tc_make_map(&M.o, W.w_o, (uint64_t)D.Hq * D.d, D.h, 128);
+      bad |= tc_make_map(&M.gate, W.w_gate, D.h, (uint64_t)F * D.inter, 128);
+      bad |= tc_make_map(&M.up, W.w_up, D.h, (uint64_t)F * D.inter, 128);
+      bad |= tc_make_map(&M.down, W.w_down, D.inter, (uint64_t)F * D.h, 128);
+    }
+    bad |= tc_make_map(&m->tc_lm, m->lm_head, D.h, D.V, 128);
+    bad |= tc_make_map(&m->tc_xn, B.xn_bf16, D.h, T, 32);
+    bad |= tc_make_map(&m->tc_o, B.o_bf16, (uint64_t)D.Hq * D.d, T, 32);
+    bad |= tc_make_map(&m->tc_xperm, B.xperm, D.h, (uint64_t)T * NS, 32);
+    bad |= tc_make_map(&m->tc_hperm, B.hperm, D.inter, (uint64_t)T * NS, 32);
+    bad |= tc_make_map(&m->tc_xn_lo, B.xn_lo, D.h, T, 32);
+    bad |= tc_make_map(&m->tc_o_lo, B.o_lo, (uint64_t)D.Hq * D.d, T, 32);
+    bad |= tc_make_map(&m->tc_xperm_lo, B.xperm_lo, D.h, (uint64_t)T * NS, 32);
+    bad |= tc_make_map(&m->tc_hperm_lo, B.hperm_lo, D.inter, (uint64_t)T * NS, 32);
+    if (bad) return fail(SPEC_ERR_CUDA, "tensor map encoding failed");
+  }
   m->step_in_n = c.max_batch * (2 + m->K);
   m->step_out_n = 2 * c.max_batch + 1;   // acc | bonus | device error bits
   // [out_ptrs (2 x 64-bit) | step inputs]: one host copy refreshes both
@@ -447,8 +552,7 @@ static int run_prefill_rows(spec_model* m, int slot, const std::vector<int32_t>&
     launch_assemble_prefill(m->D, m->S, m->B, m->tok_embed, vis, slot, start + c0, T, m->stream);
     const float* xf = m->enqueue_layers(T, T);
     if (c0 + T == n && out_tok) {
-      launch_lmhead_step(m->D, m->S, m->B, m->lm_head, m->final_norm, xf + (size_t)(T - 1) * m->D.h, 1, nullptr,
-                         false, 0, 0, m->stream);
+      m->enqueue_lmhead(xf + (size_t)(T - 1) * m->D.h, 1, nullptr, false, 0);
       CU(cudaMemcpyAsync(m->pin_out, m->B.g, sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
     }
     // the staging buffer is reused by the next chunk
@@ -834,6 +938,8 @@ int spec_free_pages(spec_model* m) {
 
 int spec_step_launches(spec_model* m, int n_seq) {
   if (!m || n_seq < 1) return fail(SPEC_ERR_ARG, "bad arguments");
+  if (m->use_tc)   // per layer: norm, QKV, RoPE/KV, attention, O, router, gather, gate/up, down, combine
+    return 1 + m->D.L * 10 + 3;
   return launches_per_step(m->D, n_seq * m->R);
 }
 

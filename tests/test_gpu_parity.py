@@ -308,3 +308,50 @@ def test_mid_size_lossless_and_parity():
     lg = g3.debug_logits([0], np.array(d))
     ol = oracle.verify_rows(om, cache, int(toks[-1]), d)
     assert row_tol_ok(lg, ol, 2e-2).all()
+
+
+@pytest.mark.parametrize("cfg,K,nseq", [(MOE_SMALL, 3, 3), (DENSE_SMALL, 31, 1)])
+def test_tensor_core_path_parity_and_invariance(cfg, K, nseq):
+    """Models with more than 8 rows per step run every projection on the
+    tcgen05 GEMM. Verify rows match the oracle within 2e-2 of each row's
+    range (bf16 operands), and a sequence decoded alone and decoded in a batch
+    with other sequences commits identical tokens (batch invariance)."""
+    from lossless_speculative_decoding_gb300 import binding as B
+    w = syn.generate_weights(cfg, 11)
+    om = oracle.OracleModel(w)
+    wl = syn.Workload("t", cfg, nseq, K, "iid", 0.6, (64, 0, 0), 8, 0, (40,))
+    prompts = syn.make_prompts(wl, n_seq=3)
+    gm = gpu_model(cfg, w, max_ctx=384, max_draft=K, max_seqs=3, max_batch=3, n_pages=128)
+    assert B.spec_step_launches(gm.h, 1) > 1 + cfg.n_layers * 7 + 1       # the tensor-core layer form
+    p = prompts[0]
+    first = gm.prefill(0, p.visual, p.tokens)
+    cache = oracle.KVCache(cfg)
+    x = oracle.prompt_embeddings(om, p)
+    lg0 = oracle.forward(om, cache, x, np.arange(len(x)))[-1]
+    assert first == int(np.argmax(lg0)) or margin_exempt(lg0)
+    rng = np.random.default_rng(4)
+    toks = [first]
+    bad = 0
+    for step in range(4):
+        d = [int(t) for t in rng.integers(0, cfg.vocab, K)]
+        lg = gm.debug_logits([0], np.array(d))
+        base = cache.length
+        ol = oracle.verify_rows(om, cache, toks[-1], d)
+        bad += int((~row_tol_ok(lg, ol, 2e-2)).sum())
+        a, b = gm.verify(0, d)
+        assert (a, b) == oracle.accept(d, np.argmax(lg, -1))
+        cache.truncate(base + a + 1)
+        toks += d[:a] + [b]
+    assert bad == 0
+    # batch invariance: the same sequence, greedy alone vs greedy beside two others
+    gm.release(0)
+    alone = run_spec(gm, 0, p, 24, K, lambda n, m, s: [])[0]
+    gm.release(0)
+    gm.prefill(0, p.visual, p.tokens)
+    gm.prefill(1, prompts[1].visual, prompts[1].tokens)
+    gm.prefill(2, prompts[2].visual, prompts[2].tokens)
+    together = [int(B.spec_seq_tokens(gm.h, 0)[0])]
+    while len(together) < 24:
+        acc, bon = gm.verify_batch([0, 1, 2], np.zeros((3, K), np.int32), [0, 0, 0])
+        together.append(int(bon[0]))
+    assert np.array_equal(alone, np.array(together))

@@ -1,7 +1,9 @@
 """Tensor-core GEMM (tcgen05, TMA-staged, TMEM accumulator) against a plain
 float64 matmul of the same bf16 values: the store epilogue (fp32 out) and
 the dual SwiGLU epilogue (bf16 out), over shapes with partial activation
-boxes, more K tiles than pipeline stages, and two column tiles."""
+boxes, more K tiles than pipeline stages, and several column tiles; and the
+hi + lo split of fp32 activations, which must reach near-fp32 accuracy (a
+bound a single bf16 operand misses by two orders of magnitude)."""
 import numpy as np
 import pytest
 
@@ -27,7 +29,7 @@ def test_tc_gemm_store(M, N, K):
     b = torch.from_numpy(bb.view(np.int16)).cuda()
     out = torch.full((N, M), float("nan"), device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    B.spec_tc_gemm_test(a, None, b, M, N, K, 0, out, err, 0)
+    B.spec_tc_gemm_test(a, None, b, None, M, N, K, 0, out, err, 0)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     ref = bf.astype(np.float64) @ af.astype(np.float64).T
@@ -49,7 +51,7 @@ def test_tc_gemm_swiglu(M, N, K):
     b = torch.from_numpy(bb.view(np.int16)).cuda()
     out = torch.zeros((N, M), dtype=torch.int16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    B.spec_tc_gemm_test(g, u, b, M, N, K, 1, out, err, 0)
+    B.spec_tc_gemm_test(g, u, b, None, M, N, K, 1, out, err, 0)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     gg = bf.astype(np.float64) @ gf.astype(np.float64).T
@@ -57,3 +59,27 @@ def test_tc_gemm_swiglu(M, N, K):
     ref = gg / (1 + np.exp(-gg)) * uu
     got = oracle.decode_bf16(out.cpu().numpy().view(np.uint16)).astype(np.float64)
     np.testing.assert_allclose(got, ref, rtol=1e-2, atol=1e-2 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 300, 512), (128, 9, 2048)])
+def test_tc_gemm_split_activations(M, N, K):
+    import torch
+    from lossless_speculative_decoding_gb300 import binding as B
+    rng = np.random.default_rng(11 * M + N)
+    ab, af = _bf16(rng, (M, K), 0.05)
+    x = rng.standard_normal((N, K)).astype(np.float32)
+    hi = syn.f32_to_bf16_bits(x)
+    lo = syn.f32_to_bf16_bits((x - oracle.decode_bf16(hi)).astype(np.float32))
+    a = torch.from_numpy(ab.view(np.int16)).cuda()
+    bh = torch.from_numpy(hi.view(np.int16)).cuda()
+    bl = torch.from_numpy(lo.view(np.int16)).cuda()
+    out = torch.full((N, M), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.spec_tc_gemm_test(a, None, bh, bl, M, N, K, 0, out, err, 0)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = x.astype(np.float64) @ af.astype(np.float64).T
+    got = out.cpu().numpy()
+    # hi + lo carries ~16 mantissa bits (relative residual <= 2^-17); bf16
+    # alone would leave errors near 2^-9 of the row scale
+    np.testing.assert_allclose(got, ref, rtol=0, atol=5e-5 * np.abs(ref).max())
