@@ -167,6 +167,17 @@ def class_bytes(cfg, stats: dict, T: int, ctx_sum: float, n_steps: int) -> dict:
     return out
 
 
+def step_flops_of(cfg, T: int, R: int, ctx_sum: float, n_steps: int) -> float:
+    """Algorithmic FLOPs per step: 2 x T x (parameters each row meets:
+    attention, router, its k routed + shared experts, LM head), plus
+    4 x keys x Hq x d for each of a sequence's R rows (QK^T and PV)."""
+    h, d, L = cfg.hidden, cfg.head_dim, cfg.n_layers
+    attn = cfg.qkv_rows * h + h * cfg.n_q_heads * d
+    ffn = (cfg.top_k + cfg.n_shared) * 3 * h * cfg.inter + cfg.n_experts * h
+    per_row = L * (attn + ffn) + cfg.vocab * h
+    return 2.0 * T * per_row + 4.0 * L * cfg.n_q_heads * d * R * ctx_sum / n_steps
+
+
 # --------------------------------------------------------------------------- #
 # CPU oracle timing (cpu_baseline leg and --impl reference)
 # --------------------------------------------------------------------------- #
@@ -262,6 +273,26 @@ def traffic_for(kernel: str):
     return e["bytes_per_launch"]
 
 
+def steady_state_prompts(wl, prompts, rank: int):
+    """Closed-loop workloads (sampled output lengths) are measured in steady
+    state: sequence i starts the timed window already u_i tokens into its
+    output, u_i ~ U{0..out_len_i - 1}, so the batch holds the spread of
+    contexts a closed loop keeps busy. The u_i earlier outputs are seeded
+    random ids appended to the instruction tokens (their KV costs the same as
+    generated ones). Fixed-length workloads start at their first output."""
+    if len(wl.out_len) == 1:
+        return [0] * len(prompts), prompts
+    import dataclasses
+    g = np.random.Generator(np.random.PCG64([4 + rank, 0x5EED]))
+    out, pre = [], []
+    for p in prompts:
+        u = int(g.integers(0, p.out_len))
+        extra = g.integers(0, wl.model.vocab, size=u, dtype=np.int64).astype(np.int32)
+        out.append(dataclasses.replace(p, tokens=np.concatenate([p.tokens, extra])))
+        pre.append(u)
+    return pre, out
+
+
 def run_ours(args):
     import torch
     ws, rank, local = dist_env()
@@ -281,47 +312,74 @@ def run_ours(args):
         import dataclasses
         wl = dataclasses.replace(wl, model=syn.scaled(wl.model, n_layers=args.layers))
     cfg = wl.model
-    if wl.batch != 1:
-        raise SystemExit(f"bench.py runs the batch-1 workloads; {wl.name} has batch {wl.batch}")
-    K = wl.n_draft
+    NB, K, R = wl.batch, wl.n_draft, wl.n_draft + 1
     W, KS, P = args.warmup, args.steps, max(1, args.profile_steps)
+    total = W + KS + P
     t_setup = time.time()
     w = syn.generate_weights(cfg, 0)
-    prompt = syn.make_prompts(wl, n_seq=1, seed=1 + rank)[0]
-    total = W + KS + P
-    n_ref = 1 + total * (K + 1) + K + 1
-    max_ctx = prompt.length + n_ref + 2 * (K + 1)
-    pages = -(-max_ctx // wl.page_size) + 4
-    gm = SpecModel(cfg, w.arrays, page_size=wl.page_size, n_pages=pages, max_seqs=1, max_ctx=max_ctx,
-                   max_draft=K)
+    prompts0 = syn.make_prompts(wl, n_seq=NB, seed=1 + rank)
+    pre, prompts = steady_state_prompts(wl, prompts0, rank)
+    n_prefix = len(prompts[0].prefix_tokens)
+    # reference tokens needed: up to R per step (iid drafter); the geometric
+    # block drafter commits ~6.6 per step, so its reference is grown on demand
+    grow = R if wl.drafter == "iid" else min(R, 12)
+    n_ref0 = 1 + total * grow + R
+    max_ref = 1 + total * R + R
+    ctx_need = [p.length + max_ref + 2 * R for p in prompts]
+    max_ctx = max(ctx_need)
+    pages = sum(-(-c // wl.page_size) for c in ctx_need) + 8 * NB + 8
+    gm = SpecModel(cfg, w.arrays, page_size=wl.page_size, n_pages=pages, max_seqs=NB, max_ctx=max_ctx,
+                   max_draft=K, max_batch=NB)
     st = gm.stream
     h = gm.h
+    ids = list(range(NB))
+    prefix_id = gm.register_prefix(prompts[0].prefix_tokens) if n_prefix else -1
 
-    # 1) the GPU's own non-speculative greedy trajectory (drafter reference)
-    ref = [gm.prefill(0, prompt.visual, prompt.tokens)]
-    while len(ref) < n_ref:
-        ref.append(gm.verify(0, [])[1])
-    ref = np.array(ref, np.int32)
-    gm.release(0)
+    def prefill_all():
+        return [gm.prefill(i, prompts[i].visual, prompts[i].tokens, prefix_id) for i in ids]
+
+    # 1) the GPU's own non-speculative greedy trajectories (drafter reference)
+    refs = [[t] for t in prefill_all()]
+    zero_d = np.zeros((NB, K), np.int32)
+
+    def extend(n):
+        while min(len(r) for r in refs) < n:
+            _, bon = gm.verify_batch(ids, zero_d, [0] * NB)
+            for i in ids:
+                refs[i].append(int(bon[i]))
+
+    extend(n_ref0)
     drafter = syn.Drafter(wl.drafter, wl.q, cfg.vocab, seed=2)
-    drafts, agree, n_before = syn.draft_schedule(drafter, ref, total, K, seq=rank)
+    while True:
+        plans = [syn.draft_schedule(drafter, np.array(refs[i], np.int32), total, K, seq=rank * NB + i) for i in ids]
+        need = max(int(pl[2][-1] + pl[1][-1] + 1 + R) for pl in plans)
+        if need <= min(len(r) for r in refs) or min(len(r) for r in refs) >= max_ref:
+            break
+        extend(min(need + total, max_ref))
+    refs = [np.array(r, np.int32) for r in refs]
+    for i in ids:
+        gm.release(i)
+    drafts = np.stack([pl[0] for pl in plans], 1)          # [total, NB, K]
+    agree = np.stack([pl[1] for pl in plans], 1)           # [total, NB]
+    n_before = np.stack([pl[2] for pl in plans], 1)        # [total, NB]
 
     # 2) device-resident run: inputs in HBM, graph replay per step
-    first = gm.prefill(0, prompt.visual, prompt.tokens)
-    assert first == ref[0]
-    B.spec_reserve_seq(h, 0, min(max_ctx, prompt.length + n_ref + K + 1))
+    first = prefill_all()
+    assert first == [int(r[0]) for r in refs]
+    for i in ids:
+        B.spec_reserve_seq(h, i, min(max_ctx, prompts[i].length + len(refs[i]) + R))
     with torch.cuda.stream(st):
         d_drafts = torch.from_numpy(drafts.reshape(-1).copy()).cuda()
-        d_seq = torch.zeros(1, dtype=torch.int32, device="cuda")
-        d_nd = torch.full((1,), K, dtype=torch.int32, device="cuda")
-        d_acc = torch.zeros(total, dtype=torch.int32, device="cuda")
-        d_bon = torch.zeros(total, dtype=torch.int32, device="cuda")
+        d_seq = torch.arange(NB, dtype=torch.int32, device="cuda")
+        d_nd = torch.full((NB,), K, dtype=torch.int32, device="cuda")
+        d_acc = torch.zeros(total * NB, dtype=torch.int32, device="cuda")
+        d_bon = torch.zeros(total * NB, dtype=torch.int32, device="cuda")
     st.synchronize()
     esz = 4
 
     def dev_step(s):
-        B.spec_verify_step_batch_dev(h, 1, d_seq, d_drafts.data_ptr() + s * K * esz, d_nd,
-                                     d_acc.data_ptr() + s * esz, d_bon.data_ptr() + s * esz)
+        B.spec_verify_step_batch_dev(h, NB, d_seq, d_drafts.data_ptr() + s * NB * K * esz, d_nd,
+                                     d_acc.data_ptr() + s * NB * esz, d_bon.data_ptr() + s * NB * esz)
 
     for s in range(W):
         dev_step(s)
@@ -341,62 +399,79 @@ def run_ours(args):
     clk = clocks.stop()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    acc = d_acc.cpu().numpy()
+    acc = d_acc.cpu().numpy().reshape(total, NB)
     committed = int((acc[W:W + KS] + 1).sum())
     ms_all, committed_all = aggregate(ms, committed, device="cuda")
 
-    # 3) profiled steps (events around every kernel launch) on the same sequence
-    stats = B.spec_profile_steps_dev(h, 1, d_seq, d_drafts.data_ptr() + (W + KS) * K * esz, d_nd, P, K)
+    # 3) profiled steps (events around every kernel launch) on the same sequences
+    stats = B.spec_profile_steps_dev(h, NB, d_seq, d_drafts.data_ptr() + (W + KS) * NB * K * esz, d_nd, P,
+                                     NB * K)
     B.spec_sync_seqs(h)
-    gen = gm.tokens(0)
-    n_done = int(n_before[total - 1] + agree[total - 1] + 1) if total else 1
-    lossless = bool(np.array_equal(gen[:n_done], ref[:n_done]))
-    acc_ok = bool(np.array_equal(acc[:W + KS], agree[:W + KS]))
-    gm.release(0)
+    acc = d_acc.cpu().numpy().reshape(total, NB)
+    lossless = acc_ok = True
+    for i in ids:
+        gen = gm.tokens(i)
+        n_done = int(n_before[total - 1, i] + agree[total - 1, i] + 1)
+        lossless &= bool(np.array_equal(gen[:n_done], refs[i][:n_done]))
+        acc_ok &= bool(np.array_equal(acc[:W + KS, i], agree[:W + KS, i]))
+    for i in ids:
+        gm.release(i)
 
     # 4) end to end through the host C-ABI call (H2D drafts, D2H results each step)
-    gm.prefill(0, prompt.visual, prompt.tokens)
+    prefill_all()
+    nd_host = [K] * NB
     for s in range(W):
-        B.spec_verify_step_batch(h, [0], drafts[s], [K])
+        B.spec_verify_step_batch(h, ids, drafts[s].reshape(-1), nd_host)
     h2d0, d2h0 = B.spec_io_bytes(h)
     if ws > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
     e2e_committed = 0
     for s in range(W, W + KS):
-        a, _ = B.spec_verify_step_batch(h, [0], drafts[s], [K])
-        e2e_committed += int(a[0]) + 1
+        a, _ = B.spec_verify_step_batch(h, ids, drafts[s].reshape(-1), nd_host)
+        e2e_committed += int(np.sum(a)) + NB
     e2e_s = time.perf_counter() - t0
     h2d1, d2h1 = B.spec_io_bytes(h)
-    e2e_ok = bool(np.array_equal(gm.tokens(0)[:len(ref)], ref[:len(gm.tokens(0))]))
-    gm.release(0)
+    e2e_ok = True
+    for i in ids:
+        t = gm.tokens(i)
+        e2e_ok &= bool(np.array_equal(t, refs[i][:len(t)]))
+        gm.release(i)
     e2e_s, e2e_committed = aggregate(e2e_s, e2e_committed, device="cuda")
 
     # 5) roofline of the dominant kernel and of the whole step
     peaks = measured_peaks()
-    T = K + 1
-    ctx_sum = float(sum(prompt.length + n_before[s] for s in range(W + KS, total)))
+    T = NB * R
+    # keys a layer's attention reads per profiled step (shared-prefix pages once)
+    ctx_sum = float(sum(prompts[i].length + n_before[s, i] for s in range(W + KS, total) for i in ids)
+                    - (NB - 1) * n_prefix * P)
     cb = class_bytes(cfg, stats, T, ctx_sum, P)
     dom = max((k for k in stats if k in cb), key=lambda k: stats[k]["ms"])
     dom_bytes_per_launch = cb[dom] / max(stats[dom]["launches"], 1)
     dom_ms_per_launch = stats[dom]["ms"] / max(stats[dom]["launches"], 1)
     achieved = dom_bytes_per_launch / (dom_ms_per_launch * 1e-3) / 1e9
     step_bytes = sum(cb.values()) / P
+    step_flops = step_flops_of(cfg, T, R, ctx_sum, P)
     prof_ms = sum(v["ms"] for v in stats.values()) / P
-    t_roof_us = step_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+    t_hbm_us = step_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+    t_tc_us = step_flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+    t_roof_us = max(t_hbm_us, t_tc_us)
     ms_per_step = ms_all / KS
-    launches = B.spec_step_launches(h, 1) + 1     # + the staging kernel
+    launches = B.spec_step_launches(h, NB) + 1     # + the staging kernel
     share = {k: round(v["ms"] / max(sum(x["ms"] for x in stats.values()), 1e-9), 4) for k, v in stats.items()}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        r = oracle_rate(w, prompt, wl, max_steps=KS, warmup=1, budget_s=args.cpu_budget_s)
+        i0 = min(ids, key=lambda i: prompts0[i].length)
+        r = oracle_rate(w, prompts0[i0], wl, max_steps=KS, warmup=1, budget_s=args.cpu_budget_s, seq=rank * NB + i0)
         cpu = {"value": r["tok_s"], "unit": "tokens/s", "cores": r["cores"], "kind": "oracle",
-               "sample": f"{r['steps']} oracle verify steps (T={T} rows each) after one warm-up step, "
-                         f"same workload and drafter; oracle prefill of the {prompt.length}-row prompt "
-                         f"({r['prefill_s']:.1f}s) excluded"}
+               "sample": f"{r['steps']} oracle verify steps (one sequence, {R} rows each) after one warm-up "
+                         f"step, same model and drafter; oracle prefill of the {prompts0[i0].length}-row "
+                         f"prompt ({r['prefill_s']:.1f}s) excluded" + (
+                             f"; the shortest of the {NB} prompts, from its first output" if NB > 1 else "")}
 
     if rank == 0:
+        steady = len(wl.out_len) > 1
         line = {
             "metric": "committed tokens/s (greedy speculative verify, excl. prefill)",
             "value": committed_all / (ms_all * 1e-3),
@@ -404,16 +479,23 @@ def run_ours(args):
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": {syn.F32: "f32", syn.BF16: "bf16", syn.FP8: "e4m3 weights / f32 activations"}[cfg.wdtype],
             "data": "synthetic (random-init weights, N(0,1) visual rows, seeded drafter)",
-            "config": {"workload": wl.name, "model": cfg.name, "layers": cfg.n_layers, "batch": wl.batch, "n_draft": K,
-                       "draft_match_prob": wl.q, "prompt_rows": prompt.length, "page_size": wl.page_size,
-                       "tau": committed / KS, "l2": "weights read per step (>2 GB) exceed the 126 MB L2",
+            "config": {"workload": wl.name, "model": cfg.name, "layers": cfg.n_layers, "batch": NB, "n_draft": K,
+                       "drafter": f"{wl.drafter} q={wl.q}", "rows_per_step": T,
+                       "prompt_rows": [p.length for p in prompts0] if NB > 1 else prompts0[0].length,
+                       "page_size": wl.page_size, "shared_prefix": n_prefix,
+                       "tau": committed / (KS * NB),
+                       "start": "steady state: seq i starts u_i ~ U{0..out_len_i-1} tokens into its output"
+                       if steady else "first output token",
+                       "l2": "weights + KV read per step exceed the 126 MB L2",
                        "parallelism": f"replicas x{ws}"},
             "verify_step_us": ms_per_step * 1e3,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "traffic": traffic_for(dom), "peak_source": peaks["source"],
                          "bytes_per_launch": dom_bytes_per_launch, "us_per_launch": dom_ms_per_launch * 1e3},
-            "step_roofline": {"bytes_per_step": step_bytes, "t_roof_us": t_roof_us,
+            "step_roofline": {"bytes_per_step": step_bytes, "flops_per_step": step_flops,
+                              "t_hbm_us": t_hbm_us, "t_tensor_us": t_tc_us,
+                              "bound": "hbm" if t_hbm_us >= t_tc_us else "tensor", "t_roof_us": t_roof_us,
                               "t_meas_us": ms_per_step * 1e3, "frac": t_roof_us / (ms_per_step * 1e3),
                               "profiled_kernel_us_per_step": prof_ms * 1e3, "kernel_share": share},
             "e2e": {"value": e2e_committed / e2e_s, "unit": "tokens/s",

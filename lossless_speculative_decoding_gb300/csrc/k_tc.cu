@@ -15,8 +15,15 @@
 // CTA computes the columns of one group, so each token column only ever sees
 // its own row of X -- its result does not depend on the other tokens.
 //
+// FP8 weights (e4m3, per-row fp32 scale applied in the epilogue): TMA brings
+// the e4m3 tile unswizzled into a staging buffer, four converter warps widen
+// it to bf16 -- exactly, every e4m3 value is a bf16 value -- into the
+// 128-byte-swizzled operand tile and signal the MMA thread, so the tensor
+// cores run the same bf16 MMA while HBM carries one byte per weight.
+//
 // Every wait on an mbarrier is bounded; a timeout sets an error bit, the CTA
 // stops issuing work, frees its TMEM and returns.
+#include <cuda_fp8.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -32,10 +39,16 @@ constexpr int TC_MAXN = 128;          // columns per CTA
 constexpr uint32_t TC_WAIT_LIMIT = 1u << 20;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;        // 16 KB
 constexpr int TC_B_BYTES = TC_MAXN * TC_BK * 2;      // 16 KB (hi) + 16 KB (lo)
+constexpr int TC_A8_BYTES = TC_BM * TC_BK;           // 8 KB e4m3 staging per weight operand
 
-__host__ __device__ constexpr int tc_stages(int dual) { return dual ? 3 : 4; }
-__host__ __device__ constexpr int tc_stage_bytes(int dual) { return TC_A_BYTES * (1 + dual) + 2 * TC_B_BYTES; }
-__host__ __device__ constexpr int tc_smem_bytes(int dual) { return tc_stages(dual) * tc_stage_bytes(dual) + 1024 + 256; }
+__host__ __device__ constexpr int tc_stages(int dual, int f8) { return f8 ? (dual ? 2 : 4) : (dual ? 3 : 4); }
+__host__ __device__ constexpr int tc_stage_bytes(int dual, int f8) {
+  return (TC_A_BYTES + (f8 ? TC_A8_BYTES : 0)) * (1 + dual) + 2 * TC_B_BYTES;
+}
+__host__ __device__ constexpr int tc_smem_bytes(int dual, int f8) {
+  return tc_stages(dual, f8) * tc_stage_bytes(dual, f8) + 1024 + 256;
+}
+__host__ __device__ constexpr int tc_threads(int f8) { return f8 ? 256 : 128; }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -84,17 +97,48 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int DUAL>
-__global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUtensorMap mapA,
-                                                     const __grid_constant__ CUtensorMap mapA2,
-                                                     const __grid_constant__ CUtensorMap mapB,
-                                                     const __grid_constant__ CUtensorMap mapBlo, TcParams P) {
-  constexpr int STAGES = tc_stages(DUAL);
-  constexpr int SB = tc_stage_bytes(DUAL);
+// Eight e4m3 values (one 8-byte word pair) as eight bf16 values.
+__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 v) {
+  const uint32_t w[2] = {v.x, v.y};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[i] >> (16 * h)) & 0xFFFF), __NV_E4M3);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+      o[2 * i + h] = (__float_as_uint(f.x) >> 16) | (__float_as_uint(f.y) & 0xFFFF0000u);
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Stage s of the FP8 form: e4m3 staging [128 rows][64 B] -> bf16 tile [128
+// rows][128 B] with the 128-byte swizzle (16-byte piece c of row r at
+// (c ^ (r % 8)) * 16). 128 converter threads, 8 pieces each.
+__device__ __forceinline__ void convert_tile(const unsigned char* stg, unsigned char* dst, int t) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = t + 128 * j, r = i >> 3, c = i & 7;
+    const uint2 v = *reinterpret_cast<const uint2*>(stg + r * 64 + c * 8);
+    *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = e4m3x8_to_bf16x8(v);
+  }
+}
+
+template <int DUAL, int F8>
+__global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_constant__ CUtensorMap mapA,
+                                                               const __grid_constant__ CUtensorMap mapA2,
+                                                               const __grid_constant__ CUtensorMap mapB,
+                                                               const __grid_constant__ CUtensorMap mapBlo, TcParams P) {
+  constexpr int STAGES = tc_stages(DUAL, F8);
+  constexpr int SB = tc_stage_bytes(DUAL, F8);
+  // stage layout: [A bf16 (x2 if DUAL)][B hi][B lo][A e4m3 staging (x2 if DUAL), F8 only]
+  constexpr int STG_OFF = TC_A_BYTES * (1 + DUAL) + 2 * TC_B_BYTES;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * SB);   // full[STAGES], empty[STAGES], done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  // full[STAGES], empty[STAGES], done, conv[STAGES] (F8: converted tile ready)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * SB);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -117,6 +161,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUte
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2 * STAGES + 1; ++i)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bars + i)));
+    for (int i = 0; i < STAGES; ++i)    // one arrival per converter warp
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(smem_u32(bars + 2 * STAGES + 1 + i)));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *abort_flag = 0;
   }
@@ -132,7 +178,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUte
 
   if (warp == 0 && lane == 0) {
     // ---- TMA producer ----
-    const uint32_t bytes = TC_A_BYTES * (1 + DUAL) + (P.split ? 2 : 1) * nsub * TC_NSUB * TC_BK * 2;
+    const uint32_t bytes = (F8 ? TC_A8_BYTES : TC_A_BYTES) * (1 + DUAL) + (P.split ? 2 : 1) * nsub * TC_NSUB * TC_BK * 2;
     for (int kt = 0; kt < KT; ++kt) {
       const int s = kt % STAGES;
       if (kt >= STAGES && !mbar_wait(smem_u32(bars + STAGES + s), ((kt / STAGES) - 1) & 1)) {
@@ -143,8 +189,10 @@ __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUte
       unsigned char* st = smem + s * SB;
       const uint32_t full = smem_u32(bars + s);
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full), "r"(bytes) : "memory");
-      tma_2d(smem_u32(st), &mapA, kt * TC_BK, wrow, full);
-      if (DUAL) tma_2d(smem_u32(st + TC_A_BYTES), &mapA2, kt * TC_BK, wrow, full);
+      unsigned char* at = F8 ? st + STG_OFF : st;
+      constexpr int AST = F8 ? TC_A8_BYTES : TC_A_BYTES;
+      tma_2d(smem_u32(at), &mapA, kt * TC_BK, wrow, full);
+      if (DUAL) tma_2d(smem_u32(at + AST), &mapA2, kt * TC_BK, wrow, full);
       unsigned char* bt = st + TC_A_BYTES * (1 + DUAL);
       for (int j = 0; j < nsub; ++j) {
         tma_2d(smem_u32(bt + j * TC_NSUB * TC_BK * 2), &mapB, kt * TC_BK, off + n0 + j * TC_NSUB, full);
@@ -159,7 +207,8 @@ __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUte
     bool ok = true;
     for (int kt = 0; kt < KT && ok; ++kt) {
       const int s = kt % STAGES;
-      if (!mbar_wait(smem_u32(bars + s), (kt / STAGES) & 1)) {
+      // bf16: the TMA bytes of the stage; F8: the converters' signal (after those bytes)
+      if (!mbar_wait(smem_u32(bars + (F8 ? 2 * STAGES + 1 : 0) + s), (kt / STAGES) & 1)) {
         atomicOr(P.err, DERR_TIMEOUT);
         *abort_flag = 1;
         ok = false;
@@ -194,6 +243,22 @@ __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUte
     if (ok)
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                    ::"r"(smem_u32(bars + 2 * STAGES)) : "memory");
+  } else if (F8 && warp >= 4) {
+    // ---- converters: e4m3 staging -> swizzled bf16 operand tile ----
+    const int t = threadIdx.x - 128;
+    for (int kt = 0; kt < KT; ++kt) {
+      const int s = kt % STAGES;
+      if (!mbar_wait(smem_u32(bars + s), (kt / STAGES) & 1)) {
+        if (lane == 0) atomicOr(P.err, DERR_TIMEOUT);
+        break;
+      }
+      unsigned char* st = smem + s * SB;
+      convert_tile(st + STG_OFF, st, t);
+      if (DUAL) convert_tile(st + STG_OFF + TC_A8_BYTES, st + TC_A_BYTES, t);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bars + 2 * STAGES + 1 + s)) : "memory");
+    }
   }
   __syncwarp();
 
@@ -201,6 +266,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUte
   const bool have = __syncthreads_and(mbar_wait(smem_u32(bars + 2 * STAGES), 0)) != 0;   // block-uniform
   if (!have && threadIdx.x == 0) atomicOr(P.err, DERR_TIMEOUT);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (warp < 4) {
   const int m = warp * 32 + lane;                     // row within the tile
   const int col = mt * TC_BM + m;                     // output feature (row within the group)
   const float sc = (P.scale && have) ? P.scale[wrow + m] : 1.f;
@@ -271,6 +337,7 @@ __global__ void __launch_bounds__(128, 1) k_tc_gemm(const __grid_constant__ CUte
       }
     }
   }
+  }   // warp < 4
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -306,13 +373,34 @@ int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t row
   return r == CUDA_SUCCESS ? 0 : -3;
 }
 
+// 2D e4m3 (byte) tensor map over rows of `inner` bytes, box of 64 x box_rows,
+// no swizzle (the converters place the bytes).
+int tc_make_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return -1;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || inner % 16 || inner % TC_BK) return -2;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {(cuuint32_t)TC_BK, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -3;
+}
+
 }  // namespace spec
 
 // ---------------------------------------------------------------------------
 // Kernel-level entry point (tests and tools): with X = B (+ B_lo when given),
 // out[n][m] = sum_k A[m][k] X[n][k] (dual = 0) or
 // out_bf16[n][m] = silu(A[m]·X[n]) * (A2[m]·X[n]) (dual = 1).
-extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const void* b_dev, const void* b_lo_dev,
+// Kernel-level entry point (tests and tools): with X = B (+ B_lo when given)
+// and weights A (bf16, or e4m3 when a_fp8, times the per-row scales),
+// out[n][m] = sum_k A[m][k] X[n][k] (dual = 0) or
+// out_bf16[n][m] = silu(A[m]·X[n]) * (A2[m]·X[n]) (dual = 1).
+extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const float* a_scale_dev,
+                                 const float* a2_scale_dev, int a_fp8, const void* b_dev, const void* b_lo_dev,
                                  int M, int N, int K, int dual, void* out_dev, int* err_dev, uintptr_t cuda_stream) {
   using namespace spec;
   if (!a_dev || !b_dev || !out_dev || !err_dev || (dual && !a2_dev)) return set_last_error(-1, "null pointer");
@@ -324,8 +412,12 @@ extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const vo
   }
   TcMaps maps;
   maps.dual = dual;
-  if (tc_make_map(&maps.a, a_dev, K, M, TC_BM) || (dual && tc_make_map(&maps.a2, a2_dev, K, M, TC_BM)) ||
-      tc_make_map(&maps.b, b_dev, K, N, TC_NSUB) || (b_lo_dev && tc_make_map(&maps.blo, b_lo_dev, K, N, TC_NSUB)))
+  maps.f8 = a_fp8 ? 1 : 0;
+  auto amap = [&](CUtensorMap* mp, const void* p) {
+    return a_fp8 ? tc_make_map_u8(mp, p, K, M, TC_BM) : tc_make_map(mp, p, K, M, TC_BM);
+  };
+  if (amap(&maps.a, a_dev) || (dual && amap(&maps.a2, a2_dev)) || tc_make_map(&maps.b, b_dev, K, N, TC_NSUB) ||
+      (b_lo_dev && tc_make_map(&maps.blo, b_lo_dev, K, N, TC_NSUB)))
     return set_last_error(-6, "tensor map encoding failed");
   if (!dual) maps.a2 = maps.a;
   if (!b_lo_dev) maps.blo = maps.b;
@@ -333,6 +425,8 @@ extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const vo
   P.K = K; P.Mg = M; P.N = N; P.ldo = M; P.epi = dual ? TC_SWIGLU : TC_STORE;
   P.out_f32 = dual ? nullptr : reinterpret_cast<float*>(out_dev);
   P.out_bf16 = dual ? reinterpret_cast<uint16_t*>(out_dev) : nullptr;
+  P.scale = a_scale_dev;
+  P.scale2 = a2_scale_dev;
   P.err = err_dev;
   P.split = b_lo_dev != nullptr;
   launch_tc_gemm(maps, P, M / TC_BM, 1, (N + TC_MAXN - 1) / TC_MAXN, reinterpret_cast<cudaStream_t>(cuda_stream));
@@ -343,17 +437,26 @@ extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const vo
 namespace spec {
 
 cudaError_t configure_tc_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(k_tc_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem_bytes(0));
-  cudaError_t f = cudaFuncSetAttribute(k_tc_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem_bytes(1));
-  return e != cudaSuccess ? e : f;
+  cudaError_t e = cudaSuccess, r;
+#define ALLOW(D, F)                                                                                        \
+  if ((r = cudaFuncSetAttribute(k_tc_gemm<D, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,             \
+                                tc_smem_bytes(D, F))) != cudaSuccess)                                      \
+    e = r
+  ALLOW(0, 0); ALLOW(1, 0); ALLOW(0, 1); ALLOW(1, 1);
+#undef ALLOW
+  return e;
 }
 
 void launch_tc_gemm(const TcMaps& maps, const TcParams& P, int m_tiles, int groups, int n_tiles, cudaStream_t st) {
-  const dim3 grid(m_tiles, groups, n_tiles), blk(128);
-  if (maps.dual)
-    k_tc_gemm<1><<<grid, blk, tc_smem_bytes(1), st>>>(maps.a, maps.a2, maps.b, maps.blo, P);
-  else
-    k_tc_gemm<0><<<grid, blk, tc_smem_bytes(0), st>>>(maps.a, maps.a, maps.b, maps.blo, P);
+  const dim3 grid(m_tiles, groups, n_tiles);
+  const CUtensorMap& a2 = maps.dual ? maps.a2 : maps.a;
+  if (maps.f8) {
+    if (maps.dual) k_tc_gemm<1, 1><<<grid, tc_threads(1), tc_smem_bytes(1, 1), st>>>(maps.a, a2, maps.b, maps.blo, P);
+    else k_tc_gemm<0, 1><<<grid, tc_threads(1), tc_smem_bytes(0, 1), st>>>(maps.a, a2, maps.b, maps.blo, P);
+  } else {
+    if (maps.dual) k_tc_gemm<1, 0><<<grid, tc_threads(0), tc_smem_bytes(1, 0), st>>>(maps.a, a2, maps.b, maps.blo, P);
+    else k_tc_gemm<0, 0><<<grid, tc_threads(0), tc_smem_bytes(0, 0), st>>>(maps.a, a2, maps.b, maps.blo, P);
+  }
 }
 
 }  // namespace spec

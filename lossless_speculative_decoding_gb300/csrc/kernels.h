@@ -151,11 +151,13 @@ struct TcParams {
 struct TcMaps {
   CUtensorMap a, a2, b, blo;   // weights, second weights (dual), activations hi, lo
   int dual;
+  int f8 = 0;                  // weights are e4m3 (maps from tc_make_map_u8)
 };
 
 // 2D bf16 tensor map: rows of `inner` elements, box 64 x box_rows, 128-byte
 // swizzle. Returns 0 on success.
 int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+int tc_make_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 void launch_tc_gemm(const TcMaps& maps, const TcParams& P, int m_tiles, int groups, int n_tiles, cudaStream_t st);
 cudaError_t configure_tc_kernels();
 void launch_norm_bf16(const Dims& D, const float* x, const float* gamma, uint16_t* out, uint16_t* out_lo, int T,

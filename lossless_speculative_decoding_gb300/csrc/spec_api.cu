@@ -220,21 +220,23 @@ struct spec_model {
   // Tensor-core GEMM launches. Dense: one group covering T rows. Grouped: the
   // active-expert list of the step (rows of the permuted operand).
   void tc_dense(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, int K, int M, int T, int epi,
-                float* out, int ldo) {
+                float* out, int ldo, const float* scale = nullptr) {
     TcMaps mp;
-    mp.a = a; mp.a2 = a; mp.b = b; mp.blo = blo; mp.dual = 0;
+    mp.a = a; mp.a2 = a; mp.b = b; mp.blo = blo; mp.dual = 0; mp.f8 = scale != nullptr;
     TcParams P = {};
     P.K = K; P.Mg = M; P.N = T; P.ldo = ldo; P.epi = epi; P.out_f32 = out; P.err = S.err; P.split = 1;
+    P.scale = scale;
     if (epi == TC_ARGMAX) { P.am_val = B.am_val; P.am_idx = B.am_idx; P.am_ld = M / 128; }
     launch_tc_gemm(mp, P, M / 128, 1, (T + 127) / 128, stream);
   }
   void tc_grouped(const CUtensorMap& a, const CUtensorMap* a2, const CUtensorMap& b, const CUtensorMap& blo, int K,
-                  int Mg, int T, int epi, float* out_f32, uint16_t* out_bf16, uint16_t* out_lo, int ldo) {
+                  int Mg, int T, int epi, float* out_f32, uint16_t* out_bf16, uint16_t* out_lo, int ldo,
+                  const float* scale = nullptr, const float* scale2 = nullptr) {
     TcMaps mp;
-    mp.a = a; mp.a2 = a2 ? *a2 : a; mp.b = b; mp.blo = blo; mp.dual = a2 ? 1 : 0;
+    mp.a = a; mp.a2 = a2 ? *a2 : a; mp.b = b; mp.blo = blo; mp.dual = a2 ? 1 : 0; mp.f8 = scale != nullptr;
     TcParams P = {};
     P.K = K; P.Mg = Mg; P.N = T; P.ldo = ldo; P.epi = epi; P.out_f32 = out_f32; P.out_bf16 = out_bf16;
-    P.out_bf16_lo = out_lo; P.split = 1;
+    P.out_bf16_lo = out_lo; P.split = 1; P.scale = scale; P.scale2 = scale2;
     P.perm = B.perm; P.err = S.err;
     P.g_expert = B.act_expert; P.g_off = B.act_off; P.g_cnt = B.act_cnt; P.g_n = B.n_active;
     const int max_active = (D.E > 0 ? std::min(D.E, T * D.k) : 0) + D.S;
@@ -252,22 +254,23 @@ struct spec_model {
         const TcLayer& M = tcl[l];
         run_k(p, KC_QKV, [&] {
           launch_norm_bf16(D, cur, W.attn_norm, B.xn_bf16, B.xn_lo, T, stream);
-          tc_dense(M.qkv, tc_xn, tc_xn_lo, D.h, qkv_rows, T, TC_STORE, B.qkv, qkv_rows);
+          tc_dense(M.qkv, tc_xn, tc_xn_lo, D.h, qkv_rows, T, TC_STORE, B.qkv, qkv_rows, W.s_qkv);
           launch_rope_kv(D, S, B, l, T, stream);
         });
         run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, stream); });
-        run_k(p, KC_OPROJ, [&] { tc_dense(M.o, tc_o, tc_o_lo, D.Hq * D.d, D.h, T, TC_ADD, cur, D.h); });
+        run_k(p, KC_OPROJ, [&] { tc_dense(M.o, tc_o, tc_o_lo, D.Hq * D.d, D.h, T, TC_ADD, cur, D.h, W.s_o); });
         run_k(p, KC_ROUTER, [&] {
           launch_router(D, B, W, T, cur, true, stream);
           launch_gather_bf16(D, B, T, stream);
         });
         run_k(p, KC_GATEUP, [&] {
           tc_grouped(M.gate, &M.up, tc_xperm, tc_xperm_lo, D.h, D.inter, T, TC_SWIGLU, nullptr, B.hperm, B.hperm_lo,
-                     D.inter);
+                     D.inter, W.s_gate, W.s_up);
         });
         if (p) cudaMemcpyAsync(p->act + p->nact++, B.n_active, 4, cudaMemcpyDeviceToHost, stream);
         run_k(p, KC_DOWN, [&] {
-          tc_grouped(M.down, nullptr, tc_hperm, tc_hperm_lo, D.inter, D.h, T, TC_SCATTER, B.y, nullptr, nullptr, D.h);
+          tc_grouped(M.down, nullptr, tc_hperm, tc_hperm_lo, D.inter, D.h, T, TC_SCATTER, B.y, nullptr, nullptr, D.h,
+                     W.s_down);
         });
         run_k(p, KC_COMBINE, [&] { launch_combine(D, B, cur, T, stream); });
         continue;
@@ -471,12 +474,12 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
       (rc = m->dalloc(&B.am_val, (size_t)T * B.n_vblocks)) || (rc = m->dalloc(&B.am_idx, (size_t)T * B.n_vblocks)) ||
       (rc = m->dalloc(&B.g, T)))
     return rc;
-  // tensor-core path: bf16 weights with more than 8 rows per verify step
+  // tensor-core path: bf16 or e4m3 weights with more than 8 rows per verify step
   {
     const int qkv_rows = (D.Hq + 2 * D.Hkv) * D.d;
     const bool shapes = D.h % 128 == 0 && qkv_rows % 128 == 0 && D.inter % 128 == 0 && D.V % 128 == 0 &&
                         (D.Hq * D.d) % 64 == 0 && D.h % 64 == 0 && D.inter % 64 == 0;
-    m->use_tc = c.wdtype == SPEC_BF16 && c.max_batch * m->R > 8 && shapes;
+    m->use_tc = (c.wdtype == SPEC_BF16 || c.wdtype == SPEC_FP8) && c.max_batch * m->R > 8 && shapes;
   }
   if (m->use_tc) {
     const int qkv_rows = (D.Hq + 2 * D.Hkv) * D.d;
@@ -490,14 +493,16 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
     const int F = D.E + D.S;
     m->tcl.resize(D.L);
     int bad = 0;
+    // weight maps: bf16 (128-byte swizzle) or e4m3 (unswizzled bytes, widened in the kernel)
+    auto wmap = c.wdtype == SPEC_FP8 ? tc_make_map_u8 : tc_make_map;
     for (int l = 0; l < D.L; ++l) {
       const LayerW& W = m->layers[l];
       auto& M = m->tcl[l];
-      bad |= tc_make_map(&M.qkv, W.w_qkv, D.h, qkv_rows, 128);
-      bad |= tc_make_map(&M.o, W.w_o, (uint64_t)D.Hq * D.d, D.h, 128);
-      bad |= tc_make_map(&M.gate, W.w_gate, D.h, (uint64_t)F * D.inter, 128);
-      bad |= tc_make_map(&M.up, W.w_up, D.h, (uint64_t)F * D.inter, 128);
-      bad |= tc_make_map(&M.down, W.w_down, D.inter, (uint64_t)F * D.h, 128);
+      bad |= wmap(&M.qkv, W.w_qkv, D.h, qkv_rows, 128);
+      bad |= wmap(&M.o, W.w_o, (uint64_t)D.Hq * D.d, D.h, 128);
+      bad |= wmap(&M.gate, W.w_gate, D.h, (uint64_t)F * D.inter, 128);
+      bad |= wmap(&M.up, W.w_up, D.h, (uint64_t)F * D.inter, 128);
+      bad |= wmap(&M.down, W.w_down, D.inter, (uint64_t)F * D.h, 128);
     }
     bad |= tc_make_map(&m->tc_lm, m->lm_head, D.h, D.V, 128);
     bad |= tc_make_map(&m->tc_xn, B.xn_bf16, D.h, T, 32);

@@ -310,7 +310,7 @@ def test_mid_size_lossless_and_parity():
     assert row_tol_ok(lg, ol, 2e-2).all()
 
 
-@pytest.mark.parametrize("cfg,K,nseq", [(MOE_SMALL, 3, 3), (DENSE_SMALL, 31, 1)])
+@pytest.mark.parametrize("cfg,K,nseq", [(MOE_SMALL, 3, 3), (MOE_SMALL_FP8, 3, 3), (DENSE_SMALL, 31, 1)])
 def test_tensor_core_path_parity_and_invariance(cfg, K, nseq):
     """Models with more than 8 rows per step run every projection on the
     tcgen05 GEMM. Verify rows match the oracle within 2e-2 of each row's

@@ -83,3 +83,44 @@ def test_tc_gemm_split_activations(M, N, K):
     # hi + lo carries ~16 mantissa bits (relative residual <= 2^-17); bf16
     # alone would leave errors near 2^-9 of the row scale
     np.testing.assert_allclose(got, ref, rtol=0, atol=5e-5 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("M,N,K,dual", [(256, 40, 320, 0), (128, 200, 1280, 0), (256, 48, 192, 1), (128, 130, 896, 1)])
+def test_tc_gemm_fp8_weights(M, N, K, dual):
+    """e4m3 weights widened to bf16 in shared memory, per-row scales applied in
+    the epilogue: against float64 of the decoded e4m3 values times the scales."""
+    import torch
+    from lossless_speculative_decoding_gb300 import binding as B
+    rng = np.random.default_rng(5 * M + N + dual)
+
+    def q8(shape):
+        w = (rng.standard_normal(shape) * 0.05).astype(np.float32)
+        codes, sc = syn.quantize_rows_e4m3(w)
+        return codes, sc, oracle.decode_e4m3(codes).astype(np.float64) * sc[:, None].astype(np.float64)
+
+    c1, s1, w1 = q8((M, K))
+    c2, s2, w2 = q8((M, K))
+    x = rng.standard_normal((N, K)).astype(np.float32)
+    hi = syn.f32_to_bf16_bits(x)
+    lo = syn.f32_to_bf16_bits((x - oracle.decode_bf16(hi)).astype(np.float32))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    a, a2, sa, sa2 = dev(c1.view(np.int8)), dev(c2.view(np.int8)), dev(s1), dev(s2)
+    bh, bl = dev(hi.view(np.int16)), dev(lo.view(np.int16))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if dual:
+        out = torch.zeros((N, M), dtype=torch.int16, device="cuda")
+        B.spec_tc_gemm_test(a, a2, bh, bl, M, N, K, 1, out, err, 0, a_scale_dev=sa, a2_scale_dev=sa2, a_fp8=True)
+    else:
+        out = torch.full((N, M), float("nan"), device="cuda")
+        B.spec_tc_gemm_test(a, None, bh, bl, M, N, K, 0, out, err, 0, a_scale_dev=sa, a_fp8=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    xf = x.astype(np.float64)
+    if dual:
+        gg, uu = xf @ w1.T, xf @ w2.T
+        ref = gg / (1 + np.exp(-gg)) * uu
+        got = oracle.decode_bf16(out.cpu().numpy().view(np.uint16)).astype(np.float64)
+        np.testing.assert_allclose(got, ref, rtol=1e-2, atol=1e-2 * np.abs(ref).max())
+    else:
+        ref = xf @ w1.T
+        np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=0, atol=5e-5 * np.abs(ref).max())
