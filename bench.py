@@ -155,7 +155,7 @@ def class_bytes(cfg, stats: dict, T: int, ctx_sum: float, n_steps: int) -> dict:
     u = lambda k: stats.get(k, {}).get("units", 0)
     out["qkv_rope_kvwrite"] = n("qkv_rope_kvwrite") * (cfg.qkv_rows * (h * we + sc) + T * h * 4 + T * cfg.n_q_heads * d * 4
                                                        + T * 2 * cfg.n_kv_heads * d * kve)
-    out["attn_splitkv"] = L * ctx_sum * 2 * cfg.n_kv_heads * d * kve
+    out["attn_splitkv_merge"] = L * ctx_sum * 2 * cfg.n_kv_heads * d * kve
     out["oproj_residual"] = n("oproj_residual") * (h * (cfg.n_q_heads * d * we + sc) + 2 * T * h * 4 + T * cfg.n_q_heads * d * 4)
     out["router_topk_permute"] = n("router_topk_permute") * (cfg.n_experts * h * se + 2 * T * h * 4)
     out["expert_gateup_swiglu"] = u("expert_gateup_swiglu") * 2 * cfg.inter * (h * we + sc) + \

@@ -246,8 +246,7 @@ cudaError_t configure_small_kernels() {
 
 void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, const float* xres, bool full,
                    cudaStream_t st) {
-  const int E1 = D.E > 0 ? D.E : 1;
-  const size_t perm_words = (size_t)T * D.k + 2 * E1;
+  const size_t perm_words = (size_t)T * D.k + permute_scratch_words(D.E, T * D.k);
   const dim3 grid(T, D.E > 0 ? (D.E + RT_EXPERTS - 1) / RT_EXPERTS : 1);
   if (!full && T <= RT_SMALL_T) {
     const size_t sm = (size_t)D.h * sizeof(float);

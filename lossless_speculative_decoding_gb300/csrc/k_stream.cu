@@ -236,7 +236,7 @@ __device__ __forceinline__ void route_in_block(const Dims& D, const StepBuf& B, 
 // Shared-memory words of the gate/up kernel: active list (+ routing scratch).
 __host__ __device__ inline int gateup_words(const Dims& D, int T, int max_active, bool route) {
   int w = ActCache::words(max_active, T * D.NS);
-  if (route) w += T * D.E + 2 * T * D.k + 2 * (D.E > 0 ? D.E : 1);
+  if (route) w += T * D.E + 2 * T * D.k + permute_scratch_words(D.E, T * D.k);
   return w;
 }
 

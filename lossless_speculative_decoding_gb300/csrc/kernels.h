@@ -7,6 +7,7 @@
 namespace spec {
 
 constexpr int ATT_CHUNK = 64;     // keys per split-KV chunk (fixed at absolute positions)
+constexpr int ATT_MAX_GROUPS = 1024;   // row groups (sequence slices of <= 32 rows) per attention launch
 constexpr int GEMV_TP = 4;        // activation rows per GEMV pass
 constexpr int GEMV_WARPS = 8;     // warps per GEMV block
 constexpr int GEMV_G = 4;         // 16-byte weight chunks loaded per lane before use
@@ -98,6 +99,8 @@ void launch_assemble_prefill(const Dims& D, const DevState& S, const StepBuf& B,
                              const void* vis, int seq, int pos0, int T, cudaStream_t st);
 void launch_qkv(const Dims& D, const DevState& S, const StepBuf& B, const LayerW& W, int layer, int T,
                 const float* x, cudaStream_t st);
+bool attn_separate_merge(const Dims& D, int R);   // merge as its own launch (many pairs per group)
+int attn_groups(int T, int R);
 void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
                       cudaStream_t st);
 void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, float* xres, cudaStream_t st);

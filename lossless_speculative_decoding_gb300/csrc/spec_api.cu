@@ -373,6 +373,9 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
   m->R = c.max_draft + 1;
   m->prefill_chunk = c.prefill_chunk > 0 ? c.prefill_chunk : 256;
   m->Tmax = std::max(c.max_batch * m->R, m->prefill_chunk);
+  if (attn_groups(c.max_batch * m->R, m->R) > ATT_MAX_GROUPS ||
+      attn_groups(m->prefill_chunk, m->prefill_chunk) > ATT_MAX_GROUPS)
+    return fail(SPEC_ERR_ARG, "max_batch x ceil((max_draft + 1) / 32) exceeds the attention group limit");
   Dims& D = m->D;
   D.L = c.n_layers; D.h = c.hidden; D.Hq = c.n_q_heads; D.Hkv = c.n_kv_heads; D.d = c.head_dim;
   D.E = c.n_experts; D.k = c.top_k; D.S = c.n_shared; D.inter = c.inter; D.V = c.vocab;
@@ -943,9 +946,10 @@ int spec_free_pages(spec_model* m) {
 
 int spec_step_launches(spec_model* m, int n_seq) {
   if (!m || n_seq < 1) return fail(SPEC_ERR_ARG, "bad arguments");
+  const int merge = attn_separate_merge(m->D, m->R) ? m->D.L : 0;   // + the standalone attention merges
   if (m->use_tc)   // per layer: norm, QKV, RoPE/KV, attention, O, router, gather, gate/up, down, combine
-    return 1 + m->D.L * 10 + 3;
-  return launches_per_step(m->D, n_seq * m->R);
+    return 1 + m->D.L * 10 + 3 + merge;
+  return launches_per_step(m->D, n_seq * m->R) + merge;
 }
 
 // ---- host-only allocator entry points --------------------------------------
