@@ -351,4 +351,144 @@ __device__ __forceinline__ void row_inv_rms(const float* x, int T, int K, float 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Warp tensor-core GEMV (bf16 / e4m3 weights, at most 8 activation columns):
+// mma.sync m16n8k16 with A = 16 weight rows, B = 8 columns (tokens or routed
+// pairs), C = fp32. Lane (g, q) = (lane / 4, lane % 4) streams 16 contiguous
+// bytes of weight rows g and g + 8 per step -- 8 bf16 (or 16 e4m3 widened to
+// bf16) at k = kb + EPL * q -- and those bytes are the lane's A fragment as
+// they are: the MMA's K slots are a permutation of the step's k values, and
+// the B fragment (column g's activations at the same k) uses the same one.
+// For MMA j of a 8-element group starting at k0: A slots (2q, 2q+1) <- k0 +
+// 4j + {0,1}, slots (2q+8, 2q+9) <- k0 + 4j + {2,3}. Activations are fp32,
+// split into bf16 hi + lo (two MMAs, two accumulators added at the end), so
+// a column's result keeps near-fp32 precision and depends only on that
+// column's own inputs. Result: c[0], c[1] = rows g x columns 2q, 2q+1;
+// c[2], c[3] = rows g + 8 x the same columns.
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// x, y -> bf16x2 hi = (bf16(x), bf16(y)) and lo = (bf16(x - hi.x), bf16(y - hi.y)),
+// x in the low half (the lower k index).
+__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(y), "f"(x));
+  const float xh = __uint_as_float(hi << 16), yh = __uint_as_float(hi & 0xFFFF0000u);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(y - yh), "f"(x - xh));
+}
+
+// Eight e4m3 values (two 32-bit words) -> four bf16x2 words, exactly.
+__device__ __forceinline__ void e4m3x8_bf16(uint32_t w0, uint32_t w1, uint32_t (&o)[4]) {
+  const uint32_t w[2] = {w0, w1};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[i] >> (16 * h)) & 0xFFFF), __NV_E4M3);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+      o[2 * i + h] = (__float_as_uint(f.x) >> 16) | (__float_as_uint(f.y) & 0xFFFF0000u);
+    }
+  }
+}
+
+template <class WT> struct MmaStep;                   // k values one step covers (4 lanes x EPL)
+template <> struct MmaStep<bf16_t> { static constexpr int EPL = 8, K = 32; };
+template <> struct MmaStep<fp8_t> { static constexpr int EPL = 16, K = 64; };
+
+// Two MMAs (hi, lo) of one 8-element group: weights wa (row g) / wb (row g+8)
+// as four bf16x2 words, activations x[0..8) of column g at the group's k.
+__device__ __forceinline__ void mma_group8(float (&ch)[4], float (&cl)[4], const uint32_t (&wa)[4],
+                                           const uint32_t (&wb)[4], const float4& x0, const float4& x1) {
+  uint32_t h0, l0, h1, l1;
+  split_bf16x2(x0.x, x0.y, h0, l0);
+  split_bf16x2(x0.z, x0.w, h1, l1);
+  mma16816(ch, wa[0], wb[0], wa[1], wb[1], h0, h1);
+  mma16816(cl, wa[0], wb[0], wa[1], wb[1], l0, l1);
+  split_bf16x2(x1.x, x1.y, h0, l0);
+  split_bf16x2(x1.z, x1.w, h1, l1);
+  mma16816(ch, wa[2], wb[2], wa[3], wb[3], h0, h1);
+  mma16816(cl, wa[2], wb[2], wa[3], wb[3], l0, l1);
+}
+
+// Block-split units: the 8 warps of a block share one 16-row unit and split
+// its K steps -- warp w takes steps w, w + 8, w + 16, ... -- in batches of NB
+// steps whose loads are all in flight at once; block_sum4 then adds the
+// warps' partial c[4] in warp order (a fixed order) for warp 0.
+template <class WT, int NB>
+__device__ __forceinline__ void mma_load_batch(uint4 (&va)[NB], uint4 (&vb)[NB], const WT* wlo, const WT* whi,
+                                               int K, int s0) {
+  constexpr int SK = MmaStep<WT>::K, EPL = MmaStep<WT>::EPL;
+  const int q = threadIdx.x & 3, nsteps = K / SK;
+#pragma unroll
+  for (int u = 0; u < NB; ++u) {
+    const int st = s0 + 8 * u;
+    const int k = st * SK + EPL * q;
+    va[u] = st < nsteps ? ld_stream(wlo + k) : make_uint4(0, 0, 0, 0);
+    vb[u] = st < nsteps ? ld_stream(whi + k) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// This warp's partial c[4] of the unit (weight rows g / g + 8 against column
+// x, nullptr = zeros). va/vb hold the warp's first batch on entry
+// (mma_load_batch at s0 = warp).
+template <class WT, int NB>
+__device__ __forceinline__ void mma_part(uint4 (&va)[NB], uint4 (&vb)[NB], const WT* wlo, const WT* whi, int K,
+                                         const float* x, float (&c)[4]) {
+  constexpr int SK = MmaStep<WT>::K, EPL = MmaStep<WT>::EPL;
+  const int q = threadIdx.x & 3, w = threadIdx.x >> 5, nsteps = K / SK;
+  float ch[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s0 = w; s0 < nsteps; s0 += 8 * NB) {
+    if (s0 != w) mma_load_batch<WT, NB>(va, vb, wlo, whi, K, s0);
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      const int st = s0 + 8 * u;
+      if (st < nsteps) {
+        const int k = st * SK + EPL * q;
+#pragma unroll
+        for (int h = 0; h < EPL / 8; ++h) {
+          uint32_t wa[4], wb[4];
+          if constexpr (EPL == 8) {
+            wa[0] = va[u].x; wa[1] = va[u].y; wa[2] = va[u].z; wa[3] = va[u].w;
+            wb[0] = vb[u].x; wb[1] = vb[u].y; wb[2] = vb[u].z; wb[3] = vb[u].w;
+          } else {
+            e4m3x8_bf16(h ? va[u].z : va[u].x, h ? va[u].w : va[u].y, wa);
+            e4m3x8_bf16(h ? vb[u].z : vb[u].x, h ? vb[u].w : vb[u].y, wb);
+          }
+          float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+          if (x != nullptr) {
+            x0 = *reinterpret_cast<const float4*>(x + k + 8 * h);
+            x1 = *reinterpret_cast<const float4*>(x + k + 8 * h + 4);
+          }
+          mma_group8(ch, cl, wa, wb, x0, x1);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = ch[i] + cl[i];
+}
+
+// Sum of the 8 warps' c[4] in warp order into warp 0's c (one barrier). red:
+// shared [2][8][32] float4, alternated by the caller's unit parity, so the
+// next unit's writes never meet warp 0's reads of this one.
+__device__ __forceinline__ void block_sum4(float (&c)[4], float4* red, int parity) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float4* r = red + parity * 256;
+  r[w * 32 + lane] = make_float4(c[0], c[1], c[2], c[3]);
+  __syncthreads();
+  if (w == 0) {
+    float4 t = r[lane];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+      const float4 v = r[i * 32 + lane];
+      t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+    }
+    c[0] = t.x; c[1] = t.y; c[2] = t.z; c[3] = t.w;
+  }
+}
+
 }  // namespace spec

@@ -518,6 +518,434 @@ __global__ void __launch_bounds__(256, SBPS) k_lmhead_s(Dims D, DevState S, Step
   for (int s = threadIdx.x; s < n_seq; s += blockDim.x) commit_seq(D, S, B, s, K, B.g);
 }
 
+// ===========================================================================
+// Tensor-core forms (bf16 / e4m3 weights): a block takes one unit of 16
+// weight rows at a time against up to 8 columns through mma.sync, its 8
+// warps splitting the unit's K steps (mma_part), and block_sum4 adds the
+// warps' parts in a fixed order for warp 0, which runs the epilogue. A warp's
+// loads of its K slice are all in flight at once, and the next unit's loads
+// are issued before the current unit's reduction. Columns are activation rows
+// (tokens) or, in the expert kernels, routed pairs; more than 8 (a prefill
+// chunk) are taken in passes of 8 over the same weights.
+constexpr int MNB = 5;           // K steps per warp in flight
+constexpr int MC = 8;            // columns per pass
+
+// normalised rows [t0, t0 + n) of x into xs[MC][K + 4] (zeros past n); the
+// 4-float pad keeps the lanes' float4 reads on distinct banks
+__device__ __forceinline__ void stage_cols(float* xs, const float* x, int t0, int n, int K, const float* inv,
+                                           const float* gamma) {
+  const int K4 = K / 4, ld4 = K4 + 1;
+  for (int i = threadIdx.x; i < MC * K4; i += blockDim.x) {
+    const int t = i / K4, k4 = i % K4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < n) {
+      v = reinterpret_cast<const float4*>(x + (size_t)(t0 + t) * K)[k4];
+      if (gamma != nullptr) {
+        const float sc = inv[t0 + t];
+        const float4 g = reinterpret_cast<const float4*>(gamma)[k4];
+        v = make_float4((v.x * sc) * g.x, (v.y * sc) * g.y, (v.z * sc) * g.z, (v.w * sc) * g.w);
+      }
+    }
+    reinterpret_cast<float4*>(xs)[t * ld4 + k4] = v;
+  }
+}
+
+// QKV + RoPE + paged KV write. Unit = rows i0..i0+7 (first half of a head)
+// and i0+d/2..i0+d/2+7 (their rotary partners): lane (g, q) of warp 0 holds
+// both values of rotary pair i0 + g for columns 2q, 2q+1.
+template <class WT>
+__global__ void __launch_bounds__(256, SBPS) k_qkv_m(Dims D, DevState S, StepBuf B, const float* __restrict__ gamma,
+                                                     const WT* __restrict__ W, const float* __restrict__ scale,
+                                                     int layer, int T, const float* x) {
+  extern __shared__ __align__(16) float sm[];
+  __shared__ float4 red[512];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const int half = D.d / 2, upu = half / 8;
+  const int nunits = (D.Hq + 2 * D.Hkv) * upu;
+  const int npass = cdiv(T, MC);
+  float* inv = sm;
+  float* xs = sm + ((T + 3) & ~3);
+  uint4 va[MNB], vb[MNB];
+  const WT *wlo = W, *whi = W;
+  auto set_rows = [&](int unit) {
+    const int base = (unit / upu) * D.d + (unit % upu) * 8 + g;
+    wlo = W + (size_t)base * D.h;
+    whi = W + (size_t)(base + half) * D.h;
+  };
+  if ((int)blockIdx.x < nunits) {
+    set_rows(blockIdx.x);
+    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp);
+  }
+  pdl_wait();
+  pdl_trigger();
+  row_inv_rms(x, T, D.h, D.eps, inv);
+  __syncthreads();
+  int par = 0;
+  for (int pass = 0; pass < npass; ++pass) {
+    const int t0 = pass * MC, nvalid = min(MC, T - t0);
+    if (pass > 0) __syncthreads();
+    stage_cols(xs, x, t0, nvalid, D.h, inv, gamma);
+    __syncthreads();
+    for (int unit = blockIdx.x; unit < nunits; unit += gridDim.x) {
+      const int head = unit / upu, j = (unit % upu) * 8 + g;       // rotary frequency index
+      float c[4];
+      mma_part<WT, MNB>(va, vb, wlo, whi, D.h, g < nvalid ? xs + g * (D.h + 4) : nullptr, c);
+      const int nx = unit + (int)gridDim.x < nunits ? unit + gridDim.x : (pass + 1 < npass ? (int)blockIdx.x : -1);
+      if (nx >= 0) {
+        set_rows(nx);
+        mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp);
+      }
+      block_sum4(c, red, par);
+      par ^= 1;
+      if (warp != 0) continue;
+      float a[2] = {c[0], c[1]}, b[2] = {c[2], c[3]};            // first / second half, columns 2q, 2q+1
+      if (scale != nullptr) {
+        const float sa = scale[head * D.d + j], sb = scale[head * D.d + j + half];
+        a[0] *= sa; a[1] *= sa; b[0] *= sb; b[1] *= sb;
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int col = 2 * q + e;
+        if (col >= nvalid) continue;
+        const int row = t0 + col;
+        const int pos = B.row_pos[row];
+        if (pos < 0 || pos >= D.max_ctx) { atomicOr(S.err, DERR_POS); continue; }
+        float o0 = a[e], o1 = b[e];
+        if (head < D.Hq + D.Hkv) {
+          const float cs = S.rope_cos[(size_t)pos * half + j], sn = S.rope_sin[(size_t)pos * half + j];
+          o0 = a[e] * cs - b[e] * sn;
+          o1 = b[e] * cs + a[e] * sn;
+        }
+        if (head < D.Hq) {
+          float* qd = B.q + ((size_t)row * D.Hq + head) * D.d;
+          qd[j] = o0;
+          qd[j + half] = o1;
+          continue;
+        }
+        const int is_v = head >= D.Hq + D.Hkv;
+        const int hk = head - D.Hq - (is_v ? D.Hkv : 0);
+        const int pi = pos / D.P;
+        const int page = pi < D.max_pages ? S.bt[(size_t)B.row_seq[row] * D.max_pages + pi] : -1;
+        if (page < 0) { atomicOr(S.err, DERR_PAGE); continue; }
+        const size_t off = (size_t)page * D.page_elems +
+                           ((((size_t)layer * 2 + is_v) * D.Hkv + hk) * D.P + (pos % D.P)) * D.d + j;
+        reinterpret_cast<uint16_t*>(S.kv)[off] = f_to_bf16(o0);
+        reinterpret_cast<uint16_t*>(S.kv)[off + half] = f_to_bf16(o1);
+      }
+    }
+  }
+}
+
+// Output projection + residual: x[t][o] += sum_k W_o[o][k] * attn[t][k].
+template <class WT>
+__global__ void __launch_bounds__(256, SBPS) k_oproj_m(Dims D, StepBuf B, const WT* __restrict__ W,
+                                                       const float* __restrict__ scale, int T, float* xres) {
+  __shared__ float4 red[512];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const int K = D.Hq * D.d;
+  const int npass = cdiv(T, MC);
+  const int nitems = (D.h / 16) * npass;
+  uint4 va[MNB], vb[MNB];
+  const WT *wlo = W, *whi = W;
+  auto set_rows = [&](int item) {
+    const int o = (item / npass) * 16 + g;
+    wlo = W + (size_t)o * K;
+    whi = W + (size_t)(o + 8) * K;
+  };
+  int it = blockIdx.x;
+  if (it < nitems) {
+    set_rows(it);
+    mma_load_batch<WT, MNB>(va, vb, wlo, whi, K, warp);
+  }
+  pdl_wait();
+  pdl_trigger();
+  int par = 0;
+  for (; it < nitems; it += gridDim.x) {
+    const int o = (it / npass) * 16 + g, t0 = (it % npass) * MC, nvalid = min(MC, T - t0);
+    float c[4];
+    mma_part<WT, MNB>(va, vb, wlo, whi, K, g < nvalid ? B.o + (size_t)(t0 + g) * K : nullptr, c);
+    if (it + (int)gridDim.x < nitems) {
+      set_rows(it + gridDim.x);
+      mma_load_batch<WT, MNB>(va, vb, wlo, whi, K, warp);
+    }
+    block_sum4(c, red, par);
+    par ^= 1;
+    if (warp != 0) continue;
+    const float s0 = scale != nullptr ? scale[o] : 1.f, s1 = scale != nullptr ? scale[o + 8] : 1.f;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int col = 2 * q + e;
+      if (col >= nvalid) continue;
+      float* xr = xres + (size_t)(t0 + col) * D.h;
+      xr[o] += c[e] * s0;
+      xr[o + 8] += c[2 + e] * s1;
+    }
+  }
+}
+
+// Expert gate/up + SwiGLU. Items: (active slot, gate/up rows j..j+7, pass of
+// 8 routed pairs); lanes of warp 0 hold gate row j+g and up row j+g of their
+// columns.
+template <class WT>
+__global__ void __launch_bounds__(256, SBPS) k_gateup_m(Dims D, StepBuf B, const WT* __restrict__ Wg,
+                                                        const float* __restrict__ sg, const WT* __restrict__ Wu,
+                                                        const float* __restrict__ su, int T, int max_active,
+                                                        int route) {
+  extern __shared__ __align__(16) int smi[];
+  __shared__ float4 red[512];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const int npass = cdiv(T, MC);
+  const int upe = D.inter / 8;
+  const int per_slot = upe * npass;
+  const int stride = gridDim.x;
+  const ActCache A(smi, max_active, T * D.NS);
+  uint4 va[MNB], vb[MNB];
+  const WT *wlo = Wg, *whi = Wu;
+  auto set_rows_e = [&](int e, int it) {
+    const size_t r = (size_t)e * D.inter + ((it % per_slot) / npass) * 8 + g;
+    wlo = Wg + r * D.h;
+    whi = Wu + r * D.h;
+  };
+  const int it0 = blockIdx.x;
+  const bool pre = it0 < D.S * per_slot;             // shared-expert item: expert known now
+  if (pre) {
+    set_rows_e(D.E + it0 / per_slot, it0);
+    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp);
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (route) {
+    float* lg = reinterpret_cast<float*>(smi + ActCache::words(max_active, T * D.NS));
+    int* ids = reinterpret_cast<int*>(lg + T * D.E);
+    float* wts = reinterpret_cast<float*>(ids + T * D.k);
+    int* scratch = reinterpret_cast<int*>(wts + T * D.k);
+    route_in_block(D, B, A, T, lg, ids, wts, scratch);
+  } else {
+    copy_active(B, A, max_active, T * D.NS);
+  }
+  const int nitems = *A.nact * per_slot;
+  auto valid = [&](int it) { return ((it % per_slot) % npass) * MC < A.cnt[it / per_slot]; };
+  auto next_valid = [&](int it) {
+    while (it < nitems && !valid(it)) it += stride;
+    return it;
+  };
+  int it = next_valid(it0);
+  if (it < nitems && !(pre && it == it0)) {
+    set_rows_e(A.ex[it / per_slot], it);
+    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp);
+  }
+  int par = 0;
+  while (it < nitems) {
+    const int slot = it / per_slot, rem = it % per_slot;
+    const int j = (rem / npass) * 8 + g, p0 = (rem % npass) * MC;
+    const int e = A.ex[slot];
+    const int nvalid = min(MC, A.cnt[slot] - p0);
+    const int* pairs = A.perm + A.off[slot] + p0;
+    float c[4];
+    mma_part<WT, MNB>(va, vb, wlo, whi, D.h, g < nvalid ? B.u + (size_t)(pairs[g] / D.NS) * D.h : nullptr, c);
+    const int nx = next_valid(it + stride);
+    if (nx < nitems) {
+      set_rows_e(A.ex[nx / per_slot], nx);
+      mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp);
+    }
+    block_sum4(c, red, par);
+    par ^= 1;
+    if (warp == 0) {
+      const float s0 = sg != nullptr ? sg[(size_t)e * D.inter + j] : 1.f;
+      const float s1 = su != nullptr ? su[(size_t)e * D.inter + j] : 1.f;
+#pragma unroll
+      for (int ee = 0; ee < 2; ++ee) {
+        const int col = 2 * q + ee;
+        if (col < nvalid) B.h_act[(size_t)pairs[col] * D.inter + j] = silu(c[ee] * s0) * (c[2 + ee] * s1);
+      }
+    }
+    it = nx;
+  }
+}
+
+// Expert down projection y[pair][o] = sum_j W_d[e][o][j] * h_act[pair][j].
+template <class WT>
+__global__ void __launch_bounds__(256, SBPS) k_down_m(Dims D, StepBuf B, const WT* __restrict__ Wd,
+                                                      const float* __restrict__ sd, int T, int max_active) {
+  extern __shared__ __align__(16) int smi[];
+  __shared__ float4 red[512];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const int npass = cdiv(T, MC);
+  const int upe = D.h / 16;
+  const int per_slot = upe * npass;
+  const int stride = gridDim.x;
+  const ActCache A(smi, max_active, T * D.NS);
+  uint4 va[MNB], vb[MNB];
+  const WT *wlo = Wd, *whi = Wd;
+  auto set_rows_e = [&](int e, int it) {
+    const size_t o = (size_t)e * D.h + ((it % per_slot) / npass) * 16 + g;
+    wlo = Wd + o * D.inter;
+    whi = Wd + (o + 8) * D.inter;
+  };
+  const int it0 = blockIdx.x;
+  const bool pre = it0 < D.S * per_slot;
+  if (pre) {
+    set_rows_e(D.E + it0 / per_slot, it0);
+    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.inter, warp);
+  }
+  pdl_wait();
+  pdl_trigger();
+  copy_active(B, A, max_active, T * D.NS);
+  const int nitems = *A.nact * per_slot;
+  auto valid = [&](int it) { return ((it % per_slot) % npass) * MC < A.cnt[it / per_slot]; };
+  auto next_valid = [&](int it) {
+    while (it < nitems && !valid(it)) it += stride;
+    return it;
+  };
+  int it = next_valid(it0);
+  if (it < nitems && !(pre && it == it0)) {
+    set_rows_e(A.ex[it / per_slot], it);
+    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.inter, warp);
+  }
+  int par = 0;
+  while (it < nitems) {
+    const int slot = it / per_slot, rem = it % per_slot;
+    const int o = (rem / npass) * 16 + g, p0 = (rem % npass) * MC;
+    const int e = A.ex[slot];
+    const int nvalid = min(MC, A.cnt[slot] - p0);
+    const int* pairs = A.perm + A.off[slot] + p0;
+    float c[4];
+    mma_part<WT, MNB>(va, vb, wlo, whi, D.inter, g < nvalid ? B.h_act + (size_t)pairs[g] * D.inter : nullptr, c);
+    const int nx = next_valid(it + stride);
+    if (nx < nitems) {
+      set_rows_e(A.ex[nx / per_slot], nx);
+      mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.inter, warp);
+    }
+    block_sum4(c, red, par);
+    par ^= 1;
+    if (warp == 0) {
+      const float s0 = sd != nullptr ? sd[(size_t)e * D.h + o] : 1.f;
+      const float s1 = sd != nullptr ? sd[(size_t)e * D.h + o + 8] : 1.f;
+#pragma unroll
+      for (int ee = 0; ee < 2; ++ee) {
+        const int col = 2 * q + ee;
+        if (col >= nvalid) continue;
+        float* y = B.y + (size_t)pairs[col] * D.h;
+        y[o] = c[ee] * s0;
+        y[o + 8] = c[2 + ee] * s1;
+      }
+    }
+    it = nx;
+  }
+}
+
+// Final RMSNorm + LM head + greedy argmax (+ accept/commit), bf16 weights.
+// Warp 0's lanes keep the running best (value, index) of the block's rows for
+// their two columns; the block's candidates go to scratch and the last block
+// reduces them (larger value wins, equal values keep the lower index).
+__global__ void __launch_bounds__(256, SBPS) k_lmhead_m(Dims D, DevState S, StepBuf B, const bf16_t* __restrict__ W,
+                                                        const float* __restrict__ gamma, const float* x, int T,
+                                                        float* __restrict__ logits_dbg, int commit, int n_seq,
+                                                        int K) {
+  extern __shared__ __align__(16) float sm[];
+  __shared__ float4 red[512];
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const int nunits = D.V / 16;
+  const int npass = cdiv(T, MC);
+  float* inv = sm;
+  float* xs = sm + ((T + 3) & ~3);
+  uint4 va[MNB], vb[MNB];
+  const bf16_t *wlo = W, *whi = W;
+  auto set_rows = [&](int u) {
+    wlo = W + (size_t)(u * 16 + g) * D.h;
+    whi = W + (size_t)(u * 16 + g + 8) * D.h;
+  };
+  if ((int)blockIdx.x < nunits) {
+    set_rows(blockIdx.x);
+    mma_load_batch<bf16_t, MNB>(va, vb, wlo, whi, D.h, warp);
+  }
+  pdl_wait();
+  pdl_trigger();
+  row_inv_rms(x, T, D.h, D.eps, inv);
+  __syncthreads();
+  int par = 0;
+  for (int pass = 0; pass < npass; ++pass) {
+    const int t0 = pass * MC, nvalid = min(MC, T - t0);
+    if (pass > 0) __syncthreads();
+    stage_cols(xs, x, t0, nvalid, D.h, inv, gamma);
+    __syncthreads();
+    float best[2] = {-INFINITY, -INFINITY};
+    int bidx[2] = {0x7fffffff, 0x7fffffff};
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+      float c[4];
+      mma_part<bf16_t, MNB>(va, vb, wlo, whi, D.h, g < nvalid ? xs + g * (D.h + 4) : nullptr, c);
+      const int un = u + (int)gridDim.x < nunits ? u + gridDim.x : (pass + 1 < npass ? (int)blockIdx.x : -1);
+      if (un >= 0) {
+        set_rows(un);
+        mma_load_batch<bf16_t, MNB>(va, vb, wlo, whi, D.h, warp);
+      }
+      block_sum4(c, red, par);
+      par ^= 1;
+      if (warp != 0) continue;
+      const int r0 = u * 16 + g;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int col = 2 * q + e;
+        if (logits_dbg != nullptr && col < nvalid) {
+          logits_dbg[(size_t)(t0 + col) * D.V + r0] = c[e];
+          logits_dbg[(size_t)(t0 + col) * D.V + r0 + 8] = c[2 + e];
+        }
+        if (c[e] > best[e]) { best[e] = c[e]; bidx[e] = r0; }          // rows in increasing order
+        if (c[2 + e] > best[e]) { best[e] = c[2 + e]; bidx[e] = r0 + 8; }
+      }
+    }
+    if (warp == 0) {
+      // reduce over the eight row groups (lane bits 2..4) for each column
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, best[e], o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bidx[e], o);
+          if (ov > best[e] || (ov == best[e] && oi < bidx[e])) { best[e] = ov; bidx[e] = oi; }
+        }
+        const int col = 2 * q + e;
+        if (g == 0 && col < nvalid) {
+          B.am_val[(size_t)(t0 + col) * B.n_vblocks + blockIdx.x] = best[e];
+          B.am_idx[(size_t)(t0 + col) * B.n_vblocks + blockIdx.x] = bidx[e];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = (atomicAdd(B.cnt_lm, 1) == (int)gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int nc = gridDim.x;
+  for (int row = warp; row < T; row += GEMV_WARPS) {
+    const size_t base = (size_t)row * B.n_vblocks;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int i = lane; i < nc; i += 32) {
+      const float c = __ldcg(B.am_val + base + i);
+      const int ci = __ldcg(B.am_idx + base + i);
+      if (c > bv || (c == bv && ci < bi)) { bv = c; bi = ci; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == 0) B.g[row] = bi;
+  }
+  if (threadIdx.x == 0) *B.cnt_lm = 0;
+  if (!commit) return;
+  __syncthreads();
+  __threadfence();
+  for (int sq = threadIdx.x; sq < n_seq; sq += blockDim.x) commit_seq(D, S, B, sq, K, B.g);
+}
+
 // ---------------------------------------------------------------------------
 static int grid_for(const Dims& D, int items) {
   const int want = cdiv(items, GEMV_WARPS);
@@ -529,8 +957,31 @@ static int max_active_of(const Dims& D, int T) {
   return (D.E > 0 ? (D.E < T * D.k ? D.E : T * D.k) : 0) + D.S;
 }
 
+// The tensor-core forms serve bf16 / e4m3 weights whose widths are whole
+// steps (32 bf16 or 64 e4m3 elements) and whose row counts split into
+// 16-row units; fp32 weights (and other shapes) keep the FMA forms.
+static bool mma_form(const Dims& D) {
+  if (D.wdtype == 0) return false;
+  const int sk = D.wdtype == 1 ? 32 : 64;
+  return D.h % sk == 0 && (D.Hq * D.d) % sk == 0 && D.inter % sk == 0 && D.h % 16 == 0 && D.inter % 8 == 0 &&
+         (D.d / 2) % 8 == 0 && D.V % 16 == 0 && D.h % 4 == 0;
+}
+static size_t mma_stage_bytes(const Dims& D, int T) { return (size_t)(((T + 3) & ~3) + MC * (D.h + 4)) * sizeof(float); }
+// persistent grid for block-level units
+static int grid_blocks(const Dims& D, int units) {
+  const int cap = D.n_sm * SBPS;
+  return units < 1 ? 1 : (units < cap ? units : cap);
+}
+
 void launch_qkv(const Dims& D, const DevState& S, const StepBuf& B, const LayerW& W, int layer, int T,
                 const float* x, cudaStream_t st) {
+  if (mma_form(D)) {
+    const dim3 g(grid_blocks(D, (D.Hq + 2 * D.Hkv) * (D.d / 16))), b(256);
+    const size_t sm = mma_stage_bytes(D, T);
+    if (D.wdtype == 1) launch_k(k_qkv_m<bf16_t>, g, b, sm, st, D, S, B, W.attn_norm, (const bf16_t*)W.w_qkv, (const float*)nullptr, layer, T, x);
+    else launch_k(k_qkv_m<fp8_t>, g, b, sm, st, D, S, B, W.attn_norm, (const fp8_t*)W.w_qkv, W.s_qkv, layer, T, x);
+    return;
+  }
   const int units = (D.Hq + 2 * D.Hkv) * (D.d / 4);
   const dim3 g(grid_for(D, units)), b(256);
   const size_t sm = (size_t)StageLayout(T, D.h).total * sizeof(float);
@@ -542,6 +993,12 @@ void launch_qkv(const Dims& D, const DevState& S, const StepBuf& B, const LayerW
 }
 
 void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, float* xres, cudaStream_t st) {
+  if (mma_form(D)) {
+    const dim3 g(grid_blocks(D, (D.h / 16) * cdiv(T, MC))), b(256);
+    if (D.wdtype == 1) launch_k(k_oproj_m<bf16_t>, g, b, 0, st, D, B, (const bf16_t*)W.w_o, (const float*)nullptr, T, xres);
+    else launch_k(k_oproj_m<fp8_t>, g, b, 0, st, D, B, (const fp8_t*)W.w_o, W.s_o, T, xres);
+    return;
+  }
   const int items = (D.h / 4) * cdiv(T, GEMV_TP);
   const dim3 g(grid_for(D, items)), b(256);
   switch (D.wdtype) {
@@ -553,11 +1010,21 @@ void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, float
 
 void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
   const int ma = max_active_of(D, T);
-  const int items = ma * (D.inter / 2) * cdiv(T, GEMV_TP);
-  const dim3 g(grid_for(D, items)), b(256);
   const bool route = route_in_gateup(T);
   const size_t sm = (size_t)gateup_words(D, T, ma, route) * sizeof(int);
   const int rt = route ? 1 : 0;
+  if (mma_form(D)) {
+    const dim3 g(grid_blocks(D, ma * (D.inter / 8) * cdiv(T, MC))), b(256);
+    if (D.wdtype == 1)
+      launch_k(k_gateup_m<bf16_t>, g, b, sm, st, D, B, (const bf16_t*)W.w_gate, (const float*)nullptr,
+               (const bf16_t*)W.w_up, (const float*)nullptr, T, ma, rt);
+    else
+      launch_k(k_gateup_m<fp8_t>, g, b, sm, st, D, B, (const fp8_t*)W.w_gate, W.s_gate, (const fp8_t*)W.w_up,
+               W.s_up, T, ma, rt);
+    return;
+  }
+  const int items = ma * (D.inter / 2) * cdiv(T, GEMV_TP);
+  const dim3 g(grid_for(D, items)), b(256);
   switch (D.wdtype) {
     case 0: launch_k(k_gateup_s<float>, g, b, sm, st, D, B, (const float*)W.w_gate, (const float*)nullptr,
                      (const float*)W.w_up, (const float*)nullptr, T, ma, rt); break;
@@ -570,9 +1037,15 @@ void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, cuda
 
 void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
   const int ma = max_active_of(D, T);
+  const size_t sm = (size_t)ActCache::words(ma, T * D.NS) * sizeof(int);
+  if (mma_form(D)) {
+    const dim3 g(grid_blocks(D, (D.h / 16) * ma * cdiv(T, MC))), b(256);
+    if (D.wdtype == 1) launch_k(k_down_m<bf16_t>, g, b, sm, st, D, B, (const bf16_t*)W.w_down, (const float*)nullptr, T, ma);
+    else launch_k(k_down_m<fp8_t>, g, b, sm, st, D, B, (const fp8_t*)W.w_down, W.s_down, T, ma);
+    return;
+  }
   const int items = (D.h / 4) * ma * cdiv(T, GEMV_TP);
   const dim3 g(grid_for(D, items)), b(256);
-  const size_t sm = (size_t)ActCache::words(ma, T * D.NS) * sizeof(int);
   switch (D.wdtype) {
     case 0: launch_k(k_down_s<float>, g, b, sm, st, D, B, (const float*)W.w_down, (const float*)nullptr, T, ma); break;
     case 1: launch_k(k_down_s<bf16_t>, g, b, sm, st, D, B, (const bf16_t*)W.w_down, (const float*)nullptr, T, ma); break;
@@ -592,6 +1065,12 @@ int lmhead_step_warps(const Dims& D) { return grid_for(D, D.V / 4) * GEMV_WARPS;
 void launch_lmhead_step(const Dims& D, const DevState& S, const StepBuf& B, const void* lm_head,
                         const float* final_norm, const float* x, int T, float* logits_dbg, bool commit,
                         int n_seq, int K, cudaStream_t st) {
+  if (mma_form(D)) {
+    const dim3 g(grid_blocks(D, D.V / 16)), b(256);
+    launch_k(k_lmhead_m, g, b, mma_stage_bytes(D, T), st, D, S, B, (const bf16_t*)lm_head, final_norm, x, T,
+             logits_dbg, (int)commit, n_seq, K);
+    return;
+  }
   const dim3 g(grid_for(D, D.V / 4)), b(256);
   const size_t sm = (size_t)StageLayout(T, D.h).total * sizeof(float);
   if (D.act_f32)
@@ -609,6 +1088,8 @@ cudaError_t configure_stream_kernels() {
   ALLOW(k_gateup_s<float>); ALLOW(k_gateup_s<bf16_t>); ALLOW(k_gateup_s<fp8_t>);
   ALLOW(k_down_s<float>); ALLOW(k_down_s<bf16_t>); ALLOW(k_down_s<fp8_t>);
   ALLOW(k_lmhead_s<float>); ALLOW(k_lmhead_s<bf16_t>);
+  ALLOW(k_qkv_m<bf16_t>); ALLOW(k_qkv_m<fp8_t>); ALLOW(k_gateup_m<bf16_t>); ALLOW(k_gateup_m<fp8_t>);
+  ALLOW(k_down_m<bf16_t>); ALLOW(k_down_m<fp8_t>); ALLOW(k_lmhead_m);
 #undef ALLOW
   return e;
 }

@@ -6,17 +6,20 @@
 // activations are given as two bf16 operands, X = X_hi + X_lo (about 16
 // mantissa bits), and both are multiplied into the same fp32 accumulator, so
 // the result keeps near-fp32 activation precision while the weights stay
-// exact bf16. Tiles of 64 K-elements (one 128-byte swizzle row) are brought into
-// shared memory by TMA (cp.async.bulk.tensor, 128-byte swizzle) through a
-// multi-stage mbarrier pipeline; one thread issues tcgen05.mma into a TMEM
+// exact bf16. Weights are stored pre-tiled (tc_pack_weights): every 128-row x
+// 64-element tile is one contiguous 16 KB block holding the exact 128-byte-
+// swizzled shared-memory image, so a stage fetches it with a single linear
+// bulk copy (cp.async.bulk) instead of 128 strided row pieces; activation tiles
+// come by TMA (cp.async.bulk.tensor, 128-byte swizzle). Stages run through a
+// multi-stage mbarrier pipeline as deep as shared memory allows; one thread issues tcgen05.mma into a TMEM
 // accumulator (fp32, lane = weight row, column = token); four warps read it
 // back with tcgen05.ld for the epilogue. Experts are groups: the activation
 // rows of group g are rows [off_g, off_g + cnt_g) of a permuted buffer, and a
 // CTA computes the columns of one group, so each token column only ever sees
 // its own row of X -- its result does not depend on the other tokens.
 //
-// FP8 weights (e4m3, per-row fp32 scale applied in the epilogue): TMA brings
-// the e4m3 tile unswizzled into a staging buffer, four converter warps widen
+// FP8 weights (e4m3, per-row fp32 scale applied in the epilogue): the 8 KB
+// e4m3 tile (row-major inside the tile) lands in a staging buffer, four converter warps widen
 // it to bf16 -- exactly, every e4m3 value is a bf16 value -- into the
 // 128-byte-swizzled operand tile and signal the MMA thread, so the tensor
 // cores run the same bf16 MMA while HBM carries one byte per weight.
@@ -24,6 +27,7 @@
 // Every wait on an mbarrier is bounded; a timeout sets an error bit, the CTA
 // stops issuing work, frees its TMEM and returns.
 #include <cuda_fp8.h>
+#include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -35,18 +39,26 @@ namespace spec {
 constexpr int TC_BM = 128;            // weight rows per CTA (MMA M)
 constexpr int TC_BK = 64;             // K elements per stage (128 bytes of bf16)
 constexpr int TC_NSUB = 32;           // activation rows per TMA box
-constexpr int TC_MAXN = 128;          // columns per CTA
+constexpr int TC_MAXN = 128;          // columns per CTA (largest N tile)
 constexpr uint32_t TC_WAIT_LIMIT = 1u << 20;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;        // 16 KB
-constexpr int TC_B_BYTES = TC_MAXN * TC_BK * 2;      // 16 KB (hi) + 16 KB (lo)
 constexpr int TC_A8_BYTES = TC_BM * TC_BK;           // 8 KB e4m3 staging per weight operand
 
-__host__ __device__ constexpr int tc_stages(int dual, int f8) { return f8 ? (dual ? 2 : 4) : (dual ? 3 : 4); }
-__host__ __device__ constexpr int tc_stage_bytes(int dual, int f8) {
-  return (TC_A_BYTES + (f8 ? TC_A8_BYTES : 0)) * (1 + dual) + 2 * TC_B_BYTES;
+constexpr int TC_MAXST = 12;          // pipeline stages at most
+constexpr int TC_SMEM = 220 * 1024;   // dynamic shared memory of every CTA
+constexpr int TC_HDR = 1024;          // barriers + TMEM slot, ahead of the stages
+
+// Bytes of one pipeline stage for nsub 32-row activation boxes: weight
+// tile(s), activation hi (+ lo), e4m3 staging (FP8). Every part is a multiple
+// of 1024 bytes, so each stays aligned for the 128-byte swizzle.
+__host__ __device__ constexpr int tc_stage_bytes(int dual, int f8, int nsub, int split) {
+  return (TC_A_BYTES + (f8 ? TC_A8_BYTES : 0)) * (1 + dual) + (split ? 2 : 1) * nsub * TC_NSUB * TC_BK * 2;
 }
-__host__ __device__ constexpr int tc_smem_bytes(int dual, int f8) {
-  return tc_stages(dual, f8) * tc_stage_bytes(dual, f8) + 1024 + 256;
+// Stages that fit: as many weight tiles in flight as shared memory allows.
+__host__ __device__ constexpr int tc_stage_count(int dual, int f8, int nsub, int split) {
+  return (TC_SMEM - TC_HDR - 1024) / tc_stage_bytes(dual, f8, nsub, split) < TC_MAXST
+             ? (TC_SMEM - TC_HDR - 1024) / tc_stage_bytes(dual, f8, nsub, split)
+             : TC_MAXST;
 }
 __host__ __device__ constexpr int tc_threads(int f8) { return f8 ? 256 : 128; }
 
@@ -84,6 +96,12 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar) : "memory");
+}
+
+// Linear global -> shared copy completing on an mbarrier (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
@@ -126,43 +144,51 @@ __device__ __forceinline__ void convert_tile(const unsigned char* stg, unsigned 
 }
 
 template <int DUAL, int F8>
-__global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_constant__ CUtensorMap mapA,
-                                                               const __grid_constant__ CUtensorMap mapA2,
-                                                               const __grid_constant__ CUtensorMap mapB,
+__global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_constant__ CUtensorMap mapB,
                                                                const __grid_constant__ CUtensorMap mapBlo, TcParams P) {
-  constexpr int STAGES = tc_stages(DUAL, F8);
-  constexpr int SB = tc_stage_bytes(DUAL, F8);
-  // stage layout: [A bf16 (x2 if DUAL)][B hi][B lo][A e4m3 staging (x2 if DUAL), F8 only]
-  constexpr int STG_OFF = TC_A_BYTES * (1 + DUAL) + 2 * TC_B_BYTES;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // full[STAGES], empty[STAGES], done, conv[STAGES] (F8: converted tile ready)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * SB);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 1);
+  // header: full[MAXST], empty[MAXST], done, conv[MAXST] (F8: converted tile ready), TMEM slot, abort flag
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * TC_MAXST + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- the CTA's group and columns (whole-CTA early exits happen before any set-up) ----
-  const int mt = blockIdx.x, slot = blockIdx.y, nt = blockIdx.z;
-  const int n_groups = P.g_n ? *P.g_n : (int)gridDim.y;
+  const int nt = blockIdx.x, mt = blockIdx.y, slot = blockIdx.z;   // N tiles vary fastest: CTAs sharing a weight tile run together
+  const int n_groups = P.g_n ? *P.g_n : (int)gridDim.z;
   if (slot >= n_groups) return;
   const int grp = P.g_expert ? P.g_expert[slot] : slot;
   const int off = P.g_off ? P.g_off[slot] : 0;
   const int cnt = P.g_cnt ? P.g_cnt[slot] : P.N;
-  const int n0 = nt * TC_MAXN;
+  const int ntile = P.ntile;
+  const int n0 = nt * ntile;
   if (n0 >= cnt) return;
-  const int nrows = min(TC_MAXN, cnt - n0);
+  const int nrows = min(ntile, cnt - n0);
   const int nsub = (nrows + TC_NSUB - 1) / TC_NSUB;
   const int N = nsub * TC_NSUB;                       // MMA N: multiple of 32, <= 128
+  // stage layout: [A bf16 (x2 if DUAL)][B hi: nsub boxes][B lo: nsub boxes][A e4m3 staging (x2 if DUAL), F8 only]
+  const int BB = nsub * TC_NSUB * TC_BK * 2;          // one activation part
+  const int SB = tc_stage_bytes(DUAL, F8, nsub, P.split);
+  const int STAGES = tc_stage_count(DUAL, F8, nsub, P.split);
+  const int STG_OFF = TC_A_BYTES * (1 + DUAL) + (P.split ? 2 : 1) * BB;
+  unsigned char* stages = smem + TC_HDR;
   const int KT = P.K / TC_BK;
   const int wrow = grp * P.Mg + mt * TC_BM;           // first weight row of the tile
-  constexpr uint32_t NCOL = DUAL ? 2 * TC_MAXN : TC_MAXN;   // TMEM columns
+  // Independent accumulators, so consecutive MMAs do not wait on each other:
+  // accumulator (part, kb) takes the hi (part 0) or lo (part 1) activations of
+  // the 16-wide K steps k with k % NKB == kb; the epilogue adds them in a fixed
+  // order. Matrix 2 (DUAL) starts at column TC_MAXN * NACC.
+  constexpr int NKB = DUAL ? 1 : 2;
+  constexpr int NACC = 2 * NKB;
+  constexpr uint32_t NCOL = 512;                      // TMEM columns: (1 + DUAL) * NACC * TC_MAXN
 
+  // barrier indices: full s, empty TC_MAXST + s, done 2 TC_MAXST, conv 2 TC_MAXST + 1 + s
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2 * STAGES + 1; ++i)
+    for (int i = 0; i < 2 * TC_MAXST + 1; ++i)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bars + i)));
-    for (int i = 0; i < STAGES; ++i)    // one arrival per converter warp
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(smem_u32(bars + 2 * STAGES + 1 + i)));
+    for (int i = 0; i < TC_MAXST; ++i)    // one arrival per converter warp
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(smem_u32(bars + 2 * TC_MAXST + 1 + i)));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *abort_flag = 0;
   }
@@ -181,24 +207,24 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
     const uint32_t bytes = (F8 ? TC_A8_BYTES : TC_A_BYTES) * (1 + DUAL) + (P.split ? 2 : 1) * nsub * TC_NSUB * TC_BK * 2;
     for (int kt = 0; kt < KT; ++kt) {
       const int s = kt % STAGES;
-      if (kt >= STAGES && !mbar_wait(smem_u32(bars + STAGES + s), ((kt / STAGES) - 1) & 1)) {
+      if (kt >= STAGES && !mbar_wait(smem_u32(bars + TC_MAXST + s), ((kt / STAGES) - 1) & 1)) {
         atomicOr(P.err, DERR_TIMEOUT);
         *abort_flag = 1;
         break;
       }
-      unsigned char* st = smem + s * SB;
+      unsigned char* st = stages + s * SB;
       const uint32_t full = smem_u32(bars + s);
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full), "r"(bytes) : "memory");
       unsigned char* at = F8 ? st + STG_OFF : st;
       constexpr int AST = F8 ? TC_A8_BYTES : TC_A_BYTES;
-      tma_2d(smem_u32(at), &mapA, kt * TC_BK, wrow, full);
-      if (DUAL) tma_2d(smem_u32(at + AST), &mapA2, kt * TC_BK, wrow, full);
+      const size_t toff = ((size_t)(wrow / TC_BM) * KT + kt) * AST;   // pre-tiled weights
+      bulk_g2s(smem_u32(at), static_cast<const unsigned char*>(P.wa) + toff, AST, full);
+      if (DUAL) bulk_g2s(smem_u32(at + AST), static_cast<const unsigned char*>(P.wa2) + toff, AST, full);
       unsigned char* bt = st + TC_A_BYTES * (1 + DUAL);
       for (int j = 0; j < nsub; ++j) {
         tma_2d(smem_u32(bt + j * TC_NSUB * TC_BK * 2), &mapB, kt * TC_BK, off + n0 + j * TC_NSUB, full);
         if (P.split)
-          tma_2d(smem_u32(bt + TC_B_BYTES + j * TC_NSUB * TC_BK * 2), &mapBlo, kt * TC_BK, off + n0 + j * TC_NSUB,
-                 full);
+          tma_2d(smem_u32(bt + BB + j * TC_NSUB * TC_BK * 2), &mapBlo, kt * TC_BK, off + n0 + j * TC_NSUB, full);
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -208,41 +234,42 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
     for (int kt = 0; kt < KT && ok; ++kt) {
       const int s = kt % STAGES;
       // bf16: the TMA bytes of the stage; F8: the converters' signal (after those bytes)
-      if (!mbar_wait(smem_u32(bars + (F8 ? 2 * STAGES + 1 : 0) + s), (kt / STAGES) & 1)) {
+      if (!mbar_wait(smem_u32(bars + (F8 ? 2 * TC_MAXST + 1 : 0) + s), (kt / STAGES) & 1)) {
         atomicOr(P.err, DERR_TIMEOUT);
         *abort_flag = 1;
         ok = false;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t a0 = smem_u32(smem + s * SB);
+      const uint32_t a0 = smem_u32(stages + s * SB);
       const uint32_t b0 = a0 + TC_A_BYTES * (1 + DUAL);
 #pragma unroll
       for (int k = 0; k < TC_BK / 16; ++k) {
-        // hi then (optionally) lo activations into the same accumulator
+        // hi and (optionally) lo activations, each into its own accumulator
         for (int part = 0; part < (P.split ? 2 : 1); ++part) {
-          const uint64_t bd = sw128_desc(b0 + part * TC_B_BYTES + k * 32);
-          const uint32_t acc = (kt | k | part) != 0;
+          const uint64_t bd = sw128_desc(b0 + part * BB + k * 32);
+          const uint32_t acc = (kt > 0 || k >= NKB) ? 1u : 0u;   // first MMA of an accumulator overwrites
+          const uint32_t col = (uint32_t)((part * NKB + (k % NKB)) * TC_MAXN);
           const uint64_t ad = sw128_desc(a0 + k * 32);
           asm volatile(
               "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
               " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-              ::"r"(tmem), "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
+              ::"r"(tmem + col), "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
           if (DUAL) {
             const uint64_t ad2 = sw128_desc(a0 + TC_A_BYTES + k * 32);
             asm volatile(
                 "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
                 " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-                ::"r"(tmem + (uint32_t)TC_MAXN), "l"(ad2), "l"(bd), "r"(idesc), "r"(acc));
+                ::"r"(tmem + (uint32_t)(NACC * TC_MAXN) + col), "l"(ad2), "l"(bd), "r"(idesc), "r"(acc));
           }
         }
       }
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                   ::"r"(smem_u32(bars + STAGES + s)) : "memory");
+                   ::"r"(smem_u32(bars + TC_MAXST + s)) : "memory");
     }
     if (ok)
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                   ::"r"(smem_u32(bars + 2 * STAGES)) : "memory");
+                   ::"r"(smem_u32(bars + 2 * TC_MAXST)) : "memory");
   } else if (F8 && warp >= 4) {
     // ---- converters: e4m3 staging -> swizzled bf16 operand tile ----
     const int t = threadIdx.x - 128;
@@ -252,18 +279,19 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
         if (lane == 0) atomicOr(P.err, DERR_TIMEOUT);
         break;
       }
-      unsigned char* st = smem + s * SB;
+      unsigned char* st = stages + s * SB;
       convert_tile(st + STG_OFF, st, t);
       if (DUAL) convert_tile(st + STG_OFF + TC_A8_BYTES, st + TC_A_BYTES, t);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bars + 2 * STAGES + 1 + s)) : "memory");
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bars + 2 * TC_MAXST + 1 + s)) : "memory");
     }
   }
   __syncwarp();
 
   // ---- epilogue: warp w holds TMEM lanes 32w..32w+31 = weight rows ----
-  const bool have = __syncthreads_and(mbar_wait(smem_u32(bars + 2 * STAGES), 0)) != 0;   // block-uniform
+  const bool have = __syncthreads_and(mbar_wait(smem_u32(bars + 2 * TC_MAXST), 0)) != 0;   // block-uniform
   if (!have && threadIdx.x == 0) atomicOr(P.err, DERR_TIMEOUT);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   if (warp < 4) {
@@ -275,10 +303,33 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   __shared__ float red_v[4][TC_NSUB];
   __shared__ int red_i[4][TC_NSUB];
   for (int c0 = 0; c0 < N; c0 += 16) {
+    // v = sum of the used accumulators in order (part 0 kb 0, part 0 kb 1, part 1 ...)
     float v[16], u2[16];
-    tmem_ld16(trow + c0, v);
-    if (DUAL) tmem_ld16(trow + TC_MAXN + c0, u2);
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    {
+      float t[NACC][16], t2[NACC][16];
+      const int nacc = (P.split ? 2 : 1) * NKB;
+#pragma unroll
+      for (int a = 0; a < NACC; ++a) {
+        if (a < nacc) {
+          tmem_ld16(trow + a * TC_MAXN + c0, t[a]);
+          if (DUAL) tmem_ld16(trow + (NACC + a) * TC_MAXN + c0, t2[a]);
+        }
+      }
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float x = t[0][j], y = DUAL ? t2[0][j] : 0.f;
+#pragma unroll
+        for (int a = 1; a < NACC; ++a) {
+          if (a < nacc) {
+            x += t[a][j];
+            if (DUAL) y += t2[a][j];
+          }
+        }
+        v[j] = x;
+        u2[j] = y;
+      }
+    }
     if (!have) continue;
     if (P.epi == TC_ARGMAX) {
       // per column: max over the tile's 128 rows, lowest row on ties
@@ -317,6 +368,22 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
       }
       continue;
     }
+    if (P.epi == TC_ADD) {
+      // all sixteen residual values are loaded before any store (a load-add-
+      // store chain would wait for each round trip in turn)
+      float old[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int n = n0 + c0 + j;
+        old[j] = n < n0 + nrows ? P.out_f32[(size_t)(off + n) * P.ldo + col] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int n = n0 + c0 + j;
+        if (n < n0 + nrows) P.out_f32[(size_t)(off + n) * P.ldo + col] = old[j] + v[j] * sc;
+      }
+      continue;
+    }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int n = n0 + c0 + j;
@@ -325,8 +392,6 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
       const size_t r = (size_t)(off + n);
       if (P.epi == TC_STORE) {
         P.out_f32[r * P.ldo + col] = val;
-      } else if (P.epi == TC_ADD) {
-        P.out_f32[r * P.ldo + col] += val;
       } else if (P.epi == TC_SCATTER) {
         P.out_f32[(size_t)P.perm[r] * P.ldo + col] = val;
       } else if (DUAL && P.epi == TC_SWIGLU) {
@@ -342,6 +407,35 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NCOL));
+}
+
+// ---------------------------------------------------------------------------
+// Weight tiling: W [rows, K] row-major -> tiles (row tile R, K tile kt) in
+// order R * (K / 64) + kt. bf16: 16 KB per tile, row r's 16-byte piece c at
+// r * 128 + (c ^ (r % 8)) * 16 (the 128-byte swizzle); e4m3: 8 KB per tile,
+// row r's piece c at r * 64 + c * 16. One thread per 16-byte piece.
+__global__ void k_pack_weights(const uint4* __restrict__ src, uint4* __restrict__ dst, int rows, int K, int f8) {
+  const int ppr = f8 ? K / 16 : K / 8;                 // 16-byte pieces per row
+  const int ppt = f8 ? 4 : 8;                          // pieces per row inside a tile
+  const int KT = K / TC_BK;
+  const size_t n = (size_t)rows * ppr;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int row = (int)(i / ppr), pc = (int)(i % ppr);
+    const int R = row / TC_BM, r = row % TC_BM, kt = pc / ppt, c = pc % ppt;
+    const size_t tile = (size_t)R * KT + kt;
+    const size_t piece = f8 ? tile * (TC_A8_BYTES / 16) + (size_t)r * 4 + c
+                            : tile * (TC_A_BYTES / 16) + (size_t)r * 8 + (c ^ (r & 7));
+    dst[piece] = src[i];
+  }
+}
+
+int tc_pack_weights(void* dst, const void* src, int rows, int K, int f8, cudaStream_t st) {
+  if (rows % TC_BM || K % TC_BK || (reinterpret_cast<uintptr_t>(dst) & 15) || (reinterpret_cast<uintptr_t>(src) & 15))
+    return -1;
+  const size_t pieces = (size_t)rows * (f8 ? K / 16 : K / 8);
+  const int blocks = (int)std::min<size_t>((pieces + 255) / 256, 65535);
+  k_pack_weights<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), rows, K, f8);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
 // ---------------------------------------------------------------------------
@@ -373,22 +467,6 @@ int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t row
   return r == CUDA_SUCCESS ? 0 : -3;
 }
 
-// 2D e4m3 (byte) tensor map over rows of `inner` bytes, box of 64 x box_rows,
-// no swizzle (the converters place the bytes).
-int tc_make_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return -1;
-  if ((reinterpret_cast<uintptr_t>(base) & 15) || inner % 16 || inner % TC_BK) return -2;
-  const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner};
-  const cuuint32_t box[2] = {(cuuint32_t)TC_BK, box_rows};
-  const cuuint32_t es[2] = {1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? 0 : -3;
-}
-
 }  // namespace spec
 
 // ---------------------------------------------------------------------------
@@ -401,10 +479,13 @@ int tc_make_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t 
 // out_bf16[n][m] = silu(A[m]·X[n]) * (A2[m]·X[n]) (dual = 1).
 extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const float* a_scale_dev,
                                  const float* a2_scale_dev, int a_fp8, const void* b_dev, const void* b_lo_dev,
-                                 int M, int N, int K, int dual, void* out_dev, int* err_dev, uintptr_t cuda_stream) {
+                                 int M, int N, int K, int dual, int n_tile, void* out_dev, int* err_dev,
+                                 uintptr_t cuda_stream) {
   using namespace spec;
   if (!a_dev || !b_dev || !out_dev || !err_dev || (dual && !a2_dev)) return set_last_error(-1, "null pointer");
   if (M < TC_BM || M % TC_BM || K < TC_BK || K % TC_BK || N < 1) return set_last_error(-1, "M, K multiples of 128, 64");
+  if (n_tile == 0) n_tile = TC_MAXN;
+  if (n_tile != 32 && n_tile != 64 && n_tile != 128) return set_last_error(-1, "n_tile: 32, 64 or 128");
   static bool configured = false;
   if (!configured) {
     if (configure_tc_kernels() != cudaSuccess) return set_last_error(-3, "tc kernel attributes");
@@ -413,15 +494,20 @@ extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const fl
   TcMaps maps;
   maps.dual = dual;
   maps.f8 = a_fp8 ? 1 : 0;
-  auto amap = [&](CUtensorMap* mp, const void* p) {
-    return a_fp8 ? tc_make_map_u8(mp, p, K, M, TC_BM) : tc_make_map(mp, p, K, M, TC_BM);
-  };
-  if (amap(&maps.a, a_dev) || (dual && amap(&maps.a2, a2_dev)) || tc_make_map(&maps.b, b_dev, K, N, TC_NSUB) ||
-      (b_lo_dev && tc_make_map(&maps.blo, b_lo_dev, K, N, TC_NSUB)))
+  if (tc_make_map(&maps.b, b_dev, K, N, TC_NSUB) || (b_lo_dev && tc_make_map(&maps.blo, b_lo_dev, K, N, TC_NSUB)))
     return set_last_error(-6, "tensor map encoding failed");
-  if (!dual) maps.a2 = maps.a;
   if (!b_lo_dev) maps.blo = maps.b;
+  // the weights in the tiled layout, in stream-ordered scratch
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
+  const size_t wbytes = (size_t)M * K * (a_fp8 ? 1 : 2);
+  void* wt[2] = {nullptr, nullptr};
+  for (int i = 0; i < 1 + (dual ? 1 : 0); ++i) {
+    if (cudaMallocAsync(&wt[i], wbytes, st) != cudaSuccess) return set_last_error(-5, "scratch allocation");
+    if (tc_pack_weights(wt[i], i ? a2_dev : a_dev, M, K, a_fp8, st)) return set_last_error(-3, "weight tiling");
+  }
   TcParams P = {};
+  P.wa = wt[0];
+  P.wa2 = dual ? wt[1] : wt[0];
   P.K = K; P.Mg = M; P.N = N; P.ldo = M; P.epi = dual ? TC_SWIGLU : TC_STORE;
   P.out_f32 = dual ? nullptr : reinterpret_cast<float*>(out_dev);
   P.out_bf16 = dual ? reinterpret_cast<uint16_t*>(out_dev) : nullptr;
@@ -429,7 +515,10 @@ extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const fl
   P.scale2 = a2_scale_dev;
   P.err = err_dev;
   P.split = b_lo_dev != nullptr;
-  launch_tc_gemm(maps, P, M / TC_BM, 1, (N + TC_MAXN - 1) / TC_MAXN, reinterpret_cast<cudaStream_t>(cuda_stream));
+  P.ntile = n_tile;
+  launch_tc_gemm(maps, P, M / TC_BM, 1, (N + n_tile - 1) / n_tile, st);
+  for (int i = 0; i < 2; ++i)
+    if (wt[i]) cudaFreeAsync(wt[i], st);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? 0 : set_last_error(-3, cudaGetErrorString(e));
 }
@@ -440,7 +529,7 @@ cudaError_t configure_tc_kernels() {
   cudaError_t e = cudaSuccess, r;
 #define ALLOW(D, F)                                                                                        \
   if ((r = cudaFuncSetAttribute(k_tc_gemm<D, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,             \
-                                tc_smem_bytes(D, F))) != cudaSuccess)                                      \
+                                TC_SMEM)) != cudaSuccess)                                                  \
     e = r
   ALLOW(0, 0); ALLOW(1, 0); ALLOW(0, 1); ALLOW(1, 1);
 #undef ALLOW
@@ -448,14 +537,15 @@ cudaError_t configure_tc_kernels() {
 }
 
 void launch_tc_gemm(const TcMaps& maps, const TcParams& P, int m_tiles, int groups, int n_tiles, cudaStream_t st) {
-  const dim3 grid(m_tiles, groups, n_tiles);
-  const CUtensorMap& a2 = maps.dual ? maps.a2 : maps.a;
+  const dim3 grid(n_tiles, m_tiles, groups);
+  TcParams Q = P;
+  if (Q.ntile == 0) Q.ntile = TC_MAXN;
   if (maps.f8) {
-    if (maps.dual) k_tc_gemm<1, 1><<<grid, tc_threads(1), tc_smem_bytes(1, 1), st>>>(maps.a, a2, maps.b, maps.blo, P);
-    else k_tc_gemm<0, 1><<<grid, tc_threads(1), tc_smem_bytes(0, 1), st>>>(maps.a, a2, maps.b, maps.blo, P);
+    if (maps.dual) k_tc_gemm<1, 1><<<grid, tc_threads(1), TC_SMEM, st>>>(maps.b, maps.blo, Q);
+    else k_tc_gemm<0, 1><<<grid, tc_threads(1), TC_SMEM, st>>>(maps.b, maps.blo, Q);
   } else {
-    if (maps.dual) k_tc_gemm<1, 0><<<grid, tc_threads(0), tc_smem_bytes(1, 0), st>>>(maps.a, a2, maps.b, maps.blo, P);
-    else k_tc_gemm<0, 0><<<grid, tc_threads(0), tc_smem_bytes(0, 0), st>>>(maps.a, a2, maps.b, maps.blo, P);
+    if (maps.dual) k_tc_gemm<1, 0><<<grid, tc_threads(0), TC_SMEM, st>>>(maps.b, maps.blo, Q);
+    else k_tc_gemm<0, 0><<<grid, tc_threads(0), TC_SMEM, st>>>(maps.b, maps.blo, Q);
   }
 }
 

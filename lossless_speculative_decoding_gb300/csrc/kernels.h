@@ -127,6 +127,8 @@ void launch_argmax(const StepBuf& B, int T, cudaStream_t st);
 enum TcEpi { TC_STORE = 0, TC_SWIGLU = 1, TC_ADD = 2, TC_ARGMAX = 3, TC_SCATTER = 4 };
 
 struct TcParams {
+  const void* wa;         // weights, tiled by tc_pack_weights
+  const void* wa2;        // second weights (SWIGLU up), tiled
   int K;                  // reduction length (multiple of 64)
   int Mg;                 // weight rows per group (multiple of 128)
   int N;                  // activation rows when not grouped
@@ -142,6 +144,7 @@ struct TcParams {
   uint16_t* out_bf16;     // SWIGLU [off+n][col] (hi part)
   uint16_t* out_bf16_lo;  // SWIGLU low part (value - hi), nullable
   int split;              // activations given as hi + lo operands
+  int ntile;              // activation rows per CTA: 32, 64 or 128 (0: 128)
   const int* perm;
   const float* scale;     // per weight row (nullable)
   const float* scale2;    // per weight row of the second operand (SWIGLU up)
@@ -152,15 +155,17 @@ struct TcParams {
 };
 
 struct TcMaps {
-  CUtensorMap a, a2, b, blo;   // weights, second weights (dual), activations hi, lo
+  CUtensorMap b, blo;          // activations hi, lo
   int dual;
-  int f8 = 0;                  // weights are e4m3 (maps from tc_make_map_u8)
+  int f8 = 0;                  // weights are e4m3
 };
 
 // 2D bf16 tensor map: rows of `inner` elements, box 64 x box_rows, 128-byte
 // swizzle. Returns 0 on success.
 int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
-int tc_make_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+// Rewrites W [rows, K] (row-major; bf16, or e4m3 when f8) into the tiled
+// layout the tensor-core GEMM streams (rows a multiple of 128, K of 64).
+int tc_pack_weights(void* dst, const void* src, int rows, int K, int f8, cudaStream_t st);
 void launch_tc_gemm(const TcMaps& maps, const TcParams& P, int m_tiles, int groups, int n_tiles, cudaStream_t st);
 cudaError_t configure_tc_kernels();
 void launch_norm_bf16(const Dims& D, const float* x, const float* gamma, uint16_t* out, uint16_t* out_lo, int T,

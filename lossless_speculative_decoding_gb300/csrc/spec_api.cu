@@ -142,9 +142,7 @@ struct spec_model {
   // tensor-core path (bf16 weights, more than 8 rows per step): tensor maps of
   // every weight and of the bf16 activation operands
   bool use_tc = false;
-  struct TcLayer { CUtensorMap qkv, o, gate, up, down; };
-  std::vector<TcLayer> tcl;
-  CUtensorMap tc_lm, tc_xn, tc_o, tc_xperm, tc_hperm;          // activations: hi
+  CUtensorMap tc_xn, tc_o, tc_xperm, tc_hperm;                 // activations: hi
   CUtensorMap tc_xn_lo, tc_o_lo, tc_xperm_lo, tc_hperm_lo;     //              lo
 
   ~spec_model() {
@@ -219,27 +217,34 @@ struct spec_model {
 
   // Tensor-core GEMM launches. Dense: one group covering T rows. Grouped: the
   // active-expert list of the step (rows of the permuted operand).
-  void tc_dense(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& blo, int K, int M, int T, int epi,
+  void tc_dense(const void* w, const CUtensorMap& b, const CUtensorMap& blo, int K, int M, int T, int epi,
                 float* out, int ldo, const float* scale = nullptr) {
     TcMaps mp;
-    mp.a = a; mp.a2 = a; mp.b = b; mp.blo = blo; mp.dual = 0; mp.f8 = scale != nullptr;
+    mp.b = b; mp.blo = blo; mp.dual = 0; mp.f8 = scale != nullptr;
     TcParams P = {};
+    P.wa = w; P.wa2 = w;
     P.K = K; P.Mg = M; P.N = T; P.ldo = ldo; P.epi = epi; P.out_f32 = out; P.err = S.err; P.split = 1;
     P.scale = scale;
     if (epi == TC_ARGMAX) { P.am_val = B.am_val; P.am_idx = B.am_idx; P.am_ld = M / 128; }
-    launch_tc_gemm(mp, P, M / 128, 1, (T + 127) / 128, stream);
+    // too few CTAs for the GPU with 128-row activation tiles (small projections
+    // at moderate T): 32-row tiles quadruple them; the weight tile is then read
+    // by CTAs that run side by side (N tiles vary fastest) and hits in L2
+    P.ntile = (M / 128) * ((T + 127) / 128) < D.n_sm ? 32 : 128;
+    launch_tc_gemm(mp, P, M / 128, 1, (T + P.ntile - 1) / P.ntile, stream);
   }
-  void tc_grouped(const CUtensorMap& a, const CUtensorMap* a2, const CUtensorMap& b, const CUtensorMap& blo, int K,
-                  int Mg, int T, int epi, float* out_f32, uint16_t* out_bf16, uint16_t* out_lo, int ldo,
+  void tc_grouped(const void* w, const void* w2, const CUtensorMap& b, const CUtensorMap& blo, int K, int Mg, int T,
+                  int epi, float* out_f32, uint16_t* out_bf16, uint16_t* out_lo, int ldo,
                   const float* scale = nullptr, const float* scale2 = nullptr) {
     TcMaps mp;
-    mp.a = a; mp.a2 = a2 ? *a2 : a; mp.b = b; mp.blo = blo; mp.dual = a2 ? 1 : 0; mp.f8 = scale != nullptr;
+    mp.b = b; mp.blo = blo; mp.dual = w2 ? 1 : 0; mp.f8 = scale != nullptr;
     TcParams P = {};
+    P.wa = w; P.wa2 = w2 ? w2 : w;
     P.K = K; P.Mg = Mg; P.N = T; P.ldo = ldo; P.epi = epi; P.out_f32 = out_f32; P.out_bf16 = out_bf16;
     P.out_bf16_lo = out_lo; P.split = 1; P.scale = scale; P.scale2 = scale2;
     P.perm = B.perm; P.err = S.err;
     P.g_expert = B.act_expert; P.g_off = B.act_off; P.g_cnt = B.act_cnt; P.g_n = B.n_active;
     const int max_active = (D.E > 0 ? std::min(D.E, T * D.k) : 0) + D.S;
+    P.ntile = 128;   // a small group's CTA still runs N = 32 with a deeper pipeline
     launch_tc_gemm(mp, P, Mg / 128, max_active, (T + 127) / 128, stream);
   }
 
@@ -251,26 +256,25 @@ struct spec_model {
     for (int l = 0; l < D.L; ++l) {
       const LayerW& W = layers[l];
       if (use_tc) {
-        const TcLayer& M = tcl[l];
         run_k(p, KC_QKV, [&] {
           launch_norm_bf16(D, cur, W.attn_norm, B.xn_bf16, B.xn_lo, T, stream);
-          tc_dense(M.qkv, tc_xn, tc_xn_lo, D.h, qkv_rows, T, TC_STORE, B.qkv, qkv_rows, W.s_qkv);
+          tc_dense(W.w_qkv, tc_xn, tc_xn_lo, D.h, qkv_rows, T, TC_STORE, B.qkv, qkv_rows, W.s_qkv);
           launch_rope_kv(D, S, B, l, T, stream);
         });
         run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, stream); });
-        run_k(p, KC_OPROJ, [&] { tc_dense(M.o, tc_o, tc_o_lo, D.Hq * D.d, D.h, T, TC_ADD, cur, D.h, W.s_o); });
+        run_k(p, KC_OPROJ, [&] { tc_dense(W.w_o, tc_o, tc_o_lo, D.Hq * D.d, D.h, T, TC_ADD, cur, D.h, W.s_o); });
         run_k(p, KC_ROUTER, [&] {
           launch_router(D, B, W, T, cur, true, stream);
           launch_gather_bf16(D, B, T, stream);
         });
         run_k(p, KC_GATEUP, [&] {
-          tc_grouped(M.gate, &M.up, tc_xperm, tc_xperm_lo, D.h, D.inter, T, TC_SWIGLU, nullptr, B.hperm, B.hperm_lo,
-                     D.inter, W.s_gate, W.s_up);
+          tc_grouped(W.w_gate, W.w_up, tc_xperm, tc_xperm_lo, D.h, D.inter, T, TC_SWIGLU, nullptr, B.hperm,
+                     B.hperm_lo, D.inter, W.s_gate, W.s_up);
         });
         if (p) cudaMemcpyAsync(p->act + p->nact++, B.n_active, 4, cudaMemcpyDeviceToHost, stream);
         run_k(p, KC_DOWN, [&] {
-          tc_grouped(M.down, nullptr, tc_hperm, tc_hperm_lo, D.inter, D.h, T, TC_SCATTER, B.y, nullptr, nullptr, D.h,
-                     W.s_down);
+          tc_grouped(W.w_down, nullptr, tc_hperm, tc_hperm_lo, D.inter, D.h, T, TC_SCATTER, B.y, nullptr, nullptr,
+                     D.h, W.s_down);
         });
         run_k(p, KC_COMBINE, [&] { launch_combine(D, B, cur, T, stream); });
         continue;
@@ -294,8 +298,8 @@ struct spec_model {
       return;
     }
     launch_norm_bf16(D, x, final_norm, B.xn_bf16, B.xn_lo, T, stream);
-    if (logits_dbg) tc_dense(tc_lm, tc_xn, tc_xn_lo, D.h, D.V, T, TC_STORE, logits_dbg, D.V);
-    tc_dense(tc_lm, tc_xn, tc_xn_lo, D.h, D.V, T, TC_ARGMAX, nullptr, 0);
+    if (logits_dbg) tc_dense(lm_head, tc_xn, tc_xn_lo, D.h, D.V, T, TC_STORE, logits_dbg, D.V);
+    tc_dense(lm_head, tc_xn, tc_xn_lo, D.h, D.V, T, TC_ARGMAX, nullptr, 0);
     launch_argmax_commit(D, S, B, T, D.V / 128, commit, n_seq, K, stream);
   }
 
@@ -494,20 +498,34 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
       return rc;
     CU(configure_tc_kernels());
     const int F = D.E + D.S;
-    m->tcl.resize(D.L);
-    int bad = 0;
-    // weight maps: bf16 (128-byte swizzle) or e4m3 (unswizzled bytes, widened in the kernel)
-    auto wmap = c.wdtype == SPEC_FP8 ? tc_make_map_u8 : tc_make_map;
+    // weights the tensor cores stream are rewritten, in place, into the tiled
+    // layout (one contiguous swizzled block per 128 x 64 tile); the SIMT
+    // kernels that read them row-major do not run on this path
+    const int f8 = c.wdtype == SPEC_FP8 ? 1 : 0;
+    struct Mat { void* p; int rows, K, f8; };
+    std::vector<Mat> mats;
     for (int l = 0; l < D.L; ++l) {
       const LayerW& W = m->layers[l];
-      auto& M = m->tcl[l];
-      bad |= wmap(&M.qkv, W.w_qkv, D.h, qkv_rows, 128);
-      bad |= wmap(&M.o, W.w_o, (uint64_t)D.Hq * D.d, D.h, 128);
-      bad |= wmap(&M.gate, W.w_gate, D.h, (uint64_t)F * D.inter, 128);
-      bad |= wmap(&M.up, W.w_up, D.h, (uint64_t)F * D.inter, 128);
-      bad |= wmap(&M.down, W.w_down, D.inter, (uint64_t)F * D.h, 128);
+      mats.push_back({const_cast<void*>(W.w_qkv), qkv_rows, D.h, f8});
+      mats.push_back({const_cast<void*>(W.w_o), D.h, D.Hq * D.d, f8});
+      mats.push_back({const_cast<void*>(W.w_gate), F * D.inter, D.h, f8});
+      mats.push_back({const_cast<void*>(W.w_up), F * D.inter, D.h, f8});
+      mats.push_back({const_cast<void*>(W.w_down), F * D.h, D.inter, f8});
     }
-    bad |= tc_make_map(&m->tc_lm, m->lm_head, D.h, D.V, 128);
+    mats.push_back({m->lm_head, D.V, D.h, 0});
+    size_t tmp_bytes = 0;
+    for (const Mat& x : mats) tmp_bytes = std::max(tmp_bytes, (size_t)x.rows * x.K * (x.f8 ? 1 : 2));
+    void* tmp = nullptr;
+    CU(cudaMalloc(&tmp, tmp_bytes));
+    int bad = 0;
+    for (const Mat& x : mats) {
+      const size_t nb = (size_t)x.rows * x.K * (x.f8 ? 1 : 2);
+      bad |= tc_pack_weights(tmp, x.p, x.rows, x.K, x.f8, m->stream);
+      if (cudaMemcpyAsync(x.p, tmp, nb, cudaMemcpyDeviceToDevice, m->stream) != cudaSuccess) bad = 1;
+    }
+    const cudaError_t se = cudaStreamSynchronize(m->stream);
+    cudaFree(tmp);
+    if (bad || se != cudaSuccess) return fail(SPEC_ERR_CUDA, "weight tiling failed");
     bad |= tc_make_map(&m->tc_xn, B.xn_bf16, D.h, T, 32);
     bad |= tc_make_map(&m->tc_o, B.o_bf16, (uint64_t)D.Hq * D.d, T, 32);
     bad |= tc_make_map(&m->tc_xperm, B.xperm, D.h, (uint64_t)T * NS, 32);

@@ -61,8 +61,8 @@ def test_tc_gemm_swiglu(M, N, K):
     np.testing.assert_allclose(got, ref, rtol=1e-2, atol=1e-2 * np.abs(ref).max())
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 300, 512), (128, 9, 2048)])
-def test_tc_gemm_split_activations(M, N, K):
+@pytest.mark.parametrize("M,N,K,nt", [(256, 300, 512, 0), (128, 9, 2048, 0), (256, 300, 512, 32), (384, 100, 768, 64)])
+def test_tc_gemm_split_activations(M, N, K, nt):
     import torch
     from lossless_speculative_decoding_gb300 import binding as B
     rng = np.random.default_rng(11 * M + N)
@@ -75,7 +75,7 @@ def test_tc_gemm_split_activations(M, N, K):
     bl = torch.from_numpy(lo.view(np.int16)).cuda()
     out = torch.full((N, M), float("nan"), device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    B.spec_tc_gemm_test(a, None, bh, bl, M, N, K, 0, out, err, 0)
+    B.spec_tc_gemm_test(a, None, bh, bl, M, N, K, 0, out, err, 0, n_tile=nt)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     ref = x.astype(np.float64) @ af.astype(np.float64).T
@@ -85,8 +85,9 @@ def test_tc_gemm_split_activations(M, N, K):
     np.testing.assert_allclose(got, ref, rtol=0, atol=5e-5 * np.abs(ref).max())
 
 
-@pytest.mark.parametrize("M,N,K,dual", [(256, 40, 320, 0), (128, 200, 1280, 0), (256, 48, 192, 1), (128, 130, 896, 1)])
-def test_tc_gemm_fp8_weights(M, N, K, dual):
+@pytest.mark.parametrize("M,N,K,dual,nt", [(256, 40, 320, 0, 0), (128, 200, 1280, 0, 32), (256, 48, 192, 1, 0),
+                                           (128, 130, 896, 1, 32)])
+def test_tc_gemm_fp8_weights(M, N, K, dual, nt):
     """e4m3 weights widened to bf16 in shared memory, per-row scales applied in
     the epilogue: against float64 of the decoded e4m3 values times the scales."""
     import torch
@@ -109,10 +110,11 @@ def test_tc_gemm_fp8_weights(M, N, K, dual):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     if dual:
         out = torch.zeros((N, M), dtype=torch.int16, device="cuda")
-        B.spec_tc_gemm_test(a, a2, bh, bl, M, N, K, 1, out, err, 0, a_scale_dev=sa, a2_scale_dev=sa2, a_fp8=True)
+        B.spec_tc_gemm_test(a, a2, bh, bl, M, N, K, 1, out, err, 0, a_scale_dev=sa, a2_scale_dev=sa2, a_fp8=True,
+                            n_tile=nt)
     else:
         out = torch.full((N, M), float("nan"), device="cuda")
-        B.spec_tc_gemm_test(a, None, bh, bl, M, N, K, 0, out, err, 0, a_scale_dev=sa, a_fp8=True)
+        B.spec_tc_gemm_test(a, None, bh, bl, M, N, K, 0, out, err, 0, a_scale_dev=sa, a_fp8=True, n_tile=nt)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     xf = x.astype(np.float64)
