@@ -257,20 +257,24 @@ def run_reference(args):
 # --------------------------------------------------------------------------- #
 # our arm
 # --------------------------------------------------------------------------- #
-def traffic_for(kernel: str):
-    """Per-launch DRAM bytes from the committed ncu summary, when it was taken
-    on the current kernel sources (else None)."""
+def traffic_for(kernel: str, alg_bytes_per_launch: float):
+    """Per-launch DRAM bytes of a kernel class from the committed ncu summary
+    (profiles/ncu_traffic.json), while the kernel sources still hash to what
+    was captured (else None). The capture ran a smaller case; its measured
+    traffic / algorithmic bytes ratio is applied to this launch's algorithmic
+    bytes (traffic grows with the units -- active experts -- processed)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
-    e = d.get(kernel)
-    if not e:
+    e = json.load(open(p)).get(kernel)
+    if not e or "traffic_over_algorithmic" not in e:
         return None
-    src = os.path.join(ROOT, "lossless_speculative_decoding_gb300", "csrc", e["source"])
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() != e["sha256"]:
+    h = hashlib.sha256()
+    for f in e["sources"]:
+        h.update(open(os.path.join(ROOT, "lossless_speculative_decoding_gb300", "csrc", f), "rb").read())
+    if h.hexdigest() != e["sha256"]:
         return None
-    return e["bytes_per_launch"]
+    return e["traffic_over_algorithmic"] * alg_bytes_per_launch
 
 
 def steady_state_prompts(wl, prompts, rank: int):
@@ -491,7 +495,7 @@ def run_ours(args):
             "verify_step_us": ms_per_step * 1e3,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": traffic_for(dom), "peak_source": peaks["source"],
+                         "traffic": traffic_for(dom, dom_bytes_per_launch), "peak_source": peaks["source"],
                          "bytes_per_launch": dom_bytes_per_launch, "us_per_launch": dom_ms_per_launch * 1e3},
             "step_roofline": {"bytes_per_step": step_bytes, "flops_per_step": step_flops,
                               "t_hbm_us": t_hbm_us, "t_tensor_us": t_tc_us,
