@@ -18,6 +18,7 @@
 // fixed grid strides over them, so long and short sequences share the GPU
 // evenly and no block waits on a serial walk over a long context.
 #include "common.cuh"
+#include "gemv.cuh"
 #include "kernels.h"
 
 namespace spec {
@@ -158,24 +159,10 @@ struct AttGroup {
   }
 };
 
-template <int D_HEAD, class KT>
-__global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, StepBuf B, int layer, int T,
-                                                           int R, int RG, int n_groups, int inline_merge) {
-  using L = AttSmem<D_HEAD, KT>;
-  constexpr int KST = L::KST;
-  constexpr int PPR = D_HEAD * (int)sizeof(KT) / 16;          // 16-byte pieces per key row
-  extern __shared__ __align__(16) unsigned char smraw[];
-  KT* Ks = reinterpret_cast<KT*>(smraw);                        // [64][KST]
-  KT* Vs = reinterpret_cast<KT*>(smraw + L::k_bytes);           // [64][D_HEAD]
-  float* Qw = reinterpret_cast<float*>(smraw + L::k_bytes + L::v_bytes);    // [warps][D_HEAD]
-  float* Pw = Qw + (ATT_THREADS / 32) * D_HEAD;                 // [warps][64]
-  int* pg = reinterpret_cast<int*>(Pw + (ATT_THREADS / 32) * ATT_CHUNK);  // [64] page of each key
-  __shared__ int s_last;
-  __shared__ int s_pref[ATT_MAX_GROUPS + 1];          // chunk items before group g
-  pdl_wait();
-  pdl_trigger();
+// Work list: per-group chunk counts -> exclusive prefix s_pref[0..n_groups]
+// (warp 0; lane l owns groups [l*per, (l+1)*per)), then a block barrier.
+__device__ __forceinline__ void att_prefix(const StepBuf& B, int T, int R, int RG, int n_groups, int* s_pref) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // ---- per-group chunk counts -> exclusive prefix (warp 0; lane l owns groups [l*per, (l+1)*per)) ----
   if (warp == 0) {
     const int per = (n_groups + 31) / 32, g0 = lane * per;
     int sum = 0;
@@ -200,6 +187,36 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
     if (lane == 31) s_pref[n_groups] = inc;
   }
   __syncthreads();
+}
+
+// The item's group: s_pref[g] <= q < s_pref[g + 1] (the last such g is never empty).
+__device__ __forceinline__ int att_group_of(const int* s_pref, int n_groups, int q) {
+  int lo = 0, hi = n_groups;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_pref[mid] <= q) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+template <int D_HEAD, class KT>
+__global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, StepBuf B, int layer, int T,
+                                                           int R, int RG, int n_groups, int inline_merge) {
+  using L = AttSmem<D_HEAD, KT>;
+  constexpr int KST = L::KST;
+  constexpr int PPR = D_HEAD * (int)sizeof(KT) / 16;          // 16-byte pieces per key row
+  extern __shared__ __align__(16) unsigned char smraw[];
+  KT* Ks = reinterpret_cast<KT*>(smraw);                        // [64][KST]
+  KT* Vs = reinterpret_cast<KT*>(smraw + L::k_bytes);           // [64][D_HEAD]
+  float* Qw = reinterpret_cast<float*>(smraw + L::k_bytes + L::v_bytes);    // [warps][D_HEAD]
+  float* Pw = Qw + (ATT_THREADS / 32) * D_HEAD;                 // [warps][64]
+  int* pg = reinterpret_cast<int*>(Pw + (ATT_THREADS / 32) * ATT_CHUNK);  // [64] page of each key
+  __shared__ int s_last;
+  __shared__ int s_pref[ATT_MAX_GROUPS + 1];          // chunk items before group g
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  att_prefix(B, T, R, RG, n_groups, s_pref);
   const int G = D.Hq / D.Hkv;
   const float scale = 1.0f / sqrtf((float)D_HEAD);
   const size_t v_off = (size_t)D.Hkv * D.P * D_HEAD;                            // K -> V
@@ -210,12 +227,7 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
 
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int q = item / D.Hkv, hk = item % D.Hkv;
-    int lo = 0, hi = n_groups;                        // group: s_pref[g] <= q < s_pref[g + 1]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_pref[mid] <= q) lo = mid; else hi = mid;
-    }
-    const int g = lo, c = q - s_pref[g];
+    const int g = att_group_of(s_pref, n_groups, q), c = q - s_pref[g];
     const AttGroup grp(g, T, R, RG);
     const int r0 = grp.r0, nr = grp.nr;
     const int seq = B.row_seq[r0];
@@ -331,6 +343,232 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
   }
 }
 
+// ===========================================================================
+// Tensor-core form (bf16 K/V): warp-level mma.sync m16n8k16 with the chunk's
+// 64 keys as M and the group's (row, q head) pairs as N (8 per tile, at most
+// 32 per group: a group holds 32 / G rows). Per item:
+//   S^T = K Q^T   (A = K rows by ldmatrix, B = Q as bf16 hi + lo: two MMAs),
+//   softmax of each pair column over the chunk (fp32, causal mask),
+//   O^T = V^T P^T (A = V by ldmatrix.trans, B = P as bf16 hi + lo).
+// K and V are bf16 already, so the products are exact and the hi/lo split
+// keeps Q and P near fp32. Warp w scores keys 16w..16w+15 and then outputs
+// dims [D/4 w, D/4 (w+1)). Each pair column only meets its own Q and P, so a
+// row's result does not depend on the group, the batch or its place in them.
+constexpr int ATQ = 32;          // pairs per group at most (4 N tiles)
+
+template <int D_HEAD>
+struct AttTcSmem {
+  static constexpr int KST = D_HEAD + 8;               // padded bf16 rows (ldmatrix without bank conflicts)
+  static constexpr int PST = ATT_CHUNK + 8;
+  static constexpr size_t k = 0;
+  static constexpr size_t v = k + (size_t)ATT_CHUNK * KST * 2;
+  static constexpr size_t qh = v + (size_t)ATT_CHUNK * KST * 2;
+  static constexpr size_t ql = qh + (size_t)ATQ * KST * 2;
+  static constexpr size_t ph = ql + (size_t)ATQ * KST * 2;
+  static constexpr size_t pl = ph + (size_t)ATQ * PST * 2;
+  static constexpr size_t sf = pl + (size_t)ATQ * PST * 2;      // fp32 S [64 keys][ATQ + 1]
+  static constexpr size_t pg = sf + (size_t)ATT_CHUNK * (ATQ + 1) * 4;
+  static constexpr size_t total = pg + ATT_CHUNK * 4;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, const void* p) {
+  const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(a));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int D_HEAD>
+__global__ void __launch_bounds__(ATT_THREADS) k_attn_tc(Dims D, DevState S, StepBuf B, int layer, int T, int R,
+                                                         int RG, int n_groups, int inline_merge) {
+  using L = AttTcSmem<D_HEAD>;
+  constexpr int KST = L::KST, PST = L::PST;
+  constexpr int PPR = D_HEAD * 2 / 16;                 // 16-byte pieces per K/V row
+  constexpr int DMT = D_HEAD / 16 / 4;                 // output dim tiles per warp
+  extern __shared__ __align__(16) unsigned char smraw[];
+  bf16_t* Ks = reinterpret_cast<bf16_t*>(smraw + L::k);
+  bf16_t* Vs = reinterpret_cast<bf16_t*>(smraw + L::v);
+  uint16_t* Qh = reinterpret_cast<uint16_t*>(smraw + L::qh);
+  uint16_t* Ql = reinterpret_cast<uint16_t*>(smraw + L::ql);
+  uint16_t* Ph = reinterpret_cast<uint16_t*>(smraw + L::ph);
+  uint16_t* Pl = reinterpret_cast<uint16_t*>(smraw + L::pl);
+  float* Sf = reinterpret_cast<float*>(smraw + L::sf);
+  int* pg = reinterpret_cast<int*>(smraw + L::pg);
+  __shared__ int s_last;
+  __shared__ int s_pref[ATT_MAX_GROUPS + 1];
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3;
+  att_prefix(B, T, R, RG, n_groups, s_pref);
+  const int G = D.Hq / D.Hkv;
+  const float scale = 1.0f / sqrtf((float)D_HEAD);
+  const size_t v_off = (size_t)D.Hkv * D.P * D_HEAD;
+  const bf16_t* kv = reinterpret_cast<const bf16_t*>(S.kv);
+  const int n_items = s_pref[n_groups] * D.Hkv;
+
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int qi = item / D.Hkv, hk = item % D.Hkv;
+    const int gi = att_group_of(s_pref, n_groups, qi), c = qi - s_pref[gi];
+    const AttGroup grp(gi, T, R, RG);
+    const int r0 = grp.r0, nr = grp.nr;
+    const int seq = B.row_seq[r0];
+    const int maxpos = B.row_pos[r0 + nr - 1];
+    const int nch = maxpos / ATT_CHUNK + 1;
+    const int npairs = nr * G;
+    const int nnt = (npairs + 7) / 8;
+    const int k0 = c * ATT_CHUNK;
+    const int nk = min(ATT_CHUNK, maxpos + 1 - k0);
+    const size_t head_off = (((size_t)layer * 2) * D.Hkv + hk) * D.P * D_HEAD;
+    __syncthreads();
+    // ---- pages, K/V pieces in flight, Q of the group's pairs as hi/lo ----
+    for (int key = threadIdx.x; key < ATT_CHUNK; key += ATT_THREADS) {
+      int page = -1;
+      if (key < nk) {
+        page = S.bt[(size_t)seq * D.max_pages + (k0 + key) / D.P];
+        if (page < 0) atomicOr(S.err, DERR_PAGE);
+      }
+      pg[key] = page;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 2 * ATT_CHUNK * PPR; i += ATT_THREADS) {
+      const int isv = i >= ATT_CHUNK * PPR;
+      const int j = isv ? i - ATT_CHUNK * PPR : i;
+      const int key = j / PPR, piece = j % PPR;
+      bf16_t* dst = (isv ? Vs : Ks) + key * KST + piece * 8;
+      const int page = pg[key];
+      if (page < 0) {                                 // keys past the chunk's end (or a missing page): zeros
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      const size_t e = (size_t)page * D.page_elems + head_off + (isv ? v_off : 0) +
+                       (size_t)((k0 + key) % D.P) * D_HEAD + piece * 8;
+      cp_async16(dst, kv + e);
+    }
+    for (int i = threadIdx.x; i < nnt * 8 * (D_HEAD / 4); i += ATT_THREADS) {
+      const int p = i / (D_HEAD / 4), d4 = (i % (D_HEAD / 4)) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (p < npairs) {
+        const int row = r0 + p / G, hq = hk * G + p % G;
+        v = *reinterpret_cast<const float4*>(B.q + ((size_t)row * D.Hq + hq) * D_HEAD + d4);
+      }
+      uint32_t h0, l0, h1, l1;
+      split_bf16x2(v.x, v.y, h0, l0);
+      split_bf16x2(v.z, v.w, h1, l1);
+      *reinterpret_cast<uint2*>(Qh + p * KST + d4) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2*>(Ql + p * KST + d4) = make_uint2(l0, l1);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // ---- S^T (keys 16 warp .. +15) x pairs, scaled and causally masked, into Sf ----
+    for (int nt = 0; nt < nnt; ++nt) {
+      float ch[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < D_HEAD / 16; ++ks) {
+        uint32_t a[4], bh0, bh1, bl0, bl1;
+        ldsm_x4(a, Ks + (16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1)) * KST + 16 * ks + 8 * (lane >> 4));
+        const int prow = 8 * nt + (lane & 7), pcol = 16 * ks + 8 * ((lane >> 3) & 1);
+        ldsm_x2(bh0, bh1, Qh + prow * KST + pcol);
+        ldsm_x2(bl0, bl1, Ql + prow * KST + pcol);
+        mma_bf16(ch, a, bh0, bh1);
+        mma_bf16(cl, a, bl0, bl1);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = 16 * warp + g + 8 * (e >> 1), p = 8 * nt + 2 * q4 + (e & 1);
+        float sv = -INFINITY;
+        if (p < npairs && key < nk && k0 + key <= B.row_pos[r0 + p / G]) sv = (ch[e] + cl[e]) * scale;
+        Sf[key * (ATQ + 1) + p] = sv;
+      }
+    }
+    __syncthreads();
+    // ---- softmax of each pair over the chunk: P (hi/lo) and the partial (max, sum) ----
+    for (int p = warp; p < nnt * 8; p += ATT_THREADS / 32) {
+      const float s0 = Sf[lane * (ATQ + 1) + p], s1 = Sf[(lane + 32) * (ATQ + 1) + p];
+      const float m = warp_max(fmaxf(s0, s1));
+      float e0 = 0.f, e1 = 0.f;
+      if (m != -INFINITY) {
+        e0 = expf(s0 - m);
+        e1 = expf(s1 - m);
+      }
+      const float l = warp_sum(e0 + e1);
+      const uint16_t h0 = f_to_bf16(e0), h1 = f_to_bf16(e1);
+      Ph[p * PST + lane] = h0;
+      Ph[p * PST + lane + 32] = h1;
+      Pl[p * PST + lane] = f_to_bf16(e0 - bf16_to_f(h0));
+      Pl[p * PST + lane + 32] = f_to_bf16(e1 - bf16_to_f(h1));
+      if (lane == 0 && p < npairs && m != -INFINITY) {
+        const int row = r0 + p / G, hq = hk * G + p % G;
+        const size_t pidx = ((size_t)row * D.Hq + hq) * B.n_chunk_max + c;
+        reinterpret_cast<float2*>(B.att_ml)[pidx] = make_float2(m, l);
+      }
+    }
+    __syncthreads();
+    // ---- O^T (dims of this warp) x pairs -> chunk partials ----
+    for (int nt = 0; nt < nnt; ++nt) {
+      float oh[DMT][4], ol[DMT][4];
+#pragma unroll
+      for (int mt = 0; mt < DMT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) { oh[mt][e] = 0.f; ol[mt][e] = 0.f; }
+#pragma unroll
+      for (int ks = 0; ks < ATT_CHUNK / 16; ++ks) {
+        uint32_t bh0, bh1, bl0, bl1;
+        const int prow = 8 * nt + (lane & 7), pcol = 16 * ks + 8 * ((lane >> 3) & 1);
+        ldsm_x2(bh0, bh1, Ph + prow * PST + pcol);
+        ldsm_x2(bl0, bl1, Pl + prow * PST + pcol);
+#pragma unroll
+        for (int mt = 0; mt < DMT; ++mt) {
+          const int dm = 16 * (DMT * warp + mt);
+          uint32_t a[4];
+          // A = V^T [dims dm..dm+15][keys 16 ks..]: matrices (dims 0-7 | 8-15) x (keys 0-7 | 8-15)
+          ldsm_x4_t(a, Vs + (16 * ks + (lane & 7) + 8 * (lane >> 4)) * KST + dm + 8 * ((lane >> 3) & 1));
+          mma_bf16(oh[mt], a, bh0, bh1);
+          mma_bf16(ol[mt], a, bl0, bl1);
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < DMT; ++mt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int dim = 16 * (DMT * warp + mt) + g + 8 * (e >> 1), p = 8 * nt + 2 * q4 + (e & 1);
+          if (p >= npairs) continue;
+          const int row = r0 + p / G, hq = hk * G + p % G;
+          if (B.row_pos[row] < k0) continue;              // chunk lies after this row: no partial
+          const size_t pidx = ((size_t)row * D.Hq + hq) * B.n_chunk_max + c;
+          B.att_o[pidx * D_HEAD + dim] = oh[mt][e] + ol[mt][e];
+        }
+      }
+    }
+    // ---- the last chunk of this (group, kv head) to finish merges its pairs ----
+    if (!inline_merge) continue;
+    __syncthreads();
+    int* ctr = B.cnt_att + (size_t)gi * D.Hkv + hk;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s_last = (atomicAdd(ctr, 1) == nch - 1);
+    }
+    __syncthreads();
+    if (!s_last) continue;
+    __threadfence();
+    for (int p = warp; p < npairs; p += ATT_THREADS / 32) merge_pair<D_HEAD>(D, B, r0 + p / G, hk * G + p % G);
+    if (threadIdx.x == 0) *ctr = 0;
+  }
+}
+
 // Standalone merge: one warp per (row, q head) pair of rows [0, T).
 template <int D_HEAD>
 __global__ void __launch_bounds__(256) k_attn_merge(Dims D, StepBuf B, int T) {
@@ -345,6 +583,7 @@ cudaError_t configure_attn_kernels() {
 #define ALLOW(k) if ((r = allow_dyn_smem(k)) != cudaSuccess) e = r
   ALLOW((k_attn_part<128, float>)); ALLOW((k_attn_part<128, bf16_t>));
   ALLOW((k_attn_part<64, float>)); ALLOW((k_attn_part<64, bf16_t>));
+  ALLOW(k_attn_tc<128>); ALLOW(k_attn_tc<64>);
 #undef ALLOW
   return e;
 }
@@ -352,20 +591,32 @@ cudaError_t configure_attn_kernels() {
 // Pairs per group above which the merge runs as its own kernel.
 constexpr int ATT_INLINE_PAIRS = 16;
 
-bool attn_separate_merge(const Dims& D, int R) {
-  const int RG = R < 32 ? R : 32;
-  return RG * (D.Hq / D.Hkv) > ATT_INLINE_PAIRS;
+// bf16 K/V with head dim 64 or 128 take the tensor-core form when a
+// sequence's rows bring at least 16 (row, q head) pairs per kv head (block
+// drafts, GQA); with fewer, most of each 8-column tile would be padding and
+// the FMA form is faster. The choice depends only on the model (R is fixed
+// by max_draft), so greedy and speculative steps share it.
+static bool att_tc(const Dims& D, int R) {
+  return !D.act_f32 && (D.d == 128 || D.d == 64) && D.Hq / D.Hkv <= ATQ && R * (D.Hq / D.Hkv) >= 16;
 }
 
-int attn_groups(int T, int R) {
-  const int RG = R < 32 ? R : 32;
+// Rows per group: the tensor-core form takes at most 32 (row, q head) pairs.
+static int att_rg(const Dims& D, int R) {
+  const int cap = att_tc(D, R) ? ATQ / (D.Hq / D.Hkv) : 32;
+  return R < cap ? R : cap;
+}
+
+bool attn_separate_merge(const Dims& D, int R) { return att_rg(D, R) * (D.Hq / D.Hkv) > ATT_INLINE_PAIRS; }
+
+int attn_groups(const Dims& D, int T, int R) {
+  const int RG = att_rg(D, R);
   return ((T + R - 1) / R) * ((R + RG - 1) / RG);
 }
 
 void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
                       cudaStream_t st) {
-  const int RG = R < 32 ? R : 32;
-  const int groups = attn_groups(T, R);
+  const int RG = att_rg(D, R);
+  const int groups = attn_groups(D, T, R);
   const bool sep = attn_separate_merge(D, R);
   // fixed grid over the step's (group, chunk, kv head) items
   long long items = (long long)groups * B.n_chunk_max * D.Hkv;
@@ -373,7 +624,10 @@ void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int la
   if (items < blocks) blocks = (int)items;
   const dim3 grid(blocks), blk(ATT_THREADS);
   const int im = sep ? 0 : 1;
-  if (D.d == 128) {
+  if (att_tc(D, R)) {
+    if (D.d == 128) launch_k(k_attn_tc<128>, grid, blk, AttTcSmem<128>::total, st, D, S, B, layer, T, R, RG, groups, im);
+    else launch_k(k_attn_tc<64>, grid, blk, AttTcSmem<64>::total, st, D, S, B, layer, T, R, RG, groups, im);
+  } else if (D.d == 128) {
     if (D.act_f32) launch_k(k_attn_part<128, float>, grid, blk, AttSmem<128, float>::total, st, D, S, B, layer, T, R, RG, groups, im);
     else launch_k(k_attn_part<128, bf16_t>, grid, blk, AttSmem<128, bf16_t>::total, st, D, S, B, layer, T, R, RG, groups, im);
   } else {

@@ -100,7 +100,7 @@ void launch_assemble_prefill(const Dims& D, const DevState& S, const StepBuf& B,
 void launch_qkv(const Dims& D, const DevState& S, const StepBuf& B, const LayerW& W, int layer, int T,
                 const float* x, cudaStream_t st);
 bool attn_separate_merge(const Dims& D, int R);   // merge as its own launch (many pairs per group)
-int attn_groups(int T, int R);
+int attn_groups(const Dims& D, int T, int R);
 void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
                       cudaStream_t st);
 void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, float* xres, cudaStream_t st);

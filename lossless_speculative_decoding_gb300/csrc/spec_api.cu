@@ -377,9 +377,6 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
   m->R = c.max_draft + 1;
   m->prefill_chunk = c.prefill_chunk > 0 ? c.prefill_chunk : 256;
   m->Tmax = std::max(c.max_batch * m->R, m->prefill_chunk);
-  if (attn_groups(c.max_batch * m->R, m->R) > ATT_MAX_GROUPS ||
-      attn_groups(m->prefill_chunk, m->prefill_chunk) > ATT_MAX_GROUPS)
-    return fail(SPEC_ERR_ARG, "max_batch x ceil((max_draft + 1) / 32) exceeds the attention group limit");
   Dims& D = m->D;
   D.L = c.n_layers; D.h = c.hidden; D.Hq = c.n_q_heads; D.Hkv = c.n_kv_heads; D.d = c.head_dim;
   D.E = c.n_experts; D.k = c.top_k; D.S = c.n_shared; D.inter = c.inter; D.V = c.vocab;
@@ -392,6 +389,9 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
     CU(cudaDeviceGetAttribute(&D.n_sm, cudaDevAttrMultiProcessorCount, dev));
   }
   D.page_elems = (size_t)c.n_layers * 2 * c.n_kv_heads * c.page_size * c.head_dim;
+  if (attn_groups(D, c.max_batch * m->R, m->R) > ATT_MAX_GROUPS ||
+      attn_groups(D, m->prefill_chunk, m->prefill_chunk) > ATT_MAX_GROUPS)
+    return fail(SPEC_ERR_ARG, "max_batch x ceil((max_draft + 1) / rows per group) exceeds the attention group limit");
   const size_t kv_elt = D.act_f32 ? 4 : 2;
 
   CU(configure_gemv_kernels());
