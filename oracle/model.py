@@ -203,12 +203,18 @@ def moe_ffn(cfg, layer: dict, u: np.ndarray) -> np.ndarray:
     return y
 
 
-def forward(m: OracleModel, cache: KVCache, x: np.ndarray, positions: np.ndarray) -> np.ndarray:
+def forward(m: OracleModel, cache: KVCache, x: np.ndarray, positions: np.ndarray,
+            trace: Optional[dict] = None) -> np.ndarray:
     """Run rows ``x`` [n, h] at consecutive absolute ``positions`` (the first
     equal to the current cache length) through the decoder, appending their
     keys/values to ``cache``; returns float32 logits [n, vocab]. Rows attend
     causally to the cache and to earlier rows of the same call, which is the
-    teacher-forced parallel scoring a verify step performs ([E2E] section 6.1)."""
+    teacher-forced parallel scoring a verify step performs ([E2E] section 6.1).
+
+    With ``trace`` (a dict), ``trace["route_gap"]`` receives, per row, the
+    smallest gap over the layers between the k-th and (k+1)-th largest router
+    logits: how close the row's expert choice came to a tie (a diagnostic
+    output only; the arithmetic is unchanged)."""
     cfg = m.cfg
     positions = np.asarray(positions)
     assert positions[0] == cache.length
@@ -228,6 +234,10 @@ def forward(m: OracleModel, cache: KVCache, x: np.ndarray, positions: np.ndarray
         o = attention_rows(q, cache.k[l], cache.v[l], positions, hk)
         x = x + (o.reshape(n, hq * d) @ L["w_o"].T).astype(np.float32)
         u = rms_norm(x, L["ffn_norm"], cfg.rms_eps)
+        if trace is not None and cfg.n_experts > cfg.top_k:
+            rl = np.sort((u @ L["w_router"].T).astype(np.float32), axis=-1)[:, ::-1]
+            gap = rl[:, cfg.top_k - 1] - rl[:, cfg.top_k]
+            trace["route_gap"] = np.minimum(trace.get("route_gap", np.full(n, np.inf, np.float32)), gap)
         x = x + moe_ffn(cfg, L, u)
     u = rms_norm(x, m.final_norm, cfg.rms_eps)
     return (u @ m.lm_head.T).astype(np.float32)
@@ -287,13 +297,13 @@ def accept(drafts: Sequence[int], g: Sequence[int]) -> Tuple[int, int]:
 
 
 def verify_rows(m: OracleModel, cache: KVCache, last_token: int,
-                drafts: Sequence[int]) -> np.ndarray:
+                drafts: Sequence[int], trace: Optional[dict] = None) -> np.ndarray:
     """One verify forward: score rows [last_token, d_1..d_m] at the next
     positions in a single teacher-forced pass; returns logits [m+1, vocab]
     (the cache gains m+1 rows; the caller rolls back rejected ones)."""
     toks = np.array([last_token] + [int(d) for d in drafts], dtype=np.int64)
     p0 = cache.length
-    return forward(m, cache, m.tok_embed[toks], np.arange(p0, p0 + len(toks)))
+    return forward(m, cache, m.tok_embed[toks], np.arange(p0, p0 + len(toks)), trace)
 
 
 def spec_decode(m: OracleModel, prompt, n_new: int, k: int,
