@@ -231,7 +231,8 @@ int spec_lmhead_argmax(const float* x_dev, int T, int hidden, int vocab, const v
 /* Tensor-core GEMM check: with weights A [M, K] (bf16, or e4m3 when a_fp8,
  * then scaled per row by a_scale_dev[m]) and activations X = B + B_lo (bf16
  * [N, K] each, row-major, device; b_lo_dev may be NULL), in CTAs of n_tile
- * activation rows (32, 64 or 128; 0 = 128), dual = 0 writes
+ * activation rows (32, 64 or 128; 0 = 128) and k_split K splits (0 or 1: none;
+ * partials summed in split order by the tile's last split), dual = 0 writes
  * out_dev[n][m] = sum_k A[m][k] * X[n][k] (fp32 [N, M]); dual = 1 writes
  * out_dev[n][m] = bf16(silu(A[m]·X[n]) * (A2[m]·X[n])) (bf16 [N, M]) -- the
  * epilogues the expert GEMMs use. The scale pointers may be NULL (1.0). M a
@@ -239,7 +240,7 @@ int spec_lmhead_argmax(const float* x_dev, int T, int hidden, int vocab, const v
  * (8 = an mbarrier wait ran out). Enqueued on cuda_stream. */
 int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const float* a_scale_dev, const float* a2_scale_dev,
                       int a_fp8, const void* b_dev, const void* b_lo_dev, int M, int N, int K, int dual, int n_tile,
-                      void* out_dev, int* err_dev, uintptr_t cuda_stream);
+                      int k_split, void* out_dev, int* err_dev, uintptr_t cuda_stream);
 
 /* Same computation as spec_lmhead_argmax for callers that cannot allocate
  * device memory (no cudaMalloc of their own, none by the library): the

@@ -155,8 +155,10 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- the CTA's group and columns (whole-CTA early exits happen before any set-up) ----
-  const int nt = blockIdx.x, mt = blockIdx.y, slot = blockIdx.z;   // N tiles vary fastest: CTAs sharing a weight tile run together
-  const int n_groups = P.g_n ? *P.g_n : (int)gridDim.z;
+  // N tiles vary fastest (CTAs sharing a weight tile run together); z = group x K split
+  const int ksn = P.ksplit > 1 ? P.ksplit : 1;
+  const int nt = blockIdx.x, mt = blockIdx.y, slot = blockIdx.z / ksn, ks = blockIdx.z % ksn;
+  const int n_groups = P.g_n ? *P.g_n : (int)gridDim.z / ksn;
   if (slot >= n_groups) return;
   const int grp = P.g_expert ? P.g_expert[slot] : slot;
   const int off = P.g_off ? P.g_off[slot] : 0;
@@ -173,7 +175,9 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   const int STAGES = tc_stage_count(DUAL, F8, nsub, P.split);
   const int STG_OFF = TC_A_BYTES * (1 + DUAL) + (P.split ? 2 : 1) * BB;
   unsigned char* stages = smem + TC_HDR;
-  const int KT = P.K / TC_BK;
+  // this split's K tiles [kt0, kt1) (the host picks splits that are never empty)
+  const int KTall = P.K / TC_BK, KTs = (KTall + ksn - 1) / ksn;
+  const int kt0 = ks * KTs, kt1 = min(KTall, kt0 + KTs), KT = kt1 - kt0;
   const int wrow = grp * P.Mg + mt * TC_BM;           // first weight row of the tile
   // Independent accumulators, so consecutive MMAs do not wait on each other:
   // accumulator (part, kb) takes the hi (part 0) or lo (part 1) activations of
@@ -205,9 +209,9 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   if (warp == 0 && lane == 0) {
     // ---- TMA producer ----
     const uint32_t bytes = (F8 ? TC_A8_BYTES : TC_A_BYTES) * (1 + DUAL) + (P.split ? 2 : 1) * nsub * TC_NSUB * TC_BK * 2;
-    for (int kt = 0; kt < KT; ++kt) {
-      const int s = kt % STAGES;
-      if (kt >= STAGES && !mbar_wait(smem_u32(bars + TC_MAXST + s), ((kt / STAGES) - 1) & 1)) {
+    for (int i = 0; i < KT; ++i) {
+      const int kt = kt0 + i, s = i % STAGES;
+      if (i >= STAGES && !mbar_wait(smem_u32(bars + TC_MAXST + s), ((i / STAGES) - 1) & 1)) {
         atomicOr(P.err, DERR_TIMEOUT);
         *abort_flag = 1;
         break;
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full), "r"(bytes) : "memory");
       unsigned char* at = F8 ? st + STG_OFF : st;
       constexpr int AST = F8 ? TC_A8_BYTES : TC_A_BYTES;
-      const size_t toff = ((size_t)(wrow / TC_BM) * KT + kt) * AST;   // pre-tiled weights
+      const size_t toff = ((size_t)(wrow / TC_BM) * KTall + kt) * AST;   // pre-tiled weights
       bulk_g2s(smem_u32(at), static_cast<const unsigned char*>(P.wa) + toff, AST, full);
       if (DUAL) bulk_g2s(smem_u32(at + AST), static_cast<const unsigned char*>(P.wa2) + toff, AST, full);
       unsigned char* bt = st + TC_A_BYTES * (1 + DUAL);
@@ -231,10 +235,10 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
     // ---- MMA issuer ----
     const uint32_t idesc = tc_idesc(N);
     bool ok = true;
-    for (int kt = 0; kt < KT && ok; ++kt) {
-      const int s = kt % STAGES;
+    for (int i = 0; i < KT && ok; ++i) {
+      const int s = i % STAGES;
       // bf16: the TMA bytes of the stage; F8: the converters' signal (after those bytes)
-      if (!mbar_wait(smem_u32(bars + (F8 ? 2 * TC_MAXST + 1 : 0) + s), (kt / STAGES) & 1)) {
+      if (!mbar_wait(smem_u32(bars + (F8 ? 2 * TC_MAXST + 1 : 0) + s), (i / STAGES) & 1)) {
         atomicOr(P.err, DERR_TIMEOUT);
         *abort_flag = 1;
         ok = false;
@@ -248,7 +252,7 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
         // hi and (optionally) lo activations, each into its own accumulator
         for (int part = 0; part < (P.split ? 2 : 1); ++part) {
           const uint64_t bd = sw128_desc(b0 + part * BB + k * 32);
-          const uint32_t acc = (kt > 0 || k >= NKB) ? 1u : 0u;   // first MMA of an accumulator overwrites
+          const uint32_t acc = (i > 0 || k >= NKB) ? 1u : 0u;    // first MMA of an accumulator overwrites
           const uint32_t col = (uint32_t)((part * NKB + (k % NKB)) * TC_MAXN);
           const uint64_t ad = sw128_desc(a0 + k * 32);
           asm volatile(
@@ -273,9 +277,9 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   } else if (F8 && warp >= 4) {
     // ---- converters: e4m3 staging -> swizzled bf16 operand tile ----
     const int t = threadIdx.x - 128;
-    for (int kt = 0; kt < KT; ++kt) {
-      const int s = kt % STAGES;
-      if (!mbar_wait(smem_u32(bars + s), (kt / STAGES) & 1)) {
+    for (int i = 0; i < KT; ++i) {
+      const int s = i % STAGES;
+      if (!mbar_wait(smem_u32(bars + s), (i / STAGES) & 1)) {
         if (lane == 0) atomicOr(P.err, DERR_TIMEOUT);
         break;
       }
@@ -294,43 +298,42 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   const bool have = __syncthreads_and(mbar_wait(smem_u32(bars + 2 * TC_MAXST), 0)) != 0;   // block-uniform
   if (!have && threadIdx.x == 0) atomicOr(P.err, DERR_TIMEOUT);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  if (warp < 4) {
   const int m = warp * 32 + lane;                     // row within the tile
   const int col = mt * TC_BM + m;                     // output feature (row within the group)
-  const float sc = (P.scale && have) ? P.scale[wrow + m] : 1.f;
-  const float sc2 = (DUAL && P.scale2 && have) ? P.scale2[wrow + m] : 1.f;
-  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  const float sc = (P.scale && have && warp < 4) ? P.scale[wrow + m] : 1.f;
+  const float sc2 = (DUAL && P.scale2 && have && warp < 4) ? P.scale2[wrow + m] : 1.f;
+  const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   __shared__ float red_v[4][TC_NSUB];
   __shared__ int red_i[4][TC_NSUB];
-  for (int c0 = 0; c0 < N; c0 += 16) {
-    // v = sum of the used accumulators in order (part 0 kb 0, part 0 kb 1, part 1 ...)
-    float v[16], u2[16];
-    {
-      float t[NACC][16], t2[NACC][16];
-      const int nacc = (P.split ? 2 : 1) * NKB;
+  __shared__ int s_last;
+  // v = sum of the used accumulators in order (part 0 kb 0, part 0 kb 1, part 1 ...)
+  auto load_acc = [&](int c0, float (&v)[16], float (&u2)[16]) {
+    float t[NACC][16], t2[NACC][16];
+    const int nacc = (P.split ? 2 : 1) * NKB;
 #pragma unroll
-      for (int a = 0; a < NACC; ++a) {
-        if (a < nacc) {
-          tmem_ld16(trow + a * TC_MAXN + c0, t[a]);
-          if (DUAL) tmem_ld16(trow + (NACC + a) * TC_MAXN + c0, t2[a]);
-        }
-      }
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float x = t[0][j], y = DUAL ? t2[0][j] : 0.f;
-#pragma unroll
-        for (int a = 1; a < NACC; ++a) {
-          if (a < nacc) {
-            x += t[a][j];
-            if (DUAL) y += t2[a][j];
-          }
-        }
-        v[j] = x;
-        u2[j] = y;
+    for (int a = 0; a < NACC; ++a) {
+      if (a < nacc) {
+        tmem_ld16(trow + a * TC_MAXN + c0, t[a]);
+        if (DUAL) tmem_ld16(trow + (NACC + a) * TC_MAXN + c0, t2[a]);
       }
     }
-    if (!have) continue;
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float x = t[0][j], y = DUAL ? t2[0][j] : 0.f;
+#pragma unroll
+      for (int a = 1; a < NACC; ++a) {
+        if (a < nacc) {
+          x += t[a][j];
+          if (DUAL) y += t2[a][j];
+        }
+      }
+      v[j] = x;
+      u2[j] = y;
+    }
+  };
+  // the epilogue of columns c0..c0+15 (warps 0-3)
+  auto emit = [&](int c0, const float (&v)[16], const float (&u2)[16]) {
     if (P.epi == TC_ARGMAX) {
       // per column: max over the tile's 128 rows, lowest row on ties
 #pragma unroll
@@ -366,7 +369,7 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
       }
-      continue;
+      return;
     }
     if (P.epi == TC_ADD) {
       // all sixteen residual values are loaded before any store (a load-add-
@@ -382,7 +385,7 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
         const int n = n0 + c0 + j;
         if (n < n0 + nrows) P.out_f32[(size_t)(off + n) * P.ldo + col] = old[j] + v[j] * sc;
       }
-      continue;
+      return;
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -401,8 +404,65 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
         if (P.out_bf16_lo) P.out_bf16_lo[r * P.ldo + col] = f_to_bf16(hv - bf16_to_f(hi));
       }
     }
+  };
+  if (ksn == 1) {
+    if (warp < 4) {
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        float v[16], u2[16];
+        load_acc(c0, v, u2);
+        if (have) emit(c0, v, u2);
+      }
+    }
+  } else {
+    // split K: every split stores its fp32 partial [split][part][row][feature];
+    // the last split of the tile to arrive adds them in split order and runs
+    // the epilogue (the order does not depend on which split came last)
+    const size_t pstride = (size_t)P.part_n * P.part_m;
+    const size_t feat = (size_t)wrow + m;
+    if (warp < 4) {
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        float v[16], u2[16];
+        load_acc(c0, v, u2);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int n = n0 + c0 + j;
+          if (n >= n0 + nrows) break;
+          const size_t e = (size_t)(off + n) * P.part_m + feat;
+          P.part[(size_t)ks * (1 + DUAL) * pstride + e] = v[j];
+          if (DUAL) P.part[((size_t)ks * 2 + 1) * pstride + e] = u2[j];
+        }
+      }
+    }
+    __threadfence();
+    __syncthreads();
+    const int tile = ((slot * (int)gridDim.y) + mt) * (int)gridDim.x + nt;
+    if (threadIdx.x == 0) s_last = atomicAdd(P.tile_cnt + tile, 1) == ksn - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      if (warp < 4 && have) {
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          float v[16], u2[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = n0 + c0 + j;
+            float x = 0.f, y = 0.f;
+            if (n < n0 + nrows) {
+              const size_t e = (size_t)(off + n) * P.part_m + feat;
+              for (int q = 0; q < ksn; ++q) {
+                x += __ldcg(P.part + (size_t)q * (1 + DUAL) * pstride + e);
+                if (DUAL) y += __ldcg(P.part + ((size_t)q * 2 + 1) * pstride + e);
+              }
+            }
+            v[j] = x;
+            u2[j] = y;
+          }
+          emit(c0, v, u2);
+        }
+      }
+      if (threadIdx.x == 0) P.tile_cnt[tile] = 0;
+    }
   }
-  }   // warp < 4
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -479,13 +539,19 @@ int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t row
 // out_bf16[n][m] = silu(A[m]·X[n]) * (A2[m]·X[n]) (dual = 1).
 extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const float* a_scale_dev,
                                  const float* a2_scale_dev, int a_fp8, const void* b_dev, const void* b_lo_dev,
-                                 int M, int N, int K, int dual, int n_tile, void* out_dev, int* err_dev,
-                                 uintptr_t cuda_stream) {
+                                 int M, int N, int K, int dual, int n_tile, int k_split, void* out_dev,
+                                 int* err_dev, uintptr_t cuda_stream) {
   using namespace spec;
   if (!a_dev || !b_dev || !out_dev || !err_dev || (dual && !a2_dev)) return set_last_error(-1, "null pointer");
   if (M < TC_BM || M % TC_BM || K < TC_BK || K % TC_BK || N < 1) return set_last_error(-1, "M, K multiples of 128, 64");
   if (n_tile == 0) n_tile = TC_MAXN;
   if (n_tile != 32 && n_tile != 64 && n_tile != 128) return set_last_error(-1, "n_tile: 32, 64 or 128");
+  if (k_split < 1) k_split = 1;
+  if (k_split > K / TC_BK) return set_last_error(-1, "k_split larger than the K tiles");
+  {
+    const int kts = (K / TC_BK + k_split - 1) / k_split;   // splits the kernel sees are never empty
+    k_split = (K / TC_BK + kts - 1) / kts;
+  }
   static bool configured = false;
   if (!configured) {
     if (configure_tc_kernels() != cudaSuccess) return set_last_error(-3, "tc kernel attributes");
@@ -516,9 +582,23 @@ extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const fl
   P.err = err_dev;
   P.split = b_lo_dev != nullptr;
   P.ntile = n_tile;
-  launch_tc_gemm(maps, P, M / TC_BM, 1, (N + n_tile - 1) / n_tile, st);
+  P.ksplit = k_split;
+  const int n_tiles = (N + n_tile - 1) / n_tile;
+  float* part = nullptr;
+  int* cnt = nullptr;
+  if (k_split > 1) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&part), (size_t)k_split * (1 + dual) * N * M * sizeof(float), st) !=
+            cudaSuccess ||
+        cudaMallocAsync(reinterpret_cast<void**>(&cnt), (size_t)(M / TC_BM) * n_tiles * sizeof(int), st) != cudaSuccess)
+      return set_last_error(-5, "scratch allocation");
+    cudaMemsetAsync(cnt, 0, (size_t)(M / TC_BM) * n_tiles * sizeof(int), st);
+    P.part = part; P.part_n = N; P.part_m = M; P.tile_cnt = cnt;
+  }
+  launch_tc_gemm(maps, P, M / TC_BM, k_split, n_tiles, st);
   for (int i = 0; i < 2; ++i)
     if (wt[i]) cudaFreeAsync(wt[i], st);
+  if (part) cudaFreeAsync(part, st);
+  if (cnt) cudaFreeAsync(cnt, st);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? 0 : set_last_error(-3, cudaGetErrorString(e));
 }

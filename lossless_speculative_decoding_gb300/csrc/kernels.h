@@ -145,6 +145,10 @@ struct TcParams {
   uint16_t* out_bf16_lo;  // SWIGLU low part (value - hi), nullable
   int split;              // activations given as hi + lo operands
   int ntile;              // activation rows per CTA: 32, 64 or 128 (0: 128)
+  int ksplit;             // K splits (grid z = groups x ksplit); > 1: partials in `part`, summed by the last split
+  float* part;            // [ksplit][1 + dual][part_n][part_m] fp32 partials
+  int part_n, part_m;     // activation rows / weight rows of the launch
+  int* tile_cnt;          // per (group, m tile, n tile) arrival counters, zero between launches
   const int* perm;
   const float* scale;     // per weight row (nullable)
   const float* scale2;    // per weight row of the second operand (SWIGLU up)

@@ -111,6 +111,24 @@ struct Prefix {
 
 int spec::set_last_error(int code, const char* msg) { return fail(code, msg); }
 
+// K splits of a tensor-core launch: when its CTAs (weight tiles x activation
+// tiles x groups) leave SMs idle, as many splits as still fit in one wave of
+// one CTA per SM, each keeping >= 16 K tiles and none empty. The CTA count is
+// taken at the model's verify rows (max_batch x (K + 1)), a model constant,
+// never at a step's own rows, so a row's arithmetic is the same in every
+// step. MoE launches have many groups and never split.
+static int tc_ksplit(int n_sm, int m_tiles, int groups, int n_tiles, int KT) {
+  if (groups > 1) return 1;
+  int ks = n_sm / (m_tiles * n_tiles);
+  ks = std::min(ks, std::max(1, KT / 16));
+  if (ks <= 1) return 1;
+  const int kts = (KT + ks - 1) / ks;
+  return (KT + kts - 1) / kts;
+}
+
+// activation rows per CTA of a dense tensor-core launch (see tc_dense)
+static int tc_dense_ntile(int n_sm, int M, int T) { return (M / 128) * ((T + 127) / 128) < n_sm ? 32 : 128; }
+
 struct spec_model {
   spec_config cfg{};
   cudaStream_t stream = nullptr;
@@ -118,6 +136,7 @@ struct spec_model {
   DevState S{};
   StepBuf B{};
   int K = 0, R = 1, Tmax = 1, prefill_chunk = 256;
+  int Tv = 1;                      // verify rows of the largest batch (max_batch x R)
   std::vector<void*> allocs;
   std::vector<void*> wptr;         // device pointer per tensor (nullptr if absent)
   std::vector<LayerW> layers;
@@ -142,6 +161,8 @@ struct spec_model {
   // tensor-core path (bf16 weights, more than 8 rows per step): tensor maps of
   // every weight and of the bf16 activation operands
   bool use_tc = false;
+  float* tc_part = nullptr;                                     // split-K partials
+  int* tc_cnt = nullptr;                                        // split-K tile arrival counters
   CUtensorMap tc_xn, tc_o, tc_xperm, tc_hperm;                 // activations: hi
   CUtensorMap tc_xn_lo, tc_o_lo, tc_xperm_lo, tc_hperm_lo;     //              lo
 
@@ -229,8 +250,11 @@ struct spec_model {
     // too few CTAs for the GPU with 128-row activation tiles (small projections
     // at moderate T): 32-row tiles quadruple them; the weight tile is then read
     // by CTAs that run side by side (N tiles vary fastest) and hits in L2
-    P.ntile = (M / 128) * ((T + 127) / 128) < D.n_sm ? 32 : 128;
-    launch_tc_gemm(mp, P, M / 128, 1, (T + P.ntile - 1) / P.ntile, stream);
+    P.ntile = tc_dense_ntile(D.n_sm, M, T);
+    const int tv = Tv, ntv = tc_dense_ntile(D.n_sm, M, tv);
+    P.ksplit = tc_ksplit(D.n_sm, M / 128, 1, (tv + ntv - 1) / ntv, K / 64);
+    P.part = tc_part; P.part_n = T; P.part_m = M; P.tile_cnt = tc_cnt;
+    launch_tc_gemm(mp, P, M / 128, P.ksplit, (T + P.ntile - 1) / P.ntile, stream);
   }
   void tc_grouped(const void* w, const void* w2, const CUtensorMap& b, const CUtensorMap& blo, int K, int Mg, int T,
                   int epi, float* out_f32, uint16_t* out_bf16, uint16_t* out_lo, int ldo,
@@ -245,7 +269,9 @@ struct spec_model {
     P.g_expert = B.act_expert; P.g_off = B.act_off; P.g_cnt = B.act_cnt; P.g_n = B.n_active;
     const int max_active = (D.E > 0 ? std::min(D.E, T * D.k) : 0) + D.S;
     P.ntile = 128;   // a small group's CTA still runs N = 32 with a deeper pipeline
-    launch_tc_gemm(mp, P, Mg / 128, max_active, (T + 127) / 128, stream);
+    P.ksplit = tc_ksplit(D.n_sm, Mg / 128, max_active, (Tv * D.NS + 127) / 128, K / 64);
+    P.part = tc_part; P.part_n = T * D.NS; P.part_m = Mg * max_active; P.tile_cnt = tc_cnt;
+    launch_tc_gemm(mp, P, Mg / 128, max_active * P.ksplit, (T + 127) / 128, stream);
   }
 
   // Enqueue one forward over T rows already assembled in B (row meta + x);
@@ -377,6 +403,7 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
   m->R = c.max_draft + 1;
   m->prefill_chunk = c.prefill_chunk > 0 ? c.prefill_chunk : 256;
   m->Tmax = std::max(c.max_batch * m->R, m->prefill_chunk);
+  m->Tv = c.max_batch * m->R;
   Dims& D = m->D;
   D.L = c.n_layers; D.h = c.hidden; D.Hq = c.n_q_heads; D.Hkv = c.n_kv_heads; D.d = c.head_dim;
   D.E = c.n_experts; D.k = c.top_k; D.S = c.n_shared; D.inter = c.inter; D.V = c.vocab;
@@ -535,6 +562,33 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
     bad |= tc_make_map(&m->tc_xperm_lo, B.xperm_lo, D.h, (uint64_t)T * NS, 32);
     bad |= tc_make_map(&m->tc_hperm_lo, B.hperm_lo, D.inter, (uint64_t)T * NS, 32);
     if (bad) return fail(SPEC_ERR_CUDA, "tensor map encoding failed");
+    // split-K scratch: the largest [splits][1 + dual][rows][features] of the step's launches
+    {
+      const int tv = m->Tv;
+      auto dn = [&](int M) { const int nt = tc_dense_ntile(D.n_sm, M, tv); return (tv + nt - 1) / nt; };
+      const int ks_q = tc_ksplit(D.n_sm, qkv_rows / 128, 1, dn(qkv_rows), D.h / 64);
+      const int ks_o = tc_ksplit(D.n_sm, D.h / 128, 1, dn(D.h), D.Hq * D.d / 64);
+      const int ks_l = tc_ksplit(D.n_sm, D.V / 128, 1, dn(D.V), D.h / 64);
+      const int gmin = (D.E > 0 ? 1 : 0) + D.S;        // fewest groups an expert launch can have
+      const int ga = (D.E > 0 ? std::min(D.E, T * D.k) : 0) + D.S;   // most groups
+      const int ks_g = tc_ksplit(D.n_sm, D.inter / 128, gmin, (tv * NS + 127) / 128, D.h / 64);
+      const int ks_d = tc_ksplit(D.n_sm, D.h / 128, gmin, (tv * NS + 127) / 128, D.inter / 64);
+      size_t part = 0, tiles = 0;
+      auto need = [&](int ks, int dual, size_t rows, size_t feats, size_t mtiles, size_t ntiles) {
+        if (ks <= 1) return;
+        part = std::max(part, (size_t)ks * (1 + dual) * rows * feats);
+        tiles = std::max(tiles, mtiles * ntiles);
+      };
+      need(ks_q, 0, T, qkv_rows, qkv_rows / 128, (T + 31) / 32);
+      need(ks_o, 0, T, D.h, D.h / 128, (T + 31) / 32);
+      need(ks_l, 0, T, D.V, D.V / 128, (T + 31) / 32);
+      need(ks_g, 1, (size_t)T * NS, (size_t)D.inter * ga, D.inter / 128, ((size_t)T * NS + 127) / 128);
+      need(ks_d, 0, (size_t)T * NS, (size_t)D.h * ga, D.h / 128, ((size_t)T * NS + 127) / 128);
+      if (part) {
+        if ((rc = m->dalloc(&m->tc_part, part)) || (rc = m->dalloc(&m->tc_cnt, tiles))) return rc;
+        CU(cudaMemset(m->tc_cnt, 0, tiles * sizeof(int)));
+      }
+    }
   }
   m->step_in_n = c.max_batch * (2 + m->K);
   m->step_out_n = 2 * c.max_batch + 1;   // acc | bonus | device error bits

@@ -126,3 +126,47 @@ def test_tc_gemm_fp8_weights(M, N, K, dual, nt):
     else:
         ref = xf @ w1.T
         np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=0, atol=5e-5 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("M,N,K,dual,ks,fp8", [(256, 40, 1280, 0, 4, 0), (128, 300, 2048, 0, 8, 0), (256, 48, 1280, 1, 3, 0),
+                                               (128, 33, 1280, 0, 5, 1), (128, 64, 640, 1, 2, 1)])
+def test_tc_gemm_split_k(M, N, K, dual, ks, fp8):
+    """K split across CTAs: each split's fp32 partial is stored and the tile's
+    last split adds them in split order, then runs the store / SwiGLU epilogue."""
+    import torch
+    from lossless_speculative_decoding_gb300 import binding as B
+    rng = np.random.default_rng(13 * M + N + ks)
+    if fp8:
+        def mat():
+            w = (rng.standard_normal((M, K)) * 0.05).astype(np.float32)
+            codes, sc = syn.quantize_rows_e4m3(w)
+            return codes.view(np.int8), sc, oracle.decode_e4m3(codes).astype(np.float64) * sc[:, None]
+    else:
+        def mat():
+            bits, f = _bf16(rng, (M, K), 0.05)
+            return bits.view(np.int16), None, f.astype(np.float64)
+    a, sa, w1 = mat()
+    a2, sa2, w2 = mat()
+    x = rng.standard_normal((N, K)).astype(np.float32)
+    hi = syn.f32_to_bf16_bits(x)
+    lo = syn.f32_to_bf16_bits((x - oracle.decode_bf16(hi)).astype(np.float32))
+    dev = lambda v: None if v is None else torch.from_numpy(np.ascontiguousarray(v)).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    xf = x.astype(np.float64)
+    if dual:
+        out = torch.zeros((N, M), dtype=torch.int16, device="cuda")
+        B.spec_tc_gemm_test(dev(a), dev(a2), dev(hi.view(np.int16)), dev(lo.view(np.int16)), M, N, K, 1, out, err, 0,
+                            a_scale_dev=dev(sa), a2_scale_dev=dev(sa2), a_fp8=bool(fp8), k_split=ks)
+        torch.cuda.synchronize()
+        gg, uu = xf @ w1.T, xf @ w2.T
+        ref = gg / (1 + np.exp(-gg)) * uu
+        got = oracle.decode_bf16(out.cpu().numpy().view(np.uint16)).astype(np.float64)
+        np.testing.assert_allclose(got, ref, rtol=1e-2, atol=1e-2 * np.abs(ref).max())
+    else:
+        out = torch.full((N, M), float("nan"), device="cuda")
+        B.spec_tc_gemm_test(dev(a), None, dev(hi.view(np.int16)), dev(lo.view(np.int16)), M, N, K, 0, out, err, 0,
+                            a_scale_dev=dev(sa), a_fp8=bool(fp8), k_split=ks)
+        torch.cuda.synchronize()
+        ref = xf @ w1.T
+        np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=0, atol=5e-5 * np.abs(ref).max())
+    assert int(err.item()) == 0
