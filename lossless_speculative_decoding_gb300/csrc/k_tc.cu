@@ -4,12 +4,14 @@
 // fill the MMA's M = 128 rows, activation rows X its N <= 128 columns, so a
 // CTA streams one 128-row weight tile once for all of its tokens. The
 // activations are given as two bf16 operands, X = X_hi + X_lo (about 16
-// mantissa bits), and both are multiplied into the same fp32 accumulator, so
-// the result keeps near-fp32 activation precision while the weights stay
-// exact bf16. Weights are stored pre-tiled (tc_pack_weights): every 128-row x
-// 64-element tile is one contiguous 16 KB block holding the exact 128-byte-
-// swizzled shared-memory image, so a stage fetches it with a single linear
-// bulk copy (cp.async.bulk) instead of 128 strided row pieces; activation tiles
+// mantissa bits): one MMA takes the hi rows and then the lo rows as its N
+// columns and the epilogue adds the two, so the result keeps near-fp32
+// activation precision while the weights stay exact bf16. Weights are stored
+// pre-tiled (tc_pack_weights): every 128-row x 64-element tile (an atom) is
+// one contiguous 16 KB block holding the exact 128-byte-swizzled shared-memory
+// image, and the atoms of a row tile follow each other along K, so a stage
+// fetches its one or two atoms with a single linear bulk copy
+// (cp.async.bulk) instead of 128 strided row pieces; activation tiles
 // come by TMA (cp.async.bulk.tensor, 128-byte swizzle). Stages run through a
 // multi-stage mbarrier pipeline as deep as shared memory allows; one thread issues tcgen05.mma into a TMEM
 // accumulator (fp32, lane = weight row, column = token); four warps read it
@@ -37,9 +39,10 @@
 namespace spec {
 
 constexpr int TC_BM = 128;            // weight rows per CTA (MMA M)
-constexpr int TC_BK = 64;             // K elements per stage (128 bytes of bf16)
+constexpr int TC_BK = 64;             // K elements per atom (128 bytes of bf16, one swizzle row)
 constexpr int TC_NSUB = 32;           // activation rows per TMA box
-constexpr int TC_MAXN = 128;          // columns per CTA (largest N tile)
+constexpr int TC_MAXN = 128;          // activation rows per CTA (largest N tile)
+constexpr int TC_ACCW = 2 * TC_MAXN;  // TMEM columns of one accumulator (hi rows, then lo rows)
 constexpr uint32_t TC_WAIT_LIMIT = 1u << 20;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;        // 16 KB
 constexpr int TC_A8_BYTES = TC_BM * TC_BK;           // 8 KB e4m3 staging per weight operand
@@ -48,17 +51,22 @@ constexpr int TC_MAXST = 12;          // pipeline stages at most
 constexpr int TC_SMEM = 220 * 1024;   // dynamic shared memory of every CTA
 constexpr int TC_HDR = 1024;          // barriers + TMEM slot, ahead of the stages
 
-// Bytes of one pipeline stage for nsub 32-row activation boxes: weight
-// tile(s), activation hi (+ lo), e4m3 staging (FP8). Every part is a multiple
-// of 1024 bytes, so each stays aligned for the 128-byte swizzle.
-__host__ __device__ constexpr int tc_stage_bytes(int dual, int f8, int nsub, int split) {
-  return (TC_A_BYTES + (f8 ? TC_A8_BYTES : 0)) * (1 + dual) + (split ? 2 : 1) * nsub * TC_NSUB * TC_BK * 2;
+// Bytes of one pipeline stage of `at` K atoms for nsub 32-row activation
+// boxes: weight tile(s), activation hi (+ lo), e4m3 staging (FP8). Every part
+// is a multiple of 1024 bytes, so each stays aligned for the 128-byte swizzle.
+__host__ __device__ constexpr int tc_stage_bytes(int dual, int f8, int nsub, int split, int at) {
+  return at * ((TC_A_BYTES + (f8 ? TC_A8_BYTES : 0)) * (1 + dual) + (split ? 2 : 1) * nsub * TC_NSUB * TC_BK * 2);
 }
 // Stages that fit: as many weight tiles in flight as shared memory allows.
-__host__ __device__ constexpr int tc_stage_count(int dual, int f8, int nsub, int split) {
-  return (TC_SMEM - TC_HDR - 1024) / tc_stage_bytes(dual, f8, nsub, split) < TC_MAXST
-             ? (TC_SMEM - TC_HDR - 1024) / tc_stage_bytes(dual, f8, nsub, split)
+__host__ __device__ constexpr int tc_stage_count(int dual, int f8, int nsub, int split, int at) {
+  return (TC_SMEM - TC_HDR - 1024) / tc_stage_bytes(dual, f8, nsub, split, at) < TC_MAXST
+             ? (TC_SMEM - TC_HDR - 1024) / tc_stage_bytes(dual, f8, nsub, split, at)
              : TC_MAXST;
+}
+// K atoms per stage: two (half the barrier round trips per weight byte)
+// where three such stages still fit, else one.
+__host__ __device__ constexpr int tc_atoms(int dual, int f8, int nsub, int split) {
+  return tc_stage_count(dual, f8, nsub, split, 2) >= 3 ? 2 : 1;
 }
 __host__ __device__ constexpr int tc_threads(int f8) { return f8 ? 256 : 128; }
 
@@ -76,7 +84,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Shared-memory matrix descriptor of a K-major bf16 tile stored as 128-byte
-// rows with the 128-byte swizzle (8-row groups 1024 bytes apart).
+// rows with the 128-byte swizzle (8-row groups 1024 bytes apart). The start
+// address sits in the low 14 bits (16-byte units) and shared addresses stay
+// below 256 KB, so the descriptor of address + o is this one + o / 16.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
@@ -168,24 +178,33 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   if (n0 >= cnt) return;
   const int nrows = min(ntile, cnt - n0);
   const int nsub = (nrows + TC_NSUB - 1) / TC_NSUB;
-  const int N = nsub * TC_NSUB;                       // MMA N: multiple of 32, <= 128
-  // stage layout: [A bf16 (x2 if DUAL)][B hi: nsub boxes][B lo: nsub boxes][A e4m3 staging (x2 if DUAL), F8 only]
-  const int BB = nsub * TC_NSUB * TC_BK * 2;          // one activation part
-  const int SB = tc_stage_bytes(DUAL, F8, nsub, P.split);
-  const int STAGES = tc_stage_count(DUAL, F8, nsub, P.split);
-  const int STG_OFF = TC_A_BYTES * (1 + DUAL) + (P.split ? 2 : 1) * BB;
+  const int N = nsub * TC_NSUB;                       // activation rows: multiple of 32, <= 128
+  const int NP = (P.split ? 2 : 1) * N;               // MMA N: the hi rows, then the lo rows
+  // stage layout, AT K atoms per stage: [A atoms][A2 atoms (DUAL)][B atoms,
+  // each hi rows then lo rows][e4m3 staging (F8): A atoms, A2 atoms]. The lo
+  // box follows the hi box at N x 128 bytes (a whole number of 8-row swizzle
+  // groups), so one MMA with N = NP multiplies the weights into both.
+  const int AT = tc_atoms(DUAL, F8, nsub, P.split);
+  const int BB = N * TC_BK * 2;                       // one activation part of one atom
+  const int BAT = (P.split ? 2 : 1) * BB;             // one B atom
+  const int SB = tc_stage_bytes(DUAL, F8, nsub, P.split, AT);
+  const int STAGES = tc_stage_count(DUAL, F8, nsub, P.split, AT);
+  const int BOFF = AT * TC_A_BYTES * (1 + DUAL);
+  const int STG_OFF = BOFF + AT * BAT;
   unsigned char* stages = smem + TC_HDR;
-  // this split's K tiles [kt0, kt1) (the host picks splits that are never empty)
+  // this split's K atoms [kt0, kt1) (the host picks splits that are never empty)
   const int KTall = P.K / TC_BK, KTs = (KTall + ksn - 1) / ksn;
   const int kt0 = ks * KTs, kt1 = min(KTall, kt0 + KTs), KT = kt1 - kt0;
+  const int NST = (KT + AT - 1) / AT;                 // stages of this CTA
   const int wrow = grp * P.Mg + mt * TC_BM;           // first weight row of the tile
   // Independent accumulators, so consecutive MMAs do not wait on each other:
-  // accumulator (part, kb) takes the hi (part 0) or lo (part 1) activations of
-  // the 16-wide K steps k with k % NKB == kb; the epilogue adds them in a fixed
-  // order. Matrix 2 (DUAL) starts at column TC_MAXN * NACC.
+  // accumulator kb takes the 16-wide K steps k with k % NKB == kb, columns
+  // [0, N) the hi and [N, 2N) the lo activations; the epilogue adds (hi, kb 0),
+  // (hi, kb 1), (lo, kb 0), (lo, kb 1) in that order. Accumulator kb of
+  // matrix mat starts at column (mat * NKB + kb) * TC_ACCW.
   constexpr int NKB = DUAL ? 1 : 2;
   constexpr int NACC = 2 * NKB;
-  constexpr uint32_t NCOL = 512;                      // TMEM columns: (1 + DUAL) * NACC * TC_MAXN
+  constexpr uint32_t NCOL = 512;                      // TMEM columns: (1 + DUAL) * NKB * TC_ACCW
 
   // barrier indices: full s, empty TC_MAXST + s, done 2 TC_MAXST, conv 2 TC_MAXST + 1 + s
   if (threadIdx.x == 0) {
@@ -208,9 +227,9 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
 
   if (warp == 0 && lane == 0) {
     // ---- TMA producer ----
-    const uint32_t bytes = (F8 ? TC_A8_BYTES : TC_A_BYTES) * (1 + DUAL) + (P.split ? 2 : 1) * nsub * TC_NSUB * TC_BK * 2;
-    for (int i = 0; i < KT; ++i) {
-      const int kt = kt0 + i, s = i % STAGES;
+    constexpr int AST = F8 ? TC_A8_BYTES : TC_A_BYTES;
+    for (int i = 0; i < NST; ++i) {
+      const int a0 = i * AT, na = min(AT, KT - a0), s = i % STAGES;
       if (i >= STAGES && !mbar_wait(smem_u32(bars + TC_MAXST + s), ((i / STAGES) - 1) & 1)) {
         atomicOr(P.err, DERR_TIMEOUT);
         *abort_flag = 1;
@@ -218,25 +237,30 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
       }
       unsigned char* st = stages + s * SB;
       const uint32_t full = smem_u32(bars + s);
+      const uint32_t bytes = (uint32_t)na * (AST * (1 + DUAL) + BAT);
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full), "r"(bytes) : "memory");
+      // the stage's atoms of a row tile are contiguous in the pre-tiled weights
       unsigned char* at = F8 ? st + STG_OFF : st;
-      constexpr int AST = F8 ? TC_A8_BYTES : TC_A_BYTES;
-      const size_t toff = ((size_t)(wrow / TC_BM) * KTall + kt) * AST;   // pre-tiled weights
-      bulk_g2s(smem_u32(at), static_cast<const unsigned char*>(P.wa) + toff, AST, full);
-      if (DUAL) bulk_g2s(smem_u32(at + AST), static_cast<const unsigned char*>(P.wa2) + toff, AST, full);
-      unsigned char* bt = st + TC_A_BYTES * (1 + DUAL);
-      for (int j = 0; j < nsub; ++j) {
-        tma_2d(smem_u32(bt + j * TC_NSUB * TC_BK * 2), &mapB, kt * TC_BK, off + n0 + j * TC_NSUB, full);
-        if (P.split)
-          tma_2d(smem_u32(bt + BB + j * TC_NSUB * TC_BK * 2), &mapBlo, kt * TC_BK, off + n0 + j * TC_NSUB, full);
+      const size_t toff = ((size_t)(wrow / TC_BM) * KTall + kt0 + a0) * AST;
+      bulk_g2s(smem_u32(at), static_cast<const unsigned char*>(P.wa) + toff, na * AST, full);
+      if (DUAL) bulk_g2s(smem_u32(at + AT * AST), static_cast<const unsigned char*>(P.wa2) + toff, na * AST, full);
+      for (int j = 0; j < na; ++j) {
+        unsigned char* bt = st + BOFF + j * BAT;
+        const int kx = (kt0 + a0 + j) * TC_BK;
+        for (int q = 0; q < nsub; ++q) {
+          tma_2d(smem_u32(bt + q * TC_NSUB * TC_BK * 2), &mapB, kx, off + n0 + q * TC_NSUB, full);
+          if (P.split) tma_2d(smem_u32(bt + BB + q * TC_NSUB * TC_BK * 2), &mapBlo, kx, off + n0 + q * TC_NSUB, full);
+        }
       }
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
-    const uint32_t idesc = tc_idesc(N);
+    const uint32_t idesc = tc_idesc(NP);
+    const uint64_t d0 = sw128_desc(smem_u32(stages));
     bool ok = true;
-    for (int i = 0; i < KT && ok; ++i) {
-      const int s = i % STAGES;
+    int kstep = 0;                                    // 16-wide K steps issued so far
+    for (int i = 0; i < NST && ok; ++i) {
+      const int s = i % STAGES, na = min(AT, KT - i * AT);
       // bf16: the TMA bytes of the stage; F8: the converters' signal (after those bytes)
       if (!mbar_wait(smem_u32(bars + (F8 ? 2 * TC_MAXST + 1 : 0) + s), (i / STAGES) & 1)) {
         atomicOr(P.err, DERR_TIMEOUT);
@@ -245,27 +269,24 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t a0 = smem_u32(stages + s * SB);
-      const uint32_t b0 = a0 + TC_A_BYTES * (1 + DUAL);
+      const uint64_t ds = d0 + (uint64_t)((s * SB) >> 4);
+      for (int j = 0; j < na; ++j) {
+        const uint64_t da = ds + (uint64_t)((j * TC_A_BYTES) >> 4);
+        const uint64_t db = ds + (uint64_t)((BOFF + j * BAT) >> 4);
 #pragma unroll
-      for (int k = 0; k < TC_BK / 16; ++k) {
-        // hi and (optionally) lo activations, each into its own accumulator
-        for (int part = 0; part < (P.split ? 2 : 1); ++part) {
-          const uint64_t bd = sw128_desc(b0 + part * BB + k * 32);
-          const uint32_t acc = (i > 0 || k >= NKB) ? 1u : 0u;    // first MMA of an accumulator overwrites
-          const uint32_t col = (uint32_t)((part * NKB + (k % NKB)) * TC_MAXN);
-          const uint64_t ad = sw128_desc(a0 + k * 32);
+        for (int k = 0; k < TC_BK / 16; ++k, ++kstep) {
+          const uint32_t acc = kstep >= NKB ? 1u : 0u;   // first MMA of an accumulator overwrites
+          const uint32_t col = (uint32_t)((kstep % NKB) * TC_ACCW);
           asm volatile(
               "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
               " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-              ::"r"(tmem + col), "l"(ad), "l"(bd), "r"(idesc), "r"(acc));
-          if (DUAL) {
-            const uint64_t ad2 = sw128_desc(a0 + TC_A_BYTES + k * 32);
+              ::"r"(tmem + col), "l"(da + 2 * k), "l"(db + 2 * k), "r"(idesc), "r"(acc));
+          if (DUAL)
             asm volatile(
                 "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
                 " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-                ::"r"(tmem + (uint32_t)(NACC * TC_MAXN) + col), "l"(ad2), "l"(bd), "r"(idesc), "r"(acc));
-          }
+                ::"r"(tmem + (uint32_t)(NKB * TC_ACCW) + col), "l"(da + (uint64_t)((AT * TC_A_BYTES) >> 4) + 2 * k),
+                  "l"(db + 2 * k), "r"(idesc), "r"(acc));
         }
       }
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -277,15 +298,17 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   } else if (F8 && warp >= 4) {
     // ---- converters: e4m3 staging -> swizzled bf16 operand tile ----
     const int t = threadIdx.x - 128;
-    for (int i = 0; i < KT; ++i) {
-      const int s = i % STAGES;
+    for (int i = 0; i < NST; ++i) {
+      const int s = i % STAGES, na = min(AT, KT - i * AT);
       if (!mbar_wait(smem_u32(bars + s), (i / STAGES) & 1)) {
         if (lane == 0) atomicOr(P.err, DERR_TIMEOUT);
         break;
       }
       unsigned char* st = stages + s * SB;
-      convert_tile(st + STG_OFF, st, t);
-      if (DUAL) convert_tile(st + STG_OFF + TC_A8_BYTES, st + TC_A_BYTES, t);
+      for (int j = 0; j < na; ++j) {
+        convert_tile(st + STG_OFF + j * TC_A8_BYTES, st + j * TC_A_BYTES, t);
+        if (DUAL) convert_tile(st + STG_OFF + (AT + j) * TC_A8_BYTES, st + (AT + j) * TC_A_BYTES, t);
+      }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0)
@@ -313,8 +336,9 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
 #pragma unroll
     for (int a = 0; a < NACC; ++a) {
       if (a < nacc) {
-        tmem_ld16(trow + a * TC_MAXN + c0, t[a]);
-        if (DUAL) tmem_ld16(trow + (NACC + a) * TC_MAXN + c0, t2[a]);
+        const uint32_t c = (uint32_t)((a % NKB) * TC_ACCW + (a / NKB) * N + c0);   // (part a / NKB, kb a % NKB)
+        tmem_ld16(trow + c, t[a]);
+        if (DUAL) tmem_ld16(trow + (uint32_t)(NKB * TC_ACCW) + c, t2[a]);
       }
     }
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -387,6 +411,18 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
       }
       return;
     }
+    if (P.epi == TC_SCATTER) {
+      int dst[16];   // destination rows, all loaded before the first store
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int n = n0 + c0 + j;
+        dst[j] = n < n0 + nrows ? P.perm[off + n] : -1;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (dst[j] >= 0) P.out_f32[(size_t)dst[j] * P.ldo + col] = v[j] * sc;
+      return;
+    }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int n = n0 + c0 + j;
@@ -395,8 +431,6 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
       const size_t r = (size_t)(off + n);
       if (P.epi == TC_STORE) {
         P.out_f32[r * P.ldo + col] = val;
-      } else if (P.epi == TC_SCATTER) {
-        P.out_f32[(size_t)P.perm[r] * P.ldo + col] = val;
       } else if (DUAL && P.epi == TC_SWIGLU) {
         const float hv = silu(val) * (u2[j] * sc2);
         const uint16_t hi = f_to_bf16(hv);
@@ -444,18 +478,24 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
         for (int c0 = 0; c0 < N; c0 += 16) {
           float v[16], u2[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = n0 + c0 + j;
-            float x = 0.f, y = 0.f;
-            if (n < n0 + nrows) {
-              const size_t e = (size_t)(off + n) * P.part_m + feat;
-              for (int q = 0; q < ksn; ++q) {
-                x += __ldcg(P.part + (size_t)q * (1 + DUAL) * pstride + e);
-                if (DUAL) y += __ldcg(P.part + ((size_t)q * 2 + 1) * pstride + e);
-              }
+          for (int j = 0; j < 16; ++j) v[j] = u2[j] = 0.f;
+          // split by split, the sixteen columns' loads are all issued before
+          // any add (one round trip per split, not per column and split)
+          for (int q = 0; q < ksn; ++q) {
+            const float* pq = P.part + (size_t)q * (1 + DUAL) * pstride + feat;
+            float t[16], t2[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = n0 + c0 + j;
+              const size_t e = (size_t)(off + n) * P.part_m;
+              t[j] = n < n0 + nrows ? __ldcg(pq + e) : 0.f;
+              t2[j] = DUAL && n < n0 + nrows ? __ldcg(pq + pstride + e) : 0.f;
             }
-            v[j] = x;
-            u2[j] = y;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              v[j] += t[j];
+              if (DUAL) u2[j] += t2[j];
+            }
           }
           emit(c0, v, u2);
         }
