@@ -344,45 +344,49 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
 }
 
 // ===========================================================================
-// Tensor-core form (bf16 K/V): warp-level mma.sync m16n8k16 with the chunk's
-// 64 keys as M and the group's (row, q head) pairs as N (8 per tile, at most
-// 32 per group: a group holds 32 / G rows). Per item:
-//   S^T = K Q^T   (A = K rows by ldmatrix, B = Q as bf16 hi + lo: two MMAs),
-//   softmax of each pair column over the chunk (fp32, causal mask),
-//   O^T = V^T P^T (A = V by ldmatrix.trans, B = P as bf16 hi + lo).
+// Tensor-core form (bf16 K/V): warp-level mma.sync m16n8k16. Each warp owns
+// one N tile of eight (row, q head) pairs of the group (a block of NW warps
+// covers up to 8 NW pairs) and, per 64-key chunk:
+//   S^T = K Q^T   (M = the 64 keys, A = K by ldmatrix, B = Q as bf16 hi + lo,
+//                  both multiplied into the same accumulator),
+//   softmax of each pair column over the chunk (fp32, causal mask; the
+//                  column max and sum by shuffles inside the warp),
+//   O^T = V^T P^T (M = head dims, A = V by ldmatrix.trans, B = P as bf16
+//                  hi + lo through a small per-warp transpose buffer).
 // K and V are bf16 already, so the products are exact and the hi/lo split
-// keeps Q and P near fp32. Warp w scores keys 16w..16w+15 and then outputs
-// dims [D/4 w, D/4 (w+1)). Each pair column only meets its own Q and P, so a
+// keeps Q and P near fp32. Each pair column only meets its own Q and P, so a
 // row's result does not depend on the group, the batch or its place in them.
-constexpr int ATQ = 32;          // pairs per group at most (4 N tiles)
+//
+// Streaming: items are ordered (group, kv head, chunk); every block takes one
+// contiguous run of them and keeps the Q fragments of its current (group, kv
+// head) in registers. The K/V of a chunk arrive by TMA from a tensor map over
+// the paged pool (dims: head dim, key in page, (layer, K|V, kv head), page;
+// box 64 dims x 16 keys with the 128-byte swizzle -- page sizes are multiples
+// of 16, so a box never straddles pages), NB chunks deep, on one mbarrier per
+// buffer; boxes past the chunk's last key read page -1 (zero fill). Which
+// block computes an item never changes its arithmetic.
+constexpr int ATQ = 32;          // pairs per group at most (four warps)
+constexpr int ATT_NB = 2;        // chunk buffers per block
+constexpr uint32_t ATT_WAIT_LIMIT = 1u << 22;
 
-template <int D_HEAD>
-struct AttTcSmem {
-  static constexpr int KST = D_HEAD + 8;               // padded bf16 rows (ldmatrix without bank conflicts)
-  static constexpr int PST = ATT_CHUNK + 8;
-  static constexpr size_t k = 0;
-  static constexpr size_t v = k + (size_t)ATT_CHUNK * KST * 2;
-  static constexpr size_t qh = v + (size_t)ATT_CHUNK * KST * 2;
-  static constexpr size_t ql = qh + (size_t)ATQ * KST * 2;
-  static constexpr size_t ph = ql + (size_t)ATQ * KST * 2;
-  static constexpr size_t pl = ph + (size_t)ATQ * PST * 2;
-  static constexpr size_t sf = pl + (size_t)ATQ * PST * 2;      // fp32 S [64 keys][ATQ + 1]
-  static constexpr size_t pg = sf + (size_t)ATT_CHUNK * (ATQ + 1) * 4;
-  static constexpr size_t total = pg + ATT_CHUNK * 4;
+template <int D_HEAD, int NW, int NB>
+struct AttWSmem {
+  static constexpr int HB = ATT_CHUNK * 128;            // 64 dims of K or V for the chunk's keys
+  static constexpr int BUF = 2 * (D_HEAD / 64) * HB;    // K then V of one chunk
+  static constexpr int PST = ATT_CHUNK + 8;             // P row stride (bf16), padded
+  static constexpr int PW = 2 * 8 * PST * 2;            // one warp's P hi + lo [8 pairs][PST]
+  static constexpr size_t total = 1024 + (size_t)NB * BUF + (size_t)NW * PW;   // + 1024-byte alignment slack
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-  const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t a) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
-  const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t a) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
 }
-__device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, const void* p) {
-  const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+__device__ __forceinline__ void ldsm_x2(uint32_t& r0, uint32_t& r1, uint32_t a) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(a));
 }
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -391,181 +395,271 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ bool att_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < ATT_WAIT_LIMIT; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+// Byte offset of 16-byte piece c (0..7) of row r in a 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
-template <int D_HEAD>
-__global__ void __launch_bounds__(ATT_THREADS) k_attn_tc(Dims D, DevState S, StepBuf B, int layer, int T, int R,
-                                                         int RG, int n_groups, int inline_merge) {
-  using L = AttTcSmem<D_HEAD>;
-  constexpr int KST = L::KST, PST = L::PST;
-  constexpr int PPR = D_HEAD * 2 / 16;                 // 16-byte pieces per K/V row
-  constexpr int DMT = D_HEAD / 16 / 4;                 // output dim tiles per warp
-  extern __shared__ __align__(16) unsigned char smraw[];
-  bf16_t* Ks = reinterpret_cast<bf16_t*>(smraw + L::k);
-  bf16_t* Vs = reinterpret_cast<bf16_t*>(smraw + L::v);
-  uint16_t* Qh = reinterpret_cast<uint16_t*>(smraw + L::qh);
-  uint16_t* Ql = reinterpret_cast<uint16_t*>(smraw + L::ql);
-  uint16_t* Ph = reinterpret_cast<uint16_t*>(smraw + L::ph);
-  uint16_t* Pl = reinterpret_cast<uint16_t*>(smraw + L::pl);
-  float* Sf = reinterpret_cast<float*>(smraw + L::sf);
-  int* pg = reinterpret_cast<int*>(smraw + L::pg);
-  __shared__ int s_last;
+// Item i of the (group, kv head, chunk) order.
+struct AttItem {
+  int g, hk, c;
+  __device__ AttItem(const int* s_pref, int n_groups, int Hkv, int i) {
+    g = att_group_of(s_pref, n_groups, i / Hkv);     // s_pref[g] Hkv <= i
+    const int nc = s_pref[g + 1] - s_pref[g], r = i - s_pref[g] * Hkv;
+    hk = r / nc;
+    c = r % nc;
+  }
+};
+
+template <int D_HEAD, int NW, int NB>
+__global__ void __launch_bounds__(NW * 32) k_attn_w(const __grid_constant__ CUtensorMap kvmap, Dims D, DevState S,
+                                                    StepBuf B, int layer, int T, int R, int RG, int n_groups,
+                                                    int inline_merge) {
+  using L = AttWSmem<D_HEAD, NW, NB>;
+  constexpr int HALVES = D_HEAD / 64, HB = L::HB, BUF = L::BUF, PST = L::PST;
+  constexpr int NTHR = NW * 32;
+  constexpr int KS = D_HEAD / 16;                      // 16-wide K steps over the head dim
+  extern __shared__ unsigned char smraw[];
+  const uint32_t sbase = ((uint32_t)__cvta_generic_to_shared(smraw) + 1023u) & ~1023u;
+  const uint32_t bufs = sbase;                         // NB x [K halves][V halves], 1024-aligned
+  __shared__ __align__(8) uint64_t full[NB];
   __shared__ int s_pref[ATT_MAX_GROUPS + 1];
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3;
+  const uint32_t pw = bufs + NB * BUF + warp * L::PW; // this warp's P hi [8][PST]; lo at + 8 PST 2
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < NB; ++b)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(full + b)));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   pdl_wait();
   pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3;
-  att_prefix(B, T, R, RG, n_groups, s_pref);
+  att_prefix(B, T, R, RG, n_groups, s_pref);          // ends with a block barrier (also publishes the barrier init)
   const int G = D.Hq / D.Hkv;
   const float scale = 1.0f / sqrtf((float)D_HEAD);
-  const size_t v_off = (size_t)D.Hkv * D.P * D_HEAD;
-  const bf16_t* kv = reinterpret_cast<const bf16_t*>(S.kv);
   const int n_items = s_pref[n_groups] * D.Hkv;
+  const int per = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int i0 = blockIdx.x * per, i1 = min(n_items, i0 + per);
+  if (i0 >= i1) return;
 
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int qi = item / D.Hkv, hk = item % D.Hkv;
-    const int gi = att_group_of(s_pref, n_groups, qi), c = qi - s_pref[gi];
+  // warp 0: the TMA boxes of item i into buffer b (lane = box: 16-key
+  // block j, 64-dim half h, K or V); boxes past the chunk's last key (and a
+  // missing page, which also sets the error bit) read page -1: zeros
+  auto issue = [&](int i, int b) {
+    const AttItem it(s_pref, n_groups, D.Hkv, i);
+    const AttGroup grp(it.g, T, R, RG);
+    const int k0 = it.c * ATT_CHUNK;
+    const int nk = min(ATT_CHUNK, B.row_pos[grp.r0 + grp.nr - 1] + 1 - k0);
+    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(full + b);
+    if (lane == 0)
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"((uint32_t)BUF) : "memory");
+    __syncwarp();
+    if (lane < 8 * HALVES) {
+      const int j = lane & 3, h = (lane >> 2) % HALVES, kvsel = lane / (4 * HALVES);
+      const int key = k0 + 16 * j;
+      int page = -1;
+      if (16 * j < nk) {
+        page = S.bt[(size_t)B.row_seq[grp.r0] * D.max_pages + key / D.P];
+        if (page < 0) atomicOr(S.err, DERR_PAGE);
+      }
+      const uint32_t dst = bufs + b * BUF + (kvsel * HALVES + h) * HB + j * 2048;
+      const int c2 = (layer * 2 + kvsel) * D.Hkv + it.hk;
+      asm volatile(
+          "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+          ::"r"(dst), "l"(reinterpret_cast<uint64_t>(&kvmap)), "r"(h * 64), "r"(key % D.P), "r"(c2), "r"(page), "r"(bar)
+          : "memory");
+    }
+  };
+
+  if (warp == 0)
+    for (int j = 0; j < NB - 1; ++j)
+      if (i0 + j < i1) issue(i0 + j, j);
+  uint32_t parity = 0;                                 // bit b: phase of buffer b to wait for
+  int staged_g = -1, staged_hk = -1;
+  uint32_t qh[KS][2], ql[KS][2];                       // B fragments of Q (this warp's pairs)
+  int pos[2] = {-1, -1};                               // positions of pairs 2 q4, 2 q4 + 1 of the tile
+  int aborted_at = -1;
+  int issued = min(i1, i0 + NB - 1);                   // items whose copies were issued
+  for (int i = i0; i < i1; ++i) {
+    const int b = (i - i0) % NB;
+    const AttItem it(s_pref, n_groups, D.Hkv, i);
+    const int gi = it.g, hk = it.hk, c = it.c;
     const AttGroup grp(gi, T, R, RG);
     const int r0 = grp.r0, nr = grp.nr;
-    const int seq = B.row_seq[r0];
     const int maxpos = B.row_pos[r0 + nr - 1];
     const int nch = maxpos / ATT_CHUNK + 1;
     const int npairs = nr * G;
-    const int nnt = (npairs + 7) / 8;
     const int k0 = c * ATT_CHUNK;
     const int nk = min(ATT_CHUNK, maxpos + 1 - k0);
-    const size_t head_off = (((size_t)layer * 2) * D.Hkv + hk) * D.P * D_HEAD;
-    __syncthreads();
-    // ---- pages, K/V pieces in flight, Q of the group's pairs as hi/lo ----
-    for (int key = threadIdx.x; key < ATT_CHUNK; key += ATT_THREADS) {
-      int page = -1;
-      if (key < nk) {
-        page = S.bt[(size_t)seq * D.max_pages + (k0 + key) / D.P];
-        if (page < 0) atomicOr(S.err, DERR_PAGE);
-      }
-      pg[key] = page;
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < 2 * ATT_CHUNK * PPR; i += ATT_THREADS) {
-      const int isv = i >= ATT_CHUNK * PPR;
-      const int j = isv ? i - ATT_CHUNK * PPR : i;
-      const int key = j / PPR, piece = j % PPR;
-      bf16_t* dst = (isv ? Vs : Ks) + key * KST + piece * 8;
-      const int page = pg[key];
-      if (page < 0) {                                 // keys past the chunk's end (or a missing page): zeros
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-        continue;
-      }
-      const size_t e = (size_t)page * D.page_elems + head_off + (isv ? v_off : 0) +
-                       (size_t)((k0 + key) % D.P) * D_HEAD + piece * 8;
-      cp_async16(dst, kv + e);
-    }
-    for (int i = threadIdx.x; i < nnt * 8 * (D_HEAD / 4); i += ATT_THREADS) {
-      const int p = i / (D_HEAD / 4), d4 = (i % (D_HEAD / 4)) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (p < npairs) {
-        const int row = r0 + p / G, hq = hk * G + p % G;
-        v = *reinterpret_cast<const float4*>(B.q + ((size_t)row * D.Hq + hq) * D_HEAD + d4);
-      }
-      uint32_t h0, l0, h1, l1;
-      split_bf16x2(v.x, v.y, h0, l0);
-      split_bf16x2(v.z, v.w, h1, l1);
-      *reinterpret_cast<uint2*>(Qh + p * KST + d4) = make_uint2(h0, h1);
-      *reinterpret_cast<uint2*>(Ql + p * KST + d4) = make_uint2(l0, l1);
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    // ---- S^T (keys 16 warp .. +15) x pairs, scaled and causally masked, into Sf ----
-    for (int nt = 0; nt < nnt; ++nt) {
-      float ch[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- Q fragments and pair positions, when the (group, kv head) changes ----
+    if (gi != staged_g || hk != staged_hk) {
+      const int p = 8 * warp + g;
+      const float* qr = nullptr;
+      if (p < npairs) qr = B.q + ((size_t)(r0 + p / G) * D.Hq + hk * G + p % G) * D_HEAD;
 #pragma unroll
-      for (int ks = 0; ks < D_HEAD / 16; ++ks) {
-        uint32_t a[4], bh0, bh1, bl0, bl1;
-        ldsm_x4(a, Ks + (16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1)) * KST + 16 * ks + 8 * (lane >> 4));
-        const int prow = 8 * nt + (lane & 7), pcol = 16 * ks + 8 * ((lane >> 3) & 1);
-        ldsm_x2(bh0, bh1, Qh + prow * KST + pcol);
-        ldsm_x2(bl0, bl1, Ql + prow * KST + pcol);
-        mma_bf16(ch, a, bh0, bh1);
-        mma_bf16(cl, a, bl0, bl1);
-      }
+      for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = 16 * warp + g + 8 * (e >> 1), p = 8 * nt + 2 * q4 + (e & 1);
-        float sv = -INFINITY;
-        if (p < npairs && key < nk && k0 + key <= B.row_pos[r0 + p / G]) sv = (ch[e] + cl[e]) * scale;
-        Sf[key * (ATQ + 1) + p] = sv;
-      }
-    }
-    __syncthreads();
-    // ---- softmax of each pair over the chunk: P (hi/lo) and the partial (max, sum) ----
-    for (int p = warp; p < nnt * 8; p += ATT_THREADS / 32) {
-      const float s0 = Sf[lane * (ATQ + 1) + p], s1 = Sf[(lane + 32) * (ATQ + 1) + p];
-      const float m = warp_max(fmaxf(s0, s1));
-      float e0 = 0.f, e1 = 0.f;
-      if (m != -INFINITY) {
-        e0 = expf(s0 - m);
-        e1 = expf(s1 - m);
-      }
-      const float l = warp_sum(e0 + e1);
-      const uint16_t h0 = f_to_bf16(e0), h1 = f_to_bf16(e1);
-      Ph[p * PST + lane] = h0;
-      Ph[p * PST + lane + 32] = h1;
-      Pl[p * PST + lane] = f_to_bf16(e0 - bf16_to_f(h0));
-      Pl[p * PST + lane + 32] = f_to_bf16(e1 - bf16_to_f(h1));
-      if (lane == 0 && p < npairs && m != -INFINITY) {
-        const int row = r0 + p / G, hq = hk * G + p % G;
-        const size_t pidx = ((size_t)row * D.Hq + hq) * B.n_chunk_max + c;
-        reinterpret_cast<float2*>(B.att_ml)[pidx] = make_float2(m, l);
-      }
-    }
-    __syncthreads();
-    // ---- O^T (dims of this warp) x pairs -> chunk partials ----
-    for (int nt = 0; nt < nnt; ++nt) {
-      float oh[DMT][4], ol[DMT][4];
-#pragma unroll
-      for (int mt = 0; mt < DMT; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) { oh[mt][e] = 0.f; ol[mt][e] = 0.f; }
-#pragma unroll
-      for (int ks = 0; ks < ATT_CHUNK / 16; ++ks) {
-        uint32_t bh0, bh1, bl0, bl1;
-        const int prow = 8 * nt + (lane & 7), pcol = 16 * ks + 8 * ((lane >> 3) & 1);
-        ldsm_x2(bh0, bh1, Ph + prow * PST + pcol);
-        ldsm_x2(bl0, bl1, Pl + prow * PST + pcol);
-#pragma unroll
-        for (int mt = 0; mt < DMT; ++mt) {
-          const int dm = 16 * (DMT * warp + mt);
-          uint32_t a[4];
-          // A = V^T [dims dm..dm+15][keys 16 ks..]: matrices (dims 0-7 | 8-15) x (keys 0-7 | 8-15)
-          ldsm_x4_t(a, Vs + (16 * ks + (lane & 7) + 8 * (lane >> 4)) * KST + dm + 8 * ((lane >> 3) & 1));
-          mma_bf16(oh[mt], a, bh0, bh1);
-          mma_bf16(ol[mt], a, bl0, bl1);
+        for (int u = 0; u < 2; ++u) {
+          float2 v = make_float2(0.f, 0.f);
+          if (qr) v = *reinterpret_cast<const float2*>(qr + 16 * ks + 2 * q4 + 8 * u);
+          split_bf16x2(v.x, v.y, qh[ks][u], ql[ks][u]);
         }
       }
 #pragma unroll
-      for (int mt = 0; mt < DMT; ++mt) {
+      for (int j = 0; j < 2; ++j) {
+        const int pj = 8 * warp + 2 * q4 + j;
+        pos[j] = pj < npairs ? B.row_pos[r0 + pj / G] : -1;
+      }
+      staged_g = gi;
+      staged_hk = hk;
+    }
+    // ---- this item's chunk: wait, zero V rows past the last key, publish ----
+    const bool ok = att_wait((uint32_t)__cvta_generic_to_shared(full + b), (parity >> b) & 1);
+    parity ^= 1u << b;
+    const uint32_t kb = bufs + b * BUF, vb = kb + HALVES * HB;
+    if (nk < ATT_CHUNK) {
+      for (int e = threadIdx.x; e < (ATT_CHUNK - nk) * HALVES * 8; e += NTHR) {
+        const int h = e / ((ATT_CHUNK - nk) * 8), r = nk + (e / 8) % (ATT_CHUNK - nk), pc = e % 8;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vb + h * HB + r * 128 + pc * 16), "r"(0u)
+                     : "memory");
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // before TMA refills this buffer
+    }
+    if (!__syncthreads_and(ok)) {
+      if (threadIdx.x == 0) atomicOr(S.err, DERR_TIMEOUT);
+      parity ^= 1u << b;                               // item i's phase is still owed
+      aborted_at = i;
+      break;
+    }
+    // the buffer of item i - 1 is free now: refill it NB - 1 items ahead
+    if (warp == 0 && i + NB - 1 < i1) issue(i + NB - 1, (b + NB - 1) % NB);
+    if (i + NB - 1 < i1) issued = i + NB;
+    if (8 * warp < npairs) {
+      // ---- S^T: four 16-key tiles x this warp's 8 pairs ----
+      float sacc[4][4];
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mt][e] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int col = 16 * ks + 8 * (lane >> 4);
+        const uint32_t hbase = kb + (col >> 6) * HB;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          const int key = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
+          uint32_t a[4];
+          ldsm_x4(a, hbase + sw128(key, (col & 63) >> 3));
+          mma_bf16(sacc[mt], a, qh[ks][0], qh[ks][1]);
+          mma_bf16(sacc[mt], a, ql[ks][0], ql[ks][1]);
+        }
+      }
+      // ---- scale, mask, column max / sum over the 64 keys ----
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int dim = 16 * (DMT * warp + mt) + g + 8 * (e >> 1), p = 8 * nt + 2 * q4 + (e & 1);
-          if (p >= npairs) continue;
-          const int row = r0 + p / G, hq = hk * G + p % G;
-          if (B.row_pos[row] < k0) continue;              // chunk lies after this row: no partial
-          const size_t pidx = ((size_t)row * D.Hq + hq) * B.n_chunk_max + c;
-          B.att_o[pidx * D_HEAD + dim] = oh[mt][e] + ol[mt][e];
+          const int key = 16 * mt + g + 8 * (e >> 1), j = e & 1;
+          const float v = (key < nk && k0 + key <= pos[j]) ? sacc[mt][e] * scale : -INFINITY;
+          sacc[mt][e] = v;
+          mx[j] = fmaxf(mx[j], v);
+        }
+      float sm[2] = {0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], o));
+      const uint32_t ph = pw, pl = pw + 8 * PST * 2;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = 16 * mt + g + 8 * (e >> 1), j = e & 1;
+          const float pe = mx[j] == -INFINITY ? 0.f : expf(sacc[mt][e] - mx[j]);
+          sm[j] += pe;
+          const uint16_t hi = f_to_bf16(pe), lo = f_to_bf16(pe - bf16_to_f(hi));
+          const uint32_t off = (uint32_t)(((2 * q4 + j) * PST + key) * 2);
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(ph + off), "h"(hi) : "memory");
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(pl + off), "h"(lo) : "memory");
+        }
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) sm[j] += __shfl_xor_sync(0xffffffffu, sm[j], o);
+      if (g == 0) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int pj = 8 * warp + 2 * q4 + j;
+          if (pj < npairs && mx[j] != -INFINITY) {
+            const size_t pidx = ((size_t)(r0 + pj / G) * D.Hq + hk * G + pj % G) * B.n_chunk_max + c;
+            reinterpret_cast<float2*>(B.att_ml)[pidx] = make_float2(mx[j], sm[j]);
+          }
+        }
+      }
+      __syncwarp();
+      // ---- O^T: head dims x this warp's pairs, keys in 16-wide steps ----
+      float o[KS][4];
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < ATT_CHUNK / 16; ++ks) {
+        uint32_t bh0, bh1, bl0, bl1;
+        const uint32_t poff = (uint32_t)(((lane & 7) * PST + 16 * ks + 8 * ((lane >> 3) & 1)) * 2);
+        ldsm_x2(bh0, bh1, ph + poff);
+        ldsm_x2(bl0, bl1, pl + poff);
+        const int key = 16 * ks + (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          const int col = 16 * mt + 8 * ((lane >> 3) & 1);
+          uint32_t a[4];
+          ldsm_x4_t(a, vb + (col >> 6) * HB + sw128(key, (col & 63) >> 3));
+          mma_bf16(o[mt], a, bh0, bh1);
+          mma_bf16(o[mt], a, bl0, bl1);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int pj = 8 * warp + 2 * q4 + j;
+        if (pj >= npairs || pos[j] < k0) continue;     // chunk lies after this row: no partial
+        float* og = B.att_o + (((size_t)(r0 + pj / G) * D.Hq + hk * G + pj % G) * B.n_chunk_max + c) * D_HEAD;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          og[16 * mt + g] = o[mt][j];
+          og[16 * mt + g + 8] = o[mt][2 + j];
         }
       }
     }
     // ---- the last chunk of this (group, kv head) to finish merges its pairs ----
     if (!inline_merge) continue;
+    __threadfence();
     __syncthreads();
     int* ctr = B.cnt_att + (size_t)gi * D.Hkv + hk;
-    if (threadIdx.x == 0) {
-      __threadfence();
-      s_last = (atomicAdd(ctr, 1) == nch - 1);
-    }
+    if (threadIdx.x == 0) s_last = (atomicAdd(ctr, 1) == nch - 1);
     __syncthreads();
     if (!s_last) continue;
     __threadfence();
-    for (int p = warp; p < npairs; p += ATT_THREADS / 32) merge_pair<D_HEAD>(D, B, r0 + p / G, hk * G + p % G);
+    for (int p = 8 * warp; p < min(npairs, 8 * warp + 8); ++p) merge_pair<D_HEAD>(D, B, r0 + p / G, hk * G + p % G);
     if (threadIdx.x == 0) *ctr = 0;
+  }
+  if (aborted_at >= 0 && threadIdx.x == 0) {
+    // copies still in flight (items aborted_at .. issued - 1, one per buffer)
+    // land before the block's shared memory is released; these waits are bounded too
+    for (int k = aborted_at; k < issued; ++k) {
+      const int bk = (k - i0) % NB;
+      att_wait((uint32_t)__cvta_generic_to_shared(full + bk), (parity >> bk) & 1);
+      parity ^= 1u << bk;
+    }
   }
 }
 
@@ -583,7 +677,8 @@ cudaError_t configure_attn_kernels() {
 #define ALLOW(k) if ((r = allow_dyn_smem(k)) != cudaSuccess) e = r
   ALLOW((k_attn_part<128, float>)); ALLOW((k_attn_part<128, bf16_t>));
   ALLOW((k_attn_part<64, float>)); ALLOW((k_attn_part<64, bf16_t>));
-  ALLOW(k_attn_tc<128>); ALLOW(k_attn_tc<64>);
+  ALLOW((k_attn_w<128, 1, ATT_NB>)); ALLOW((k_attn_w<128, 2, ATT_NB>)); ALLOW((k_attn_w<128, 4, ATT_NB>));
+  ALLOW((k_attn_w<64, 1, ATT_NB>)); ALLOW((k_attn_w<64, 2, ATT_NB>)); ALLOW((k_attn_w<64, 4, ATT_NB>));
 #undef ALLOW
   return e;
 }
@@ -591,16 +686,15 @@ cudaError_t configure_attn_kernels() {
 // Pairs per group above which the merge runs as its own kernel.
 constexpr int ATT_INLINE_PAIRS = 16;
 
-// bf16 K/V with head dim 64 or 128 take the tensor-core form when a
-// sequence's rows bring at least 16 (row, q head) pairs per kv head (block
-// drafts, GQA); with fewer, most of each 8-column tile would be padding and
-// the FMA form is faster. The choice depends only on the model (R is fixed
-// by max_draft), so greedy and speculative steps share it.
+// bf16 K/V with head dim 64 or 128 take the tensor-core form (fp32 K/V the
+// FMA form). The choice depends only on the model, so greedy and
+// speculative steps share it.
 static bool att_tc(const Dims& D, int R) {
-  return !D.act_f32 && (D.d == 128 || D.d == 64) && D.Hq / D.Hkv <= ATQ && R * (D.Hq / D.Hkv) >= 16;
+  (void)R;
+  return !D.act_f32 && (D.d == 128 || D.d == 64) && D.Hq / D.Hkv <= ATQ;
 }
 
-// Rows per group: the tensor-core form takes at most 32 (row, q head) pairs.
+// Rows per group: the tensor-core form takes at most 32 (row, q head) pairs (four warps).
 static int att_rg(const Dims& D, int R) {
   const int cap = att_tc(D, R) ? ATQ / (D.Hq / D.Hkv) : 32;
   return R < cap ? R : cap;
@@ -613,26 +707,51 @@ int attn_groups(const Dims& D, int T, int R) {
   return ((T + R - 1) / R) * ((R + RG - 1) / RG);
 }
 
+// Resident blocks per SM of a warp-tiled attention instantiation (cached).
+template <int DH, int NW>
+static int att_w_blocks_per_sm() {
+  static int n = 0;
+  if (n == 0) {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_attn_w<DH, NW, ATT_NB>, NW * 32,
+                                                      AttWSmem<DH, NW, ATT_NB>::total) != cudaSuccess || b < 1)
+      b = 1;
+    n = b;
+  }
+  return n;
+}
+
 void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
-                      cudaStream_t st) {
+                      const CUtensorMap& kvmap, cudaStream_t st) {
   const int RG = att_rg(D, R);
   const int groups = attn_groups(D, T, R);
   const bool sep = attn_separate_merge(D, R);
-  // fixed grid over the step's (group, chunk, kv head) items
-  long long items = (long long)groups * B.n_chunk_max * D.Hkv;
-  int blocks = 8 * D.n_sm;
-  if (items < blocks) blocks = (int)items;
-  const dim3 grid(blocks), blk(ATT_THREADS);
   const int im = sep ? 0 : 1;
   if (att_tc(D, R)) {
-    if (D.d == 128) launch_k(k_attn_tc<128>, grid, blk, AttTcSmem<128>::total, st, D, S, B, layer, T, R, RG, groups, im);
-    else launch_k(k_attn_tc<64>, grid, blk, AttTcSmem<64>::total, st, D, S, B, layer, T, R, RG, groups, im);
-  } else if (D.d == 128) {
-    if (D.act_f32) launch_k(k_attn_part<128, float>, grid, blk, AttSmem<128, float>::total, st, D, S, B, layer, T, R, RG, groups, im);
-    else launch_k(k_attn_part<128, bf16_t>, grid, blk, AttSmem<128, bf16_t>::total, st, D, S, B, layer, T, R, RG, groups, im);
+    // one warp per 8 pairs of a group; every resident block streams its run of items
+    const int nw = (RG * (D.Hq / D.Hkv) + 7) / 8;
+#define ATT_W(DH, NW)                                                                                         \
+  launch_k(k_attn_w<DH, NW, ATT_NB>, dim3(att_w_blocks_per_sm<DH, NW>() * D.n_sm), dim3(NW * 32),            \
+           AttWSmem<DH, NW, ATT_NB>::total, st, kvmap, D, S, B, layer, T, R, RG, groups, im)
+    if (D.d == 128) {
+      if (nw <= 1) ATT_W(128, 1); else if (nw <= 2) ATT_W(128, 2); else ATT_W(128, 4);
+    } else {
+      if (nw <= 1) ATT_W(64, 1); else if (nw <= 2) ATT_W(64, 2); else ATT_W(64, 4);
+    }
+#undef ATT_W
   } else {
-    if (D.act_f32) launch_k(k_attn_part<64, float>, grid, blk, AttSmem<64, float>::total, st, D, S, B, layer, T, R, RG, groups, im);
-    else launch_k(k_attn_part<64, bf16_t>, grid, blk, AttSmem<64, bf16_t>::total, st, D, S, B, layer, T, R, RG, groups, im);
+    // fixed grid over the step's (group, chunk, kv head) items
+    long long items = (long long)groups * B.n_chunk_max * D.Hkv;
+    int blocks = 8 * D.n_sm;
+    if (items < blocks) blocks = (int)items;
+    const dim3 grid(blocks), blk(ATT_THREADS);
+    if (D.d == 128) {
+      if (D.act_f32) launch_k(k_attn_part<128, float>, grid, blk, AttSmem<128, float>::total, st, D, S, B, layer, T, R, RG, groups, im);
+      else launch_k(k_attn_part<128, bf16_t>, grid, blk, AttSmem<128, bf16_t>::total, st, D, S, B, layer, T, R, RG, groups, im);
+    } else {
+      if (D.act_f32) launch_k(k_attn_part<64, float>, grid, blk, AttSmem<64, float>::total, st, D, S, B, layer, T, R, RG, groups, im);
+      else launch_k(k_attn_part<64, bf16_t>, grid, blk, AttSmem<64, bf16_t>::total, st, D, S, B, layer, T, R, RG, groups, im);
+    }
   }
   if (sep) {
     int mb = (T * D.Hq + 7) / 8;

@@ -567,6 +567,22 @@ int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t row
   return r == CUDA_SUCCESS ? 0 : -3;
 }
 
+int kv_make_map(CUtensorMap* map, const void* kv, int head_dim, int page_size, int planes, int n_pages,
+                size_t page_elems) {
+  auto fn = encode_fn();
+  if (!fn) return -1;
+  if ((reinterpret_cast<uintptr_t>(kv) & 15) || head_dim % 64 || page_size % 16) return -2;
+  const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)page_size, (cuuint64_t)planes, (cuuint64_t)n_pages};
+  const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)page_size * head_dim * 2,
+                                 (cuuint64_t)page_elems * 2};
+  const cuuint32_t box[4] = {64, 16, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -3;
+}
+
 }  // namespace spec
 
 // ---------------------------------------------------------------------------

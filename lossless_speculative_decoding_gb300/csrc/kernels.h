@@ -102,7 +102,7 @@ void launch_qkv(const Dims& D, const DevState& S, const StepBuf& B, const LayerW
 bool attn_separate_merge(const Dims& D, int R);   // merge as its own launch (many pairs per group)
 int attn_groups(const Dims& D, int T, int R);
 void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
-                      cudaStream_t st);
+                      const CUtensorMap& kvmap, cudaStream_t st);
 void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, float* xres, cudaStream_t st);
 // full: always compute top-k and the permutation (the tensor-core path needs them)
 void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, const float* xres, bool full,
@@ -167,6 +167,11 @@ struct TcMaps {
 // 2D bf16 tensor map: rows of `inner` elements, box 64 x box_rows, 128-byte
 // swizzle. Returns 0 on success.
 int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+// 4D bf16 tensor map over the paged KV pool [pages][layer][K|V][kv head][key][dim]
+// for the tensor-core attention: dims (head_dim, page_size, layers x 2 x kv
+// heads, n_pages), box 64 x 16 x 1 x 1, 128-byte swizzle, zero fill outside.
+int kv_make_map(CUtensorMap* map, const void* kv, int head_dim, int page_size, int planes, int n_pages,
+                size_t page_elems);
 // Rewrites W [rows, K] (row-major; bf16, or e4m3 when f8) into the tiled
 // layout the tensor-core GEMM streams (rows a multiple of 128, K of 64).
 int tc_pack_weights(void* dst, const void* src, int rows, int K, int f8, cudaStream_t st);

@@ -163,6 +163,7 @@ struct spec_model {
   bool use_tc = false;
   float* tc_part = nullptr;                                     // split-K partials
   int* tc_cnt = nullptr;                                        // split-K tile arrival counters
+  CUtensorMap kv_map{};                                        // paged KV pool (tensor-core attention)
   CUtensorMap tc_xn, tc_o, tc_xperm, tc_hperm;                 // activations: hi
   CUtensorMap tc_xn_lo, tc_o_lo, tc_xperm_lo, tc_hperm_lo;     //              lo
 
@@ -287,7 +288,7 @@ struct spec_model {
           tc_dense(W.w_qkv, tc_xn, tc_xn_lo, D.h, qkv_rows, T, TC_STORE, B.qkv, qkv_rows, W.s_qkv);
           launch_rope_kv(D, S, B, l, T, stream);
         });
-        run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, stream); });
+        run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, kv_map, stream); });
         run_k(p, KC_OPROJ, [&] { tc_dense(W.w_o, tc_o, tc_o_lo, D.Hq * D.d, D.h, T, TC_ADD, cur, D.h, W.s_o); });
         run_k(p, KC_ROUTER, [&] {
           launch_router(D, B, W, T, cur, true, stream);
@@ -306,7 +307,7 @@ struct spec_model {
         continue;
       }
       run_k(p, KC_QKV, [&] { launch_qkv(D, S, B, W, l, T, cur, stream); });
-      run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, stream); });
+      run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, kv_map, stream); });
       run_k(p, KC_OPROJ, [&] { launch_oproj(D, B, W, T, cur, stream); });
       run_k(p, KC_ROUTER, [&] { launch_router(D, B, W, T, cur, false, stream); });
       run_k(p, KC_GATEUP, [&] { launch_gateup(D, B, W, T, stream); });
@@ -455,6 +456,9 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
   m->n_slots = c.max_seqs + MAX_PREFIXES;
   m->pool.reset(new KvPool(c.n_pages, c.page_size, m->n_slots, D.max_pages));
   if ((rc = m->dalloc((char**)&m->S.kv, (size_t)c.n_pages * D.page_elems * kv_elt))) return rc;
+  if (!D.act_f32 && (D.d == 64 || D.d == 128) &&
+      kv_make_map(&m->kv_map, m->S.kv, D.d, D.P, D.L * 2 * D.Hkv, c.n_pages, D.page_elems))
+    return fail(SPEC_ERR_CUDA, "KV pool tensor map");
   int* bt = nullptr;
   if ((rc = m->dalloc(&bt, (size_t)m->n_slots * D.max_pages))) return rc;
   m->S.bt = bt;
