@@ -161,7 +161,10 @@ struct AttGroup {
 
 // Work list: per-group chunk counts -> exclusive prefix s_pref[0..n_groups]
 // (warp 0; lane l owns groups [l*per, (l+1)*per)), then a block barrier.
-__device__ __forceinline__ void att_prefix(const StepBuf& B, int T, int R, int RG, int n_groups, int* s_pref) {
+// With s_maxpos / s_seq given, also records each group's last position and
+// sequence.
+__device__ __forceinline__ void att_prefix(const StepBuf& B, int T, int R, int RG, int n_groups, int* s_pref,
+                                           int* s_maxpos = nullptr, int* s_seq = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
     const int per = (n_groups + 31) / 32, g0 = lane * per;
@@ -181,7 +184,14 @@ __device__ __forceinline__ void att_prefix(const StepBuf& B, int T, int R, int R
       if (g0 + i < n_groups) {
         s_pref[g0 + i] = run;
         const AttGroup a(g0 + i, T, R, RG);
-        if (a.nr > 0) run += B.row_pos[a.r0 + a.nr - 1] / ATT_CHUNK + 1;
+        if (a.nr > 0) {
+          const int mp = B.row_pos[a.r0 + a.nr - 1];
+          run += mp / ATT_CHUNK + 1;
+          if (s_maxpos) {
+            s_maxpos[g0 + i] = mp;
+            s_seq[g0 + i] = B.row_seq[a.r0];
+          }
+        }
       }
     }
     if (lane == 31) s_pref[n_groups] = inc;
@@ -344,9 +354,10 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
 }
 
 // ===========================================================================
-// Tensor-core form (bf16 K/V): warp-level mma.sync m16n8k16. Each warp owns
-// one N tile of eight (row, q head) pairs of the group (a block of NW warps
-// covers up to 8 NW pairs) and, per 64-key chunk:
+// Tensor-core form (bf16 K/V): warp-level mma.sync m16n8k16. A consumer group
+// of NW warps takes one (group, kv head, chunk) item at a time; its warp w
+// owns the N tile of pairs 8w..8w+7 of the group (NW warps cover up to 8 NW
+// (row, q head) pairs) and, per 64-key chunk:
 //   S^T = K Q^T   (M = the 64 keys, A = K by ldmatrix, B = Q as bf16 hi + lo,
 //                  both multiplied into the same accumulator),
 //   softmax of each pair column over the chunk (fp32, causal mask; the
@@ -358,24 +369,25 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
 // row's result does not depend on the group, the batch or its place in them.
 //
 // Streaming: items are ordered (group, kv head, chunk); every block takes one
-// contiguous run of them and keeps the Q fragments of its current (group, kv
-// head) in registers. The K/V of a chunk arrive by TMA from a tensor map over
-// the paged pool (dims: head dim, key in page, (layer, K|V, kv head), page;
-// box 64 dims x 16 keys with the 128-byte swizzle -- page sizes are multiples
-// of 16, so a box never straddles pages), NB chunks deep, on one mbarrier per
-// buffer; boxes past the chunk's last key read page -1 (zero fill). Which
-// block computes an item never changes its arithmetic.
+// contiguous run of them, and its CG consumer groups take every CG-th item.
+// One producer warp looks up the pages and issues the K/V of each item by TMA
+// into a ring of NB chunk buffers (full / empty mbarriers, every wait
+// bounded). The tensor map spans the paged pool (dims: head dim, key in
+// page, (layer, K|V, kv head), page; box 64 dims x 16 keys, 128-byte swizzle
+// -- page sizes are multiples of 16, so a box never straddles pages); boxes
+// past the chunk's last key read page -1 (zero fill). Which block or group
+// computes an item never changes its arithmetic.
 constexpr int ATQ = 32;          // pairs per group at most (four warps)
-constexpr int ATT_NB = 2;        // chunk buffers per block
+constexpr int ATT_NB = 6;        // chunk buffers per block
 constexpr uint32_t ATT_WAIT_LIMIT = 1u << 22;
 
-template <int D_HEAD, int NW, int NB>
+template <int D_HEAD, int NW, int CG, int NB>
 struct AttWSmem {
   static constexpr int HB = ATT_CHUNK * 128;            // 64 dims of K or V for the chunk's keys
   static constexpr int BUF = 2 * (D_HEAD / 64) * HB;    // K then V of one chunk
   static constexpr int PST = ATT_CHUNK + 8;             // P row stride (bf16), padded
   static constexpr int PW = 2 * 8 * PST * 2;            // one warp's P hi + lo [8 pairs][PST]
-  static constexpr size_t total = 1024 + (size_t)NB * BUF + (size_t)NW * PW;   // + 1024-byte alignment slack
+  static constexpr size_t total = 1024 + (size_t)NB * BUF + (size_t)CG * NW * PW;   // + alignment slack
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t a) {
@@ -405,6 +417,24 @@ __device__ __forceinline__ bool att_wait(uint32_t bar, uint32_t parity) {
   }
   return false;
 }
+// Barrier of one consumer group (named barrier 1 + cg, NW warps) that also
+// reduces a flag: true when it holds in every thread of the group.
+template <int NW>
+__device__ __forceinline__ bool group_sync_and(int cg, bool v) {
+  if constexpr (NW == 1) {
+    return __all_sync(0xffffffffu, v);
+  } else {
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+                 : "=r"(r) : "r"((uint32_t)v), "r"(1 + cg), "r"(NW * 32) : "memory");
+    return r != 0;
+  }
+}
+template <int NW>
+__device__ __forceinline__ void group_sync(int cg) {
+  if constexpr (NW == 1) __syncwarp();
+  else asm volatile("bar.sync %0, %1;" ::"r"(1 + cg), "r"(NW * 32) : "memory");
+}
 // Byte offset of 16-byte piece c (0..7) of row r in a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
@@ -419,89 +449,100 @@ struct AttItem {
   }
 };
 
-template <int D_HEAD, int NW, int NB>
-__global__ void __launch_bounds__(NW * 32) k_attn_w(const __grid_constant__ CUtensorMap kvmap, Dims D, DevState S,
-                                                    StepBuf B, int layer, int T, int R, int RG, int n_groups,
-                                                    int inline_merge) {
-  using L = AttWSmem<D_HEAD, NW, NB>;
+template <int D_HEAD, int NW, int CG, int NB>
+__global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
+    k_attn_w(const __grid_constant__ CUtensorMap kvmap, Dims D, DevState S, StepBuf B, int layer, int T, int R,
+             int RG, int n_groups, int inline_merge) {
+  using L = AttWSmem<D_HEAD, NW, CG, NB>;
   constexpr int HALVES = D_HEAD / 64, HB = L::HB, BUF = L::BUF, PST = L::PST;
-  constexpr int NTHR = NW * 32;
   constexpr int KS = D_HEAD / 16;                      // 16-wide K steps over the head dim
+  constexpr int NCW = CG * NW;                         // consumer warps; the producer is warp NCW
   extern __shared__ unsigned char smraw[];
-  const uint32_t sbase = ((uint32_t)__cvta_generic_to_shared(smraw) + 1023u) & ~1023u;
-  const uint32_t bufs = sbase;                         // NB x [K halves][V halves], 1024-aligned
-  __shared__ __align__(8) uint64_t full[NB];
-  __shared__ int s_pref[ATT_MAX_GROUPS + 1];
-  __shared__ int s_last;
+  const uint32_t bufs = ((uint32_t)__cvta_generic_to_shared(smraw) + 1023u) & ~1023u;   // NB x [K halves][V halves]
+  __shared__ __align__(8) uint64_t full[NB], empty[NB];
+  __shared__ int s_pref[ATT_MAX_GROUPS + 1], s_maxpos[ATT_MAX_GROUPS], s_seq[ATT_MAX_GROUPS];
+  __shared__ int s_last[CG];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3;
-  const uint32_t pw = bufs + NB * BUF + warp * L::PW; // this warp's P hi [8][PST]; lo at + 8 PST 2
+  auto bar_of = [&](uint64_t* b) { return (uint32_t)__cvta_generic_to_shared(b); };
   if (threadIdx.x == 0) {
-    for (int b = 0; b < NB; ++b)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(full + b)));
+    for (int b = 0; b < NB; ++b) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_of(full + b)));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar_of(empty + b)), "r"(NW));
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   pdl_wait();
   pdl_trigger();
-  att_prefix(B, T, R, RG, n_groups, s_pref);          // ends with a block barrier (also publishes the barrier init)
-  const int G = D.Hq / D.Hkv;
-  const float scale = 1.0f / sqrtf((float)D_HEAD);
+  att_prefix(B, T, R, RG, n_groups, s_pref, s_maxpos, s_seq);   // ends with a block barrier
   const int n_items = s_pref[n_groups] * D.Hkv;
   const int per = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
   const int i0 = blockIdx.x * per, i1 = min(n_items, i0 + per);
   if (i0 >= i1) return;
+  const int n = i1 - i0;
 
-  // warp 0: the TMA boxes of item i into buffer b (lane = box: 16-key
-  // block j, 64-dim half h, K or V); boxes past the chunk's last key (and a
-  // missing page, which also sets the error bit) read page -1: zeros
-  auto issue = [&](int i, int b) {
-    const AttItem it(s_pref, n_groups, D.Hkv, i);
-    const AttGroup grp(it.g, T, R, RG);
-    const int k0 = it.c * ATT_CHUNK;
-    const int nk = min(ATT_CHUNK, B.row_pos[grp.r0 + grp.nr - 1] + 1 - k0);
-    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(full + b);
-    if (lane == 0)
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"((uint32_t)BUF) : "memory");
-    __syncwarp();
-    if (lane < 8 * HALVES) {
-      const int j = lane & 3, h = (lane >> 2) % HALVES, kvsel = lane / (4 * HALVES);
-      const int key = k0 + 16 * j;
-      int page = -1;
-      if (16 * j < nk) {
-        page = S.bt[(size_t)B.row_seq[grp.r0] * D.max_pages + key / D.P];
-        if (page < 0) atomicOr(S.err, DERR_PAGE);
+  if (warp == NCW) {
+    // ---- producer: item k into buffer k % NB once its previous item is consumed ----
+    int k = 0;
+    for (; k < n; ++k) {
+      const int b = k % NB;
+      if (k >= NB && !att_wait(bar_of(empty + b), ((k / NB) - 1) & 1)) {
+        if (lane == 0) atomicOr(S.err, DERR_TIMEOUT);
+        break;
       }
-      const uint32_t dst = bufs + b * BUF + (kvsel * HALVES + h) * HB + j * 2048;
-      const int c2 = (layer * 2 + kvsel) * D.Hkv + it.hk;
-      asm volatile(
-          "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
-          ::"r"(dst), "l"(reinterpret_cast<uint64_t>(&kvmap)), "r"(h * 64), "r"(key % D.P), "r"(c2), "r"(page), "r"(bar)
-          : "memory");
+      const AttItem it(s_pref, n_groups, D.Hkv, i0 + k);
+      const int k0 = it.c * ATT_CHUNK;
+      const int nk = min(ATT_CHUNK, s_maxpos[it.g] + 1 - k0);
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_of(full + b)), "r"((uint32_t)BUF)
+                     : "memory");
+      __syncwarp();
+      if (lane < 8 * HALVES) {
+        // lane = box: 16-key block j, 64-dim half h, K or V; a missing page sets the error bit
+        const int j = lane & 3, h = (lane >> 2) % HALVES, kvsel = lane / (4 * HALVES);
+        const int key = k0 + 16 * j;
+        int page = -1;
+        if (16 * j < nk) {
+          page = S.bt[(size_t)s_seq[it.g] * D.max_pages + key / D.P];
+          if (page < 0) atomicOr(S.err, DERR_PAGE);
+        }
+        const uint32_t dst = bufs + b * BUF + (kvsel * HALVES + h) * HB + j * 2048;
+        const int c2 = (layer * 2 + kvsel) * D.Hkv + it.hk;
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+            ::"r"(dst), "l"(reinterpret_cast<uint64_t>(&kvmap)), "r"(h * 64), "r"(key % D.P), "r"(c2), "r"(page),
+              "r"(bar_of(full + b))
+            : "memory");
+      }
     }
-  };
+    // the block's shared memory outlives every copy: wait (bounded) for the
+    // last phase issued into each buffer (already complete unless aborted)
+    if (lane == 0)
+      for (int q = max(0, k - NB); q < k; ++q) att_wait(bar_of(full + q % NB), (q / NB) & 1);
+    return;
+  }
 
-  if (warp == 0)
-    for (int j = 0; j < NB - 1; ++j)
-      if (i0 + j < i1) issue(i0 + j, j);
-  uint32_t parity = 0;                                 // bit b: phase of buffer b to wait for
+  // ---- consumer group cg, warp wl of it: pairs 8 wl .. 8 wl + 7 of the group ----
+  const int cg = warp / NW, wl = warp % NW;
+  const float scale = 1.0f / sqrtf((float)D_HEAD);
+  const int G = D.Hq / D.Hkv;
+  const uint32_t ph = bufs + NB * BUF + warp * L::PW, pl = ph + 8 * PST * 2;
   int staged_g = -1, staged_hk = -1;
   uint32_t qh[KS][2], ql[KS][2];                       // B fragments of Q (this warp's pairs)
   int pos[2] = {-1, -1};                               // positions of pairs 2 q4, 2 q4 + 1 of the tile
-  int aborted_at = -1;
-  int issued = min(i1, i0 + NB - 1);                   // items whose copies were issued
-  for (int i = i0; i < i1; ++i) {
-    const int b = (i - i0) % NB;
-    const AttItem it(s_pref, n_groups, D.Hkv, i);
+  for (int k = cg; k < n; k += CG) {
+    const int b = k % NB;
+    const AttItem it(s_pref, n_groups, D.Hkv, i0 + k);
     const int gi = it.g, hk = it.hk, c = it.c;
     const AttGroup grp(gi, T, R, RG);
-    const int r0 = grp.r0, nr = grp.nr;
-    const int maxpos = B.row_pos[r0 + nr - 1];
+    const int r0 = grp.r0;
+    const int maxpos = s_maxpos[gi];
     const int nch = maxpos / ATT_CHUNK + 1;
-    const int npairs = nr * G;
+    const int npairs = grp.nr * G;
     const int k0 = c * ATT_CHUNK;
     const int nk = min(ATT_CHUNK, maxpos + 1 - k0);
     // ---- Q fragments and pair positions, when the (group, kv head) changes ----
     if (gi != staged_g || hk != staged_hk) {
-      const int p = 8 * warp + g;
+      const int p = 8 * wl + g;
       const float* qr = nullptr;
       if (p < npairs) qr = B.q + ((size_t)(r0 + p / G) * D.Hq + hk * G + p % G) * D_HEAD;
 #pragma unroll
@@ -515,34 +556,28 @@ __global__ void __launch_bounds__(NW * 32) k_attn_w(const __grid_constant__ CUte
       }
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int pj = 8 * warp + 2 * q4 + j;
+        const int pj = 8 * wl + 2 * q4 + j;
         pos[j] = pj < npairs ? B.row_pos[r0 + pj / G] : -1;
       }
       staged_g = gi;
       staged_hk = hk;
     }
-    // ---- this item's chunk: wait, zero V rows past the last key, publish ----
-    const bool ok = att_wait((uint32_t)__cvta_generic_to_shared(full + b), (parity >> b) & 1);
-    parity ^= 1u << b;
+    // ---- this item's chunk: wait, zero V rows past the last key, publish in the group ----
+    const bool ok = att_wait(bar_of(full + b), (k / NB) & 1);
     const uint32_t kb = bufs + b * BUF, vb = kb + HALVES * HB;
-    if (nk < ATT_CHUNK) {
-      for (int e = threadIdx.x; e < (ATT_CHUNK - nk) * HALVES * 8; e += NTHR) {
+    if (ok && nk < ATT_CHUNK) {
+      for (int e = wl * 32 + lane; e < (ATT_CHUNK - nk) * HALVES * 8; e += NW * 32) {
         const int h = e / ((ATT_CHUNK - nk) * 8), r = nk + (e / 8) % (ATT_CHUNK - nk), pc = e % 8;
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vb + h * HB + r * 128 + pc * 16), "r"(0u)
                      : "memory");
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // before TMA refills this buffer
     }
-    if (!__syncthreads_and(ok)) {
-      if (threadIdx.x == 0) atomicOr(S.err, DERR_TIMEOUT);
-      parity ^= 1u << b;                               // item i's phase is still owed
-      aborted_at = i;
+    if (!group_sync_and<NW>(cg, ok)) {
+      if (wl == 0 && lane == 0) atomicOr(S.err, DERR_TIMEOUT);
       break;
     }
-    // the buffer of item i - 1 is free now: refill it NB - 1 items ahead
-    if (warp == 0 && i + NB - 1 < i1) issue(i + NB - 1, (b + NB - 1) % NB);
-    if (i + NB - 1 < i1) issued = i + NB;
-    if (8 * warp < npairs) {
+    if (8 * wl < npairs) {
       // ---- S^T: four 16-key tiles x this warp's 8 pairs ----
       float sacc[4][4];
 #pragma unroll
@@ -578,7 +613,6 @@ __global__ void __launch_bounds__(NW * 32) k_attn_w(const __grid_constant__ CUte
       for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], o));
-      const uint32_t ph = pw, pl = pw + 8 * PST * 2;
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
@@ -598,7 +632,7 @@ __global__ void __launch_bounds__(NW * 32) k_attn_w(const __grid_constant__ CUte
       if (g == 0) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const int pj = 8 * warp + 2 * q4 + j;
+          const int pj = 8 * wl + 2 * q4 + j;
           if (pj < npairs && mx[j] != -INFINITY) {
             const size_t pidx = ((size_t)(r0 + pj / G) * D.Hq + hk * G + pj % G) * B.n_chunk_max + c;
             reinterpret_cast<float2*>(B.att_ml)[pidx] = make_float2(mx[j], sm[j]);
@@ -628,9 +662,12 @@ __global__ void __launch_bounds__(NW * 32) k_attn_w(const __grid_constant__ CUte
           mma_bf16(o[mt], a, bl0, bl1);
         }
       }
+      // the chunk's K/V are no longer read by this warp
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_of(empty + b)) : "memory");
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int pj = 8 * warp + 2 * q4 + j;
+        const int pj = 8 * wl + 2 * q4 + j;
         if (pj >= npairs || pos[j] < k0) continue;     // chunk lies after this row: no partial
         float* og = B.att_o + (((size_t)(r0 + pj / G) * D.Hq + hk * G + pj % G) * B.n_chunk_max + c) * D_HEAD;
 #pragma unroll
@@ -639,27 +676,23 @@ __global__ void __launch_bounds__(NW * 32) k_attn_w(const __grid_constant__ CUte
           og[16 * mt + g + 8] = o[mt][2 + j];
         }
       }
+    } else {
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_of(empty + b)) : "memory");
     }
     // ---- the last chunk of this (group, kv head) to finish merges its pairs ----
     if (!inline_merge) continue;
     __threadfence();
-    __syncthreads();
+    group_sync<NW>(cg);
     int* ctr = B.cnt_att + (size_t)gi * D.Hkv + hk;
-    if (threadIdx.x == 0) s_last = (atomicAdd(ctr, 1) == nch - 1);
-    __syncthreads();
-    if (!s_last) continue;
+    if (wl == 0 && lane == 0) s_last[cg] = (atomicAdd(ctr, 1) == nch - 1);
+    group_sync<NW>(cg);
+    const bool last = s_last[cg] != 0;
+    group_sync<NW>(cg);                                // s_last[cg] is rewritten for the group's next item
+    if (!last) continue;
     __threadfence();
-    for (int p = 8 * warp; p < min(npairs, 8 * warp + 8); ++p) merge_pair<D_HEAD>(D, B, r0 + p / G, hk * G + p % G);
-    if (threadIdx.x == 0) *ctr = 0;
-  }
-  if (aborted_at >= 0 && threadIdx.x == 0) {
-    // copies still in flight (items aborted_at .. issued - 1, one per buffer)
-    // land before the block's shared memory is released; these waits are bounded too
-    for (int k = aborted_at; k < issued; ++k) {
-      const int bk = (k - i0) % NB;
-      att_wait((uint32_t)__cvta_generic_to_shared(full + bk), (parity >> bk) & 1);
-      parity ^= 1u << bk;
-    }
+    for (int p = 8 * wl; p < min(npairs, 8 * wl + 8); ++p) merge_pair<D_HEAD>(D, B, r0 + p / G, hk * G + p % G);
+    if (wl == 0 && lane == 0) *ctr = 0;
   }
 }
 
@@ -677,14 +710,16 @@ cudaError_t configure_attn_kernels() {
 #define ALLOW(k) if ((r = allow_dyn_smem(k)) != cudaSuccess) e = r
   ALLOW((k_attn_part<128, float>)); ALLOW((k_attn_part<128, bf16_t>));
   ALLOW((k_attn_part<64, float>)); ALLOW((k_attn_part<64, bf16_t>));
-  ALLOW((k_attn_w<128, 1, ATT_NB>)); ALLOW((k_attn_w<128, 2, ATT_NB>)); ALLOW((k_attn_w<128, 4, ATT_NB>));
-  ALLOW((k_attn_w<64, 1, ATT_NB>)); ALLOW((k_attn_w<64, 2, ATT_NB>)); ALLOW((k_attn_w<64, 4, ATT_NB>));
+  ALLOW((k_attn_w<128, 1, 4, ATT_NB>)); ALLOW((k_attn_w<128, 2, 2, ATT_NB>)); ALLOW((k_attn_w<128, 4, 2, ATT_NB>));
+  ALLOW((k_attn_w<64, 1, 4, ATT_NB>)); ALLOW((k_attn_w<64, 2, 2, ATT_NB>)); ALLOW((k_attn_w<64, 4, 2, ATT_NB>));
 #undef ALLOW
   return e;
 }
 
 // Pairs per group above which the merge runs as its own kernel.
 constexpr int ATT_INLINE_PAIRS = 16;
+// (group, kv head) units of a step above which the merge runs as its own kernel.
+constexpr int ATT_INLINE_UNITS = 64;
 
 // bf16 K/V with head dim 64 or 128 take the tensor-core form (fp32 K/V the
 // FMA form). The choice depends only on the model, so greedy and
@@ -700,43 +735,36 @@ static int att_rg(const Dims& D, int R) {
   return R < cap ? R : cap;
 }
 
-bool attn_separate_merge(const Dims& D, int R) { return att_rg(D, R) * (D.Hq / D.Hkv) > ATT_INLINE_PAIRS; }
+// The merge runs as its own kernel when a group has many pairs, or when the
+// step has many (group, kv head) units (then per-chunk arrival counting
+// costs more than a launch). Either way each pair is merged by the same
+// merge_pair arithmetic, so the choice may depend on T.
+bool attn_separate_merge(const Dims& D, int R, int T) {
+  return att_rg(D, R) * (D.Hq / D.Hkv) > ATT_INLINE_PAIRS || attn_groups(D, T, R) * D.Hkv > ATT_INLINE_UNITS;
+}
 
 int attn_groups(const Dims& D, int T, int R) {
   const int RG = att_rg(D, R);
   return ((T + R - 1) / R) * ((R + RG - 1) / RG);
 }
 
-// Resident blocks per SM of a warp-tiled attention instantiation (cached).
-template <int DH, int NW>
-static int att_w_blocks_per_sm() {
-  static int n = 0;
-  if (n == 0) {
-    int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_attn_w<DH, NW, ATT_NB>, NW * 32,
-                                                      AttWSmem<DH, NW, ATT_NB>::total) != cudaSuccess || b < 1)
-      b = 1;
-    n = b;
-  }
-  return n;
-}
-
 void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
                       const CUtensorMap& kvmap, cudaStream_t st) {
   const int RG = att_rg(D, R);
   const int groups = attn_groups(D, T, R);
-  const bool sep = attn_separate_merge(D, R);
+  const bool sep = attn_separate_merge(D, R, T);
   const int im = sep ? 0 : 1;
   if (att_tc(D, R)) {
-    // one warp per 8 pairs of a group; every resident block streams its run of items
+    // one persistent block per SM: a producer warp and consumer groups of
+    // one warp per 8 pairs of a group
     const int nw = (RG * (D.Hq / D.Hkv) + 7) / 8;
-#define ATT_W(DH, NW)                                                                                         \
-  launch_k(k_attn_w<DH, NW, ATT_NB>, dim3(att_w_blocks_per_sm<DH, NW>() * D.n_sm), dim3(NW * 32),            \
-           AttWSmem<DH, NW, ATT_NB>::total, st, kvmap, D, S, B, layer, T, R, RG, groups, im)
+#define ATT_W(DH, NW, CG)                                                                                     \
+  launch_k(k_attn_w<DH, NW, CG, ATT_NB>, dim3(D.n_sm), dim3((CG * NW + 1) * 32),                               \
+           AttWSmem<DH, NW, CG, ATT_NB>::total, st, kvmap, D, S, B, layer, T, R, RG, groups, im)
     if (D.d == 128) {
-      if (nw <= 1) ATT_W(128, 1); else if (nw <= 2) ATT_W(128, 2); else ATT_W(128, 4);
+      if (nw <= 1) ATT_W(128, 1, 4); else if (nw <= 2) ATT_W(128, 2, 2); else ATT_W(128, 4, 2);
     } else {
-      if (nw <= 1) ATT_W(64, 1); else if (nw <= 2) ATT_W(64, 2); else ATT_W(64, 4);
+      if (nw <= 1) ATT_W(64, 1, 4); else if (nw <= 2) ATT_W(64, 2, 2); else ATT_W(64, 4, 2);
     }
 #undef ATT_W
   } else {

@@ -99,7 +99,7 @@ void launch_assemble_prefill(const Dims& D, const DevState& S, const StepBuf& B,
                              const void* vis, int seq, int pos0, int T, cudaStream_t st);
 void launch_qkv(const Dims& D, const DevState& S, const StepBuf& B, const LayerW& W, int layer, int T,
                 const float* x, cudaStream_t st);
-bool attn_separate_merge(const Dims& D, int R);   // merge as its own launch (many pairs per group)
+bool attn_separate_merge(const Dims& D, int R, int T);   // merge as its own launch
 int attn_groups(const Dims& D, int T, int R);
 void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, int R,
                       const CUtensorMap& kvmap, cudaStream_t st);

@@ -1022,7 +1022,7 @@ int spec_free_pages(spec_model* m) {
 
 int spec_step_launches(spec_model* m, int n_seq) {
   if (!m || n_seq < 1) return fail(SPEC_ERR_ARG, "bad arguments");
-  const int merge = attn_separate_merge(m->D, m->R) ? m->D.L : 0;   // + the standalone attention merges
+  const int merge = attn_separate_merge(m->D, m->R, n_seq * m->R) ? m->D.L : 0;   // + the standalone attention merges
   if (m->use_tc)   // per layer: norm, QKV, RoPE/KV, attention, O, router, gather, gate/up, down, combine
     return 1 + m->D.L * 10 + 3 + merge;
   return launches_per_step(m->D, n_seq * m->R) + merge;
