@@ -482,29 +482,46 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
 
   if (warp == NCW) {
     // ---- producer: item k into buffer k % NB once its previous item is consumed ----
+    // Page ids are looked up eight items ahead, lane 4 u + j holding item
+    // kb + u's 16-key block j (-1 past the chunk's last key; a missing page
+    // sets the error bit), so no lookup latency sits between a freed buffer
+    // and its refill.
+    auto lookup = [&](int kb) {
+      const int kk = kb + (lane >> 2), j = lane & 3;
+      int page = -1;
+      if (kk < n) {
+        const AttItem it(s_pref, n_groups, D.Hkv, i0 + kk);
+        const int key = it.c * ATT_CHUNK + 16 * j;
+        if (key <= s_maxpos[it.g]) {
+          page = S.bt[(size_t)s_seq[it.g] * D.max_pages + key / D.P];
+          if (page < 0) atomicOr(S.err, DERR_PAGE);
+        }
+      }
+      return page;
+    };
+    int pcur = lookup(0), pnext = lookup(8);
     int k = 0;
     for (; k < n; ++k) {
       const int b = k % NB;
+      if (k > 0 && k % 8 == 0) {
+        pcur = pnext;
+        pnext = lookup(k + 8);
+      }
       if (k >= NB && !att_wait(bar_of(empty + b), ((k / NB) - 1) & 1)) {
         if (lane == 0) atomicOr(S.err, DERR_TIMEOUT);
         break;
       }
       const AttItem it(s_pref, n_groups, D.Hkv, i0 + k);
       const int k0 = it.c * ATT_CHUNK;
-      const int nk = min(ATT_CHUNK, s_maxpos[it.g] + 1 - k0);
+      const int page = __shfl_sync(0xffffffffu, pcur, ((k % 8) << 2) | (lane & 3));
       if (lane == 0)
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_of(full + b)), "r"((uint32_t)BUF)
                      : "memory");
       __syncwarp();
       if (lane < 8 * HALVES) {
-        // lane = box: 16-key block j, 64-dim half h, K or V; a missing page sets the error bit
+        // lane = box: 16-key block j, 64-dim half h, K or V
         const int j = lane & 3, h = (lane >> 2) % HALVES, kvsel = lane / (4 * HALVES);
         const int key = k0 + 16 * j;
-        int page = -1;
-        if (16 * j < nk) {
-          page = S.bt[(size_t)s_seq[it.g] * D.max_pages + key / D.P];
-          if (page < 0) atomicOr(S.err, DERR_PAGE);
-        }
         const uint32_t dst = bufs + b * BUF + (kvsel * HALVES + h) * HB + j * 2048;
         const int c2 = (layer * 2 + kvsel) * D.Hkv + it.hk;
         asm volatile(
@@ -578,12 +595,13 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
       break;
     }
     if (8 * wl < npairs) {
-      // ---- S^T: four 16-key tiles x this warp's 8 pairs ----
-      float sacc[4][4];
+      // ---- S^T: four 16-key tiles x this warp's 8 pairs (hi and lo Q in
+      // separate accumulators, added in that order) ----
+      float sacc[4][4], slo[4][4];
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mt][e] = 0.f;
+        for (int e = 0; e < 4; ++e) sacc[mt][e] = slo[mt][e] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const int col = 16 * ks + 8 * (lane >> 4);
@@ -594,9 +612,13 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
           uint32_t a[4];
           ldsm_x4(a, hbase + sw128(key, (col & 63) >> 3));
           mma_bf16(sacc[mt], a, qh[ks][0], qh[ks][1]);
-          mma_bf16(sacc[mt], a, ql[ks][0], ql[ks][1]);
+          mma_bf16(slo[mt], a, ql[ks][0], ql[ks][1]);
         }
       }
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mt][e] += slo[mt][e];
       // ---- scale, mask, column max / sum over the 64 keys ----
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
