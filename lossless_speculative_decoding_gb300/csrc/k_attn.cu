@@ -732,8 +732,8 @@ cudaError_t configure_attn_kernels() {
 #define ALLOW(k) if ((r = allow_dyn_smem(k)) != cudaSuccess) e = r
   ALLOW((k_attn_part<128, float>)); ALLOW((k_attn_part<128, bf16_t>));
   ALLOW((k_attn_part<64, float>)); ALLOW((k_attn_part<64, bf16_t>));
-  ALLOW((k_attn_w<128, 1, 4, ATT_NB>)); ALLOW((k_attn_w<128, 2, 2, ATT_NB>)); ALLOW((k_attn_w<128, 4, 2, ATT_NB>));
-  ALLOW((k_attn_w<64, 1, 4, ATT_NB>)); ALLOW((k_attn_w<64, 2, 2, ATT_NB>)); ALLOW((k_attn_w<64, 4, 2, ATT_NB>));
+  ALLOW((k_attn_w<128, 1, 6, ATT_NB>)); ALLOW((k_attn_w<128, 2, 2, ATT_NB>)); ALLOW((k_attn_w<128, 4, 2, ATT_NB>));
+  ALLOW((k_attn_w<64, 1, 6, ATT_NB>)); ALLOW((k_attn_w<64, 2, 2, ATT_NB>)); ALLOW((k_attn_w<64, 4, 2, ATT_NB>));
 #undef ALLOW
   return e;
 }
@@ -784,9 +784,9 @@ void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int la
   launch_k(k_attn_w<DH, NW, CG, ATT_NB>, dim3(D.n_sm), dim3((CG * NW + 1) * 32),                               \
            AttWSmem<DH, NW, CG, ATT_NB>::total, st, kvmap, D, S, B, layer, T, R, RG, groups, im)
     if (D.d == 128) {
-      if (nw <= 1) ATT_W(128, 1, 4); else if (nw <= 2) ATT_W(128, 2, 2); else ATT_W(128, 4, 2);
+      if (nw <= 1) ATT_W(128, 1, 6); else if (nw <= 2) ATT_W(128, 2, 2); else ATT_W(128, 4, 2);
     } else {
-      if (nw <= 1) ATT_W(64, 1, 4); else if (nw <= 2) ATT_W(64, 2, 2); else ATT_W(64, 4, 2);
+      if (nw <= 1) ATT_W(64, 1, 6); else if (nw <= 2) ATT_W(64, 2, 2); else ATT_W(64, 4, 2);
     }
 #undef ATT_W
   } else {
