@@ -54,7 +54,7 @@ int spec_lmhead_argmax(const float* x_dev, int T, int hidden, int vocab, const v
   if (!scratch_dev || (int64_t)scratch_bytes < spec_lmhead_argmax_scratch_bytes(T, vocab))
     return op_fail(SPEC_ERR_ARG, "scratch smaller than spec_lmhead_argmax_scratch_bytes(T, vocab)");
   if (configure_gemv_kernels() != cudaSuccess) return op_fail(SPEC_ERR_CUDA, "kernel attribute set-up failed");
-  Dims D;
+  Dims D{};
   StepBuf B;
   lmhead_setup(T, hidden, vocab, w_dtype, eps, &D, &B);
   B.am_val = reinterpret_cast<float*>(scratch_dev);
@@ -116,7 +116,7 @@ extern "C" int spec_lmhead_argmax_noalloc(const float* x_dev, int T, int hidden,
     return op_fail(SPEC_ERR_ARG, "T * ceil(vocab / 32) exceeds SPEC_LMHEAD_NOALLOC_MAX_PAIRS");
   void* scratch = nullptr;
   if ((rc = noalloc_setup(&scratch))) return rc;
-  Dims D;
+  Dims D{};
   StepBuf B;
   lmhead_setup(T, hidden, vocab, w_dtype, eps, &D, &B);
   // every candidate slot is written by its block before the reduction reads
