@@ -355,3 +355,52 @@ def test_tensor_core_path_parity_and_invariance(cfg, K, nseq):
         acc, bon = gm.verify_batch([0, 1, 2], np.zeros((3, K), np.int32), [0, 0, 0])
         together.append(int(bon[0]))
     assert np.array_equal(alone, np.array(together))
+
+
+def test_tensor_core_attention_paging_is_addressing_only():
+    """The bf16 attention fetches K/V as 16-key TMA boxes from the paged pool.
+    Page sizes 16, 48 (64-key chunks then straddle pages) and 256 must give
+    identical bits, including the partially filled last chunk."""
+    cfg = MOE_SMALL
+    w = syn.generate_weights(cfg, 5)
+    wl = syn.Workload("t", cfg, 1, 3, "iid", 0.6, (150, 0, 0), 8, 0, (40,))
+    prompt = syn.make_prompts(wl)[0]
+    outs = []
+    for ps in (16, 48, 256):
+        gm = gpu_model(cfg, w, max_ctx=512, max_draft=3, page_size=ps, n_pages=-(-512 // ps) + 8)
+        first = gm.prefill(0, prompt.visual, prompt.tokens)
+        lg = gm.debug_logits([0], np.array([first, 2, 3]))
+        a, b = gm.verify(0, [first, 2, 3])
+        lg2 = gm.debug_logits([0], np.array([b, 5, 6]))
+        outs.append((first, lg, a, b, lg2))
+        gm.close()
+    for o in outs[1:]:
+        assert o[0] == outs[0][0] and (o[2], o[3]) == (outs[0][2], outs[0][3])
+        assert np.array_equal(o[1], outs[0][1]) and np.array_equal(o[4], outs[0][4])
+
+
+def test_attention_merge_placement_is_invariant():
+    """With few (group, kv head) units a step's last chunk merges its pairs in
+    the attention kernel; with many the merge runs as its own kernel. Both use
+    the same chunk-order merge, so a sequence's verify rows are bit-identical
+    scored alone and inside a 40-sequence step."""
+    from lossless_speculative_decoding_gb300 import binding as B
+    cfg = MOE_SMALL
+    n = 40
+    w = syn.generate_weights(cfg, 6)
+    wl = syn.Workload("t", cfg, n, 3, "iid", 0.6, (96, 0, 0), 8, 0, (40,))
+    prompts = syn.make_prompts(wl, n_seq=n)
+    gm = gpu_model(cfg, w, max_ctx=256, max_draft=3, max_seqs=n, max_batch=n, n_pages=n * 9 + 16)
+    try:
+        # the 40-sequence step adds one standalone merge launch per layer
+        assert B.spec_step_launches(gm.h, n) == B.spec_step_launches(gm.h, 1) + cfg.n_layers
+        for i, p in enumerate(prompts):
+            gm.prefill(i, p.visual, p.tokens)
+        d = np.array([[7, 8, 9]] * n, np.int32)
+        alone = gm.debug_logits([0], d[:1])
+        together = gm.debug_logits(list(range(n)), d).reshape(n, 4, cfg.vocab)
+        assert np.array_equal(alone.reshape(4, cfg.vocab), together[0])
+        alone5 = gm.debug_logits([5], d[:1])
+        assert np.array_equal(alone5.reshape(4, cfg.vocab), together[5])
+    finally:
+        gm.close()
