@@ -30,6 +30,9 @@ GPU path):
 * Acceptance: a = the longest prefix of drafts with d_j = g_(j-1); the bonus
   token g_a is always committed, so a verify step commits a + 1 tokens.
 
+``oracle.sampling`` holds the stochastic counterpart of the acceptance rule
+(rejection-sampling verification), pinned by tests/test_oracle_sampling.py.
+
 Parity pins (tests/test_oracle_*.py): brute-force recompute without a cache,
 spec == greedy for random / all-correct / all-wrong drafts, dense special
 case, one-key attention, RoPE identity and relative-position property, e4m3 and
