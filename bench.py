@@ -297,6 +297,57 @@ def steady_state_prompts(wl, prompts, rank: int):
     return pre, out
 
 
+def sampling_leg(NB: int, K: int, V: int, hbm_gbs: float) -> dict:
+    """Rejection-sampling verification (spec_rejection_sample) at the step's
+    shape: NB sequences x (K+1) logit rows x V, a drafter certain of its
+    drafts (70% of them the target's likeliest token), temperature 1. Inputs
+    rotate through a ring of copies larger than the L2. The algorithmic bytes
+    of a call are the logit rows the rule must read: rows 0..a of each
+    sequence (a = drafts accepted), V * 4 bytes each."""
+    import math
+    import torch
+    from lossless_speculative_decoding_gb300 import binding as B
+    g = torch.Generator(device="cuda").manual_seed(7)
+    per = NB * (K + 1) * V * 4
+    copies = int(min(128, max(2, math.ceil(256e6 / per))))
+    logits = [torch.randn(NB, K + 1, V, device="cuda", generator=g) * 3.0 for _ in range(copies)]
+    drafts = []
+    for lg in logits:
+        top = torch.argmax(lg[:, :K], dim=-1) if K else torch.zeros(NB, 0, dtype=torch.int64, device="cuda")
+        rnd = torch.randint(0, V, (NB, K), device="cuda", generator=g)
+        keep = torch.rand(NB, K, device="cuda", generator=g) < 0.7
+        drafts.append(torch.where(keep, top, rnd).to(torch.int32).contiguous())
+    ua = torch.rand(NB, max(K, 1), device="cuda", generator=g)
+    us = torch.rand(NB, K + 1, device="cuda", generator=g)
+    acc = torch.empty(NB, dtype=torch.int32, device="cuda")
+    tok = torch.empty(NB, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+
+    def call(c):
+        B.spec_rejection_sample(logits[c], drafts[c], None, ua, us, NB, K, V, 1.0, acc, tok, st.cuda_stream)
+
+    rows = 0
+    for c in range(copies):                          # warm-up, and the rows each copy reads
+        call(c)
+        rows += int(acc.sum().item()) + NB
+    n_calls = 4 * copies
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for i in range(n_calls):
+        call(i % copies)
+    e1.record(st)
+    e1.synchronize()
+    us_call = e0.elapsed_time(e1) * 1e3 / n_calls
+    bytes_call = rows / copies * V * 4
+    ach = bytes_call / (us_call * 1e-6) / 1e9
+    del logits, drafts
+    return {"kernel": "k_rejection_sample", "shape": f"{NB} x {K + 1} x {V}", "us_per_call": us_call,
+            "bytes_per_call": bytes_call, "achieved_gbs": ach, "frac": ach / hbm_gbs,
+            "drafter": "certain of its drafts (70% the target argmax)", "temperature": 1.0,
+            "l2": f"ring of {copies} input copies ({copies * per / 1e6:.0f} MB)"}
+
+
 def run_ours(args):
     import torch
     ws, rank, local = dist_env()
@@ -512,6 +563,7 @@ def run_ours(args):
         }
         if cpu:
             line["cpu_baseline"] = cpu
+        line["rejection_sampling"] = sampling_leg(NB, K, cfg.vocab, peaks["hbm_gbs"])
         print(json.dumps(line), flush=True)
     gm.close()
     if ws > 1:

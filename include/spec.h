@@ -242,6 +242,37 @@ int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const float* a_scal
                       int a_fp8, const void* b_dev, const void* b_lo_dev, int M, int N, int K, int dual, int n_tile,
                       int k_split, void* out_dev, int* err_dev, uintptr_t cuda_stream);
 
+/* Rejection-sampling verification, the stochastic counterpart of the greedy
+ * acceptance rule ("End-to-end OCR expert model architecture and acceleration
+ * principles", section 6.1 and section 11 item 2: rejection sampling keeps
+ * the output distribution equal to the target model's own). Read as the
+ * published speculative-sampling rule: with p_j = softmax(row j-1 of the
+ * sequence's logits / temperature), j = 1..K+1, and the drafter's q_j:
+ *   accept d_j while u_accept[j-1] * q_j(d_j) < p_j(d_j);
+ *   at the first rejection (draft j) append a draw from max(0, p_j - q_j)
+ *   (normalised; p_j itself if that is zero everywhere) with u_sample[j-1];
+ *   if all K are accepted append a draw from p_(K+1) with u_sample[K].
+ * A draw with weights w and uniform u is the smallest v whose running sum of
+ * w (index order) exceeds u * sum(w). Computed in fp32 with fixed reduction
+ * orders (rounding can move a draw across a bucket edge that u * sum(w) lies
+ * within about 1e-6 of sum(w)).
+ *   logits_dev:  [n_seq][K+1][vocab] f32, 16-byte aligned (the layout
+ *                spec_debug_logits writes).
+ *   drafts_dev:  [n_seq][K] int32 draft tokens.
+ *   q_dev:       [n_seq][K][vocab] f32 drafter probabilities, or NULL for a
+ *                drafter certain of its drafts (q_j one-hot at d_j).
+ *   u_accept_dev [n_seq][K], u_sample_dev [n_seq][K+1]: f32 uniforms in [0, 1).
+ *   out_accepted_dev / out_token_dev: [n_seq] int32: drafts accepted and the
+ *                appended token; -1 / -1 for a sequence with a draft outside
+ *                [0, vocab).
+ * All device pointers, caller-owned; enqueued on cuda_stream. vocab must be a
+ * multiple of 4 and at most 262144; K >= 0 (K = 0 samples row 0).
+ * Errors: SPEC_ERR_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA (launch). */
+int spec_rejection_sample(const float* logits_dev, const int32_t* drafts_dev, const float* q_dev,
+                          const float* u_accept_dev, const float* u_sample_dev, int n_seq, int K, int vocab,
+                          float temperature, int32_t* out_accepted_dev, int32_t* out_token_dev,
+                          uintptr_t cuda_stream);
+
 /* Same computation as spec_lmhead_argmax for callers that cannot allocate
  * device memory (no cudaMalloc of their own, none by the library): the
  * candidate scratch is a fixed device array inside the library, sized for

@@ -87,6 +87,9 @@ _SIGS = [
                                          ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_size_t]),
+    ("spec_rejection_sample", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]),
     ("spec_strerror", ctypes.c_char_p, [ctypes.c_int]),
     ("spec_last_error", ctypes.c_char_p, []),
     ("spec_pool_create", ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -292,6 +295,13 @@ def spec_lmhead_argmax_noalloc(x_dev, T: int, hidden: int, vocab: int, w_dev, w_
                                eps: float, out_tokens_dev, cuda_stream: int = 0) -> None:
     _check(lib().spec_lmhead_argmax_noalloc(_ptr(x_dev), T, hidden, vocab, _ptr(w_dev), w_dtype, _ptr(gamma_dev),
                                             eps, _ptr(out_tokens_dev), cuda_stream))
+
+
+def spec_rejection_sample(logits_dev, drafts_dev, q_dev, u_accept_dev, u_sample_dev, n_seq: int, K: int,
+                          vocab: int, temperature: float, out_accepted_dev, out_token_dev, cuda_stream: int = 0) -> None:
+    _check(lib().spec_rejection_sample(_ptr(logits_dev), _ptr(drafts_dev), _ptr(q_dev), _ptr(u_accept_dev),
+                                       _ptr(u_sample_dev), n_seq, K, vocab, float(temperature),
+                                       _ptr(out_accepted_dev), _ptr(out_token_dev), cuda_stream))
 
 
 def spec_tc_gemm_test(a_dev, a2_dev, b_dev, b_lo_dev, M: int, N: int, K: int, dual: int, out_dev, err_dev,
