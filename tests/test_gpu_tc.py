@@ -1,7 +1,9 @@
 """Tensor-core GEMM (tcgen05, TMA-staged, TMEM accumulator) against a plain
 float64 matmul of the same bf16 values: the store epilogue (fp32 out) and
 the dual SwiGLU epilogue (bf16 out), over shapes with partial activation
-boxes, more K tiles than pipeline stages, and several column tiles; and the
+boxes, more K tiles than pipeline stages, several column tiles, CTAs of 1 to
+4 activation boxes (MMA N of 32 to 256 with the hi and lo rows) and one- and
+two-atom stages with an odd number of K atoms; and the
 hi + lo split of fp32 activations, which must reach near-fp32 accuracy (a
 bound a single bf16 operand misses by two orders of magnitude)."""
 import numpy as np
@@ -18,7 +20,7 @@ def _bf16(rng, shape, scale):
     return bits, oracle.decode_bf16(bits)
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 32, 64), (256, 40, 320), (384, 300, 1280), (128, 1, 896)])
+@pytest.mark.parametrize("M,N,K", [(128, 32, 64), (256, 40, 320), (384, 300, 1280), (128, 1, 896), (128, 96, 1344)])
 def test_tc_gemm_store(M, N, K):
     import torch
     from lossless_speculative_decoding_gb300 import binding as B
@@ -61,7 +63,8 @@ def test_tc_gemm_swiglu(M, N, K):
     np.testing.assert_allclose(got, ref, rtol=1e-2, atol=1e-2 * np.abs(ref).max())
 
 
-@pytest.mark.parametrize("M,N,K,nt", [(256, 300, 512, 0), (128, 9, 2048, 0), (256, 300, 512, 32), (384, 100, 768, 64)])
+@pytest.mark.parametrize("M,N,K,nt", [(256, 300, 512, 0), (128, 9, 2048, 0), (256, 300, 512, 32), (384, 100, 768, 64),
+                                     (128, 80, 640, 0), (256, 96, 1344, 0)])
 def test_tc_gemm_split_activations(M, N, K, nt):
     import torch
     from lossless_speculative_decoding_gb300 import binding as B
@@ -86,7 +89,7 @@ def test_tc_gemm_split_activations(M, N, K, nt):
 
 
 @pytest.mark.parametrize("M,N,K,dual,nt", [(256, 40, 320, 0, 0), (128, 200, 1280, 0, 32), (256, 48, 192, 1, 0),
-                                           (128, 130, 896, 1, 32)])
+                                           (128, 130, 896, 1, 32), (128, 90, 704, 0, 0), (128, 70, 448, 1, 0)])
 def test_tc_gemm_fp8_weights(M, N, K, dual, nt):
     """e4m3 weights widened to bf16 in shared memory, per-row scales applied in
     the epilogue: against float64 of the decoded e4m3 values times the scales."""
