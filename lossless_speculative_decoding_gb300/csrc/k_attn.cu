@@ -5,18 +5,26 @@
 // are cut into chunks at absolute positions c*64 -- never at boundaries that
 // depend on the number of rows, the batch or the page size -- so a row's
 // result is the same whether it is scored alone (greedy step), with drafts,
-// or during prefill. One block loads the K/V of one chunk of one kv head once
-// (page by page, converted to fp32 in shared memory) and serves every query
-// row of one sequence group and every q head that shares that kv head (GQA).
-// A partial (unnormalised output, running max, running sum) per (row, head,
-// chunk) goes to scratch and the partials are merged in chunk order: by the
-// last block of a (group, kv head) to finish when a group has few (row, q
-// head) pairs, else by a separate kernel with one warp per pair.
+// or during prefill. A chunk's K/V are read once per (row group, kv head) and
+// serve every query row of the group and every q head sharing that kv head
+// (GQA). A partial (unnormalised output, running max, running sum) per (row,
+// head, chunk) goes to scratch and the partials are merged in chunk order: by
+// the last chunk of a (group, kv head) to finish when the step has few such
+// units and a group few pairs, else by a separate kernel with one warp per
+// pair -- the same merge arithmetic either way.
 //
-// Work list: the (group, chunk, kv head) items of the step are numbered
-// group by group (each group has ceil((last position + 1) / 64) chunks) and a
-// fixed grid strides over them, so long and short sequences share the GPU
-// evenly and no block waits on a serial walk over a long context.
+// Two forms, chosen per model:
+//  * bf16 K/V, head dim 64 or 128: k_attn_w, persistent blocks with a TMA
+//    producer warp and mma.sync consumer warps (described below);
+//  * fp32 K/V: k_attn_part, SIMT dot products per (row, q head) pair over a
+//    chunk staged with cp.async, a fixed grid striding over the items, so
+//    the fp32 model keeps exact fp32 arithmetic.
+// Work list: the step's (group, chunk, kv head) items, numbered group by
+// group from a per-block prefix over the groups' last positions (each group
+// has ceil((last position + 1) / 64) chunks; the SIMT form takes a group's
+// items chunk by chunk, the tensor-core form kv head by kv head), so long and
+// short sequences share the GPU evenly and no block waits on a serial walk
+// over a long context.
 #include "common.cuh"
 #include "gemv.cuh"
 #include "kernels.h"
