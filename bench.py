@@ -552,7 +552,9 @@ def run_ours(args):
                               "t_hbm_us": t_hbm_us, "t_tensor_us": t_tc_us,
                               "bound": "hbm" if t_hbm_us >= t_tc_us else "tensor", "t_roof_us": t_roof_us,
                               "t_meas_us": ms_per_step * 1e3, "frac": t_roof_us / (ms_per_step * 1e3),
-                              "profiled_kernel_us_per_step": prof_ms * 1e3, "kernel_share": share},
+                              "profiled_kernel_us_per_step": prof_ms * 1e3, "kernel_share": share,
+                              "class_bytes_per_launch": {k: cb[k] / max(stats[k]["launches"], 1)
+                                                         for k in cb if k in stats}},
             "e2e": {"value": e2e_committed / e2e_s, "unit": "tokens/s",
                     "h2d_bytes_per_step": (h2d1 - h2d0) / KS, "d2h_bytes_per_step": (d2h1 - d2h0) / KS},
             "gpu_launches": launches * KS,
