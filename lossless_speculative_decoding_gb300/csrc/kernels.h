@@ -66,7 +66,6 @@ struct StepBuf {
   float* rlogit;                     // [Tmax, E] router logits
   int* cnt_row;                      // [Tmax] router arrivals per row (expert-group blocks)
   int* cnt_att;                      // [Tmax * Hkv] attention arrivals per (row group, kv head)
-  int* cnt_down;                     // [h/4 + 1] expert-down arrivals per 4-column output tile
   int* cnt_lm;                       // [ceil(Tmax/TP)] LM-head arrivals per row pass
   float* h_act;      // [T*NS, inter]
   float* y;          // [T*NS, h]

@@ -507,7 +507,7 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
       (rc = m->dalloc(&B.act_cnt, max_active)) || (rc = m->dalloc(&B.n_active, 1)) ||
       (rc = m->dalloc(&B.counter, 4)) || (rc = m->dalloc(&B.rlogit, (size_t)T * std::max(D.E, 1))) ||
       (rc = m->dalloc(&B.cnt_row, T)) || (rc = m->dalloc(&B.cnt_att, (size_t)T * D.Hkv)) ||
-      (rc = m->dalloc(&B.cnt_down, D.h / 4 + 1)) || (rc = m->dalloc(&B.cnt_lm, (T + GEMV_TP - 1) / GEMV_TP)) || (rc = m->dalloc(&B.h_act, (size_t)T * NS * D.inter)) ||
+      (rc = m->dalloc(&B.cnt_lm, (T + GEMV_TP - 1) / GEMV_TP)) || (rc = m->dalloc(&B.h_act, (size_t)T * NS * D.inter)) ||
       (rc = m->dalloc(&B.y, (size_t)T * NS * D.h)) ||
       (rc = m->dalloc(&B.am_val, (size_t)T * B.n_vblocks)) || (rc = m->dalloc(&B.am_idx, (size_t)T * B.n_vblocks)) ||
       (rc = m->dalloc(&B.g, T)))
@@ -604,7 +604,6 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
   CU(cudaMemset(B.counter, 0, 4 * sizeof(int)));
   CU(cudaMemset(B.cnt_row, 0, (size_t)T * sizeof(int)));
   CU(cudaMemset(B.cnt_att, 0, (size_t)T * D.Hkv * sizeof(int)));
-  CU(cudaMemset(B.cnt_down, 0, (D.h / 4 + 1) * sizeof(int)));
   CU(cudaMemset(B.cnt_lm, 0, ((T + GEMV_TP - 1) / GEMV_TP) * sizeof(int)));
   CU(cudaMemset(stage, 0, (4 + m->step_in_n) * sizeof(int)));
   CU(cudaMallocHost(&m->pin_in, std::max(4 + m->step_in_n, T) * sizeof(int32_t)));
