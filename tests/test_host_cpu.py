@@ -114,3 +114,24 @@ def test_replica_aggregation_two_ranks():
     for p in ps:
         p.join(60)
     assert res == [(0, 11.0, 300), (1, 11.0, 300)]
+
+
+def test_rejection_sample_argument_contract(B):
+    """spec_rejection_sample checks its arguments on the host before any CUDA
+    call, with the error codes its declaration states (the pointers here are
+    never dereferenced)."""
+    fake = 1 << 20                                       # 16-byte aligned, never dereferenced
+    ok = dict(logits_dev=fake, drafts_dev=fake, q_dev=None, u_accept_dev=fake, u_sample_dev=fake, n_seq=2, K=3,
+              vocab=1024, temperature=1.0, out_accepted_dev=fake, out_token_dev=fake)
+    cases = [
+        (dict(logits_dev=None), -1), (dict(u_sample_dev=None), -1), (dict(out_token_dev=None), -1),
+        (dict(drafts_dev=None), -1),                     # K > 0 needs drafts and acceptance uniforms
+        (dict(n_seq=0), -1), (dict(K=-1), -1), (dict(vocab=2), -1),
+        (dict(temperature=0.0), -1), (dict(temperature=float("nan")), -1),
+        (dict(vocab=1022), -6), (dict(vocab=262_148), -6),
+        (dict(logits_dev=fake + 4), -1),                 # logits must be 16-byte aligned
+    ]
+    for change, code in cases:
+        with pytest.raises(B.SpecError) as e:
+            B.spec_rejection_sample(**{**ok, **change})
+        assert e.value.code == code, (change, str(e.value))
