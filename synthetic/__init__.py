@@ -319,6 +319,42 @@ def generate_weights(cfg: ModelConfig, seed: int = 0, threads: Optional[int] = N
 
 
 # --------------------------------------------------------------------------- #
+# Draft head (FastMTP) weights
+# --------------------------------------------------------------------------- #
+MTP_TENSORS = ("enorm", "hnorm", "eh_proj", "attn_norm", "w_qkv", "w_o", "ffn_norm", "w_gate", "w_up", "w_down")
+
+
+def mtp_inter(cfg: ModelConfig) -> int:
+    """Width of the draft block's dense SwiGLU: the FFN width one token meets
+    in the decoder ((top_k + n_shared) * inter; inter for a dense decoder)."""
+    return (cfg.top_k + cfg.n_shared) * cfg.inter if cfg.n_experts else cfg.inter
+
+
+def mtp_tensor_shapes(cfg: ModelConfig) -> Dict[str, Tuple[int, ...]]:
+    h, d, f = cfg.hidden, cfg.head_dim, mtp_inter(cfg)
+    return {"enorm": (h,), "hnorm": (h,), "eh_proj": (h, 2 * h), "attn_norm": (h,),
+            "w_qkv": (cfg.qkv_rows, h), "w_o": (h, cfg.n_q_heads * d), "ffn_norm": (h,),
+            "w_gate": (f, h), "w_up": (f, h), "w_down": (h, f)}
+
+
+def generate_mtp_weights(cfg: ModelConfig, seed: int = 0, norm_gamma_std: float = 0.0) -> Dict[str, np.ndarray]:
+    """The draft head's own tensors (the embedding, output norm and LM head are
+    the decoder's), float32: matrices ~ N(0, init_std^2) from PCG64 streams
+    keyed by (seed, 10,000 + tensor index) -- disjoint from the decoder's --
+    rounded to bf16 values for bf16 / fp8 models (the head stays bf16); norm
+    gains ones, or 1 + N(0, norm_gamma_std^2)."""
+    out = {}
+    for i, (name, shape) in enumerate(mtp_tensor_shapes(cfg).items()):
+        if name.endswith("norm"):
+            g = 1.0 + _normal(seed, 10_000 + i, 0, shape, norm_gamma_std) if norm_gamma_std > 0 else np.ones(shape)
+            out[name] = np.asarray(g, np.float32)
+            continue
+        m = _normal(seed, 10_000 + i, 0, shape, cfg.init_std)
+        out[name] = m if cfg.wdtype == F32 else bf16_bits_to_f32(f32_to_bf16_bits(m))
+    return out
+
+
+# --------------------------------------------------------------------------- #
 # Prompts, output lengths
 # --------------------------------------------------------------------------- #
 
