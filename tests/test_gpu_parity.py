@@ -404,3 +404,33 @@ def test_attention_merge_placement_is_invariant():
         assert np.array_equal(alone5.reshape(4, cfg.vocab), together[5])
     finally:
         gm.close()
+
+
+GQA2_SMALL = syn.scaled(DENSE_SMALL, name="dense-small-gqa2", n_q_heads=4, n_kv_heads=2)
+
+
+@pytest.mark.parametrize("cfg", [DENSE_SMALL, GQA2_SMALL])
+def test_attention_group_forms_parity_and_lossless(cfg):
+    """K = 3 (4 rows per sequence) with 4 or 2 q heads per kv head: 16 pairs per
+    group (two warps of the tensor-core attention) or 8 pairs spread over two
+    heads (one warp). Verify rows match the oracle within 2e-2 of each row's
+    range, and speculative decoding reproduces the one-row greedy decode."""
+    w = syn.generate_weights(cfg, 12)
+    om = oracle.OracleModel(w)
+    wl = syn.Workload("t", cfg, 1, 3, "iid", 0.6, (70, 0, 0), 8, 0, (40,))
+    prompt = syn.make_prompts(wl)[0]
+    g0 = gpu_model(cfg, w, max_ctx=256, max_draft=0)
+    greedy, _ = run_spec(g0, 0, prompt, 32, 0, lambda n, m, s: [])
+    g0.close()
+    g3 = gpu_model(cfg, w, max_ctx=256, max_draft=3)
+    toks, _ = run_spec(g3, 0, prompt, 32, 3, _drafter_vs(greedy, 0.6, cfg.vocab))
+    assert np.array_equal(toks, greedy)
+    cache = oracle.KVCache(cfg)
+    x = oracle.prompt_embeddings(om, prompt)
+    rows = np.concatenate([x, om.tok_embed[toks[:-1]]])
+    oracle.forward(om, cache, rows, np.arange(len(rows)))
+    d = [int(t) for t in np.random.default_rng(2).integers(0, cfg.vocab, 3)]
+    lg = g3.debug_logits([0], np.array(d))
+    ol = oracle.verify_rows(om, cache, int(toks[-1]), d)
+    assert row_tol_ok(lg, ol, 2e-2).all()
+    g3.close()
