@@ -56,6 +56,28 @@ def decode_e4m3(codes: np.ndarray, scale: Optional[np.ndarray] = None) -> np.nda
     return v.astype(np.float32)
 
 
+def decode_e2m1(codes: np.ndarray) -> np.ndarray:
+    """FP4 E2M1 codes (low 4 bits) as float32: bit 3 the sign, bits 2-1 the
+    exponent with bias 1, bit 0 the mantissa; exponent 0 is subnormal
+    (0 or 0.5); no infinities or NaN."""
+    c = np.asarray(codes, dtype=np.uint8) & np.uint8(0xF)
+    e = ((c >> 1) & 3).astype(np.int32)
+    m = (c & 1).astype(np.float64)
+    mag = np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2(e - 1))
+    return np.where(c & 8, -mag, mag).astype(np.float32)
+
+
+def decode_nvfp4(codes: np.ndarray, block_scales: np.ndarray, tensor_scale: float) -> np.ndarray:
+    """NVFP4 values: each run of 16 consecutive elements along the last axis
+    shares one E4M3 block scale, and the whole tensor one float32 scale:
+    value = e2m1(code) * e4m3(block scale) * tensor_scale.
+    codes: [..., K] (one 4-bit code per element); block_scales: [..., K/16]."""
+    v = decode_e2m1(codes).astype(np.float64)
+    s = decode_e4m3(block_scales).astype(np.float64)
+    v = v.reshape(*v.shape[:-1], -1, 16) * s[..., None] * float(tensor_scale)
+    return v.reshape(codes.shape).astype(np.float32)
+
+
 class OracleModel:
     """The decoder of one model configuration with every weight decoded to
     float32 (bf16 values upcast exactly; e4m3 codes times their per-row fp32

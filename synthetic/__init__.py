@@ -227,6 +227,38 @@ def quantize_rows_e4m3(w: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     return codes, scale
 
 
+_E2M1_POS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def f32_to_e2m1(a: np.ndarray) -> np.ndarray:
+    """binary32 -> FP4 E2M1 codes (one per byte, low nibble), round to nearest
+    (ties to the even code), saturating at +-6; -0 encodes as 0."""
+    a = np.asarray(a, dtype=np.float32)
+    mag = np.minimum(np.abs(a).astype(np.float64), 6.0)
+    hi = np.searchsorted(_E2M1_POS, mag, side="left").clip(0, 7)
+    lo = np.maximum(hi - 1, 0)
+    dlo, dhi = mag - _E2M1_POS[lo], _E2M1_POS[hi] - mag
+    code = np.where((dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0)), hi, lo)
+    code = np.where(mag == _E2M1_POS[hi], hi, code).astype(np.uint8)
+    return (code | ((np.signbit(a) & (code != 0)).astype(np.uint8) << np.uint8(3))).astype(np.uint8)
+
+
+def quantize_nvfp4(w: np.ndarray):
+    """NVFP4 encoding of w [..., K] (K a multiple of 16): tensor scale
+    amax(w) / (6 * 448); per 16-element block an E4M3 scale of
+    amax(block) / (6 * tensor scale); codes E2M1(w / (block scale * tensor
+    scale)). Returns (codes [..., K], block scale codes [..., K/16], tensor scale)."""
+    w = np.asarray(w, dtype=np.float32)
+    amax = float(np.max(np.abs(w)))
+    ts = np.float32(amax / (6.0 * 448.0)) if amax > 0 else np.float32(1.0)
+    blocks = w.reshape(*w.shape[:-1], -1, 16)
+    bs_codes = f32_to_e4m3(np.max(np.abs(blocks), axis=-1) / (6.0 * ts))
+    bs = _E4M3_POS[bs_codes & 0x7F].astype(np.float64)
+    denom = np.where(bs > 0, bs * float(ts), 1.0)[..., None]
+    codes = f32_to_e2m1((blocks / denom).astype(np.float32)).reshape(w.shape)
+    return codes, bs_codes, float(ts)
+
+
 # --------------------------------------------------------------------------- #
 # Weights
 # --------------------------------------------------------------------------- #
