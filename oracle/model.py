@@ -235,8 +235,9 @@ def forward(m: OracleModel, cache: KVCache, x: np.ndarray, positions: np.ndarray
 
     With ``trace`` (a dict), ``trace["route_gap"]`` receives, per row, the
     smallest gap over the layers between the k-th and (k+1)-th largest router
-    logits: how close the row's expert choice came to a tie (a diagnostic
-    output only; the arithmetic is unchanged)."""
+    logits: how close the row's expert choice came to a tie, and
+    ``trace["hidden"]`` the rows' final-normed states (diagnostic outputs
+    only; the arithmetic is unchanged)."""
     cfg = m.cfg
     positions = np.asarray(positions)
     assert positions[0] == cache.length
@@ -262,6 +263,8 @@ def forward(m: OracleModel, cache: KVCache, x: np.ndarray, positions: np.ndarray
             trace["route_gap"] = np.minimum(trace.get("route_gap", np.full(n, np.inf, np.float32)), gap)
         x = x + moe_ffn(cfg, L, u)
     u = rms_norm(x, m.final_norm, cfg.rms_eps)
+    if trace is not None:
+        trace["hidden"] = u                              # the LM head's input (post-norm state)
     return (u @ m.lm_head.T).astype(np.float32)
 
 

@@ -37,7 +37,8 @@ from typing import Dict, List, Optional, Sequence, Tuple
 
 import numpy as np
 
-from .model import OracleModel, _silu, attention_rows, rms_norm, rope
+from .model import (KVCache, OracleModel, _silu, accept, argmax_lowest, attention_rows, forward,
+                    prompt_embeddings, rms_norm, rope, verify_rows)
 
 
 class MtpHead:
@@ -119,3 +120,36 @@ def draft(head: MtpHead, b: np.ndarray, tokens: Sequence[int], p0: int, K: int) 
         d.append(t)
         ext.append(t)
     return d
+
+
+def spec_decode(m: OracleModel, head: MtpHead, prompt, n_new: int, K: int):
+    """Speculative decoding with the draft head's own drafts and greedy
+    verification: after each verify step the committed rows' states extend
+    b, the head drafts K tokens after the last committed token, and the
+    target keeps the longest agreeing prefix plus its own next token.
+    Returns (tokens, per-step accepted counts). Visual positions carry no
+    token id (the grid never reads them), so they hold 0 here."""
+    cache = KVCache(m.cfg)
+    x = prompt_embeddings(m, prompt)
+    tr = {}
+    lg = forward(m, cache, x, np.arange(len(x)), tr)
+    b = tr["hidden"]
+    n_vis = len(prompt.visual)
+    p0 = max(n_vis - 1, 0)
+    tokens = [0] * n_vis + [int(t) for t in prompt.tokens]
+    out = [int(argmax_lowest(lg[-1:])[0])]
+    tokens.append(out[-1])
+    accepted = []
+    while len(out) < n_new:
+        k = min(K, n_new - len(out) - 1)
+        d = draft(head, b, tokens, p0, k) if k > 0 else []
+        tr = {}
+        base = cache.length
+        g = argmax_lowest(verify_rows(m, cache, out[-1], d, tr))
+        a, bonus = accept(d, g)
+        cache.truncate(base + a + 1)
+        b = np.concatenate([b, tr["hidden"][: a + 1]])
+        out += [int(t) for t in d[:a]] + [bonus]
+        tokens += [int(t) for t in d[:a]] + [bonus]
+        accepted.append(a)
+    return np.array(out[:n_new], np.int32), accepted

@@ -113,3 +113,34 @@ def test_drafting_is_prefix_consistent_and_causal(head):
     U = mtp.grid(head, b, tokens, P0, 1)
     assert d3[0] == int(np.argmax(head.lm_head @ U[0][N - 1]))
     assert all(0 <= t < CFG.vocab for t in d3)
+
+
+def test_speculative_decoding_with_the_head_is_lossless(head):
+    """Driving the verify loop with the head's own drafts reproduces greedy
+    decoding token for token (the losslessness of greedy verification holds
+    for any drafter, so a drafting bug cannot hide behind it -- but a state
+    or cache bookkeeping bug in the loop would break it)."""
+    m = oracle.OracleModel(syn.generate_weights(CFG, 0))
+    wl = syn.WORKLOADS["tiny_fp32_b1"]
+    prompt = syn.make_prompts(wl)[0]
+    ref = oracle.greedy_decode(m, prompt, 24)
+    toks, acc = mtp.spec_decode(m, head, prompt, 24, K)
+    assert np.array_equal(toks, ref)
+    assert all(0 <= a <= K for a in acc)
+
+
+def test_drafts_follow_the_grid_on_teacher_forced_states(head):
+    """After a prefill, the first drafts are exactly mtp.draft on the prompt's
+    final-normed states and its tokens."""
+    m = oracle.OracleModel(syn.generate_weights(CFG, 0))
+    prompt = syn.make_prompts(syn.WORKLOADS["tiny_fp32_b1"])[0]
+    cache = oracle.KVCache(CFG)
+    x = oracle.prompt_embeddings(m, prompt)
+    tr = {}
+    lg = oracle.forward(m, cache, x, np.arange(len(x)), tr)
+    first = int(np.argmax(lg[-1]))
+    tokens = [0] * len(prompt.visual) + [int(t) for t in prompt.tokens] + [first]
+    d = mtp.draft(head, tr["hidden"], tokens, len(prompt.visual) - 1, K)
+    # the hidden rows are the LM head's inputs: they reproduce the logits
+    np.testing.assert_allclose(tr["hidden"] @ m.lm_head.T, lg, rtol=1e-5, atol=1e-5)
+    assert len(d) == K
