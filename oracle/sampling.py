@@ -98,3 +98,27 @@ def rejection_sample(logits: np.ndarray, drafts: Sequence[int], q: Optional[np.n
         trace["accept_margins"] = margins
         trace["sample_margin"] = m
     return K, t
+
+
+def spec_sample_decode(m, prompt, n_new: int, K: int, propose, temperature: float, rng):
+    """Speculative decoding with rejection-sampling verification (the loop of
+    the end-to-end OCR explainer, section 7: draft, verify, append), the
+    target's own first token drawn from its distribution too.
+    ``propose(tokens, k)`` returns (drafts [k], q [k, V] or None); uniforms
+    come from ``rng`` (numpy Generator): per step k acceptance uniforms, then
+    k + 1 sampling uniforms. Returns the generated tokens [n_new]."""
+    from .model import KVCache, forward, prompt_embeddings, verify_rows
+    cache = KVCache(m.cfg)
+    x = prompt_embeddings(m, prompt)
+    lg = forward(m, cache, x, np.arange(len(x)))
+    out = [inverse_cdf(target_probs(lg[-1], temperature), float(rng.random()))[0]]
+    while len(out) < n_new:
+        k = min(K, n_new - len(out) - 1)
+        d, q = propose(list(out), k)
+        base = cache.length
+        logits = verify_rows(m, cache, out[-1], d)
+        ua, us = rng.random(k), rng.random(k + 1)
+        a, t = rejection_sample(logits, d, q, ua, us, temperature)
+        cache.truncate(base + a + 1)
+        out += [int(v) for v in d[:a]] + [int(t)]
+    return np.array(out[:n_new], np.int32)

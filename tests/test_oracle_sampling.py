@@ -103,3 +103,23 @@ def test_q_equal_to_p_accepts_every_draft():
         a, t = smp.rejection_sample(logits, drafts, q, rng.random(K), us, temperature=0.7)
         assert a == K
         assert t == smp.inverse_cdf(smp.target_probs(logits[K], 0.7), us[K])[0]
+
+
+def test_sampling_loop_at_zero_temperature_is_greedy_decoding():
+    """At a temperature far below the logit gaps every p_j is one-hot at the
+    target's argmax, so the stochastic loop commits exactly greedy decoding,
+    whatever the drafts and uniforms."""
+    import synthetic as syn
+    wl = syn.WORKLOADS["tiny_fp32_b1"]
+    m = oracle.OracleModel(syn.generate_weights(wl.model, 0))
+    prompt = syn.make_prompts(wl)[0]
+    ref = oracle.greedy_decode(m, prompt, 20)
+    drng = np.random.default_rng(3)
+
+    def propose(out, k):                    # a certain drafter: right 60% of the time
+        n = len(out)
+        return [int(ref[n + j]) if n + j < len(ref) and drng.random() < 0.6 else int(drng.integers(0, 1024))
+                for j in range(k)], None
+
+    toks = smp.spec_sample_decode(m, prompt, 20, 3, propose, 1e-6, np.random.default_rng(4))
+    assert np.array_equal(toks, ref)
