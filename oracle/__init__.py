@@ -29,6 +29,9 @@ GPU path):
 * Greedy argmax and the acceptance rule break ties toward the lowest index.
 * Acceptance: a = the longest prefix of drafts with d_j = g_(j-1); the bonus
   token g_a is always committed, so a verify step commits a + 1 tokens.
+* The KV cache holds keys and values in the model's activation storage type
+  (bf16 for bf16 and e4m3-weight models, f32 for f32 models), as the model's
+  own state; all arithmetic on them is float32.
 
 ``oracle.sampling`` holds the stochastic counterpart of the acceptance rule
 (rejection-sampling verification), pinned by tests/test_oracle_sampling.py.
@@ -43,9 +46,10 @@ through these checks: the pages print no worked example.
 from .model import (OracleModel, KVCache, rms_norm, rope, attention_rows, moe_ffn,
                     forward, prompt_embeddings, greedy_decode, spec_decode, accept,
                     brute_force_logits, teacher_forced_logits, verify_rows,
-                    decode_bf16, decode_e4m3, decode_e2m1, decode_nvfp4, route, commit_pages)
+                    decode_bf16, decode_e4m3, decode_e2m1, decode_nvfp4, route, commit_pages,
+                    round_bf16)
 
 __all__ = ["OracleModel", "KVCache", "rms_norm", "rope", "attention_rows", "moe_ffn",
            "forward", "prompt_embeddings", "greedy_decode", "spec_decode", "accept",
            "brute_force_logits", "teacher_forced_logits", "verify_rows", "decode_bf16",
-           "decode_e4m3", "decode_e2m1", "decode_nvfp4", "route", "commit_pages"]
+           "decode_e4m3", "decode_e2m1", "decode_nvfp4", "route", "commit_pages", "round_bf16"]

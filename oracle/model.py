@@ -113,15 +113,42 @@ class OracleModel:
                 w_gate=dec("w_gate", l), w_up=dec("w_up", l), w_down=dec("w_down", l)))
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """float32 -> the nearest bfloat16 value (ties to the even 16-bit pattern),
+    returned as float32. A bf16 value is a binary32 whose low 16 bits are zero,
+    so rounding adds half an ulp of the kept part (0x7FFF, plus the kept part's
+    lowest bit for ties) and clears the low half. Finite inputs only."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return b.astype(np.uint32).view(np.float32).reshape(np.shape(x))
+
+
 class KVCache:
     """Contiguous per-layer key/value history (the oracle has no paging: paging
-    only changes addresses, never values)."""
+    only changes addresses, never values).
 
-    def __init__(self, cfg):
+    The cache stores keys and values in the model's activation storage type:
+    float32 for an f32 model, bfloat16 for a bf16 or e4m3-weight model (the
+    KV cache is model state, held in the model's precision like its weights;
+    the arithmetic on the stored values stays float32). ``kv_dtype`` ("f32" or
+    "bf16") overrides that choice."""
+
+    def __init__(self, cfg, kv_dtype: Optional[str] = None):
         self.k = [np.zeros((0, cfg.n_kv_heads, cfg.head_dim), np.float32)
                   for _ in range(cfg.n_layers)]
         self.v = [np.zeros((0, cfg.n_kv_heads, cfg.head_dim), np.float32)
                   for _ in range(cfg.n_layers)]
+        if kv_dtype is None:
+            kv_dtype = "f32" if cfg.wdtype == 0 else "bf16"
+        assert kv_dtype in ("f32", "bf16")
+        self.kv_dtype = kv_dtype
+
+    def append(self, layer: int, k: np.ndarray, v: np.ndarray) -> None:
+        """Store the keys/values of new positions (rounded to the storage type)."""
+        if self.kv_dtype == "bf16":
+            k, v = round_bf16(k), round_bf16(v)
+        self.k[layer] = np.concatenate([self.k[layer], k.astype(np.float32)])
+        self.v[layer] = np.concatenate([self.v[layer], v.astype(np.float32)])
 
     @property
     def length(self) -> int:
@@ -136,6 +163,7 @@ class KVCache:
         c = KVCache.__new__(KVCache)
         c.k = list(self.k)
         c.v = list(self.v)
+        c.kv_dtype = self.kv_dtype
         return c
 
 
@@ -252,8 +280,7 @@ def forward(m: OracleModel, cache: KVCache, x: np.ndarray, positions: np.ndarray
         v = qkv[:, (hq + hk) * d:].reshape(n, hk, d)
         q = rope(q, positions, cfg.rope_theta)
         k = rope(k, positions, cfg.rope_theta)
-        cache.k[l] = np.concatenate([cache.k[l], k])
-        cache.v[l] = np.concatenate([cache.v[l], v])
+        cache.append(l, k, v)
         o = attention_rows(q, cache.k[l], cache.v[l], positions, hk)
         x = x + (o.reshape(n, hq * d) @ L["w_o"].T).astype(np.float32)
         u = rms_norm(x, L["ffn_norm"], cfg.rms_eps)
