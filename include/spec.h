@@ -215,7 +215,9 @@ const char* spec_last_error(void);
  * (the target's token at every verified position: "Jina-OCR-v1", abstract,
  * greedy verification; "End-to-end OCR expert model ...", section 6.1):
  *   out_tokens_dev[t] = argmax_v  sum_k W[v][k] * gamma[k] * x[t][k] / rms(x[t]),
- *   rms(z) = sqrt(mean(z^2) + eps); ties keep the lowest index v.
+ *   rms(z) = sqrt(mean(z^2) + eps); ties keep the lowest index v; a NaN logit
+ *   ranks below every number (a row of NaNs gives 0), so the token is always
+ *   a valid index.
  * x_dev: [T, hidden] f32. w_dev: [vocab, hidden] row-major, w_dtype SPEC_F32 or
  * SPEC_BF16. gamma_dev: [hidden] f32. scratch_dev: caller-owned device memory
  * of at least spec_lmhead_argmax_scratch_bytes(T, vocab) bytes (per-block
@@ -237,10 +239,15 @@ int spec_lmhead_argmax(const float* x_dev, int T, int hidden, int vocab, const v
  * out_dev[n][m] = bf16(silu(A[m]·X[n]) * (A2[m]·X[n])) (bf16 [N, M]) -- the
  * epilogues the expert GEMMs use. The scale pointers may be NULL (1.0). M a
  * multiple of 128, K of 64. err_dev: device int that receives error bits
- * (8 = an mbarrier wait ran out). Enqueued on cuda_stream. */
+ * (8 = an mbarrier wait ran out: every wait ends by a 250 ms deadline, after
+ * which the kernel stops, drains what it has in flight and returns).
+ * flags: 0 normally; SPEC_TC_TEST_STALL makes the kernel issue no loads, so
+ * its waits run out (a check of the deadline: err_dev gets bit 8, out_dev is
+ * not written and the context stays usable). Enqueued on cuda_stream. */
+#define SPEC_TC_TEST_STALL 1
 int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const float* a_scale_dev, const float* a2_scale_dev,
                       int a_fp8, const void* b_dev, const void* b_lo_dev, int M, int N, int K, int dual, int n_tile,
-                      int k_split, void* out_dev, int* err_dev, uintptr_t cuda_stream);
+                      int k_split, int flags, void* out_dev, int* err_dev, uintptr_t cuda_stream);
 
 /* Rejection-sampling verification, the stochastic counterpart of the greedy
  * acceptance rule ("End-to-end OCR expert model architecture and acceleration

@@ -85,8 +85,8 @@ _SIGS = [
                                                   ctypes.c_void_p, ctypes.c_size_t]),
     ("spec_tc_gemm_test", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
-                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
-                                         ctypes.c_void_p, ctypes.c_size_t]),
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]),
     ("spec_rejection_sample", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]),
@@ -306,10 +306,10 @@ def spec_rejection_sample(logits_dev, drafts_dev, q_dev, u_accept_dev, u_sample_
 
 def spec_tc_gemm_test(a_dev, a2_dev, b_dev, b_lo_dev, M: int, N: int, K: int, dual: int, out_dev, err_dev,
                       cuda_stream: int = 0, a_scale_dev=None, a2_scale_dev=None, a_fp8: bool = False,
-                      n_tile: int = 0, k_split: int = 1) -> None:
+                      n_tile: int = 0, k_split: int = 1, flags: int = 0) -> None:
     _check(lib().spec_tc_gemm_test(_ptr(a_dev), _ptr(a2_dev), _ptr(a_scale_dev), _ptr(a2_scale_dev), int(a_fp8),
-                                   _ptr(b_dev), _ptr(b_lo_dev), M, N, K, dual, n_tile, k_split, _ptr(out_dev),
-                                   _ptr(err_dev), cuda_stream))
+                                   _ptr(b_dev), _ptr(b_lo_dev), M, N, K, dual, n_tile, k_split, flags,
+                                   _ptr(out_dev), _ptr(err_dev), cuda_stream))
 
 
 def spec_strerror(code: int) -> str:

@@ -15,6 +15,38 @@ constexpr int WARP = 32;
 // Error bits a kernel may raise (read back by the host after a step).
 enum : int { DERR_PAGE = 1, DERR_TOKEN = 2, DERR_POS = 4, DERR_TIMEOUT = 8 };
 
+// Longest time one wait on an mbarrier may take before the kernel gives up
+// (sets DERR_TIMEOUT, stops issuing work, frees what it holds and returns).
+constexpr unsigned long long WAIT_DEADLINE_NS = 250ull * 1000 * 1000;
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for phase `parity` of the mbarrier at shared address `bar`. Returns
+// false once WAIT_DEADLINE_NS have passed, or as soon as another thread of
+// the grid has raised DERR_TIMEOUT in *err (then every waiter gives up
+// together instead of each spending its own deadline).
+__device__ __forceinline__ bool mbar_wait_deadline(uint32_t bar, uint32_t parity, const int* err) {
+  auto try_once = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+  };
+  for (int i = 0; i < 32; ++i)
+    if (try_once()) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    if (try_once()) return true;
+    if (globaltimer_ns() - t0 > WAIT_DEADLINE_NS) return false;
+    if (err != nullptr && (*reinterpret_cast<const volatile int*>(err) & DERR_TIMEOUT)) return false;
+  }
+}
+
 // ---- storage element types --------------------------------------------------
 struct bf16_t { uint16_t v; };
 struct fp8_t { uint8_t v; };
@@ -100,6 +132,10 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   __syncthreads();
   return t;
 }
+
+// Argmax key of a logit: NaN ranks below every number (like -inf), so every
+// argmax here returns a valid index even for a row of NaNs (then the lowest).
+__device__ __forceinline__ float am_key(float v) { return v == v ? v : -INFINITY; }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 

@@ -399,19 +399,33 @@ template <class WT> struct MmaStep;                   // k values one step cover
 template <> struct MmaStep<bf16_t> { static constexpr int EPL = 8, K = 32; };
 template <> struct MmaStep<fp8_t> { static constexpr int EPL = 16, K = 64; };
 
-// Two MMAs (hi, lo) of one 8-element group: weights wa (row g) / wb (row g+8)
-// as four bf16x2 words, activations x[0..8) of column g at the group's k.
-__device__ __forceinline__ void mma_group8(float (&ch)[4], float (&cl)[4], const uint32_t (&wa)[4],
-                                           const uint32_t (&wb)[4], const float4& x0, const float4& x1) {
-  uint32_t h0, l0, h1, l1;
-  split_bf16x2(x0.x, x0.y, h0, l0);
-  split_bf16x2(x0.z, x0.w, h1, l1);
-  mma16816(ch, wa[0], wb[0], wa[1], wb[1], h0, h1);
-  mma16816(cl, wa[0], wb[0], wa[1], wb[1], l0, l1);
-  split_bf16x2(x1.x, x1.y, h0, l0);
-  split_bf16x2(x1.z, x1.w, h1, l1);
-  mma16816(ch, wa[2], wb[2], wa[3], wb[3], h0, h1);
-  mma16816(cl, wa[2], wb[2], wa[3], wb[3], l0, l1);
+// NP MMAs (activation parts) of one 8-element group: weights wa (row g) / wb
+// (row g+8) as four bf16x2 words, activations x[0..8) of column g at the
+// group's k. NP = 2: hi = bf16(x), lo = bf16(x - hi) (~16 bits); NP = 3 adds
+// lo2 = bf16(x - hi - lo) (the full fp32 significand), for the projection
+// whose outputs are rounded to bf16 for storage (the K/V cache), where a
+// value's rounding must not depend on the split.
+template <int NP>
+__device__ __forceinline__ void mma_group8(float (&c)[NP][4], const uint32_t (&wa)[4], const uint32_t (&wb)[4],
+                                           const float4& x0, const float4& x1) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const float4 v = half ? x1 : x0;
+    float r[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int part = 0; part < NP; ++part) {
+      uint32_t b0, b1;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b0) : "f"(r[1]), "f"(r[0]));
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b1) : "f"(r[3]), "f"(r[2]));
+      mma16816(c[part], wa[2 * half], wb[2 * half], wa[2 * half + 1], wb[2 * half + 1], b0, b1);
+      if (part + 1 < NP) {
+        r[0] -= __uint_as_float(b0 << 16);
+        r[1] -= __uint_as_float(b0 & 0xFFFF0000u);
+        r[2] -= __uint_as_float(b1 << 16);
+        r[3] -= __uint_as_float(b1 & 0xFFFF0000u);
+      }
+    }
+  }
 }
 
 // Block-split units: the 8 warps of a block share one 16-row unit and split
@@ -435,12 +449,16 @@ __device__ __forceinline__ void mma_load_batch(uint4 (&va)[NB], uint4 (&vb)[NB],
 // This warp's partial c[4] of the unit (weight rows g / g + 8 against column
 // x, nullptr = zeros). va/vb hold the warp's first batch on entry
 // (mma_load_batch at s0 = warp).
-template <class WT, int NB>
+template <class WT, int NB, int NP = 2>
 __device__ __forceinline__ void mma_part(uint4 (&va)[NB], uint4 (&vb)[NB], const WT* wlo, const WT* whi, int K,
                                          const float* x, float (&c)[4]) {
   constexpr int SK = MmaStep<WT>::K, EPL = MmaStep<WT>::EPL;
   const int q = threadIdx.x & 3, w = threadIdx.x >> 5, nsteps = K / SK;
-  float ch[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f};
+  float cp[NP][4];
+#pragma unroll
+  for (int part = 0; part < NP; ++part)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cp[part][i] = 0.f;
   for (int s0 = w; s0 < nsteps; s0 += 8 * NB) {
     if (s0 != w) mma_load_batch<WT, NB>(va, vb, wlo, whi, K, s0);
 #pragma unroll
@@ -463,13 +481,18 @@ __device__ __forceinline__ void mma_part(uint4 (&va)[NB], uint4 (&vb)[NB], const
             x0 = *reinterpret_cast<const float4*>(x + k + 8 * h);
             x1 = *reinterpret_cast<const float4*>(x + k + 8 * h + 4);
           }
-          mma_group8(ch, cl, wa, wb, x0, x1);
+          mma_group8<NP>(cp, wa, wb, x0, x1);
         }
       }
     }
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) c[i] = ch[i] + cl[i];
+  for (int i = 0; i < 4; ++i) {
+    float t = cp[0][i];
+#pragma unroll
+    for (int part = 1; part < NP; ++part) t += cp[part][i];
+    c[i] = t;
+  }
 }
 
 // Sum of the 8 warps' c[4] in warp order into warp 0's c (one barrier). red:

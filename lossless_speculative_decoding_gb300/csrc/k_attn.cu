@@ -387,7 +387,6 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
 // computes an item never changes its arithmetic.
 constexpr int ATQ = 32;          // pairs per group at most (four warps)
 constexpr int ATT_NB = 6;        // chunk buffers per block
-constexpr uint32_t ATT_WAIT_LIMIT = 1u << 22;
 
 template <int D_HEAD, int NW, int CG, int NB>
 struct AttWSmem {
@@ -414,16 +413,6 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ bool att_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < ATT_WAIT_LIMIT; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    if (ok) return true;
-  }
-  return false;
 }
 // Barrier of one consumer group (named barrier 1 + cg, NW warps) that also
 // reduces a flag: true when it holds in every thread of the group.
@@ -515,7 +504,7 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
         pcur = pnext;
         pnext = lookup(k + 8);
       }
-      if (k >= NB && !att_wait(bar_of(empty + b), ((k / NB) - 1) & 1)) {
+      if (k >= NB && !mbar_wait_deadline(bar_of(empty + b), ((k / NB) - 1) & 1, S.err)) {
         if (lane == 0) atomicOr(S.err, DERR_TIMEOUT);
         break;
       }
@@ -542,7 +531,7 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
     // the block's shared memory outlives every copy: wait (bounded) for the
     // last phase issued into each buffer (already complete unless aborted)
     if (lane == 0)
-      for (int q = max(0, k - NB); q < k; ++q) att_wait(bar_of(full + q % NB), (q / NB) & 1);
+      for (int q = max(0, k - NB); q < k; ++q) mbar_wait_deadline(bar_of(full + q % NB), (q / NB) & 1, nullptr);
     return;
   }
 
@@ -588,7 +577,7 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
       staged_hk = hk;
     }
     // ---- this item's chunk: wait, zero V rows past the last key, publish in the group ----
-    const bool ok = att_wait(bar_of(full + b), (k / NB) & 1);
+    const bool ok = mbar_wait_deadline(bar_of(full + b), (k / NB) & 1, S.err);
     const uint32_t kb = bufs + b * BUF, vb = kb + HALVES * HB;
     if (ok && nk < ATT_CHUNK) {
       for (int e = wl * 32 + lane; e < (ATT_CHUNK - nk) * HALVES * 8; e += NW * 32) {

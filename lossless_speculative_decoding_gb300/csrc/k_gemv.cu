@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(256) k_lmhead(Dims D, StepBuf B, const WT* __r
     for (int i = 0; i < GEMV_WARPS * 4; ++i) {
       const int vi = blockIdx.x * GEMV_WARPS * 4 + i;
       if (vi >= D.V) break;
-      const float c = cand[tt][i];
+      const float c = am_key(cand[tt][i]);
       if (bi < 0 || c > best) { best = c; bi = vi; }
     }
     B.am_val[(size_t)(t0 + tt) * B.n_vblocks + blockIdx.x] = best;
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(256) k_lmhead(Dims D, StepBuf B, const WT* __r
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     for (int i = lane; i < B.n_vblocks; i += 32) {
-      const float c = __ldcg(B.am_val + base + i);
+      const float c = am_key(__ldcg(B.am_val + base + i));
       const int ci = __ldcg(B.am_idx + base + i);
       if (c > bv || (c == bv && ci < bi)) { bv = c; bi = ci; }
     }
@@ -91,7 +91,7 @@ __global__ void k_argmax_reduce(StepBuf B, int T, int* out) {
   float best = -INFINITY;
   int bi = 0x7fffffff;
   for (int i = threadIdx.x; i < B.n_vblocks; i += blockDim.x) {
-    const float c = B.am_val[(size_t)r * B.n_vblocks + i];
+    const float c = am_key(B.am_val[(size_t)r * B.n_vblocks + i]);
     const int ci = B.am_idx[(size_t)r * B.n_vblocks + i];
     if (c > best || (c == best && ci < bi)) { best = c; bi = ci; }
   }

@@ -470,7 +470,8 @@ __global__ void __launch_bounds__(256, SBPS) k_lmhead_s(Dims D, DevState S, Step
       const float val = reduce_scatter<16>(acc);
       const int vi = u * 4 + r;
       if (logits_dbg != nullptr && !(lane & 1) && t < nvalid) logits_dbg[(size_t)(t0 + t) * D.V + vi] = val;
-      if (val > best) { best = val; bidx = vi; }
+      const float kv = am_key(val);
+      if (kv > best || (kv == best && vi < bidx)) { best = kv; bidx = vi; }
     }
     // combine the four row lanes (r in lane bits 3..4) of each activation row t
 #pragma unroll
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(256, SBPS) k_lmhead_s(Dims D, DevState S, Step
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     for (int i = lane; i < nw; i += 32) {
-      const float c = __ldcg(B.am_val + base + i);
+      const float c = am_key(__ldcg(B.am_val + base + i));
       const int ci = __ldcg(B.am_idx + base + i);
       if (c > bv || (c == bv && ci < bi)) { bv = c; bi = ci; }
     }
@@ -589,7 +590,10 @@ __global__ void __launch_bounds__(256, SBPS) k_qkv_m(Dims D, DevState S, StepBuf
     for (int unit = blockIdx.x; unit < nunits; unit += gridDim.x) {
       const int head = unit / upu, j = (unit % upu) * 8 + g;       // rotary frequency index
       float c[4];
-      mma_part<WT, MNB>(va, vb, wlo, whi, D.h, g < nvalid ? xs + g * (D.h + 4) : nullptr, c);
+      // three activation parts: the K/V outputs are rounded to bf16 for the
+      // cache, and a two-part split would move some of them across a rounding
+      // boundary that the exact product does not cross
+      mma_part<WT, MNB, 3>(va, vb, wlo, whi, D.h, g < nvalid ? xs + g * (D.h + 4) : nullptr, c);
       const int nx = unit + (int)gridDim.x < nunits ? unit + gridDim.x : (pass + 1 < npass ? (int)blockIdx.x : -1);
       if (nx >= 0) {
         set_rows(nx);
@@ -891,8 +895,9 @@ __global__ void __launch_bounds__(256, SBPS) k_lmhead_m(Dims D, DevState S, Step
           logits_dbg[(size_t)(t0 + col) * D.V + r0] = c[e];
           logits_dbg[(size_t)(t0 + col) * D.V + r0 + 8] = c[2 + e];
         }
-        if (c[e] > best[e]) { best[e] = c[e]; bidx[e] = r0; }          // rows in increasing order
-        if (c[2 + e] > best[e]) { best[e] = c[2 + e]; bidx[e] = r0 + 8; }
+        const float k0 = am_key(c[e]), k1 = am_key(c[2 + e]);       // rows in increasing order
+        if (k0 > best[e] || (k0 == best[e] && r0 < bidx[e])) { best[e] = k0; bidx[e] = r0; }
+        if (k1 > best[e] || (k1 == best[e] && r0 + 8 < bidx[e])) { best[e] = k1; bidx[e] = r0 + 8; }
       }
     }
     if (warp == 0) {
@@ -927,7 +932,7 @@ __global__ void __launch_bounds__(256, SBPS) k_lmhead_m(Dims D, DevState S, Step
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     for (int i = lane; i < nc; i += 32) {
-      const float c = __ldcg(B.am_val + base + i);
+      const float c = am_key(__ldcg(B.am_val + base + i));
       const int ci = __ldcg(B.am_idx + base + i);
       if (c > bv || (c == bv && ci < bi)) { bv = c; bi = ci; }
     }

@@ -26,8 +26,10 @@
 // 128-byte-swizzled operand tile and signal the MMA thread, so the tensor
 // cores run the same bf16 MMA while HBM carries one byte per weight.
 //
-// Every wait on an mbarrier is bounded; a timeout sets an error bit, the CTA
-// stops issuing work, frees its TMEM and returns.
+// Every wait on an mbarrier ends by a deadline read from %globaltimer (or as
+// soon as another CTA has reported a timeout); a timeout sets an error bit,
+// the CTA stops issuing work, waits (to the deadline) for the copies and MMAs
+// it has in flight, frees its TMEM and returns.
 #include <cuda_fp8.h>
 #include <algorithm>
 #include <cuda.h>
@@ -35,6 +37,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "spec.h"
 
 namespace spec {
 
@@ -43,7 +46,6 @@ constexpr int TC_BK = 64;             // K elements per atom (128 bytes of bf16,
 constexpr int TC_NSUB = 32;           // activation rows per TMA box
 constexpr int TC_MAXN = 128;          // activation rows per CTA (largest N tile)
 constexpr int TC_ACCW = 2 * TC_MAXN;  // TMEM columns of one accumulator (hi rows, then lo rows)
-constexpr uint32_t TC_WAIT_LIMIT = 1u << 20;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;        // 16 KB
 constexpr int TC_A8_BYTES = TC_BM * TC_BK;           // 8 KB e4m3 staging per weight operand
 
@@ -55,7 +57,7 @@ constexpr int TC_HDR = 1024;          // barriers + TMEM slot, ahead of the stag
 // boxes: weight tile(s), activation hi (+ lo), e4m3 staging (FP8). Every part
 // is a multiple of 1024 bytes, so each stays aligned for the 128-byte swizzle.
 __host__ __device__ constexpr int tc_stage_bytes(int dual, int f8, int nsub, int split, int at) {
-  return at * ((TC_A_BYTES + (f8 ? TC_A8_BYTES : 0)) * (1 + dual) + (split ? 2 : 1) * nsub * TC_NSUB * TC_BK * 2);
+  return at * ((TC_A_BYTES + (f8 ? TC_A8_BYTES : 0)) * (1 + dual) + (1 + split) * nsub * TC_NSUB * TC_BK * 2);
 }
 // Stages that fit: as many weight tiles in flight as shared memory allows.
 __host__ __device__ constexpr int tc_stage_count(int dual, int f8, int nsub, int split, int at) {
@@ -71,17 +73,6 @@ __host__ __device__ constexpr int tc_atoms(int dual, int f8, int nsub, int split
 __host__ __device__ constexpr int tc_threads(int f8) { return f8 ? 256 : 128; }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < TC_WAIT_LIMIT; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    if (ok) return true;
-  }
-  return false;
-}
 
 // Shared-memory matrix descriptor of a K-major bf16 tile stored as 128-byte
 // rows with the 128-byte swizzle (8-row groups 1024 bytes apart). The start
@@ -155,7 +146,8 @@ __device__ __forceinline__ void convert_tile(const unsigned char* stg, unsigned 
 
 template <int DUAL, int F8>
 __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_constant__ CUtensorMap mapB,
-                                                               const __grid_constant__ CUtensorMap mapBlo, TcParams P) {
+                                                               const __grid_constant__ CUtensorMap mapBlo,
+                                                               const __grid_constant__ CUtensorMap mapBlo2, TcParams P) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // header: full[MAXST], empty[MAXST], done, conv[MAXST] (F8: converted tile ready), TMEM slot, abort flag
@@ -179,14 +171,14 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   const int nrows = min(ntile, cnt - n0);
   const int nsub = (nrows + TC_NSUB - 1) / TC_NSUB;
   const int N = nsub * TC_NSUB;                       // activation rows: multiple of 32, <= 128
-  const int NP = (P.split ? 2 : 1) * N;               // MMA N: the hi rows, then the lo rows
+  const int NP = (1 + P.split) * N;                   // MMA N: the hi rows, then the lo (and lo2) rows
   // stage layout, AT K atoms per stage: [A atoms][A2 atoms (DUAL)][B atoms,
   // each hi rows then lo rows][e4m3 staging (F8): A atoms, A2 atoms]. The lo
   // box follows the hi box at N x 128 bytes (a whole number of 8-row swizzle
   // groups), so one MMA with N = NP multiplies the weights into both.
   const int AT = tc_atoms(DUAL, F8, nsub, P.split);
   const int BB = N * TC_BK * 2;                       // one activation part of one atom
-  const int BAT = (P.split ? 2 : 1) * BB;             // one B atom
+  const int BAT = (1 + P.split) * BB;                 // one B atom
   const int SB = tc_stage_bytes(DUAL, F8, nsub, P.split, AT);
   const int STAGES = tc_stage_count(DUAL, F8, nsub, P.split, AT);
   const int BOFF = AT * TC_A_BYTES * (1 + DUAL);
@@ -203,7 +195,7 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   // (hi, kb 1), (lo, kb 0), (lo, kb 1) in that order. Accumulator kb of
   // matrix mat starts at column (mat * NKB + kb) * TC_ACCW.
   constexpr int NKB = DUAL ? 1 : 2;
-  constexpr int NACC = 2 * NKB;
+  constexpr int NACC = 3 * NKB;                       // accumulators read back at most (three parts)
   constexpr uint32_t NCOL = 512;                      // TMEM columns: (1 + DUAL) * NKB * TC_ACCW
 
   // barrier indices: full s, empty TC_MAXST + s, done 2 TC_MAXST, conv 2 TC_MAXST + 1 + s
@@ -228,11 +220,17 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   if (warp == 0 && lane == 0) {
     // ---- TMA producer ----
     constexpr int AST = F8 ? TC_A8_BYTES : TC_A_BYTES;
-    for (int i = 0; i < NST; ++i) {
+    // P.test_stall: issue nothing, so every wait on these copies runs to its
+    // deadline (the check of the bounded waits)
+    for (int i = 0; i < (P.test_stall ? 0 : NST); ++i) {
       const int a0 = i * AT, na = min(AT, KT - a0), s = i % STAGES;
-      if (i >= STAGES && !mbar_wait(smem_u32(bars + TC_MAXST + s), ((i / STAGES) - 1) & 1)) {
+      if (i >= STAGES && !mbar_wait_deadline(smem_u32(bars + TC_MAXST + s), ((i / STAGES) - 1) & 1, P.err)) {
         atomicOr(P.err, DERR_TIMEOUT);
         *abort_flag = 1;
+        // shared memory must outlive the copies already issued: wait (to the
+        // deadline, whatever other CTAs report) for each stage still in flight
+        for (int j = i - STAGES; j < i; ++j)
+          if (j >= 0) mbar_wait_deadline(smem_u32(bars + j % STAGES), (j / STAGES) & 1, nullptr);
         break;
       }
       unsigned char* st = stages + s * SB;
@@ -249,7 +247,9 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
         const int kx = (kt0 + a0 + j) * TC_BK;
         for (int q = 0; q < nsub; ++q) {
           tma_2d(smem_u32(bt + q * TC_NSUB * TC_BK * 2), &mapB, kx, off + n0 + q * TC_NSUB, full);
-          if (P.split) tma_2d(smem_u32(bt + BB + q * TC_NSUB * TC_BK * 2), &mapBlo, kx, off + n0 + q * TC_NSUB, full);
+          if (P.split > 0) tma_2d(smem_u32(bt + BB + q * TC_NSUB * TC_BK * 2), &mapBlo, kx, off + n0 + q * TC_NSUB, full);
+          if (P.split > 1)
+            tma_2d(smem_u32(bt + 2 * BB + q * TC_NSUB * TC_BK * 2), &mapBlo2, kx, off + n0 + q * TC_NSUB, full);
         }
       }
     }
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
     for (int i = 0; i < NST && ok; ++i) {
       const int s = i % STAGES, na = min(AT, KT - i * AT);
       // bf16: the TMA bytes of the stage; F8: the converters' signal (after those bytes)
-      if (!mbar_wait(smem_u32(bars + (F8 ? 2 * TC_MAXST + 1 : 0) + s), (i / STAGES) & 1)) {
+      if (!mbar_wait_deadline(smem_u32(bars + (F8 ? 2 * TC_MAXST + 1 : 0) + s), (i / STAGES) & 1, P.err)) {
         atomicOr(P.err, DERR_TIMEOUT);
         *abort_flag = 1;
         ok = false;
@@ -292,15 +292,16 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                    ::"r"(smem_u32(bars + TC_MAXST + s)) : "memory");
     }
-    if (ok)
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                   ::"r"(smem_u32(bars + 2 * TC_MAXST)) : "memory");
+    // "done" fires once every MMA issued so far has completed -- also after an
+    // abort, so TMEM is never freed under an MMA in flight
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bars + 2 * TC_MAXST)) : "memory");
   } else if (F8 && warp >= 4) {
     // ---- converters: e4m3 staging -> swizzled bf16 operand tile ----
     const int t = threadIdx.x - 128;
     for (int i = 0; i < NST; ++i) {
       const int s = i % STAGES, na = min(AT, KT - i * AT);
-      if (!mbar_wait(smem_u32(bars + s), (i / STAGES) & 1)) {
+      if (!mbar_wait_deadline(smem_u32(bars + s), (i / STAGES) & 1, P.err)) {
         if (lane == 0) atomicOr(P.err, DERR_TIMEOUT);
         break;
       }
@@ -318,7 +319,8 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   __syncwarp();
 
   // ---- epilogue: warp w holds TMEM lanes 32w..32w+31 = weight rows ----
-  const bool have = __syncthreads_and(mbar_wait(smem_u32(bars + 2 * TC_MAXST), 0)) != 0;   // block-uniform
+  const bool done = mbar_wait_deadline(smem_u32(bars + 2 * TC_MAXST), 0, nullptr);
+  const bool have = __syncthreads_and(done && *abort_flag == 0) != 0;   // block-uniform
   if (!have && threadIdx.x == 0) atomicOr(P.err, DERR_TIMEOUT);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const int m = warp * 32 + lane;                     // row within the tile
@@ -332,7 +334,7 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   // v = sum of the used accumulators in order (part 0 kb 0, part 0 kb 1, part 1 ...)
   auto load_acc = [&](int c0, float (&v)[16], float (&u2)[16]) {
     float t[NACC][16], t2[NACC][16];
-    const int nacc = (P.split ? 2 : 1) * NKB;
+    const int nacc = (1 + P.split) * NKB;
 #pragma unroll
     for (int a = 0; a < NACC; ++a) {
       if (a < nacc) {
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
       // per column: max over the tile's 128 rows, lowest row on ties
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        float bv = v[j] * sc;
+        float bv = am_key(v[j] * sc);
         int bi = P.row0 + wrow + m;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -595,8 +597,8 @@ int kv_make_map(CUtensorMap* map, const void* kv, int head_dim, int page_size, i
 // out_bf16[n][m] = silu(A[m]·X[n]) * (A2[m]·X[n]) (dual = 1).
 extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const float* a_scale_dev,
                                  const float* a2_scale_dev, int a_fp8, const void* b_dev, const void* b_lo_dev,
-                                 int M, int N, int K, int dual, int n_tile, int k_split, void* out_dev,
-                                 int* err_dev, uintptr_t cuda_stream) {
+                                 int M, int N, int K, int dual, int n_tile, int k_split, int flags,
+                                 void* out_dev, int* err_dev, uintptr_t cuda_stream) {
   using namespace spec;
   if (!a_dev || !b_dev || !out_dev || !err_dev || (dual && !a2_dev)) return set_last_error(-1, "null pointer");
   if (M < TC_BM || M % TC_BM || K < TC_BK || K % TC_BK || N < 1) return set_last_error(-1, "M, K multiples of 128, 64");
@@ -619,6 +621,7 @@ extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const fl
   if (tc_make_map(&maps.b, b_dev, K, N, TC_NSUB) || (b_lo_dev && tc_make_map(&maps.blo, b_lo_dev, K, N, TC_NSUB)))
     return set_last_error(-6, "tensor map encoding failed");
   if (!b_lo_dev) maps.blo = maps.b;
+  maps.blo2 = maps.blo;
   // the weights in the tiled layout, in stream-ordered scratch
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
   const size_t wbytes = (size_t)M * K * (a_fp8 ? 1 : 2);
@@ -639,6 +642,7 @@ extern "C" int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const fl
   P.split = b_lo_dev != nullptr;
   P.ntile = n_tile;
   P.ksplit = k_split;
+  P.test_stall = (flags & SPEC_TC_TEST_STALL) ? 1 : 0;
   const int n_tiles = (N + n_tile - 1) / n_tile;
   float* part = nullptr;
   int* cnt = nullptr;
@@ -677,11 +681,11 @@ void launch_tc_gemm(const TcMaps& maps, const TcParams& P, int m_tiles, int grou
   TcParams Q = P;
   if (Q.ntile == 0) Q.ntile = TC_MAXN;
   if (maps.f8) {
-    if (maps.dual) k_tc_gemm<1, 1><<<grid, tc_threads(1), TC_SMEM, st>>>(maps.b, maps.blo, Q);
-    else k_tc_gemm<0, 1><<<grid, tc_threads(1), TC_SMEM, st>>>(maps.b, maps.blo, Q);
+    if (maps.dual) k_tc_gemm<1, 1><<<grid, tc_threads(1), TC_SMEM, st>>>(maps.b, maps.blo, maps.blo2, Q);
+    else k_tc_gemm<0, 1><<<grid, tc_threads(1), TC_SMEM, st>>>(maps.b, maps.blo, maps.blo2, Q);
   } else {
-    if (maps.dual) k_tc_gemm<1, 0><<<grid, tc_threads(0), TC_SMEM, st>>>(maps.b, maps.blo, Q);
-    else k_tc_gemm<0, 0><<<grid, tc_threads(0), TC_SMEM, st>>>(maps.b, maps.blo, Q);
+    if (maps.dual) k_tc_gemm<1, 0><<<grid, tc_threads(0), TC_SMEM, st>>>(maps.b, maps.blo, maps.blo2, Q);
+    else k_tc_gemm<0, 0><<<grid, tc_threads(0), TC_SMEM, st>>>(maps.b, maps.blo, maps.blo2, Q);
   }
 }
 

@@ -8,11 +8,11 @@
 
 namespace spec {
 
-// v = (x[t][k] * inv_t) * gamma[k] as hi = bf16(v), lo = bf16(v - hi); one
-// block per row. The inverse RMS uses row_inv_rms, the arithmetic of every
-// other RMSNorm here.
+// v = (x[t][k] * inv_t) * gamma[k] as hi = bf16(v), lo = bf16(v - hi) and,
+// when out_lo2 is given, lo2 = bf16(v - hi - lo); one block per row. The
+// inverse RMS uses row_inv_rms, the arithmetic of every other RMSNorm here.
 __global__ void k_norm_bf16(Dims D, const float* __restrict__ x, const float* __restrict__ gamma,
-                            uint16_t* __restrict__ out, uint16_t* __restrict__ out_lo) {
+                            uint16_t* __restrict__ out, uint16_t* __restrict__ out_lo, uint16_t* __restrict__ out_lo2) {
   __shared__ float inv[1];
   pdl_wait();
   pdl_trigger();
@@ -24,8 +24,11 @@ __global__ void k_norm_bf16(Dims D, const float* __restrict__ x, const float* __
   for (int k = threadIdx.x; k < D.h; k += blockDim.x) {
     const float v = (xr[k] * s) * gamma[k];
     const uint16_t hi = f_to_bf16(v);
+    const float r = v - bf16_to_f(hi);
+    const uint16_t lo = f_to_bf16(r);
     out[(size_t)t * D.h + k] = hi;
-    out_lo[(size_t)t * D.h + k] = f_to_bf16(v - bf16_to_f(hi));
+    out_lo[(size_t)t * D.h + k] = lo;
+    if (out_lo2) out_lo2[(size_t)t * D.h + k] = f_to_bf16(r - bf16_to_f(lo));
   }
 }
 
@@ -103,7 +106,7 @@ __global__ void k_argmax_commit(Dims D, DevState S, StepBuf B, int T, int ld, in
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     for (int i = lane; i < ld; i += 32) {
-      const float c = B.am_val[(size_t)row * ld + i];
+      const float c = am_key(B.am_val[(size_t)row * ld + i]);
       const int ci = B.am_idx[(size_t)row * ld + i];
       if (c > bv || (c == bv && ci < bi)) { bv = c; bi = ci; }
     }
@@ -120,9 +123,9 @@ __global__ void k_argmax_commit(Dims D, DevState S, StepBuf B, int T, int ld, in
   for (int s = threadIdx.x; s < n_seq; s += blockDim.x) commit_seq(D, S, B, s, K, B.g);
 }
 
-void launch_norm_bf16(const Dims& D, const float* x, const float* gamma, uint16_t* out, uint16_t* out_lo, int T,
-                      cudaStream_t st) {
-  launch_k(k_norm_bf16, dim3(T), dim3(256), 0, st, D, x, gamma, out, out_lo);
+void launch_norm_bf16(const Dims& D, const float* x, const float* gamma, uint16_t* out, uint16_t* out_lo,
+                      uint16_t* out_lo2, int T, cudaStream_t st) {
+  launch_k(k_norm_bf16, dim3(T), dim3(256), 0, st, D, x, gamma, out, out_lo, out_lo2);
 }
 
 void launch_rope_kv(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, cudaStream_t st) {

@@ -76,6 +76,7 @@ struct StepBuf {
   // each bf16 operand X is stored as hi = bf16(X) and lo = bf16(X - hi)
   uint16_t* xn_bf16;      // [T, h] RMS-normalised rows
   uint16_t* xn_lo;
+  uint16_t* xn_lo2;       // third part bf16(X - hi - lo) (QKV input: outputs rounded for the KV cache)
   uint16_t* o_bf16;       // [T, Hq d] attention output
   uint16_t* o_lo;
   uint16_t* xperm;        // [T*NS, h] FFN input rows in expert-permuted order
@@ -142,7 +143,7 @@ struct TcParams {
   float* out_f32;         // STORE [off+n][col] / ADD (+=) / SCATTER [perm[off+n]][col]
   uint16_t* out_bf16;     // SWIGLU [off+n][col] (hi part)
   uint16_t* out_bf16_lo;  // SWIGLU low part (value - hi), nullable
-  int split;              // activations given as hi + lo operands
+  int split;              // extra activation parts: 0 (one bf16 operand), 1 (hi + lo), 2 (hi + lo + lo2)
   int ntile;              // activation rows per CTA: 32, 64 or 128 (0: 128)
   int ksplit;             // K splits (grid z = groups x ksplit); > 1: partials in `part`, summed by the last split
   float* part;            // [ksplit][1 + dual][part_n][part_m] fp32 partials
@@ -155,10 +156,11 @@ struct TcParams {
   int* am_idx;
   int am_ld;
   int* err;
+  int test_stall;         // test only: the producer issues no copies, so every wait times out
 };
 
 struct TcMaps {
-  CUtensorMap b, blo;          // activations hi, lo
+  CUtensorMap b, blo, blo2;    // activation parts hi, lo, lo2
   int dual;
   int f8 = 0;                  // weights are e4m3
 };
@@ -176,8 +178,9 @@ int kv_make_map(CUtensorMap* map, const void* kv, int head_dim, int page_size, i
 int tc_pack_weights(void* dst, const void* src, int rows, int K, int f8, cudaStream_t st);
 void launch_tc_gemm(const TcMaps& maps, const TcParams& P, int m_tiles, int groups, int n_tiles, cudaStream_t st);
 cudaError_t configure_tc_kernels();
-void launch_norm_bf16(const Dims& D, const float* x, const float* gamma, uint16_t* out, uint16_t* out_lo, int T,
-                      cudaStream_t st);
+// out_lo2 (nullable): the third part bf16(v - hi - lo).
+void launch_norm_bf16(const Dims& D, const float* x, const float* gamma, uint16_t* out, uint16_t* out_lo,
+                      uint16_t* out_lo2, int T, cudaStream_t st);
 void launch_rope_kv(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, cudaStream_t st);
 void launch_gather_bf16(const Dims& D, const StepBuf& B, int T, cudaStream_t st);
 void launch_argmax_commit(const Dims& D, const DevState& S, const StepBuf& B, int T, int ld, bool commit, int n_seq,

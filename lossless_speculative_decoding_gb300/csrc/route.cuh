@@ -28,7 +28,10 @@ __device__ __forceinline__ void router_topk(const float* logit, int E, int k, in
   }
   z = warp_sum(z);
 #pragma unroll
-  for (int i = 0; i < MAXE; ++i) v[i] = (lane + 32 * i < E) ? v[i] / z : -1.f;
+  for (int i = 0; i < MAXE; ++i) {
+    const float p = v[i] / z;                     // a NaN probability ranks as 0, so ids stay < E
+    v[i] = (lane + 32 * i < E) ? (p == p ? p : 0.f) : -1.f;
+  }
   for (int r = 0; r < k; ++r) {
     float bv = -1.f;
     int bi = 0x7fffffff;

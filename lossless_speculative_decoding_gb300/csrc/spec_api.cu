@@ -126,8 +126,12 @@ static int tc_ksplit(int n_sm, int m_tiles, int groups, int n_tiles, int KT) {
   return (KT + kts - 1) / kts;
 }
 
-// activation rows per CTA of a dense tensor-core launch (see tc_dense)
-static int tc_dense_ntile(int n_sm, int M, int T) { return (M / 128) * ((T + 127) / 128) < n_sm ? 32 : 128; }
+// activation rows per CTA of a dense tensor-core launch (see tc_dense); with
+// three activation parts the MMA's N (3 x rows) stays within 256
+static int tc_dense_ntile(int n_sm, int M, int T, bool three_parts = false) {
+  const int nt = (M / 128) * ((T + 127) / 128) < n_sm ? 32 : 128;
+  return three_parts && nt > 64 ? 64 : nt;
+}
 
 struct spec_model {
   spec_config cfg{};
@@ -166,6 +170,7 @@ struct spec_model {
   CUtensorMap kv_map{};                                        // paged KV pool (tensor-core attention)
   CUtensorMap tc_xn, tc_o, tc_xperm, tc_hperm;                 // activations: hi
   CUtensorMap tc_xn_lo, tc_o_lo, tc_xperm_lo, tc_hperm_lo;     //              lo
+  CUtensorMap tc_xn_lo2;                                       //              lo2 (QKV input)
 
   ~spec_model() {
     for (auto& g : graphs) cudaGraphExecDestroy(g.second);
@@ -239,20 +244,21 @@ struct spec_model {
 
   // Tensor-core GEMM launches. Dense: one group covering T rows. Grouped: the
   // active-expert list of the step (rows of the permuted operand).
+  // blo2: a third activation part (the QKV input), else two parts
   void tc_dense(const void* w, const CUtensorMap& b, const CUtensorMap& blo, int K, int M, int T, int epi,
-                float* out, int ldo, const float* scale = nullptr) {
+                float* out, int ldo, const float* scale = nullptr, const CUtensorMap* blo2 = nullptr) {
     TcMaps mp;
-    mp.b = b; mp.blo = blo; mp.dual = 0; mp.f8 = scale != nullptr;
+    mp.b = b; mp.blo = blo; mp.blo2 = blo2 ? *blo2 : blo; mp.dual = 0; mp.f8 = scale != nullptr;
     TcParams P = {};
     P.wa = w; P.wa2 = w;
-    P.K = K; P.Mg = M; P.N = T; P.ldo = ldo; P.epi = epi; P.out_f32 = out; P.err = S.err; P.split = 1;
+    P.K = K; P.Mg = M; P.N = T; P.ldo = ldo; P.epi = epi; P.out_f32 = out; P.err = S.err; P.split = blo2 ? 2 : 1;
     P.scale = scale;
     if (epi == TC_ARGMAX) { P.am_val = B.am_val; P.am_idx = B.am_idx; P.am_ld = M / 128; }
     // too few CTAs for the GPU with 128-row activation tiles (small projections
     // at moderate T): 32-row tiles quadruple them; the weight tile is then read
     // by CTAs that run side by side (N tiles vary fastest) and hits in L2
-    P.ntile = tc_dense_ntile(D.n_sm, M, T);
-    const int tv = Tv, ntv = tc_dense_ntile(D.n_sm, M, tv);
+    P.ntile = tc_dense_ntile(D.n_sm, M, T, blo2 != nullptr);
+    const int tv = Tv, ntv = tc_dense_ntile(D.n_sm, M, tv, blo2 != nullptr);
     P.ksplit = tc_ksplit(D.n_sm, M / 128, 1, (tv + ntv - 1) / ntv, K / 64);
     P.part = tc_part; P.part_n = T; P.part_m = M; P.tile_cnt = tc_cnt;
     launch_tc_gemm(mp, P, M / 128, P.ksplit, (T + P.ntile - 1) / P.ntile, stream);
@@ -261,7 +267,7 @@ struct spec_model {
                   int epi, float* out_f32, uint16_t* out_bf16, uint16_t* out_lo, int ldo,
                   const float* scale = nullptr, const float* scale2 = nullptr) {
     TcMaps mp;
-    mp.b = b; mp.blo = blo; mp.dual = w2 ? 1 : 0; mp.f8 = scale != nullptr;
+    mp.b = b; mp.blo = blo; mp.blo2 = blo; mp.dual = w2 ? 1 : 0; mp.f8 = scale != nullptr;
     TcParams P = {};
     P.wa = w; P.wa2 = w2 ? w2 : w;
     P.K = K; P.Mg = Mg; P.N = T; P.ldo = ldo; P.epi = epi; P.out_f32 = out_f32; P.out_bf16 = out_bf16;
@@ -284,8 +290,8 @@ struct spec_model {
       const LayerW& W = layers[l];
       if (use_tc) {
         run_k(p, KC_QKV, [&] {
-          launch_norm_bf16(D, cur, W.attn_norm, B.xn_bf16, B.xn_lo, T, stream);
-          tc_dense(W.w_qkv, tc_xn, tc_xn_lo, D.h, qkv_rows, T, TC_STORE, B.qkv, qkv_rows, W.s_qkv);
+          launch_norm_bf16(D, cur, W.attn_norm, B.xn_bf16, B.xn_lo, B.xn_lo2, T, stream);
+          tc_dense(W.w_qkv, tc_xn, tc_xn_lo, D.h, qkv_rows, T, TC_STORE, B.qkv, qkv_rows, W.s_qkv, &tc_xn_lo2);
           launch_rope_kv(D, S, B, l, T, stream);
         });
         run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, kv_map, stream); });
@@ -324,7 +330,7 @@ struct spec_model {
       launch_lmhead_step(D, S, B, lm_head, final_norm, x, T, logits_dbg, commit, n_seq, K, stream);
       return;
     }
-    launch_norm_bf16(D, x, final_norm, B.xn_bf16, B.xn_lo, T, stream);
+    launch_norm_bf16(D, x, final_norm, B.xn_bf16, B.xn_lo, nullptr, T, stream);
     if (logits_dbg) tc_dense(lm_head, tc_xn, tc_xn_lo, D.h, D.V, T, TC_STORE, logits_dbg, D.V);
     tc_dense(lm_head, tc_xn, tc_xn_lo, D.h, D.V, T, TC_ARGMAX, nullptr, 0);
     launch_argmax_commit(D, S, B, T, D.V / 128, commit, n_seq, K, stream);
@@ -522,7 +528,8 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
   if (m->use_tc) {
     const int qkv_rows = (D.Hq + 2 * D.Hkv) * D.d;
     if ((rc = m->dalloc(&B.qkv, (size_t)T * qkv_rows)) || (rc = m->dalloc(&B.xn_bf16, (size_t)T * D.h)) ||
-        (rc = m->dalloc(&B.xn_lo, (size_t)T * D.h)) || (rc = m->dalloc(&B.o_bf16, (size_t)T * D.Hq * D.d)) ||
+        (rc = m->dalloc(&B.xn_lo, (size_t)T * D.h)) || (rc = m->dalloc(&B.xn_lo2, (size_t)T * D.h)) ||
+        (rc = m->dalloc(&B.o_bf16, (size_t)T * D.Hq * D.d)) ||
         (rc = m->dalloc(&B.o_lo, (size_t)T * D.Hq * D.d)) || (rc = m->dalloc(&B.xperm, (size_t)T * NS * D.h)) ||
         (rc = m->dalloc(&B.xperm_lo, (size_t)T * NS * D.h)) || (rc = m->dalloc(&B.hperm, (size_t)T * NS * D.inter)) ||
         (rc = m->dalloc(&B.hperm_lo, (size_t)T * NS * D.inter)))
@@ -562,6 +569,7 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
     bad |= tc_make_map(&m->tc_xperm, B.xperm, D.h, (uint64_t)T * NS, 32);
     bad |= tc_make_map(&m->tc_hperm, B.hperm, D.inter, (uint64_t)T * NS, 32);
     bad |= tc_make_map(&m->tc_xn_lo, B.xn_lo, D.h, T, 32);
+    bad |= tc_make_map(&m->tc_xn_lo2, B.xn_lo2, D.h, T, 32);
     bad |= tc_make_map(&m->tc_o_lo, B.o_lo, (uint64_t)D.Hq * D.d, T, 32);
     bad |= tc_make_map(&m->tc_xperm_lo, B.xperm_lo, D.h, (uint64_t)T * NS, 32);
     bad |= tc_make_map(&m->tc_hperm_lo, B.hperm_lo, D.inter, (uint64_t)T * NS, 32);
@@ -569,8 +577,11 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
     // split-K scratch: the largest [splits][1 + dual][rows][features] of the step's launches
     {
       const int tv = m->Tv;
-      auto dn = [&](int M) { const int nt = tc_dense_ntile(D.n_sm, M, tv); return (tv + nt - 1) / nt; };
-      const int ks_q = tc_ksplit(D.n_sm, qkv_rows / 128, 1, dn(qkv_rows), D.h / 64);
+      auto dn = [&](int M, bool three = false) {
+        const int nt = tc_dense_ntile(D.n_sm, M, tv, three);
+        return (tv + nt - 1) / nt;
+      };
+      const int ks_q = tc_ksplit(D.n_sm, qkv_rows / 128, 1, dn(qkv_rows, true), D.h / 64);
       const int ks_o = tc_ksplit(D.n_sm, D.h / 128, 1, dn(D.h), D.Hq * D.d / 64);
       const int ks_l = tc_ksplit(D.n_sm, D.V / 128, 1, dn(D.V), D.h / 64);
       const int gmin = (D.E > 0 ? 1 : 0) + D.S;        // fewest groups an expert launch can have
