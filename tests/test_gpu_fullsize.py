@@ -1,26 +1,32 @@
 """Parity at full model sizes, in the launch configurations bench.py times.
 
-The oracle computes sampled verify rows of the full 3B-MoE (bf16 and e4m3)
-and dense 4B shapes one step at a time, teacher-forced on the GPU's own
-committed sequence: every row's logits must sit within 2e-2 of the oracle
-row's range, every GPU argmax must equal the oracle's outside near-ties
-(top-1 - top-2 < 1e-3), and the accepted length and bonus must be those the
-acceptance rule gives for the GPU argmaxes.
+The oracle scores sampled verify steps of the full 3B-MoE (bf16 and e4m3) and
+dense 4B shapes, teacher-forced on the GPU's own committed sequences. The
+bar, per scored row:
 
-Expert routing is a discrete choice: where the oracle's k-th and (k+1)-th
-router logits of a row come within ROUTE_TIE of each other at some layer,
-the GPU (whose activations differ from the oracle's by rounding) may pick the
-other expert, and the row's logits then move by more than the tolerance.
-Such rows are exempt from the two row checks, counted, and must stay a
-minority (at most a quarter of the rows).
+* logits within 2e-2 of the oracle row's range (max |GPU - oracle|);
+* the GPU argmax equals the oracle's, except where the oracle's top-1 - top-2
+  margin is below 1e-3 (a near-tie; such rows are counted);
+* the accepted length and bonus token are exactly what the acceptance rule
+  gives for the GPU argmaxes.
 
-Tokens: bf16 KV and activation rounding move a row's logits by up to the 2e-2
-row tolerance, which at these vocabulary sizes is often more than the
-oracle's top-1 - top-2 margin. A token mismatch therefore also passes where
-that margin is below twice the row's largest |GPU - oracle| logit difference
-(the flip is explained by an error the row check already bounds); these are
-counted against the same quarter.
+The one other counted class is a router near-tie. Expert choice is discrete:
+where the oracle's k-th and (k+1)-th router logits of a row come within
+ROUTE_TIE of each other at some layer, the GPU (whose activations differ from
+the oracle's by float32 rounding, plus the odd bf16 rounding of a stored
+key/value that lands on the other side of a rounding boundary) may take the
+other expert, which moves the row by more than the tolerance. Only a row that
+misses the logit bar AND is such a near-tie is exempt from the row checks; it
+is counted, and such rows must stay rare (at most MAX_ROUTE_EXEMPT of the
+rows). ROUTE_TIE is twice the largest logit error measured on rows whose
+routing cannot flip.
+
+The counts of every run are printed and, when SPEC_PARITY_LOG names a file,
+appended to it as one JSON line per workload.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 
@@ -30,89 +36,153 @@ from _util import gpu_model, margin_exempt, row_tol_ok
 
 pytestmark = pytest.mark.gpu
 
-
 ROUTE_TIE = 4e-3
+MAX_ROUTE_EXEMPT = 1 / 8
 
 
-def _check_rows(lg, ol, route_gap, rel=2e-2):
-    """Returns the number of rows that needed an exemption."""
-    tie = route_gap < ROUTE_TIE if route_gap is not None else np.zeros(len(lg), bool)
-    ok = row_tol_ok(lg, ol, rel)
-    assert (ok | tie).all(), f"logits outside 2e-2 of the row range (rows {np.nonzero(~ok)[0].tolist()})"
-    g_gpu, g_or = np.argmax(lg, -1), np.argmax(ol, -1)
+class Counts:
+    def __init__(self, name):
+        self.name = name
+        self.rows = self.route_exempt = self.margin_exempt = 0
+        self.max_abs = self.max_rel = 0.0          # over rows that are not route-exempt
+
+    def report(self):
+        d = {"workload": self.name, "rows": self.rows, "margin_exempt_tokens": self.margin_exempt,
+             "route_tie_rows": self.route_exempt, "max_abs": self.max_abs, "max_rel_of_range": self.max_rel}
+        print("parity counts:", json.dumps(d))
+        path = os.environ.get("SPEC_PARITY_LOG")
+        if path:
+            with open(path, "a") as f:
+                f.write(json.dumps(d) + "\n")
+        return d
+
+
+def _check_rows(lg, ol, route_gap, c: Counts):
+    n = len(lg)
+    tie = route_gap < ROUTE_TIE if route_gap is not None else np.zeros(n, bool)
+    ok = row_tol_ok(lg, ol, 2e-2)
+    bad = np.nonzero(~ok & ~tie)[0]
+    assert len(bad) == 0, f"logits outside 2e-2 of the row range at rows {bad.tolist()}"
+    exempt = ~ok & tie
+    c.rows += n
+    c.route_exempt += int(exempt.sum())
     err = np.abs(lg - ol).max(-1)
-    flipped = np.zeros(len(lg), bool)
+    rng = ol.max(-1) - ol.min(-1)
+    keep = ~exempt
+    if keep.any():
+        c.max_abs = max(c.max_abs, float(err[keep].max()))
+        c.max_rel = max(c.max_rel, float((err[keep] / rng[keep]).max()))
+    g_gpu, g_or = np.argmax(lg, -1), np.argmax(ol, -1)
     for i in np.nonzero(g_gpu != g_or)[0]:
+        if exempt[i]:
+            continue
         s = np.sort(ol[i])
-        margin = float(s[-1] - s[-2])
-        assert margin_exempt(ol[i]) or tie[i] or margin < 2 * err[i], \
-            f"token mismatch at row {i}: oracle margin {margin:.4g} >= 2 x row error {err[i]:.4g}"
-        flipped[i] = True
-    return int(((~ok) & tie).sum() + flipped.sum())
+        assert margin_exempt(ol[i]), \
+            f"token mismatch at row {i}: oracle top-1 - top-2 = {s[-1] - s[-2]:.4g} >= 1e-3"
+        c.margin_exempt += 1
 
 
-def _run(wl_name, n_seq, max_batch, steps, seed_drafts):
+def _prefix_prompts(wl, n_seq, step):
+    """n_seq prompts that are prefixes of one prompt (the longest first), so
+    one oracle prefill serves every sequence: sequence i keeps the first
+    length - i * step rows. Only for prompts of visual rows alone."""
+    p = syn.make_prompts(wl, n_seq=1)[0]
+    assert len(p.tokens) == 0 and len(p.prefix_tokens) == 0
+    import dataclasses
+    return [dataclasses.replace(p, visual=p.visual[:len(p.visual) - i * step]) for i in range(n_seq)]
+
+
+def _run(wl_name, n_seq, n_check, max_batch, steps, seed_drafts, prefix_step=0):
+    """Prefill n_seq sequences on a model sized for max_batch, run `steps`
+    verify steps over all of them in one batch, and score the first n_check
+    sequences' rows with the oracle."""
     wl = syn.WORKLOADS[wl_name]
     cfg = wl.model
     K = wl.n_draft
     w = syn.generate_weights(cfg, 0)
     om = oracle.OracleModel(w)
-    prompts = syn.make_prompts(wl, n_seq=n_seq)
+    prompts = _prefix_prompts(wl, n_seq, prefix_step) if prefix_step else syn.make_prompts(wl, n_seq=n_seq)
     max_ctx = max(p.length for p in prompts) + steps * (K + 1) + 2 * (K + 1)
     pages = sum(-(-max_ctx // wl.page_size) for _ in prompts) + 16
     gm = gpu_model(cfg, w, page_size=wl.page_size, n_pages=pages, max_seqs=max(n_seq, max_batch), max_ctx=max_ctx,
                    max_draft=K, max_batch=max_batch)
+    counts = Counts(wl_name)
     try:
         prefix = gm.register_prefix(prompts[0].prefix_tokens) if len(prompts[0].prefix_tokens) else -1
-        caches, last = [], []
-        for i, p in enumerate(prompts):
-            first = gm.prefill(i, p.visual, p.tokens, prefix)
-            cache = oracle.KVCache(cfg)
-            lg0 = oracle.forward(om, cache, oracle.prompt_embeddings(om, p), np.arange(p.length))[-1]
-            assert first == int(np.argmax(lg0)) or margin_exempt(lg0)
+        last = [gm.prefill(i, p.visual, p.tokens, prefix) for i, p in enumerate(prompts)]
+        caches = []
+        if prefix_step:
+            full = oracle.KVCache(cfg)
+            x = oracle.prompt_embeddings(om, prompts[0])
+            lg_full = oracle.forward(om, full, x, np.arange(len(x)))
+        for i in range(n_check):
+            p = prompts[i]
+            if prefix_step:
+                cache = full.copy()
+                cache.truncate(p.length)                     # causal: a prefix's KV ignores what follows
+                lg0 = lg_full[p.length - 1]
+            else:
+                cache = oracle.KVCache(cfg)
+                lg0 = oracle.forward(om, cache, oracle.prompt_embeddings(om, p), np.arange(p.length))[-1]
+            assert last[i] == int(np.argmax(lg0)) or margin_exempt(lg0)
             caches.append(cache)
-            last.append(first)
         rng = np.random.default_rng(seed_drafts)
-        exempt = rows = 0
+        ids = list(range(n_seq))
         for step in range(steps):
             d = rng.integers(0, cfg.vocab, (n_seq, K)).astype(np.int32)
-            # the first draft is the GPU's own next token (row 0 does not depend on
-            # the drafts), so every step accepts at least one draft
-            pre = gm.debug_logits(list(range(n_seq)), d).reshape(n_seq, K + 1, cfg.vocab)
+            # the first draft is the GPU's own next token (row 0 does not depend
+            # on the drafts), so every step accepts at least one draft
+            pre = gm.debug_logits(ids, d).reshape(n_seq, K + 1, cfg.vocab)
             d[:, 0] = np.argmax(pre[:, 0], -1)
-            lg = gm.debug_logits(list(range(n_seq)), d).reshape(n_seq, K + 1, cfg.vocab)
-            for i in range(n_seq):
+            lg = gm.debug_logits(ids, d).reshape(n_seq, K + 1, cfg.vocab)
+            assert np.array_equal(lg[:, 0], pre[:, 0])       # row 0 ignores the drafts, bit for bit
+            for i in range(n_check):
                 tr = {}
                 ol = oracle.verify_rows(om, caches[i], last[i], d[i], tr)
-                exempt += _check_rows(lg[i], ol, tr.get("route_gap"))
-                rows += K + 1
-            a, b = gm.verify_batch(list(range(n_seq)), d, [K] * n_seq)
+                _check_rows(lg[i], ol, tr.get("route_gap"), counts)
+            a, b = gm.verify_batch(ids, d, [K] * n_seq)
             for i in range(n_seq):
-                exp = oracle.accept(list(d[i]), np.argmax(lg[i], -1))
-                assert (int(a[i]), int(b[i])) == exp
+                assert (int(a[i]), int(b[i])) == oracle.accept(list(d[i]), np.argmax(lg[i], -1))
                 assert int(a[i]) >= 1
-                caches[i].truncate(caches[i].length - (K + 1) + int(a[i]) + 1)
+                if i < n_check:
+                    caches[i].truncate(caches[i].length - (K + 1) + int(a[i]) + 1)
                 last[i] = int(b[i])
-        assert exempt * 4 <= rows, f"{exempt} of {rows} rows needed a near-tie exemption"
     finally:
         gm.close()
+    counts.report()
+    assert counts.route_exempt <= MAX_ROUTE_EXEMPT * counts.rows, \
+        f"{counts.route_exempt} of {counts.rows} rows needed the router near-tie exemption"
 
 
 def test_fullsize_moe3b_bf16_b1():
     """3B-MoE bf16, 12 layers, V = 129,280, one sequence, 4 rows per step:
     the warp tensor-core GEMV path the batch-1 benchmark times."""
-    _run("moe3b_bf16_b1", n_seq=1, max_batch=1, steps=3, seed_drafts=5)
+    _run("moe3b_bf16_b1", n_seq=1, n_check=1, max_batch=1, steps=8, seed_drafts=5)
 
 
-def test_fullsize_moe3b_fp8_tensor_core():
-    """3B-MoE with e4m3 weights and a shared 64-token prefix, model sized for
-    64 sequences (the tcgen05 path the concurrency-64 benchmark times); two
-    sequences are scored (a row's arithmetic does not depend on the batch)."""
-    _run("moe3b_fp8_c64", n_seq=2, max_batch=64, steps=2, seed_drafts=6)
+def test_fullsize_moe3b_bf16_c32():
+    """3B-MoE bf16 at concurrency 32: 32 sequences of 256 + 100 n visual rows
+    per step on the grouped tcgen05 GEMMs and the tensor-core attention; the
+    oracle scores 8 of them over 4 steps."""
+    _run("moe3b_bf16_c32", n_seq=32, n_check=8, max_batch=32, steps=4, seed_drafts=8)
 
 
-def test_fullsize_dense4b_block_draft():
+def test_fullsize_moe3b_fp8_c64():
+    """3B-MoE with e4m3 weights and a shared 64-token prefix at concurrency 64
+    (the headline benchmark's launch configuration); the oracle scores 4 of
+    the 64 sequences over 4 steps."""
+    _run("moe3b_fp8_c64", n_seq=64, n_check=4, max_batch=64, steps=4, seed_drafts=6)
+
+
+def test_fullsize_dense4b_block_draft_b1():
     """Dense 4B shape (36 layers, GQA 32/8, inter 9,728, V = 151,936) with one
     31-token block draft per step: the tcgen05 GEMMs and the tensor-core
-    attention."""
-    _run("dense4b_bf16_b1", n_seq=1, max_batch=1, steps=1, seed_drafts=7)
+    attention, 32 rows per step."""
+    _run("dense4b_bf16_b1", n_seq=1, n_check=1, max_batch=1, steps=2, seed_drafts=7)
+
+
+def test_fullsize_dense4b_block_draft_b8():
+    """The same dense 4B shape at batch 8 (256 rows, 1,024 (row, q head) pairs
+    per layer): eight prefixes of one 1,288-row visual prompt, 1,288 down to
+    1,029 rows, all scored by the oracle from one prefill."""
+    _run("dense4b_bf16_b8", n_seq=8, n_check=8, max_batch=8, steps=1, seed_drafts=9, prefix_step=37)

@@ -62,3 +62,33 @@ def test_lmhead_argmax_ties_lowest_index():
     with pytest.raises(B.SpecError):
         B.spec_lmhead_argmax(torch.from_numpy(x).cuda(), T, h, V, torch.from_numpy(w).cuda(), syn.F32,
                              torch.ones(h, device="cuda"), 1e-6, scratch, nbytes - 8, out, 0)
+
+
+def test_lmhead_argmax_nan_rows_give_valid_index():
+    """A NaN logit ranks below every number: a row of NaNs yields index 0 (the
+    lowest), and a NaN among numbers never wins, on both the scratch and the
+    allocation-free entry points."""
+    import torch
+    from lossless_speculative_decoding_gb300 import binding as B
+    T, h, V = 3, 256, 4096
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((T, h)).astype(np.float32)
+    x[0, 5] = np.nan                                           # row 0: every logit NaN
+    w = (rng.standard_normal((V, h)) * 0.02).astype(np.float32)
+    w[[7, 2000], :] = np.nan                                   # two NaN vocabulary rows
+    gamma = np.ones(h, np.float32)
+    ref = np.argmax(np.where(np.isnan(_ref_tokens(x, w, gamma, 1e-6)[1]), -np.inf,
+                             _ref_tokens(x, w, gamma, 1e-6)[1]), -1)
+    ref[0] = 0
+    nbytes = B.spec_lmhead_argmax_scratch_bytes(T, V)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    for noalloc in (False, True):
+        out = torch.full((T,), -1, dtype=torch.int32, device="cuda")
+        args = (torch.from_numpy(x).cuda(), T, h, V, torch.from_numpy(w).cuda(), syn.F32,
+                torch.from_numpy(gamma).cuda(), 1e-6)
+        if noalloc:
+            B.spec_lmhead_argmax_noalloc(*args, out, 0)
+        else:
+            B.spec_lmhead_argmax(*args, scratch, nbytes, out, 0)
+        torch.cuda.synchronize()
+        assert out.cpu().tolist() == ref.tolist()

@@ -173,3 +173,35 @@ def test_tc_gemm_split_k(M, N, K, dual, ks, fp8):
         ref = xf @ w1.T
         np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=0, atol=5e-5 * np.abs(ref).max())
     assert int(err.item()) == 0
+
+
+def test_wait_deadline_reports_timeout_and_context_survives():
+    """Every mbarrier wait of the tensor-core GEMM ends by a deadline read from
+    %globaltimer. With the test-only stall flag the kernel issues no loads, so
+    its waits must run out: the call returns within a few deadlines, the
+    timeout bit (8) is set, the output is untouched, and the next normal GEMM
+    on the same context is correct."""
+    import time
+    import torch
+    from lossless_speculative_decoding_gb300 import binding as B
+    M, N, K = 256, 32, 512
+    rng = np.random.default_rng(41)
+    a = torch.from_numpy(syn.f32_to_bf16_bits((rng.standard_normal((M, K)) * 0.05).astype(np.float32))
+                         .view(np.int16)).cuda()
+    x = torch.from_numpy(syn.f32_to_bf16_bits(rng.standard_normal((N, K)).astype(np.float32)).view(np.int16)).cuda()
+    out = torch.full((N, M), 7.0, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.time()
+    B.spec_tc_gemm_test(a, None, x, None, M, N, K, 0, out, err, 0, flags=1)
+    torch.cuda.synchronize()
+    dt = time.time() - t0
+    assert int(err.item()) & 8, "the stalled kernel did not report a timeout"
+    assert dt < 5.0, f"the stalled kernel took {dt:.2f} s to give up"
+    assert bool((out == 7.0).all()), "a stalled kernel wrote results"
+    err.zero_()
+    B.spec_tc_gemm_test(a, None, x, None, M, N, K, 0, out, err, 0)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.decode_bf16(x.cpu().numpy().view(np.uint16)) @ oracle.decode_bf16(a.cpu().numpy().view(np.uint16)).T
+    np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=1e-5, atol=1e-4)

@@ -34,11 +34,21 @@ def test_noalloc_lmhead_matches_scratch_entry():
         torch.cuda.synchronize()
         assert np.array_equal(got.cpu().numpy(), ref.cpu().numpy())
         assert (ref.cpu().numpy() >= 0).all()
+        # a warm call takes no device memory: the device's free bytes (as the
+        # driver reports them, whatever torch's allocator caches) do not move
+        free0 = torch.cuda.mem_get_info()[0]
+        B.spec_lmhead_argmax_noalloc(x, T, h, V, w, syn.BF16, gamma, 1e-6, got, 0)
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
+        assert np.array_equal(got.cpu().numpy(), ref.cpu().numpy())
 
 
 def test_noalloc_rejects_oversize():
     import torch
+    from lossless_speculative_decoding_gb300 import build
+    build.build()
     from lossless_speculative_decoding_gb300 import binding as B
+    torch.cuda.set_device(0)
     T, h, V = 64, 256, 151936            # 64 * 4748 candidates > the fixed array
     x = torch.zeros((T, h), device="cuda")
     w = torch.zeros((V, h), dtype=torch.int16, device="cuda")
