@@ -4,16 +4,21 @@
 Metric: committed tokens/s of speculative decoding (excluding prefill), the
 verify-step latency, and the fraction of the HBM roofline reached.
 
-Default workload: the DeepSeek-3B-MoE-shaped bf16 decoder at batch 1 (12
-layers, hidden 1280, 10x128 MHA, 64 routed experts top-6 + 2 shared of width
-896, vocab 129,280), a prompt of 256 N(0,1) visual rows + 16 token ids, K = 3
-drafts from a seeded synthetic drafter whose per-position match probability
-is 0.576, 1,085-token pages. Weights are random (N(0, 0.02), seed 0).
+Default workload (the largest single-GPU configuration): the
+DeepSeek-3B-MoE-shaped decoder (12 layers, hidden 1280, 10x128 MHA, 64 routed
+experts top-6 + 2 shared of width 896, vocab 129,280) with e4m3 attention and
+expert weights at concurrency 64: a shared 64-token prefix (its KV pages
+reused by every sequence) + 256 + 100 n visual rows per sequence, K = 3 drafts
+from a seeded synthetic drafter whose per-position match probability is
+0.576, output lengths N(1085, 300^2) clipped to [200, 4000], measured in steady
+state. The same model in bf16 at batch 1 (256 visual rows + 16 token ids,
+1,085-token pages) is measured in the same run and reported under
+"extra_workloads". Weights are random (N(0, 0.02), seed 0).
 
 One process per GPU; with torchrun each rank runs an independent replica (the
 step does not shard) and rank 0 prints one JSON line.
 
-  python bench.py [--steps K] [--warmup W] [--impl reference] [--workload NAME]
+  python bench.py [--steps K] [--warmup W] [--impl reference] [--workload NAME] [--extra NAME,...]
 """
 from __future__ import annotations
 
@@ -38,7 +43,8 @@ import numpy as np  # noqa: E402
 
 import synthetic as syn  # noqa: E402
 
-DEFAULT_WORKLOAD = "moe3b_bf16_b1"
+DEFAULT_WORKLOAD = "moe3b_fp8_c64"
+DEFAULT_EXTRA = "moe3b_bf16_b1"
 
 
 def parse():
@@ -48,6 +54,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--extra", default=None,
+                    help="comma-separated workloads measured after the main one (default: the batch-1 bf16 "
+                         "workload when the main one is the default; 'none' for none)")
+    ap.add_argument("--no-parity", action="store_true", help="skip the oracle parity leg")
     ap.add_argument("--profile-steps", type=int, default=64)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -181,14 +191,14 @@ def step_flops_of(cfg, T: int, R: int, ctx_sum: float, n_steps: int) -> float:
 # --------------------------------------------------------------------------- #
 # CPU oracle timing (cpu_baseline leg and --impl reference)
 # --------------------------------------------------------------------------- #
-def oracle_rate(w, prompt, wl, max_steps: int, warmup: int, budget_s: float, seq: int = 0) -> dict:
+def oracle_rate(w, prompt, wl, max_steps: int, warmup: int, budget_s: float, seq: int = 0, om=None) -> dict:
     """Committed tokens/s of the oracle's speculative loop (prefill excluded),
     over up to max_steps verify steps after `warmup` steps, stopping once
     budget_s seconds of timed steps have run."""
     import oracle
     K = wl.n_draft
     t0 = time.time()
-    om = oracle.OracleModel(w)
+    om = om if om is not None else oracle.OracleModel(w)
     t_load = time.time() - t0
     n_ref = 1 + (warmup + max_steps) * (K + 1) + K + 1
     # greedy reference of the oracle itself (untimed), for the synthetic drafter
@@ -228,6 +238,67 @@ def oracle_rate(w, prompt, wl, max_steps: int, warmup: int, budget_s: float, seq
     return {"tok_s": committed / t_run if t_run else 0.0, "steps": steps, "committed": committed,
             "s_per_step": t_run / max(steps, 1), "prefill_s": t_prefill, "load_s": t_load,
             "cores": os.cpu_count()}
+
+
+ROUTE_TIE = 4e-3     # router logit gap below which a row's expert choice may flip (see the parity tests)
+
+
+def parity_leg(gm, wl, om, prompt, prefix_id: int, steps: int, seed: int) -> dict:
+    """Oracle parity of the benchmarked model on one of its sequences: the
+    sequence is prefilled afresh, `steps` verify steps score the last token +
+    K drafts (the first draft the GPU's own next token, the rest random), and
+    the oracle scores the same rows teacher-forced. Counts rows, logits within
+    2e-2 of the oracle row range, token mismatches at oracle near-ties
+    (top-1 - top-2 < 1e-3) and rows exempted as router near-ties."""
+    import oracle
+    cfg = wl.model
+    K = wl.n_draft
+    t0 = time.time()
+    last = gm.prefill(0, prompt.visual, prompt.tokens, prefix_id)
+    cache = oracle.KVCache(cfg)
+    lg0 = oracle.forward(om, cache, oracle.prompt_embeddings(om, prompt), np.arange(prompt.length))[-1]
+    s0 = np.sort(lg0)
+    first_ok = last == int(np.argmax(lg0)) or s0[-1] - s0[-2] < 1e-3
+    rng = np.random.default_rng(seed)
+    rows = margin_ex = route_ex = bad_rows = bad_tokens = 0
+    max_abs = max_rel = 0.0
+    accept_ok = True
+    for _ in range(steps):
+        d = rng.integers(0, cfg.vocab, (1, K)).astype(np.int32)
+        d[0, 0] = np.argmax(gm.debug_logits([0], d)[0])
+        lg = gm.debug_logits([0], d)
+        tr = {}
+        ol = oracle.verify_rows(om, cache, last, d[0], tr)
+        err = np.abs(lg - ol).max(-1)
+        rng_row = ol.max(-1) - ol.min(-1)
+        ok = err <= 2e-2 * rng_row
+        gap = tr.get("route_gap", np.full(len(lg), np.inf))
+        exempt = ~ok & (gap < ROUTE_TIE)
+        bad_rows += int((~ok & ~exempt).sum())
+        route_ex += int(exempt.sum())
+        rows += len(lg)
+        if (~exempt).any():
+            max_abs = max(max_abs, float(err[~exempt].max()))
+            max_rel = max(max_rel, float((err[~exempt] / rng_row[~exempt]).max()))
+        for i in np.nonzero(np.argmax(lg, -1) != np.argmax(ol, -1))[0]:
+            if exempt[i]:
+                continue
+            s = np.sort(ol[i])
+            if s[-1] - s[-2] < 1e-3:
+                margin_ex += 1
+            else:
+                bad_tokens += 1
+        a, b = gm.verify(0, list(d[0]))
+        accept_ok &= (a, b) == oracle.accept(list(d[0]), np.argmax(lg, -1))
+        cache.truncate(cache.length - (K + 1) + a + 1)
+        last = b
+    gm.release(0)
+    return {"ok": bool(first_ok and bad_rows == 0 and bad_tokens == 0 and accept_ok),
+            "rows": rows, "margin_exempt_tokens": margin_ex, "route_tie_rows": route_ex,
+            "rows_outside_tolerance": bad_rows, "token_mismatches_outside_near_ties": bad_tokens,
+            "acceptance_exact": bool(accept_ok), "max_abs": max_abs, "max_rel_of_range": max_rel,
+            "sequence": f"{prompt.length}-row prompt, {steps} verify steps of {K + 1} rows",
+            "oracle": "fp32 CPU oracle, bf16 KV storage", "seconds": round(time.time() - t0, 1)}
 
 
 def run_reference(args):
@@ -348,21 +419,15 @@ def sampling_leg(NB: int, K: int, V: int, hbm_gbs: float) -> dict:
             "l2": f"ring of {copies} input copies ({copies * per / 1e6:.0f} MB)"}
 
 
-def run_ours(args):
+def measure(wl_name: str, args, primary: bool) -> dict:
+    """One workload: setup, the device-resident timed region, the profiled
+    pass, the end-to-end leg, the roofline, and (rank 0) the oracle legs.
+    Returns the fields of the JSON line (rank 0) or {} (other ranks)."""
     import torch
-    ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    from lossless_speculative_decoding_gb300 import build as libbuild
-    libbuild.build()
     from lossless_speculative_decoding_gb300 import binding as B
     from lossless_speculative_decoding_gb300.runtime import SpecModel
-
-    wl = syn.WORKLOADS[args.workload]
+    ws, rank, local = dist_env()
+    wl = syn.WORKLOADS[wl_name]
     if args.layers:
         import dataclasses
         wl = dataclasses.replace(wl, model=syn.scaled(wl.model, n_layers=args.layers))
@@ -445,15 +510,16 @@ def run_ours(args):
     clocks = Clocks(local)
     clocks.start()
     time.sleep(0.3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(KS + 1)]
+    ev[0].record(st)
     for s in range(W, W + KS):
         dev_step(s)
-    e1.record(st)
-    e1.synchronize()
+        ev[s - W + 1].record(st)
+    ev[KS].synchronize()
     clk = clocks.stop()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    ms = ev[0].elapsed_time(ev[KS])
+    step_us = np.array([ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(KS)])
     acc = d_acc.cpu().numpy().reshape(total, NB)
     committed = int((acc[W:W + KS] + 1).sum())
     ms_all, committed_all = aggregate(ms, committed, device="cuda")
@@ -514,36 +580,46 @@ def run_ours(args):
     ms_per_step = ms_all / KS
     launches = B.spec_step_launches(h, NB) + 1     # + the staging kernel
     share = {k: round(v["ms"] / max(sum(x["ms"] for x in stats.values()), 1e-9), 4) for k, v in stats.items()}
+    tau = committed / (KS * NB)
+    tau_exp = 1 + (syn.expected_accept_iid(wl.q, K) if wl.drafter == "iid" else syn.expected_accept_geometric(wl.q, K))
 
-    cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        i0 = min(ids, key=lambda i: prompts0[i].length)
-        r = oracle_rate(w, prompts0[i0], wl, max_steps=KS, warmup=1, budget_s=args.cpu_budget_s, seq=rank * NB + i0)
-        cpu = {"value": r["tok_s"], "unit": "tokens/s", "cores": r["cores"], "kind": "oracle",
-               "sample": f"{r['steps']} oracle verify steps (one sequence, {R} rows each) after one warm-up "
-                         f"step, same model and drafter; oracle prefill of the {prompts0[i0].length}-row "
-                         f"prompt ({r['prefill_s']:.1f}s) excluded" + (
-                             f"; the shortest of the {NB} prompts, from its first output" if NB > 1 else "")}
-
+    out = {}
     if rank == 0:
+        om = None
+        if not args.no_parity or (primary and ws == 1 and not args.no_cpu_baseline):
+            import oracle
+            om = oracle.OracleModel(w)
+        i0 = min(ids, key=lambda i: prompts0[i].length)
+        if not args.no_parity:
+            out["parity"] = parity_leg(gm, wl, om, prompts0[i0], prefix_id, steps=3, seed=17)
+        if primary and ws == 1 and not args.no_cpu_baseline:
+            r = oracle_rate(w, prompts0[i0], wl, max_steps=KS, warmup=1, budget_s=args.cpu_budget_s,
+                            seq=rank * NB + i0, om=om)
+            out["cpu_baseline"] = {
+                "value": r["tok_s"], "unit": "tokens/s", "cores": r["cores"], "kind": "oracle",
+                "sample": f"{r['steps']} oracle verify steps (one sequence, {R} rows each) after one warm-up "
+                          f"step, same model and drafter; oracle prefill of the {prompts0[i0].length}-row "
+                          f"prompt ({r['prefill_s']:.1f}s) excluded" + (
+                              f"; the shortest of the {NB} prompts, from its first output" if NB > 1 else "")}
+        del om
         steady = len(wl.out_len) > 1
-        line = {
-            "metric": "committed tokens/s (greedy speculative verify, excl. prefill)",
+        out.update({
             "value": committed_all / (ms_all * 1e-3),
-            "unit": "tokens/s", "n_gpus": ws, "steps": KS, "warmup": W,
-            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {syn.F32: "f32", syn.BF16: "bf16", syn.FP8: "e4m3 weights / f32 activations"}[cfg.wdtype],
-            "data": "synthetic (random-init weights, N(0,1) visual rows, seeded drafter)",
+            "ms_per_step": ms_per_step,
+            "dtype": {syn.F32: "f32", syn.BF16: "bf16",
+                      syn.FP8: "e4m3 weights widened to bf16; activations bf16 hi+lo pairs; fp32 accumulate"}[cfg.wdtype],
             "config": {"workload": wl.name, "model": cfg.name, "layers": cfg.n_layers, "batch": NB, "n_draft": K,
                        "drafter": f"{wl.drafter} q={wl.q}", "rows_per_step": T,
                        "prompt_rows": [p.length for p in prompts0] if NB > 1 else prompts0[0].length,
                        "page_size": wl.page_size, "shared_prefix": n_prefix,
-                       "tau": committed / (KS * NB),
+                       "tau": tau, "tau_expected": tau_exp,
                        "start": "steady state: seq i starts u_i ~ U{0..out_len_i-1} tokens into its output"
                        if steady else "first output token",
-                       "l2": "weights + KV read per step exceed the 126 MB L2",
+                       "l2": "weights + KV read per step exceed the 126 MB L2 (no flush needed)",
                        "parallelism": f"replicas x{ws}"},
-            "verify_step_us": ms_per_step * 1e3,
+            "verify_step_us": {"mean": ms_per_step * 1e3, "p10": float(np.percentile(step_us, 10)),
+                               "p50": float(np.percentile(step_us, 50)), "p90": float(np.percentile(step_us, 90))},
+            "value_at_expected_tau": NB * tau_exp * ws / (ms_per_step * 1e-3),
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "traffic": traffic_for(dom, dom_bytes_per_launch), "peak_source": peaks["source"],
@@ -562,12 +638,40 @@ def run_ours(args):
             "checks": {"lossless_vs_gpu_greedy": lossless, "acceptance_matches_schedule": acc_ok,
                        "e2e_tokens_match": e2e_ok},
             "setup_s": round(time.time() - t_setup, 1),
-        }
-        if cpu:
-            line["cpu_baseline"] = cpu
-        line["rejection_sampling"] = sampling_leg(NB, K, cfg.vocab, peaks["hbm_gbs"])
-        print(json.dumps(line), flush=True)
+        })
+        if primary:
+            out["rejection_sampling"] = sampling_leg(NB, K, cfg.vocab, peaks["hbm_gbs"])
     gm.close()
+    del w
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from lossless_speculative_decoding_gb300 import build as libbuild
+    libbuild.build()
+    extra = args.extra if args.extra is not None else (DEFAULT_EXTRA if args.workload == DEFAULT_WORKLOAD else "none")
+    extra = [e for e in extra.split(",") if e and e != "none" and e != args.workload]
+    main_res = measure(args.workload, args, primary=True)
+    extras = {e: measure(e, args, primary=False) for e in extra}
+    if rank == 0:
+        line = {"metric": "committed tokens/s (greedy speculative verify, excl. prefill)",
+                "value": main_res.pop("value"), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": main_res.pop("ms_per_step"), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": main_res.pop("dtype"),
+                "data": "synthetic (random-init weights, N(0,1) visual rows, seeded drafter)"}
+        line.update(main_res)
+        if extras:
+            line["extra_workloads"] = extras
+        print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
 
