@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
   att_prefix(B, T, R, RG, n_groups, s_pref);
   const int G = D.Hq / D.Hkv;
   const float scale = 1.0f / sqrtf((float)D_HEAD);
-  const size_t v_off = (size_t)D.Hkv * D.P * D_HEAD;                            // K -> V
+  const size_t v_off = (size_t)D.P * D_HEAD;                                     // K -> V
   const KT* kv = reinterpret_cast<const KT*>(S.kv);
   float* qw = Qw + warp * D_HEAD;
   float* pw = Pw + warp * ATT_CHUNK;
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
     const int maxpos = B.row_pos[r0 + nr - 1];
     const int nch = maxpos / ATT_CHUNK + 1;
     const int npairs = nr * G;
-    const size_t head_off = (((size_t)layer * 2) * D.Hkv + hk) * D.P * D_HEAD;   // K of (layer, hk)
+    const size_t head_off = (((size_t)layer * D.Hkv + hk) * 2) * D.P * D_HEAD;   // K of (layer, hk)
     {
       const int k0 = c * ATT_CHUNK;
       const int nk = min(ATT_CHUNK, maxpos + 1 - k0);
@@ -391,7 +391,9 @@ constexpr int ATT_NB = 6;        // chunk buffers per block
 template <int D_HEAD, int NW, int CG, int NB>
 struct AttWSmem {
   static constexpr int HB = ATT_CHUNK * 128;            // 64 dims of K or V for the chunk's keys
-  static constexpr int BUF = 2 * (D_HEAD / 64) * HB;    // K then V of one chunk
+  static constexpr int BUF = 2 * (D_HEAD / 64) * HB;    // K and V of one chunk: four 16-key boxes
+  static constexpr int BOXB = BUF / 4;                  // one box: K then V of 16 keys, all dims
+  static constexpr int KPART = BOXB / 2;                // its K part
   static constexpr int PST = ATT_CHUNK + 8;             // P row stride (bf16), padded
   static constexpr int PW = 2 * 8 * PST * 2;            // one warp's P hi + lo [8 pairs][PST]
   static constexpr size_t total = 1024 + (size_t)NB * BUF + (size_t)CG * NW * PW;   // + alignment slack
@@ -434,6 +436,19 @@ __device__ __forceinline__ void group_sync(int cg) {
 }
 // Byte offset of 16-byte piece c (0..7) of row r in a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+// Shared address of dims col..col+7 of key `key` (0..63) of a chunk buffer,
+// K (kv = 0) or V (kv = 1). The buffer holds four 16-key boxes as the TMA
+// writes them: box j = keys 16 j..16 j + 15, its K part then its V part, each
+// [key][64-dim half] rows of 128 bytes with the 128-byte swizzle (the boxes
+// and parts start on 1024-byte boundaries, so a row's swizzle is its index
+// within the part).
+template <int HALVES>
+__device__ __forceinline__ uint32_t kv_addr(uint32_t base, int key, int col, int kv) {
+  constexpr int BOXB = ATT_CHUNK / 4 * 2 * HALVES * 128, KPART = BOXB / 2;
+  const int row = (key & 15) * HALVES + (col >> 6);
+  return base + (uint32_t)((key >> 4) * BOXB + kv * KPART) + sw128(row, (col & 63) >> 3);
+}
 
 // Item i of the (group, kv head, chunk) order.
 struct AttItem {
@@ -515,15 +530,16 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_of(full + b)), "r"((uint32_t)BUF)
                      : "memory");
       __syncwarp();
-      if (lane < 8 * HALVES) {
-        // lane = box: 16-key block j, 64-dim half h, K or V
-        const int j = lane & 3, h = (lane >> 2) % HALVES, kvsel = lane / (4 * HALVES);
+      if (lane < 4) {
+        // lane j: the K and V (every dim) of keys k0 + 16 j .. k0 + 16 j + 15,
+        // one box of the (layer, kv head) plane pair -- four copies per chunk
+        const int j = lane;
         const int key = k0 + 16 * j;
-        const uint32_t dst = bufs + b * BUF + (kvsel * HALVES + h) * HB + j * 2048;
-        const int c2 = (layer * 2 + kvsel) * D.Hkv + it.hk;
+        const uint32_t dst = bufs + b * BUF + j * L::BOXB;
+        const int plane = (layer * D.Hkv + it.hk) * 2;
         asm volatile(
-            "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
-            ::"r"(dst), "l"(reinterpret_cast<uint64_t>(&kvmap)), "r"(h * 64), "r"(key % D.P), "r"(c2), "r"(page),
+            "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+            ::"r"(dst), "l"(reinterpret_cast<uint64_t>(&kvmap)), "r"(0), "r"(0), "r"(key % D.P), "r"(plane), "r"(page),
               "r"(bar_of(full + b))
             : "memory");
       }
@@ -542,7 +558,8 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
   const uint32_t ph = bufs + NB * BUF + warp * L::PW, pl = ph + 8 * PST * 2;
   int staged_g = -1, staged_hk = -1;
   uint32_t qh[KS][2], ql[KS][2];                       // B fragments of Q (this warp's pairs)
-  int pos[2] = {-1, -1};                               // positions of pairs 2 q4, 2 q4 + 1 of the tile
+  int pos[2] = {-1, -1};                               // positions of this lane's two pair columns
+  bool compact = false;                                // <= 4 pairs: hi parts in columns 0-3, lo in 4-7
   for (int k = cg; k < n; k += CG) {
     const int b = k % NB;
     const AttItem it(s_pref, n_groups, D.Hkv, i0 + k);
@@ -556,7 +573,12 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
     const int nk = min(ATT_CHUNK, maxpos + 1 - k0);
     // ---- Q fragments and pair positions, when the (group, kv head) changes ----
     if (gi != staged_g || hk != staged_hk) {
-      const int p = 8 * wl + g;
+      // compact form (at most 4 pairs, warp 0 only): column n < 4 is the hi
+      // part of pair n, column n + 4 its lo part, so one MMA takes both and a
+      // shuffle (lanes q4, q4 ^ 2) adds them; every column sum is the one the
+      // two-MMA form computes, so a pair's bits do not depend on the form
+      compact = npairs <= 4;
+      const int p = compact ? (g & 3) : 8 * wl + g;
       const float* qr = nullptr;
       if (p < npairs) qr = B.q + ((size_t)(r0 + p / G) * D.Hq + hk * G + p % G) * D_HEAD;
 #pragma unroll
@@ -566,11 +588,12 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
           float2 v = make_float2(0.f, 0.f);
           if (qr) v = *reinterpret_cast<const float2*>(qr + 16 * ks + 2 * q4 + 8 * u);
           split_bf16x2(v.x, v.y, qh[ks][u], ql[ks][u]);
+          if (compact && g >= 4) qh[ks][u] = ql[ks][u];
         }
       }
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int pj = 8 * wl + 2 * q4 + j;
+        const int pj = compact ? 2 * (q4 & 1) + j : 8 * wl + 2 * q4 + j;
         pos[j] = pj < npairs ? B.row_pos[r0 + pj / G] : -1;
       }
       staged_g = gi;
@@ -578,12 +601,12 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
     }
     // ---- this item's chunk: wait, zero V rows past the last key, publish in the group ----
     const bool ok = mbar_wait_deadline(bar_of(full + b), (k / NB) & 1, S.err);
-    const uint32_t kb = bufs + b * BUF, vb = kb + HALVES * HB;
+    const uint32_t kb = bufs + b * BUF;
     if (ok && nk < ATT_CHUNK) {
       for (int e = wl * 32 + lane; e < (ATT_CHUNK - nk) * HALVES * 8; e += NW * 32) {
         const int h = e / ((ATT_CHUNK - nk) * 8), r = nk + (e / 8) % (ATT_CHUNK - nk), pc = e % 8;
-        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vb + h * HB + r * 128 + pc * 16), "r"(0u)
-                     : "memory");
+        const uint32_t za = kb + (uint32_t)((r >> 4) * L::BOXB + L::KPART + ((r & 15) * HALVES + h) * 128 + pc * 16);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(za), "r"(0u) : "memory");
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // before TMA refills this buffer
     }
@@ -602,20 +625,20 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const int col = 16 * ks + 8 * (lane >> 4);
-        const uint32_t hbase = kb + (col >> 6) * HB;
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
           const int key = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
           uint32_t a[4];
-          ldsm_x4(a, hbase + sw128(key, (col & 63) >> 3));
+          ldsm_x4(a, kv_addr<HALVES>(kb, key, col, 0));
           mma_bf16(sacc[mt], a, qh[ks][0], qh[ks][1]);
-          mma_bf16(slo[mt], a, ql[ks][0], ql[ks][1]);
+          if (!compact) mma_bf16(slo[mt], a, ql[ks][0], ql[ks][1]);
         }
       }
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mt][e] += slo[mt][e];
+        for (int e = 0; e < 4; ++e)
+          sacc[mt][e] += compact ? __shfl_xor_sync(0xffffffffu, sacc[mt][e], 2) : slo[mt][e];
       // ---- scale, mask, column max / sum over the 64 keys ----
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -641,17 +664,21 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
           sm[j] += pe;
           const uint16_t hi = f_to_bf16(pe), lo = f_to_bf16(pe - bf16_to_f(hi));
           const uint32_t off = (uint32_t)(((2 * q4 + j) * PST + key) * 2);
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(ph + off), "h"(hi) : "memory");
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(pl + off), "h"(lo) : "memory");
+          if (compact) {   // row 2 q4 + j: the hi part of a pair (q4 < 2) or the lo part (q4 >= 2)
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(ph + off), "h"(q4 < 2 ? hi : lo) : "memory");
+          } else {
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(ph + off), "h"(hi) : "memory");
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(pl + off), "h"(lo) : "memory");
+          }
         }
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) sm[j] += __shfl_xor_sync(0xffffffffu, sm[j], o);
-      if (g == 0) {
+      if (g == 0 && (!compact || q4 < 2)) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const int pj = 8 * wl + 2 * q4 + j;
+          const int pj = compact ? 2 * q4 + j : 8 * wl + 2 * q4 + j;
           if (pj < npairs && mx[j] != -INFINITY) {
             const size_t pidx = ((size_t)(r0 + pj / G) * D.Hq + hk * G + pj % G) * B.n_chunk_max + c;
             reinterpret_cast<float2*>(B.att_ml)[pidx] = make_float2(mx[j], sm[j]);
@@ -659,35 +686,40 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
         }
       }
       __syncwarp();
-      // ---- O^T: head dims x this warp's pairs, keys in 16-wide steps ----
-      float o[KS][4];
+      // ---- O^T: head dims x this warp's pairs, keys in 16-wide steps (the
+      // hi and lo parts of P in separate accumulators, added in that order) ----
+      float o[KS][4], olo[KS][4];
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
+        for (int e = 0; e < 4; ++e) o[mt][e] = olo[mt][e] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < ATT_CHUNK / 16; ++ks) {
-        uint32_t bh0, bh1, bl0, bl1;
+        uint32_t bh0, bh1, bl0 = 0, bl1 = 0;
         const uint32_t poff = (uint32_t)(((lane & 7) * PST + 16 * ks + 8 * ((lane >> 3) & 1)) * 2);
         ldsm_x2(bh0, bh1, ph + poff);
-        ldsm_x2(bl0, bl1, pl + poff);
+        if (!compact) ldsm_x2(bl0, bl1, pl + poff);
         const int key = 16 * ks + (lane & 7) + 8 * (lane >> 4);
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           const int col = 16 * mt + 8 * ((lane >> 3) & 1);
           uint32_t a[4];
-          ldsm_x4_t(a, vb + (col >> 6) * HB + sw128(key, (col & 63) >> 3));
+          ldsm_x4_t(a, kv_addr<HALVES>(kb, key, col, 1));
           mma_bf16(o[mt], a, bh0, bh1);
-          mma_bf16(o[mt], a, bl0, bl1);
+          if (!compact) mma_bf16(olo[mt], a, bl0, bl1);
         }
       }
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][e] += compact ? __shfl_xor_sync(0xffffffffu, o[mt][e], 2) : olo[mt][e];
       // the chunk's K/V are no longer read by this warp
       __syncwarp();
       if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_of(empty + b)) : "memory");
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int pj = 8 * wl + 2 * q4 + j;
-        if (pj >= npairs || pos[j] < k0) continue;     // chunk lies after this row: no partial
+        const int pj = compact ? 2 * q4 + j : 8 * wl + 2 * q4 + j;
+        if ((compact && q4 >= 2) || pj >= npairs || pos[j] < k0) continue;   // chunk after this row: no partial
         float* og = B.att_o + (((size_t)(r0 + pj / G) * D.Hq + hk * G + pj % G) * B.n_chunk_max + c) * D_HEAD;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(256, SBPS) k_qkv_s(Dims D, DevState S, StepBuf
       const int page = pi < D.max_pages ? S.bt[(size_t)seq * D.max_pages + pi] : -1;
       if (page < 0) { atomicOr(S.err, DERR_PAGE); continue; }
       const size_t off = (size_t)page * D.page_elems +
-                         ((((size_t)layer * 2 + is_v) * D.Hkv + hk) * D.P + (pos % D.P)) * D.d + dim;
+                         ((((size_t)layer * D.Hkv + hk) * 2 + is_v) * D.P + (pos % D.P)) * D.d + dim;
       if (D.act_f32) reinterpret_cast<float*>(S.kv)[off] = outv;
       else reinterpret_cast<uint16_t*>(S.kv)[off] = f_to_bf16(outv);
     }
@@ -632,7 +632,7 @@ __global__ void __launch_bounds__(256, SBPS) k_qkv_m(Dims D, DevState S, StepBuf
         const int page = pi < D.max_pages ? S.bt[(size_t)B.row_seq[row] * D.max_pages + pi] : -1;
         if (page < 0) { atomicOr(S.err, DERR_PAGE); continue; }
         const size_t off = (size_t)page * D.page_elems +
-                           ((((size_t)layer * 2 + is_v) * D.Hkv + hk) * D.P + (pos % D.P)) * D.d + j;
+                           ((((size_t)layer * D.Hkv + hk) * 2 + is_v) * D.P + (pos % D.P)) * D.d + j;
         reinterpret_cast<uint16_t*>(S.kv)[off] = f_to_bf16(o0);
         reinterpret_cast<uint16_t*>(S.kv)[off + half] = f_to_bf16(o1);
       }

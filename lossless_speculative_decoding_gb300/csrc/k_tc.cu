@@ -21,10 +21,13 @@
 // its own row of X -- its result does not depend on the other tokens.
 //
 // FP8 weights (e4m3, per-row fp32 scale applied in the epilogue): the 8 KB
-// e4m3 tile (row-major inside the tile) lands in a staging buffer, four converter warps widen
-// it to bf16 -- exactly, every e4m3 value is a bf16 value -- into the
-// 128-byte-swizzled operand tile and signal the MMA thread, so the tensor
-// cores run the same bf16 MMA while HBM carries one byte per weight.
+// e4m3 tile (row-major inside the tile) lands in the stage, four converter
+// warps widen it to bf16 -- exactly, every e4m3 value is a bf16 value -- into
+// one of two 128-byte-swizzled operand buffers and signal the MMA thread, so
+// the tensor cores run the same bf16 MMA while HBM carries one byte per
+// weight. The widened tiles live in their own two-deep ring, not in the
+// stages, so the stages (e4m3 + activations only) are small and many loads
+// stay in flight.
 //
 // Every wait on an mbarrier ends by a deadline read from %globaltimer (or as
 // soon as another CTA has reported a timeout); a timeout sets an error bit,
@@ -53,16 +56,23 @@ constexpr int TC_MAXST = 12;          // pipeline stages at most
 constexpr int TC_SMEM = 220 * 1024;   // dynamic shared memory of every CTA
 constexpr int TC_HDR = 1024;          // barriers + TMEM slot, ahead of the stages
 
+constexpr int TC_NCONV = 2;           // FP8: widened bf16 weight buffers (converter -> MMA ring)
+
 // Bytes of one pipeline stage of `at` K atoms for nsub 32-row activation
-// boxes: weight tile(s), activation hi (+ lo), e4m3 staging (FP8). Every part
-// is a multiple of 1024 bytes, so each stays aligned for the 128-byte swizzle.
+// boxes: the weight tile(s) as stored (bf16, or e4m3 staging for FP8) and the
+// activation parts. Every part is a multiple of 1024 bytes, so each stays
+// aligned for the 128-byte swizzle.
 __host__ __device__ constexpr int tc_stage_bytes(int dual, int f8, int nsub, int split, int at) {
-  return at * ((TC_A_BYTES + (f8 ? TC_A8_BYTES : 0)) * (1 + dual) + (1 + split) * nsub * TC_NSUB * TC_BK * 2);
+  return at * ((f8 ? TC_A8_BYTES : TC_A_BYTES) * (1 + dual) + (1 + split) * nsub * TC_NSUB * TC_BK * 2);
+}
+// FP8: the ring of widened bf16 weight tiles the MMAs read, after the stages.
+__host__ __device__ constexpr int tc_conv_bytes(int dual, int f8, int at) {
+  return f8 ? TC_NCONV * at * TC_A_BYTES * (1 + dual) : 0;
 }
 // Stages that fit: as many weight tiles in flight as shared memory allows.
 __host__ __device__ constexpr int tc_stage_count(int dual, int f8, int nsub, int split, int at) {
-  return (TC_SMEM - TC_HDR - 1024) / tc_stage_bytes(dual, f8, nsub, split, at) < TC_MAXST
-             ? (TC_SMEM - TC_HDR - 1024) / tc_stage_bytes(dual, f8, nsub, split, at)
+  return (TC_SMEM - TC_HDR - 1024 - tc_conv_bytes(dual, f8, at)) / tc_stage_bytes(dual, f8, nsub, split, at) < TC_MAXST
+             ? (TC_SMEM - TC_HDR - 1024 - tc_conv_bytes(dual, f8, at)) / tc_stage_bytes(dual, f8, nsub, split, at)
              : TC_MAXST;
 }
 // K atoms per stage: two (half the barrier round trips per weight byte)
@@ -132,15 +142,24 @@ __device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 v) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+constexpr int TC_NCONVW = 6;          // FP8 converter warps (warps 2..7)
+
 // Stage s of the FP8 form: e4m3 staging [128 rows][64 B] -> bf16 tile [128
 // rows][128 B] with the 128-byte swizzle (16-byte piece c of row r at
-// (c ^ (r % 8)) * 16). 128 converter threads, 8 pieces each.
+// (c ^ (r % 8)) * 16). The converter threads take the 1024 pieces round
+// robin; a thread loads all its pieces before widening any.
 __device__ __forceinline__ void convert_tile(const unsigned char* stg, unsigned char* dst, int t) {
+  constexpr int NT = TC_NCONVW * 32, NI = (1024 + NT - 1) / NT;
+  uint2 v[NI];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int i = t + 128 * j, r = i >> 3, c = i & 7;
-    const uint2 v = *reinterpret_cast<const uint2*>(stg + r * 64 + c * 8);
-    *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = e4m3x8_to_bf16x8(v);
+  for (int j = 0; j < NI; ++j) {
+    const int i = t + NT * j, r = i >> 3, c = i & 7;
+    if (i < 1024) v[j] = *reinterpret_cast<const uint2*>(stg + r * 64 + c * 8);
+  }
+#pragma unroll
+  for (int j = 0; j < NI; ++j) {
+    const int i = t + NT * j, r = i >> 3, c = i & 7;
+    if (i < 1024) *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = e4m3x8_to_bf16x8(v[j]);
   }
 }
 
@@ -150,9 +169,11 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
                                                                const __grid_constant__ CUtensorMap mapBlo2, TcParams P) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // header: full[MAXST], empty[MAXST], done, conv[MAXST] (F8: converted tile ready), TMEM slot, abort flag
+  // header: full[MAXST], empty[MAXST], done, cfull[MAXST] (F8: widened tile ready; the first
+  // TC_NCONV used), cempty[TC_NCONV] (F8: widened buffer free), TMEM slot, abort flag
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * TC_MAXST + 1);
+  uint64_t* cempty = bars + 3 * TC_MAXST + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + TC_NCONV);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -172,18 +193,21 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   const int nsub = (nrows + TC_NSUB - 1) / TC_NSUB;
   const int N = nsub * TC_NSUB;                       // activation rows: multiple of 32, <= 128
   const int NP = (1 + P.split) * N;                   // MMA N: the hi rows, then the lo (and lo2) rows
-  // stage layout, AT K atoms per stage: [A atoms][A2 atoms (DUAL)][B atoms,
-  // each hi rows then lo rows][e4m3 staging (F8): A atoms, A2 atoms]. The lo
-  // box follows the hi box at N x 128 bytes (a whole number of 8-row swizzle
-  // groups), so one MMA with N = NP multiplies the weights into both.
+  // stage layout, AT K atoms per stage: bf16: [A atoms][A2 atoms (DUAL)][B
+  // atoms, each hi rows then lo (lo2) rows]; FP8: [B atoms][e4m3 A atoms, A2
+  // atoms], the widened tiles in the ring after the stages. The lo box follows
+  // the hi box at N x 128 bytes (a whole number of 8-row swizzle groups), so
+  // one MMA with N = NP multiplies the weights into all parts.
   const int AT = tc_atoms(DUAL, F8, nsub, P.split);
   const int BB = N * TC_BK * 2;                       // one activation part of one atom
   const int BAT = (1 + P.split) * BB;                 // one B atom
   const int SB = tc_stage_bytes(DUAL, F8, nsub, P.split, AT);
   const int STAGES = tc_stage_count(DUAL, F8, nsub, P.split, AT);
-  const int BOFF = AT * TC_A_BYTES * (1 + DUAL);
+  const int BOFF = F8 ? 0 : AT * TC_A_BYTES * (1 + DUAL);
   const int STG_OFF = BOFF + AT * BAT;
+  const int CONV_ONE = AT * TC_A_BYTES * (1 + DUAL);  // one widened buffer (FP8)
   unsigned char* stages = smem + TC_HDR;
+  unsigned char* conv = stages + STAGES * SB;         // FP8: TC_NCONV widened buffers
   // this split's K atoms [kt0, kt1) (the host picks splits that are never empty)
   const int KTall = P.K / TC_BK, KTs = (KTall + ksn - 1) / ksn;
   const int kt0 = ks * KTs, kt1 = min(KTall, kt0 + KTs), KT = kt1 - kt0;
@@ -198,12 +222,15 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   constexpr int NACC = 3 * NKB;                       // accumulators read back at most (three parts)
   constexpr uint32_t NCOL = 512;                      // TMEM columns: (1 + DUAL) * NKB * TC_ACCW
 
-  // barrier indices: full s, empty TC_MAXST + s, done 2 TC_MAXST, conv 2 TC_MAXST + 1 + s
+  // barrier indices: full s, empty TC_MAXST + s, done 2 TC_MAXST, cfull 2 TC_MAXST + 1 + c
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2 * TC_MAXST + 1; ++i)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bars + i)));
     for (int i = 0; i < TC_MAXST; ++i)    // one arrival per converter warp
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(smem_u32(bars + 2 * TC_MAXST + 1 + i)));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bars + 2 * TC_MAXST + 1 + i)),
+                   "r"(TC_NCONVW));
+    for (int i = 0; i < TC_NCONV; ++i)    // one MMA commit
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(cempty + i)));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *abort_flag = 0;
   }
@@ -220,6 +247,9 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   if (warp == 0 && lane == 0) {
     // ---- TMA producer ----
     constexpr int AST = F8 ? TC_A8_BYTES : TC_A_BYTES;
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapB)) : "memory");
+    if (P.split > 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapBlo)) : "memory");
+    if (P.split > 1) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapBlo2)) : "memory");
     // P.test_stall: issue nothing, so every wait on these copies runs to its
     // deadline (the check of the bounded waits)
     for (int i = 0; i < (P.test_stall ? 0 : NST); ++i) {
@@ -260,9 +290,11 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
     bool ok = true;
     int kstep = 0;                                    // 16-wide K steps issued so far
     for (int i = 0; i < NST && ok; ++i) {
-      const int s = i % STAGES, na = min(AT, KT - i * AT);
-      // bf16: the TMA bytes of the stage; F8: the converters' signal (after those bytes)
-      if (!mbar_wait_deadline(smem_u32(bars + (F8 ? 2 * TC_MAXST + 1 : 0) + s), (i / STAGES) & 1, P.err)) {
+      const int s = i % STAGES, na = min(AT, KT - i * AT), c = i % TC_NCONV;
+      // bf16: the TMA bytes of the stage; F8: the converters' signal for widened buffer c
+      const bool arrived = F8 ? mbar_wait_deadline(smem_u32(bars + 2 * TC_MAXST + 1 + c), (i / TC_NCONV) & 1, P.err)
+                              : mbar_wait_deadline(smem_u32(bars + s), (i / STAGES) & 1, P.err);
+      if (!arrived) {
         atomicOr(P.err, DERR_TIMEOUT);
         *abort_flag = 1;
         ok = false;
@@ -270,8 +302,9 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const uint64_t ds = d0 + (uint64_t)((s * SB) >> 4);
+      const uint64_t dsa = F8 ? sw128_desc(smem_u32(conv + c * CONV_ONE)) : ds;   // the weight tiles
       for (int j = 0; j < na; ++j) {
-        const uint64_t da = ds + (uint64_t)((j * TC_A_BYTES) >> 4);
+        const uint64_t da = dsa + (uint64_t)((j * TC_A_BYTES) >> 4);
         const uint64_t db = ds + (uint64_t)((BOFF + j * BAT) >> 4);
 #pragma unroll
         for (int k = 0; k < TC_BK / 16; ++k, ++kstep) {
@@ -291,29 +324,34 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
       }
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                    ::"r"(smem_u32(bars + TC_MAXST + s)) : "memory");
+      if (F8)   // widened buffer c is free once these MMAs complete
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                     ::"r"(smem_u32(cempty + c)) : "memory");
     }
     // "done" fires once every MMA issued so far has completed -- also after an
     // abort, so TMEM is never freed under an MMA in flight
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  ::"r"(smem_u32(bars + 2 * TC_MAXST)) : "memory");
-  } else if (F8 && warp >= 4) {
-    // ---- converters: e4m3 staging -> swizzled bf16 operand tile ----
-    const int t = threadIdx.x - 128;
+  } else if (F8 && warp >= 2) {
+    // ---- converters (warps 2..7): e4m3 staging -> swizzled bf16 operand tile ----
+    const int t = threadIdx.x - 64;
     for (int i = 0; i < NST; ++i) {
-      const int s = i % STAGES, na = min(AT, KT - i * AT);
-      if (!mbar_wait_deadline(smem_u32(bars + s), (i / STAGES) & 1, P.err)) {
+      const int s = i % STAGES, na = min(AT, KT - i * AT), c = i % TC_NCONV;
+      if (!mbar_wait_deadline(smem_u32(bars + s), (i / STAGES) & 1, P.err) ||
+          (i >= TC_NCONV && !mbar_wait_deadline(smem_u32(cempty + c), ((i / TC_NCONV) - 1) & 1, P.err))) {
         if (lane == 0) atomicOr(P.err, DERR_TIMEOUT);
         break;
       }
       unsigned char* st = stages + s * SB;
+      unsigned char* cv = conv + c * CONV_ONE;
       for (int j = 0; j < na; ++j) {
-        convert_tile(st + STG_OFF + j * TC_A8_BYTES, st + j * TC_A_BYTES, t);
-        if (DUAL) convert_tile(st + STG_OFF + (AT + j) * TC_A8_BYTES, st + (AT + j) * TC_A_BYTES, t);
+        convert_tile(st + STG_OFF + j * TC_A8_BYTES, cv + j * TC_A_BYTES, t);
+        if (DUAL) convert_tile(st + STG_OFF + (AT + j) * TC_A8_BYTES, cv + (AT + j) * TC_A_BYTES, t);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0)
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bars + 2 * TC_MAXST + 1 + s)) : "memory");
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bars + 2 * TC_MAXST + 1 + c)) : "memory");
     }
   }
   __syncwarp();
@@ -441,7 +479,42 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
       }
     }
   };
-  if (ksn == 1) {
+  if (ksn == 1 && P.epi == TC_ARGMAX && TC_BM * (N + 1) * 4 <= STAGES * SB) {
+    // per column: max over the tile's 128 rows, lowest row on ties. Every MMA
+    // has completed and every copy has landed, so the stage memory holds the
+    // [row][column] values (row stride N + 1: conflict-free both ways) and one
+    // thread per column scans its rows -- no chain of warp shuffles
+    float* tv = reinterpret_cast<float*>(stages);
+    const int LD = N + 1;
+    if (warp < 4) {
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        float v[16], u2[16];
+        load_acc(c0, v, u2);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tv[m * LD + c0 + j] = am_key(v[j] * sc);
+      }
+    }
+    __syncthreads();
+    const int n = threadIdx.x;
+    if (have && n < nrows) {
+      float bv[4];
+      int bi[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) { bv[u] = tv[u * LD + n]; bi[u] = u; }
+      for (int r = 4; r < TC_BM; r += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float c = tv[(r + u) * LD + n];
+          if (c > bv[u]) { bv[u] = c; bi[u] = r + u; }        // rows in increasing order: ties keep the lower
+        }
+      }
+#pragma unroll
+      for (int u = 1; u < 4; ++u)
+        if (bv[u] > bv[0] || (bv[u] == bv[0] && bi[u] < bi[0])) { bv[0] = bv[u]; bi[0] = bi[u]; }
+      P.am_val[(size_t)(off + n0 + n) * P.am_ld + mt] = bv[0];
+      P.am_idx[(size_t)(off + n0 + n) * P.am_ld + mt] = P.row0 + wrow + bi[0];
+    }
+  } else if (ksn == 1) {
     if (warp < 4) {
       for (int c0 = 0; c0 < N; c0 += 16) {
         float v[16], u2[16];
@@ -574,12 +647,14 @@ int kv_make_map(CUtensorMap* map, const void* kv, int head_dim, int page_size, i
   auto fn = encode_fn();
   if (!fn) return -1;
   if ((reinterpret_cast<uintptr_t>(kv) & 15) || head_dim % 64 || page_size % 16) return -2;
-  const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)page_size, (cuuint64_t)planes, (cuuint64_t)n_pages};
-  const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)page_size * head_dim * 2,
+  const int halves = head_dim / 64;
+  const cuuint64_t dims[5] = {64, (cuuint64_t)halves, (cuuint64_t)page_size, (cuuint64_t)planes,
+                              (cuuint64_t)n_pages};
+  const cuuint64_t strides[4] = {128, (cuuint64_t)head_dim * 2, (cuuint64_t)page_size * head_dim * 2,
                                  (cuuint64_t)page_elems * 2};
-  const cuuint32_t box[4] = {64, 16, 1, 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv), dims, strides, box, es,
+  const cuuint32_t box[5] = {64, (cuuint32_t)halves, 16, 2, 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kv), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : -3;

@@ -57,7 +57,7 @@ __global__ void k_rope_kv(Dims D, DevState S, StepBuf B, int layer) {
       return;
     }
     const int hk = head - D.Hq - (is_v ? D.Hkv : 0);
-    base = (size_t)page * D.page_elems + ((((size_t)layer * 2 + (is_v ? 1 : 0)) * D.Hkv + hk) * D.P + (pos % D.P)) * D.d;
+    base = (size_t)page * D.page_elems + ((((size_t)layer * D.Hkv + hk) * 2 + (is_v ? 1 : 0)) * D.P + (pos % D.P)) * D.d;
   }
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
     const float a = src[i], b = src[i + half];

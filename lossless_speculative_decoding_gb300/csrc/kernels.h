@@ -38,7 +38,7 @@ struct Dims {
 };
 
 struct DevState {
-  void* kv;              // [n_pages][L][2][Hkv][P][d]
+  void* kv;              // [n_pages][L][Hkv][2 (K, V)][P][d]
   const int* bt;         // [slots][max_pages]
   int* seq_len;          // [slots]
   int* last_tok;         // [slots]
@@ -168,9 +168,11 @@ struct TcMaps {
 // 2D bf16 tensor map: rows of `inner` elements, box 64 x box_rows, 128-byte
 // swizzle. Returns 0 on success.
 int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
-// 4D bf16 tensor map over the paged KV pool [pages][layer][K|V][kv head][key][dim]
-// for the tensor-core attention: dims (head_dim, page_size, layers x 2 x kv
-// heads, n_pages), box 64 x 16 x 1 x 1, 128-byte swizzle, zero fill outside.
+// 5D bf16 tensor map over the paged KV pool [pages][layer][kv head][K|V][key][dim]
+// for the tensor-core attention: dims (64 dims, head_dim / 64 halves,
+// page_size keys, layers x kv heads x 2 planes, n_pages), box 64 x halves x
+// 16 x 2 x 1 -- the K and V of 16 keys of one (layer, kv head) in one copy --
+// 128-byte swizzle, zero fill outside.
 int kv_make_map(CUtensorMap* map, const void* kv, int head_dim, int page_size, int planes, int n_pages,
                 size_t page_elems);
 // Rewrites W [rows, K] (row-major; bf16, or e4m3 when f8) into the tiled
