@@ -232,7 +232,9 @@ int spec_lmhead_argmax(const float* x_dev, int T, int hidden, int vocab, const v
 
 /* Tensor-core GEMM check: with weights A [M, K] (bf16, or e4m3 when a_fp8,
  * then scaled per row by a_scale_dev[m]) and activations X = B + B_lo (bf16
- * [N, K] each, row-major, device; b_lo_dev may be NULL), in CTAs of n_tile
+ * [N, K] each, row-major, device; b_lo_dev may be NULL; with a_fp8 the
+ * operands are f16 and B + B_lo = 256 X, the f16 parts the e4m3-weight GEMMs
+ * of a model take, and the dual output is f16(256 h)), in CTAs of n_tile
  * activation rows (32, 64 or 128; 0 = 128) and k_split K splits (0 or 1: none;
  * partials summed in split order by the tile's last split), dual = 0 writes
  * out_dev[n][m] = sum_k A[m][k] * X[n][k] (fp32 [N, M]); dual = 1 writes

@@ -57,9 +57,30 @@ template <> struct Elt<bf16_t> { static constexpr int per16 = 8; };
 template <> struct Elt<fp8_t>  { static constexpr int per16 = 16; };
 
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
 __device__ __forceinline__ uint16_t f_to_bf16(float f) {
   __nv_bfloat16 h = __float2bfloat16_rn(f);
   return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// Operand parts of the tensor-core GEMMs. bf16 models: parts of x in bf16.
+// e4m3-weight models: parts of x * F16_OP_SCALE in f16 (the MMA runs on f16,
+// to which e4m3 widens in one instruction; f16 hi + lo keeps ~22 bits, and
+// the exact power-of-two scale keeps the lo parts of the activations, which
+// stay far below 255 in magnitude, clear of f16's subnormal range). The
+// GEMM epilogue multiplies by 1 / F16_OP_SCALE.
+constexpr float F16_OP_SCALE = 256.0f;
+__device__ __forceinline__ uint16_t f_to_f16(float f) { return __half_as_ushort(__float2half_rn(f)); }
+__device__ __forceinline__ float f16_to_f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+// Split x into n_parts 16-bit parts (bf16 or, with f16, of x * F16_OP_SCALE),
+// each the rounding of what the earlier parts leave.
+__device__ __forceinline__ void split_parts(float x, int f16, int n_parts, uint16_t* out) {
+  float r = f16 ? x * F16_OP_SCALE : x;
+  for (int i = 0; i < n_parts; ++i) {
+    const uint16_t p = f16 ? f_to_f16(r) : f_to_bf16(r);
+    out[i] = p;
+    r -= f16 ? f16_to_f(p) : bf16_to_f(p);
+  }
 }
 
 // 16-byte streaming load that does not allocate in L1 (weights are read once).

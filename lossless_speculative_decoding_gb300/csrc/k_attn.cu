@@ -149,9 +149,10 @@ __device__ __forceinline__ void merge_pair(const Dims& D, const StepBuf& B, int 
     const size_t e = (size_t)row * D.Hq * D_HEAD + (size_t)hq * D_HEAD + NV * lane;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-      const uint16_t hi = f_to_bf16(r[i]);
-      B.o_bf16[e + i] = hi;
-      B.o_lo[e + i] = f_to_bf16(r[i] - bf16_to_f(hi));
+      uint16_t p[2];
+      split_parts(r[i], D.op_f16, 2, p);
+      B.o_bf16[e + i] = p[0];
+      B.o_lo[e + i] = p[1];
     }
   }
 }
@@ -434,6 +435,14 @@ __device__ __forceinline__ void group_sync(int cg) {
   if constexpr (NW == 1) __syncwarp();
   else asm volatile("bar.sync %0, %1;" ::"r"(1 + cg), "r"(NW * 32) : "memory");
 }
+// 2^x by the hardware approximation (relative error about 2^-22); e^y is
+// computed as 2^(y log2 e).
+__device__ __forceinline__ float exp2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // Byte offset of 16-byte piece c (0..7) of row r in a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
@@ -554,6 +563,7 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
   // ---- consumer group cg, warp wl of it: pairs 8 wl .. 8 wl + 7 of the group ----
   const int cg = warp / NW, wl = warp % NW;
   const float scale = 1.0f / sqrtf((float)D_HEAD);
+  const float scale_l2e = scale * 1.4426950408889634f;    // scale * log2(e)
   const int G = D.Hq / D.Hkv;
   const uint32_t ph = bufs + NB * BUF + warp * L::PW, pl = ph + 8 * PST * 2;
   int staged_g = -1, staged_hk = -1;
@@ -625,13 +635,14 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const int col = 16 * ks + 8 * (lane >> 4);
+        uint32_t a[4][4];                              // the K step's four key tiles, loaded before any MMA
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+          ldsm_x4(a[mt], kv_addr<HALVES>(kb, 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1), col, 0));
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
-          const int key = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1);
-          uint32_t a[4];
-          ldsm_x4(a, kv_addr<HALVES>(kb, key, col, 0));
-          mma_bf16(sacc[mt], a, qh[ks][0], qh[ks][1]);
-          if (!compact) mma_bf16(slo[mt], a, ql[ks][0], ql[ks][1]);
+          mma_bf16(sacc[mt], a[mt], qh[ks][0], qh[ks][1]);
+          if (!compact) mma_bf16(slo[mt], a[mt], ql[ks][0], ql[ks][1]);
         }
       }
 #pragma unroll
@@ -639,14 +650,15 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           sacc[mt][e] += compact ? __shfl_xor_sync(0xffffffffu, sacc[mt][e], 2) : slo[mt][e];
-      // ---- scale, mask, column max / sum over the 64 keys ----
+      // ---- mask, column max / sum over the 64 keys: p = 2^((s - max) * scale * log2 e),
+      // the chunk's max kept in scaled units (max(s * scale) = max(s) * scale) ----
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int key = 16 * mt + g + 8 * (e >> 1), j = e & 1;
-          const float v = (key < nk && k0 + key <= pos[j]) ? sacc[mt][e] * scale : -INFINITY;
+          const float v = (key < nk && k0 + key <= pos[j]) ? sacc[mt][e] : -INFINITY;
           sacc[mt][e] = v;
           mx[j] = fmaxf(mx[j], v);
         }
@@ -660,7 +672,7 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int key = 16 * mt + g + 8 * (e >> 1), j = e & 1;
-          const float pe = mx[j] == -INFINITY ? 0.f : expf(sacc[mt][e] - mx[j]);
+          const float pe = mx[j] == -INFINITY ? 0.f : exp2_approx((sacc[mt][e] - mx[j]) * scale_l2e);
           sm[j] += pe;
           const uint16_t hi = f_to_bf16(pe), lo = f_to_bf16(pe - bf16_to_f(hi));
           const uint32_t off = (uint32_t)(((2 * q4 + j) * PST + key) * 2);
@@ -681,7 +693,7 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
           const int pj = compact ? 2 * q4 + j : 8 * wl + 2 * q4 + j;
           if (pj < npairs && mx[j] != -INFINITY) {
             const size_t pidx = ((size_t)(r0 + pj / G) * D.Hq + hk * G + pj % G) * B.n_chunk_max + c;
-            reinterpret_cast<float2*>(B.att_ml)[pidx] = make_float2(mx[j], sm[j]);
+            reinterpret_cast<float2*>(B.att_ml)[pidx] = make_float2(mx[j] * scale, sm[j]);
           }
         }
       }

@@ -401,14 +401,43 @@ __global__ void __launch_bounds__(256, SBPS) k_down_s(Dims D, StepBuf B, const W
 }
 
 // Expert combine, in place: x[t][k] += sum over slots s (in order) of
-// w[t][s] * y[t*NS + s][k] (routed weight p, shared weight 1).
+// w[t][s] * y[t*NS + s][k] (routed weight p, shared weight 1): a = 0, then
+// a = fma(w_s, y_s, a) slot by slot, then x + a. A thread takes four
+// consecutive columns of one row and loads all of its slots' values before
+// the first sum (up to COMB_MAXS slots; more slots take the scalar loop).
+constexpr int COMB_MAXS = 16;
 __global__ void k_combine(Dims D, StepBuf B, float* x, int T) {
   pdl_wait();
   pdl_trigger();
-  const int n = T * D.h;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    const int t = i / D.h, kk = i % D.h;
-    x[i] = combine_one(x, B.y, B.wts, t, kk, D.h, D.NS, D.k);
+  const int h4 = D.h / 4, n4 = T * h4;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += gridDim.x * blockDim.x) {
+    const int t = i / h4, k4 = i % h4;
+    if (D.NS > COMB_MAXS) {
+      for (int c = 0; c < 4; ++c) x[(size_t)t * D.h + 4 * k4 + c] = combine_one(x, B.y, B.wts, t, 4 * k4 + c, D.h, D.NS, D.k);
+      continue;
+    }
+    float4 yv[COMB_MAXS];
+    float wv[COMB_MAXS];
+#pragma unroll
+    for (int s = 0; s < COMB_MAXS; ++s) {
+      if (s < D.NS) {
+        yv[s] = reinterpret_cast<const float4*>(B.y + ((size_t)t * D.NS + s) * D.h)[k4];
+        wv[s] = s < D.k ? B.wts[t * D.k + s] : 1.f;
+      }
+    }
+    float4 xv = reinterpret_cast<const float4*>(x + (size_t)t * D.h)[k4];
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int s = 0; s < COMB_MAXS; ++s) {
+      if (s < D.NS) {
+        a0 = fmaf(wv[s], yv[s].x, a0);
+        a1 = fmaf(wv[s], yv[s].y, a1);
+        a2 = fmaf(wv[s], yv[s].z, a2);
+        a3 = fmaf(wv[s], yv[s].w, a3);
+      }
+    }
+    xv.x += a0; xv.y += a1; xv.z += a2; xv.w += a3;
+    reinterpret_cast<float4*>(x + (size_t)t * D.h)[k4] = xv;
   }
 }
 
@@ -1059,9 +1088,9 @@ void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaSt
 }
 
 void launch_combine(const Dims& D, const StepBuf& B, float* x, int T, cudaStream_t st) {
-  const int n = T * D.h;
-  int blocks = cdiv(n, 256);
-  if (blocks > 4 * D.n_sm) blocks = 4 * D.n_sm;
+  const int n4 = T * D.h / 4;                      // hidden is a multiple of 4 (checked at init)
+  int blocks = cdiv(n4, 256);
+  if (blocks > 8 * D.n_sm) blocks = 8 * D.n_sm;
   launch_k(k_combine, dim3(blocks), dim3(256), 0, st, D, B, x, T);
 }
 

@@ -21,11 +21,12 @@
 // its own row of X -- its result does not depend on the other tokens.
 //
 // FP8 weights (e4m3, per-row fp32 scale applied in the epilogue): the 8 KB
-// e4m3 tile (row-major inside the tile) lands in the stage, four converter
-// warps widen it to bf16 -- exactly, every e4m3 value is a bf16 value -- into
+// e4m3 tile (row-major inside the tile) lands in the stage, six converter
+// warps widen it to f16 -- exactly, one conversion per pair of values -- into
 // one of two 128-byte-swizzled operand buffers and signal the MMA thread, so
-// the tensor cores run the same bf16 MMA while HBM carries one byte per
-// weight. The widened tiles live in their own two-deep ring, not in the
+// the tensor cores run an f16 MMA while HBM carries one byte per weight. The
+// activations of these GEMMs come as f16 parts of 256 x (hi + lo carry ~22
+// significant bits); the epilogue divides the 256 back out. The widened tiles live in their own two-deep ring, not in the
 // stages, so the stages (e4m3 + activations only) are small and many loads
 // stay in flight.
 //
@@ -98,9 +99,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major.
-__device__ __forceinline__ uint32_t tc_idesc(int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(TC_BM >> 4) << 24);
+// Instruction descriptor: bf16 x bf16 (f16 x f16 with f16) -> fp32, both operands K-major.
+__device__ __forceinline__ uint32_t tc_idesc(int N, int f16) {
+  const uint32_t ab = f16 ? 0u : 1u;                  // operand format: 0 f16, 1 bf16
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(TC_BM >> 4) << 24);
 }
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
@@ -126,6 +128,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Eight e4m3 values (one 8-byte word pair) as eight f16 values, exactly (one
+// conversion per pair; every e4m3 value is an f16 normal or zero).
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 v) {
+  const uint32_t w[2] = {v.x, v.y};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[i] >> (16 * h)) & 0xFFFF), __NV_E4M3);
+      o[2 * i + h] = (uint32_t)hr.x | ((uint32_t)hr.y << 16);
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Eight e4m3 values (one 8-byte word pair) as eight bf16 values.
 __device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 v) {
   const uint32_t w[2] = {v.x, v.y};
@@ -144,7 +162,7 @@ __device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 v) {
 
 constexpr int TC_NCONVW = 6;          // FP8 converter warps (warps 2..7)
 
-// Stage s of the FP8 form: e4m3 staging [128 rows][64 B] -> bf16 tile [128
+// Stage s of the FP8 form: e4m3 staging [128 rows][64 B] -> f16 tile [128
 // rows][128 B] with the 128-byte swizzle (16-byte piece c of row r at
 // (c ^ (r % 8)) * 16). The converter threads take the 1024 pieces round
 // robin; a thread loads all its pieces before widening any.
@@ -159,7 +177,7 @@ __device__ __forceinline__ void convert_tile(const unsigned char* stg, unsigned 
 #pragma unroll
   for (int j = 0; j < NI; ++j) {
     const int i = t + NT * j, r = i >> 3, c = i & 7;
-    if (i < 1024) *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = e4m3x8_to_bf16x8(v[j]);
+    if (i < 1024) *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = e4m3x8_to_f16x8(v[j]);
   }
 }
 
@@ -285,7 +303,7 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer ----
-    const uint32_t idesc = tc_idesc(NP);
+    const uint32_t idesc = tc_idesc(NP, F8);
     const uint64_t d0 = sw128_desc(smem_u32(stages));
     bool ok = true;
     int kstep = 0;                                    // 16-wide K steps issued so far
@@ -363,8 +381,10 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const int m = warp * 32 + lane;                     // row within the tile
   const int col = mt * TC_BM + m;                     // output feature (row within the group)
-  const float sc = (P.scale && have && warp < 4) ? P.scale[wrow + m] : 1.f;
-  const float sc2 = (DUAL && P.scale2 && have && warp < 4) ? P.scale2[wrow + m] : 1.f;
+  // e4m3 weights multiply f16 parts of 256 x: the epilogue takes the 256 out (exactly)
+  const float osc = F8 ? 1.0f / F16_OP_SCALE : 1.0f;
+  const float sc = ((P.scale && have && warp < 4) ? P.scale[wrow + m] : 1.f) * osc;
+  const float sc2 = ((DUAL && P.scale2 && have && warp < 4) ? P.scale2[wrow + m] : 1.f) * osc;
   const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   __shared__ float red_v[4][TC_NSUB];
   __shared__ int red_i[4][TC_NSUB];
@@ -473,9 +493,10 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
         P.out_f32[r * P.ldo + col] = val;
       } else if (DUAL && P.epi == TC_SWIGLU) {
         const float hv = silu(val) * (u2[j] * sc2);
-        const uint16_t hi = f_to_bf16(hv);
-        P.out_bf16[r * P.ldo + col] = hi;
-        if (P.out_bf16_lo) P.out_bf16_lo[r * P.ldo + col] = f_to_bf16(hv - bf16_to_f(hi));
+        uint16_t pp[2];
+        split_parts(hv, F8, 2, pp);                    // operand parts of the (same-format) down GEMM
+        P.out_bf16[r * P.ldo + col] = pp[0];
+        if (P.out_bf16_lo) P.out_bf16_lo[r * P.ldo + col] = pp[1];
       }
     }
   };

@@ -8,11 +8,13 @@
 
 namespace spec {
 
-// v = (x[t][k] * inv_t) * gamma[k] as hi = bf16(v), lo = bf16(v - hi) and,
-// when out_lo2 is given, lo2 = bf16(v - hi - lo); one block per row. The
-// inverse RMS uses row_inv_rms, the arithmetic of every other RMSNorm here.
+// v = (x[t][k] * inv_t) * gamma[k] as operand parts hi, lo and, when out_lo2
+// is given, lo2 (split_parts: bf16 parts of v, or with f16 f16 parts of
+// 256 v); one block per row. The inverse RMS uses row_inv_rms, the arithmetic
+// of every other RMSNorm here.
 __global__ void k_norm_bf16(Dims D, const float* __restrict__ x, const float* __restrict__ gamma,
-                            uint16_t* __restrict__ out, uint16_t* __restrict__ out_lo, uint16_t* __restrict__ out_lo2) {
+                            uint16_t* __restrict__ out, uint16_t* __restrict__ out_lo, uint16_t* __restrict__ out_lo2,
+                            int f16) {
   __shared__ float inv[1];
   pdl_wait();
   pdl_trigger();
@@ -23,12 +25,11 @@ __global__ void k_norm_bf16(Dims D, const float* __restrict__ x, const float* __
   const float s = inv[0];
   for (int k = threadIdx.x; k < D.h; k += blockDim.x) {
     const float v = (xr[k] * s) * gamma[k];
-    const uint16_t hi = f_to_bf16(v);
-    const float r = v - bf16_to_f(hi);
-    const uint16_t lo = f_to_bf16(r);
-    out[(size_t)t * D.h + k] = hi;
-    out_lo[(size_t)t * D.h + k] = lo;
-    if (out_lo2) out_lo2[(size_t)t * D.h + k] = f_to_bf16(r - bf16_to_f(lo));
+    uint16_t p[3];
+    split_parts(v, f16, out_lo2 ? 3 : 2, p);
+    out[(size_t)t * D.h + k] = p[0];
+    out_lo[(size_t)t * D.h + k] = p[1];
+    if (out_lo2) out_lo2[(size_t)t * D.h + k] = p[2];
   }
 }
 
@@ -81,7 +82,7 @@ __global__ void k_rope_kv(Dims D, DevState S, StepBuf B, int layer) {
   }
 }
 
-// xperm[i] = u[perm[i] / NS] as hi + lo bf16, for the T * NS permuted pairs.
+// xperm[i] = u[perm[i] / NS] as hi + lo operand parts, for the T * NS permuted pairs.
 __global__ void k_gather_bf16(Dims D, StepBuf B, int T) {
   pdl_wait();
   pdl_trigger();
@@ -90,9 +91,10 @@ __global__ void k_gather_bf16(Dims D, StepBuf B, int T) {
   const int row = B.perm[i] / D.NS;
   const float* u = B.u + (size_t)row * D.h;
   for (int k = threadIdx.x; k < D.h; k += blockDim.x) {
-    const uint16_t hi = f_to_bf16(u[k]);
-    B.xperm[(size_t)i * D.h + k] = hi;
-    B.xperm_lo[(size_t)i * D.h + k] = f_to_bf16(u[k] - bf16_to_f(hi));
+    uint16_t p[2];
+    split_parts(u[k], D.op_f16, 2, p);
+    B.xperm[(size_t)i * D.h + k] = p[0];
+    B.xperm_lo[(size_t)i * D.h + k] = p[1];
   }
 }
 
@@ -124,8 +126,8 @@ __global__ void k_argmax_commit(Dims D, DevState S, StepBuf B, int T, int ld, in
 }
 
 void launch_norm_bf16(const Dims& D, const float* x, const float* gamma, uint16_t* out, uint16_t* out_lo,
-                      uint16_t* out_lo2, int T, cudaStream_t st) {
-  launch_k(k_norm_bf16, dim3(T), dim3(256), 0, st, D, x, gamma, out, out_lo, out_lo2);
+                      uint16_t* out_lo2, int T, int f16, cudaStream_t st) {
+  launch_k(k_norm_bf16, dim3(T), dim3(256), 0, st, D, x, gamma, out, out_lo, out_lo2, f16);
 }
 
 void launch_rope_kv(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, cudaStream_t st) {

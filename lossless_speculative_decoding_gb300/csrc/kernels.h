@@ -28,6 +28,7 @@ struct Dims {
   int L, h, Hq, Hkv, d, E, k, S, inter, V;
   int wdtype;            // 0 f32, 1 bf16, 2 fp8 (attention + experts)
   int act_f32;           // KV cache / embeddings / LM head in f32 (else bf16)
+  int op_f16;            // operands of the e4m3-weight tensor-core GEMMs are f16 parts of 256 x (else bf16 parts of x)
   int P;                 // page size
   int max_pages;         // block-table row length
   int max_ctx;
@@ -182,7 +183,7 @@ void launch_tc_gemm(const TcMaps& maps, const TcParams& P, int m_tiles, int grou
 cudaError_t configure_tc_kernels();
 // out_lo2 (nullable): the third part bf16(v - hi - lo).
 void launch_norm_bf16(const Dims& D, const float* x, const float* gamma, uint16_t* out, uint16_t* out_lo,
-                      uint16_t* out_lo2, int T, cudaStream_t st);
+                      uint16_t* out_lo2, int T, int f16, cudaStream_t st);
 void launch_rope_kv(const Dims& D, const DevState& S, const StepBuf& B, int layer, int T, cudaStream_t st);
 void launch_gather_bf16(const Dims& D, const StepBuf& B, int T, cudaStream_t st);
 void launch_argmax_commit(const Dims& D, const DevState& S, const StepBuf& B, int T, int ld, bool commit, int n_seq,

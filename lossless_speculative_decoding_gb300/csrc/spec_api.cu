@@ -290,7 +290,7 @@ struct spec_model {
       const LayerW& W = layers[l];
       if (use_tc) {
         run_k(p, KC_QKV, [&] {
-          launch_norm_bf16(D, cur, W.attn_norm, B.xn_bf16, B.xn_lo, B.xn_lo2, T, stream);
+          launch_norm_bf16(D, cur, W.attn_norm, B.xn_bf16, B.xn_lo, B.xn_lo2, T, D.op_f16, stream);
           tc_dense(W.w_qkv, tc_xn, tc_xn_lo, D.h, qkv_rows, T, TC_STORE, B.qkv, qkv_rows, W.s_qkv, &tc_xn_lo2);
           launch_rope_kv(D, S, B, l, T, stream);
         });
@@ -330,7 +330,7 @@ struct spec_model {
       launch_lmhead_step(D, S, B, lm_head, final_norm, x, T, logits_dbg, commit, n_seq, K, stream);
       return;
     }
-    launch_norm_bf16(D, x, final_norm, B.xn_bf16, B.xn_lo, nullptr, T, stream);
+    launch_norm_bf16(D, x, final_norm, B.xn_bf16, B.xn_lo, nullptr, T, 0, stream);
     if (logits_dbg) tc_dense(lm_head, tc_xn, tc_xn_lo, D.h, D.V, T, TC_STORE, logits_dbg, D.V);
     tc_dense(lm_head, tc_xn, tc_xn_lo, D.h, D.V, T, TC_ARGMAX, nullptr, 0);
     launch_argmax_commit(D, S, B, T, D.V / 128, commit, n_seq, K, stream);
@@ -524,6 +524,7 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
     const bool shapes = D.h % 128 == 0 && qkv_rows % 128 == 0 && D.inter % 128 == 0 && D.V % 128 == 0 &&
                         (D.Hq * D.d) % 64 == 0 && D.h % 64 == 0 && D.inter % 64 == 0;
     m->use_tc = (c.wdtype == SPEC_BF16 || c.wdtype == SPEC_FP8) && c.max_batch * m->R > 8 && shapes;
+    D.op_f16 = m->use_tc && c.wdtype == SPEC_FP8 ? 1 : 0;
   }
   if (m->use_tc) {
     const int qkv_rows = (D.Hq + 2 * D.Hkv) * D.d;
