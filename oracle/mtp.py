@@ -19,6 +19,8 @@ Readings of what the section leaves open:
   + FFN(RMSNorm(.)). Its attention is causal over the rows of the same depth:
   the equations define u on a grid of (position, depth), and row p of depth k
   attends to rows <= p of depth k, at RoPE position p.
+* The block's keys and values are stored like the decoder's KV cache: bf16
+  for bf16 and e4m3-weight models, f32 for f32 models.
 * N_e and N_h are RMSNorms with their own gains; P is [h, 2h] applied to the
   concatenation [N_e(e); N_h(a)]; b_p is the decoder's final-normed state (the
   LM head's input).
@@ -37,7 +39,7 @@ from typing import Dict, List, Optional, Sequence, Tuple
 
 import numpy as np
 
-from .model import (KVCache, OracleModel, _silu, accept, argmax_lowest, attention_rows, forward,
+from .model import (KVCache, OracleModel, _silu, accept, argmax_lowest, attention_rows, forward, round_bf16,
                     prompt_embeddings, rms_norm, rope, verify_rows)
 
 
@@ -69,6 +71,8 @@ def block(head: MtpHead, z: np.ndarray, positions: np.ndarray,
     if cache is None:
         cache = (np.zeros((0, hk, d), np.float32), np.zeros((0, hk, d), np.float32))
         first_pos = int(positions[0])
+    if cfg.wdtype != 0:       # the block's cache is held in the model's storage type, like the decoder's
+        k, v = round_bf16(k), round_bf16(v)
     kk = np.concatenate([cache[0], k])
     vv = np.concatenate([cache[1], v])
     o = attention_rows(q, kk, vv, positions - first_pos, hk)     # key j sits at first_pos + j

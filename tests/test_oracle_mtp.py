@@ -144,3 +144,31 @@ def test_drafts_follow_the_grid_on_teacher_forced_states(head):
     # the hidden rows are the LM head's inputs: they reproduce the logits
     np.testing.assert_allclose(tr["hidden"] @ m.lm_head.T, lg, rtol=1e-5, atol=1e-5)
     assert len(d) == K
+
+
+def test_block_cache_is_held_in_the_storage_type():
+    """The block's keys and values are stored like the decoder's cache: for a
+    bf16 model they are the f32 model's keys and values rounded to bf16 (same
+    weights), and a single row attends to exactly its own stored value."""
+    cfg16 = syn.scaled(CFG, name="tiny-bf16", wdtype=syn.BF16)
+    m16 = oracle.OracleModel(syn.generate_weights(cfg16, 0))
+    h16 = mtp.MtpHead(m16, syn.generate_mtp_weights(cfg16, 3, norm_gamma_std=0.1))
+    h32 = mtp.MtpHead.__new__(mtp.MtpHead)
+    h32.cfg, h32.tok_embed, h32.final_norm, h32.lm_head, h32.w = CFG, h16.tok_embed, h16.final_norm, h16.lm_head, h16.w
+    z = np.random.default_rng(9).standard_normal((5, CFG.hidden)).astype(np.float32)
+    pos = np.arange(3, 8)
+    _, (k16, v16) = mtp.block(h16, z, pos)
+    _, (k32, v32) = mtp.block(h32, z, pos)
+    assert np.array_equal(k16, oracle.round_bf16(k32)) and np.array_equal(v16, oracle.round_bf16(v32))
+    assert not np.array_equal(k32, k16)
+    assert (k16.view(np.uint32) & 0xFFFF == 0).all() and (v16.view(np.uint32) & 0xFFFF == 0).all()
+    # one row: softmax over one key is 1, so the attention output is that key's stored value
+    y1, (_, v1) = mtp.block(h16, z[:1], pos[:1])
+    w = h16.w
+    hq, hk, d = CFG.n_q_heads, CFG.n_kv_heads, CFG.head_dim
+    o = np.repeat(v1.astype(np.float64), hq // hk, axis=1).reshape(1, hq * d)
+    x = z[:1].astype(np.float64) + o @ w["w_o"].T.astype(np.float64)
+    u = _rms(x, w["ffn_norm"])
+    g = u @ w["w_gate"].T.astype(np.float64)
+    x = x + ((g / (1 + np.exp(-g))) * (u @ w["w_up"].T.astype(np.float64))) @ w["w_down"].T.astype(np.float64)
+    np.testing.assert_allclose(y1, x, rtol=1e-4, atol=1e-4)
