@@ -607,7 +607,7 @@ def measure(wl_name: str, args, primary: bool) -> dict:
             "value": committed_all / (ms_all * 1e-3),
             "ms_per_step": ms_per_step,
             "dtype": {syn.F32: "f32", syn.BF16: "bf16",
-                      syn.FP8: "e4m3 weights widened to bf16; activations bf16 hi+lo pairs; fp32 accumulate"}[cfg.wdtype],
+                      syn.FP8: "e4m3 weights widened to f16; activations f16 hi+lo parts; fp32 accumulate"}[cfg.wdtype],
             "config": {"workload": wl.name, "model": cfg.name, "layers": cfg.n_layers, "batch": NB, "n_draft": K,
                        "drafter": f"{wl.drafter} q={wl.q}", "rows_per_step": T,
                        "prompt_rows": [p.length for p in prompts0] if NB > 1 else prompts0[0].length,

@@ -184,6 +184,47 @@ int spec_debug_logits(spec_model* m, int n_seq, const int32_t* seq_ids,
 /* Number of kernel launches one verify step of n_seq sequences enqueues. */
 int spec_step_launches(spec_model* m, int n_seq);
 
+/* ---- FastMTP draft head ----------------------------------------------------
+ * "Jina-OCR-v1: efficient document parsing with speculative decoding and
+ * dense verifiable rewards", section 3.1: one shared draft block applied
+ * recursively, K steps per verify step. For position p and depth k, with b_p
+ * the decoder's final-normed state of row p and N_o the decoder's final norm:
+ *   a_p^(1) = b_p,  a_p^(k) = u_(p-1)^(k-1),
+ *   z_p^(k) = P [N_e(E(x_(p+1))) ; N_h(a_p^(k))],
+ *   u_p^(k) = N_o(B(z_p^(k); RoPE position p)),  d_k = argmax W_lm u_(p+k-1)^(k)
+ * where x_(p+1), ... are the committed tokens followed by d_1..d_(k-1). E, N_o
+ * and W_lm are the decoder's (tied). B is one pre-norm decoder layer of the
+ * decoder's attention shape with a dense SwiGLU FFN of width `inter`, causal
+ * over the rows of its own depth; its keys and values are stored like the
+ * decoder's (bf16, f32 for an f32 decoder). Depth k's rows start at row
+ * p0 + k - 1, p0 the last visual row of the prompt (0 without visual rows).
+ * Ties keep the lowest token id.
+ *
+ * spec_mtp_init attaches a head to a model with max_draft <= 4.
+ * host_tensors[13] (host memory, copied; the caller keeps ownership), row-major:
+ *   0 tok_embed, 1 final_norm, 2 lm_head: the decoder's tensors 0..2 as given
+ *     to spec_init_model;
+ *   3 enorm [hidden] f32, 4 hnorm [hidden] f32,
+ *   5 eh_proj [hidden][2 hidden], 6 attn_norm [hidden] f32,
+ *   7 w_qkv [(Hq + 2 Hkv) head_dim][hidden], 8 w_o [hidden][Hq head_dim],
+ *   9 ffn_norm [hidden] f32, 10 w_gate [inter][hidden], 11 w_up [inter][hidden],
+ *   12 w_down [hidden][inter];
+ *   matrices in f32 for an f32 decoder, else bf16 (also for e4m3 decoders).
+ * Errors: SPEC_ERR_STATE if the model already has a head; SPEC_ERR_UNSUPPORTED
+ * for max_draft > 4; SPEC_ERR_NOMEM.
+ *
+ * spec_mtp_draft writes d_1..d_K (1 <= K <= max_draft) for sequence seq_id
+ * after its committed tokens to out_drafts[K] (host). Each depth's cache
+ * keeps the committed rows; the rows made from drafts are recomputed by the
+ * next call. Valid right after spec_prefill (prompt tail <= 256 rows after
+ * p0) or right after the host-mode verify step that committed the new tokens
+ * (any step call in between, or a _dev step, makes it SPEC_ERR_STATE; so does
+ * a second draft with no new committed token); sequences prefilled with a
+ * shared prefix give SPEC_ERR_UNSUPPORTED. The call synchronizes the model's
+ * stream once. */
+int spec_mtp_init(spec_model* m, const void* const* host_tensors, int inter);
+int spec_mtp_draft(spec_model* m, int32_t seq_id, int K, int32_t* out_drafts);
+
 /* ---- profiling ------------------------------------------------------------ */
 /* Per kernel class: summed device time (ms, CUDA events on the model's stream
  * around each launch), launch count, and work units (active experts for the

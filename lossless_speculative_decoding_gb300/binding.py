@@ -17,6 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspec.so")
 
 SPEC_F32, SPEC_BF16, SPEC_FP8 = 0, 1, 2
+SPEC_ERR_ARG, SPEC_ERR_NO_PAGES, SPEC_ERR_CUDA, SPEC_ERR_STATE, SPEC_ERR_NOMEM, SPEC_ERR_UNSUPPORTED = -1, -2, -3, -4, -5, -6
 ERRORS = {-1: "SPEC_ERR_ARG", -2: "SPEC_ERR_NO_PAGES", -3: "SPEC_ERR_CUDA", -4: "SPEC_ERR_STATE",
           -5: "SPEC_ERR_NOMEM", -6: "SPEC_ERR_UNSUPPORTED"}
 
@@ -70,6 +71,8 @@ _SIGS = [
     ("spec_free_pages", ctypes.c_int, [ctypes.c_void_p]),
     ("spec_debug_logits", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, _I32P, _I32P, ctypes.c_void_p]),
     ("spec_step_launches", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    ("spec_mtp_init", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
+    ("spec_mtp_draft", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int, _I32P]),
     ("spec_profile_steps_dev", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                               ctypes.POINTER(spec_kernel_stat), ctypes.c_int]),
@@ -257,6 +260,21 @@ def spec_debug_logits(m: int, seq_ids, drafts, logits_dev) -> None:
 
 def spec_step_launches(m: int, n_seq: int) -> int:
     return _check(lib().spec_step_launches(m, n_seq))
+
+
+def spec_mtp_init(m: int, host_tensors: Sequence[np.ndarray], inter: int) -> None:
+    """host_tensors: the 13 arrays in the order of spec.h (encoded as stored)."""
+    if len(host_tensors) != 13:
+        raise ValueError(f"expected 13 tensors, got {len(host_tensors)}")
+    arrs = [np.ascontiguousarray(a) for a in host_tensors]
+    ptrs = (ctypes.c_void_p * 13)(*[a.ctypes.data for a in arrs])
+    _check(lib().spec_mtp_init(m, ptrs, inter))
+
+
+def spec_mtp_draft(m: int, seq_id: int, K: int) -> np.ndarray:
+    out = np.zeros(K, np.int32)
+    _check(lib().spec_mtp_draft(m, seq_id, K, _p(out)))
+    return out
 
 
 def spec_profile_steps_dev(m: int, n_seq: int, seq_ids_dev, drafts_dev, n_draft_dev, n_steps: int,

@@ -106,7 +106,8 @@ __global__ void __launch_bounds__(256, SBPS) k_qkv_s(Dims D, DevState S, StepBuf
       const int dim = (r < 2) ? j : j + half;
       float outv = val;
       if (head < D.Hq + D.Hkv) {
-        const float c = S.rope_cos[(size_t)pos * half + j], s = S.rope_sin[(size_t)pos * half + j];
+        const int rp = B.row_rope ? B.row_rope[row] : pos;
+        const float c = S.rope_cos[(size_t)rp * half + j], s = S.rope_sin[(size_t)rp * half + j];
         // first half: a cos - b sin; second half: b cos + a sin (a = first-half value)
         outv = (r < 2) ? (val * c - partner * s) : (val * c + partner * s);
       }
@@ -645,7 +646,8 @@ __global__ void __launch_bounds__(256, SBPS) k_qkv_m(Dims D, DevState S, StepBuf
         if (pos < 0 || pos >= D.max_ctx) { atomicOr(S.err, DERR_POS); continue; }
         float o0 = a[e], o1 = b[e];
         if (head < D.Hq + D.Hkv) {
-          const float cs = S.rope_cos[(size_t)pos * half + j], sn = S.rope_sin[(size_t)pos * half + j];
+          const int rp = B.row_rope ? B.row_rope[row] : pos;
+          const float cs = S.rope_cos[(size_t)rp * half + j], sn = S.rope_sin[(size_t)rp * half + j];
           o0 = a[e] * cs - b[e] * sn;
           o1 = b[e] * cs + a[e] * sn;
         }

@@ -64,7 +64,8 @@ __global__ void k_rope_kv(Dims D, DevState S, StepBuf B, int layer) {
     const float a = src[i], b = src[i + half];
     float o0 = a, o1 = b;
     if (!is_v) {
-      const float c = S.rope_cos[(size_t)pos * half + i], s = S.rope_sin[(size_t)pos * half + i];
+      const int rp = B.row_rope ? B.row_rope[t] : pos;
+      const float c = S.rope_cos[(size_t)rp * half + i], s = S.rope_sin[(size_t)rp * half + i];
       o0 = a * c - b * s;
       o1 = b * c + a * s;
     }

@@ -54,6 +54,7 @@ struct DevState {
 // Per-step scratch (sized for the largest T the model runs).
 struct StepBuf {
   int* row_tok; int* row_pos; int* row_seq; int* row_src;
+  int* row_rope;     // RoPE position of a row when it differs from its cache index (null: the same)
   float* x;          // [T, h] residual stream
   float* q;          // [T, Hq, d]
   float* att_o;      // [T, Hq, n_chunk_max, d] partial outputs
@@ -196,6 +197,13 @@ void launch_commit(const Dims& D, const DevState& S, const StepBuf& B, int n_seq
 void launch_stage_dev(const StepBuf& B, int n_seq, int K, const int* seq_ids, const int* drafts,
                       const int* n_draft, int* out_acc, int* out_bonus, cudaStream_t st);
 int launches_per_step(const Dims& D, int T);
+// FastMTP draft-block input rows (ops_mtp.cu): cat = [N_e(E tok) ; N_h(N_o src)],
+// z = P cat for n_rows rows (src[r] null: a padding row; tok[r] = -(j + 1):
+// the token is drafts[j]).
+void launch_mtp_input(const Dims& D, const int* tok, const float* const* src, const int* drafts, int n_rows,
+                      const void* tok_embed,
+                      const float* enorm, const float* final_norm, const float* hnorm, const void* P, float* cat,
+                      float* z, cudaStream_t st);
 // Record `msg` as the calling thread's last error (spec_last_error) and return code.
 int set_last_error(int code, const char* msg);
 // Programmatic dependent launch is used for every step kernel unless this

@@ -107,6 +107,37 @@ struct Prefix {
   int full_pages = 0;
 };
 
+// FastMTP draft head attached to a model ("Jina-OCR-v1", section 3.1). The
+// shared draft block runs as an internal one-layer dense model `blk` whose
+// sequence slot seq * Kmax + (k - 1) holds depth k's cache of sequence seq:
+// row r of depth k sits at cache index r - (p0 + k - 1) and is rotated at
+// absolute position r. Per call, every depth takes its newly committed rows
+// (kept) and k - 1 speculative rows (recomputed by the next call), in passes
+// of R rows (padding rows after the real ones).
+struct MtpHead {
+  spec_model* blk = nullptr;
+  int Kmax = 0, R = 0, B0 = 0, ymax = 0;
+  float* enorm = nullptr;
+  float* hnorm = nullptr;
+  void* P = nullptr;                    // eh_proj [h][2h]
+  float* cat = nullptr;                 // [R][2h]
+  float* Y = nullptr;                   // [Kmax][ymax][h] outputs (before N_o) of one call's rows, per depth
+  float* ylast = nullptr;               // [max_seqs][Kmax][h] output of each depth's last committed row
+  float* b0 = nullptr;                  // [max_seqs][B0][h] decoder states of prompt rows p0..
+  int* d_meta = nullptr;                // one pass: [4][R] tokens, cache index, RoPE position, slot; [R] source rows
+  int* d_drafts = nullptr;              // [Kmax] drafts of the call (tokens -(j + 1) read draft j)
+  int pass_ints = 0, max_pass = 0;      // ints per pass (meta + pointers); passes per call
+  int* pin = nullptr;                   // pinned staging: max_pass passes
+  std::vector<int> p0, p_done, b0_rows, last_pos0, last_idx;
+  std::vector<std::vector<int32_t>> prompt_tok;   // token id per prompt position (0 for visual rows)
+  std::vector<void*> allocs;
+  ~MtpHead() {
+    if (blk) spec_free_model(blk);
+    for (void* q : allocs) cudaFree(q);
+    if (pin) cudaFreeHost(pin);
+  }
+};
+
 }  // namespace
 
 int spec::set_last_error(int code, const char* msg) { return fail(code, msg); }
@@ -172,7 +203,10 @@ struct spec_model {
   CUtensorMap tc_xn_lo, tc_o_lo, tc_xperm_lo, tc_hperm_lo;     //              lo
   CUtensorMap tc_xn_lo2;                                       //              lo2 (QKV input)
 
+  MtpHead* mtp = nullptr;                 // draft head (spec_mtp_init), null without one
+
   ~spec_model() {
+    delete mtp;
     for (auto& g : graphs) cudaGraphExecDestroy(g.second);
     if (own_stream) cudaStreamDestroy(stream);
     for (void* p : allocs) cudaFree(p);
@@ -362,6 +396,12 @@ struct spec_model {
 
   bool seq_ok(int s) const { return s >= 0 && s < cfg.max_seqs && busy[s]; }
 };
+
+// The decoder's step buffer now holds other rows: no sequence can be drafted
+// from the last step's states any more.
+static void mtp_forget_steps(spec_model* m) {
+  if (m->mtp) std::fill(m->mtp->last_idx.begin(), m->mtp->last_idx.end(), -1);
+}
 
 // ---------------------------------------------------------------------------
 extern "C" {
@@ -646,6 +686,14 @@ static int run_prefill_rows(spec_model* m, int slot, const std::vector<int32_t>&
     CU(cudaMemcpyAsync(m->B.row_src, m->pin_in, T * sizeof(int32_t), cudaMemcpyHostToDevice, m->stream));
     launch_assemble_prefill(m->D, m->S, m->B, m->tok_embed, vis, slot, start + c0, T, m->stream);
     const float* xf = m->enqueue_layers(T, T);
+    if (m->mtp && slot < m->cfg.max_seqs && m->mtp->p0[slot] >= 0) {
+      // the draft head's first call needs the decoder states of rows p0.. (kept while they fit)
+      MtpHead& H = *m->mtp;
+      const int a = std::max(H.p0[slot], start + c0), b = std::min(start + c0 + T, H.p0[slot] + H.B0);
+      if (b > a)
+        CU(cudaMemcpyAsync(H.b0 + ((size_t)slot * H.B0 + (a - H.p0[slot])) * m->D.h, xf + (size_t)(a - start - c0) * m->D.h,
+                           (size_t)(b - a) * m->D.h * sizeof(float), cudaMemcpyDeviceToDevice, m->stream));
+    }
     if (c0 + T == n && out_tok) {
       m->enqueue_lmhead(xf + (size_t)(T - 1) * m->D.h, 1, nullptr, false, 0);
       CU(cudaMemcpyAsync(m->pin_out, m->B.g, sizeof(int32_t), cudaMemcpyDeviceToHost, m->stream));
@@ -675,6 +723,7 @@ int spec_register_prefix(spec_model* m, const int32_t* tok, int n_tok, int32_t* 
   if (rc) return fail(rc, "prefix: KV pool exhausted");
   if ((rc = m->push_table(slot))) { m->pool->release(slot); return rc; }
   std::vector<int32_t> src(tok, tok + n_tok);
+  mtp_forget_steps(m);
   rc = run_prefill_rows(m, slot, src, 0, nullptr, nullptr);
   if (rc) { m->pool->release(slot); m->push_table(slot); return rc; }
   Prefix& p = m->prefixes[id];
@@ -736,7 +785,20 @@ int spec_prefill(spec_model* m, int32_t seq_id, int32_t prefix_id, const void* v
     else if (p < n_pre + n_vis) src.push_back(-(p - n_pre) - 1);
     else src.push_back(tok[p - n_pre - n_vis]);
   }
+  if (m->mtp) {
+    // the head's grid starts at the last visual row (row 0 without visual rows);
+    // sequences with a shared prefix are not drafted by the head
+    MtpHead& H = *m->mtp;
+    H.p0[seq_id] = pre ? -1 : std::max(n_vis - 1, 0);
+    H.p_done[seq_id] = H.p0[seq_id] - 1;
+    H.b0_rows[seq_id] = std::max(0, std::min(H.B0, len - std::max(H.p0[seq_id], 0)));
+    H.last_idx[seq_id] = -1;
+    H.prompt_tok[seq_id].assign(len, 0);
+    for (int i = 0; i < n_tok; ++i) H.prompt_tok[seq_id][n_pre + n_vis + i] = tok[i];
+    for (int k = 0; k < H.Kmax; ++k) H.blk->pool->release(seq_id * H.Kmax + k);
+  }
   int32_t first = -1;
+  mtp_forget_steps(m);
   rc = run_prefill_rows(m, seq_id, src, start, vis_embeds_dev, &first);
   if (rc) { pool.release(seq_id); m->push_table(seq_id); return rc; }
   m->busy[seq_id] = 1;
@@ -794,6 +856,7 @@ static int verify_host(spec_model* m, int n_seq, const int32_t* seq_ids, const i
                      m->stream));
   m->h2d_bytes += (int64_t)(4 + m->step_in_n) * sizeof(int32_t);
   if (logits_dev) {
+    mtp_forget_steps(m);
     m->enqueue_verify(n_seq, logits_dev, false);
     CU(cudaStreamSynchronize(m->stream));
     CU(cudaGetLastError());
@@ -813,8 +876,13 @@ static int verify_host(spec_model* m, int n_seq, const int32_t* seq_ids, const i
     return fail(SPEC_ERR_STATE, "device error bits " + std::to_string(m->pin_out[2 * mb]) +
                                     " (1 page, 2 token, 4 position out of range); step not committed on the host");
   }
+  mtp_forget_steps(m);
   for (int s = 0; s < n_seq; ++s) {
     const int q = seq_ids[s];
+    if (m->mtp) {   // the draft head reads this step's rows of q: row 0 at position seq_len_h[q]
+      m->mtp->last_idx[q] = s;
+      m->mtp->last_pos0[q] = m->seq_len_h[q];
+    }
     const int a = m->pin_out[s], bonus = m->pin_out[mb + s];
     const int nd = n_draft ? n_draft[s] : K;
     for (int j = 0; j < a; ++j) m->gen[q].push_back(drafts[s * K + j]);
@@ -866,6 +934,7 @@ int spec_verify_step_batch_dev(spec_model* m, int n_seq, const int32_t* seq_ids_
                    m->stream);
   CU(cudaGraphLaunch(ge, m->stream));
   m->host_dirty = true;
+  mtp_forget_steps(m);
   return SPEC_OK;
 }
 
@@ -988,6 +1057,12 @@ int spec_release_seq(spec_model* m, int32_t seq_id) {
   if (!m || !m->seq_ok(seq_id)) return fail(SPEC_ERR_ARG, "sequence not active");
   if (m->host_dirty) return fail(SPEC_ERR_STATE, "call spec_sync_seqs after device-resident steps");
   m->pool->release(seq_id);
+  if (m->mtp) {   // the draft head's caches of this sequence
+    MtpHead& H = *m->mtp;
+    for (int k = 0; k < H.Kmax; ++k) H.blk->pool->release(seq_id * H.Kmax + k);
+    H.p0[seq_id] = -1;
+    H.last_idx[seq_id] = -1;
+  }
   m->busy[seq_id] = 0;
   m->seq_len_h[seq_id] = 0;
   m->keep_h[seq_id] = 0;
@@ -1037,6 +1112,175 @@ int spec_step_launches(spec_model* m, int n_seq) {
   if (m->use_tc)   // per layer: norm, QKV, RoPE/KV, attention, O, router, gather, gate/up, down, combine
     return 1 + m->D.L * 10 + 3 + merge;
   return launches_per_step(m->D, n_seq * m->R) + merge;
+}
+
+// ---- FastMTP draft head -----------------------------------------------------
+int spec_mtp_init(spec_model* m, const void* const* host_tensors, int inter) {
+  if (!m || !host_tensors || inter < 4) return fail(SPEC_ERR_ARG, "bad draft-head arguments");
+  if (m->mtp) return fail(SPEC_ERR_STATE, "the model already has a draft head");
+  if (m->K < 1) return fail(SPEC_ERR_ARG, "a draft head needs max_draft >= 1");
+  for (int i = 0; i < 13; ++i)
+    if (!host_tensors[i]) return fail(SPEC_ERR_ARG, "missing draft-head tensor " + std::to_string(i));
+  const spec_config& c = m->cfg;
+  std::unique_ptr<MtpHead> H(new MtpHead());
+  H->Kmax = m->K;
+  H->R = 2 * m->K;                      // a depth's rows per call: a + k <= 2 K
+  H->B0 = 256;
+  H->ymax = H->B0 + 2 * m->K;
+  H->pass_ints = 4 * H->R + H->R * (int)(sizeof(float*) / sizeof(int));
+  H->max_pass = H->Kmax * ((H->ymax + H->R - 1) / H->R);
+  spec_config bc = c;                   // the draft block: one layer, dense SwiGLU of width `inter`
+  bc.n_layers = 1;
+  bc.n_experts = 0;
+  bc.top_k = 0;
+  bc.n_shared = 1;
+  bc.inter = inter;
+  bc.wdtype = c.wdtype == SPEC_F32 ? SPEC_F32 : SPEC_BF16;
+  bc.max_seqs = c.max_seqs * m->K;
+  bc.max_batch = 1;
+  bc.max_draft = H->R - 1;
+  bc.max_ctx = c.max_ctx + 2 * H->R;
+  bc.n_pages = bc.max_seqs * ((bc.max_ctx + c.page_size - 1) / c.page_size + 1) + 8;
+  bc.prefill_chunk = H->R;
+  // tensor list of the block model: tok_embed, final_norm, lm_head (tied), then one layer
+  const void* null = nullptr;
+  const void* bt[N_GLOBAL + PER_LAYER] = {host_tensors[0], host_tensors[1], host_tensors[2],
+                                          host_tensors[6], host_tensors[7], null, host_tensors[8], null,
+                                          host_tensors[9], null, host_tensors[10], null, host_tensors[11], null,
+                                          host_tensors[12], null};
+  spec_model* blk = nullptr;
+  int rc = spec_init_model(&bc, bt, reinterpret_cast<uintptr_t>(m->stream), &blk);
+  if (rc) return rc;
+  H->blk = blk;
+  if (blk->use_tc) return fail(SPEC_ERR_UNSUPPORTED, "draft head: more than 4 drafts per step");
+  const int h = c.hidden, welt = c.wdtype == SPEC_F32 ? 4 : 2;
+  auto dal = [&](void** q, size_t bytes) -> int {
+    if (cudaMalloc(q, bytes ? bytes : 1) != cudaSuccess) return fail(SPEC_ERR_NOMEM, "draft head allocation");
+    H->allocs.push_back(*q);
+    return SPEC_OK;
+  };
+  if ((rc = dal((void**)&H->enorm, h * 4)) || (rc = dal((void**)&H->hnorm, h * 4)) ||
+      (rc = dal(&H->P, (size_t)h * 2 * h * welt)) || (rc = dal((void**)&H->cat, (size_t)H->R * 2 * h * 4)) ||
+      (rc = dal((void**)&H->Y, (size_t)H->Kmax * H->ymax * h * 4)) ||
+      (rc = dal((void**)&H->ylast, (size_t)c.max_seqs * H->Kmax * h * 4)) ||
+      (rc = dal((void**)&H->b0, (size_t)c.max_seqs * H->B0 * h * 4)) ||
+      (rc = dal((void**)&H->d_meta, (size_t)H->pass_ints * 4)) || (rc = dal((void**)&H->d_drafts, H->Kmax * 4)))
+    return rc;
+  CU(cudaMemcpy(H->enorm, host_tensors[3], h * 4, cudaMemcpyHostToDevice));
+  CU(cudaMemcpy(H->hnorm, host_tensors[4], h * 4, cudaMemcpyHostToDevice));
+  CU(cudaMemcpy(H->P, host_tensors[5], (size_t)h * 2 * h * welt, cudaMemcpyHostToDevice));
+  CU(cudaMallocHost(&H->pin, (size_t)H->max_pass * H->pass_ints * sizeof(int)));
+  blk->B.row_rope = H->d_meta + 2 * H->R;
+  H->p0.assign(c.max_seqs, -1);
+  H->p_done.assign(c.max_seqs, -2);
+  H->b0_rows.assign(c.max_seqs, 0);
+  H->last_pos0.assign(c.max_seqs, -1);
+  H->last_idx.assign(c.max_seqs, -1);
+  H->prompt_tok.assign(c.max_seqs, {});
+  m->mtp = H.release();
+  return SPEC_OK;
+}
+
+int spec_mtp_draft(spec_model* m, int32_t seq_id, int K, int32_t* out_drafts) {
+  if (!m || !out_drafts) return fail(SPEC_ERR_ARG, "null argument");
+  if (!m->mtp) return fail(SPEC_ERR_STATE, "no draft head (spec_mtp_init)");
+  if (!m->seq_ok(seq_id)) return fail(SPEC_ERR_ARG, "sequence not active");
+  if (m->host_dirty) return fail(SPEC_ERR_STATE, "call spec_sync_seqs after device-resident steps");
+  MtpHead& H = *m->mtp;
+  if (K < 1 || K > H.Kmax) return fail(SPEC_ERR_ARG, "K out of range");
+  const int p0 = H.p0[seq_id];
+  if (p0 < 0) return fail(SPEC_ERR_UNSUPPORTED, "the draft head does not take sequences with a shared prefix");
+  const int N = m->seq_len_h[seq_id], p = N - 1, done = H.p_done[seq_id];
+  if (p <= done) return fail(SPEC_ERR_STATE, "no new committed rows since the last draft");
+  // decoder state of committed row r (depth 1): the prompt rows kept at
+  // prefill (first call), else the rows of the verify step just run
+  const bool first = done < p0;
+  if (first && p - p0 + 1 > H.b0_rows[seq_id])
+    return fail(SPEC_ERR_STATE, "the first draft must follow the prefill (and the prompt tail fit the head)");
+  if (!first && (H.last_idx[seq_id] < 0 || H.last_pos0[seq_id] != done + 1))
+    return fail(SPEC_ERR_STATE, "draft right after the verify step that committed the new rows");
+  spec_model* blk = H.blk;
+  const int h = m->D.h, R = H.R;
+  const std::vector<int32_t>& pt = H.prompt_tok[seq_id];
+  const std::vector<int32_t>& gen = m->gen[seq_id];
+  const int plen = (int)pt.size();
+  // x_i: committed tokens, then the drafts as -(j + 1) (read on the device)
+  auto tok_at = [&](int i) -> int32_t {
+    if (i < plen) return pt[i];
+    if (i - plen < (int)gen.size()) return gen[i - plen];
+    return -(i - N);
+  };
+  auto dec_row = [&](int r) -> const float* {
+    if (first) return H.b0 + ((size_t)seq_id * H.B0 + (r - p0)) * h;
+    return m->B.x + ((size_t)H.last_idx[seq_id] * m->R + (r - (done + 1))) * h;
+  };
+  // Every depth advances over the new committed rows, so a shorter K leaves
+  // no depth's cache behind; depths 1..K add their speculative rows up to
+  // p + k - 1, whose last one gives d_k.
+  std::vector<int> start(H.Kmax + 1, 0), last(H.Kmax + 1, -1);
+  int npass = 0;
+  for (int k = 1; k <= H.Kmax; ++k) {
+    const int first_row = p0 + k - 1;            // cache index 0 of depth k
+    const int s0 = std::max(done + 1, first_row), s1 = k <= K ? p + k - 1 : p;
+    start[k] = s0;
+    last[k] = s1;
+    if (s1 < s0) continue;
+    if (s1 - s0 + 1 > H.ymax) return fail(SPEC_ERR_UNSUPPORTED, "draft head: too many new rows");
+    const int slot = seq_id * H.Kmax + (k - 1);
+    int rc = blk->pool->reserve(slot, s0 + ((s1 - s0) / R + 1) * R - first_row);
+    if (rc) return fail(rc, "draft head: KV pool exhausted");
+    if ((rc = blk->push_table(slot))) return rc;
+    float* Yk = H.Y + (size_t)(k - 1) * H.ymax * h;
+    for (int ps = s0; ps <= s1; ps += R, ++npass) {
+      if (npass >= H.max_pass) return fail(SPEC_ERR_UNSUPPORTED, "draft head: too many passes");
+      const int nreal = std::min(R, s1 - ps + 1);
+      int* meta = H.pin + (size_t)npass * H.pass_ints;
+      const float** srcp = reinterpret_cast<const float**>(meta + 4 * R);
+      for (int i = 0; i < R; ++i) {
+        const int r = ps + i;
+        const bool real = i < nreal;
+        meta[i] = real ? tok_at(r + 1) : 0;                    // x_(r+1)
+        meta[R + i] = r - first_row;                           // cache index
+        meta[2 * R + i] = r;                                   // RoPE position
+        meta[3 * R + i] = slot;
+        const float* src = nullptr;
+        if (real) {
+          if (k == 1) src = dec_row(r);
+          else if (r - 1 < start[k - 1]) src = H.ylast + ((size_t)seq_id * H.Kmax + (k - 2)) * h;   // kept row
+          else src = H.Y + ((size_t)(k - 2) * H.ymax + (r - 1 - start[k - 1])) * h;
+        }
+        srcp[i] = src;
+      }
+      // the pinned area of each pass stays untouched until the call's final sync
+      CU(cudaMemcpyAsync(H.d_meta, meta, H.pass_ints * sizeof(int), cudaMemcpyHostToDevice, m->stream));
+      CU(cudaMemcpyAsync(blk->B.row_pos, H.d_meta + R, R * 4, cudaMemcpyDeviceToDevice, m->stream));
+      CU(cudaMemcpyAsync(blk->B.row_seq, H.d_meta + 3 * R, R * 4, cudaMemcpyDeviceToDevice, m->stream));
+      launch_mtp_input(blk->D, H.d_meta, reinterpret_cast<const float* const*>(H.d_meta + 4 * R), H.d_drafts, R,
+                       blk->tok_embed, H.enorm, blk->final_norm, H.hnorm, H.P, H.cat, blk->B.x, m->stream);
+      const float* y = blk->enqueue_layers(R, R);
+      CU(cudaMemcpyAsync(Yk + (size_t)(ps - s0) * h, y, (size_t)nreal * h * 4, cudaMemcpyDeviceToDevice, m->stream));
+    }
+    if (k <= K) {
+      // d_k: greedy token of N_o(y) at row p + k - 1, the depth's last row
+      blk->enqueue_lmhead(Yk + (size_t)(s1 - s0) * h, 1, nullptr, false, 0);
+      CU(cudaMemcpyAsync(H.d_drafts + (k - 1), blk->B.g, 4, cudaMemcpyDeviceToDevice, m->stream));
+    }
+  }
+  // keep each depth's row p for the next call
+  for (int k = 1; k <= H.Kmax; ++k)
+    if (p >= start[k] && p <= last[k])
+      CU(cudaMemcpyAsync(H.ylast + ((size_t)seq_id * H.Kmax + (k - 1)) * h,
+                         H.Y + ((size_t)(k - 1) * H.ymax + (p - start[k])) * h, h * 4, cudaMemcpyDeviceToDevice,
+                         m->stream));
+  int32_t* dout = blk->pin_out;
+  CU(cudaMemcpyAsync(dout, H.d_drafts, K * 4, cudaMemcpyDeviceToHost, m->stream));
+  CU(cudaStreamSynchronize(m->stream));
+  CU(cudaGetLastError());
+  int rc = blk->check_err();
+  if (rc) return rc;
+  H.p_done[seq_id] = p;
+  for (int k = 0; k < K; ++k) out_drafts[k] = dout[k];
+  return SPEC_OK;
 }
 
 // ---- host-only allocator entry points --------------------------------------

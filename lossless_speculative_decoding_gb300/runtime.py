@@ -18,7 +18,7 @@ def bf16_bits(a: np.ndarray) -> np.ndarray:
     """float32 values that are already bf16-exact -> their bf16 bit patterns."""
     b = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
     if np.any(b & 0xFFFF):
-        raise ValueError("visual rows of a bf16 model must be bf16-exact")
+        raise ValueError("values stored as bf16 must be bf16-exact")
     return (b >> 16).astype(np.uint16)
 
 
@@ -39,6 +39,24 @@ class SpecModel:
             rope_theta=cfg.rope_theta, rms_eps=cfg.rms_eps)
         self.K = max_draft
         self.h = B.spec_init_model(self.c, tensors, int(self.stream.cuda_stream))
+        self._tied = list(tensors[:3])     # embedding, final norm, LM head: shared with a draft head
+
+    # -- FastMTP draft head ----------------------------------------------------
+    MTP_ORDER = ("enorm", "hnorm", "eh_proj", "attn_norm", "w_qkv", "w_o", "ffn_norm", "w_gate", "w_up", "w_down")
+
+    def attach_mtp(self, weights: dict, inter: int) -> None:
+        """Attach a draft head: ``weights`` maps the head's tensor names to
+        float32 arrays (bf16-exact matrices for bf16 / e4m3 decoders)."""
+        enc = []
+        for name in self.MTP_ORDER:
+            a = np.ascontiguousarray(weights[name], np.float32)
+            if not name.endswith("norm") and self.cfg.wdtype != B.SPEC_F32:
+                a = bf16_bits(a)
+            enc.append(a)
+        B.spec_mtp_init(self.h, self._tied + enc, inter)
+
+    def mtp_draft(self, seq: int, K: int) -> list:
+        return [int(t) for t in B.spec_mtp_draft(self.h, seq, K)]
 
     def close(self) -> None:
         if self.h:
