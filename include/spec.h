@@ -224,6 +224,16 @@ int spec_step_launches(spec_model* m, int n_seq);
  * stream once. */
 int spec_mtp_init(spec_model* m, const void* const* host_tensors, int inter);
 int spec_mtp_draft(spec_model* m, int32_t seq_id, int K, int32_t* out_drafts);
+/* Debug: spec_mtp_draft that also writes
+ *  - the fp32 logits W_lm u_(p+k-1)^(k) of each depth's draft row to
+ *    logits_dev ([K][vocab], device, depth order);
+ *  - the decoder states this call reads for depth 1 -- the final residual
+ *    rows (before N_o) of positions max(p_last + 1, p0) .. p, p_last the
+ *    previous call's p -- to states_dev ([states_cap][hidden] fp32, device),
+ *    their count to *out_n_states (SPEC_ERR_ARG if above states_cap).
+ * The sequence's head state advances exactly as in spec_mtp_draft. */
+int spec_mtp_debug_draft(spec_model* m, int32_t seq_id, int K, int32_t* out_drafts, float* logits_dev,
+                         float* states_dev, int states_cap, int32_t* out_n_states);
 
 /* ---- profiling ------------------------------------------------------------ */
 /* Per kernel class: summed device time (ms, CUDA events on the model's stream

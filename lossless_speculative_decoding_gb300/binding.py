@@ -73,6 +73,8 @@ _SIGS = [
     ("spec_step_launches", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     ("spec_mtp_init", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
     ("spec_mtp_draft", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int, _I32P]),
+    ("spec_mtp_debug_draft", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int, _I32P, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_int, _I32P]),
     ("spec_profile_steps_dev", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                               ctypes.POINTER(spec_kernel_stat), ctypes.c_int]),
@@ -275,6 +277,15 @@ def spec_mtp_draft(m: int, seq_id: int, K: int) -> np.ndarray:
     out = np.zeros(K, np.int32)
     _check(lib().spec_mtp_draft(m, seq_id, K, _p(out)))
     return out
+
+
+def spec_mtp_debug_draft(m: int, seq_id: int, K: int, logits_dev, states_dev, states_cap: int) -> tuple:
+    """(drafts, number of state rows written)."""
+    out = np.zeros(K, np.int32)
+    n = ctypes.c_int32()
+    _check(lib().spec_mtp_debug_draft(m, seq_id, K, _p(out), _ptr(logits_dev), _ptr(states_dev), states_cap,
+                                      ctypes.byref(n)))
+    return out, n.value
 
 
 def spec_profile_steps_dev(m: int, n_seq: int, seq_ids_dev, drafts_dev, n_draft_dev, n_steps: int,

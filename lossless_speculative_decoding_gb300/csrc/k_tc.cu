@@ -684,9 +684,6 @@ int kv_make_map(CUtensorMap* map, const void* kv, int head_dim, int page_size, i
 }  // namespace spec
 
 // ---------------------------------------------------------------------------
-// Kernel-level entry point (tests and tools): with X = B (+ B_lo when given),
-// out[n][m] = sum_k A[m][k] X[n][k] (dual = 0) or
-// out_bf16[n][m] = silu(A[m]·X[n]) * (A2[m]·X[n]) (dual = 1).
 // Kernel-level entry point (tests and tools): with X = B (+ B_lo when given)
 // and weights A (bf16, or e4m3 when a_fp8, times the per-row scales),
 // out[n][m] = sum_k A[m][k] X[n][k] (dual = 0) or

@@ -1181,7 +1181,8 @@ int spec_mtp_init(spec_model* m, const void* const* host_tensors, int inter) {
   return SPEC_OK;
 }
 
-int spec_mtp_draft(spec_model* m, int32_t seq_id, int K, int32_t* out_drafts) {
+static int mtp_draft(spec_model* m, int32_t seq_id, int K, int32_t* out_drafts, float* logits_dev,
+                     float* states_dev = nullptr, int states_cap = 0, int32_t* out_n_states = nullptr) {
   if (!m || !out_drafts) return fail(SPEC_ERR_ARG, "null argument");
   if (!m->mtp) return fail(SPEC_ERR_STATE, "no draft head (spec_mtp_init)");
   if (!m->seq_ok(seq_id)) return fail(SPEC_ERR_ARG, "sequence not active");
@@ -1217,6 +1218,13 @@ int spec_mtp_draft(spec_model* m, int32_t seq_id, int K, int32_t* out_drafts) {
   // Every depth advances over the new committed rows, so a shorter K leaves
   // no depth's cache behind; depths 1..K add their speculative rows up to
   // p + k - 1, whose last one gives d_k.
+  if (states_dev) {   // debug: the decoder rows depth 1 reads in this call (rows max(done + 1, p0) .. p)
+    const int r0 = std::max(done + 1, p0), n = p - r0 + 1;
+    if (n > states_cap) return fail(SPEC_ERR_ARG, "states_dev holds fewer rows than the call reads");
+    for (int r = r0; r <= p; ++r)
+      CU(cudaMemcpyAsync(states_dev + (size_t)(r - r0) * h, dec_row(r), h * 4, cudaMemcpyDeviceToDevice, m->stream));
+    *out_n_states = n;
+  }
   std::vector<int> start(H.Kmax + 1, 0), last(H.Kmax + 1, -1);
   int npass = 0;
   for (int k = 1; k <= H.Kmax; ++k) {
@@ -1262,7 +1270,8 @@ int spec_mtp_draft(spec_model* m, int32_t seq_id, int K, int32_t* out_drafts) {
     }
     if (k <= K) {
       // d_k: greedy token of N_o(y) at row p + k - 1, the depth's last row
-      blk->enqueue_lmhead(Yk + (size_t)(s1 - s0) * h, 1, nullptr, false, 0);
+      blk->enqueue_lmhead(Yk + (size_t)(s1 - s0) * h, 1, logits_dev ? logits_dev + (size_t)(k - 1) * m->D.V : nullptr,
+                          false, 0);
       CU(cudaMemcpyAsync(H.d_drafts + (k - 1), blk->B.g, 4, cudaMemcpyDeviceToDevice, m->stream));
     }
   }
@@ -1281,6 +1290,16 @@ int spec_mtp_draft(spec_model* m, int32_t seq_id, int K, int32_t* out_drafts) {
   H.p_done[seq_id] = p;
   for (int k = 0; k < K; ++k) out_drafts[k] = dout[k];
   return SPEC_OK;
+}
+
+int spec_mtp_draft(spec_model* m, int32_t seq_id, int K, int32_t* out_drafts) {
+  return mtp_draft(m, seq_id, K, out_drafts, nullptr);
+}
+
+int spec_mtp_debug_draft(spec_model* m, int32_t seq_id, int K, int32_t* out_drafts, float* logits_dev,
+                         float* states_dev, int states_cap, int32_t* out_n_states) {
+  if (!logits_dev || !states_dev || !out_n_states) return fail(SPEC_ERR_ARG, "null debug output");
+  return mtp_draft(m, seq_id, K, out_drafts, logits_dev, states_dev, states_cap, out_n_states);
 }
 
 // ---- host-only allocator entry points --------------------------------------

@@ -58,6 +58,16 @@ class SpecModel:
     def mtp_draft(self, seq: int, K: int) -> list:
         return [int(t) for t in B.spec_mtp_draft(self.h, seq, K)]
 
+    def mtp_debug_draft(self, seq: int, K: int, states_cap: int = 512):
+        """(drafts, fp32 logits [K, vocab] of each depth's draft row, the
+        decoder's final residual rows [n, hidden] the call read for depth 1)."""
+        torch = self.torch
+        out = torch.empty((K, self.cfg.vocab), dtype=torch.float32, device="cuda")
+        st = self._ready(torch.empty((states_cap, self.cfg.hidden), dtype=torch.float32, device="cuda"))
+        d, n = B.spec_mtp_debug_draft(self.h, seq, K, out, st, states_cap)
+        self.stream.synchronize()
+        return [int(t) for t in d], out.cpu().numpy(), st[:n].cpu().numpy()
+
     def close(self) -> None:
         if self.h:
             B.spec_free_model(self.h)

@@ -5,11 +5,20 @@ verifiable rewards", section 3.1).
 The oracle follows the GPU's trajectory: its decoder states b are the
 oracle's own verify-row states of the tokens the GPU committed, and every
 draft is checked teacher-forced -- depth k is evaluated by the definition on
-the committed tokens followed by the GPU's d_1..d_(k-1). A GPU draft must be
-the oracle's argmax, or score within 1e-3 of the oracle's maximum logit (a
-near-tie, counted, at most 1 in 8). Speculative decoding with the head's
-drafts must equal the GPU's greedy decode token for token (lossless), also
-when K changes from step to step (every depth's cache advances each call)."""
+the committed tokens followed by the GPU's d_1..d_(k-1). Per draft, with the
+head's logits from spec_mtp_debug_draft:
+
+* the GPU's logits lie within 2e-2 of the oracle row's range (the verify
+  step's bar) -- their error includes that of the decoder states b the head
+  starts from;
+* the draft is the argmax of the GPU's own logits (lowest index on ties);
+* the draft equals the oracle's argmax, or it scores at most
+  max(1e-3, 2 e) below the oracle's maximum, e the row's largest logit
+  error: a choice the measured error explains (counted, at most 1 in 8).
+
+Speculative decoding with the head's drafts must equal the GPU's greedy
+decode token for token (lossless), also when K changes from step to step
+(every depth's cache advances each call)."""
 import numpy as np
 import pytest
 
@@ -29,43 +38,63 @@ TIE = 1e-3
 
 
 class Track:
-    """Oracle side of one sequence on the GPU's trajectory."""
+    """Oracle side of one sequence on the GPU's trajectory. With
+    gpu_states, the head's input states b come from the GPU's decoder (the
+    rows spec_mtp_debug_draft reports, final-normed by the oracle's RMSNorm):
+    the head alone is compared. Otherwise b is the oracle decoder's own."""
 
-    def __init__(self, om, head, prompt):
-        self.om, self.head = om, head
+    def __init__(self, om, head, prompt, gpu_states=False):
+        self.om, self.head, self.gpu_states = om, head, gpu_states
+        n_vis = len(prompt.visual)
+        self.p0 = max(n_vis - 1, 0)
+        self.tokens = [0] * n_vis + [int(t) for t in prompt.tokens]
+        if gpu_states:
+            self.b = np.zeros((self.p0, om.cfg.hidden), np.float32)   # rows before p0 are never read
+            self.first_logits = None
+            return
         self.cache = oracle.KVCache(om.cfg)
         x = oracle.prompt_embeddings(om, prompt)
         tr = {}
         lg = oracle.forward(om, self.cache, x, np.arange(len(x)), tr)
         self.b = tr["hidden"]
-        n_vis = len(prompt.visual)
-        self.p0 = max(n_vis - 1, 0)
-        self.tokens = [0] * n_vis + [int(t) for t in prompt.tokens]
         self.first_logits = lg[-1]
 
     def start(self, first: int):
-        s = np.sort(self.first_logits)
-        assert first == int(np.argmax(self.first_logits)) or s[-1] - s[-2] < TIE
+        if self.first_logits is not None:
+            s = np.sort(self.first_logits)
+            assert first == int(np.argmax(self.first_logits)) or s[-1] - s[-2] < TIE
         self.tokens.append(int(first))
 
-    def check(self, d, counts):
-        p = len(self.b) - 1
+    def check(self, d, lg_gpu, states, counts):
+        p = len(self.tokens) - 2                     # x_(p+1) is the last committed token
+        if self.gpu_states:
+            assert len(self.b) + len(states) == p + 1, "the call read other decoder rows than the new ones"
+            nb = oracle.rms_norm(states, self.om.final_norm, self.om.cfg.rms_eps).astype(np.float32)
+            self.b = np.concatenate([self.b, nb])
+        assert len(self.b) == p + 1
         for k in range(1, len(d) + 1):
             ext = self.tokens + [int(t) for t in d[:k - 1]]
             u = mtp.grid(self.head, self.b, ext, self.p0, k)[k - 1][p + k - 1]
             lg = (self.head.lm_head @ u).astype(np.float32)
+            g = lg_gpu[k - 1]
+            err = float(np.abs(g - lg).max())
+            rel = err / float(lg.max() - lg.min())
             counts["drafts"] += 1
+            counts["max_rel"] = max(counts["max_rel"], rel)
+            assert rel <= 2e-2, f"draft {k}: logits {err} off the oracle ({rel:.3g} of the range)"
+            assert int(d[k - 1]) == int(np.argmax(g)), "draft is not the argmax of the head's own logits"
             if int(d[k - 1]) != int(np.argmax(lg)):
                 gap = float(lg.max() - lg[int(d[k - 1])])
-                assert gap < TIE, f"draft {k}: token {d[k - 1]} scores {gap} below the oracle's maximum"
-                counts["near_tie"] += 1
+                assert gap <= max(TIE, 2 * err), f"draft {k}: token {d[k - 1]} scores {gap} below the oracle's maximum"
+                counts["explained"] += 1
 
     def commit(self, d, a: int, bonus: int):
-        tr = {}
-        base = self.cache.length
-        oracle.verify_rows(self.om, self.cache, self.tokens[-1], list(d), tr)
-        self.cache.truncate(base + a + 1)
-        self.b = np.concatenate([self.b, tr["hidden"][: a + 1]])
+        if not self.gpu_states:
+            tr = {}
+            base = self.cache.length
+            oracle.verify_rows(self.om, self.cache, self.tokens[-1], list(d), tr)
+            self.cache.truncate(base + a + 1)
+            self.b = np.concatenate([self.b, tr["hidden"][: a + 1]])
         self.tokens += [int(t) for t in d[:a]] + [int(bonus)]
 
 
@@ -92,19 +121,20 @@ def _run_parity(cfg, n_seq, K, n_vis, n_text, n_steps, seed=0):
     tracks = [Track(om, head, p) for p in prompts]
     for i, p in enumerate(prompts):
         tracks[i].start(gm.prefill(i, p.visual, p.tokens))
-    counts = {"drafts": 0, "near_tie": 0}
+    counts = {"drafts": 0, "explained": 0, "max_rel": 0.0}
     for step in range(n_steps):
         k = _ks(K, step)
         drafts = np.zeros((n_seq, K), np.int32)
         for i in ids:
-            d = gm.mtp_draft(i, k)
-            tracks[i].check(d, counts)
+            d, lg, st = gm.mtp_debug_draft(i, k)
+            tracks[i].check(d, lg, st, counts)
             drafts[i, :k] = d
         a, b = gm.verify_batch(ids, drafts, [k] * n_seq)
         for i in ids:
             tracks[i].commit(list(drafts[i, :k]), int(a[i]), int(b[i]))
     gm.close()
-    assert counts["near_tie"] * 8 <= counts["drafts"], counts
+    print("mtp parity counts:", counts)
+    assert counts["explained"] * 8 <= counts["drafts"], counts
     return counts
 
 
@@ -202,3 +232,33 @@ def test_mtp_call_states():
         gm.mtp_draft(0, 3)
     assert e.value.code == B.SPEC_ERR_UNSUPPORTED
     gm.close()
+
+
+def test_mtp_fullsize_moe3b_bf16_b1():
+    """The draft head on the full 3B-MoE bf16 shape (12 layers, h 1,280,
+    V 129,280; the head's FFN 7,168 wide) after a 256-visual + 16-token
+    prompt, K = 3, the batch-1 launch configuration: every draft of 8 steps
+    checked against the oracle head run on the GPU decoder's states (the
+    decoder itself is checked at this size by the verify-step tests)."""
+    wl = syn.WORKLOADS["moe3b_bf16_b1"]
+    cfg = wl.model
+    w = syn.generate_weights(cfg, 0)
+    mw = syn.generate_mtp_weights(cfg, 7, norm_gamma_std=0.1)
+    om = oracle.OracleModel(w)
+    head = mtp.MtpHead(om, mw)
+    p = syn.make_prompts(wl, n_seq=1)[0]
+    gm = gpu_model(cfg, w, page_size=wl.page_size, n_pages=64, max_ctx=p.length + 64, max_draft=3)
+    gm.attach_mtp(mw, syn.mtp_inter(cfg))
+    tr = Track(om, head, p, gpu_states=True)
+    tr.start(gm.prefill(0, p.visual, p.tokens))
+    counts = {"drafts": 0, "explained": 0, "max_rel": 0.0}
+    try:
+        for step in range(8):
+            d, lg, st = gm.mtp_debug_draft(0, 3)
+            tr.check(d, lg, st, counts)
+            a, b = gm.verify(0, d)
+            tr.commit(d, a, b)
+    finally:
+        gm.close()
+    print("mtp parity counts:", counts)
+    assert counts["explained"] * 8 <= counts["drafts"], counts
