@@ -46,10 +46,10 @@ through these checks: the pages print no worked example.
 from .model import (OracleModel, KVCache, rms_norm, rope, attention_rows, moe_ffn,
                     forward, prompt_embeddings, greedy_decode, spec_decode, accept,
                     brute_force_logits, teacher_forced_logits, verify_rows,
-                    decode_bf16, decode_e4m3, decode_e2m1, decode_nvfp4, route, commit_pages,
+                    decode_bf16, decode_e4m3, decode_e2m1, decode_nvfp4, unpack_nvfp4, route, commit_pages,
                     round_bf16)
 
 __all__ = ["OracleModel", "KVCache", "rms_norm", "rope", "attention_rows", "moe_ffn",
            "forward", "prompt_embeddings", "greedy_decode", "spec_decode", "accept",
            "brute_force_logits", "teacher_forced_logits", "verify_rows", "decode_bf16",
-           "decode_e4m3", "decode_e2m1", "decode_nvfp4", "route", "commit_pages", "round_bf16"]
+           "decode_e4m3", "decode_e2m1", "decode_nvfp4", "unpack_nvfp4", "route", "commit_pages", "round_bf16"]

@@ -78,15 +78,29 @@ def decode_nvfp4(codes: np.ndarray, block_scales: np.ndarray, tensor_scale: floa
     return v.reshape(codes.shape).astype(np.float32)
 
 
+def unpack_nvfp4(record: np.ndarray, rows: int, K: int):
+    """The stored nvfp4 record of a [rows, K] matrix -> (codes [rows, K],
+    block scale codes [rows, K/16]). Byte j of a row holds element 2j in its
+    low nibble and element 2j + 1 in its high nibble; the rows' codes come
+    first (rows * K / 2 bytes), then the block scales."""
+    rec = np.asarray(record, dtype=np.uint8).reshape(-1)
+    nc = rows * K // 2
+    packed = rec[:nc].reshape(rows, K // 2)
+    codes = np.empty((rows, K), dtype=np.uint8)
+    codes[:, 0::2] = packed & 0xF
+    codes[:, 1::2] = packed >> 4
+    return codes, rec[nc:nc + rows * K // 16].reshape(rows, K // 16)
+
+
 class OracleModel:
     """The decoder of one model configuration with every weight decoded to
     float32 (bf16 values upcast exactly; e4m3 codes times their per-row fp32
-    scale)."""
+    scale; nvfp4 codes times their block and matrix scales)."""
 
     def __init__(self, weights):
         cfg = weights.cfg
         self.cfg = cfg
-        F32, BF16, FP8 = 0, 1, 2
+        F32, BF16, FP8, NVFP4 = 0, 1, 2, 3
 
         def dec(name, layer=-1):
             i = next(k for k, (n, _, _, l) in enumerate(weights.specs)
@@ -100,6 +114,11 @@ class OracleModel:
             if dtype == BF16:
                 return decode_bf16(a)
             scale = weights.get("s" + name[1:], layer)
+            if dtype == NVFP4:
+                rows, K = shape[-2], shape[-1]
+                recs = np.asarray(a).reshape(-1, rows * K // 2 + rows * K // 16)
+                mats = [decode_nvfp4(*unpack_nvfp4(r, rows, K), float(ts)) for r, ts in zip(recs, scale)]
+                return np.stack(mats).reshape(shape)
             return decode_e4m3(a, scale)
 
         self.tok_embed = dec("tok_embed")

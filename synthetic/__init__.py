@@ -15,6 +15,14 @@ Encodings produced here (the byte formats the C-ABI consumes):
   largest finite 448), round-to-nearest-even with saturation to +-448, plus one
   fp32 scale per output channel (row): ``s_o = max_j |W_oj| / 448`` and
   ``code_oj = e4m3(W_oj / s_o)``.
+* ``nvfp4`` -- 4-bit E2M1 codes with one E4M3 scale per 16 consecutive
+  elements of a row and one fp32 scale per matrix (per expert for stacked
+  experts), ``value = e2m1 * e4m3(block scale) * tensor scale``
+  (``quantize_nvfp4``). A [rows, K] matrix is stored as its codes packed two
+  per byte -- element 2j in the low nibble of byte j of the row, element 2j+1
+  in the high nibble -- rows * K / 2 bytes, followed by the block scale codes
+  [rows, K / 16]; stacked experts store one such record per expert. The
+  tensor scales go in the matrix's scale tensor (fp32, one per matrix).
 
 Model shapes and workload recipes follow the five workloads the pages
 describe for document-OCR serving (Jina-OCR-v1, section 3 "model
@@ -33,8 +41,8 @@ from typing import Dict, List, Optional, Sequence, Tuple
 
 import numpy as np
 
-F32, BF16, FP8 = 0, 1, 2          # storage dtype codes (same numbering as the C-ABI)
-DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8: "e4m3"}
+F32, BF16, FP8, NVFP4 = 0, 1, 2, 3    # storage dtype codes (same numbering as the C-ABI)
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8: "e4m3", NVFP4: "nvfp4"}
 
 # --------------------------------------------------------------------------- #
 # Model configuration
@@ -101,6 +109,7 @@ MOE3B = ModelConfig("deepseek-3b-moe-shape", n_layers=12, hidden=1280, n_q_heads
                     n_kv_heads=10, head_dim=128, n_experts=64, top_k=6, n_shared=2,
                     inter=896, vocab=129280, wdtype=BF16)
 MOE3B_FP8 = dataclasses.replace(MOE3B, name="deepseek-3b-moe-shape-fp8", wdtype=FP8)
+MOE3B_NVFP4 = dataclasses.replace(MOE3B, name="deepseek-3b-moe-shape-nvfp4", wdtype=NVFP4)
 DENSE4B = ModelConfig("qwen3-4b-shape", n_layers=36, hidden=2560, n_q_heads=32,
                       n_kv_heads=8, head_dim=128, n_experts=0, top_k=0, n_shared=1,
                       inter=9728, vocab=151936, wdtype=BF16, rope_theta=1_000_000.0)
@@ -124,6 +133,10 @@ WORKLOADS: Dict[str, Workload] = {
     "dense4b_bf16_b8": Workload("dense4b_bf16_b8", DENSE4B, batch=8, n_draft=31,
                                 drafter="geometric", q=0.15, visual=(1288, 0, 0), n_text=0,
                                 shared_prefix=0, out_len=(1200,)),
+    # the batch-1 3B-MoE workload with NVFP4 attention and expert weights
+    "moe3b_nvfp4_b1": Workload("moe3b_nvfp4_b1", MOE3B_NVFP4, batch=1, n_draft=3, drafter="iid",
+                               q=0.576, visual=(256, 0, 0), n_text=16, shared_prefix=0,
+                               out_len=(1085,)),
     # 3B-MoE with e4m3 weights at concurrency 64, shared 64-token prefix
     "moe3b_fp8_c64": Workload("moe3b_fp8_c64", MOE3B_FP8, batch=64, n_draft=3, drafter="iid",
                               q=0.576, visual=(256, 100, 9), n_text=0, shared_prefix=64,
@@ -147,14 +160,20 @@ N_GLOBAL = 3  # tok_embed, final_norm, lm_head
 def tensor_specs(cfg: ModelConfig) -> List[Tuple[str, Tuple[int, ...], int, int]]:
     """(name, shape, storage dtype, layer) for every tensor, in C-ABI order.
 
-    Storage: norms and fp8 scales are always f32; the router, embedding and LM
+    Storage: norms and scales are always f32; the router, embedding and LM
     head are f32 for f32 models and bf16 otherwise; attention and expert
-    matrices use ``cfg.wdtype``. Absent tensors (scales of non-fp8 models, the
-    router of a dense model) have shape (0,)."""
+    matrices use ``cfg.wdtype`` (their shape is the logical [.., rows, K]; an
+    nvfp4 array holds the packed record, ``nvfp4_bytes`` per matrix). Scales:
+    one per output row for e4m3, one per matrix for nvfp4. Absent tensors
+    (scales of other models, the router of a dense model) have shape (0,)."""
     h, d = cfg.hidden, cfg.head_dim
     side = F32 if cfg.wdtype == F32 else BF16
     fp8 = cfg.wdtype == FP8
+    q4 = cfg.wdtype == NVFP4
     F = cfg.n_ffn
+
+    def sc(fp8_shape, q4_shape):
+        return fp8_shape if fp8 else q4_shape if q4 else (0,)
     out = [("tok_embed", (cfg.vocab, h), side, -1),
            ("final_norm", (h,), F32, -1),
            ("lm_head", (cfg.vocab, h), side, -1)]
@@ -162,17 +181,17 @@ def tensor_specs(cfg: ModelConfig) -> List[Tuple[str, Tuple[int, ...], int, int]
         out += [
             ("attn_norm", (h,), F32, l),
             ("w_qkv", (cfg.qkv_rows, h), cfg.wdtype, l),
-            ("s_qkv", (cfg.qkv_rows,) if fp8 else (0,), F32, l),
+            ("s_qkv", sc((cfg.qkv_rows,), (1,)), F32, l),
             ("w_o", (h, cfg.n_q_heads * d), cfg.wdtype, l),
-            ("s_o", (h,) if fp8 else (0,), F32, l),
+            ("s_o", sc((h,), (1,)), F32, l),
             ("ffn_norm", (h,), F32, l),
             ("w_router", (cfg.n_experts, h) if cfg.n_experts else (0,), side, l),
             ("w_gate", (F, cfg.inter, h), cfg.wdtype, l),
-            ("s_gate", (F, cfg.inter) if fp8 else (0,), F32, l),
+            ("s_gate", sc((F, cfg.inter), (F,)), F32, l),
             ("w_up", (F, cfg.inter, h), cfg.wdtype, l),
-            ("s_up", (F, cfg.inter) if fp8 else (0,), F32, l),
+            ("s_up", sc((F, cfg.inter), (F,)), F32, l),
             ("w_down", (F, h, cfg.inter), cfg.wdtype, l),
-            ("s_down", (F, h) if fp8 else (0,), F32, l),
+            ("s_down", sc((F, h), (F,)), F32, l),
         ]
     return out
 
@@ -243,6 +262,19 @@ def f32_to_e2m1(a: np.ndarray) -> np.ndarray:
     return (code | ((np.signbit(a) & (code != 0)).astype(np.uint8) << np.uint8(3))).astype(np.uint8)
 
 
+def nvfp4_bytes(rows: int, K: int) -> int:
+    """Bytes of one packed nvfp4 matrix record: codes, then block scales."""
+    return rows * K // 2 + rows * K // 16
+
+
+def pack_nvfp4(codes: np.ndarray, block_scales: np.ndarray) -> np.ndarray:
+    """One matrix record: codes [rows, K] two per byte (element 2j in the low
+    nibble of byte j), then the block scale codes [rows, K/16]; flat uint8."""
+    c = np.asarray(codes, dtype=np.uint8)
+    packed = (c[:, 0::2] & 0xF) | ((c[:, 1::2] & 0xF) << 4)
+    return np.concatenate([packed.reshape(-1), np.asarray(block_scales, dtype=np.uint8).reshape(-1)])
+
+
 def quantize_nvfp4(w: np.ndarray):
     """NVFP4 encoding of w [..., K] (K a multiple of 16): tensor scale
     amax(w) / (6 * 448); per 16-element block an E4M3 scale of
@@ -309,6 +341,9 @@ def generate_weights(cfg: ModelConfig, seed: int = 0, threads: Optional[int] = N
             return mat, None
         if dtype == BF16:
             return f32_to_bf16_bits(mat), None
+        if dtype == NVFP4:
+            codes, bs, ts = quantize_nvfp4(mat)
+            return pack_nvfp4(codes, bs), np.float32(ts)
         return quantize_rows_e4m3(mat)
 
     jobs = []
@@ -333,19 +368,19 @@ def generate_weights(cfg: ModelConfig, seed: int = 0, threads: Optional[int] = N
                 parts.append(enc)
                 scales.append(sc)
             arrays[i] = np.stack(parts)
-            if dtype == FP8:
-                arrays[index[(scale_of[name], layer)]] = np.stack(scales)
+            if dtype in (FP8, NVFP4):
+                arrays[index[(scale_of[name], layer)]] = np.stack(scales).astype(np.float32)
         else:
             enc, sc = encode(_normal(seed, i, 0, shape, cfg.init_std), dtype)
             arrays[i] = enc
             if sc is not None:
-                arrays[index[(scale_of[name], layer)]] = sc
+                arrays[index[(scale_of[name], layer)]] = np.atleast_1d(np.asarray(sc, np.float32))
 
     with ThreadPoolExecutor(threads) as ex:
         list(ex.map(run, jobs))
     for i, (name, shape, dtype, layer) in enumerate(specs):
         if arrays[i] is None:
-            npdt = {F32: np.float32, BF16: np.uint16, FP8: np.uint8}[dtype]
+            npdt = {F32: np.float32, BF16: np.uint16, FP8: np.uint8, NVFP4: np.uint8}[dtype]
             arrays[i] = np.zeros(shape, dtype=npdt)
     return Weights(cfg, specs, arrays)  # type: ignore[arg-type]
 

@@ -56,3 +56,45 @@ def test_quantisation_error_within_the_grid():
     assert np.abs(q - w).mean() < 0.12 * np.abs(w).mean()      # about 9% for Gaussian rows
     # the tensor scale puts the largest block scale at the top of the E4M3 range
     assert abs(ts - np.abs(w).max() / (6 * 448)) <= 1e-6 * ts
+
+
+def test_packed_record_layout():
+    """Two codes per byte, element 2j in the low nibble of byte j, row after
+    row, then the block scales: a literal 2 x 32 record."""
+    codes = np.array([[(j % 16) for j in range(32)], [(15 - j % 16) for j in range(32)]], np.uint8)
+    bs = np.array([[0x38, 0x40], [0x30, 0x48]], np.uint8)
+    rec = syn.pack_nvfp4(codes, bs)
+    row0 = [0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE] * 2
+    row1 = [0xEF, 0xCD, 0xAB, 0x89, 0x67, 0x45, 0x23, 0x01] * 2
+    assert list(rec) == row0 + row1 + [0x38, 0x40, 0x30, 0x48]
+    assert len(rec) == syn.nvfp4_bytes(2, 32)
+    c2, b2 = oracle.unpack_nvfp4(rec, 2, 32)
+    np.testing.assert_array_equal(c2, codes)
+    np.testing.assert_array_equal(b2, bs)
+
+
+def test_model_weights_decode_near_their_draws():
+    """An nvfp4 model's decoded matrices lie within the grid's error bound of
+    the same N(0, 0.02) draws the bf16 model rounds, expert by expert (each
+    expert has its own tensor scale), and the LM head and router stay bf16."""
+    cfg16 = syn.scaled(syn.MOE3B, name="m16", n_layers=1, hidden=256, n_q_heads=2, n_kv_heads=2, head_dim=64,
+                       n_experts=4, top_k=2, n_shared=1, inter=128, vocab=512)
+    cfg4 = syn.scaled(cfg16, name="m4", wdtype=syn.NVFP4)
+    w16, w4 = syn.generate_weights(cfg16, 0), syn.generate_weights(cfg4, 0)
+    m16, m4 = oracle.OracleModel(w16), oracle.OracleModel(w4)
+    np.testing.assert_array_equal(m16.lm_head, m4.lm_head)
+    np.testing.assert_array_equal(m16.layers[0]["w_router"], m4.layers[0]["w_router"])
+    for name in ("w_qkv", "w_o", "w_gate", "w_up", "w_down"):
+        a, b = m16.layers[0][name], m4.layers[0][name]
+        assert a.shape == b.shape
+        blk = np.abs(a).reshape(-1, 16).max(-1)
+        err = np.abs(b - a).reshape(-1, 16).max(-1)
+        assert (err <= 0.22 * blk + 1e-6).all(), name      # the grid's bound plus the bf16 rounding of a
+        assert not np.array_equal(a, b)
+    s = w4.get("s_gate", 0)
+    assert s.shape == (5,) and len(set(s.tolist())) == 5    # one tensor scale per expert
+    w4b = syn.generate_weights(cfg4, 0)
+    w4b.get("s_gate", 0)[2] *= 2
+    g = oracle.OracleModel(w4b).layers[0]["w_gate"]
+    np.testing.assert_array_equal(g[2], 2 * m4.layers[0]["w_gate"][2])
+    np.testing.assert_array_equal(np.delete(g, 2, 0), np.delete(m4.layers[0]["w_gate"], 2, 0))
