@@ -44,7 +44,7 @@ import numpy as np  # noqa: E402
 import synthetic as syn  # noqa: E402
 
 DEFAULT_WORKLOAD = "moe3b_fp8_c64"
-DEFAULT_EXTRA = "moe3b_bf16_b1"
+DEFAULT_EXTRA = "moe3b_bf16_b1,moe3b_nvfp4_b1"
 
 
 def parse():
@@ -144,8 +144,9 @@ def measured_peaks() -> dict:
 # --------------------------------------------------------------------------- #
 # algorithmic bytes per kernel class (weights actually read + KV + activations)
 # --------------------------------------------------------------------------- #
-def welt(cfg) -> int:
-    return {syn.F32: 4, syn.BF16: 2, syn.FP8: 1}[cfg.wdtype]
+def welt(cfg) -> float:
+    """Stored bytes per weight element (nvfp4: a 4-bit code plus 1/16 of an E4M3 block scale)."""
+    return {syn.F32: 4, syn.BF16: 2, syn.FP8: 1, syn.NVFP4: 9 / 16}[cfg.wdtype]
 
 
 def side_elt(cfg) -> int:
@@ -419,6 +420,61 @@ def sampling_leg(NB: int, K: int, V: int, hbm_gbs: float) -> dict:
             "l2": f"ring of {copies} input copies ({copies * per / 1e6:.0f} MB)"}
 
 
+MTP_WORKLOADS = ("moe3b_bf16_b1",)
+
+
+def mtp_bytes_per_call(cfg, K: int, ctx: float) -> float:
+    """Algorithmic bytes of one steady-state spec_mtp_draft call: each of the
+    K depths runs one pass of the draft block (its weights and P once, plus
+    the keys and values of ctx cached rows), and depths 1..K each read the
+    LM head once for their draft."""
+    h, d = cfg.hidden, cfg.head_dim
+    we = 4 if cfg.wdtype == syn.F32 else 2
+    f = syn.mtp_inter(cfg)
+    block = (cfg.qkv_rows * h + h * cfg.n_q_heads * d + 3 * f * h + 2 * h * h) * we
+    kv = ctx * 2 * cfg.n_kv_heads * d * we
+    return K * (block + kv) + K * cfg.vocab * h * we
+
+
+def mtp_leg(gm, cfg, prompt, K: int, warmup: int, steps: int, hbm_gbs: float) -> dict:
+    """Draft -> verify loop with the FastMTP draft head (spec_mtp_draft) on
+    one sequence. The head's weights are random like the decoder's, so its
+    drafts rarely match and acceptance says nothing here: the leg measures
+    what drafting costs next to the verify step. Device time of each call
+    from CUDA events on the model's stream (both calls return synchronized)."""
+    import torch
+    mw = syn.generate_mtp_weights(cfg, 7, norm_gamma_std=0.1)
+    gm.attach_mtp(mw, syn.mtp_inter(cfg))
+    gm.prefill(0, prompt.visual, prompt.tokens)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    d_us, v_us, acc, ctx = [], [], [], []
+    for s in range(warmup + steps):
+        n0 = gm.length(0)
+        ev[0].record(gm.stream)
+        d = gm.mtp_draft(0, K)
+        ev[1].record(gm.stream)
+        a, _ = gm.verify(0, d)
+        ev[2].record(gm.stream)
+        ev[2].synchronize()
+        if s >= warmup:
+            d_us.append(ev[0].elapsed_time(ev[1]) * 1e3)
+            v_us.append(ev[1].elapsed_time(ev[2]) * 1e3)
+            acc.append(a)
+            ctx.append(n0 - (len(prompt.visual) - 1) + K)       # rows cached per depth, roughly
+    gm.release(0)
+    dm, vm = float(np.mean(d_us)), float(np.mean(v_us))
+    by = mtp_bytes_per_call(cfg, K, float(np.mean(ctx)))
+    ach = by / (dm * 1e-6) / 1e9
+    return {"entry": "spec_mtp_draft", "K": K, "steps": steps,
+            "draft_us": {"mean": dm, "p50": float(np.median(d_us))},
+            "verify_us": {"mean": vm, "p50": float(np.median(v_us))},
+            "draft_share_of_step": dm / (dm + vm),
+            "tokens_per_step": 1 + float(np.mean(acc)),
+            "tok_s": (len(acc) + sum(acc)) / ((sum(d_us) + sum(v_us)) * 1e-6),
+            "bytes_per_draft_call": by, "achieved_gbs": ach, "frac": ach / hbm_gbs,
+            "note": "random-init head and decoder: acceptance is not meaningful; cost only"}
+
+
 def measure(wl_name: str, args, primary: bool) -> dict:
     """One workload: setup, the device-resident timed region, the profiled
     pass, the end-to-end leg, the roofline, and (rank 0) the oracle legs.
@@ -607,7 +663,9 @@ def measure(wl_name: str, args, primary: bool) -> dict:
             "value": committed_all / (ms_all * 1e-3),
             "ms_per_step": ms_per_step,
             "dtype": {syn.F32: "f32", syn.BF16: "bf16",
-                      syn.FP8: "e4m3 weights widened to f16; activations f16 hi+lo parts; fp32 accumulate"}[cfg.wdtype],
+                      syn.FP8: "e4m3 weights widened to f16; activations f16 hi+lo parts; fp32 accumulate",
+                      syn.NVFP4: "nvfp4 weights (e2m1 x e4m3 block scale) widened to f16; activations f16 "
+                                 "hi+lo parts; fp32 accumulate"}[cfg.wdtype],
             "config": {"workload": wl.name, "model": cfg.name, "layers": cfg.n_layers, "batch": NB, "n_draft": K,
                        "drafter": f"{wl.drafter} q={wl.q}", "rows_per_step": T,
                        "prompt_rows": [p.length for p in prompts0] if NB > 1 else prompts0[0].length,
@@ -641,6 +699,10 @@ def measure(wl_name: str, args, primary: bool) -> dict:
         })
         if primary:
             out["rejection_sampling"] = sampling_leg(NB, K, cfg.vocab, peaks["hbm_gbs"])
+    if wl_name in MTP_WORKLOADS and NB == 1:
+        r = mtp_leg(gm, cfg, prompts0[0], K, warmup=3, steps=max(8, KS), hbm_gbs=peaks["hbm_gbs"])
+        if rank == 0:
+            out["mtp"] = r
     gm.close()
     del w
     torch.cuda.empty_cache()

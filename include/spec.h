@@ -59,6 +59,9 @@ extern "C" {
 #define SPEC_F32  0   /* IEEE binary32                                         */
 #define SPEC_BF16 1   /* bfloat16 (top half of binary32, round-to-nearest-even) */
 #define SPEC_FP8  2   /* OCP E4M3 codes + one fp32 scale per output row        */
+#define SPEC_NVFP4 3  /* E2M1 codes + E4M3 scale per 16 elements + fp32 scale  */
+                      /* per matrix ("OCRia-1 technical report guide",          */
+                      /* inference stack: NVFP4 weights)                        */
 
 /* Model and pool shape. n_experts == 0 selects a dense SwiGLU FFN, stored as
  * one always-on ("shared") expert of width `inter` (n_shared must be 1).
@@ -88,15 +91,22 @@ typedef struct spec_config {
  *   per layer l, index 3 + 13 l + j:
  *   j=0 attn_norm [h] f32       j=1 w_qkv [(Hq+2Hkv) d, h] wdtype (rows: q heads,
  *                                   then k heads, then v heads; each head d rows)
- *   j=2 s_qkv [(Hq+2Hkv) d] f32 (FP8 only)
- *   j=3 w_o [h, Hq d] wdtype    j=4 s_o [h] f32 (FP8 only)
+ *   j=2 s_qkv [(Hq+2Hkv) d] f32 (FP8) / [1] f32 (NVFP4)
+ *   j=3 w_o [h, Hq d] wdtype    j=4 s_o [h] f32 (FP8) / [1] (NVFP4)
  *   j=5 ffn_norm [h] f32        j=6 w_router [E, h] (f32 if F32 model, else bf16;
  *                                   absent when E == 0)
- *   j=7 w_gate [E+S, inter, h]  j=8 s_gate [E+S, inter] f32 (FP8 only)
- *   j=9 w_up [E+S, inter, h]    j=10 s_up [E+S, inter] f32 (FP8 only)
- *   j=11 w_down [E+S, h, inter] j=12 s_down [E+S, h] f32 (FP8 only)
+ *   j=7 w_gate [E+S, inter, h]  j=8 s_gate [E+S, inter] f32 (FP8) / [E+S] (NVFP4)
+ *   j=9 w_up [E+S, inter, h]    j=10 s_up [E+S, inter] f32 (FP8) / [E+S] (NVFP4)
+ *   j=11 w_down [E+S, h, inter] j=12 s_down [E+S, h] f32 (FP8) / [E+S] (NVFP4)
  * Matrices are row-major [out, in]; experts 0..E-1 are routed, E..E+S-1
- * shared. Absent tensors have 0 bytes and their pointer may be NULL. */
+ * shared. Absent tensors have 0 bytes and their pointer may be NULL.
+ * An NVFP4 matrix [rows, K] (each expert of a stack in turn) is one record:
+ * its E2M1 codes, two per byte (element 2j of a row in the low nibble of
+ * byte j), rows * K / 2 bytes, then its E4M3 block-scale codes [rows, K / 16];
+ * value = e2m1 * e4m3(block scale) * the matrix's fp32 scale (the s_ tensor).
+ * NVFP4 models take at most 8 rows per verify step (max_batch * (max_draft +
+ * 1) <= 8), and hidden, inter and Hq * head_dim multiples of 128
+ * (SPEC_ERR_UNSUPPORTED otherwise). */
 int spec_tensor_count(const spec_config* cfg);
 /* Byte size of tensor `index` (0 for absent ones), or a negative error. */
 int64_t spec_tensor_bytes(const spec_config* cfg, int index);

@@ -16,7 +16,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspec.so")
 
-SPEC_F32, SPEC_BF16, SPEC_FP8 = 0, 1, 2
+SPEC_F32, SPEC_BF16, SPEC_FP8, SPEC_NVFP4 = 0, 1, 2, 3
 SPEC_ERR_ARG, SPEC_ERR_NO_PAGES, SPEC_ERR_CUDA, SPEC_ERR_STATE, SPEC_ERR_NOMEM, SPEC_ERR_UNSUPPORTED = -1, -2, -3, -4, -5, -6
 ERRORS = {-1: "SPEC_ERR_ARG", -2: "SPEC_ERR_NO_PAGES", -3: "SPEC_ERR_CUDA", -4: "SPEC_ERR_STATE",
           -5: "SPEC_ERR_NOMEM", -6: "SPEC_ERR_UNSUPPORTED"}

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
+#include <cuda_fp4.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -50,6 +51,7 @@ __device__ __forceinline__ bool mbar_wait_deadline(uint32_t bar, uint32_t parity
 // ---- storage element types --------------------------------------------------
 struct bf16_t { uint16_t v; };
 struct fp8_t { uint8_t v; };
+struct fp4_t { uint8_t v; };     // two E2M1 codes: element 2j in the low nibble of byte j
 
 template <class T> struct Elt;
 template <> struct Elt<float>  { static constexpr int per16 = 4; };

@@ -398,6 +398,88 @@ __device__ __forceinline__ void e4m3x8_bf16(uint32_t w0, uint32_t w1, uint32_t (
 template <class WT> struct MmaStep;                   // k values one step covers (4 lanes x EPL)
 template <> struct MmaStep<bf16_t> { static constexpr int EPL = 8, K = 32; };
 template <> struct MmaStep<fp8_t> { static constexpr int EPL = 16, K = 64; };
+template <> struct MmaStep<fp4_t> { static constexpr int EPL = 32, K = 128; };
+
+template <class WT> struct IsQ4 { static constexpr bool v = false; };
+template <> struct IsQ4<fp4_t> { static constexpr bool v = true; };
+
+// Element k of a weight row (an nvfp4 row holds two elements per byte).
+template <class WT>
+__device__ __forceinline__ const WT* at_k(const WT* row, int k) {
+  if constexpr (IsQ4<WT>::v) return row + (k >> 1);
+  else return row + k;
+}
+
+// Row r of matrix e in a stack of [rows][K] matrices. An nvfp4 stack holds
+// one record per matrix -- the codes of all rows (K / 2 bytes a row), then
+// the block-scale codes (K / 16 a row) -- and *sc gets the row's scales.
+template <class WT>
+__device__ __forceinline__ const WT* stack_row(const WT* W, int e, int rows, int r, int K, const uint8_t** sc) {
+  if constexpr (IsQ4<WT>::v) {
+    const uint8_t* rec = reinterpret_cast<const uint8_t*>(W) + (size_t)e * rows * (K / 2 + K / 16);
+    *sc = rec + (size_t)rows * (K / 2) + (size_t)r * (K / 16);
+    return reinterpret_cast<const WT*>(rec + (size_t)r * (K / 2));
+  } else {
+    *sc = nullptr;
+    return W + ((size_t)e * rows + r) * K;
+  }
+}
+
+// nvfp4 block scales of a unit's two rows: the row pointers and, per loaded
+// step, the lane's two scale codes (its 32 elements span two 16-element blocks).
+template <int NB> struct Q4Scales {
+  const uint8_t* lo = nullptr;
+  const uint8_t* hi = nullptr;
+  uint32_t a[NB], b[NB];
+};
+
+// Eight E2M1 codes (one word, element i in nibble i) times the E4M3 block
+// scale `sc` -> four f16x2 words (element 2j in the low half of word j).
+// Every product is exact in f16: at most 2 x 4 significant bits, magnitudes
+// 2^-10 .. 2688.
+__device__ __forceinline__ void q4x8_f16(uint32_t w, uint32_t sc, uint32_t (&o)[4]) {
+  const __half_raw sr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)(sc & 0xFF), __NV_E4M3);
+  const __half2 s2 = __halves2half2(__half(sr), __half(sr));
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((w >> (8 * j)) & 0xFF), __NV_E2M1);
+    const __half2 v = __hmul2(__half2(hr), s2);
+    o[j] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+}
+
+__device__ __forceinline__ void mma16816_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// mma_group8 with f16 weights: the activations enter as NP f16 parts of
+// x * F16_OP_SCALE (each part the rounding of what the earlier ones leave).
+template <int NP>
+__device__ __forceinline__ void mma_group8_f16(float (&c)[NP][4], const uint32_t (&wa)[4], const uint32_t (&wb)[4],
+                                               const float4& x0, const float4& x1) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const float4 v = half ? x1 : x0;
+    float r[4] = {v.x * F16_OP_SCALE, v.y * F16_OP_SCALE, v.z * F16_OP_SCALE, v.w * F16_OP_SCALE};
+#pragma unroll
+    for (int part = 0; part < NP; ++part) {
+      uint32_t b0, b1;
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(b0) : "f"(r[1]), "f"(r[0]));
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(b1) : "f"(r[3]), "f"(r[2]));
+      mma16816_f16(c[part], wa[2 * half], wb[2 * half], wa[2 * half + 1], wb[2 * half + 1], b0, b1);
+      if (part + 1 < NP) {
+        r[0] -= f16_to_f((uint16_t)(b0 & 0xFFFF));
+        r[1] -= f16_to_f((uint16_t)(b0 >> 16));
+        r[2] -= f16_to_f((uint16_t)(b1 & 0xFFFF));
+        r[3] -= f16_to_f((uint16_t)(b1 >> 16));
+      }
+    }
+  }
+}
 
 // NP MMAs (activation parts) of one 8-element group: weights wa (row g) / wb
 // (row g+8) as four bf16x2 words, activations x[0..8) of column g at the
@@ -434,15 +516,19 @@ __device__ __forceinline__ void mma_group8(float (&c)[NP][4], const uint32_t (&w
 // warps' partial c[4] in warp order (a fixed order) for warp 0.
 template <class WT, int NB>
 __device__ __forceinline__ void mma_load_batch(uint4 (&va)[NB], uint4 (&vb)[NB], const WT* wlo, const WT* whi,
-                                               int K, int s0) {
+                                               int K, int s0, Q4Scales<NB>& qs) {
   constexpr int SK = MmaStep<WT>::K, EPL = MmaStep<WT>::EPL;
   const int q = threadIdx.x & 3, nsteps = K / SK;
 #pragma unroll
   for (int u = 0; u < NB; ++u) {
     const int st = s0 + 8 * u;
     const int k = st * SK + EPL * q;
-    va[u] = st < nsteps ? ld_stream(wlo + k) : make_uint4(0, 0, 0, 0);
-    vb[u] = st < nsteps ? ld_stream(whi + k) : make_uint4(0, 0, 0, 0);
+    va[u] = st < nsteps ? ld_stream(at_k(wlo, k)) : make_uint4(0, 0, 0, 0);
+    vb[u] = st < nsteps ? ld_stream(at_k(whi, k)) : make_uint4(0, 0, 0, 0);
+    if constexpr (IsQ4<WT>::v) {   // the two block scales of the lane's 32 elements (k / 16 is even)
+      qs.a[u] = st < nsteps ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(qs.lo + k / 16)) : 0u;
+      qs.b[u] = st < nsteps ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(qs.hi + k / 16)) : 0u;
+    }
   }
 }
 
@@ -451,7 +537,7 @@ __device__ __forceinline__ void mma_load_batch(uint4 (&va)[NB], uint4 (&vb)[NB],
 // (mma_load_batch at s0 = warp).
 template <class WT, int NB, int NP = 2>
 __device__ __forceinline__ void mma_part(uint4 (&va)[NB], uint4 (&vb)[NB], const WT* wlo, const WT* whi, int K,
-                                         const float* x, float (&c)[4]) {
+                                         const float* x, float (&c)[4], Q4Scales<NB>& qs) {
   constexpr int SK = MmaStep<WT>::K, EPL = MmaStep<WT>::EPL;
   const int q = threadIdx.x & 3, w = threadIdx.x >> 5, nsteps = K / SK;
   float cp[NP][4];
@@ -460,7 +546,7 @@ __device__ __forceinline__ void mma_part(uint4 (&va)[NB], uint4 (&vb)[NB], const
 #pragma unroll
     for (int i = 0; i < 4; ++i) cp[part][i] = 0.f;
   for (int s0 = w; s0 < nsteps; s0 += 8 * NB) {
-    if (s0 != w) mma_load_batch<WT, NB>(va, vb, wlo, whi, K, s0);
+    if (s0 != w) mma_load_batch<WT, NB>(va, vb, wlo, whi, K, s0, qs);
 #pragma unroll
     for (int u = 0; u < NB; ++u) {
       const int st = s0 + 8 * u;
@@ -469,7 +555,20 @@ __device__ __forceinline__ void mma_part(uint4 (&va)[NB], uint4 (&vb)[NB], const
 #pragma unroll
         for (int h = 0; h < EPL / 8; ++h) {
           uint32_t wa[4], wb[4];
-          if constexpr (EPL == 8) {
+          if constexpr (IsQ4<WT>::v) {
+            // group h: elements k + 8h .. k + 8h + 7, block scale h / 2 of the lane's pair
+            const uint32_t ca = h == 0 ? va[u].x : h == 1 ? va[u].y : h == 2 ? va[u].z : va[u].w;
+            const uint32_t cb = h == 0 ? vb[u].x : h == 1 ? vb[u].y : h == 2 ? vb[u].z : vb[u].w;
+            q4x8_f16(ca, qs.a[u] >> (8 * (h >> 1)), wa);
+            q4x8_f16(cb, qs.b[u] >> (8 * (h >> 1)), wb);
+            float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+            if (x != nullptr) {
+              x0 = *reinterpret_cast<const float4*>(x + k + 8 * h);
+              x1 = *reinterpret_cast<const float4*>(x + k + 8 * h + 4);
+            }
+            mma_group8_f16<NP>(cp, wa, wb, x0, x1);
+            continue;
+          } else if constexpr (EPL == 8) {
             wa[0] = va[u].x; wa[1] = va[u].y; wa[2] = va[u].z; wa[3] = va[u].w;
             wb[0] = vb[u].x; wb[1] = vb[u].y; wb[2] = vb[u].z; wb[3] = vb[u].w;
           } else {

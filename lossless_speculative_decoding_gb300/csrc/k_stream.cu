@@ -597,15 +597,17 @@ __global__ void __launch_bounds__(256, SBPS) k_qkv_m(Dims D, DevState S, StepBuf
   float* inv = sm;
   float* xs = sm + ((T + 3) & ~3);
   uint4 va[MNB], vb[MNB];
+  Q4Scales<MNB> qs;
   const WT *wlo = W, *whi = W;
+  const int nrows = (D.Hq + 2 * D.Hkv) * D.d;
   auto set_rows = [&](int unit) {
     const int base = (unit / upu) * D.d + (unit % upu) * 8 + g;
-    wlo = W + (size_t)base * D.h;
-    whi = W + (size_t)(base + half) * D.h;
+    wlo = stack_row(W, 0, nrows, base, D.h, &qs.lo);
+    whi = stack_row(W, 0, nrows, base + half, D.h, &qs.hi);
   };
   if ((int)blockIdx.x < nunits) {
     set_rows(blockIdx.x);
-    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp);
+    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp, qs);
   }
   pdl_wait();
   pdl_trigger();
@@ -623,17 +625,20 @@ __global__ void __launch_bounds__(256, SBPS) k_qkv_m(Dims D, DevState S, StepBuf
       // three activation parts: the K/V outputs are rounded to bf16 for the
       // cache, and a two-part split would move some of them across a rounding
       // boundary that the exact product does not cross
-      mma_part<WT, MNB, 3>(va, vb, wlo, whi, D.h, g < nvalid ? xs + g * (D.h + 4) : nullptr, c);
+      mma_part<WT, MNB, 3>(va, vb, wlo, whi, D.h, g < nvalid ? xs + g * (D.h + 4) : nullptr, c, qs);
       const int nx = unit + (int)gridDim.x < nunits ? unit + gridDim.x : (pass + 1 < npass ? (int)blockIdx.x : -1);
       if (nx >= 0) {
         set_rows(nx);
-        mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp);
+        mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp, qs);
       }
       block_sum4(c, red, par);
       par ^= 1;
       if (warp != 0) continue;
       float a[2] = {c[0], c[1]}, b[2] = {c[2], c[3]};            // first / second half, columns 2q, 2q+1
-      if (scale != nullptr) {
+      if constexpr (IsQ4<WT>::v) {                                // nvfp4: the matrix's tensor scale
+        const float ts = scale[0] * (1.0f / F16_OP_SCALE);
+        a[0] *= ts; a[1] *= ts; b[0] *= ts; b[1] *= ts;
+      } else if (scale != nullptr) {
         const float sa = scale[head * D.d + j], sb = scale[head * D.d + j + half];
         a[0] *= sa; a[1] *= sa; b[0] *= sb; b[1] *= sb;
       }
@@ -681,16 +686,17 @@ __global__ void __launch_bounds__(256, SBPS) k_oproj_m(Dims D, StepBuf B, const 
   const int npass = cdiv(T, MC);
   const int nitems = (D.h / 16) * npass;
   uint4 va[MNB], vb[MNB];
+  Q4Scales<MNB> qs;
   const WT *wlo = W, *whi = W;
   auto set_rows = [&](int item) {
     const int o = (item / npass) * 16 + g;
-    wlo = W + (size_t)o * K;
-    whi = W + (size_t)(o + 8) * K;
+    wlo = stack_row(W, 0, D.h, o, K, &qs.lo);
+    whi = stack_row(W, 0, D.h, o + 8, K, &qs.hi);
   };
   int it = blockIdx.x;
   if (it < nitems) {
     set_rows(it);
-    mma_load_batch<WT, MNB>(va, vb, wlo, whi, K, warp);
+    mma_load_batch<WT, MNB>(va, vb, wlo, whi, K, warp, qs);
   }
   pdl_wait();
   pdl_trigger();
@@ -698,15 +704,17 @@ __global__ void __launch_bounds__(256, SBPS) k_oproj_m(Dims D, StepBuf B, const 
   for (; it < nitems; it += gridDim.x) {
     const int o = (it / npass) * 16 + g, t0 = (it % npass) * MC, nvalid = min(MC, T - t0);
     float c[4];
-    mma_part<WT, MNB>(va, vb, wlo, whi, K, g < nvalid ? B.o + (size_t)(t0 + g) * K : nullptr, c);
+    mma_part<WT, MNB>(va, vb, wlo, whi, K, g < nvalid ? B.o + (size_t)(t0 + g) * K : nullptr, c, qs);
     if (it + (int)gridDim.x < nitems) {
       set_rows(it + gridDim.x);
-      mma_load_batch<WT, MNB>(va, vb, wlo, whi, K, warp);
+      mma_load_batch<WT, MNB>(va, vb, wlo, whi, K, warp, qs);
     }
     block_sum4(c, red, par);
     par ^= 1;
     if (warp != 0) continue;
-    const float s0 = scale != nullptr ? scale[o] : 1.f, s1 = scale != nullptr ? scale[o + 8] : 1.f;
+    float s0 = 1.f, s1 = 1.f;
+    if constexpr (IsQ4<WT>::v) s0 = s1 = scale[0] * (1.0f / F16_OP_SCALE);
+    else if (scale != nullptr) { s0 = scale[o]; s1 = scale[o + 8]; }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int col = 2 * q + e;
@@ -735,17 +743,18 @@ __global__ void __launch_bounds__(256, SBPS) k_gateup_m(Dims D, StepBuf B, const
   const int stride = gridDim.x;
   const ActCache A(smi, max_active, T * D.NS);
   uint4 va[MNB], vb[MNB];
+  Q4Scales<MNB> qs;
   const WT *wlo = Wg, *whi = Wu;
   auto set_rows_e = [&](int e, int it) {
-    const size_t r = (size_t)e * D.inter + ((it % per_slot) / npass) * 8 + g;
-    wlo = Wg + r * D.h;
-    whi = Wu + r * D.h;
+    const int r = ((it % per_slot) / npass) * 8 + g;
+    wlo = stack_row(Wg, e, D.inter, r, D.h, &qs.lo);
+    whi = stack_row(Wu, e, D.inter, r, D.h, &qs.hi);
   };
   const int it0 = blockIdx.x;
   const bool pre = it0 < D.S * per_slot;             // shared-expert item: expert known now
   if (pre) {
     set_rows_e(D.E + it0 / per_slot, it0);
-    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp);
+    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp, qs);
   }
   pdl_wait();
   pdl_trigger();
@@ -767,7 +776,7 @@ __global__ void __launch_bounds__(256, SBPS) k_gateup_m(Dims D, StepBuf B, const
   int it = next_valid(it0);
   if (it < nitems && !(pre && it == it0)) {
     set_rows_e(A.ex[it / per_slot], it);
-    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp);
+    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp, qs);
   }
   int par = 0;
   while (it < nitems) {
@@ -777,17 +786,23 @@ __global__ void __launch_bounds__(256, SBPS) k_gateup_m(Dims D, StepBuf B, const
     const int nvalid = min(MC, A.cnt[slot] - p0);
     const int* pairs = A.perm + A.off[slot] + p0;
     float c[4];
-    mma_part<WT, MNB>(va, vb, wlo, whi, D.h, g < nvalid ? B.u + (size_t)(pairs[g] / D.NS) * D.h : nullptr, c);
+    mma_part<WT, MNB>(va, vb, wlo, whi, D.h, g < nvalid ? B.u + (size_t)(pairs[g] / D.NS) * D.h : nullptr, c, qs);
     const int nx = next_valid(it + stride);
     if (nx < nitems) {
       set_rows_e(A.ex[nx / per_slot], nx);
-      mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp);
+      mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.h, warp, qs);
     }
     block_sum4(c, red, par);
     par ^= 1;
     if (warp == 0) {
-      const float s0 = sg != nullptr ? sg[(size_t)e * D.inter + j] : 1.f;
-      const float s1 = su != nullptr ? su[(size_t)e * D.inter + j] : 1.f;
+      float s0 = 1.f, s1 = 1.f;
+      if constexpr (IsQ4<WT>::v) {
+        s0 = sg[e] * (1.0f / F16_OP_SCALE);
+        s1 = su[e] * (1.0f / F16_OP_SCALE);
+      } else {
+        if (sg != nullptr) s0 = sg[(size_t)e * D.inter + j];
+        if (su != nullptr) s1 = su[(size_t)e * D.inter + j];
+      }
 #pragma unroll
       for (int ee = 0; ee < 2; ++ee) {
         const int col = 2 * q + ee;
@@ -811,17 +826,18 @@ __global__ void __launch_bounds__(256, SBPS) k_down_m(Dims D, StepBuf B, const W
   const int stride = gridDim.x;
   const ActCache A(smi, max_active, T * D.NS);
   uint4 va[MNB], vb[MNB];
+  Q4Scales<MNB> qs;
   const WT *wlo = Wd, *whi = Wd;
   auto set_rows_e = [&](int e, int it) {
-    const size_t o = (size_t)e * D.h + ((it % per_slot) / npass) * 16 + g;
-    wlo = Wd + o * D.inter;
-    whi = Wd + (o + 8) * D.inter;
+    const int o = ((it % per_slot) / npass) * 16 + g;
+    wlo = stack_row(Wd, e, D.h, o, D.inter, &qs.lo);
+    whi = stack_row(Wd, e, D.h, o + 8, D.inter, &qs.hi);
   };
   const int it0 = blockIdx.x;
   const bool pre = it0 < D.S * per_slot;
   if (pre) {
     set_rows_e(D.E + it0 / per_slot, it0);
-    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.inter, warp);
+    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.inter, warp, qs);
   }
   pdl_wait();
   pdl_trigger();
@@ -835,7 +851,7 @@ __global__ void __launch_bounds__(256, SBPS) k_down_m(Dims D, StepBuf B, const W
   int it = next_valid(it0);
   if (it < nitems && !(pre && it == it0)) {
     set_rows_e(A.ex[it / per_slot], it);
-    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.inter, warp);
+    mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.inter, warp, qs);
   }
   int par = 0;
   while (it < nitems) {
@@ -845,17 +861,19 @@ __global__ void __launch_bounds__(256, SBPS) k_down_m(Dims D, StepBuf B, const W
     const int nvalid = min(MC, A.cnt[slot] - p0);
     const int* pairs = A.perm + A.off[slot] + p0;
     float c[4];
-    mma_part<WT, MNB>(va, vb, wlo, whi, D.inter, g < nvalid ? B.h_act + (size_t)pairs[g] * D.inter : nullptr, c);
+    mma_part<WT, MNB>(va, vb, wlo, whi, D.inter, g < nvalid ? B.h_act + (size_t)pairs[g] * D.inter : nullptr, c,
+                      qs);
     const int nx = next_valid(it + stride);
     if (nx < nitems) {
       set_rows_e(A.ex[nx / per_slot], nx);
-      mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.inter, warp);
+      mma_load_batch<WT, MNB>(va, vb, wlo, whi, D.inter, warp, qs);
     }
     block_sum4(c, red, par);
     par ^= 1;
     if (warp == 0) {
-      const float s0 = sd != nullptr ? sd[(size_t)e * D.h + o] : 1.f;
-      const float s1 = sd != nullptr ? sd[(size_t)e * D.h + o + 8] : 1.f;
+      float s0 = 1.f, s1 = 1.f;
+      if constexpr (IsQ4<WT>::v) s0 = s1 = sd[e] * (1.0f / F16_OP_SCALE);
+      else if (sd != nullptr) { s0 = sd[(size_t)e * D.h + o]; s1 = sd[(size_t)e * D.h + o + 8]; }
 #pragma unroll
       for (int ee = 0; ee < 2; ++ee) {
         const int col = 2 * q + ee;
@@ -886,6 +904,7 @@ __global__ void __launch_bounds__(256, SBPS) k_lmhead_m(Dims D, DevState S, Step
   float* inv = sm;
   float* xs = sm + ((T + 3) & ~3);
   uint4 va[MNB], vb[MNB];
+  Q4Scales<MNB> qs;                      // unused: the LM head is bf16
   const bf16_t *wlo = W, *whi = W;
   auto set_rows = [&](int u) {
     wlo = W + (size_t)(u * 16 + g) * D.h;
@@ -893,7 +912,7 @@ __global__ void __launch_bounds__(256, SBPS) k_lmhead_m(Dims D, DevState S, Step
   };
   if ((int)blockIdx.x < nunits) {
     set_rows(blockIdx.x);
-    mma_load_batch<bf16_t, MNB>(va, vb, wlo, whi, D.h, warp);
+    mma_load_batch<bf16_t, MNB>(va, vb, wlo, whi, D.h, warp, qs);
   }
   pdl_wait();
   pdl_trigger();
@@ -909,11 +928,11 @@ __global__ void __launch_bounds__(256, SBPS) k_lmhead_m(Dims D, DevState S, Step
     int bidx[2] = {0x7fffffff, 0x7fffffff};
     for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
       float c[4];
-      mma_part<bf16_t, MNB>(va, vb, wlo, whi, D.h, g < nvalid ? xs + g * (D.h + 4) : nullptr, c);
+      mma_part<bf16_t, MNB>(va, vb, wlo, whi, D.h, g < nvalid ? xs + g * (D.h + 4) : nullptr, c, qs);
       const int un = u + (int)gridDim.x < nunits ? u + gridDim.x : (pass + 1 < npass ? (int)blockIdx.x : -1);
       if (un >= 0) {
         set_rows(un);
-        mma_load_batch<bf16_t, MNB>(va, vb, wlo, whi, D.h, warp);
+        mma_load_batch<bf16_t, MNB>(va, vb, wlo, whi, D.h, warp, qs);
       }
       block_sum4(c, red, par);
       par ^= 1;
@@ -998,7 +1017,7 @@ static int max_active_of(const Dims& D, int T) {
 // 16-row units; fp32 weights (and other shapes) keep the FMA forms.
 static bool mma_form(const Dims& D) {
   if (D.wdtype == 0) return false;
-  const int sk = D.wdtype == 1 ? 32 : 64;
+  const int sk = D.wdtype == 1 ? 32 : D.wdtype == 2 ? 64 : 128;
   return D.h % sk == 0 && (D.Hq * D.d) % sk == 0 && D.inter % sk == 0 && D.h % 16 == 0 && D.inter % 8 == 0 &&
          (D.d / 2) % 8 == 0 && D.V % 16 == 0 && D.h % 4 == 0;
 }
@@ -1015,6 +1034,7 @@ void launch_qkv(const Dims& D, const DevState& S, const StepBuf& B, const LayerW
     const dim3 g(grid_blocks(D, (D.Hq + 2 * D.Hkv) * (D.d / 16))), b(256);
     const size_t sm = mma_stage_bytes(D, T);
     if (D.wdtype == 1) launch_k(k_qkv_m<bf16_t>, g, b, sm, st, D, S, B, W.attn_norm, (const bf16_t*)W.w_qkv, (const float*)nullptr, layer, T, x);
+    else if (D.wdtype == 3) launch_k(k_qkv_m<fp4_t>, g, b, sm, st, D, S, B, W.attn_norm, (const fp4_t*)W.w_qkv, W.s_qkv, layer, T, x);
     else launch_k(k_qkv_m<fp8_t>, g, b, sm, st, D, S, B, W.attn_norm, (const fp8_t*)W.w_qkv, W.s_qkv, layer, T, x);
     return;
   }
@@ -1032,6 +1052,7 @@ void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, float
   if (mma_form(D)) {
     const dim3 g(grid_blocks(D, (D.h / 16) * cdiv(T, MC))), b(256);
     if (D.wdtype == 1) launch_k(k_oproj_m<bf16_t>, g, b, 0, st, D, B, (const bf16_t*)W.w_o, (const float*)nullptr, T, xres);
+    else if (D.wdtype == 3) launch_k(k_oproj_m<fp4_t>, g, b, 0, st, D, B, (const fp4_t*)W.w_o, W.s_o, T, xres);
     else launch_k(k_oproj_m<fp8_t>, g, b, 0, st, D, B, (const fp8_t*)W.w_o, W.s_o, T, xres);
     return;
   }
@@ -1054,6 +1075,9 @@ void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, cuda
     if (D.wdtype == 1)
       launch_k(k_gateup_m<bf16_t>, g, b, sm, st, D, B, (const bf16_t*)W.w_gate, (const float*)nullptr,
                (const bf16_t*)W.w_up, (const float*)nullptr, T, ma, rt);
+    else if (D.wdtype == 3)
+      launch_k(k_gateup_m<fp4_t>, g, b, sm, st, D, B, (const fp4_t*)W.w_gate, W.s_gate, (const fp4_t*)W.w_up,
+               W.s_up, T, ma, rt);
     else
       launch_k(k_gateup_m<fp8_t>, g, b, sm, st, D, B, (const fp8_t*)W.w_gate, W.s_gate, (const fp8_t*)W.w_up,
                W.s_up, T, ma, rt);
@@ -1077,6 +1101,7 @@ void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaSt
   if (mma_form(D)) {
     const dim3 g(grid_blocks(D, (D.h / 16) * ma * cdiv(T, MC))), b(256);
     if (D.wdtype == 1) launch_k(k_down_m<bf16_t>, g, b, sm, st, D, B, (const bf16_t*)W.w_down, (const float*)nullptr, T, ma);
+    else if (D.wdtype == 3) launch_k(k_down_m<fp4_t>, g, b, sm, st, D, B, (const fp4_t*)W.w_down, W.s_down, T, ma);
     else launch_k(k_down_m<fp8_t>, g, b, sm, st, D, B, (const fp8_t*)W.w_down, W.s_down, T, ma);
     return;
   }
@@ -1126,6 +1151,7 @@ cudaError_t configure_stream_kernels() {
   ALLOW(k_lmhead_s<float>); ALLOW(k_lmhead_s<bf16_t>);
   ALLOW(k_qkv_m<bf16_t>); ALLOW(k_qkv_m<fp8_t>); ALLOW(k_gateup_m<bf16_t>); ALLOW(k_gateup_m<fp8_t>);
   ALLOW(k_down_m<bf16_t>); ALLOW(k_down_m<fp8_t>); ALLOW(k_lmhead_m);
+  ALLOW(k_qkv_m<fp4_t>); ALLOW(k_gateup_m<fp4_t>); ALLOW(k_down_m<fp4_t>);
 #undef ALLOW
   return e;
 }

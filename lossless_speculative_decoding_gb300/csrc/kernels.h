@@ -26,7 +26,7 @@ struct LayerW {
 // Shapes and device state shared by every kernel of a model.
 struct Dims {
   int L, h, Hq, Hkv, d, E, k, S, inter, V;
-  int wdtype;            // 0 f32, 1 bf16, 2 fp8 (attention + experts)
+  int wdtype;            // 0 f32, 1 bf16, 2 fp8, 3 nvfp4 (attention + experts)
   int act_f32;           // KV cache / embeddings / LM head in f32 (else bf16)
   int op_f16;            // operands of the e4m3-weight tensor-core GEMMs are f16 parts of 256 x (else bf16 parts of x)
   int P;                 // page size

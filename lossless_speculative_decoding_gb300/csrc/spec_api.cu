@@ -46,27 +46,30 @@ int elt_bytes(int dtype) { return dtype == SPEC_F32 ? 4 : dtype == SPEC_BF16 ? 2
 int64_t tensor_bytes(const spec_config& c, int idx) {
   const int64_t h = c.hidden, d = c.head_dim, V = c.vocab;
   const int side = c.wdtype == SPEC_F32 ? SPEC_F32 : SPEC_BF16;
-  const bool fp8 = c.wdtype == SPEC_FP8;
+  const bool fp8 = c.wdtype == SPEC_FP8, q4 = c.wdtype == SPEC_NVFP4;
   const int64_t F = c.n_experts + c.n_shared, qkv = (int64_t)(c.n_q_heads + 2 * c.n_kv_heads) * d;
   if (idx < 0 || idx >= N_GLOBAL + PER_LAYER * c.n_layers) return -1;
   if (idx == 0 || idx == 2) return V * h * elt_bytes(side);
   if (idx == 1) return h * 4;
   const int j = (idx - N_GLOBAL) % PER_LAYER;
-  const int w = elt_bytes(c.wdtype);
+  // a matrix of `rows` x `cols` elements: nvfp4 records hold codes (1/2 byte)
+  // and block scales (1/16 byte) per element
+  auto mat = [&](int64_t rows, int64_t cols) { return q4 ? rows * cols / 2 + rows * cols / 16 : rows * cols * elt_bytes(c.wdtype); };
+  auto scl = [&](int64_t fp8_n, int64_t q4_n) { return fp8 ? fp8_n * 4 : q4 ? q4_n * 4 : 0; };
   switch (j) {
     case 0: return h * 4;
-    case 1: return qkv * h * w;
-    case 2: return fp8 ? qkv * 4 : 0;
-    case 3: return h * c.n_q_heads * d * w;
-    case 4: return fp8 ? h * 4 : 0;
+    case 1: return mat(qkv, h);
+    case 2: return scl(qkv, 1);
+    case 3: return mat(h, (int64_t)c.n_q_heads * d);
+    case 4: return scl(h, 1);
     case 5: return h * 4;
     case 6: return (int64_t)c.n_experts * h * elt_bytes(side);
-    case 7: return F * c.inter * h * w;
-    case 8: return fp8 ? F * c.inter * 4 : 0;
-    case 9: return F * c.inter * h * w;
-    case 10: return fp8 ? F * c.inter * 4 : 0;
-    case 11: return F * h * c.inter * w;
-    case 12: return fp8 ? F * h * 4 : 0;
+    case 7: return F * mat(c.inter, h);
+    case 8: return scl(F * c.inter, F);
+    case 9: return F * mat(c.inter, h);
+    case 10: return scl(F * c.inter, F);
+    case 11: return F * mat(h, c.inter);
+    case 12: return scl(F * h, F);
   }
   return -1;
 }
@@ -76,7 +79,14 @@ int check_config(const spec_config& c) {
     return fail(SPEC_ERR_ARG, "config: non-positive shape");
   if (c.head_dim != 64 && c.head_dim != 128) return fail(SPEC_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (c.n_q_heads % c.n_kv_heads) return fail(SPEC_ERR_ARG, "n_q_heads must be a multiple of n_kv_heads");
-  if (c.wdtype < SPEC_F32 || c.wdtype > SPEC_FP8) return fail(SPEC_ERR_ARG, "wdtype");
+  if (c.wdtype < SPEC_F32 || c.wdtype > SPEC_NVFP4) return fail(SPEC_ERR_ARG, "wdtype");
+  if (c.wdtype == SPEC_NVFP4) {
+    // the nvfp4 kernels are the <= 8-row GEMVs: 128-element steps, 16-row units
+    if (c.max_batch * (c.max_draft + 1) > 8)
+      return fail(SPEC_ERR_UNSUPPORTED, "nvfp4 weights: at most 8 rows per verify step");
+    if (c.hidden % 128 || c.inter % 128 || (c.n_q_heads * c.head_dim) % 128 || c.vocab % 16)
+      return fail(SPEC_ERR_UNSUPPORTED, "nvfp4 weights: hidden, inter and Hq * head_dim must be multiples of 128");
+  }
   if (c.n_experts < 0 || c.top_k < 0 || c.n_shared < 0 || c.inter < 4) return fail(SPEC_ERR_ARG, "ffn shape");
   if (c.n_experts > 0 && (c.top_k < 1 || c.top_k > c.n_experts || c.top_k > 16))
     return fail(SPEC_ERR_ARG, "top_k must be in [1, min(n_experts, 16)]");
@@ -91,7 +101,7 @@ int check_config(const spec_config& c) {
   if (c.max_seqs < 1 || c.max_batch < 1 || c.max_batch > c.max_seqs) return fail(SPEC_ERR_ARG, "max_seqs/max_batch");
   if (c.max_ctx < c.max_draft + 2) return fail(SPEC_ERR_ARG, "max_ctx too small");
   if (c.n_pages < 1) return fail(SPEC_ERR_ARG, "n_pages");
-  const int w = elt_bytes(c.wdtype);
+  const int w = c.wdtype == SPEC_NVFP4 ? 1 : elt_bytes(c.wdtype);
   // 16-byte vector loads along every reduction dimension
   if ((c.hidden * w) % 16 || (c.inter * w) % 16 || (c.n_q_heads * c.head_dim * w) % 16 ||
       (c.hidden * elt_bytes(c.wdtype == SPEC_F32 ? SPEC_F32 : SPEC_BF16)) % 16)

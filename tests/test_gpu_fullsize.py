@@ -186,3 +186,9 @@ def test_fullsize_dense4b_block_draft_b8():
     per layer): eight prefixes of one 1,288-row visual prompt, 1,288 down to
     1,029 rows, all scored by the oracle from one prefill."""
     _run("dense4b_bf16_b8", n_seq=8, n_check=8, max_batch=8, steps=1, seed_drafts=9, prefix_step=37)
+
+
+def test_fullsize_moe3b_nvfp4_b1():
+    """The batch-1 3B-MoE workload with NVFP4 attention and expert weights
+    (12 layers, V = 129,280): the nvfp4 warp tensor-core GEMVs."""
+    _run("moe3b_nvfp4_b1", n_seq=1, n_check=1, max_batch=1, steps=6, seed_drafts=11)
