@@ -381,19 +381,20 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn_part(Dims D, DevState S, S
 // contiguous run of them, and its CG consumer groups take every CG-th item.
 // One producer warp looks up the pages and issues the K/V of each item by TMA
 // into a ring of NB chunk buffers (full / empty mbarriers, every wait
-// bounded). The tensor map spans the paged pool (dims: head dim, key in
-// page, (layer, K|V, kv head), page; box 64 dims x 16 keys, 128-byte swizzle
-// -- page sizes are multiples of 16, so a box never straddles pages); boxes
-// past the chunk's last key read page -1 (zero fill). Which block or group
-// computes an item never changes its arithmetic.
+// bounded). The tensor map spans the paged pool (dims: 64 dims, key in page,
+// 64-dim half, (layer, kv head, K|V) plane, page; box 64 dims x KB keys x all
+// halves x K and V, 128-byte swizzle -- page sizes are multiples of 16 (of 64
+// for KB = 64), so a box never straddles pages); boxes past the chunk's last
+// key read page -1 (zero fill). Which block or group computes an item never
+// changes its arithmetic.
 constexpr int ATQ = 32;          // pairs per group at most (four warps)
 constexpr int ATT_NB = 6;        // chunk buffers per block
 
-template <int D_HEAD, int NW, int CG, int NB>
+template <int D_HEAD, int NW, int CG, int NB, int KB = 16>
 struct AttWSmem {
   static constexpr int HB = ATT_CHUNK * 128;            // 64 dims of K or V for the chunk's keys
-  static constexpr int BUF = 2 * (D_HEAD / 64) * HB;    // K and V of one chunk: four 16-key boxes
-  static constexpr int BOXB = BUF / 4;                  // one box: K then V of 16 keys, all dims
+  static constexpr int BUF = 2 * (D_HEAD / 64) * HB;    // K and V of one chunk: ATT_CHUNK / KB boxes
+  static constexpr int BOXB = BUF / (ATT_CHUNK / KB);   // one box: K then V of KB keys, all dims
   static constexpr int KPART = BOXB / 2;                // its K part
   static constexpr int PST = ATT_CHUNK + 8;             // P row stride (bf16), padded
   static constexpr int PW = 2 * 8 * PST * 2;            // one warp's P hi + lo [8 pairs][PST]
@@ -447,16 +448,18 @@ __device__ __forceinline__ float exp2_approx(float x) {
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
 // Shared address of dims col..col+7 of key `key` (0..63) of a chunk buffer,
-// K (kv = 0) or V (kv = 1). The buffer holds four 16-key boxes as the TMA
-// writes them: box j = keys 16 j..16 j + 15, its K part then its V part, each
-// [key][64-dim half] rows of 128 bytes with the 128-byte swizzle (the boxes
-// and parts start on 1024-byte boundaries, so a row's swizzle is its index
-// within the part).
-template <int HALVES>
+// K (kv = 0) or V (kv = 1). The buffer holds the chunk's boxes of KB keys (16,
+// or 64 when a page holds whole chunks) as the TMA writes them: box j = keys
+// KB j .. KB j + KB - 1, its K part then its V part, each [64-dim half][key]
+// rows of 128 bytes with the 128-byte swizzle (boxes and parts start on
+// 1024-byte boundaries, so a row's swizzle is its index within the part).
+// The rows of consecutive keys take consecutive swizzle phases, so an 8-key
+// ldmatrix tile is conflict-free.
+template <int HALVES, int KB>
 __device__ __forceinline__ uint32_t kv_addr(uint32_t base, int key, int col, int kv) {
-  constexpr int BOXB = ATT_CHUNK / 4 * 2 * HALVES * 128, KPART = BOXB / 2;
-  const int row = (key & 15) * HALVES + (col >> 6);
-  return base + (uint32_t)((key >> 4) * BOXB + kv * KPART) + sw128(row, (col & 63) >> 3);
+  constexpr int BOXB = KB * 2 * HALVES * 128, KPART = BOXB / 2;
+  const int row = (col >> 6) * KB + key % KB;
+  return base + (uint32_t)((key / KB) * BOXB + kv * KPART) + sw128(row, (col & 63) >> 3);
 }
 
 // Item i of the (group, kv head, chunk) order.
@@ -470,11 +473,12 @@ struct AttItem {
   }
 };
 
-template <int D_HEAD, int NW, int CG, int NB>
+template <int D_HEAD, int NW, int CG, int NB, int KB>
 __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
     k_attn_w(const __grid_constant__ CUtensorMap kvmap, Dims D, DevState S, StepBuf B, int layer, int T, int R,
              int RG, int n_groups, int inline_merge) {
-  using L = AttWSmem<D_HEAD, NW, CG, NB>;
+  using L = AttWSmem<D_HEAD, NW, CG, NB, KB>;
+  constexpr int NBOX = ATT_CHUNK / KB;                 // TMA boxes per chunk (4 or 1)
   constexpr int HALVES = D_HEAD / 64, HB = L::HB, BUF = L::BUF, PST = L::PST;
   constexpr int KS = D_HEAD / 16;                      // 16-wide K steps over the head dim
   constexpr int NCW = CG * NW;                         // consumer warps; the producer is warp NCW
@@ -503,24 +507,27 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
 
   if (warp == NCW) {
     // ---- producer: item k into buffer k % NB once its previous item is consumed ----
-    // Page ids are looked up eight items ahead, lane 4 u + j holding item
-    // kb + u's 16-key block j (-1 past the chunk's last key; a missing page
-    // sets the error bit), so no lookup latency sits between a freed buffer
-    // and its refill.
+    // Items are resolved eight ahead, lane 4 u + j holding item kb + u's box j:
+    // its page (-1 past the chunk's last key; a missing page sets the error
+    // bit), the key of the box's first row and the item's (layer, kv head)
+    // plane, so neither lookup latency nor the item arithmetic sits between a
+    // freed buffer and its refill.
+    struct Box { int page, key, plane; };
     auto lookup = [&](int kb) {
       const int kk = kb + (lane >> 2), j = lane & 3;
-      int page = -1;
-      if (kk < n) {
+      Box x{-1, 0, 0};
+      if (kk < n && j < NBOX) {
         const AttItem it(s_pref, n_groups, D.Hkv, i0 + kk);
-        const int key = it.c * ATT_CHUNK + 16 * j;
-        if (key <= s_maxpos[it.g]) {
-          page = S.bt[(size_t)s_seq[it.g] * D.max_pages + key / D.P];
-          if (page < 0) atomicOr(S.err, DERR_PAGE);
+        x.key = it.c * ATT_CHUNK + KB * j;
+        x.plane = (layer * D.Hkv + it.hk) * 2;
+        if (x.key <= s_maxpos[it.g]) {
+          x.page = S.bt[(size_t)s_seq[it.g] * D.max_pages + x.key / D.P];
+          if (x.page < 0) atomicOr(S.err, DERR_PAGE);
         }
       }
-      return page;
+      return x;
     };
-    int pcur = lookup(0), pnext = lookup(8);
+    Box pcur = lookup(0), pnext = lookup(8);
     int k = 0;
     for (; k < n; ++k) {
       const int b = k % NB;
@@ -532,23 +539,21 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
         if (lane == 0) atomicOr(S.err, DERR_TIMEOUT);
         break;
       }
-      const AttItem it(s_pref, n_groups, D.Hkv, i0 + k);
-      const int k0 = it.c * ATT_CHUNK;
-      const int page = __shfl_sync(0xffffffffu, pcur, ((k % 8) << 2) | (lane & 3));
+      const int src = ((k % 8) << 2) | (lane & 3);
+      const int page = __shfl_sync(0xffffffffu, pcur.page, src);
+      const int key = __shfl_sync(0xffffffffu, pcur.key, src);
+      const int plane = __shfl_sync(0xffffffffu, pcur.plane, src);
       if (lane == 0)
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_of(full + b)), "r"((uint32_t)BUF)
                      : "memory");
       __syncwarp();
-      if (lane < 4) {
-        // lane j: the K and V (every dim) of keys k0 + 16 j .. k0 + 16 j + 15,
-        // one box of the (layer, kv head) plane pair -- four copies per chunk
-        const int j = lane;
-        const int key = k0 + 16 * j;
-        const uint32_t dst = bufs + b * BUF + j * L::BOXB;
-        const int plane = (layer * D.Hkv + it.hk) * 2;
+      if (lane < NBOX) {
+        // lane j: the K and V (every dim) of keys key .. key + KB - 1, one box
+        // of the (layer, kv head) plane pair
+        const uint32_t dst = bufs + b * BUF + lane * L::BOXB;
         asm volatile(
             "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-            ::"r"(dst), "l"(reinterpret_cast<uint64_t>(&kvmap)), "r"(0), "r"(0), "r"(key % D.P), "r"(plane), "r"(page),
+            ::"r"(dst), "l"(reinterpret_cast<uint64_t>(&kvmap)), "r"(0), "r"(key % D.P), "r"(0), "r"(plane), "r"(page),
               "r"(bar_of(full + b))
             : "memory");
       }
@@ -615,7 +620,7 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
     if (ok && nk < ATT_CHUNK) {
       for (int e = wl * 32 + lane; e < (ATT_CHUNK - nk) * HALVES * 8; e += NW * 32) {
         const int h = e / ((ATT_CHUNK - nk) * 8), r = nk + (e / 8) % (ATT_CHUNK - nk), pc = e % 8;
-        const uint32_t za = kb + (uint32_t)((r >> 4) * L::BOXB + L::KPART + ((r & 15) * HALVES + h) * 128 + pc * 16);
+        const uint32_t za = kb + (uint32_t)((r / KB) * L::BOXB + L::KPART + (h * KB + r % KB) * 128 + pc * 16);
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(za), "r"(0u) : "memory");
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // before TMA refills this buffer
@@ -638,7 +643,7 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
         uint32_t a[4][4];                              // the K step's four key tiles, loaded before any MMA
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
-          ldsm_x4(a[mt], kv_addr<HALVES>(kb, 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1), col, 0));
+          ldsm_x4(a[mt], kv_addr<HALVES, KB>(kb, 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1), col, 0));
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
           mma_bf16(sacc[mt], a[mt], qh[ks][0], qh[ks][1]);
@@ -716,7 +721,7 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
         for (int mt = 0; mt < KS; ++mt) {
           const int col = 16 * mt + 8 * ((lane >> 3) & 1);
           uint32_t a[4];
-          ldsm_x4_t(a, kv_addr<HALVES>(kb, key, col, 1));
+          ldsm_x4_t(a, kv_addr<HALVES, KB>(kb, key, col, 1));
           mma_bf16(o[mt], a, bh0, bh1);
           if (!compact) mma_bf16(olo[mt], a, bl0, bl1);
         }
@@ -773,8 +778,10 @@ cudaError_t configure_attn_kernels() {
 #define ALLOW(k) if ((r = allow_dyn_smem(k)) != cudaSuccess) e = r
   ALLOW((k_attn_part<128, float>)); ALLOW((k_attn_part<128, bf16_t>));
   ALLOW((k_attn_part<64, float>)); ALLOW((k_attn_part<64, bf16_t>));
-  ALLOW((k_attn_w<128, 1, 6, ATT_NB>)); ALLOW((k_attn_w<128, 2, 2, ATT_NB>)); ALLOW((k_attn_w<128, 4, 2, ATT_NB>));
-  ALLOW((k_attn_w<64, 1, 6, ATT_NB>)); ALLOW((k_attn_w<64, 2, 2, ATT_NB>)); ALLOW((k_attn_w<64, 4, 2, ATT_NB>));
+  ALLOW((k_attn_w<128, 1, 6, ATT_NB, 16>)); ALLOW((k_attn_w<128, 2, 2, ATT_NB, 16>)); ALLOW((k_attn_w<128, 4, 2, ATT_NB, 16>));
+  ALLOW((k_attn_w<64, 1, 6, ATT_NB, 16>)); ALLOW((k_attn_w<64, 2, 2, ATT_NB, 16>)); ALLOW((k_attn_w<64, 4, 2, ATT_NB, 16>));
+  ALLOW((k_attn_w<128, 1, 6, ATT_NB, 64>)); ALLOW((k_attn_w<128, 2, 2, ATT_NB, 64>)); ALLOW((k_attn_w<128, 4, 2, ATT_NB, 64>));
+  ALLOW((k_attn_w<64, 1, 6, ATT_NB, 64>)); ALLOW((k_attn_w<64, 2, 2, ATT_NB, 64>)); ALLOW((k_attn_w<64, 4, 2, ATT_NB, 64>));
 #undef ALLOW
   return e;
 }
@@ -822,12 +829,16 @@ void launch_attn_part(const Dims& D, const DevState& S, const StepBuf& B, int la
     // one warp per 8 pairs of a group
     const int nw = (RG * (D.Hq / D.Hkv) + 7) / 8;
 #define ATT_W(DH, NW, CG)                                                                                     \
-  launch_k(k_attn_w<DH, NW, CG, ATT_NB>, dim3(D.n_sm), dim3((CG * NW + 1) * 32),                               \
-           AttWSmem<DH, NW, CG, ATT_NB>::total, st, kvmap, D, S, B, layer, T, R, RG, groups, im)
+  if (att_box_keys(D) == 64)                                                                                  \
+    launch_k(k_attn_w<DH, NW, CG, ATT_NB, 64>, dim3(D.n_sm), dim3((CG * NW + 1) * 32),                        \
+             AttWSmem<DH, NW, CG, ATT_NB, 64>::total, st, kvmap, D, S, B, layer, T, R, RG, groups, im);       \
+  else                                                                                                         \
+    launch_k(k_attn_w<DH, NW, CG, ATT_NB, 16>, dim3(D.n_sm), dim3((CG * NW + 1) * 32),                        \
+             AttWSmem<DH, NW, CG, ATT_NB, 16>::total, st, kvmap, D, S, B, layer, T, R, RG, groups, im)
     if (D.d == 128) {
-      if (nw <= 1) ATT_W(128, 1, 6); else if (nw <= 2) ATT_W(128, 2, 2); else ATT_W(128, 4, 2);
+      if (nw <= 1) { ATT_W(128, 1, 6); } else if (nw <= 2) { ATT_W(128, 2, 2); } else { ATT_W(128, 4, 2); }
     } else {
-      if (nw <= 1) ATT_W(64, 1, 6); else if (nw <= 2) ATT_W(64, 2, 2); else ATT_W(64, 4, 2);
+      if (nw <= 1) { ATT_W(64, 1, 6); } else if (nw <= 2) { ATT_W(64, 2, 2); } else { ATT_W(64, 4, 2); }
     }
 #undef ATT_W
   } else {

@@ -669,11 +669,13 @@ int kv_make_map(CUtensorMap* map, const void* kv, int head_dim, int page_size, i
   if (!fn) return -1;
   if ((reinterpret_cast<uintptr_t>(kv) & 15) || head_dim % 64 || page_size % 16) return -2;
   const int halves = head_dim / 64;
-  const cuuint64_t dims[5] = {64, (cuuint64_t)halves, (cuuint64_t)page_size, (cuuint64_t)planes,
+  // key before half: a box lands in shared memory as [plane][half][key][64],
+  // so the 128-byte rows of consecutive keys take consecutive swizzle phases
+  const cuuint64_t dims[5] = {64, (cuuint64_t)page_size, (cuuint64_t)halves, (cuuint64_t)planes,
                               (cuuint64_t)n_pages};
-  const cuuint64_t strides[4] = {128, (cuuint64_t)head_dim * 2, (cuuint64_t)page_size * head_dim * 2,
+  const cuuint64_t strides[4] = {(cuuint64_t)head_dim * 2, 128, (cuuint64_t)page_size * head_dim * 2,
                                  (cuuint64_t)page_elems * 2};
-  const cuuint32_t box[5] = {64, (cuuint32_t)halves, 16, 2, 1};
+  const cuuint32_t box[5] = {64, (cuuint32_t)(page_size % 64 == 0 ? 64 : 16), (cuuint32_t)halves, 2, 1};
   const cuuint32_t es[5] = {1, 1, 1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kv), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -171,12 +171,16 @@ struct TcMaps {
 // swizzle. Returns 0 on success.
 int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 // 5D bf16 tensor map over the paged KV pool [pages][layer][kv head][K|V][key][dim]
-// for the tensor-core attention: dims (64 dims, head_dim / 64 halves,
-// page_size keys, layers x kv heads x 2 planes, n_pages), box 64 x halves x
-// 16 x 2 x 1 -- the K and V of 16 keys of one (layer, kv head) in one copy --
-// 128-byte swizzle, zero fill outside.
+// for the tensor-core attention: dims (64 dims, page_size keys, head_dim / 64
+// halves, layers x kv heads x 2 planes, n_pages), box 64 x att_box_keys x
+// halves x 2 x 1 -- the K and V of 16 (or 64) keys of one (layer, kv head) in
+// one copy, landing as [plane][half][key][64] -- 128-byte swizzle, zero fill
+// outside.
 int kv_make_map(CUtensorMap* map, const void* kv, int head_dim, int page_size, int planes, int n_pages,
                 size_t page_elems);
+// Keys per KV box of the tensor-core attention: a whole 64-key chunk when
+// pages hold whole chunks (page_size a multiple of 64), else 16.
+inline int att_box_keys(const Dims& D) { return D.P % 64 == 0 ? 64 : 16; }
 // Rewrites W [rows, K] (row-major; bf16, or e4m3 when f8) into the tiled
 // layout the tensor-core GEMM streams (rows a multiple of 128, K of 64).
 int tc_pack_weights(void* dst, const void* src, int rows, int K, int f8, cudaStream_t st);
