@@ -717,13 +717,20 @@ __global__ void __launch_bounds__((CG * NW + 1) * 32, 1)
         ldsm_x2(bh0, bh1, ph + poff);
         if (!compact) ldsm_x2(bl0, bl1, pl + poff);
         const int key = 16 * ks + (lane & 7) + 8 * (lane >> 4);
+        // one-warp groups load the key step's V tiles before any MMA (the
+        // registers are there); wider groups interleave loads and MMAs
+        constexpr int VB = NW == 1 ? KS : 1;
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          const int col = 16 * mt + 8 * ((lane >> 3) & 1);
-          uint32_t a[4];
-          ldsm_x4_t(a, kv_addr<HALVES, KB>(kb, key, col, 1));
-          mma_bf16(o[mt], a, bh0, bh1);
-          if (!compact) mma_bf16(olo[mt], a, bl0, bl1);
+        for (int m0 = 0; m0 < KS; m0 += VB) {
+          uint32_t a[VB][4];
+#pragma unroll
+          for (int mt = 0; mt < VB; ++mt)
+            ldsm_x4_t(a[mt], kv_addr<HALVES, KB>(kb, key, 16 * (m0 + mt) + 8 * ((lane >> 3) & 1), 1));
+#pragma unroll
+          for (int mt = 0; mt < VB; ++mt) {
+            mma_bf16(o[m0 + mt], a[mt], bh0, bh1);
+            if (!compact) mma_bf16(olo[m0 + mt], a[mt], bl0, bl1);
+          }
         }
       }
 #pragma unroll
