@@ -59,6 +59,10 @@ def parse():
                          "workload when the main one is the default; 'none' for none)")
     ap.add_argument("--no-parity", action="store_true", help="skip the oracle parity leg")
     ap.add_argument("--profile-steps", type=int, default=64)
+    ap.add_argument("--ncu-window", type=int, default=0,
+                    help="profiler window: run this many device-resident steps of the main workload between "
+                         "cudaProfilerStart/Stop after the warm-up, then exit (for ncu --profile-from-start off; "
+                         "prints no measurement)")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
@@ -560,6 +564,14 @@ def measure(wl_name: str, args, primary: bool) -> dict:
     for s in range(W):
         dev_step(s)
     st.synchronize()
+    if args.ncu_window:
+        torch.cuda.profiler.start()
+        for s in range(W, W + min(args.ncu_window, KS)):
+            dev_step(s)
+        st.synchronize()
+        torch.cuda.profiler.stop()
+        gm.close()
+        return {"ncu_window": min(args.ncu_window, KS), "workload": wl.name}
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -723,6 +735,10 @@ def run_ours(args):
     extra = args.extra if args.extra is not None else (DEFAULT_EXTRA if args.workload == DEFAULT_WORKLOAD else "none")
     extra = [e for e in extra.split(",") if e and e != "none" and e != args.workload]
     main_res = measure(args.workload, args, primary=True)
+    if args.ncu_window:
+        if rank == 0:
+            print(json.dumps(main_res), flush=True)
+        return
     extras = {e: measure(e, args, primary=False) for e in extra}
     if rank == 0:
         line = {"metric": "committed tokens/s (greedy speculative verify, excl. prefill)",
