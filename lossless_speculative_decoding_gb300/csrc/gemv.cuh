@@ -535,6 +535,53 @@ __device__ __forceinline__ void mma_load_batch(uint4 (&va)[NB], uint4 (&vb)[NB],
 // This warp's partial c[4] of the unit (weight rows g / g + 8 against column
 // x, nullptr = zeros). va/vb hold the warp's first batch on entry
 // (mma_load_batch at s0 = warp).
+// One K step of a unit for this lane: its 16-byte pieces of rows g (va) and
+// g + 8 (vb) at k = step * SK + EPL * q, (nvfp4) their block-scale code pairs
+// sa / sb, against column x (nullptr = zeros), into the NP part accumulators.
+template <class WT, int NP>
+__device__ __forceinline__ void mma_step(const uint4& va, const uint4& vb, uint32_t sa, uint32_t sb, int k,
+                                         const float* x, float (&cp)[NP][4]) {
+  constexpr int EPL = MmaStep<WT>::EPL;
+#pragma unroll
+  for (int h = 0; h < EPL / 8; ++h) {
+    uint32_t wa[4], wb[4];
+    float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+    if (x != nullptr) {
+      x0 = *reinterpret_cast<const float4*>(x + k + 8 * h);
+      x1 = *reinterpret_cast<const float4*>(x + k + 8 * h + 4);
+    }
+    if constexpr (IsQ4<WT>::v) {
+      // group h: elements k + 8h .. k + 8h + 7, block scale h / 2 of the lane's pair
+      const uint32_t ca = h == 0 ? va.x : h == 1 ? va.y : h == 2 ? va.z : va.w;
+      const uint32_t cb = h == 0 ? vb.x : h == 1 ? vb.y : h == 2 ? vb.z : vb.w;
+      q4x8_f16(ca, sa >> (8 * (h >> 1)), wa);
+      q4x8_f16(cb, sb >> (8 * (h >> 1)), wb);
+      mma_group8_f16<NP>(cp, wa, wb, x0, x1);
+    } else {
+      if constexpr (EPL == 8) {
+        wa[0] = va.x; wa[1] = va.y; wa[2] = va.z; wa[3] = va.w;
+        wb[0] = vb.x; wb[1] = vb.y; wb[2] = vb.z; wb[3] = vb.w;
+      } else {
+        e4m3x8_bf16(h ? va.z : va.x, h ? va.w : va.y, wa);
+        e4m3x8_bf16(h ? vb.z : vb.x, h ? vb.w : vb.y, wb);
+      }
+      mma_group8<NP>(cp, wa, wb, x0, x1);
+    }
+  }
+}
+
+// The unit's result for this lane: the parts' accumulators added in part order.
+template <int NP>
+__device__ __forceinline__ void sum_parts(const float (&cp)[NP][4], float (&c)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float t = cp[0][i];
+#pragma unroll
+    for (int part = 1; part < NP; ++part) t += cp[part][i];
+    c[i] = t;
+  }
+}
+
 template <class WT, int NB, int NP = 2>
 __device__ __forceinline__ void mma_part(uint4 (&va)[NB], uint4 (&vb)[NB], const WT* wlo, const WT* whi, int K,
                                          const float* x, float (&c)[4], Q4Scales<NB>& qs) {
@@ -551,47 +598,13 @@ __device__ __forceinline__ void mma_part(uint4 (&va)[NB], uint4 (&vb)[NB], const
     for (int u = 0; u < NB; ++u) {
       const int st = s0 + 8 * u;
       if (st < nsteps) {
-        const int k = st * SK + EPL * q;
-#pragma unroll
-        for (int h = 0; h < EPL / 8; ++h) {
-          uint32_t wa[4], wb[4];
-          if constexpr (IsQ4<WT>::v) {
-            // group h: elements k + 8h .. k + 8h + 7, block scale h / 2 of the lane's pair
-            const uint32_t ca = h == 0 ? va[u].x : h == 1 ? va[u].y : h == 2 ? va[u].z : va[u].w;
-            const uint32_t cb = h == 0 ? vb[u].x : h == 1 ? vb[u].y : h == 2 ? vb[u].z : vb[u].w;
-            q4x8_f16(ca, qs.a[u] >> (8 * (h >> 1)), wa);
-            q4x8_f16(cb, qs.b[u] >> (8 * (h >> 1)), wb);
-            float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-            if (x != nullptr) {
-              x0 = *reinterpret_cast<const float4*>(x + k + 8 * h);
-              x1 = *reinterpret_cast<const float4*>(x + k + 8 * h + 4);
-            }
-            mma_group8_f16<NP>(cp, wa, wb, x0, x1);
-            continue;
-          } else if constexpr (EPL == 8) {
-            wa[0] = va[u].x; wa[1] = va[u].y; wa[2] = va[u].z; wa[3] = va[u].w;
-            wb[0] = vb[u].x; wb[1] = vb[u].y; wb[2] = vb[u].z; wb[3] = vb[u].w;
-          } else {
-            e4m3x8_bf16(h ? va[u].z : va[u].x, h ? va[u].w : va[u].y, wa);
-            e4m3x8_bf16(h ? vb[u].z : vb[u].x, h ? vb[u].w : vb[u].y, wb);
-          }
-          float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-          if (x != nullptr) {
-            x0 = *reinterpret_cast<const float4*>(x + k + 8 * h);
-            x1 = *reinterpret_cast<const float4*>(x + k + 8 * h + 4);
-          }
-          mma_group8<NP>(cp, wa, wb, x0, x1);
-        }
+        uint32_t sa = 0, sb = 0;
+        if constexpr (IsQ4<WT>::v) { sa = qs.a[u]; sb = qs.b[u]; }
+        mma_step<WT, NP>(va[u], vb[u], sa, sb, st * SK + EPL * q, x, cp);
       }
     }
   }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float t = cp[0][i];
-#pragma unroll
-    for (int part = 1; part < NP; ++part) t += cp[part][i];
-    c[i] = t;
-  }
+  sum_parts<NP>(cp, c);
 }
 
 // Sum of the 8 warps' c[4] in warp order into warp 0's c (one barrier). red:
@@ -602,6 +615,24 @@ __device__ __forceinline__ void block_sum4(float (&c)[4], float4* red, int parit
   float4* r = red + parity * 256;
   r[w * 32 + lane] = make_float4(c[0], c[1], c[2], c[3]);
   __syncthreads();
+  if (w == 0) {
+    float4 t = r[lane];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+      const float4 v = r[i * 32 + lane];
+      t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+    }
+    c[0] = t.x; c[1] = t.y; c[2] = t.z; c[3] = t.w;
+  }
+}
+
+// block_sum4 for the 8 warps 0..7 of a block that has more warps: the same
+// order and buffers, with named barrier 1 (256 threads) for the block barrier.
+__device__ __forceinline__ void block_sum4_w8(float (&c)[4], float4* red, int parity) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float4* r = red + parity * 256;
+  r[w * 32 + lane] = make_float4(c[0], c[1], c[2], c[3]);
+  asm volatile("bar.sync 1, 256;" ::: "memory");
   if (w == 0) {
     float4 t = r[lane];
 #pragma unroll

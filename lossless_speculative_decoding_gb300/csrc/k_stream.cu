@@ -887,6 +887,182 @@ __global__ void __launch_bounds__(256, SBPS) k_down_m(Dims D, StepBuf B, const W
   }
 }
 
+// ---------------------------------------------------------------------------
+// Streamed expert GEMVs (steps of at most 8 columns, bf16 or e4m3 weights).
+// The register form keeps one unit's weights in flight per block, so every
+// unit costs a DRAM round trip; here a producer warp runs ahead over the
+// block's units and copies each unit's rows by TMA into a ring of stages in
+// shared memory (a stage: the unit's rows over KST of K, landing as
+// [128-byte chunk][row][128 bytes], 128-byte swizzle), while the 8 consumer
+// warps split each stage's K steps exactly as the register form splits a
+// unit's (warp w: steps w, w + 8, ...; mma_step; block_sum4 in warp order),
+// so a unit's arithmetic is the register form's. Units of the block's shared
+// experts are issued before the kernel waits for the router. Every wait is
+// bounded; a timed-out wait raises DERR_TIMEOUT and the kernel runs on to
+// its end without touching the stage again (no barrier loses a member). Two
+// blocks share an SM (2 x 152 blocks).
+constexpr int FT_MAXSLOT = 8;
+
+__device__ __forceinline__ void ft_tma3d(uint32_t dst, const CUtensorMap* map, int row, int chunk, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(chunk), "r"(bar)
+      : "memory");
+}
+
+// 16 bytes of row r at byte offset kb of a stage box of RB rows.
+template <int RB>
+__device__ __forceinline__ uint4 ft_lds(uint32_t box, int r, int kb) {
+  const uint32_t a = box + (uint32_t)((((kb >> 7) * RB + r) << 7) + ((((kb & 127) >> 4) ^ (r & 7)) << 4));
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+
+// DUAL = 1: gate/up + SwiGLU (ma = gate rows, mb = up rows; a unit is gate
+// rows j..j+7 with up rows j..j+7); DUAL = 0: down (ma; rows o..o+15).
+template <class WT, int DUAL>
+__global__ void __launch_bounds__(288, 2) k_ffn_t(const __grid_constant__ CUtensorMap ma,
+                                                  const __grid_constant__ CUtensorMap mb, Dims D, StepBuf B, int* err,
+                                                  const float* __restrict__ sa, const float* __restrict__ sb, int T,
+                                                  int max_active, int route, int KST, int nslot) {
+  constexpr int SK = MmaStep<WT>::K, EPL = MmaStep<WT>::EPL, ESZ = (int)sizeof(WT);
+  constexpr int RB = DUAL ? 8 : 16;                          // rows of one box
+  extern __shared__ __align__(16) int smi[];
+  __shared__ __align__(8) uint64_t full[FT_MAXSLOT], empty[FT_MAXSLOT];
+  __shared__ float4 red[512];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const int K = DUAL ? D.h : D.inter, rows_e = DUAL ? D.inter : D.h;
+  const int per_slot = rows_e / RB;
+  const int nkc = K / KST;
+  const int box_bytes = RB * KST * ESZ, slot_bytes = (DUAL ? 2 : 1) * box_bytes;
+  const ActCache A(smi, max_active, T * D.NS);
+  const int words = DUAL ? gateup_words(D, T, max_active, route != 0) : ActCache::words(max_active, T * D.NS);
+  const uint32_t ring = ((uint32_t)__cvta_generic_to_shared(smi + words) + 1023u) & ~1023u;
+  auto bar = [](uint64_t* b) { return (uint32_t)__cvta_generic_to_shared(b); };
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nslot; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar(full + s)));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(bar(empty + s)));
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int G = gridDim.x, b0 = blockIdx.x;
+  // stage t of this block: unit i = t / nkc (item b0 + i G), K part kc = t % nkc, slot t % nslot
+  auto issue = [&](int t, int e) {                           // producer lane 0; false: gave up
+    const int s = t % nslot;
+    if (t >= nslot && !mbar_wait_deadline(bar(empty + s), ((t / nslot) - 1) & 1, err)) return false;
+    const int it = b0 + (t / nkc) * G, kc = t % nkc;
+    const int row = e * rows_e + (it % per_slot) * RB;
+    const int chunk = kc * (KST * ESZ / 128);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar(full + s)),
+                 "r"((uint32_t)slot_bytes) : "memory");
+    ft_tma3d(ring + s * slot_bytes, &ma, row, chunk, bar(full + s));
+    if (DUAL) ft_tma3d(ring + s * slot_bytes + box_bytes, &mb, row, chunk, bar(full + s));
+    return true;
+  };
+  // a block's first units of shared experts: known before the router has run
+  int npre = 0;
+  if (warp == 8 && lane == 0) {
+    for (int t = 0; t < nslot; ++t) {
+      const int it = b0 + (t / nkc) * G;
+      if (it >= D.S * per_slot) break;
+      issue(t, D.E + it / per_slot);
+      npre = t + 1;
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (DUAL && route) {
+    float* lg = reinterpret_cast<float*>(smi + ActCache::words(max_active, T * D.NS));
+    int* ids = reinterpret_cast<int*>(lg + T * D.E);
+    float* wts = reinterpret_cast<float*>(ids + T * D.k);
+    int* scratch = reinterpret_cast<int*>(wts + T * D.k);
+    route_in_block(D, B, A, T, lg, ids, wts, scratch);
+  } else {
+    copy_active(B, A, max_active, T * D.NS);
+  }
+  const int nitems = *A.nact * per_slot;
+  const int n_my = b0 < nitems ? (nitems - b0 + G - 1) / G : 0;
+  const int total = n_my * nkc;
+
+  if (warp == 8) {
+    // ---- producer ----
+    int t = npre;
+    if (lane == 0) {
+      for (; t < total; ++t)
+        if (!issue(t, A.ex[(b0 + (t / nkc) * G) / per_slot])) {
+          atomicOr(err, DERR_TIMEOUT);
+          break;
+        }
+      // the block's shared memory outlives every copy: wait (bounded) for the last ones
+      for (int u = max(0, t - nslot); u < t; ++u) mbar_wait_deadline(bar(full + u % nslot), (u / nslot) & 1, nullptr);
+    }
+    return;
+  }
+
+  // ---- consumers: warps 0..7 ----
+  float cp[2][4];
+  const float* x = nullptr;
+  int par = 0;
+  for (int t = 0; t < total; ++t) {
+    const int s = t % nslot, kc = t % nkc;
+    const int it = b0 + (t / nkc) * G, slot = it / per_slot;
+    const int nvalid = min(MC, A.cnt[slot]);
+    const int* pairs = A.perm + A.off[slot];
+    if (kc == 0) {
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cp[part][i] = 0.f;
+      x = g < nvalid ? (DUAL ? B.u + (size_t)(pairs[g] / D.NS) * D.h : B.h_act + (size_t)pairs[g] * D.inter) : nullptr;
+    }
+    const bool ok = mbar_wait_deadline(bar(full + s), (t / nslot) & 1, err);
+    if (!ok && lane == 0) atomicOr(err, DERR_TIMEOUT);
+    if (ok) {
+      const uint32_t box = ring + s * slot_bytes;
+      for (int st = warp; st < KST / SK; st += 8) {
+        const int kl = st * SK + EPL * q;                    // element within the stage
+        const uint4 va = ft_lds<RB>(box, g, kl * ESZ);
+        const uint4 vb = DUAL ? ft_lds<RB>(box + box_bytes, g, kl * ESZ) : ft_lds<RB>(box, g + 8, kl * ESZ);
+        mma_step<WT, 2>(va, vb, 0u, 0u, kc * KST + kl, x, cp);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(empty + s)) : "memory");
+    if (kc != nkc - 1) continue;
+    float c[4];
+    sum_parts<2>(cp, c);
+    block_sum4_w8(c, red, par);
+    par ^= 1;
+    if (warp != 0) continue;
+    const int e = A.ex[slot];
+    if constexpr (DUAL) {
+      const int j = (it % per_slot) * 8 + g;
+      const float s0 = sa != nullptr ? sa[(size_t)e * D.inter + j] : 1.f;
+      const float s1 = sb != nullptr ? sb[(size_t)e * D.inter + j] : 1.f;
+#pragma unroll
+      for (int ee = 0; ee < 2; ++ee) {
+        const int col = 2 * q + ee;
+        if (col < nvalid) B.h_act[(size_t)pairs[col] * D.inter + j] = silu(c[ee] * s0) * (c[2 + ee] * s1);
+      }
+    } else {
+      const int o = (it % per_slot) * 16 + g;
+      const float s0 = sa != nullptr ? sa[(size_t)e * D.h + o] : 1.f;
+      const float s1 = sa != nullptr ? sa[(size_t)e * D.h + o + 8] : 1.f;
+#pragma unroll
+      for (int ee = 0; ee < 2; ++ee) {
+        const int col = 2 * q + ee;
+        if (col >= nvalid) continue;
+        float* y = B.y + (size_t)pairs[col] * D.h;
+        y[o] = c[ee] * s0;
+        y[o + 8] = c[2 + ee] * s1;
+      }
+    }
+  }
+}
+
 // Final RMSNorm + LM head + greedy argmax (+ accept/commit), bf16 weights.
 // Warp 0's lanes keep the running best (value, index) of the block's rows for
 // their two columns; the block's candidates go to scratch and the last block
@@ -1065,11 +1241,33 @@ void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, float
   }
 }
 
-void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
+// Ring slots of the streamed form that fit next to `words` ints of shared
+// memory, two blocks to an SM (at least 2; 0: the streamed form does not fit).
+static int ffn_slots(size_t words, int slot_bytes) {
+  const long avail = 100L * 1024 - (long)words * 4 - 1024;   // two blocks an SM   // + 8.3 KB static: below 227 KB
+  const int n = (int)std::min<long>(FT_MAXSLOT, avail / slot_bytes);
+  return n >= 2 ? n : 0;
+}
+
+void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, int* err, cudaStream_t st) {
   const int ma = max_active_of(D, T);
   const bool route = route_in_gateup(T);
   const size_t sm = (size_t)gateup_words(D, T, ma, route) * sizeof(int);
   const int rt = route ? 1 : 0;
+  if (W.ffn_map != nullptr && mma_form(D) && T <= MC && (D.wdtype == 1 || D.wdtype == 2)) {
+    const int esz = D.wdtype == 1 ? 2 : 1, slot_bytes = 2 * 8 * W.kst_gu * esz;
+    const int ns = ffn_slots(gateup_words(D, T, ma, route), slot_bytes);
+    if (ns > 0) {
+      const size_t smt = sm + 1024 + (size_t)ns * slot_bytes;
+      if (D.wdtype == 1)
+        launch_k(k_ffn_t<bf16_t, 1>, dim3(2 * D.n_sm), dim3(288), smt, st, W.ffn_map[0], W.ffn_map[1], D, B, err,
+                 (const float*)nullptr, (const float*)nullptr, T, ma, rt, W.kst_gu, ns);
+      else
+        launch_k(k_ffn_t<fp8_t, 1>, dim3(2 * D.n_sm), dim3(288), smt, st, W.ffn_map[0], W.ffn_map[1], D, B, err,
+                 W.s_gate, W.s_up, T, ma, rt, W.kst_gu, ns);
+      return;
+    }
+  }
   if (mma_form(D)) {
     const dim3 g(grid_blocks(D, ma * (D.inter / 8) * cdiv(T, MC))), b(256);
     if (D.wdtype == 1)
@@ -1095,9 +1293,23 @@ void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, cuda
   }
 }
 
-void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st) {
+void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, int* err, cudaStream_t st) {
   const int ma = max_active_of(D, T);
   const size_t sm = (size_t)ActCache::words(ma, T * D.NS) * sizeof(int);
+  if (W.ffn_map != nullptr && mma_form(D) && T <= MC && (D.wdtype == 1 || D.wdtype == 2)) {
+    const int esz = D.wdtype == 1 ? 2 : 1, slot_bytes = 16 * W.kst_dn * esz;
+    const int ns = ffn_slots(ActCache::words(ma, T * D.NS), slot_bytes);
+    if (ns > 0) {
+      const size_t smt = sm + 1024 + (size_t)ns * slot_bytes;
+      if (D.wdtype == 1)
+        launch_k(k_ffn_t<bf16_t, 0>, dim3(2 * D.n_sm), dim3(288), smt, st, W.ffn_map[2], W.ffn_map[2], D, B, err,
+                 (const float*)nullptr, (const float*)nullptr, T, ma, 0, W.kst_dn, ns);
+      else
+        launch_k(k_ffn_t<fp8_t, 0>, dim3(2 * D.n_sm), dim3(288), smt, st, W.ffn_map[2], W.ffn_map[2], D, B, err,
+                 W.s_down, (const float*)nullptr, T, ma, 0, W.kst_dn, ns);
+      return;
+    }
+  }
   if (mma_form(D)) {
     const dim3 g(grid_blocks(D, (D.h / 16) * ma * cdiv(T, MC))), b(256);
     if (D.wdtype == 1) launch_k(k_down_m<bf16_t>, g, b, sm, st, D, B, (const bf16_t*)W.w_down, (const float*)nullptr, T, ma);
@@ -1119,6 +1331,16 @@ void launch_combine(const Dims& D, const StepBuf& B, float* x, int T, cudaStream
   int blocks = cdiv(n4, 256);
   if (blocks > 8 * D.n_sm) blocks = 8 * D.n_sm;
   launch_k(k_combine, dim3(blocks), dim3(256), 0, st, D, B, x, T);
+}
+
+// K elements a stage of the streamed expert GEMVs covers: K split into equal
+// parts of whole TMA chunks (128 bytes) with 16 rows of a part <= 48 KB; 0
+// when no split fits.
+int ffn_stage_k(int K, int esz) {
+  const int step = 128 / esz;                      // a TMA chunk; a multiple of the MMA step
+  for (int n = 1; n <= K / step; ++n)
+    if (K % n == 0 && (K / n) % step == 0 && 16L * (K / n) * esz <= 48 * 1024) return K / n;
+  return 0;
 }
 
 int lmhead_step_warps(const Dims& D) { return grid_for(D, D.V / 4) * GEMV_WARPS; }
@@ -1152,6 +1374,7 @@ cudaError_t configure_stream_kernels() {
   ALLOW(k_qkv_m<bf16_t>); ALLOW(k_qkv_m<fp8_t>); ALLOW(k_gateup_m<bf16_t>); ALLOW(k_gateup_m<fp8_t>);
   ALLOW(k_down_m<bf16_t>); ALLOW(k_down_m<fp8_t>); ALLOW(k_lmhead_m);
   ALLOW(k_qkv_m<fp4_t>); ALLOW(k_gateup_m<fp4_t>); ALLOW(k_down_m<fp4_t>);
+  ALLOW((k_ffn_t<bf16_t, 1>)); ALLOW((k_ffn_t<bf16_t, 0>)); ALLOW((k_ffn_t<fp8_t, 1>)); ALLOW((k_ffn_t<fp8_t, 0>));
 #undef ALLOW
   return e;
 }

@@ -647,6 +647,26 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// 3D byte map over a stack of weight rows ([rows][K] of esz-byte elements,
+// row-major) for the streamed GEMVs: dims (128 bytes, rows, K * esz / 128
+// chunks) -- the chunk before the row in memory, after it in the map, so a
+// box lands as [chunk][row][128 bytes] -- box 128 x box_rows x box_chunks,
+// 128-byte swizzle.
+int gemv_make_map(CUtensorMap* map, const void* base, int esz, uint64_t K, uint64_t rows, uint32_t box_rows,
+                  uint32_t box_chunks) {
+  auto fn = encode_fn();
+  if (!fn) return -1;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (K * esz) % 128) return -2;
+  const cuuint64_t dims[3] = {128, rows, K * esz / 128};
+  const cuuint64_t strides[2] = {K * esz, 128};
+  const cuuint32_t box[3] = {128, box_rows, box_chunks};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -3;
+}
+
 // 2D bf16 tensor map over rows of `inner` elements (row-major), box of
 // 64 x box_rows, 128-byte swizzle, zero fill outside.
 int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {

@@ -21,6 +21,10 @@ struct LayerW {
   const void* w_gate; const float* s_gate;
   const void* w_up; const float* s_up;
   const void* w_down; const float* s_down;
+  // streamed expert GEMVs (<= 8 rows, bf16 / e4m3): tensor maps of w_gate,
+  // w_up, w_down (null: the register form) and the K per stage of each
+  const CUtensorMap* ffn_map;
+  int kst_gu, kst_dn;
 };
 
 // Shapes and device state shared by every kernel of a model.
@@ -109,10 +113,10 @@ void launch_oproj(const Dims& D, const StepBuf& B, const LayerW& W, int T, float
 // full: always compute top-k and the permutation (the tensor-core path needs them)
 void launch_router(const Dims& D, const StepBuf& B, const LayerW& W, int T, const float* xres, bool full,
                    cudaStream_t st);
-void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
+void launch_gateup(const Dims& D, const StepBuf& B, const LayerW& W, int T, int* err, cudaStream_t st);
 // At small T the router kernel writes only logits and gate/up routes in its prologue.
 bool route_in_gateup(int T);
-void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, cudaStream_t st);
+void launch_down(const Dims& D, const StepBuf& B, const LayerW& W, int T, int* err, cudaStream_t st);
 // In-place expert combine of the residual x.
 void launch_combine(const Dims& D, const StepBuf& B, float* x, int T, cudaStream_t st);
 void launch_lmhead(const Dims& D, const StepBuf& B, const void* lm_head, const float* final_norm,
@@ -123,6 +127,7 @@ void launch_lmhead_step(const Dims& D, const DevState& S, const StepBuf& B, cons
                         const float* final_norm, const float* x, int T, float* logits_dbg, bool commit,
                         int n_seq, int K, cudaStream_t st);
 int lmhead_step_warps(const Dims& D);
+int ffn_stage_k(int K, int esz);
 void launch_argmax(const StepBuf& B, int T, cudaStream_t st);
 
 // ---- tensor-core GEMM (k_tc.cu) ---------------------------------------------
@@ -178,6 +183,12 @@ int tc_make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t row
 // outside.
 int kv_make_map(CUtensorMap* map, const void* kv, int head_dim, int page_size, int planes, int n_pages,
                 size_t page_elems);
+// 3D byte tensor map over a stack of [rows][K] weight rows (esz bytes an
+// element) for the streamed expert GEMVs: box 128 bytes x box_rows rows x
+// box_chunks 128-byte chunks of K, landing as [chunk][row][128] with the
+// 128-byte swizzle. Returns 0 on success.
+int gemv_make_map(CUtensorMap* map, const void* base, int esz, uint64_t K, uint64_t rows, uint32_t box_rows,
+                  uint32_t box_chunks);
 // Keys per KV box of the tensor-core attention: a whole 64-key chunk when
 // pages hold whole chunks (page_size a multiple of 64), else 16.
 inline int att_box_keys(const Dims& D) { return D.P % 64 == 0 ? 64 : 16; }

@@ -185,6 +185,7 @@ struct spec_model {
   std::vector<void*> allocs;
   std::vector<void*> wptr;         // device pointer per tensor (nullptr if absent)
   std::vector<LayerW> layers;
+  std::vector<CUtensorMap> ffn_maps;       // [layer][gate, up, down] of the streamed expert GEMVs
   void* tok_embed = nullptr;
   void* lm_head = nullptr;
   float* final_norm = nullptr;
@@ -360,9 +361,9 @@ struct spec_model {
       run_k(p, KC_ATTN, [&] { launch_attn_part(D, S, B, l, T, R_rows, kv_map, stream); });
       run_k(p, KC_OPROJ, [&] { launch_oproj(D, B, W, T, cur, stream); });
       run_k(p, KC_ROUTER, [&] { launch_router(D, B, W, T, cur, false, stream); });
-      run_k(p, KC_GATEUP, [&] { launch_gateup(D, B, W, T, stream); });
+      run_k(p, KC_GATEUP, [&] { launch_gateup(D, B, W, T, S.err, stream); });
       if (p) cudaMemcpyAsync(p->act + p->nact++, B.n_active, 4, cudaMemcpyDeviceToHost, stream);
-      run_k(p, KC_DOWN, [&] { launch_down(D, B, W, T, stream); });
+      run_k(p, KC_DOWN, [&] { launch_down(D, B, W, T, S.err, stream); });
       run_k(p, KC_COMBINE, [&] { launch_combine(D, B, cur, T, stream); });
     }
     return cur;
@@ -505,6 +506,7 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
     L.w_o = w[3]; L.s_o = (const float*)w[4]; L.ffn_norm = (const float*)w[5]; L.w_router = w[6];
     L.w_gate = w[7]; L.s_gate = (const float*)w[8]; L.w_up = w[9]; L.s_up = (const float*)w[10];
     L.w_down = w[11]; L.s_down = (const float*)w[12];
+    L.ffn_map = nullptr; L.kst_gu = L.kst_dn = 0;
     m->layers.push_back(L);
   }
 
@@ -575,6 +577,27 @@ int spec_init_model(const spec_config* cfg_in, const void* const* host_tensors, 
                         (D.Hq * D.d) % 64 == 0 && D.h % 64 == 0 && D.inter % 64 == 0;
     m->use_tc = (c.wdtype == SPEC_BF16 || c.wdtype == SPEC_FP8) && c.max_batch * m->R > 8 && shapes;
     D.op_f16 = m->use_tc && c.wdtype == SPEC_FP8 ? 1 : 0;
+  }
+  if (!m->use_tc && (c.wdtype == SPEC_BF16 || c.wdtype == SPEC_FP8)) {
+    // steps of at most 8 rows: the expert GEMVs stream their weights by TMA
+    // when the shapes split into whole 128-byte chunks (else the register form)
+    const int esz = c.wdtype == SPEC_BF16 ? 2 : 1;
+    const int kgu = ffn_stage_k(D.h, esz), kdn = ffn_stage_k(D.inter, esz);
+    if (kgu > 0 && kdn > 0 && D.inter % 8 == 0 && D.h % 16 == 0) {
+      const int F = D.E + D.S;
+      m->ffn_maps.resize((size_t)3 * D.L);
+      for (int l = 0; l < D.L; ++l) {
+        LayerW& W = m->layers[l];
+        CUtensorMap* mp = m->ffn_maps.data() + 3 * l;
+        if (gemv_make_map(mp, W.w_gate, esz, D.h, (uint64_t)F * D.inter, 8, kgu * esz / 128) ||
+            gemv_make_map(mp + 1, W.w_up, esz, D.h, (uint64_t)F * D.inter, 8, kgu * esz / 128) ||
+            gemv_make_map(mp + 2, W.w_down, esz, D.inter, (uint64_t)F * D.h, 16, kdn * esz / 128))
+          return fail(SPEC_ERR_CUDA, "expert weight tensor maps");
+        W.ffn_map = mp;
+        W.kst_gu = kgu;
+        W.kst_dn = kdn;
+      }
+    }
   }
   if (m->use_tc) {
     const int qkv_rows = (D.Hq + 2 * D.Hkv) * D.d;
