@@ -329,8 +329,9 @@ int spec_tc_gemm_test(const void* a_dev, const void* a2_dev, const float* a_scal
  *   logits_dev:  [n_seq][K+1][vocab] f32, 16-byte aligned (the layout
  *                spec_debug_logits writes).
  *   drafts_dev:  [n_seq][K] int32 draft tokens.
- *   q_dev:       [n_seq][K][vocab] f32 drafter probabilities, or NULL for a
- *                drafter certain of its drafts (q_j one-hot at d_j).
+ *   q_dev:       [n_seq][K][vocab] f32 drafter probabilities (16-byte
+ *                aligned), or NULL for a drafter certain of its drafts (q_j
+ *                one-hot at d_j).
  *   u_accept_dev [n_seq][K], u_sample_dev [n_seq][K+1]: f32 uniforms in [0, 1).
  *   out_accepted_dev / out_token_dev: [n_seq] int32: drafts accepted and the
  *                appended token; -1 / -1 for a sequence with a draft outside
@@ -342,6 +343,29 @@ int spec_rejection_sample(const float* logits_dev, const int32_t* drafts_dev, co
                           const float* u_accept_dev, const float* u_sample_dev, int n_seq, int K, int vocab,
                           float temperature, int32_t* out_accepted_dev, int32_t* out_token_dev,
                           uintptr_t cuda_stream);
+/* The same rule as one cooperative launch that spreads each sequence over
+ * several blocks, all resident at once. Each row is cut into tiles of 1,024
+ * values; the blocks of a sequence share the row's tiles and meet at a
+ * counter of the sequence after each row, and only the rows the rule reaches
+ * are read. The draw picks its tile from per-tile sums and then scans that
+ * one tile. Same arguments, plus:
+ *   ws_dev:   a caller-owned device workspace, 16-byte aligned, of at least
+ *             spec_rejection_sample_ws_bytes(n_seq, K) bytes. It must be
+ *             zero-filled before its first use; every call leaves its
+ *             counters at zero again, so it can be reused by later calls on
+ *             the same stream. One call at a time per workspace.
+ * The per-tile sums use the fast hardware exponential and another summation
+ * order than spec_rejection_sample's, so the two can differ where a decision
+ * lies within rounding of its threshold. A sequence reports (-2, -1) if a
+ * wait between its blocks ran past its deadline (not expected: the launch is
+ * cooperative); its workspace must then be zero-filled again.
+ * Errors: as spec_rejection_sample; SPEC_ERR_ARG for a small or misaligned
+ * workspace; SPEC_ERR_CUDA when the launch cannot be made cooperative. */
+int64_t spec_rejection_sample_ws_bytes(int n_seq, int K);
+int spec_rejection_sample_ws(const float* logits_dev, const int32_t* drafts_dev, const float* q_dev,
+                             const float* u_accept_dev, const float* u_sample_dev, int n_seq, int K, int vocab,
+                             float temperature, int32_t* out_accepted_dev, int32_t* out_token_dev, void* ws_dev,
+                             size_t ws_bytes, uintptr_t cuda_stream);
 
 /* Same computation as spec_lmhead_argmax for callers that cannot allocate
  * device memory (no cudaMalloc of their own, none by the library): the

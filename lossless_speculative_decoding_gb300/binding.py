@@ -95,6 +95,11 @@ _SIGS = [
     ("spec_rejection_sample", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]),
+    ("spec_rejection_sample_ws_bytes", ctypes.c_int64, [ctypes.c_int, ctypes.c_int]),
+    ("spec_rejection_sample_ws", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_size_t, ctypes.c_size_t]),
     ("spec_strerror", ctypes.c_char_p, [ctypes.c_int]),
     ("spec_last_error", ctypes.c_char_p, []),
     ("spec_pool_create", ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -331,6 +336,19 @@ def spec_rejection_sample(logits_dev, drafts_dev, q_dev, u_accept_dev, u_sample_
     _check(lib().spec_rejection_sample(_ptr(logits_dev), _ptr(drafts_dev), _ptr(q_dev), _ptr(u_accept_dev),
                                        _ptr(u_sample_dev), n_seq, K, vocab, float(temperature),
                                        _ptr(out_accepted_dev), _ptr(out_token_dev), cuda_stream))
+
+
+def spec_rejection_sample_ws_bytes(n_seq: int, K: int) -> int:
+    return _check(lib().spec_rejection_sample_ws_bytes(n_seq, K))
+
+
+def spec_rejection_sample_ws(logits_dev, drafts_dev, q_dev, u_accept_dev, u_sample_dev, n_seq: int, K: int,
+                             vocab: int, temperature: float, out_accepted_dev, out_token_dev, ws_dev, ws_bytes: int,
+                             cuda_stream: int = 0) -> None:
+    _check(lib().spec_rejection_sample_ws(_ptr(logits_dev), _ptr(drafts_dev), _ptr(q_dev), _ptr(u_accept_dev),
+                                          _ptr(u_sample_dev), n_seq, K, vocab, float(temperature),
+                                          _ptr(out_accepted_dev), _ptr(out_token_dev), _ptr(ws_dev), ws_bytes,
+                                          cuda_stream))
 
 
 def spec_tc_gemm_test(a_dev, a2_dev, b_dev, b_lo_dev, M: int, N: int, K: int, dual: int, out_dev, err_dev,

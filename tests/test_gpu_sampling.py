@@ -1,5 +1,7 @@
-"""Rejection-sampling verification on the GPU (spec_rejection_sample) against
-the oracle (oracle/sampling.py) and against the law it must produce.
+"""Rejection-sampling verification on the GPU against the oracle
+(oracle/sampling.py) and against the law it must produce, through both entry
+points: spec_rejection_sample (one block per sequence) and
+spec_rejection_sample_ws (row statistics split over many blocks).
 
 * Parity: the same logits, drafts, drafter distributions and uniforms give the
   oracle's (accepted, token) exactly, except where the oracle's float64
@@ -26,16 +28,28 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def _run(logits, drafts, q, ua, us, temperature):
+@pytest.fixture(params=["block", "split"])
+def form(request):
+    return request.param
+
+
+def _run(logits, drafts, q, ua, us, temperature, form="block", ws=None):
     import torch
     from lossless_speculative_decoding_gb300 import binding as B
     n, K1, V = logits.shape
     acc = torch.full((n,), -7, dtype=torch.int32, device="cuda")
     tok = torch.full((n,), -7, dtype=torch.int32, device="cuda")
-    B.spec_rejection_sample(_dev(logits.astype(np.float32)), _dev(drafts.astype(np.int32)) if K1 > 1 else None,
-                            None if q is None else _dev(q.astype(np.float32)),
-                            _dev(ua.astype(np.float32)) if K1 > 1 else None, _dev(us.astype(np.float32)),
-                            n, K1 - 1, V, temperature, acc, tok, 0)
+    args = (_dev(logits.astype(np.float32)), _dev(drafts.astype(np.int32)) if K1 > 1 else None,
+            None if q is None else _dev(q.astype(np.float32)),
+            _dev(ua.astype(np.float32)) if K1 > 1 else None, _dev(us.astype(np.float32)),
+            n, K1 - 1, V, temperature, acc, tok)
+    if form == "block":
+        B.spec_rejection_sample(*args, 0)
+    else:
+        nb = B.spec_rejection_sample_ws_bytes(n, K1 - 1)
+        if ws is None:
+            ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+        B.spec_rejection_sample_ws(*args, ws, nb, 0)
     torch.cuda.synchronize()
     return acc.cpu().numpy(), tok.cpu().numpy()
 
@@ -58,11 +72,11 @@ def _inputs(rng, n, K, V, with_q, scale=3.0):
 
 @pytest.mark.parametrize("V,n,with_q,temp", [(1000, 48, False, 1.0), (1000, 48, True, 0.7), (129280, 6, False, 1.0),
                                              (129280, 4, True, 1.3)])
-def test_parity_with_oracle(V, n, with_q, temp):
+def test_parity_with_oracle(V, n, with_q, temp, form):
     rng = np.random.default_rng(V + n + int(with_q))
     K = 3
     logits, drafts, q, ua, us = _inputs(rng, n, K, V, with_q)
-    acc, tok = _run(logits, drafts, q, ua, us, temp)
+    acc, tok = _run(logits, drafts, q, ua, us, temp, form)
     exempt = 0
     for s in range(n):
         tr = {}
@@ -79,7 +93,7 @@ def test_parity_with_oracle(V, n, with_q, temp):
     assert ((acc >= 0) & (acc <= K) & (tok >= 0) & (tok < V)).all()
 
 
-def test_emitted_tokens_follow_the_target():
+def test_emitted_tokens_follow_the_target(form):
     rng = np.random.default_rng(21)
     n, K, V = 200_000, 2, 16
     base = rng.standard_normal((K + 1, V)) * 1.2
@@ -89,7 +103,7 @@ def test_emitted_tokens_follow_the_target():
     drafts = np.stack([rng.choice(V, size=n, p=q1[j]) for j in range(K)], axis=1)
     ua = rng.random((n, K))
     us = rng.random((n, K + 1))
-    acc, tok = _run(logits, drafts, q, ua, us, 1.0)
+    acc, tok = _run(logits, drafts, q, ua, us, 1.0, form)
     assert ((acc >= 0) & (acc <= K)).all()
     first = np.where(acc >= 1, drafts[:, 0], tok)
     second = np.where(acc >= 2, drafts[:, 1], tok)[acc >= 1]
@@ -104,28 +118,62 @@ def test_emitted_tokens_follow_the_target():
     assert float(((obs - exp) ** 2 / exp).sum()) > 1000.0
 
 
-def test_greedy_limit_is_the_greedy_rule():
+@pytest.mark.parametrize("n,V", [(64, 4096), (12, 129280)])
+def test_greedy_limit_is_the_greedy_rule(form, n, V):
     rng = np.random.default_rng(22)
-    n, K, V = 64, 5, 4096
+    K = 5
     g = rng.integers(0, V, (n, K + 1))
     logits = rng.standard_normal((n, K + 1, V)).astype(np.float32)
     for s in range(n):
         logits[s, np.arange(K + 1), g[s]] += 60.0
     drafts = np.where(rng.random((n, K)) < 0.7, g[:, :K], rng.integers(0, V, (n, K)))
-    acc, tok = _run(logits, drafts, None, rng.random((n, K)), rng.random((n, K + 1)), 0.05)
+    acc, tok = _run(logits, drafts, None, rng.random((n, K)), rng.random((n, K + 1)), 0.05, form)
     for s in range(n):
         assert (int(acc[s]), int(tok[s])) == oracle.accept(list(drafts[s]), list(g[s]))
 
 
-def test_errors_are_reported():
+def test_errors_are_reported(form):
     from lossless_speculative_decoding_gb300 import binding as B
     rng = np.random.default_rng(23)
     logits, drafts, _, ua, us = _inputs(rng, 3, 2, 64, False)
     drafts[1, 0] = 64                                   # not a token
-    acc, tok = _run(logits, drafts, None, ua, us, 1.0)
+    acc, tok = _run(logits, drafts, None, ua, us, 1.0, form)
     assert (int(acc[1]), int(tok[1])) == (-1, -1)
     assert acc[0] >= 0 and acc[2] >= 0
     with pytest.raises(B.SpecError):
-        _run(logits[:, :, :62], drafts, None, ua, us, 1.0)     # vocab not a multiple of 4
+        _run(logits[:, :, :62], drafts, None, ua, us, 1.0, form)     # vocab not a multiple of 4
     with pytest.raises(B.SpecError):
-        _run(logits, drafts, None, ua, us, 0.0)                 # temperature must be positive
+        _run(logits, drafts, None, ua, us, 0.0, form)                 # temperature must be positive
+
+
+def test_split_form_workspace_is_checked():
+    import torch
+    from lossless_speculative_decoding_gb300 import binding as B
+    rng = np.random.default_rng(24)
+    logits, drafts, _, ua, us = _inputs(rng, 4, 3, 256, False)
+    nb = B.spec_rejection_sample_ws_bytes(4, 3)
+    assert nb >= 4 * 4 * min(64, -(-1024 // 16)) * 8        # at least the rows' partial statistics
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    acc = torch.zeros(4, dtype=torch.int32, device="cuda")
+    with pytest.raises(B.SpecError) as e:
+        B.spec_rejection_sample_ws(_dev(logits), _dev(drafts.astype(np.int32)), None, _dev(ua), _dev(us), 4, 3, 256,
+                                   1.0, acc, acc, ws, nb - 8, 0)
+    assert e.value.code == B.SPEC_ERR_ARG
+
+
+def test_split_form_workspace_is_reusable():
+    """Each call leaves its counters at zero: calls in a row on one workspace
+    give what calls on fresh workspaces give (rows walked by several blocks
+    per sequence, with and without a drafter distribution)."""
+    import torch
+    from lossless_speculative_decoding_gb300 import binding as B
+    rng = np.random.default_rng(25)
+    n, K, V = 8, 3, 129280
+    nb = B.spec_rejection_sample_ws_bytes(n, K)
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    for with_q in (False, True, False):
+        logits, drafts, q, ua, us = _inputs(rng, n, K, V, with_q)
+        got = _run(logits, drafts, q, ua, us, 1.0, "split", ws=ws)
+        fresh = _run(logits, drafts, q, ua, us, 1.0, "split")
+        assert (got[0] == fresh[0]).all() and (got[1] == fresh[1]).all()
+        assert int(ws[: 8 * n].sum().item()) == 0, "counters left non-zero"
