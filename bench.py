@@ -373,6 +373,11 @@ def steady_state_prompts(wl, prompts, rank: int):
     return pre, out
 
 
+# Temperature of the bench's sampled verify steps: the random-init models are
+# near-flat at 1, and at 0.05 the drafts the schedule makes agree with the
+# greedy tokens are accepted most of the time.
+SAMPLED_TEMPERATURE = 0.05
+
 # Per-draft acceptance 57.6% (jina-ocr-v1 thread): the sampling workload's
 # drafter proposes the target's heavy token with probability 0.7, which holds
 # 0.576 / 0.7 of the row's mass.
@@ -667,6 +672,45 @@ def measure(wl_name: str, args, primary: bool) -> dict:
         gm.release(i)
     e2e_s, e2e_committed = aggregate(e2e_s, e2e_committed, device="cuda")
 
+    # 4b) sampled verify steps (spec_verify_step_sample_dev): the same
+    # sequences and drafts, rejection-sampling acceptance in the step's graph
+    sampled = None
+    if primary and rank == 0:
+        prefill_all()
+        for i in ids:
+            B.spec_reserve_seq(h, i, min(max_ctx, prompts[i].length + 1 + (W + KS + 1) * R))
+        with torch.cuda.stream(st):
+            gu = torch.Generator(device="cuda").manual_seed(11)
+            d_ua = torch.rand(total * NB * K, device="cuda", generator=gu)
+            d_us = torch.rand(total * NB * R, device="cuda", generator=gu)
+        st.synchronize()
+
+        def smp_step(s):
+            B.spec_verify_step_sample_dev(h, NB, d_seq, d_drafts.data_ptr() + s * NB * K * esz, d_nd,
+                                          d_ua.data_ptr() + s * NB * K * 4, d_us.data_ptr() + s * NB * R * 4,
+                                          SAMPLED_TEMPERATURE, d_acc.data_ptr() + s * NB * esz,
+                                          d_bon.data_ptr() + s * NB * esz)
+
+        for s in range(W):
+            smp_step(s)
+        st.synchronize()
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e_s[0].record(st)
+        for s in range(W, W + KS):
+            smp_step(s)
+        e_s[1].record(st)
+        e_s[1].synchronize()
+        B.spec_sync_seqs(h)
+        acc_s = d_acc.cpu().numpy().reshape(total, NB)[W:W + KS]
+        ms_s = e_s[0].elapsed_time(e_s[1])
+        sampled = {"entry": "spec_verify_step_sample_dev",
+                   "graph": "decoder forward, LM head writing the step logits, k_rs_coop, commit",
+                   "temperature": SAMPLED_TEMPERATURE, "ms_per_step": ms_s / KS,
+                   "tokens_per_s": float((acc_s + 1).sum()) / (ms_s * 1e-3), "tau": float((acc_s + 1).mean()),
+                   "valid": bool((acc_s >= 0).all())}
+        for i in ids:
+            gm.release(i)
+
     # 5) roofline of the dominant kernel and of the whole step
     peaks = measured_peaks()
     T = NB * R
@@ -748,6 +792,9 @@ def measure(wl_name: str, args, primary: bool) -> dict:
                        "e2e_tokens_match": e2e_ok},
             "setup_s": round(time.time() - t_setup, 1),
         })
+        if sampled is not None:
+            sampled["vs_greedy_step"] = sampled["ms_per_step"] / ms_per_step
+            out["sampled_step"] = sampled
         if primary:
             out["rejection_sampling"] = sampling_leg(NB, K, cfg.vocab, peaks["hbm_gbs"])
     if wl_name in MTP_WORKLOADS and NB == 1:

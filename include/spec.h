@@ -164,6 +164,44 @@ int spec_verify_step_batch_dev(spec_model* m, int n_seq, const int32_t* seq_ids_
                                const int32_t* drafts_dev, const int32_t* n_draft_dev,
                                int32_t* out_accepted_dev, int32_t* out_bonus_dev);
 
+/* Batched verify step with rejection-sampling acceptance instead of the greedy
+ * rule ("End-to-end OCR expert model architecture and acceleration
+ * principles", section 6.1 and section 11 item 2: the output keeps the target
+ * model's own distribution). The drafter is taken as certain of its drafts
+ * (q one-hot at each draft), which keeps the rule lossless for any drafter.
+ * One captured graph: the decoder forward, the LM head writing the step's
+ * logits into a model-owned buffer, spec_rejection_sample_ws's cooperative
+ * kernel over them, then the device commit of what it decided. With p_j the
+ * softmax of row j-1 of the step's logits at `temperature`, for sequence s:
+ *   accept d_j while u_accept[s][j-1] < p_j(d_j), j = 1..n_draft[s];
+ *   at the first rejection append a draw from p_j without d_j (normalised)
+ *   with u_sample[s][j-1]; if all are accepted append a draw from
+ *   p_(n_draft+1) with u_sample[s][n_draft].
+ * A draw is the inverse CDF in index order (see spec_rejection_sample).
+ * Arguments as spec_verify_step_batch, plus:
+ *   u_accept: [n_seq][max_draft] f32 uniforms in [0, 1) (may be NULL when
+ *             max_draft = 0);
+ *   u_sample: [n_seq][max_draft + 1] f32 uniforms in [0, 1);
+ *   temperature > 0.
+ * out_accepted[s] drafts accepted, then out_token[s] appended: the step commits
+ * out_accepted[s] + 1 tokens, like a greedy step. The first sampled call
+ * allocates the logits buffer (max_batch x (max_draft + 1) x vocab f32) and
+ * the sampler's workspace. Needs vocab % 4 == 0 and vocab <= 262144.
+ * Errors: as spec_verify_step_batch; SPEC_ERR_UNSUPPORTED for the vocabulary;
+ * SPEC_ERR_CUDA when the cooperative launch cannot be made. */
+int spec_verify_step_sample_batch(spec_model* m, int n_seq, const int32_t* seq_ids,
+                                  const int32_t* drafts, const int32_t* n_draft,
+                                  const float* u_accept, const float* u_sample, float temperature,
+                                  int32_t* out_accepted, int32_t* out_token);
+/* Device-resident variant (every array a device pointer; see
+ * spec_verify_step_batch_dev). A sequence whose draft is not a token
+ * reports (-1, -1) and is not committed; the step then raises the token error
+ * bit, read back by spec_sync_seqs. */
+int spec_verify_step_sample_dev(spec_model* m, int n_seq, const int32_t* seq_ids_dev,
+                                const int32_t* drafts_dev, const int32_t* n_draft_dev,
+                                const float* u_accept_dev, const float* u_sample_dev, float temperature,
+                                int32_t* out_accepted_dev, int32_t* out_token_dev);
+
 /* Reserve KV pages so sequence `seq_id` can grow to n_tokens positions without
  * host involvement; the commit kernel keeps these pages. */
 int spec_reserve_seq(spec_model* m, int32_t seq_id, int n_tokens);

@@ -62,6 +62,13 @@ _SIGS = [
     ("spec_verify_step_batch_dev", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                   ctypes.c_void_p]),
+    ("spec_verify_step_sample_batch", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, _I32P, _I32P, _I32P,
+                                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, _I32P,
+                                                     _I32P]),
+    ("spec_verify_step_sample_dev", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                   ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p,
+                                                   ctypes.c_void_p]),
     ("spec_reserve_seq", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int]),
     ("spec_sync_seqs", ctypes.c_int, [ctypes.c_void_p]),
     ("spec_release_seq", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
@@ -216,6 +223,25 @@ def spec_verify_step_batch(m: int, seq_ids, drafts, n_draft) -> tuple:
     acc, bon = np.zeros(len(s), np.int32), np.zeros(len(s), np.int32)
     _check(lib().spec_verify_step_batch(m, len(s), _p(s), _p(d), _p(n), _p(acc), _p(bon)))
     return acc, bon
+
+
+def spec_verify_step_sample_batch(m: int, seq_ids, drafts, n_draft, u_accept, u_sample,
+                                  temperature: float) -> tuple:
+    s, d, n = _i32(seq_ids), _i32(drafts), _i32(n_draft)
+    ua = np.ascontiguousarray(u_accept, np.float32).reshape(-1)
+    us = np.ascontiguousarray(u_sample, np.float32).reshape(-1)
+    acc, tok = np.zeros(len(s), np.int32), np.zeros(len(s), np.int32)
+    _check(lib().spec_verify_step_sample_batch(m, len(s), _p(s), _p(d), _p(n),
+                                               ua.ctypes.data if ua.size else None, us.ctypes.data,
+                                               float(temperature), _p(acc), _p(tok)))
+    return acc, tok
+
+
+def spec_verify_step_sample_dev(m: int, n_seq: int, seq_ids_dev, drafts_dev, n_draft_dev, u_accept_dev,
+                                u_sample_dev, temperature: float, out_acc_dev, out_tok_dev) -> None:
+    _check(lib().spec_verify_step_sample_dev(m, n_seq, _ptr(seq_ids_dev), _ptr(drafts_dev), _ptr(n_draft_dev),
+                                             _ptr(u_accept_dev), _ptr(u_sample_dev), float(temperature),
+                                             _ptr(out_acc_dev), _ptr(out_tok_dev)))
 
 
 def spec_verify_step_batch_dev(m: int, n_seq: int, seq_ids_dev, drafts_dev, n_draft_dev, out_acc_dev,

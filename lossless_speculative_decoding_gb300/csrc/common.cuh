@@ -178,17 +178,12 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // drafts (length n + a + 1); the rejected rows' slots are stale and are
 // overwritten by the next step. Pages wholly past max(new length, reserved
 // pages) leave the block table (-1); the host allocator mirrors this.
-__device__ __forceinline__ void commit_seq(const Dims& D, const DevState& S, const StepBuf& B, int s, int K,
-                                           const int* g_rows) {
+// Commit of step slot s with a drafts accepted and `bonus` appended.
+__device__ __forceinline__ void commit_apply(const Dims& D, const DevState& S, const StepBuf& B, int s, int K, int a,
+                                             int bonus) {
   const int max_batch = B.max_batch;
-  const int R = K + 1;
   const int seq = B.step_in[s];
   const int* d = B.step_in + max_batch + s * K;
-  const int nd = min(max(B.step_in[max_batch + max_batch * K + s], 0), K);
-  const int* g = g_rows + s * R;
-  int a = 0;
-  while (a < nd && d[a] == g[a]) ++a;
-  const int bonus = g[a];
   const int n = S.seq_len[seq];
   const int new_len = n + a + 1;
   const int no = S.n_out[seq];
@@ -210,6 +205,17 @@ __device__ __forceinline__ void commit_seq(const Dims& D, const DevState& S, con
   int* ub = reinterpret_cast<int*>(B.out_ptrs[1]);
   if (ua) ua[s] = a;
   if (ub) ub[s] = bonus;
+}
+
+__device__ __forceinline__ void commit_seq(const Dims& D, const DevState& S, const StepBuf& B, int s, int K,
+                                           const int* g_rows) {
+  const int max_batch = B.max_batch;
+  const int* d = B.step_in + max_batch + s * K;
+  const int nd = min(max(B.step_in[max_batch + max_batch * K + s], 0), K);
+  const int* g = g_rows + s * (K + 1);
+  int a = 0;
+  while (a < nd && d[a] == g[a]) ++a;
+  commit_apply(D, S, B, s, K, a, g[a]);
 }
 
 }  // namespace spec

@@ -275,6 +275,32 @@ void launch_commit(const Dims& D, const DevState& S, const StepBuf& B, int n_seq
   launch_k(k_commit, dim3((n_seq + 63) / 64), dim3(64), 0, st, D, S, B, n_seq, K);
 }
 
+// Commit of a sampled step: the accepted count and appended token come from
+// the rejection sampler. A sequence it reports as failed (-1: a draft not a
+// token, -2: a wait ran out) raises the matching error bit and is not
+// committed.
+__global__ void k_commit_sampled(Dims D, DevState S, StepBuf B, int n_seq, int K, const int* __restrict__ acc,
+                                 const int* __restrict__ tok) {
+  pdl_wait();
+  for (int s = threadIdx.x; s < n_seq; s += blockDim.x) {
+    const int a = acc[s];
+    if (a >= 0) {
+      commit_apply(D, S, B, s, K, a, tok[s]);
+    } else {
+      atomicOr(S.err, a == -2 ? DERR_TIMEOUT : DERR_TOKEN);
+      B.step_out[s] = -1;
+      B.step_out[B.max_batch + s] = -1;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) B.step_out[2 * B.max_batch] = *reinterpret_cast<volatile int*>(S.err);
+}
+
+void launch_commit_sampled(const Dims& D, const DevState& S, const StepBuf& B, int n_seq, int K, const int* acc,
+                           const int* tok, cudaStream_t st) {
+  launch_k(k_commit_sampled, dim3(1), dim3(256), 0, st, D, S, B, n_seq, K, acc, tok);
+}
+
 // Copy device-resident step inputs into the staging block.
 __global__ void k_stage_dev(StepBuf B, int n_seq, int K, const int* seq_ids, const int* drafts,
                             const int* n_draft, int* out_acc, int* out_bonus) {

@@ -209,6 +209,21 @@ void launch_argmax_commit(const Dims& D, const DevState& S, const StepBuf& B, in
 enum KClass { KC_ASSEMBLE, KC_QKV, KC_ATTN, KC_OPROJ, KC_ROUTER, KC_GATEUP, KC_DOWN, KC_COMBINE, KC_LMHEAD,
               KC_COMMIT, KC_STAGE, KC_COUNT };
 void launch_commit(const Dims& D, const DevState& S, const StepBuf& B, int n_seq, int K, cudaStream_t st);
+// Commit of a sampled step from the sampler's [n_seq] accepted counts and tokens.
+void launch_commit_sampled(const Dims& D, const DevState& S, const StepBuf& B, int n_seq, int K, const int* acc,
+                           const int* tok, cudaStream_t st);
+// Rejection sampling, cooperative form (ops_sample.cu): logits [n_seq][K+1][vocab];
+// n_draft (nullable) gives each sequence's draft count (bonus row n_draft);
+// 1 / temperature from it_dev when non-null, else `it`. ws: rs_coop_ws_bytes
+// zero-filled bytes, left zeroed.
+size_t rs_coop_ws_bytes(int n_seq, int K);
+int rs_coop_blocks();   // blocks resident at once (queried once per device; 0 on failure)
+cudaError_t launch_rs_coop(const float* logits, const int32_t* drafts, const int32_t* n_draft, const float* q,
+                           const float* u_accept, const float* u_sample, int n_seq, int K, int vocab, float it,
+                           const float* it_dev, int32_t* out_acc, int32_t* out_tok, void* ws, cudaStream_t st);
+// [u_accept (max_batch K) | u_sample (max_batch (K+1)) | 1 / temperature] <- a sampled step's inputs.
+void launch_stage_sample(float* dst, int max_batch, int K, const float* ua, const float* us, int n_seq, float it,
+                         cudaStream_t st);
 void launch_stage_dev(const StepBuf& B, int n_seq, int K, const int* seq_ids, const int* drafts,
                       const int* n_draft, int* out_acc, int* out_bonus, cudaStream_t st);
 int launches_per_step(const Dims& D, int T);

@@ -557,10 +557,12 @@ __device__ void rc_totals_from_stats(const float4* __restrict__ ts, int NT, floa
 // Counters of a sequence in the workspace: arrivals, then blocks done.
 __global__ void __launch_bounds__(RC_THREADS, 4) k_rs_coop(
     const float* __restrict__ logits, const int32_t* __restrict__ drafts, const float* __restrict__ q,
-    const float* __restrict__ u_accept, const float* __restrict__ u_sample, int n_seq, int K, int V, float it,
-    int B, int n_groups, int first_rows, int* __restrict__ ctr, float4* __restrict__ tstat,
-    float* __restrict__ rtot, int32_t* out_acc, int32_t* out_tok) {
+    const float* __restrict__ u_accept, const float* __restrict__ u_sample, const int* __restrict__ n_draft,
+    int n_seq, int K, int V, float it_arg, const float* __restrict__ it_dev, int B, int n_groups, int first_rows,
+    int* __restrict__ ctr, float4* __restrict__ tstat, float* __restrict__ rtot, int32_t* out_acc,
+    int32_t* out_tok) {
   __shared__ RcShared sh;
+  const float it = it_dev ? *it_dev : it_arg;
   const int group = blockIdx.x / B, b = blockIdx.x % B, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NT = (V + RC_TILE - 1) / RC_TILE;
   enum { INVALID, BONUS, RESIDUAL };
@@ -568,15 +570,17 @@ __global__ void __launch_bounds__(RC_THREADS, 4) k_rs_coop(
   auto stats_of = [&](int s, int r) { return tstat + ((size_t)s * (K + 1) + r) * RC_MAX_TILES; };
   for (int s = group; s < n_seq; s += n_groups) {
     int* cnt = ctr + 2 * s;
+    // this sequence's drafts: Ks of the K slots (its bonus row is row Ks)
+    const int Ks = n_draft ? min(max(__ldg(n_draft + s), 0), K) : K;
     // the rows the walk can reach: a draft that is not a token ends it there
-    int jinv = K;
-    for (int c = 0; c < K && jinv == K; c += 32) {
+    int jinv = Ks;
+    for (int c = 0; c < Ks && jinv == Ks; c += 32) {
       const int j = c + lane;
-      const int dj = j < K ? __ldg(drafts + (size_t)s * K + j) : 0;
-      const unsigned bad = __ballot_sync(0xffffffffu, j < K && (dj < 0 || dj >= V));
+      const int dj = j < Ks ? __ldg(drafts + (size_t)s * K + j) : 0;
+      const unsigned bad = __ballot_sync(0xffffffffu, j < Ks && (dj < 0 || dj >= V));
       if (bad) jinv = c + __ffs(bad) - 1;
     }
-    const int nr = jinv < K ? jinv : K + 1;
+    const int nr = jinv < Ks ? jinv : Ks + 1;
     int kind = INVALID, jrow = -1, d = -1, phase = 0;
     bool decided = false, ok = true;
     float m = 0.f, inv_z = 0.f;
@@ -585,7 +589,7 @@ __global__ void __launch_bounds__(RC_THREADS, 4) k_rs_coop(
       const int nrow = r1 - r0, items = nrow * NT;
       // lane l holds row r0 + l's draft and the inputs of its decision
       const int rl = r0 + lane;
-      const bool dec_l = lane < nrow && rl < K;
+      const bool dec_l = lane < nrow && rl < Ks;
       const int d_l = dec_l ? __ldg(drafts + (size_t)s * K + rl) : -1;
       const float xd_l = dec_l ? __ldg(row_of(s, rl) + d_l) : 0.f;
       const float qd_l = dec_l && q ? __ldg(q + ((size_t)s * K + rl) * V + d_l) : 1.f;
@@ -613,7 +617,7 @@ __global__ void __launch_bounds__(RC_THREADS, 4) k_rs_coop(
         const float ua = __shfl_sync(0xffffffffu, ua_l, rr);
         const int dr = __shfl_sync(0xffffffffu, d_l, rr);
         const float iz = 1.f / mz.y;
-        if (r0 + rr == K) {                            // every draft accepted: the bonus from p_(K+1)
+        if (r0 + rr == Ks) {                           // every draft accepted: the bonus from p_(Ks+1)
           kind = BONUS;
         } else {
           if (ua * qd < expf(xd * it - mz.x) * iz) continue;
@@ -665,7 +669,7 @@ __global__ void __launch_bounds__(RC_THREADS, 4) k_rs_coop(
       if (!ok) {
         acc = -2;                                    // a wait ran out
       } else if (kind != INVALID) {
-        acc = kind == BONUS ? K : jrow;
+        acc = jrow;
         if (qrow) {
           for (int i = threadIdx.x; i < NT; i += RC_THREADS) sh.T[i] = __ldcg(rtot + (size_t)s * RC_MAX_TILES + i);
           __syncthreads();
@@ -759,6 +763,62 @@ extern "C" int64_t spec_rejection_sample_ws_bytes(int n_seq, int K) {
   return (int64_t)rs_ws_layout(n_seq, K, &a, &b);
 }
 
+namespace spec {
+int rs_coop_blocks() { return rs_coop_capacity(); }
+
+size_t rs_coop_ws_bytes(int n_seq, int K) {
+  size_t a, b;
+  return rs_ws_layout(n_seq, K, &a, &b);
+}
+
+cudaError_t launch_rs_coop(const float* logits, const int32_t* drafts, const int32_t* n_draft, const float* q,
+                           const float* u_accept, const float* u_sample, int n_seq, int K, int vocab, float it,
+                           const float* it_dev, int32_t* out_acc, int32_t* out_tok, void* ws, cudaStream_t st) {
+  const int cap = rs_coop_capacity();
+  if (cap < 1) return cudaErrorCooperativeLaunchTooLarge;
+  size_t off_ts, off_rt;
+  rs_ws_layout(n_seq, K, &off_ts, &off_rt);
+  // the first phase: every row when all of them are a small read (a few
+  // microseconds of HBM time, less than the phases saved), else row 0 alone
+  const int NT = (vocab + RC_TILE - 1) / RC_TILE;
+  const double all_rows = (double)n_seq * (K + 1) * vocab * sizeof(float);
+  const int first_rows = all_rows <= RS_ONE_PHASE_BYTES ? std::min(K + 1, RC_PHASE_ROWS) : 1;
+  // B blocks per sequence (no more than the first phase has tiles for their
+  // warps), as many sequences at once as fit; a block runs on over further
+  // sequences
+  const int B = std::max(1, std::min((first_rows * NT + RC_WARPS - 1) / RC_WARPS, cap / n_seq));
+  const int n_groups = std::min(n_seq, cap / B);
+  char* w = static_cast<char*>(ws);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_groups * B);
+  cfg.blockDim = dim3(RC_THREADS);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_rs_coop, logits, drafts, q, u_accept, u_sample, n_draft, n_seq, K, vocab, it,
+                            it_dev, B, n_groups, first_rows, reinterpret_cast<int*>(w),
+                            reinterpret_cast<float4*>(w + off_ts), reinterpret_cast<float*>(w + off_rt), out_acc,
+                            out_tok);
+}
+
+// Stage a sampled step's uniforms and 1 / temperature into the model's buffer
+// [u_accept (n_seq x K) | u_sample (n_seq x (K + 1)) | 1 / temperature].
+__global__ void k_stage_sample(float* dst, int ua_cap, int us_cap, const float* ua, const float* us, int n_seq,
+                               int K, float it) {
+  for (int i = threadIdx.x; i < n_seq * K; i += blockDim.x) dst[i] = ua[i];
+  for (int i = threadIdx.x; i < n_seq * (K + 1); i += blockDim.x) dst[ua_cap + i] = us[i];
+  if (threadIdx.x == 0) dst[ua_cap + us_cap] = it;
+}
+
+void launch_stage_sample(float* dst, int max_batch, int K, const float* ua, const float* us, int n_seq, float it,
+                         cudaStream_t st) {
+  k_stage_sample<<<1, 256, 0, st>>>(dst, max_batch * K, max_batch * (K + 1), ua, us, n_seq, K, it);
+}
+}  // namespace spec
+
 extern "C" int spec_rejection_sample_ws(const float* logits_dev, const int32_t* drafts_dev, const float* q_dev,
                                         const float* u_accept_dev, const float* u_sample_dev, int n_seq, int K,
                                         int vocab, float temperature, int32_t* out_accepted_dev,
@@ -774,36 +834,9 @@ extern "C" int spec_rejection_sample_ws(const float* logits_dev, const int32_t* 
   if (reinterpret_cast<uintptr_t>(logits_dev) % 16 || reinterpret_cast<uintptr_t>(q_dev) % 16 ||
       reinterpret_cast<uintptr_t>(ws_dev) % 16)
     return set_last_error(SPEC_ERR_ARG, "logits, q and the workspace must be 16-byte aligned");
-  size_t off_ts, off_rt;
-  if (ws_bytes < rs_ws_layout(n_seq, K, &off_ts, &off_rt)) return set_last_error(SPEC_ERR_ARG, "workspace too small");
-  const int cap = rs_coop_capacity();
-  if (cap < 1) return set_last_error(SPEC_ERR_CUDA, "cannot size the cooperative launch");
-  // the first phase: every row when all of them are a small read (a few
-  // microseconds of HBM time, less than the phases saved), else row 0 alone
-  const int NT = (vocab + RC_TILE - 1) / RC_TILE;
-  const double all_rows = (double)n_seq * (K + 1) * vocab * sizeof(float);
-  const int first_rows = all_rows <= RS_ONE_PHASE_BYTES ? std::min(K + 1, RC_PHASE_ROWS) : 1;
-  // B blocks per sequence (no more than the first phase has tiles for their
-  // warps), as many sequences at once as fit; a block runs on over further
-  // sequences
-  const int B = std::max(1, std::min((first_rows * NT + RC_WARPS - 1) / RC_WARPS, cap / n_seq));
-  const int n_groups = std::min(n_seq, cap / B);
-  char* ws = static_cast<char*>(ws_dev);
-  int* ctr = reinterpret_cast<int*>(ws);
-  float4* ts = reinterpret_cast<float4*>(ws + off_ts);
-  float* rt = reinterpret_cast<float*>(ws + off_rt);
-  const float it = 1.f / temperature;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_groups * B);
-  cfg.blockDim = dim3(RC_THREADS);
-  cfg.stream = reinterpret_cast<cudaStream_t>(cuda_stream);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_rs_coop, logits_dev, drafts_dev, q_dev, u_accept_dev,
-                                           u_sample_dev, n_seq, K, vocab, it, B, n_groups, first_rows, ctr, ts, rt,
-                                           out_accepted_dev, out_token_dev);
+  if (ws_bytes < rs_coop_ws_bytes(n_seq, K)) return set_last_error(SPEC_ERR_ARG, "workspace too small");
+  const cudaError_t e = launch_rs_coop(logits_dev, drafts_dev, nullptr, q_dev, u_accept_dev, u_sample_dev, n_seq, K,
+                                       vocab, 1.f / temperature, nullptr, out_accepted_dev, out_token_dev, ws_dev,
+                                       reinterpret_cast<cudaStream_t>(cuda_stream));
   return e == cudaSuccess ? SPEC_OK : set_last_error(SPEC_ERR_CUDA, cudaGetErrorString(e));
 }

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <chrono>
 #include <cstdio>
@@ -216,9 +217,19 @@ struct spec_model {
 
   MtpHead* mtp = nullptr;                 // draft head (spec_mtp_init), null without one
 
+  // sampled steps (spec_verify_step_sample*), allocated on first use
+  std::map<int, cudaGraphExec_t> graphs_sample;
+  float* smp_logits = nullptr;     // [Tv][V] f32 logits of the step rows
+  float* smp_in = nullptr;         // [u_accept (max_batch K) | u_sample (max_batch R) | 1 / temperature]
+  int* smp_out = nullptr;          // [accepted (max_batch) | token (max_batch)] from the sampler
+  void* smp_ws = nullptr;          // sampler workspace (zero-filled, left zeroed by every call)
+  float* pin_smp = nullptr;        // pinned staging of smp_in (host-mode steps)
+
   ~spec_model() {
     delete mtp;
     for (auto& g : graphs) cudaGraphExecDestroy(g.second);
+    for (auto& g : graphs_sample) cudaGraphExecDestroy(g.second);
+    if (pin_smp) cudaFreeHost(pin_smp);
     if (own_stream) cudaStreamDestroy(stream);
     for (void* p : allocs) cudaFree(p);
     if (pin_in) cudaFreeHost(pin_in);
@@ -381,26 +392,77 @@ struct spec_model {
     launch_argmax_commit(D, S, B, T, D.V / 128, commit, n_seq, K, stream);
   }
 
-  void enqueue_verify(int n_seq, float* logits_dbg, bool commit, Prof* p = nullptr) {
+  // Sampled step tail: the step rows' logits, rejection sampling over them
+  // (drafts and draft counts from the staging block, uniforms and 1 /
+  // temperature from smp_in), then the commit of what it decided.
+  void enqueue_sample(const float* x, int T, int n_seq, Prof* p, cudaError_t* err) {
+    run_k(p, KC_LMHEAD, [&] {
+      if (!use_tc) {
+        launch_lmhead_step(D, S, B, lm_head, final_norm, x, T, smp_logits, false, n_seq, K, stream);
+      } else {
+        launch_norm_bf16(D, x, final_norm, B.xn_bf16, B.xn_lo, nullptr, T, 0, stream);
+        tc_dense(lm_head, tc_xn, tc_xn_lo, D.h, D.V, T, TC_STORE, smp_logits, D.V);
+      }
+    });
+    const int mb = B.max_batch;
+    run_k(p, KC_COMMIT, [&] {
+      const cudaError_t e = launch_rs_coop(smp_logits, B.step_in + mb, B.step_in + mb + mb * K, nullptr, smp_in,
+                                           smp_in + mb * K, n_seq, K, D.V, 1.f, smp_in + mb * K + mb * R,
+                                           smp_out, smp_out + mb, smp_ws, stream);
+      if (e != cudaSuccess && err) *err = e;
+      launch_commit_sampled(D, S, B, n_seq, K, smp_out, smp_out + mb, stream);
+    });
+  }
+
+  void enqueue_verify(int n_seq, float* logits_dbg, bool commit, Prof* p = nullptr, bool sample = false,
+                      cudaError_t* err = nullptr) {
     const int T = n_seq * R;
     run_k(p, KC_ASSEMBLE, [&] { launch_assemble_verify(D, S, B, tok_embed, n_seq, K, stream); });
     const float* xf = enqueue_layers(T, R, p);
+    if (sample) {
+      enqueue_sample(xf, T, n_seq, p, err);
+      return;
+    }
     run_k(p, KC_LMHEAD, [&] { enqueue_lmhead(xf, T, logits_dbg, commit, n_seq); });
   }
 
-  int graph_for(int n_seq, cudaGraphExec_t* out) {
-    auto it = graphs.find(n_seq);
-    if (it != graphs.end()) { *out = it->second; return SPEC_OK; }
+  // Buffers of the sampled steps, on first use.
+  int ensure_sampling() {
+    if (smp_logits) return SPEC_OK;
+    if (D.V % 4 || D.V > 262144) return fail(SPEC_ERR_UNSUPPORTED, "sampled steps need vocab % 4 == 0 and <= 262144");
+    if (rs_coop_blocks() < 1) return fail(SPEC_ERR_CUDA, "cannot size the sampler's cooperative launch");
+    const int mb = B.max_batch;
+    const size_t nin = (size_t)mb * K + (size_t)mb * R + 1;
+    const size_t ws = rs_coop_ws_bytes(mb, K);
+    int rc;
+    char* w = nullptr;
+    if ((rc = dalloc(&smp_in, nin)) || (rc = dalloc(&smp_out, 2 * (size_t)mb)) || (rc = dalloc(&w, ws))) return rc;
+    CU(cudaMemsetAsync(w, 0, ws, stream));
+    CU(cudaMallocHost(&pin_smp, nin * sizeof(float)));
+    if ((rc = dalloc(&smp_logits, (size_t)Tv * D.V))) return rc;
+    smp_ws = w;
+    return SPEC_OK;
+  }
+
+  int graph_for(int n_seq, cudaGraphExec_t* out, bool sample = false) {
+    auto& cache = sample ? graphs_sample : graphs;
+    auto it = cache.find(n_seq);
+    if (it != cache.end()) { *out = it->second; return SPEC_OK; }
     cudaGraph_t g;
     CU(cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal));
-    enqueue_verify(n_seq, nullptr, true);
+    cudaError_t le = cudaSuccess;
+    enqueue_verify(n_seq, nullptr, true, nullptr, sample, &le);
     cudaError_t e = cudaStreamEndCapture(stream, &g);
+    if (e == cudaSuccess && le != cudaSuccess) {
+      cudaGraphDestroy(g);
+      return fail(SPEC_ERR_CUDA, std::string("sampler launch: ") + cudaGetErrorString(le));
+    }
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, std::string("graph capture: ") + cudaGetErrorString(e));
     cudaGraphExec_t ge;
     e = cudaGraphInstantiate(&ge, g, 0);
     cudaGraphDestroy(g);
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(e));
-    graphs[n_seq] = ge;
+    cache[n_seq] = ge;
     *out = ge;
     return SPEC_OK;
   }
@@ -849,11 +911,27 @@ int spec_prefill(spec_model* m, int32_t seq_id, int32_t prefix_id, const void* v
   return SPEC_OK;
 }
 
-// Host-mode step common to spec_verify_step(_batch) and spec_debug_logits.
+// Inputs of a sampled step (host arrays).
+struct SampleArgs {
+  const float* u_accept;   // [n_seq][K]
+  const float* u_sample;   // [n_seq][K+1]
+  float temperature;
+};
+
+// Host-mode step common to spec_verify_step(_batch), spec_verify_step_sample_batch
+// and spec_debug_logits.
 static int verify_host(spec_model* m, int n_seq, const int32_t* seq_ids, const int32_t* drafts,
-                       const int32_t* n_draft, int32_t* out_acc, int32_t* out_bonus, float* logits_dev) {
+                       const int32_t* n_draft, int32_t* out_acc, int32_t* out_bonus, float* logits_dev,
+                       const SampleArgs* smp = nullptr) {
   if (!m || n_seq < 1 || n_seq > m->cfg.max_batch || !seq_ids) return fail(SPEC_ERR_ARG, "bad batch");
   if (m->K > 0 && !drafts) return fail(SPEC_ERR_ARG, "null drafts");
+  if (smp) {
+    if (!(smp->temperature > 0.f) || !std::isfinite(1.f / smp->temperature))
+      return fail(SPEC_ERR_ARG, "temperature must be positive");
+    if (!smp->u_sample || (m->K > 0 && !smp->u_accept)) return fail(SPEC_ERR_ARG, "null uniforms");
+    int rc = m->ensure_sampling();
+    if (rc) return rc;
+  }
   if (m->host_dirty) return fail(SPEC_ERR_STATE, "call spec_sync_seqs after device-resident steps");
   const int K = m->K, mb = m->cfg.max_batch;
   for (int s = 0; s < n_seq; ++s) {
@@ -888,6 +966,15 @@ static int verify_host(spec_model* m, int n_seq, const int32_t* seq_ids, const i
   CU(cudaMemcpyAsync(m->B.out_ptrs, m->pin_in, (4 + m->step_in_n) * sizeof(int32_t), cudaMemcpyHostToDevice,
                      m->stream));
   m->h2d_bytes += (int64_t)(4 + m->step_in_n) * sizeof(int32_t);
+  if (smp) {
+    const size_t ua_n = (size_t)mb * K, us_n = (size_t)mb * m->R, nin = ua_n + us_n + 1;
+    std::fill(m->pin_smp, m->pin_smp + nin, 0.f);
+    if (K > 0) std::copy(smp->u_accept, smp->u_accept + (size_t)n_seq * K, m->pin_smp);
+    std::copy(smp->u_sample, smp->u_sample + (size_t)n_seq * m->R, m->pin_smp + ua_n);
+    m->pin_smp[ua_n + us_n] = 1.f / smp->temperature;
+    CU(cudaMemcpyAsync(m->smp_in, m->pin_smp, nin * sizeof(float), cudaMemcpyHostToDevice, m->stream));
+    m->h2d_bytes += (int64_t)(nin * sizeof(float));
+  }
   if (logits_dev) {
     mtp_forget_steps(m);
     m->enqueue_verify(n_seq, logits_dev, false);
@@ -896,7 +983,7 @@ static int verify_host(spec_model* m, int n_seq, const int32_t* seq_ids, const i
     return m->check_err();
   }
   cudaGraphExec_t ge;
-  int rc = m->graph_for(n_seq, &ge);
+  int rc = m->graph_for(n_seq, &ge, smp != nullptr);
   if (rc) return rc;
   CU(cudaGraphLaunch(ge, m->stream));
   CU(cudaMemcpyAsync(m->pin_out, m->B.step_out, m->step_out_n * sizeof(int32_t), cudaMemcpyDeviceToHost,
@@ -948,6 +1035,35 @@ int spec_verify_step_batch(spec_model* m, int n_seq, const int32_t* seq_ids, con
                            const int32_t* n_draft, int32_t* out_accepted, int32_t* out_bonus) {
   if (!out_accepted || !out_bonus) return fail(SPEC_ERR_ARG, "null outputs");
   return verify_host(m, n_seq, seq_ids, drafts, n_draft, out_accepted, out_bonus, nullptr);
+}
+
+int spec_verify_step_sample_batch(spec_model* m, int n_seq, const int32_t* seq_ids, const int32_t* drafts,
+                                  const int32_t* n_draft, const float* u_accept, const float* u_sample,
+                                  float temperature, int32_t* out_accepted, int32_t* out_token) {
+  if (!out_accepted || !out_token) return fail(SPEC_ERR_ARG, "null outputs");
+  const SampleArgs smp{u_accept, u_sample, temperature};
+  return verify_host(m, n_seq, seq_ids, drafts, n_draft, out_accepted, out_token, nullptr, &smp);
+}
+
+int spec_verify_step_sample_dev(spec_model* m, int n_seq, const int32_t* seq_ids_dev, const int32_t* drafts_dev,
+                                const int32_t* n_draft_dev, const float* u_accept_dev, const float* u_sample_dev,
+                                float temperature, int32_t* out_accepted_dev, int32_t* out_token_dev) {
+  if (!m || n_seq < 1 || n_seq > m->cfg.max_batch || !seq_ids_dev || !n_draft_dev ||
+      (m->K > 0 && (!drafts_dev || !u_accept_dev)) || !u_sample_dev || !out_accepted_dev || !out_token_dev)
+    return fail(SPEC_ERR_ARG, "bad device step arguments");
+  if (!(temperature > 0.f) || !std::isfinite(1.f / temperature)) return fail(SPEC_ERR_ARG, "temperature must be positive");
+  int rc = m->ensure_sampling();
+  if (rc) return rc;
+  cudaGraphExec_t ge;
+  if ((rc = m->graph_for(n_seq, &ge, true))) return rc;
+  launch_stage_dev(m->B, n_seq, m->K, seq_ids_dev, drafts_dev, n_draft_dev, out_accepted_dev, out_token_dev,
+                   m->stream);
+  launch_stage_sample(m->smp_in, m->cfg.max_batch, m->K, u_accept_dev, u_sample_dev, n_seq, 1.f / temperature,
+                      m->stream);
+  CU(cudaGraphLaunch(ge, m->stream));
+  m->host_dirty = true;
+  mtp_forget_steps(m);
+  return SPEC_OK;
 }
 
 int spec_debug_logits(spec_model* m, int n_seq, const int32_t* seq_ids, const int32_t* drafts, float* logits_dev) {

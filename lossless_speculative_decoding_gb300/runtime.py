@@ -107,6 +107,13 @@ class SpecModel:
     def verify_batch(self, seq_ids, drafts: np.ndarray, n_draft) -> tuple:
         return B.spec_verify_step_batch(self.h, seq_ids, np.asarray(drafts, np.int32).reshape(-1), n_draft)
 
+    def verify_sample_batch(self, seq_ids, drafts: np.ndarray, n_draft, u_accept: np.ndarray,
+                            u_sample: np.ndarray, temperature: float) -> tuple:
+        """Rejection-sampling verify step (spec_verify_step_sample_batch):
+        (accepted, appended token) per sequence."""
+        return B.spec_verify_step_sample_batch(self.h, seq_ids, np.asarray(drafts, np.int32).reshape(-1), n_draft,
+                                               u_accept, u_sample, temperature)
+
     def debug_logits(self, seq_ids, drafts: np.ndarray) -> np.ndarray:
         torch = self.torch
         n = len(seq_ids) * (self.K + 1)
