@@ -57,7 +57,7 @@ constexpr int TC_MAXST = 12;          // pipeline stages at most
 constexpr int TC_SMEM = 220 * 1024;   // dynamic shared memory of every CTA
 constexpr int TC_HDR = 1024;          // barriers + TMEM slot, ahead of the stages
 
-constexpr int TC_NCONV = 2;           // FP8: widened bf16 weight buffers (converter -> MMA ring)
+constexpr int TC_NCONV_MAX = 4;       // FP8: widened weight buffers (converter -> MMA ring) at most
 
 // Bytes of one pipeline stage of `at` K atoms for nsub 32-row activation
 // boxes: the weight tile(s) as stored (bf16, or e4m3 staging for FP8) and the
@@ -66,14 +66,19 @@ constexpr int TC_NCONV = 2;           // FP8: widened bf16 weight buffers (conve
 __host__ __device__ constexpr int tc_stage_bytes(int dual, int f8, int nsub, int split, int at) {
   return at * ((f8 ? TC_A8_BYTES : TC_A_BYTES) * (1 + dual) + (1 + split) * nsub * TC_NSUB * TC_BK * 2);
 }
+// FP8: widened buffers in the converter -> MMA ring. Two: a deeper ring
+// costs TMA stages, and on the batch-64 e4m3 step three or four buffers for
+// small activation tiles were slower (4.43 / 4.49 ms against 4.31 ms).
+__host__ __device__ constexpr int tc_nconv(int f8, int nsub) { return !f8 || nsub < 0 ? 0 : 2; }
 // FP8: the ring of widened bf16 weight tiles the MMAs read, after the stages.
-__host__ __device__ constexpr int tc_conv_bytes(int dual, int f8, int at) {
-  return f8 ? TC_NCONV * at * TC_A_BYTES * (1 + dual) : 0;
+__host__ __device__ constexpr int tc_conv_bytes(int dual, int f8, int nsub, int at) {
+  return tc_nconv(f8, nsub) * at * TC_A_BYTES * (1 + dual);
 }
 // Stages that fit: as many weight tiles in flight as shared memory allows.
 __host__ __device__ constexpr int tc_stage_count(int dual, int f8, int nsub, int split, int at) {
-  return (TC_SMEM - TC_HDR - 1024 - tc_conv_bytes(dual, f8, at)) / tc_stage_bytes(dual, f8, nsub, split, at) < TC_MAXST
-             ? (TC_SMEM - TC_HDR - 1024 - tc_conv_bytes(dual, f8, at)) / tc_stage_bytes(dual, f8, nsub, split, at)
+  return (TC_SMEM - TC_HDR - 1024 - tc_conv_bytes(dual, f8, nsub, at)) / tc_stage_bytes(dual, f8, nsub, split, at) <
+                 TC_MAXST
+             ? (TC_SMEM - TC_HDR - 1024 - tc_conv_bytes(dual, f8, nsub, at)) / tc_stage_bytes(dual, f8, nsub, split, at)
              : TC_MAXST;
 }
 // K atoms per stage: two (half the barrier round trips per weight byte)
@@ -188,10 +193,10 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // header: full[MAXST], empty[MAXST], done, cfull[MAXST] (F8: widened tile ready; the first
-  // TC_NCONV used), cempty[TC_NCONV] (F8: widened buffer free), TMEM slot, abort flag
+  // NCV used), cempty[TC_NCONV_MAX] (F8: widened buffer free), TMEM slot, abort flag
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint64_t* cempty = bars + 3 * TC_MAXST + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + TC_NCONV);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + TC_NCONV_MAX);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -225,7 +230,8 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
   const int STG_OFF = BOFF + AT * BAT;
   const int CONV_ONE = AT * TC_A_BYTES * (1 + DUAL);  // one widened buffer (FP8)
   unsigned char* stages = smem + TC_HDR;
-  unsigned char* conv = stages + STAGES * SB;         // FP8: TC_NCONV widened buffers
+  const int NCV = tc_nconv(F8, nsub);                 // FP8: widened buffers in the ring
+  unsigned char* conv = stages + STAGES * SB;         // FP8: NCV widened buffers
   // this split's K atoms [kt0, kt1) (the host picks splits that are never empty)
   const int KTall = P.K / TC_BK, KTs = (KTall + ksn - 1) / ksn;
   const int kt0 = ks * KTs, kt1 = min(KTall, kt0 + KTs), KT = kt1 - kt0;
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
     for (int i = 0; i < TC_MAXST; ++i)    // one arrival per converter warp
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bars + 2 * TC_MAXST + 1 + i)),
                    "r"(TC_NCONVW));
-    for (int i = 0; i < TC_NCONV; ++i)    // one MMA commit
+    for (int i = 0; i < TC_NCONV_MAX; ++i)    // one MMA commit
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(cempty + i)));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     *abort_flag = 0;
@@ -308,9 +314,9 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
     bool ok = true;
     int kstep = 0;                                    // 16-wide K steps issued so far
     for (int i = 0; i < NST && ok; ++i) {
-      const int s = i % STAGES, na = min(AT, KT - i * AT), c = i % TC_NCONV;
+      const int s = i % STAGES, na = min(AT, KT - i * AT), c = F8 ? i % NCV : 0;
       // bf16: the TMA bytes of the stage; F8: the converters' signal for widened buffer c
-      const bool arrived = F8 ? mbar_wait_deadline(smem_u32(bars + 2 * TC_MAXST + 1 + c), (i / TC_NCONV) & 1, P.err)
+      const bool arrived = F8 ? mbar_wait_deadline(smem_u32(bars + 2 * TC_MAXST + 1 + c), (i / NCV) & 1, P.err)
                               : mbar_wait_deadline(smem_u32(bars + s), (i / STAGES) & 1, P.err);
       if (!arrived) {
         atomicOr(P.err, DERR_TIMEOUT);
@@ -354,9 +360,9 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
     // ---- converters (warps 2..7): e4m3 staging -> swizzled bf16 operand tile ----
     const int t = threadIdx.x - 64;
     for (int i = 0; i < NST; ++i) {
-      const int s = i % STAGES, na = min(AT, KT - i * AT), c = i % TC_NCONV;
+      const int s = i % STAGES, na = min(AT, KT - i * AT), c = i % NCV;
       if (!mbar_wait_deadline(smem_u32(bars + s), (i / STAGES) & 1, P.err) ||
-          (i >= TC_NCONV && !mbar_wait_deadline(smem_u32(cempty + c), ((i / TC_NCONV) - 1) & 1, P.err))) {
+          (i >= NCV && !mbar_wait_deadline(smem_u32(cempty + c), ((i / NCV) - 1) & 1, P.err))) {
         if (lane == 0) atomicOr(P.err, DERR_TIMEOUT);
         break;
       }

@@ -101,17 +101,33 @@ __global__ void k_gather_bf16(Dims D, StepBuf B, int T) {
 
 // g[t] = argmax over the per-tile candidates (larger value wins, equal values
 // keep the lower index); then, when asked, the accept/commit of the step.
-__global__ void k_argmax_commit(Dims D, DevState S, StepBuf B, int T, int ld, int commit, int n_seq, int K) {
+// Greedy token of every row from the GEMM's per-tile candidates (one warp a
+// row, lowest index on ties), then, with commit, acceptance and commit by the
+// block that finishes last (arrival counter B.counter[1], left at zero).
+constexpr int AM_ROWS = 8;                         // rows (warps) per block
+__global__ void __launch_bounds__(AM_ROWS * 32) k_argmax_commit(Dims D, DevState S, StepBuf B, int T, int ld,
+                                                                 int commit, int n_seq, int K) {
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int row = warp; row < T; row += blockDim.x / 32) {
+  const int row = blockIdx.x * AM_ROWS + warp;
+  if (row < T) {
+    const float* vals = B.am_val + (size_t)row * ld;
+    const int* idx = B.am_idx + (size_t)row * ld;
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int i = lane; i < ld; i += 32) {
-      const float c = am_key(B.am_val[(size_t)row * ld + i]);
-      const int ci = B.am_idx[(size_t)row * ld + i];
-      if (c > bv || (c == bv && ci < bi)) { bv = c; bi = ci; }
+    for (int i0 = lane; i0 < ld; i0 += 4 * 32) {
+      float c[4];
+      int ci[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {                // four candidates in flight per lane
+        const int i = i0 + 32 * u;
+        c[u] = i < ld ? am_key(vals[i]) : -INFINITY;
+        ci[u] = i < ld ? idx[i] : 0x7fffffff;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c[u] > bv || (c[u] == bv && ci[u] < bi)) { bv = c[u]; bi = ci[u]; }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -122,8 +138,25 @@ __global__ void k_argmax_commit(Dims D, DevState S, StepBuf B, int T, int ld, in
     if (lane == 0) B.g[row] = bi;
   }
   if (!commit) return;
+  __shared__ int s_last;
   __syncthreads();
-  for (int s = threadIdx.x; s < n_seq; s += blockDim.x) commit_seq(D, S, B, s, K, B.g);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(B.counter + 1, 1) == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int mb = B.max_batch, R = K + 1;
+  for (int s = threadIdx.x; s < n_seq; s += blockDim.x) {
+    // the other blocks' tokens, read past L1
+    const int* d = B.step_in + mb + s * K;
+    const int nd = min(max(B.step_in[mb + mb * K + s], 0), K);
+    int a = 0;
+    while (a < nd && d[a] == __ldcg(B.g + s * R + a)) ++a;
+    commit_apply(D, S, B, s, K, a, __ldcg(B.g + s * R + a));
+  }
+  if (threadIdx.x == 0) B.counter[1] = 0;
 }
 
 void launch_norm_bf16(const Dims& D, const float* x, const float* gamma, uint16_t* out, uint16_t* out_lo,
@@ -142,7 +175,8 @@ void launch_gather_bf16(const Dims& D, const StepBuf& B, int T, cudaStream_t st)
 
 void launch_argmax_commit(const Dims& D, const DevState& S, const StepBuf& B, int T, int ld, bool commit, int n_seq,
                           int K, cudaStream_t st) {
-  launch_k(k_argmax_commit, dim3(1), dim3(1024), 0, st, D, S, B, T, ld, (int)commit, n_seq, K);
+  launch_k(k_argmax_commit, dim3((T + AM_ROWS - 1) / AM_ROWS), dim3(AM_ROWS * 32), 0, st, D, S, B, T, ld,
+           (int)commit, n_seq, K);
 }
 
 }  // namespace spec

@@ -68,7 +68,8 @@ struct StepBuf {
   int* ids; float* wts;              // [T, k]
   int* perm;                         // [T*NS] pair ids grouped by expert
   int* act_expert; int* act_off; int* act_cnt; int* n_active;  // active-expert list
-  int* counter;                      // router arrival counter over rows (kept at zero between launches)
+  int* counter;                      // [0] router arrivals over rows, [1] argmax-commit block arrivals
+                                     // (each kept at zero between launches)
   float* rlogit;                     // [Tmax, E] router logits
   int* cnt_row;                      // [Tmax] router arrivals per row (expert-group blocks)
   int* cnt_att;                      // [Tmax * Hkv] attention arrivals per (row group, kv head)
