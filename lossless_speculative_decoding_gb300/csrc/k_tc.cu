@@ -21,7 +21,7 @@
 // its own row of X -- its result does not depend on the other tokens.
 //
 // FP8 weights (e4m3, per-row fp32 scale applied in the epilogue): the 8 KB
-// e4m3 tile (row-major inside the tile) lands in the stage, six converter
+// e4m3 tile (row-major inside the tile) lands in the stage, eight converter
 // warps widen it to f16 -- exactly, one conversion per pair of values -- into
 // one of two 128-byte-swizzled operand buffers and signal the MMA thread, so
 // the tensor cores run an f16 MMA while HBM carries one byte per weight. The
@@ -86,7 +86,7 @@ __host__ __device__ constexpr int tc_stage_count(int dual, int f8, int nsub, int
 __host__ __device__ constexpr int tc_atoms(int dual, int f8, int nsub, int split) {
   return tc_stage_count(dual, f8, nsub, split, 2) >= 3 ? 2 : 1;
 }
-__host__ __device__ constexpr int tc_threads(int f8) { return f8 ? 256 : 128; }
+__host__ __device__ constexpr int tc_threads(int f8) { return f8 ? 320 : 128; }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -165,7 +165,7 @@ __device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 v) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-constexpr int TC_NCONVW = 6;          // FP8 converter warps (warps 2..7)
+constexpr int TC_NCONVW = 8;          // FP8 converter warps (warps 2..9: two on each SM sub-partition)
 
 // Stage s of the FP8 form: e4m3 staging [128 rows][64 B] -> f16 tile [128
 // rows][128 B] with the 128-byte swizzle (16-byte piece c of row r at
