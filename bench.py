@@ -59,6 +59,9 @@ def parse():
                          "workload when the main one is the default; 'none' for none)")
     ap.add_argument("--no-parity", action="store_true", help="skip the oracle parity leg")
     ap.add_argument("--profile-steps", type=int, default=64)
+    ap.add_argument("--sampling-probe", type=int, default=0, metavar="NB",
+                    help="profiling aid: three spec_rejection_sample_ws calls on one NB x 4 x 129,280 input of the "
+                         "sampling workload (seed 7; a 256 MB buffer zeroed before each call), then exit")
     ap.add_argument("--ncu-window", type=int, default=0,
                     help="profiler window: run this many device-resident steps of the main workload between "
                          "cudaProfilerStart/Stop after the warm-up, then exit (for ncu --profile-from-start off; "
@@ -460,7 +463,8 @@ def sampling_leg(NB: int, K: int, V: int, hbm_gbs: float) -> dict:
     r = out["split"]
     return {"kernel": "k_rs_coop (spec_rejection_sample_ws)", "shape": f"{NB} x {K + 1} x {V}",
             "us_per_call": r["us_per_call"], "bytes_per_call": bytes_call, "achieved_gbs": r["achieved_gbs"],
-            "frac": r["frac"], "one_block_per_sequence": out["one_block"],
+            "frac": r["frac"], "traffic": traffic_for("rejection_sampling", bytes_call),
+            "one_block_per_sequence": out["one_block"],
             "bytes": "the logit rows the rule must read: rows 0..a of each sequence",
             "drafter": "certain of its drafts: the target's 0.823-mass token 70% of the time (per-draft "
                        "acceptance ~0.576)", "accepted_mean": rows / copies / NB - 1.0, "temperature": 1.0,
@@ -840,8 +844,45 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def sampling_probe(NB: int, K: int = 3, V: int = 129280) -> dict:
+    """One input of the sampling workload (as sampling_leg builds its copies,
+    seed 7) and three spec_rejection_sample_ws calls on it, L2 cleared before
+    each: the launches an ncu capture of k_rs_coop takes (-s 2 -c 1)."""
+    import math
+    import torch
+    from lossless_speculative_decoding_gb300 import binding as B
+    torch.cuda.set_device(0)
+    g = torch.Generator(device="cuda").manual_seed(7)
+    lg = torch.randn(NB, K + 1, V, device="cuda", generator=g)
+    hit = torch.randint(0, V, (NB, K + 1, 1), device="cuda", generator=g)
+    lg.scatter_(2, hit, -math.inf)
+    rest = torch.logsumexp(lg, dim=2, keepdim=True)
+    lg.scatter_(2, hit, rest + math.log(SAMPLING_P_HIT / (1.0 - SAMPLING_P_HIT)))
+    rnd = torch.randint(0, V, (NB, K), device="cuda", generator=g)
+    keep = torch.rand(NB, K, device="cuda", generator=g) < SAMPLING_DRAFT_HIT
+    drafts = torch.where(keep, hit[:, :K, 0], rnd).to(torch.int32).contiguous()
+    ua = torch.rand(NB, K, device="cuda", generator=g)
+    us = torch.rand(NB, K + 1, device="cuda", generator=g)
+    acc = torch.empty(NB, dtype=torch.int32, device="cuda")
+    tok = torch.empty(NB, dtype=torch.int32, device="cuda")
+    nws = B.spec_rejection_sample_ws_bytes(NB, K)
+    ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    for _ in range(3):
+        flush.zero_()
+        B.spec_rejection_sample_ws(lg, drafts, None, ua, us, NB, K, V, 1.0, acc, tok, ws, nws, st)
+    torch.cuda.synchronize()
+    a = int(acc.sum().item())
+    return {"sampling_probe": f"{NB} x {K + 1} x {V}", "accepted_total": a,
+            "algorithmic_bytes": (a + NB) * V * 4}
+
+
 def main():
     args = parse()
+    if args.sampling_probe:
+        print(json.dumps(sampling_probe(args.sampling_probe)), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

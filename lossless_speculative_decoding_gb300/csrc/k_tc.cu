@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  ::"r"(smem_u32(bars + 2 * TC_MAXST)) : "memory");
   } else if (F8 && warp >= 2) {
-    // ---- converters (warps 2..7): e4m3 staging -> swizzled bf16 operand tile ----
+    // ---- converters (warps 2..9): e4m3 staging -> swizzled f16 operand tile ----
     const int t = threadIdx.x - 64;
     for (int i = 0; i < NST; ++i) {
       const int s = i % STAGES, na = min(AT, KT - i * AT), c = i % NCV;
