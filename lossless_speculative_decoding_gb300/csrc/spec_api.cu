@@ -169,10 +169,15 @@ static int tc_ksplit(int n_sm, int m_tiles, int groups, int n_tiles, int KT) {
 }
 
 // activation rows per CTA of a dense tensor-core launch (see tc_dense); with
-// three activation parts the MMA's N (3 x rows) stays within 256
+// three activation parts the MMA's N (3 x rows) stays within 256. A CTA's
+// time is set by its K stream, not by its rows, so the launch takes the
+// smallest tile whose CTAs fit in one wave (more CTAs only add waves), else
+// the largest tile.
 static int tc_dense_ntile(int n_sm, int M, int T, bool three_parts = false) {
-  const int nt = (M / 128) * ((T + 127) / 128) < n_sm ? 32 : 128;
-  return three_parts && nt > 64 ? 64 : nt;
+  const int largest = three_parts ? 64 : 128;
+  for (int nt = 32; nt < largest; nt *= 2)
+    if ((M / 128) * ((T + nt - 1) / nt) <= n_sm) return nt;
+  return largest;
 }
 
 struct spec_model {
