@@ -708,7 +708,8 @@ def measure(wl_name: str, args, primary: bool) -> dict:
         acc_s = d_acc.cpu().numpy().reshape(total, NB)[W:W + KS]
         ms_s = e_s[0].elapsed_time(e_s[1])
         sampled = {"entry": "spec_verify_step_sample_dev",
-                   "graph": "decoder forward, LM head writing the step logits, k_rs_coop, commit",
+                   "graph": "decoder forward, LM head with per-tile softmax statistics (TC_STATS), k_rs_tiles, "
+                            "commit",
                    "temperature": SAMPLED_TEMPERATURE, "ms_per_step": ms_s / KS,
                    "tokens_per_s": float((acc_s + 1).sum()) / (ms_s * 1e-3), "tau": float((acc_s + 1).mean()),
                    "valid": bool((acc_s >= 0).all())}

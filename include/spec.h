@@ -169,9 +169,14 @@ int spec_verify_step_batch_dev(spec_model* m, int n_seq, const int32_t* seq_ids_
  * principles", section 6.1 and section 11 item 2: the output keeps the target
  * model's own distribution). The drafter is taken as certain of its drafts
  * (q one-hot at each draft), which keeps the rule lossless for any drafter.
- * One captured graph: the decoder forward, the LM head writing the step's
- * logits into a model-owned buffer, spec_rejection_sample_ws's cooperative
- * kernel over them, then the device commit of what it decided. With p_j the
+ * One captured graph: the decoder forward, the LM head, the rejection
+ * sampler, then the device commit of what it decided. On the tensor-core
+ * path (more than 8 rows a step), the LM head's epilogue leaves per-tile
+ * softmax statistics (max, sum of exp) instead of logits. A one-block-per-
+ * sequence sampler then draws from them and recomputes only the drawn tile's
+ * 128 logits. Otherwise the LM head writes the step's logits into a
+ * model-owned buffer and spec_rejection_sample_ws's cooperative kernel
+ * samples them. With p_j the
  * softmax of row j-1 of the step's logits at `temperature`, for sequence s:
  *   accept d_j while u_accept[s][j-1] < p_j(d_j), j = 1..n_draft[s];
  *   at the first rejection append a draw from p_j without d_j (normalised)
@@ -185,7 +190,8 @@ int spec_verify_step_batch_dev(spec_model* m, int n_seq, const int32_t* seq_ids_
  *   temperature > 0.
  * out_accepted[s] drafts accepted, then out_token[s] appended: the step commits
  * out_accepted[s] + 1 tokens, like a greedy step. The first sampled call
- * allocates the logits buffer (max_batch x (max_draft + 1) x vocab f32) and
+ * allocates the statistics (max_batch x (max_draft + 1) x vocab / 128 x 16
+ * bytes) or the logits buffer (max_batch x (max_draft + 1) x vocab f32) and
  * the sampler's workspace. Needs vocab % 4 == 0 and vocab <= 262144.
  * Errors: as spec_verify_step_batch; SPEC_ERR_UNSUPPORTED for the vocabulary;
  * SPEC_ERR_CUDA when the cooperative launch cannot be made. */

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libspec.so")
 OBJ_DIR = os.path.join(HERE, "_build")
 SOURCES = ["spec_api.cu", "k_gemv.cu", "k_stream.cu", "k_attn.cu", "k_small.cu", "ops_lmhead.cu", "k_tc.cu", "k_tcglue.cu",
-           "ops_sample.cu", "ops_mtp.cu"]
+           "ops_sample.cu", "ops_sample_tiles.cu", "ops_mtp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

@@ -116,6 +116,13 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar) : "memory");
 }
 
+// 2^x by the hardware approximation (ex2.approx: relative error ~2^-22).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Linear global -> shared copy completing on an mbarrier (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -506,7 +513,7 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
       }
     }
   };
-  if (ksn == 1 && P.epi == TC_ARGMAX && TC_BM * (N + 1) * 4 <= STAGES * SB) {
+  if (ksn == 1 && (P.epi == TC_ARGMAX || P.epi == TC_STATS) && TC_BM * (N + 1) * 4 <= STAGES * SB) {
     // per column: max over the tile's 128 rows, lowest row on ties. Every MMA
     // has completed and every copy has landed, so the stage memory holds the
     // [row][column] values (row stride N + 1: conflict-free both ways) and one
@@ -518,12 +525,36 @@ __global__ void __launch_bounds__(tc_threads(F8), 1) k_tc_gemm(const __grid_cons
         float v[16], u2[16];
         load_acc(c0, v, u2);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) tv[m * LD + c0 + j] = am_key(v[j] * sc);
+        for (int j = 0; j < 16; ++j) tv[m * LD + c0 + j] = P.epi == TC_ARGMAX ? am_key(v[j] * sc) : v[j] * sc;
       }
     }
     __syncthreads();
     const int n = threadIdx.x;
-    if (have && n < nrows) {
+    if (P.epi == TC_STATS && have && n < nrows) {
+      // column n: the tile's max of x * it, then sum of exp(x * it - max) as
+      // 2^(x it log2 e - max log2 e) in row order; again without the row's
+      // draft when it lies in the tile (its logit goes to xd)
+      const StatsOut& so = P.st;
+      const int t = off + n0 + n;
+      const float it = *so.it;
+      float mx = -INFINITY;
+      for (int r = 0; r < TC_BM; ++r) mx = fmaxf(mx, tv[r * LD + n]);
+      const float mm = mx * it, cl = it * 1.4426950408889634f, mb = mm * 1.4426950408889634f;
+      float sum = 0.f;
+      for (int r = 0; r < TC_BM; ++r) sum += ex2_approx(fmaf(tv[r * LD + n], cl, -mb));
+      const int sq = t / so.R, j = t % so.R;
+      const int nd = min(max(so.nd[sq], 0), so.K);
+      const int local = j < nd ? so.drafts[sq * so.K + j] - (P.row0 + wrow) : -1;
+      float sk = sum;
+      if (local >= 0 && local < TC_BM) {
+        sk = 0.f;
+        for (int r = 0; r < TC_BM; ++r)
+          if (r != local) sk += ex2_approx(fmaf(tv[r * LD + n], cl, -mb));
+        so.xd[t] = tv[local * LD + n];
+      }
+      float* o = so.out + ((size_t)t * P.am_ld + mt) * 4;
+      *reinterpret_cast<float4*>(o) = make_float4(mm, sum, sk, 0.f);
+    } else if (have && n < nrows) {
       float bv[4];
       int bi[4];
 #pragma unroll
@@ -629,6 +660,12 @@ __global__ void k_pack_weights(const uint4* __restrict__ src, uint4* __restrict_
                             : tile * (TC_A_BYTES / 16) + (size_t)r * 8 + (c ^ (r & 7));
     dst[piece] = src[i];
   }
+}
+
+bool tc_column_scan_fits(int rows) {
+  const int nsub = (rows + TC_NSUB - 1) / TC_NSUB, N = nsub * TC_NSUB;
+  const int at = tc_atoms(0, 0, nsub, 1);
+  return TC_BM * (N + 1) * 4 <= tc_stage_count(0, 0, nsub, 1, at) * tc_stage_bytes(0, 0, nsub, 1, at);
 }
 
 int tc_pack_weights(void* dst, const void* src, int rows, int K, int f8, cudaStream_t st) {

@@ -132,7 +132,21 @@ int ffn_stage_k(int K, int esz);
 void launch_argmax(const StepBuf& B, int T, cudaStream_t st);
 
 // ---- tensor-core GEMM (k_tc.cu) ---------------------------------------------
-enum TcEpi { TC_STORE = 0, TC_SWIGLU = 1, TC_ADD = 2, TC_ARGMAX = 3, TC_SCATTER = 4 };
+enum TcEpi { TC_STORE = 0, TC_SWIGLU = 1, TC_ADD = 2, TC_ARGMAX = 3, TC_SCATTER = 4, TC_STATS = 5 };
+
+// TC_STATS (the LM head of a sampled step): per (row, 128-row tile of the
+// vocabulary) the softmax statistics of logit * it -- the max m, sum of
+// exp(x it - m), and the same sum without the row's draft -- and, from the
+// tile holding the row's draft, the draft's logit. Rows are step rows s R + j;
+// row j < n_draft[s] of sequence s has draft drafts[s K + j].
+struct StatsOut {
+  float* out;             // [rows][tiles][4]: m, sum, sum without the draft, 0
+  float* xd;              // [rows]
+  const float* it;        // 1 / temperature (device)
+  const int* drafts;      // [n_seq][K]
+  const int* nd;          // [n_seq]
+  int K, R;
+};
 
 struct TcParams {
   const void* wa;         // weights, tiled by tc_pack_weights
@@ -165,6 +179,7 @@ struct TcParams {
   int am_ld;
   int* err;
   int test_stall;         // test only: the producer issues no copies, so every wait times out
+  StatsOut st;            // TC_STATS outputs
 };
 
 struct TcMaps {
@@ -197,6 +212,9 @@ inline int att_box_keys(const Dims& D) { return D.P % 64 == 0 ? 64 : 16; }
 // layout the tensor-core GEMM streams (rows a multiple of 128, K of 64).
 int tc_pack_weights(void* dst, const void* src, int rows, int K, int f8, cudaStream_t st);
 void launch_tc_gemm(const TcMaps& maps, const TcParams& P, int m_tiles, int groups, int n_tiles, cudaStream_t st);
+// True when a bf16 single-operand launch of up to `rows` activation rows per
+// CTA (two parts) takes the shared-memory column scan TC_ARGMAX / TC_STATS use.
+bool tc_column_scan_fits(int rows);
 cudaError_t configure_tc_kernels();
 // out_lo2 (nullable): the third part bf16(v - hi - lo).
 void launch_norm_bf16(const Dims& D, const float* x, const float* gamma, uint16_t* out, uint16_t* out_lo,
@@ -222,6 +240,15 @@ int rs_coop_blocks();   // blocks resident at once (queried once per device; 0 o
 cudaError_t launch_rs_coop(const float* logits, const int32_t* drafts, const int32_t* n_draft, const float* q,
                            const float* u_accept, const float* u_sample, int n_seq, int K, int vocab, float it,
                            const float* it_dev, int32_t* out_acc, int32_t* out_tok, void* ws, cudaStream_t st);
+// Rejection sampling of a sampled step from the LM head's TC_STATS output
+// (stats [rows][V / 128][4], xd [rows]), recomputing the picked tile's logits
+// from the tiled bf16 LM head and the rows' hi / lo LM-head inputs; one block
+// per sequence. Writes the sampler's [n_seq] accepted counts and tokens.
+int rs_tiles_max_h();   // the widest LM-head input launch_rs_tiles takes
+void launch_rs_tiles(const float* stats, const float* xd, int V, const uint16_t* lm_head_tiled, const uint16_t* xn_hi,
+                     const uint16_t* xn_lo, int h, const int32_t* drafts, const int32_t* n_draft, const float* u_accept,
+                     const float* u_sample, const float* it_dev, int n_seq, int K, int32_t* out_acc, int32_t* out_tok,
+                     cudaStream_t st);
 // [u_accept (max_batch K) | u_sample (max_batch (K+1)) | 1 / temperature] <- a sampled step's inputs.
 void launch_stage_sample(float* dst, int max_batch, int K, const float* ua, const float* us, int n_seq, float it,
                          cudaStream_t st);

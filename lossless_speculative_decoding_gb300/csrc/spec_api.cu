@@ -224,7 +224,9 @@ struct spec_model {
 
   // sampled steps (spec_verify_step_sample*), allocated on first use
   std::map<int, cudaGraphExec_t> graphs_sample;
-  float* smp_logits = nullptr;     // [Tv][V] f32 logits of the step rows
+  float* smp_logits = nullptr;     // [Tv][V] f32 logits of the step rows (no tile statistics)
+  float* smp_stats = nullptr;      // [Tv][V / 128][4] LM-head tile statistics (tensor-core path)
+  float* smp_xd = nullptr;         // [Tv] the rows' draft logits (tensor-core path)
   float* smp_in = nullptr;         // [u_accept (max_batch K) | u_sample (max_batch R) | 1 / temperature]
   int* smp_out = nullptr;          // [accepted (max_batch) | token (max_batch)] from the sampler
   void* smp_ws = nullptr;          // sampler workspace (zero-filled, left zeroed by every call)
@@ -307,7 +309,8 @@ struct spec_model {
   // active-expert list of the step (rows of the permuted operand).
   // blo2: a third activation part (the QKV input), else two parts
   void tc_dense(const void* w, const CUtensorMap& b, const CUtensorMap& blo, int K, int M, int T, int epi,
-                float* out, int ldo, const float* scale = nullptr, const CUtensorMap* blo2 = nullptr) {
+                float* out, int ldo, const float* scale = nullptr, const CUtensorMap* blo2 = nullptr,
+                const StatsOut* stats = nullptr) {
     TcMaps mp;
     mp.b = b; mp.blo = blo; mp.blo2 = blo2 ? *blo2 : blo; mp.dual = 0; mp.f8 = scale != nullptr;
     TcParams P = {};
@@ -315,6 +318,7 @@ struct spec_model {
     P.K = K; P.Mg = M; P.N = T; P.ldo = ldo; P.epi = epi; P.out_f32 = out; P.err = S.err; P.split = blo2 ? 2 : 1;
     P.scale = scale;
     if (epi == TC_ARGMAX) { P.am_val = B.am_val; P.am_idx = B.am_idx; P.am_ld = M / 128; }
+    if (epi == TC_STATS && stats) { P.st = *stats; P.am_ld = M / 128; }
     // too few CTAs for the GPU with 128-row activation tiles (small projections
     // at moderate T): 32-row tiles quadruple them; the weight tile is then read
     // by CTAs that run side by side (N tiles vary fastest) and hits in L2
@@ -401,6 +405,29 @@ struct spec_model {
   // (drafts and draft counts from the staging block, uniforms and 1 /
   // temperature from smp_in), then the commit of what it decided.
   void enqueue_sample(const float* x, int T, int n_seq, Prof* p, cudaError_t* err) {
+    const int mb = B.max_batch;
+    if (smp_stats) {
+      // tensor-core LM head: softmax statistics per 128-token tile instead of logits
+      run_k(p, KC_LMHEAD, [&] {
+        launch_norm_bf16(D, x, final_norm, B.xn_bf16, B.xn_lo, nullptr, T, 0, stream);
+        StatsOut so{};
+        so.out = smp_stats;
+        so.xd = smp_xd;
+        so.it = smp_in + mb * K + mb * R;
+        so.drafts = B.step_in + mb;
+        so.nd = B.step_in + mb + mb * K;
+        so.K = K;
+        so.R = R;
+        tc_dense(lm_head, tc_xn, tc_xn_lo, D.h, D.V, T, TC_STATS, nullptr, 0, nullptr, nullptr, &so);
+      });
+      run_k(p, KC_COMMIT, [&] {
+        launch_rs_tiles(smp_stats, smp_xd, D.V, static_cast<const uint16_t*>(lm_head), B.xn_bf16, B.xn_lo, D.h,
+                        B.step_in + mb, B.step_in + mb + mb * K, smp_in, smp_in + mb * K, smp_in + mb * K + mb * R,
+                        n_seq, K, smp_out, smp_out + mb, stream);
+        launch_commit_sampled(D, S, B, n_seq, K, smp_out, smp_out + mb, stream);
+      });
+      return;
+    }
     run_k(p, KC_LMHEAD, [&] {
       if (!use_tc) {
         launch_lmhead_step(D, S, B, lm_head, final_norm, x, T, smp_logits, false, n_seq, K, stream);
@@ -409,7 +436,6 @@ struct spec_model {
         tc_dense(lm_head, tc_xn, tc_xn_lo, D.h, D.V, T, TC_STORE, smp_logits, D.V);
       }
     });
-    const int mb = B.max_batch;
     run_k(p, KC_COMMIT, [&] {
       const cudaError_t e = launch_rs_coop(smp_logits, B.step_in + mb, B.step_in + mb + mb * K, nullptr, smp_in,
                                            smp_in + mb * K, n_seq, K, D.V, 1.f, smp_in + mb * K + mb * R,
@@ -433,7 +459,7 @@ struct spec_model {
 
   // Buffers of the sampled steps, on first use.
   int ensure_sampling() {
-    if (smp_logits) return SPEC_OK;
+    if (smp_logits || smp_stats) return SPEC_OK;
     if (D.V % 4 || D.V > 262144) return fail(SPEC_ERR_UNSUPPORTED, "sampled steps need vocab % 4 == 0 and <= 262144");
     if (rs_coop_blocks() < 1) return fail(SPEC_ERR_CUDA, "cannot size the sampler's cooperative launch");
     const int mb = B.max_batch;
@@ -444,9 +470,10 @@ struct spec_model {
     if ((rc = dalloc(&smp_in, nin)) || (rc = dalloc(&smp_out, 2 * (size_t)mb)) || (rc = dalloc(&w, ws))) return rc;
     CU(cudaMemsetAsync(w, 0, ws, stream));
     CU(cudaMallocHost(&pin_smp, nin * sizeof(float)));
-    if ((rc = dalloc(&smp_logits, (size_t)Tv * D.V))) return rc;
     smp_ws = w;
-    return SPEC_OK;
+    if (use_tc && D.V % 128 == 0 && D.h % 8 == 0 && D.h <= rs_tiles_max_h() && tc_column_scan_fits(std::min(Tv, 128)))
+      return (rc = dalloc(&smp_xd, (size_t)Tv)) ? rc : dalloc(&smp_stats, (size_t)Tv * (D.V / 128) * 4);
+    return dalloc(&smp_logits, (size_t)Tv * D.V);
   }
 
   int graph_for(int n_seq, cudaGraphExec_t* out, bool sample = false) {

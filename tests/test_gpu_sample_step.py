@@ -103,12 +103,17 @@ def test_sampled_steps_follow_the_rule(cfg, temp):
     assert 0 < accepted < 3 * steps                     # the walk both accepts and rejects
 
 
-def test_first_token_follows_the_target():
+# the fp32 model scores its rows with the GEMV LM head (logits written, then
+# the cooperative sampler); the bf16 one at 64 sequences with the tensor-core
+# LM head, whose epilogue leaves per-tile softmax statistics instead
+@pytest.mark.parametrize("cfg,temp", [(syn.scaled(TINY, name="tiny-v64", vocab=64), 1.0),
+                                      (syn.scaled(MOE_SMALL, name="moe-small-v256", vocab=256), 1.0)],
+                         ids=["fp32-gemv-logits", "bf16-tcgen05-tile-stats"])
+def test_first_token_follows_the_target(cfg, temp):
     rng = np.random.default_rng(32)
-    cfg = syn.scaled(TINY, name="tiny-v64", vocab=64)
     w = syn.generate_weights(cfg, 3)
     om = oracle.OracleModel(w)
-    n, K, temp, rounds = 64, 2, 1.0, 40
+    n, K, rounds = 64, 2, 40
     gm = gpu_model(cfg, w, max_seqs=n, max_ctx=64, max_draft=K, max_batch=n, n_pages=512)
     prompt = _prompt(cfg, rng)
     g0 = gm.prefill(0, prompt.visual, prompt.tokens)
