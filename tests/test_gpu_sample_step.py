@@ -14,7 +14,9 @@ architecture and acceleration principles", section 6.1 and section 11 item 2).
 * Law: the first token emitted after the prompt, over thousands of sampled
   steps with drafts from a drafter far from the target, is distributed as the
   oracle model's p (chi-square).
-* The device-resident entry point takes the same decisions as the host one."""
+* The device-resident entry point takes the same decisions as the host one.
+* K = 0 is plain sampling (one inverse-CDF draw from p_1), and a sequence's
+  decisions do not depend on the other sequences of its step."""
 import numpy as np
 import pytest
 
@@ -178,3 +180,51 @@ def test_device_entry_point_matches_host():
         assert (acc_d.cpu().numpy() == acc_h).all() and (tok_d.cpu().numpy() == tok_h).all()
     for s in range(n_seq):
         assert list(dev.tokens(s)) == list(host.tokens(s))
+
+
+@pytest.mark.parametrize("cfg,n_seq", [(TINY, 2), (MOE_SMALL, 16)], ids=["fp32-gemv", "bf16-tcgen05"])
+def test_no_drafts_is_plain_sampling(cfg, n_seq):
+    """K = 0: the step appends one draw from p_1 (inverse CDF with u_sample)."""
+    rng = np.random.default_rng(34)
+    w = syn.generate_weights(cfg, 0)
+    gm = gpu_model(cfg, w, max_seqs=n_seq, max_ctx=128, max_draft=0, max_batch=n_seq)
+    prompts = [_prompt(cfg, rng) for _ in range(n_seq)]
+    for s, p in enumerate(prompts):
+        gm.prefill(s, p.visual, p.tokens)
+    ids = list(range(n_seq))
+    for _ in range(3):
+        us = rng.random((n_seq, 1)).astype(np.float32)
+        lg = gm.debug_logits(ids, np.zeros((n_seq, 0), np.int32)).reshape(n_seq, cfg.vocab)
+        acc, tok = gm.verify_sample_batch(ids, np.zeros((n_seq, 0), np.int32), np.zeros(n_seq, np.int32),
+                                          np.zeros((n_seq, 0), np.float32), us, 0.05)
+        assert (acc == 0).all()
+        for s in ids:
+            t, margin = smp.inverse_cdf(smp.target_probs(lg[s].astype(np.float64), 0.05), float(us[s, 0]))
+            assert int(tok[s]) == t or margin < TIE
+
+
+def test_sampled_decisions_do_not_depend_on_the_batch():
+    """A sequence's (accepted, token) is the same stepped alone or with three
+    others (same inputs and uniforms), on the tensor-core path."""
+    rng = np.random.default_rng(35)
+    cfg = MOE_SMALL
+    w = syn.generate_weights(cfg, 0)
+    n_seq, K = 4, 3
+    prompts = [_prompt(cfg, rng) for _ in range(n_seq)]
+    drafts = rng.integers(0, cfg.vocab, (3, n_seq, K)).astype(np.int32)
+    ua = rng.random((3, n_seq, K)).astype(np.float32)
+    us = rng.random((3, n_seq, K + 1)).astype(np.float32)
+    batched = gpu_model(cfg, w, max_seqs=n_seq, max_ctx=256, max_draft=K, max_batch=n_seq)
+    alone = gpu_model(cfg, w, max_seqs=n_seq, max_ctx=256, max_draft=K, max_batch=n_seq)
+    for gm in (batched, alone):
+        for s, p in enumerate(prompts):
+            gm.prefill(s, p.visual, p.tokens)
+    nd = np.full(n_seq, K, np.int32)
+    for step in range(3):
+        a_b, t_b = batched.verify_sample_batch(list(range(n_seq)), drafts[step], nd, ua[step], us[step], 0.05)
+        for s in range(n_seq):
+            a_1, t_1 = alone.verify_sample_batch([s], drafts[step, s:s + 1], nd[s:s + 1], ua[step, s:s + 1],
+                                                 us[step, s:s + 1], 0.05)
+            assert (int(a_1[0]), int(t_1[0])) == (int(a_b[s]), int(t_b[s])), f"step {step} sequence {s}"
+    for s in range(n_seq):
+        assert list(batched.tokens(s)) == list(alone.tokens(s))
