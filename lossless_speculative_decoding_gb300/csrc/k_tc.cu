@@ -69,7 +69,7 @@ __host__ __device__ constexpr int tc_stage_bytes(int dual, int f8, int nsub, int
 // FP8: widened buffers in the converter -> MMA ring. Two: a deeper ring
 // costs TMA stages, and on the batch-64 e4m3 step three or four buffers for
 // small activation tiles were slower (4.43 / 4.49 ms against 4.31 ms).
-__host__ __device__ constexpr int tc_nconv(int f8, int nsub) { return !f8 || nsub < 0 ? 0 : 2; }
+__host__ __device__ constexpr int tc_nconv(int f8, int /* nsub */) { return f8 ? 2 : 0; }
 // FP8: the ring of widened bf16 weight tiles the MMAs read, after the stages.
 __host__ __device__ constexpr int tc_conv_bytes(int dual, int f8, int nsub, int at) {
   return tc_nconv(f8, nsub) * at * TC_A_BYTES * (1 + dual);
