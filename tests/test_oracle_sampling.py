@@ -77,6 +77,33 @@ def test_first_token_is_distributed_as_the_target(seed):
     assert np.abs(wrong - p).max() > 10 * (V + 1) / N
 
 
+@pytest.mark.parametrize("seed", [7, 8, 9])
+def test_certain_drafter_is_lossless_for_any_draft_law(seed):
+    """q = None (a drafter certain of its drafts, the form the model's sampled
+    step uses) with drafts drawn from an arbitrary law r: P(first emitted = v)
+    = sum_d r(d) [p(d) 1{v = d} + (1 - p(d)) p(v) 1{v != d} / (1 - p(d))] = p(v)."""
+    logits, _ = _case(seed)
+    V = logits.shape[1]
+    r = np.random.default_rng(seed + 100).dirichlet(np.ones(V) * 0.5)
+    p = smp.target_probs(logits[0], 1.0)
+    law = np.zeros(V)
+    for d in range(V):
+        acc = np.mean([smp.rejection_sample(logits, [d], None, [u], [0.5, 0.5])[0] == 1 for u in GRID])
+        assert abs(acc - p[d]) <= 1.0 / N + 1e-12            # accepted with probability p(d)
+        law[d] += r[d] * acc
+        toks = [smp.rejection_sample(logits, [d], None, [1.0 - 1e-9], [u, 0.5])[1] for u in GRID]
+        assert d not in toks                                   # the rejected draft is never drawn
+        law += r[d] * (1.0 - acc) * np.bincount(toks, minlength=V) / N
+    np.testing.assert_allclose(law, p, atol=(V + 1) / N)
+    # a plausible mistake (the residual drawn from p itself, keeping the
+    # rejected draft: law p(v) (r(v) + 1 - E_r[p])) lies well outside that bound
+    wrong = np.zeros(V)
+    for d in range(V):
+        wrong[d] += r[d] * p[d]
+        wrong += r[d] * (1.0 - p[d]) * p
+    assert np.abs(wrong - p).max() > 5 * (V + 1) / N
+
+
 def test_greedy_limit_is_the_greedy_rule():
     """With one-hot targets (logit gaps far beyond the float64 exponent range at
     this temperature) the rule reduces to the longest-prefix greedy acceptance
