@@ -59,3 +59,18 @@ def test_flops_per_row_are_the_active_parameters():
     # attention FLOPs: 4 x keys x H_q x d per row and layer (QK^T and PV)
     extra = bench.step_flops_of(cfg, T=1, R=1, ctx_sum=100.0, n_steps=1) - 2 * per_row
     assert extra == 4 * cfg.n_layers * cfg.n_q_heads * cfg.head_dim * 100
+
+
+def test_rejection_sampling_traffic_record_is_consistent():
+    """The sampler's traffic record: its algorithmic bytes are the rows the
+    rule must read (accepted drafts plus one row per sequence, V f32 each, as
+    sampling_leg and --sampling-probe count them), and its ratio is the
+    captured DRAM bytes over those."""
+    rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))["rejection_sampling"]
+    cap = rec["captured"]
+    assert cap["algorithmic_bytes"] == (cap["accepted_total"] + 64) * 129_280 * 4
+    ratio = (cap["dram_read_bytes"] + cap["dram_write_bytes"]) / cap["algorithmic_bytes"]
+    assert abs(rec["traffic_over_algorithmic"] - ratio) < 1e-12
+    # while the sources hash to the capture, the bench scales the ratio to a launch's bytes
+    t = bench.traffic_for("rejection_sampling", 1e6)
+    assert t is None or abs(t - 1e6 * ratio) < 1e-3
